@@ -1,0 +1,16 @@
+"""Float64 CPU oracle for the tile-based 3D Gaussian splatting training step.
+
+TEST INFRASTRUCTURE. Only the test suite, the smoke check (`__graft_entry__.smoke`) and the
+benchmark's CPU-baseline leg may import this package. It shares no code with the CUDA library
+and the CUDA library never imports it.
+
+    _lib.py        ctypes binding of gs_oracle.cpp (preprocess, binning + stable sort, render
+                   forward/backward with marginal-decision flags, preprocess backward by dual numbers)
+    brute.py       numpy brute-force per-pixel renderer for tiny scenes (no tiles list, no sort code)
+    gs_oracle.cpp  the float64 implementation
+"""
+from ._lib import (bin_and_sort, build, preprocess, preprocess_bwd, quat_to_rotmat, render, sh_basis,
+                   view_step)
+
+__all__ = ["bin_and_sort", "build", "preprocess", "preprocess_bwd", "quat_to_rotmat", "render",
+           "sh_basis", "view_step"]

@@ -1,0 +1,638 @@
+// Float64 CPU oracle for the tile-based 3D Gaussian splatting training step.
+//
+// TEST INFRASTRUCTURE. This library exists to check the CUDA library. Only the test suite, the
+// smoke check and the benchmark's CPU-baseline leg may load it. It shares no code, header,
+// table or constant generator with the CUDA path, and the CUDA path never calls it.
+//
+// What it computes. The pages this build follows state the method only at the level of its
+// phases: a 3D Gaussian splatting scene is rendered by a rasterization pipeline and trained by
+// gradient descent, and the gradient computation accumulates per-Gaussian gradients with a very
+// large number of atomic updates (DISTWAR: Fast Differentiable Rendering on Raster-based
+// Rendering Pipelines, Abstract; ARC: Warp-level Adaptive Atomic Reduction in GPUs to Accelerate
+// Differentiable Rendering, Abstract). The per-view phases are preprocessing, rendering and
+// backward computation (Odin: Primitive-Level Synchronization for Distributed Point-Based Neural
+// Rendering, Figure 7). The arithmetic of each phase below is the plainest reading of that
+// pipeline as 3D Gaussian splatting defines it; each convention is stated where it is used.
+//
+// Precision. Everything is float64, except two quantities that the method turns into integers
+// from a float32 value, where the oracle takes the same float32 decision as the kernel:
+//   * the depth sort key is the float32 view-space depth, evaluated as the fused
+//     multiply-add chain fma(R20, x, fma(R21, y, fma(R22, z, t2))), and
+//   * the tile rectangle is evaluated in float64 from the float32 2D mean and integer radius.
+// Where a float32 kernel could take a different discrete decision than this float64 code (a
+// ceiling, a threshold test), the oracle reports the decision as "marginal" with a flag, using
+// an explicit bound on the float32 error; the tests compare everything else exactly.
+//
+// Parallelism: OpenMP over Gaussians (preprocess) and over tiles (render). Every per-pixel and
+// per-Gaussian computation is sequential and in the order the method states.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+extern "C" {
+
+struct OrCamera {
+    float R[9];      // world -> camera rotation, row-major
+    float t[3];      // p_cam = R p_world + t
+    float fx, fy, cx, cy;
+    int32_t width, height;
+    float bg[3];
+};
+
+struct OrOptions {
+    double near_z;          // cull when the float32 depth is <= near_z
+    double lowpass;         // screen-space dilation added to the 2D covariance diagonal (px^2)
+    double jacobian_clamp;  // clamp x/z, y/z to +-clamp * tan(half field of view); <= 0 disables
+    int32_t sh_degree;      // 0..3
+    int32_t threads;        // OpenMP threads, 0 = all
+};
+
+struct OrRenderStats {
+    int64_t pairs_evaluated;   // (pixel, list entry) pairs visited before termination
+    int64_t pairs_blended;     // pairs that were alpha-blended
+    int64_t marginal_pixels;   // pixels with at least one marginal decision
+    int64_t warp_gauss_active; // (tile, 16x2 pixel block, Gaussian) triples with >= 1 blending pixel
+    int64_t tile_gauss_active; // (tile, Gaussian) pairs with >= 1 blending pixel
+    int64_t lane_hist[33];     // histogram of blending pixels per active (16x2 block, Gaussian)
+};
+
+}  // extern "C"
+
+namespace {
+
+constexpr int kTile = 16;
+constexpr double kPi = 3.14159265358979323846;
+
+// ---------------------------------------------------------------------------------------------
+// Forward-mode dual numbers. The preprocess backward is the derivative of the preprocess
+// forward; the oracle obtains it by running the very same forward code on dual numbers.
+// ---------------------------------------------------------------------------------------------
+template <int NV>
+struct Dual {
+    double v;
+    double d[NV];
+    Dual() : v(0.0) { std::memset(d, 0, sizeof(d)); }
+    Dual(double x) : v(x) { std::memset(d, 0, sizeof(d)); }  // NOLINT: implicit on purpose
+    static Dual var(double x, int i) { Dual r(x); r.d[i] = 1.0; return r; }
+};
+
+template <int NV> Dual<NV> operator+(const Dual<NV>& a, const Dual<NV>& b) {
+    Dual<NV> r(a.v + b.v); for (int i = 0; i < NV; ++i) r.d[i] = a.d[i] + b.d[i]; return r; }
+template <int NV> Dual<NV> operator-(const Dual<NV>& a, const Dual<NV>& b) {
+    Dual<NV> r(a.v - b.v); for (int i = 0; i < NV; ++i) r.d[i] = a.d[i] - b.d[i]; return r; }
+template <int NV> Dual<NV> operator-(const Dual<NV>& a) {
+    Dual<NV> r(-a.v); for (int i = 0; i < NV; ++i) r.d[i] = -a.d[i]; return r; }
+template <int NV> Dual<NV> operator*(const Dual<NV>& a, const Dual<NV>& b) {
+    Dual<NV> r(a.v * b.v); for (int i = 0; i < NV; ++i) r.d[i] = a.d[i] * b.v + a.v * b.d[i]; return r; }
+template <int NV> Dual<NV> operator/(const Dual<NV>& a, const Dual<NV>& b) {
+    Dual<NV> r(a.v / b.v);
+    for (int i = 0; i < NV; ++i) r.d[i] = (a.d[i] * b.v - a.v * b.d[i]) / (b.v * b.v);
+    return r; }
+template <int NV> Dual<NV> operator+(const Dual<NV>& a, double b) { return a + Dual<NV>(b); }
+template <int NV> Dual<NV> operator+(double a, const Dual<NV>& b) { return Dual<NV>(a) + b; }
+template <int NV> Dual<NV> operator-(const Dual<NV>& a, double b) { return a - Dual<NV>(b); }
+template <int NV> Dual<NV> operator-(double a, const Dual<NV>& b) { return Dual<NV>(a) - b; }
+template <int NV> Dual<NV> operator*(const Dual<NV>& a, double b) { return a * Dual<NV>(b); }
+template <int NV> Dual<NV> operator*(double a, const Dual<NV>& b) { return Dual<NV>(a) * b; }
+template <int NV> Dual<NV> operator/(const Dual<NV>& a, double b) { return a / Dual<NV>(b); }
+template <int NV> Dual<NV> operator/(double a, const Dual<NV>& b) { return Dual<NV>(a) / b; }
+template <int NV> Dual<NV> exp(const Dual<NV>& a) {
+    Dual<NV> r(std::exp(a.v)); for (int i = 0; i < NV; ++i) r.d[i] = r.v * a.d[i]; return r; }
+template <int NV> Dual<NV> sqrt(const Dual<NV>& a) {
+    Dual<NV> r(std::sqrt(a.v)); for (int i = 0; i < NV; ++i) r.d[i] = a.d[i] / (2.0 * r.v); return r; }
+
+inline double val(double x) { return x; }
+template <int NV> double val(const Dual<NV>& x) { return x.v; }
+using std::exp;
+using std::sqrt;
+
+// ---------------------------------------------------------------------------------------------
+// Real spherical harmonics, degrees 0..3, index k = l*l + l + m, m = -l..l.
+// Definition: with the Condon-Shortley phase included in the associated Legendre function
+// P_l^m(z) = (-1)^m (1 - z^2)^(m/2) d^m/dz^m P_l(z) and N_lm = sqrt((2l+1)/(4 pi) (l-m)!/(l+m)!),
+//   Y_l0 = N_l0 P_l(z),  Y_l,+m = sqrt2 N_lm P_l^m(z) cos(m phi),  Y_l,-m = sqrt2 N_lm P_l^m(z) sin(m phi).
+// On the unit sphere (1 - z^2)^(m/2) cos(m phi) = Re (x + i y)^m and the sine term is Im (x + i y)^m,
+// so each Y is evaluated as a polynomial in (x, y, z). The Legendre polynomials come from
+// Bonnet's recursion (l + 1) P_{l+1} = (2l + 1) z P_l - l P_{l-1}.
+// ---------------------------------------------------------------------------------------------
+struct LegendreTable {
+    double c[4][4];  // c[l][k]: coefficient of z^k in P_l
+    LegendreTable() {
+        std::memset(c, 0, sizeof(c));
+        c[0][0] = 1.0;
+        c[1][1] = 1.0;
+        for (int l = 1; l < 3; ++l)
+            for (int k = 0; k < 4; ++k) {
+                double up = (k > 0) ? c[l][k - 1] : 0.0;
+                c[l + 1][k] = ((2 * l + 1) * up - l * c[l - 1][k]) / (l + 1);
+            }
+    }
+};
+const LegendreTable kLeg;
+
+double factorial(int n) { double r = 1.0; for (int i = 2; i <= n; ++i) r *= i; return r; }
+
+template <class S>
+void sh_basis(int deg, const S& x, const S& y, const S& z, S* Y) {
+    for (int l = 0; l <= deg; ++l) {
+        for (int m = 0; m <= l; ++m) {
+            // m-th derivative of P_l evaluated at z
+            S dm(0.0);
+            S zp(1.0);
+            for (int k = m; k <= l; ++k) {
+                double coef = kLeg.c[l][k] * factorial(k) / factorial(k - m);
+                dm = dm + coef * zp;
+                zp = zp * z;
+            }
+            // (x + i y)^m
+            S re(1.0), im(0.0);
+            for (int j = 0; j < m; ++j) {
+                S nre = re * x - im * y;
+                S nim = re * y + im * x;
+                re = nre; im = nim;
+            }
+            double nlm = std::sqrt((2 * l + 1) / (4.0 * kPi) * factorial(l - m) / factorial(l + m));
+            double cs = (m % 2) ? -1.0 : 1.0;
+            if (m == 0) {
+                Y[l * l + l] = nlm * dm;
+            } else {
+                double s2 = std::sqrt(2.0) * nlm * cs;
+                Y[l * l + l + m] = s2 * dm * re;
+                Y[l * l + l - m] = s2 * dm * im;
+            }
+        }
+    }
+}
+
+// Rotation matrix of the unit quaternion (w, x, y, z) (row-major).
+template <class S>
+void quat_to_rotmat(const S q[4], S R[9]) {
+    const S &w = q[0], &x = q[1], &y = q[2], &z = q[3];
+    R[0] = 1.0 - 2.0 * (y * y + z * z); R[1] = 2.0 * (x * y - w * z);       R[2] = 2.0 * (x * z + w * y);
+    R[3] = 2.0 * (x * y + w * z);       R[4] = 1.0 - 2.0 * (x * x + z * z); R[5] = 2.0 * (y * z - w * x);
+    R[6] = 2.0 * (x * z - w * y);       R[7] = 2.0 * (y * z + w * x);       R[8] = 1.0 - 2.0 * (x * x + y * y);
+}
+
+// Depth sort key: float32 view-space depth, fixed fused multiply-add order (see file header).
+float depth_key(const OrCamera& cam, const float* m) {
+    return std::fmaf(cam.R[6], m[0], std::fmaf(cam.R[7], m[1], std::fmaf(cam.R[8], m[2], cam.t[2])));
+}
+
+struct Rect { int x0, x1, y0, y1; bool empty; bool marginal; };
+
+// Tiles overlapped by the 3-sigma square of a projected Gaussian. In pixel-index coordinates
+// (pixel i has its centre at continuous coordinate i + 0.5, so xh = mean_x - 0.5), tile tx covers
+// pixel indices 16 tx .. 16 tx + 15 and overlaps the square [xh - r, xh + r] iff
+// ceil((xh - r - 15) / 16) <= tx <= floor((xh + r) / 16); likewise for y. Evaluated in float64 from
+// the float32 mean, where every step is exact.
+Rect tile_rect(float mx, float my, int r, int tiles_x, int tiles_y) {
+    Rect R{};
+    double xh = (double)mx - 0.5, yh = (double)my - 0.5;
+    double fx0 = std::ceil((xh - r - 15.0) / 16.0), fx1 = std::floor((xh + r) / 16.0);
+    double fy0 = std::ceil((yh - r - 15.0) / 16.0), fy1 = std::floor((yh + r) / 16.0);
+    fx0 = std::max(fx0, 0.0); fy0 = std::max(fy0, 0.0);
+    fx1 = std::min(fx1, (double)(tiles_x - 1)); fy1 = std::min(fy1, (double)(tiles_y - 1));
+    R.empty = !(fx0 <= fx1 && fy0 <= fy1);
+    if (!R.empty) { R.x0 = (int)fx0; R.x1 = (int)fx1; R.y0 = (int)fy0; R.y1 = (int)fy1; }
+    // Marginal: a boundary lies within 1e-3 px of a tile edge, where a float32 mean that differs
+    // from the float64 one in its last bits could move the rectangle.
+    auto near_edge = [](double v) {
+        double q = v / 16.0;
+        return std::fabs(q - std::nearbyint(q)) * 16.0 < 1e-3;
+    };
+    R.marginal = near_edge(xh - r - 15.0) || near_edge(xh + r) || near_edge(yh - r - 15.0) || near_edge(yh + r);
+    return R;
+}
+
+template <class S>
+struct Projected {
+    bool culled;
+    float depth32;
+    S mean2d[2];
+    S cov2d[3];   // (a, b, c) of the dilated 2D covariance [[a, b], [b, c]]
+    S conic[3];   // (A, B, C) of its inverse
+    S opacity;
+    S rgb[3];
+    bool rgb_clamped[3];
+    double lambda_max;
+    double Y[16];
+};
+
+// Per-Gaussian preprocessing (the "preprocessing" phase of one view): EWA projection of the 3D
+// covariance to a 2D conic, 3-sigma radius, opacity and view-dependent colour.
+template <class S>
+void project(const S mu[3], const S ls[3], const S q[4], const S& logit, const double* shg, int deg,
+             const OrCamera& cam, const OrOptions& opt, Projected<S>& P) {
+    P.culled = false;
+    P.lambda_max = 0.0;
+    // Culling on the float32 depth (the same value that becomes the sort key), computed from the
+    // float32 value of the mean.
+    const float mu32[3] = {(float)val(mu[0]), (float)val(mu[1]), (float)val(mu[2])};
+    P.depth32 = depth_key(cam, mu32);
+    if (!(P.depth32 > (float)opt.near_z)) { P.culled = true; return; }
+
+    double Rc[9], tc[3];
+    for (int i = 0; i < 9; ++i) Rc[i] = cam.R[i];
+    for (int i = 0; i < 3; ++i) tc[i] = cam.t[i];
+    S p[3];
+    for (int i = 0; i < 3; ++i) p[i] = Rc[3 * i] * mu[0] + Rc[3 * i + 1] * mu[1] + Rc[3 * i + 2] * mu[2] + tc[i];
+
+    // 3D covariance Sigma = Rq diag(s^2) Rq^T with s = exp(log_scale), Rq from the normalised quaternion.
+    S qn = sqrt(q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3]);
+    S qu[4] = {q[0] / qn, q[1] / qn, q[2] / qn, q[3] / qn};
+    S Rq[9];
+    quat_to_rotmat(qu, Rq);
+    S s2[3];
+    for (int k = 0; k < 3; ++k) { S s = exp(ls[k]); s2[k] = s * s; }
+    S Sig[3][3];
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j) {
+            S acc(0.0);
+            for (int k = 0; k < 3; ++k) acc = acc + Rq[3 * i + k] * s2[k] * Rq[3 * j + k];
+            Sig[i][j] = acc;
+        }
+
+    // Jacobian of the pinhole projection at p, with x/z and y/z clamped to the widened field of view.
+    const S& z = p[2];
+    S u = p[0] / z, v = p[1] / z;
+    if (opt.jacobian_clamp > 0.0) {
+        double limx = opt.jacobian_clamp * (0.5 * cam.width / (double)cam.fx);
+        double limy = opt.jacobian_clamp * (0.5 * cam.height / (double)cam.fy);
+        if (val(u) > limx) u = S(limx);
+        if (val(u) < -limx) u = S(-limx);
+        if (val(v) > limy) v = S(limy);
+        if (val(v) < -limy) v = S(-limy);
+    }
+    double fx = cam.fx, fy = cam.fy;
+    S J[2][3] = {{fx / z, S(0.0), -(fx * u) / z}, {S(0.0), fy / z, -(fy * v) / z}};
+    // T = J W with W the camera rotation; 2D covariance = T Sigma T^T + lowpass I.
+    S Tm[2][3];
+    for (int i = 0; i < 2; ++i)
+        for (int j = 0; j < 3; ++j) {
+            S acc(0.0);
+            for (int k = 0; k < 3; ++k) acc = acc + J[i][k] * Rc[3 * k + j];
+            Tm[i][j] = acc;
+        }
+    S C2[2][2];
+    for (int i = 0; i < 2; ++i)
+        for (int j = 0; j < 2; ++j) {
+            S acc(0.0);
+            for (int k = 0; k < 3; ++k)
+                for (int l = 0; l < 3; ++l) acc = acc + Tm[i][k] * Sig[k][l] * Tm[j][l];
+            C2[i][j] = acc;
+        }
+    S a = C2[0][0] + opt.lowpass, b = C2[0][1], c = C2[1][1] + opt.lowpass;
+    P.cov2d[0] = a; P.cov2d[1] = b; P.cov2d[2] = c;
+    S det = a * c - b * b;
+    if (!(val(det) > 0.0)) { P.culled = true; return; }
+    P.conic[0] = c / det; P.conic[1] = -b / det; P.conic[2] = a / det;
+    // Largest eigenvalue of the 2D covariance, m + sqrt(((a - c) / 2)^2 + b^2), m = (a + c) / 2.
+    double av = val(a), bv = val(b), cv = val(c);
+    P.lambda_max = 0.5 * (av + cv) + std::sqrt(0.25 * (av - cv) * (av - cv) + bv * bv);
+    P.mean2d[0] = fx * p[0] / z + (double)cam.cx;
+    P.mean2d[1] = fy * p[1] / z + (double)cam.cy;
+    if (!std::isfinite(P.lambda_max) || !std::isfinite(val(P.mean2d[0])) || !std::isfinite(val(P.mean2d[1]))) {
+        P.culled = true; return;
+    }
+    P.opacity = 1.0 / (1.0 + exp(-logit));
+    // View-dependent colour: real SH evaluated at the unit direction from the camera centre
+    // (-R^T t) to the mean, plus 0.5, clamped below at 0.
+    double cpos[3];
+    for (int j = 0; j < 3; ++j) cpos[j] = -(Rc[j] * tc[0] + Rc[3 + j] * tc[1] + Rc[6 + j] * tc[2]);
+    S dvec[3] = {mu[0] - cpos[0], mu[1] - cpos[1], mu[2] - cpos[2]};
+    S dn = sqrt(dvec[0] * dvec[0] + dvec[1] * dvec[1] + dvec[2] * dvec[2]);
+    S Yb[16];
+    sh_basis(deg, dvec[0] / dn, dvec[1] / dn, dvec[2] / dn, Yb);
+    int K = (deg + 1) * (deg + 1);
+    for (int k = 0; k < K; ++k) P.Y[k] = val(Yb[k]);
+    for (int ch = 0; ch < 3; ++ch) {
+        S acc(0.5);
+        for (int k = 0; k < K; ++k) acc = acc + Yb[k] * shg[k * 3 + ch];
+        P.rgb_clamped[ch] = val(acc) < 0.0;
+        P.rgb[ch] = P.rgb_clamped[ch] ? S(0.0) : acc;
+    }
+}
+
+int n_threads(int t) {
+#ifdef _OPENMP
+    return t > 0 ? t : omp_get_max_threads();
+#else
+    (void)t;
+    return 1;
+#endif
+}
+
+}  // namespace
+
+extern "C" {
+
+// Real SH basis at a direction (normalised here), degree <= 3, written to Y[(deg+1)^2].
+void or_sh_basis(int deg, const double* dir, double* Y) {
+    double n = std::sqrt(dir[0] * dir[0] + dir[1] * dir[1] + dir[2] * dir[2]);
+    sh_basis<double>(deg, dir[0] / n, dir[1] / n, dir[2] / n, Y);
+}
+
+void or_quat_to_rotmat(const double* q, double* R) {
+    double n = std::sqrt(q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3]);
+    double qu[4] = {q[0] / n, q[1] / n, q[2] / n, q[3] / n};
+    quat_to_rotmat<double>(qu, R);
+}
+
+// flags: bit0 culled, bit1 radius marginal, bit2 tile-rectangle marginal.
+int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, const double* quat,
+                  const double* logit, const double* sh, const OrCamera* cam, const OrOptions* opt,
+                  double* mean2d, double* conic, double* opacity, double* rgb, float* depth,
+                  int32_t* radius, uint32_t* tiles_touched, uint8_t* flags, double* cov2d) {
+    if (n < 0 || !cam || !opt) return -1;
+    const int deg = opt->sh_degree, K = (deg + 1) * (deg + 1);
+    const int tiles_x = (cam->width + kTile - 1) / kTile, tiles_y = (cam->height + kTile - 1) / kTile;
+#pragma omp parallel for schedule(static) num_threads(n_threads(opt->threads))
+    for (int64_t g = 0; g < n; ++g) {
+        double mu[3], ls[3], q[4];
+        for (int i = 0; i < 3; ++i) { mu[i] = mean3d[3 * g + i]; ls[i] = log_scale[3 * g + i]; }
+        for (int i = 0; i < 4; ++i) q[i] = quat[4 * g + i];
+        Projected<double> P;
+        project<double>(mu, ls, q, logit[g], sh + g * K * 3, deg, *cam, *opt, P);
+        uint8_t f = 0;
+        int r = 0;
+        uint32_t tt = 0;
+        if (!P.culled) {
+            double s = 3.0 * std::sqrt(P.lambda_max);
+            r = (int)std::ceil(s);
+            if (std::fabs(s - std::nearbyint(s)) < 1e-5 * s) f |= 2;
+            Rect R = tile_rect((float)P.mean2d[0], (float)P.mean2d[1], r, tiles_x, tiles_y);
+            if (R.marginal) f |= 4;
+            if (R.empty) P.culled = true;
+            else tt = (uint32_t)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+        }
+        if (P.culled) { f |= 1; r = 0; tt = 0; }
+        depth[g] = P.depth32;
+        radius[g] = r;
+        tiles_touched[g] = tt;
+        flags[g] = f;
+        for (int i = 0; i < 2; ++i) mean2d[2 * g + i] = P.culled ? 0.0 : P.mean2d[i];
+        for (int i = 0; i < 3; ++i) {
+            conic[3 * g + i] = P.culled ? 0.0 : P.conic[i];
+            rgb[3 * g + i] = P.culled ? 0.0 : P.rgb[i];
+            if (cov2d) cov2d[3 * g + i] = P.culled ? 0.0 : P.cov2d[i];
+        }
+        opacity[g] = P.culled ? 0.0 : P.opacity;
+    }
+    return 0;
+}
+
+// Tile duplication and sort. For every Gaussian in index order with radius > 0, one entry per
+// overlapped tile in row-major order of its rectangle: key = tile << 32 | bits(float32 depth),
+// value = Gaussian index. The list is then stably sorted by key (std::stable_sort), so ties in
+// (tile, depth) keep index order. ranges[2 t], ranges[2 t + 1] = [start, end) of tile t.
+// Returns the number of duplicates D; nothing is written when D > capacity.
+int64_t or_bin(int64_t n, const float* mean2d, const float* depth, const int32_t* radius,
+               int32_t width, int32_t height, uint64_t* keys, uint32_t* vals, int64_t capacity,
+               uint32_t* ranges) {
+    const int tiles_x = (width + kTile - 1) / kTile, tiles_y = (height + kTile - 1) / kTile;
+    const int64_t T = (int64_t)tiles_x * tiles_y;
+    std::vector<std::pair<uint64_t, uint32_t>> list;
+    for (int64_t g = 0; g < n; ++g) {
+        if (radius[g] <= 0) continue;
+        Rect R = tile_rect(mean2d[2 * g], mean2d[2 * g + 1], radius[g], tiles_x, tiles_y);
+        if (R.empty) continue;
+        uint32_t dbits;
+        std::memcpy(&dbits, &depth[g], 4);
+        for (int ty = R.y0; ty <= R.y1; ++ty)
+            for (int tx = R.x0; tx <= R.x1; ++tx) {
+                uint64_t tile = (uint64_t)ty * tiles_x + tx;
+                list.emplace_back((tile << 32) | dbits, (uint32_t)g);
+            }
+    }
+    const int64_t D = (int64_t)list.size();
+    if (D > capacity) return D;
+    std::stable_sort(list.begin(), list.end(),
+                     [](const std::pair<uint64_t, uint32_t>& a, const std::pair<uint64_t, uint32_t>& b) {
+                         return a.first < b.first;
+                     });
+    for (int64_t t = 0; t < T; ++t) { ranges[2 * t] = 0; ranges[2 * t + 1] = 0; }
+    for (int64_t i = 0; i < D; ++i) {
+        keys[i] = list[i].first;
+        vals[i] = list[i].second;
+        uint64_t tile = list[i].first >> 32;
+        if (i == 0 || (list[i - 1].first >> 32) != tile) ranges[2 * tile] = (uint32_t)i;
+        if (i == D - 1 || (list[i + 1].first >> 32) != tile) ranges[2 * tile + 1] = (uint32_t)(i + 1);
+    }
+    return D;
+}
+
+// Rendering ("rendering" phase) and, when dl_dimage is given, the gradient computation
+// ("backward computation" phase) of one view.
+//
+// Forward, per pixel (centre at (px + 0.5, py + 0.5)), front to back over its tile's list:
+//   d = mean2d - centre, power = -(A dx^2 + C dy^2) / 2 - B dx dy;
+//   skip when power > 0; alpha = min(0.99, opacity exp(power)); skip when alpha < float32(1/255);
+//   stop before a Gaussian whose T (1 - alpha) < float32(1e-4) (that Gaussian is not blended);
+//   colour += rgb alpha T; T *= 1 - alpha.
+//   image = colour + T bg; t_final = T; n_contrib = 1 + position (in the tile's list) of the last
+//   blended entry, 0 if none.
+// Backward: exact derivative of that forward with the per-pixel list of blended entries kept
+// (alpha_i, T_i), upstream gradient g = dL/dpixel:
+//   dL/drgb_i = alpha_i T_i g;  dL/dalpha_i = sum_ch g_ch (rgb_i,ch T_i - S_i,ch / (1 - alpha_i)),
+//   with S_i the colour blended behind i plus t_final bg; alpha = min(0.99, o G): its derivative
+//   is 0 where o G > 0.99, else dL/do = G dL/dalpha and dL/dpower = o G dL/dalpha.
+// grad2d[g] = (dmean_x, dmean_y, dA, dB, dC, dopacity, dr, dg, db), summed over pixels.
+int or_render(int64_t n, const double* mean2d, const double* conic, const double* opacity,
+              const double* rgb, const uint32_t* vals, const uint32_t* ranges, const OrCamera* cam,
+              const float* dl_dimage, double* image, double* t_final, uint32_t* n_contrib,
+              uint32_t* n_blended, uint8_t* pix_flags, uint64_t* pix_sig, double* grad2d,
+              OrRenderStats* stats, int threads) {
+    (void)n;
+    const int W = cam->width, H = cam->height;
+    const int tiles_x = (W + kTile - 1) / kTile, tiles_y = (H + kTile - 1) / kTile;
+    const int64_t T = (int64_t)tiles_x * tiles_y;
+    const double alpha_min = (double)(1.0f / 255.0f);
+    const double t_min = (double)1e-4f;
+    const double eps32 = std::ldexp(1.0, -24);
+    if (grad2d) std::memset(grad2d, 0, sizeof(double) * 9 * (size_t)n);
+    OrRenderStats st{};
+
+#pragma omp parallel num_threads(n_threads(threads))
+    {
+        OrRenderStats ls{};
+        struct Blend { int64_t pos; uint32_t g; double alpha, T, G, dx, dy; bool clamped; };
+        std::vector<Blend> bl;
+        std::vector<double> acc;       // per-tile gradient accumulator, by list position
+        std::vector<uint8_t> wcount;   // per-tile [8 blocks][len] blending-pixel counts
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t tile = 0; tile < T; ++tile) {
+            const int tx = (int)(tile % tiles_x), ty = (int)(tile / tiles_x);
+            const int64_t s = ranges[2 * tile], e = ranges[2 * tile + 1];
+            const int64_t len = e - s;
+            if (grad2d) acc.assign((size_t)len * 9, 0.0);
+            wcount.assign((size_t)len * 8, 0);
+            for (int ly = 0; ly < kTile; ++ly)
+                for (int lx = 0; lx < kTile; ++lx) {
+                    const int px = tx * kTile + lx, py = ty * kTile + ly;
+                    if (px >= W || py >= H) continue;
+                    const double cxp = px + 0.5, cyp = py + 0.5;
+                    double Tr = 1.0, col[3] = {0.0, 0.0, 0.0};
+                    double eT = 0.0;  // bound on the relative float32 error of T
+                    uint32_t contrib = 0, nbl = 0;
+                    uint8_t pf = 0;
+                    uint64_t sig = 1469598103934665603ull;  // FNV-1a over (position, clamped) of blended entries
+                    bl.clear();
+                    for (int64_t pos = s; pos < e; ++pos) {
+                        const uint32_t g = vals[pos];
+                        ls.pairs_evaluated++;
+                        const double dx = mean2d[2 * g] - cxp, dy = mean2d[2 * g + 1] - cyp;
+                        const double A = conic[3 * g], B = conic[3 * g + 1], C = conic[3 * g + 2];
+                        const double power = -0.5 * (A * dx * dx + C * dy * dy) - B * dx * dy;
+                        // float32 error bound of power: about 8 units in the last place of the sum of
+                        // its term magnitudes
+                        const double ep = 5e-7 * (0.5 * (std::fabs(A) * dx * dx + std::fabs(C) * dy * dy) +
+                                                  std::fabs(B * dx * dy)) + 1e-7;
+                        if (std::fabs(power) <= ep) pf |= 4;
+                        if (power > 0.0) continue;
+                        const double G = std::exp(power);
+                        const double oG = opacity[g] * G;
+                        const bool clamped = oG > 0.99;
+                        const double alpha = clamped ? 0.99 : oG;
+                        const double ea = ep + 1e-6;  // relative float32 error bound of alpha (exp included)
+                        if (!clamped && std::fabs(std::log(alpha / alpha_min)) < ea) pf |= 1;
+                        if (alpha < alpha_min) continue;
+                        const double test_T = Tr * (1.0 - alpha);
+                        const double eT_next = eT + (clamped ? 0.0 : ea * alpha / (1.0 - alpha)) + 2.0 * eps32;
+                        if (std::fabs(test_T / t_min - 1.0) < 2.0 * eT_next + 1e-6) pf |= 2;
+                        if (test_T < t_min) break;
+                        for (int ch = 0; ch < 3; ++ch) col[ch] += rgb[3 * g + ch] * alpha * Tr;
+                        bl.push_back({pos, g, alpha, Tr, G, dx, dy, clamped});
+                        sig = (sig ^ (uint64_t)(2 * (pos - s) + (clamped ? 1 : 0))) * 1099511628211ull;
+                        Tr = test_T;
+                        eT = eT_next;
+                        contrib = (uint32_t)(pos - s + 1);
+                        nbl++;
+                        ls.pairs_blended++;
+                        wcount[(size_t)(ly / 2) * len + (pos - s)]++;
+                    }
+                    const int64_t pix = (int64_t)py * W + px;
+                    for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
+                    t_final[pix] = Tr;
+                    n_contrib[pix] = contrib;
+                    if (n_blended) n_blended[pix] = nbl;
+                    if (pix_flags) pix_flags[pix] = pf;
+                    if (pix_sig) pix_sig[pix] = sig;
+                    if (pf) ls.marginal_pixels++;
+                    if (!grad2d) continue;
+                    double gpix[3];
+                    for (int ch = 0; ch < 3; ++ch) gpix[ch] = dl_dimage[(int64_t)ch * W * H + pix];
+                    double S[3];
+                    for (int ch = 0; ch < 3; ++ch) S[ch] = Tr * cam->bg[ch];
+                    for (int64_t k = (int64_t)bl.size() - 1; k >= 0; --k) {
+                        const Blend& b = bl[k];
+                        const double* c = rgb + 3 * b.g;
+                        double* a = &acc[(size_t)(b.pos - s) * 9];
+                        double dalpha = 0.0;
+                        for (int ch = 0; ch < 3; ++ch) {
+                            a[6 + ch] += b.alpha * b.T * gpix[ch];
+                            dalpha += gpix[ch] * (c[ch] * b.T - S[ch] / (1.0 - b.alpha));
+                        }
+                        for (int ch = 0; ch < 3; ++ch) S[ch] += c[ch] * b.alpha * b.T;
+                        if (b.clamped) continue;
+                        const double o = opacity[b.g];
+                        const double dpower = o * b.G * dalpha;
+                        const double A = conic[3 * b.g], B = conic[3 * b.g + 1], C = conic[3 * b.g + 2];
+                        a[0] += -(A * b.dx + B * b.dy) * dpower;
+                        a[1] += -(B * b.dx + C * b.dy) * dpower;
+                        a[2] += -0.5 * b.dx * b.dx * dpower;
+                        a[3] += -b.dx * b.dy * dpower;
+                        a[4] += -0.5 * b.dy * b.dy * dpower;
+                        a[5] += b.G * dalpha;
+                    }
+                }
+            for (int64_t k = 0; k < len; ++k) {
+                bool any = false;
+                for (int w = 0; w < 8; ++w) {
+                    uint8_t c = wcount[(size_t)w * len + k];
+                    if (c) { ls.warp_gauss_active++; ls.lane_hist[c]++; any = true; }
+                }
+                if (any) ls.tile_gauss_active++;
+            }
+            if (grad2d)
+                for (int64_t k = 0; k < len; ++k) {
+                    const uint32_t g = vals[s + k];
+                    for (int j = 0; j < 9; ++j) {
+                        double v = acc[(size_t)k * 9 + j];
+                        if (v != 0.0) {
+#pragma omp atomic
+                            grad2d[9 * (size_t)g + j] += v;
+                        }
+                    }
+                }
+        }
+#pragma omp critical
+        {
+            st.pairs_evaluated += ls.pairs_evaluated;
+            st.pairs_blended += ls.pairs_blended;
+            st.marginal_pixels += ls.marginal_pixels;
+            st.warp_gauss_active += ls.warp_gauss_active;
+            st.tile_gauss_active += ls.tile_gauss_active;
+            for (int i = 0; i < 33; ++i) st.lane_hist[i] += ls.lane_hist[i];
+        }
+    }
+    if (stats) *stats = st;
+    return 0;
+}
+
+// Preprocess backward: gradients of the loss with respect to mean3d, log_scale, quat (through the
+// normalisation), opacity logit and SH, given grad2d = dL/d(mean2d, conic, opacity, rgb) per
+// Gaussian. The Jacobian of the per-Gaussian preprocessing is taken by running project() on dual
+// numbers in the 11 non-SH parameters; SH coefficients enter the colour linearly, so
+// dL/dsh[k][ch] = Y_k dL/drgb_ch where the colour was not clamped. Culled Gaussians get zeros.
+int or_preprocess_bwd(int64_t n, const double* mean3d, const double* log_scale, const double* quat,
+                      const double* logit, const double* sh, const OrCamera* cam, const OrOptions* opt,
+                      const double* grad2d, double* d_mean3d, double* d_log_scale, double* d_quat,
+                      double* d_logit, double* d_sh) {
+    if (n < 0 || !cam || !opt) return -1;
+    const int deg = opt->sh_degree, K = (deg + 1) * (deg + 1);
+    using D = Dual<11>;
+#pragma omp parallel for schedule(static) num_threads(n_threads(opt->threads))
+    for (int64_t g = 0; g < n; ++g) {
+        D mu[3], ls[3], q[4];
+        for (int i = 0; i < 3; ++i) mu[i] = D::var(mean3d[3 * g + i], i);
+        for (int i = 0; i < 3; ++i) ls[i] = D::var(log_scale[3 * g + i], 3 + i);
+        for (int i = 0; i < 4; ++i) q[i] = D::var(quat[4 * g + i], 6 + i);
+        D lg = D::var(logit[g], 10);
+        Projected<D> P;
+        project<D>(mu, ls, q, lg, sh + g * K * 3, deg, *cam, *opt, P);
+        double grad[11] = {0};
+        for (int k = 0; k < K * 3; ++k) d_sh[(size_t)g * K * 3 + k] = 0.0;
+        bool culled = P.culled;
+        if (!culled) {
+            // a Gaussian whose tile rectangle is empty is culled as well
+            const int tiles_x = (cam->width + kTile - 1) / kTile, tiles_y = (cam->height + kTile - 1) / kTile;
+            int r = (int)std::ceil(3.0 * std::sqrt(P.lambda_max));
+            culled = tile_rect((float)P.mean2d[0].v, (float)P.mean2d[1].v, r, tiles_x, tiles_y).empty;
+        }
+        if (!culled) {
+            const double* gi = grad2d + 9 * (size_t)g;
+            const D* outs[9] = {&P.mean2d[0], &P.mean2d[1], &P.conic[0], &P.conic[1], &P.conic[2],
+                                &P.opacity, &P.rgb[0], &P.rgb[1], &P.rgb[2]};
+            for (int o = 0; o < 9; ++o)
+                for (int v = 0; v < 11; ++v) grad[v] += gi[o] * outs[o]->d[v];
+            for (int ch = 0; ch < 3; ++ch) {
+                if (P.rgb_clamped[ch]) continue;
+                for (int k = 0; k < K; ++k) d_sh[(size_t)g * K * 3 + k * 3 + ch] = P.Y[k] * gi[6 + ch];
+            }
+        }
+        for (int i = 0; i < 3; ++i) d_mean3d[3 * g + i] = grad[i];
+        for (int i = 0; i < 3; ++i) d_log_scale[3 * g + i] = grad[3 + i];
+        for (int i = 0; i < 4; ++i) d_quat[4 * g + i] = grad[6 + i];
+        d_logit[g] = grad[10];
+    }
+    return 0;
+}
+
+}  // extern "C"
