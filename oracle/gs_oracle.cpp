@@ -58,9 +58,9 @@ struct OrRenderStats {
     int64_t pairs_evaluated;   // (pixel, list entry) pairs visited before termination
     int64_t pairs_blended;     // pairs that were alpha-blended
     int64_t marginal_pixels;   // pixels with at least one marginal decision
-    int64_t warp_gauss_active; // (tile, 16x2 pixel block, Gaussian) triples with >= 1 blending pixel
+    int64_t warp_gauss_active; // (tile, 8x4 pixel block, Gaussian) triples with >= 1 blending pixel
     int64_t tile_gauss_active; // (tile, Gaussian) pairs with >= 1 blending pixel
-    int64_t lane_hist[33];     // histogram of blending pixels per active (16x2 block, Gaussian)
+    int64_t lane_hist[33];     // histogram of blending pixels per active (8x4 block, Gaussian)
 };
 
 }  // extern "C"
@@ -363,6 +363,7 @@ int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, cons
         uint8_t f = 0;
         int r = 0;
         uint32_t tt = 0;
+        if (!P.culled && !(std::ceil(3.0 * std::sqrt(P.lambda_max)) < 16777216.0)) P.culled = true;  // radius >= 2^24 px
         if (!P.culled) {
             double s = 3.0 * std::sqrt(P.lambda_max);
             r = (int)std::ceil(s);
@@ -465,7 +466,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
         struct Blend { int64_t pos; uint32_t g; double alpha, T, G, dx, dy; bool clamped; };
         std::vector<Blend> bl;
         std::vector<double> acc;       // per-tile gradient accumulator, by list position
-        std::vector<uint8_t> wcount;   // per-tile [8 blocks][len] blending-pixel counts
+        std::vector<uint8_t> wcount;   // per-tile [8 blocks of 8x4 pixels][len] blending-pixel counts
 #pragma omp for schedule(dynamic, 4)
         for (int64_t tile = 0; tile < T; ++tile) {
             const int tx = (int)(tile % tiles_x), ty = (int)(tile / tiles_x);
@@ -515,7 +516,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                         contrib = (uint32_t)(pos - s + 1);
                         nbl++;
                         ls.pairs_blended++;
-                        wcount[(size_t)(ly / 2) * len + (pos - s)]++;
+                        wcount[(size_t)((ly / 4) * 2 + lx / 8) * len + (pos - s)]++;
                     }
                     const int64_t pix = (int64_t)py * W + px;
                     for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
@@ -613,8 +614,10 @@ int or_preprocess_bwd(int64_t n, const double* mean3d, const double* log_scale, 
         if (!culled) {
             // a Gaussian whose tile rectangle is empty is culled as well
             const int tiles_x = (cam->width + kTile - 1) / kTile, tiles_y = (cam->height + kTile - 1) / kTile;
-            int r = (int)std::ceil(3.0 * std::sqrt(P.lambda_max));
-            culled = tile_rect((float)P.mean2d[0].v, (float)P.mean2d[1].v, r, tiles_x, tiles_y).empty;
+            const double rs = std::ceil(3.0 * std::sqrt(P.lambda_max));
+            culled = !(rs < 16777216.0);
+            int r = culled ? 0 : (int)rs;
+            culled = culled || tile_rect((float)P.mean2d[0].v, (float)P.mean2d[1].v, r, tiles_x, tiles_y).empty;
         }
         if (!culled) {
             const double* gi = grad2d + 9 * (size_t)g;
