@@ -1,0 +1,380 @@
+"""Benchmark of the training step of the tile-based 3D Gaussian splatting rasterizer.
+
+One step = the whole hot path for one view: gs_preprocess, gs_bin_and_sort, gs_render_fwd, the
+loss gradient (image - target), gs_render_bwd, gs_preprocess_bwd. The workload is the outdoor
+scene: 1.6M Gaussians, 1297x840, SH degree 3, a 64-cluster mixture (seeded, synthetic).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--mode sm|direct|warp|adaptive]
+
+Prints one JSON line. `value` is the whole-job throughput in Mpix/s (pixels of all ranks' views
+per second of the slowest rank), measured with CUDA events on the device with inputs resident;
+`e2e` is the same metric with each step's inputs copied from pinned host memory and its
+parameter gradients copied back inside the timed region. With N > 1 (torchrun) every rank runs an
+independent replica of the step (the path needs no exchange within a view). `--impl reference`
+times the float64 CPU oracle on the host cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd ms/view and Mpix/s at 1.6M Gaussians 1297×840; bwd L2-atomic roofline %"
+WORKLOAD = "outdoor: 1.6M Gaussians, 1297x840, SH degree 3, 64-cluster mixture, one view per step"
+CFG = 2
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+COUNTS_PATH = os.path.join(ROOT, "profiles", "workload_counts_outdoor.md")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "render_bwd_outdoor_1600k.md")
+# FP32 operations per blended (pixel, Gaussian) pair in the backward: power 11, alpha 3,
+# transmittance 4, colour gradient 3, alpha gradient 15, colour-behind update 6, opacity and
+# geometry gradients 13.
+BWD_FLOPS_PER_PAIR = 55
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", default="sm", choices=["sm", "direct", "warp", "adaptive"])
+    ap.add_argument("--staging", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------ helpers
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def load_json(path):
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def json_block(path):
+    """The first ```json block of a markdown summary under profiles/."""
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"```json\s*(\{.*?\})\s*```", text, re.S)
+    return json.loads(m.group(1)) if m else None
+
+
+def source_hash(*rel_paths):
+    h = hashlib.sha256()
+    for p in rel_paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def crop_camera(cam, frac_tiles_x: float, frac_tiles_y: float):
+    """A tile-aligned window at the centre of the view (same tiles, same per-tile lists)."""
+    import gs_scenes
+    tx, ty = cam.tiles_x, cam.tiles_y
+    wx, wy = max(1, int(round(tx * frac_tiles_x))), max(1, int(round(ty * frac_tiles_y)))
+    x0, y0 = 16 * ((tx - wx) // 2), 16 * ((ty - wy) // 2)
+    w, h = min(16 * wx, cam.width - x0), min(16 * wy, cam.height - y0)
+    return gs_scenes.Camera(R=cam.R, t=cam.t, fx=cam.fx, fy=cam.fy, cx=cam.cx - x0, cy=cam.cy - y0, width=w,
+                            height=h, bg=cam.bg), (x0, y0)
+
+
+def oracle_sample(scene, frac_x: float, frac_y: float):
+    """The oracle's whole step on a tile-aligned window of the view: preprocess of all Gaussians
+    in the window's camera, then binning, render, backward and preprocess backward of the
+    Gaussians that touch the window. Returns (pixels, seconds, description, threads)."""
+    import gs_scenes
+    import oracle
+    cam, (x0, y0) = crop_camera(scene.cameras[0], frac_x, frac_y)
+    t0 = time.perf_counter()
+    pre = oracle.preprocess(scene.mean3d, scene.log_scale, scene.quat, scene.opacity_logit, scene.sh,
+                            scene.sh_degree, cam)
+    sel = pre["radius"] > 0
+    sub = gs_scenes.Scene(name="window", mean3d=scene.mean3d[sel], log_scale=scene.log_scale[sel],
+                          quat=scene.quat[sel], opacity_logit=scene.opacity_logit[sel], sh=scene.sh[sel],
+                          sh_degree=scene.sh_degree, cameras=[cam],
+                          targets=[scene.targets[0][:, y0:y0 + cam.height, x0:x0 + cam.width]])
+    oracle.view_step(sub)
+    dt = time.perf_counter() - t0
+    desc = (f"float64 oracle, whole step on the central {cam.width}x{cam.height} tile-aligned window of the "
+            f"view ({int(sel.sum())} Gaussians touch it; preprocess over all {scene.n})")
+    return cam.width * cam.height, dt, desc, os.cpu_count()
+
+
+# ------------------------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import gs_scenes
+    import oracle
+    oracle.build()
+    scene = gs_scenes.make_scene(CFG)
+    frac = 0.25  # a quarter of the tiles in each direction: 1/16 of the pixels
+    times, pix, desc = [], 0, ""
+    for i in range(args.warmup + args.steps):
+        pix, dt, desc, cores = oracle_sample(scene, frac, frac)
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    value = pix / t / 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "Mpix/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "Mpix/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "Mpix/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import gs_scenes
+    import __graft_entry__
+    from differentiable_gaussian_splatting_gs_gb300 import _abi, api, step
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = _abi.load()
+
+    scene = gs_scenes.make_scene(CFG)
+    cam = scene.cameras[0]
+    P = cam.width * cam.height
+    names = ("mean3d", "log_scale", "quat", "opacity_logit", "sh")
+    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(scene, k))).pin_memory() for k in names}
+    host_target = torch.from_numpy(scene.targets[0]).pin_memory()
+    params = {k: host[k].to(dev) for k in names}
+    target = host_target.to(dev)
+    grads = api.alloc_param_grads(params)
+    host_grads = {k: torch.empty_like(host[k]).pin_memory() for k in names}
+    opt = api.make_options(scene.sh_degree, bwd_mode=args.mode, staging=args.staging)
+    bufs = step.StepBuffers(scene.n, dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def one_step(ev_bwd=None):
+        c = api.make_camera(cam)
+        proj = api.gs_preprocess(params, c, opt, out=bufs.proj)
+        image, t_final, n_contrib, dl, ranges = bufs.image_buffers(c.width, c.height)
+        b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges)
+        api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib))
+        torch.sub(image, target, out=dl)
+        if ev_bwd is not None:
+            ev_bwd[0].record(stream)
+        api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=bufs.grad2d)
+        if ev_bwd is not None:
+            ev_bwd[1].record(stream)
+        api.gs_preprocess_bwd(params, c, opt, proj, bufs.grad2d, out=grads)
+        return b.n_dup
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        n_dup = one_step()
+    torch.cuda.synchronize()
+    assert api.gs_device_error() == 0
+
+    # ---- device-resident timing: K steps, L2 flushed between steps (outside the events)
+    step_ms, bwd_ms = [], []
+    launches0 = lib.gs_kernel_launches()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            eb = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            e0.record(stream)
+            n_dup = one_step(eb)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+            bwd_ms.append(eb[0].elapsed_time(eb[1]))
+    barrier()
+    torch.cuda.synchronize()
+    launches = lib.gs_kernel_launches() - launches0
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * P / (ms / 1e3) / 1e6
+
+    # ---- end to end: inputs from pinned host memory, gradients back, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_target.numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in host_grads.values())
+        e_ms = []
+        barrier()
+        torch.cuda.synchronize()
+        for _ in range(max(3, args.steps // 2)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in names:
+                params[k].copy_(host[k], non_blocking=True)
+            target.copy_(host_target, non_blocking=True)
+            one_step()
+            for k in names:
+                host_grads[k].copy_(grads[k], non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            e_ms.append(e0.elapsed_time(e1))
+        barrier()
+        em = sum(e_ms) / len(e_ms)
+        if world > 1:
+            t = torch.tensor([em], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            em = float(t.item())
+        e2e = {"value": world * P / (em / 1e3) / 1e6, "unit": "Mpix/s", "ms_per_step": em,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    assert api.gs_device_error() == 0
+
+    # ---- roofline of the dominant kernel (the backward)
+    peaks = load_json(PEAKS_PATH) or {}
+    counts = json_block(COUNTS_PATH) or {}
+    clocks = clk.summary()
+    bwd_avg_ms = sum(bwd_ms) / len(bwd_ms)
+    sm_mhz_peak = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = 152 * 128 * 2 * sm_mhz_peak * 1e6 / 1e12  # FP32 FMA lanes x 2 flops x max SM clock
+    roof = None
+    if "pairs_blended" in counts:
+        flops = counts["pairs_blended"] * BWD_FLOPS_PER_PAIR
+        ach = flops / (bwd_avg_ms / 1e3) / 1e12
+        traffic = None
+        tr = json_block(TRAFFIC_PATH)
+        if tr and tr.get("source_hash") == source_hash("differentiable_gaussian_splatting_gs_gb300/csrc/render.cu"):
+            traffic = tr.get("dram_bytes_per_launch")
+        roof = {"kernel": "gs_render_bwd (k_render_bwd + gradient zeroing)", "bound": "alu", "achieved": ach,
+                "peak": alu_peak, "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": traffic,
+                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock of measured peaks file",
+                "kernel_ms": bwd_avg_ms, "algorithmic_flops": flops,
+                "hbm_frac_of_measured": (counts.get("bwd_bytes", 0) / (bwd_avg_ms / 1e3) / 1e9) /
+                float(peaks.get("hbm_gbs", 6800.0))}
+
+    line = {"metric": METRIC, "value": value, "unit": "Mpix/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n_gaussians": scene.n, "width": cam.width, "height": cam.height,
+                       "duplicates": int(n_dup), "bwd_mode": args.mode,
+                       "l2": "flushed between timed steps (256 MB write, outside the events)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
+            "bwd_ms": bwd_avg_ms, "step_ms_min": min(step_ms)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        pix, dt, desc, cores = oracle_sample(scene, 0.5, 0.5)
+        line["cpu_baseline"] = {"value": pix / dt / 1e6, "unit": "Mpix/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        # the CPU oracle runs on rank 0 only; other ranks have no work
+        if rank == 0:
+            run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+"""Python binding of the library's C ABI, with torch tensors for device memory and streams.
+
+The functions carry the C entry points' names (gs_preprocess, gs_bin_and_sort, gs_render_fwd,
+gs_render_bwd, gs_preprocess_bwd). They allocate outputs with torch when the caller passes none,
+marshal pointers and the current CUDA stream, and raise GsError on a non-zero status. All
+arithmetic runs in libgs_gb300.so.
+
+Dtypes: arrays the C ABI declares as uint32 (vals, tile ranges, contributor counts,
+tiles_touched) are torch.int32 tensors holding the same bits; 64-bit keys are torch.int64.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+
+import torch
+
+from . import _abi
+from ._abi import (GS_BWD_ADAPTIVE, GS_BWD_DIRECT, GS_BWD_SM, GS_BWD_WARP, GS_ERR_CAPACITY, GsError, check,
+                   gs_camera, gs_options, gs_params, gs_proj)
+
+__all__ = ["Proj", "BinResult", "make_camera", "make_options", "alloc_proj", "gs_preprocess",
+           "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd", "gs_preprocess_bwd",
+           "gs_device_error", "GsError", "GS_BWD_DIRECT", "GS_BWD_WARP", "GS_BWD_ADAPTIVE", "GS_BWD_SM"]
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def make_camera(cam) -> gs_camera:
+    """gs_camera from any object with R (9), t (3), fx, fy, cx, cy, width, height, bg (3)."""
+    c = gs_camera()
+    c.R[:] = [float(v) for v in torch.as_tensor(cam.R, dtype=torch.float32).reshape(9).tolist()]
+    c.t[:] = [float(v) for v in torch.as_tensor(cam.t, dtype=torch.float32).reshape(3).tolist()]
+    c.fx, c.fy, c.cx, c.cy = float(cam.fx), float(cam.fy), float(cam.cx), float(cam.cy)
+    c.width, c.height = int(cam.width), int(cam.height)
+    c.bg[:] = [float(v) for v in torch.as_tensor(cam.bg, dtype=torch.float32).reshape(3).tolist()]
+    return c
+
+
+def make_options(sh_degree: int, bwd_mode: int | str = 0, adaptive_threshold: int = 0, staging: int = 0,
+                 near_z: float = 0.0, lowpass: float = 0.0, jacobian_clamp: float = 0.0,
+                 spin_limit: int = 0) -> gs_options:
+    if isinstance(bwd_mode, str):
+        bwd_mode = _abi.BWD_MODES[bwd_mode]
+    return gs_options(bwd_mode=int(bwd_mode), adaptive_threshold=int(adaptive_threshold),
+                      sh_degree=int(sh_degree), staging=int(staging), near_z=float(near_z),
+                      lowpass=float(lowpass), jacobian_clamp=float(jacobian_clamp), spin_limit=int(spin_limit))
+
+
+@dataclasses.dataclass
+class Proj:
+    rec: torch.Tensor            # [N, 12] float32: mean_x, mean_y, A, B, C, opacity, r, g, b, 0, 0, 0
+    depth: torch.Tensor          # [N] float32
+    radius: torch.Tensor         # [N] int32
+    tiles_touched: torch.Tensor  # [N] int32 (uint32 bits)
+
+    @property
+    def n(self) -> int:
+        return int(self.rec.shape[0])
+
+    @property
+    def mean2d(self):
+        return self.rec[:, 0:2]
+
+    @property
+    def conic(self):
+        return self.rec[:, 2:5]
+
+    @property
+    def opacity(self):
+        return self.rec[:, 5]
+
+    @property
+    def rgb(self):
+        return self.rec[:, 6:9]
+
+    def struct(self) -> gs_proj:
+        return gs_proj(rec=_ptr(self.rec), depth=_ptr(self.depth), radius=_ptr(self.radius),
+                       tiles_touched=_ptr(self.tiles_touched), n=self.n)
+
+
+def alloc_proj(n: int, device) -> Proj:
+    return Proj(rec=torch.empty((n, 12), dtype=torch.float32, device=device),
+                depth=torch.empty(n, dtype=torch.float32, device=device),
+                radius=torch.empty(n, dtype=torch.int32, device=device),
+                tiles_touched=torch.empty(n, dtype=torch.int32, device=device))
+
+
+def proj_from_arrays(mean2d, conic, opacity, rgb, depth, radius, device) -> Proj:
+    """A Proj built from separate (host or device) arrays, e.g. projected Gaussians made elsewhere."""
+    n = int(torch.as_tensor(radius).shape[0])
+    rec = torch.zeros((n, 12), dtype=torch.float32)
+    rec[:, 0:2] = torch.as_tensor(mean2d, dtype=torch.float32)
+    rec[:, 2:5] = torch.as_tensor(conic, dtype=torch.float32)
+    rec[:, 5] = torch.as_tensor(opacity, dtype=torch.float32)
+    rec[:, 6:9] = torch.as_tensor(rgb, dtype=torch.float32)
+    return Proj(rec=rec.to(device), depth=torch.as_tensor(depth, dtype=torch.float32).to(device).contiguous(),
+                radius=torch.as_tensor(radius, dtype=torch.int32).to(device).contiguous(),
+                tiles_touched=torch.zeros(n, dtype=torch.int32, device=device))
+
+
+def _params(mean3d, log_scale, quat, opacity_logit, sh) -> gs_params:
+    for t in (mean3d, log_scale, quat, opacity_logit, sh):
+        if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("parameters must be contiguous float32 CUDA tensors")
+    return gs_params(mean3d=_ptr(mean3d), log_scale=_ptr(log_scale), quat=_ptr(quat),
+                     opacity_logit=_ptr(opacity_logit), sh=_ptr(sh), n=int(mean3d.shape[0]))
+
+
+def gs_preprocess(params: dict, cam, opt: gs_options, out: Proj | None = None, stream=None) -> Proj:
+    """params: dict with mean3d [N,3], log_scale [N,3], quat [N,4], opacity_logit [N], sh [N,K,3]."""
+    p = _params(params["mean3d"], params["log_scale"], params["quat"], params["opacity_logit"], params["sh"])
+    if out is None:
+        out = alloc_proj(p.n, params["mean3d"].device)
+    c, ps = make_camera(cam) if not isinstance(cam, gs_camera) else cam, out.struct()
+    check(_abi.load().gs_preprocess(C.byref(p), C.byref(c), C.byref(opt), C.byref(ps), _stream(stream)),
+          "gs_preprocess")
+    return out
+
+
+def gs_sort_workspace_bytes(n: int, capacity: int, width: int, height: int) -> int:
+    return int(_abi.load().gs_sort_workspace_bytes(int(n), int(capacity), int(width), int(height)))
+
+
+@dataclasses.dataclass
+class BinResult:
+    keys: torch.Tensor | None   # [D] int64 (uint64 bits: tile << 32 | depth bits)
+    vals: torch.Tensor          # [D] int32 Gaussian indices
+    ranges: torch.Tensor        # [T, 2] int32: [start, end) per tile
+    n_dup: int
+
+
+class SortBuffers:
+    """Device buffers of gs_bin_and_sort, grown on demand and reused across calls."""
+
+    def __init__(self, device):
+        self.device = torch.device(device)
+        self.capacity = 0
+        self.workspace = None
+        self.keys = None
+        self.vals = None
+
+    def ensure(self, n: int, capacity: int, width: int, height: int, want_keys: bool):
+        need = gs_sort_workspace_bytes(n, capacity, width, height)
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        if capacity > self.capacity or self.vals is None:
+            self.vals = torch.empty(max(capacity, 1), dtype=torch.int32, device=self.device)
+            self.keys = None
+            self.capacity = capacity
+        if want_keys and (self.keys is None or self.keys.numel() < self.vals.numel()):
+            self.keys = torch.empty(self.vals.numel(), dtype=torch.int64, device=self.device)
+
+
+def gs_bin_and_sort(proj: Proj, cam, opt: gs_options, capacity: int | None = None, buffers: SortBuffers | None = None,
+                    want_keys: bool = True, ranges: torch.Tensor | None = None, stream=None) -> BinResult:
+    """Tile duplication + stable radix sort + tile ranges. With capacity None the call retries
+    once with the exact number of duplicates when the first capacity was too small."""
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    dev = proj.rec.device
+    T = ((c.width + 15) // 16) * ((c.height + 15) // 16)
+    if ranges is None:
+        ranges = torch.empty((T, 2), dtype=torch.int32, device=dev)
+    buffers = buffers or SortBuffers(dev)
+    cap = capacity if capacity is not None else max(buffers.capacity, 1 << 16, 4 * proj.n)
+    lib = _abi.load()
+    ps = proj.struct()
+    for attempt in range(2):
+        buffers.ensure(proj.n, cap, c.width, c.height, want_keys)
+        d = C.c_int64(0)
+        st = lib.gs_bin_and_sort(C.byref(ps), C.byref(c), C.byref(opt), _ptr(buffers.workspace),
+                                 buffers.workspace.numel(), _ptr(buffers.keys) if want_keys else None,
+                                 _ptr(buffers.vals), cap, C.byref(d), _ptr(ranges), _stream(stream))
+        if st == GS_ERR_CAPACITY and capacity is None and attempt == 0:
+            cap = int(d.value)
+            continue
+        check(st, "gs_bin_and_sort")
+        D = int(d.value)
+        return BinResult(keys=buffers.keys[:D] if want_keys else None, vals=buffers.vals[:D], ranges=ranges, n_dup=D)
+    raise AssertionError("unreachable")
+
+
+def gs_render_fwd(proj: Proj, vals: torch.Tensor, ranges: torch.Tensor, cam, opt: gs_options, out=None, stream=None):
+    """Returns (image [3,H,W] float32, t_final [H,W] float32, n_contrib [H,W] int32)."""
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    dev = proj.rec.device
+    if out is None:
+        out = (torch.empty((3, c.height, c.width), dtype=torch.float32, device=dev),
+               torch.empty((c.height, c.width), dtype=torch.float32, device=dev),
+               torch.empty((c.height, c.width), dtype=torch.int32, device=dev))
+    image, t_final, n_contrib = out
+    ps = proj.struct()
+    check(_abi.load().gs_render_fwd(C.byref(ps), _ptr(vals), _ptr(ranges), C.byref(c), C.byref(opt), _ptr(image),
+                                    _ptr(t_final), _ptr(n_contrib), _stream(stream)), "gs_render_fwd")
+    return image, t_final, n_contrib
+
+
+def gs_render_bwd(proj: Proj, vals, ranges, cam, opt: gs_options, dl_dimage, t_final, n_contrib, grad2d=None,
+                  stream=None) -> torch.Tensor:
+    """Returns grad2d [N, 12] float32 (columns: dmean_x, dmean_y, dA, dB, dC, dopacity, dr, dg, db, 0, 0, 0)."""
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    if grad2d is None:
+        grad2d = torch.empty((proj.n, 12), dtype=torch.float32, device=proj.rec.device)
+    ps = proj.struct()
+    check(_abi.load().gs_render_bwd(C.byref(ps), _ptr(vals), _ptr(ranges), C.byref(c), C.byref(opt),
+                                    _ptr(dl_dimage.contiguous()), _ptr(t_final), _ptr(n_contrib), _ptr(grad2d),
+                                    _stream(stream)), "gs_render_bwd")
+    return grad2d
+
+
+def alloc_param_grads(params: dict) -> dict:
+    return {"mean3d": torch.zeros_like(params["mean3d"]), "log_scale": torch.zeros_like(params["log_scale"]),
+            "quat": torch.zeros_like(params["quat"]), "opacity_logit": torch.zeros_like(params["opacity_logit"]),
+            "sh": torch.zeros_like(params["sh"])}
+
+
+def gs_preprocess_bwd(params: dict, cam, opt: gs_options, proj: Proj, grad2d, out: dict | None = None,
+                      accumulate: bool = False, stream=None) -> dict:
+    p = _params(params["mean3d"], params["log_scale"], params["quat"], params["opacity_logit"], params["sh"])
+    if out is None:
+        out = alloc_param_grads(params)
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    ps = proj.struct()
+    check(_abi.load().gs_preprocess_bwd(C.byref(p), C.byref(c), C.byref(opt), C.byref(ps), _ptr(grad2d),
+                                        _ptr(out["mean3d"]), _ptr(out["log_scale"]), _ptr(out["quat"]),
+                                        _ptr(out["opacity_logit"]), _ptr(out["sh"]), int(bool(accumulate)),
+                                        _stream(stream)), "gs_preprocess_bwd")
+    return out
+
+
+def gs_device_error(stream=None) -> int:
+    """Synchronises and returns (and clears) the device error status: 0, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK."""
+    return int(_abi.load().gs_device_error(_stream(stream)))

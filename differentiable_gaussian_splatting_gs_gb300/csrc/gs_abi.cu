@@ -1,0 +1,310 @@
+// C ABI of the library (declared in include/gs.h): argument checks, option defaults, camera
+// set-up and kernel launches. No exception crosses this boundary; failures return a GS_ERR_*
+// status and leave a message for gs_last_error_message().
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "gs_common.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+// Device error word of this library, one per device.
+__device__ unsigned int g_error_word = 0u;
+
+static std::atomic<long long> g_launches{0};
+void count_launches(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+
+// Waits on a barrier that expects two arrivals but gets one: the bounded wait must give up.
+__global__ void k_selftest_timeout(unsigned spin_limit, unsigned* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 2);
+        fence_mbar_init();
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bar)) : "memory");
+        mbar_wait_bounded(&bar, 0u, spin_limit, err);
+    }
+}
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    return fail(GS_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kMaxImageSide = 32768;
+
+struct Opts {
+    int bwd_mode, thr, deg, staging;
+    float near_z, lowpass, jac;
+    unsigned spin;
+};
+
+int resolve_options(const gs_options* o, Opts& r) {
+    gs_options z{};
+    if (!o) o = &z;
+    r.bwd_mode = o->bwd_mode == GS_BWD_DEFAULT ? GS_BWD_SM : o->bwd_mode;
+    if (r.bwd_mode < GS_BWD_DIRECT || r.bwd_mode > GS_BWD_SM) return fail(GS_ERR_ARG, "bad bwd_mode %d", o->bwd_mode);
+    r.thr = o->adaptive_threshold == 0 ? 8 : o->adaptive_threshold;
+    if (r.thr < 1 || r.thr > 33) return fail(GS_ERR_ARG, "adaptive_threshold %d outside 1..33", o->adaptive_threshold);
+    r.deg = o->sh_degree;
+    if (r.deg < 0 || r.deg > 3) return fail(GS_ERR_ARG, "sh_degree %d outside 0..3", o->sh_degree);
+    r.staging = o->staging == GS_STAGE_DEFAULT ? GS_STAGE_BULK : o->staging;
+    if (r.staging != GS_STAGE_BULK && r.staging != GS_STAGE_LOADS) return fail(GS_ERR_ARG, "bad staging %d", o->staging);
+    r.near_z = o->near_z == 0.f ? 0.2f : o->near_z;
+    r.lowpass = o->lowpass == 0.f ? 0.3f : (o->lowpass < 0.f ? 0.f : o->lowpass);
+    r.jac = o->jacobian_clamp == 0.f ? 1.3f : o->jacobian_clamp;
+    r.spin = o->spin_limit == 0u ? (1u << 18) : o->spin_limit;
+    if (!std::isfinite(r.near_z) || !std::isfinite(r.lowpass)) return fail(GS_ERR_ARG, "non-finite near_z or lowpass");
+    return GS_OK;
+}
+
+int make_camera(const gs_camera* c, const Opts& o, KernelCamera& k) {
+    if (!c) return fail(GS_ERR_ARG, "camera is NULL");
+    if (c->width <= 0 || c->height <= 0 || c->width > kMaxImageSide || c->height > kMaxImageSide)
+        return fail(GS_ERR_ARG, "image size %dx%d outside 1..%d", c->width, c->height, kMaxImageSide);
+    if (!(c->fx > 0.f) || !(c->fy > 0.f) || !std::isfinite(c->fx) || !std::isfinite(c->fy))
+        return fail(GS_ERR_ARG, "focal lengths must be finite and positive");
+    std::memcpy(k.R, c->R, sizeof(k.R));
+    std::memcpy(k.t, c->t, sizeof(k.t));
+    std::memcpy(k.bg, c->bg, sizeof(k.bg));
+    k.fx = c->fx; k.fy = c->fy; k.cx = c->cx; k.cy = c->cy;
+    k.width = c->width; k.height = c->height;
+    k.tiles_x = (c->width + kTile - 1) / kTile;
+    k.tiles_y = (c->height + kTile - 1) / kTile;
+    for (int j = 0; j < 3; ++j)
+        k.campos[j] = (float)-((double)c->R[j] * c->t[0] + (double)c->R[3 + j] * c->t[1] + (double)c->R[6 + j] * c->t[2]);
+    if (o.jac > 0.f) {
+        k.limx = (float)(o.jac * 0.5 * c->width / (double)c->fx);
+        k.limy = (float)(o.jac * 0.5 * c->height / (double)c->fy);
+    } else {
+        k.limx = k.limy = 3.0e38f;
+    }
+    k.near_z = o.near_z;
+    k.lowpass = o.lowpass;
+    return GS_OK;
+}
+
+int check_params(const gs_params* p) {
+    if (!p) return fail(GS_ERR_ARG, "params is NULL");
+    if (p->n < 0 || p->n > 0x7fffffffll) return fail(GS_ERR_ARG, "n = %lld outside 0..2^31-1", (long long)p->n);
+    if (p->n == 0) return GS_OK;
+    const void* ptrs[5] = {p->mean3d, p->log_scale, p->quat, p->opacity_logit, p->sh};
+    for (const void* q : ptrs)
+        if (!q || !aligned(q, 4)) return fail(GS_ERR_ARG, "a parameter pointer is NULL or not 4-byte aligned");
+    return GS_OK;
+}
+
+int check_proj(const gs_proj* q, int64_t n) {
+    if (!q) return fail(GS_ERR_ARG, "proj is NULL");
+    if (q->n != n) return fail(GS_ERR_ARG, "proj.n = %lld does not match n = %lld", (long long)q->n, (long long)n);
+    if (n == 0) return GS_OK;
+    if (!q->rec || !aligned(q->rec, 16)) return fail(GS_ERR_ARG, "proj.rec is NULL or not 16-byte aligned");
+    if (!q->depth || !q->radius || !q->tiles_touched || !aligned(q->depth, 4) || !aligned(q->radius, 4) ||
+        !aligned(q->tiles_touched, 4))
+        return fail(GS_ERR_ARG, "proj.depth / radius / tiles_touched NULL or misaligned");
+    return GS_OK;
+}
+
+int check_proj_n(const gs_proj* q) {
+    if (!q) return fail(GS_ERR_ARG, "proj is NULL");
+    if (q->n < 0 || q->n > 0x7fffffffll) return fail(GS_ERR_ARG, "proj.n outside 0..2^31-1");
+    return check_proj(q, q->n);
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Device address of g_error_word for the current device (looked up once per device).
+unsigned* error_word(int* status) {
+    static unsigned* cache[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e || dev < 0 || dev >= 256) { *status = cuda_fail(e ? e : cudaErrorInvalidDevice, "cudaGetDevice"); return nullptr; }
+    if (!cache[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e) { *status = cuda_fail(e, "cudaGetSymbolAddress(error word)"); return nullptr; }
+        cache[dev] = static_cast<unsigned*>(p);
+    }
+    *status = GS_OK;
+    return cache[dev];
+}
+
+}  // namespace
+}  // namespace gs
+
+using namespace gs;
+
+extern "C" {
+
+int gs_version(void) { return (1 << 16) | 0; }
+
+int64_t gs_kernel_launches(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
+
+const char* gs_status_string(int status) {
+    switch (status) {
+        case GS_OK: return "GS_OK";
+        case GS_ERR_ARG: return "GS_ERR_ARG: invalid argument";
+        case GS_ERR_CAPACITY: return "GS_ERR_CAPACITY: duplicate capacity too small";
+        case GS_ERR_CUDA: return "GS_ERR_CUDA: CUDA runtime error";
+        case GS_ERR_TIMEOUT: return "GS_ERR_TIMEOUT: a bounded device wait gave up";
+        case GS_ERR_DEVICE_CHECK: return "GS_ERR_DEVICE_CHECK: device-side consistency check failed";
+        default: return "unknown status";
+    }
+}
+
+const char* gs_last_error_message(void) { return t_last_error.c_str(); }
+
+int gs_device_error(void* stream) {
+    unsigned word = 0;
+    cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+    if (e) return cuda_fail(e, "gs_device_error: synchronize");
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+    if (e) return cuda_fail(e, "gs_device_error: read");
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    if (e) return cuda_fail(e, "gs_device_error: clear");
+    if (word & kErrTimeout) return fail(GS_ERR_TIMEOUT, "a bounded device-side wait gave up");
+    if (word & kErrCheck) return fail(GS_ERR_DEVICE_CHECK, "a device-side consistency check failed");
+    return GS_OK;
+}
+
+int gs_selftest_timeout(uint32_t spin_limit, void* stream) {
+    int s;
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    k_selftest_timeout<<<1, 32, 0, as_stream(stream)>>>(spin_limit ? spin_limit : 1024u, err);
+    count_launches(1);
+    cudaError_t e = cudaGetLastError();
+    return e ? cuda_fail(e, "gs_selftest_timeout") : GS_OK;
+}
+
+int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* opt, gs_proj* out, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_params(p))) return s;
+    if ((s = check_proj(out, p->n))) return s;
+    cudaError_t e = launch_preprocess(o.deg, (int)p->n, *p, kc, *out, as_stream(stream));
+    return e ? cuda_fail(e, "gs_preprocess") : GS_OK;
+}
+
+size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32_t height) {
+    (void)width;
+    (void)height;
+    if (n < 0 || capacity < 0) return 0;
+    return carve_workspace(nullptr, n, capacity).bytes;
+}
+
+int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, void* workspace,
+                    size_t workspace_bytes, uint64_t* keys, uint32_t* vals, int64_t capacity, int64_t* n_dup_out,
+                    uint32_t* tile_ranges, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_proj_n(proj))) return s;
+    if (!n_dup_out) return fail(GS_ERR_ARG, "n_dup_out is NULL");
+    if (capacity < 0 || capacity > 0x7fffffffll) return fail(GS_ERR_ARG, "capacity outside 0..2^31-1");
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or not 8-byte aligned");
+    if (capacity > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
+    if (keys && !aligned(keys, 8)) return fail(GS_ERR_ARG, "keys not 8-byte aligned");
+    const size_t need = carve_workspace(nullptr, proj->n, capacity).bytes;
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return fail(GS_ERR_ARG, "workspace NULL, not 256-byte aligned or smaller than %zu bytes", need);
+    const SortWorkspace w = carve_workspace(workspace, proj->n, capacity);
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, st);
+    if (e) return cuda_fail(e, "gs_bin_and_sort: count");
+    unsigned long long d = 0;
+    if ((e = cudaMemcpyAsync(&d, w.total, 8, cudaMemcpyDeviceToHost, st))) return cuda_fail(e, "gs_bin_and_sort: read D");
+    if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "gs_bin_and_sort: synchronize");
+    *n_dup_out = (int64_t)d;
+    if (d > (unsigned long long)capacity)
+        return fail(GS_ERR_CAPACITY, "%llu duplicates exceed capacity %lld", d, (long long)capacity);
+    e = bin_emit_sort(*proj, kc.tiles_x, kc.tiles_y, (unsigned)d, (unsigned long long)capacity, w, keys, vals,
+                      tile_ranges, err, st);
+    return e ? cuda_fail(e, "gs_bin_and_sort: emit/sort") : GS_OK;
+}
+
+int gs_render_fwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges, const gs_camera* cam,
+                  const gs_options* opt, float* image, float* t_final, uint32_t* n_contrib, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_proj_n(proj))) return s;
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or misaligned");
+    if (!image || !t_final || !n_contrib || !aligned(image, 4) || !aligned(t_final, 4) || !aligned(n_contrib, 4))
+        return fail(GS_ERR_ARG, "image / t_final / n_contrib NULL or misaligned");
+    if (proj->n > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaError_t e = launch_render_fwd(o.staging, *proj, vals, tile_ranges, kc, image, t_final, n_contrib, o.spin, err,
+                                      as_stream(stream));
+    return e ? cuda_fail(e, "gs_render_fwd") : GS_OK;
+}
+
+int gs_render_bwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges, const gs_camera* cam,
+                  const gs_options* opt, const float* dl_dimage, const float* t_final, const uint32_t* n_contrib,
+                  float* grad2d, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_proj_n(proj))) return s;
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or misaligned");
+    if (!dl_dimage || !t_final || !n_contrib || !aligned(dl_dimage, 4) || !aligned(t_final, 4) || !aligned(n_contrib, 4))
+        return fail(GS_ERR_ARG, "dl_dimage / t_final / n_contrib NULL or misaligned");
+    if (proj->n > 0 && (!vals || !aligned(vals, 4) || !grad2d || !aligned(grad2d, 16)))
+        return fail(GS_ERR_ARG, "vals or grad2d NULL or misaligned (grad2d needs 16 bytes)");
+    cudaStream_t st = as_stream(stream);
+    if (proj->n > 0) {
+        cudaError_t e = cudaMemsetAsync(grad2d, 0, (size_t)proj->n * 12 * sizeof(float), st);
+        if (e) return cuda_fail(e, "gs_render_bwd: zero grad2d");
+    }
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaError_t e = launch_render_bwd(o.bwd_mode, o.staging, o.thr, *proj, vals, tile_ranges, kc, dl_dimage, t_final,
+                                      n_contrib, grad2d, o.spin, err, st);
+    return e ? cuda_fail(e, "gs_render_bwd") : GS_OK;
+}
+
+int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options* opt, const gs_proj* proj,
+                      const float* grad2d, float* d_mean3d, float* d_log_scale, float* d_quat, float* d_opacity_logit,
+                      float* d_sh, int32_t accumulate, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_params(p))) return s;
+    if ((s = check_proj(proj, p->n))) return s;
+    if (p->n > 0) {
+        if (!grad2d || !aligned(grad2d, 16)) return fail(GS_ERR_ARG, "grad2d NULL or not 16-byte aligned");
+        const void* outs[5] = {d_mean3d, d_log_scale, d_quat, d_opacity_logit, d_sh};
+        for (const void* q : outs)
+            if (!q || !aligned(q, 4)) return fail(GS_ERR_ARG, "a gradient output is NULL or misaligned");
+    }
+    cudaError_t e = launch_preprocess_bwd(o.deg, (int)p->n, *p, kc, proj->radius, grad2d, d_mean3d, d_log_scale,
+                                          d_quat, d_opacity_logit, d_sh, accumulate, as_stream(stream));
+    return e ? cuda_fail(e, "gs_preprocess_bwd") : GS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,44 @@
+// Declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "gs.h"
+
+namespace gs {
+
+struct KernelCamera;
+
+// Adds k to the process-wide count of kernel launches (reported by gs_kernel_launches).
+void count_launches(int k);
+
+// Sort workspace carved from the caller's buffer (all pieces 256-byte aligned).
+struct SortWorkspace {
+    unsigned *dkA, *dkB, *dvA, *dvB;   // depth-sort keys / values, ping-pong, N each
+    unsigned *hist, *totals;           // radix histograms [256][blocks] and digit totals [256]
+    unsigned long long *bsum, *boff, *total;  // duplicate counts per 256 Gaussians, offsets, total D
+    unsigned *tA, *tB, *vB;            // tile-sort keys ping-pong and values, capacity each
+    size_t bytes;                      // total size
+};
+
+SortWorkspace carve_workspace(void* base, long long n, long long cap);
+cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, cudaStream_t st);
+cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
+                          const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
+                          cudaStream_t st);
+
+cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
+                              cudaStream_t st);
+cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
+                                  const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
+                                  int accumulate, cudaStream_t st);
+cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* vals, const unsigned* ranges,
+                              const KernelCamera& cam, float* image, float* t_final, unsigned* n_contrib,
+                              unsigned spin_limit, unsigned* err, cudaStream_t st);
+cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& proj, const unsigned* vals,
+                              const unsigned* ranges, const KernelCamera& cam, const float* dl_dimage,
+                              const float* t_final, const unsigned* n_contrib, float* grad2d, unsigned spin_limit,
+                              unsigned* err, cudaStream_t st);
+
+}  // namespace gs

@@ -1,0 +1,348 @@
+// Preprocessing phase and its backward: one thread per Gaussian.
+//
+// Forward (3D Gaussian splatting's per-Gaussian preprocessing, the first stage of the
+// rasterization pipeline named in DISTWAR: Fast Differentiable Rendering on Raster-based
+// Rendering Pipelines, Abstract): view-space position, EWA projection of the 3D covariance to a
+// 2D conic, 3-sigma radius and tile rectangle, sigmoid opacity, spherical-harmonic colour.
+// Backward: the chain rule of that forward, recomputing its intermediates.
+#include "gs_common.cuh"
+#include "gs_internal.h"
+#include "sh.cuh"
+
+namespace gs {
+
+struct Geo {
+    float p[3];        // view-space position (p[2] is the float32 depth)
+    float qn[4];       // normalised quaternion
+    float qinv;        // 1 / |q|
+    float Rq[9];       // rotation of the Gaussian
+    float s[3];        // scales
+    float Sig[6];      // 3D covariance (xx, xy, xz, yy, yz, zz)
+    float J00, J02, J11, J12;
+    bool clx, cly;     // x/z, y/z were clamped
+    float T[6];        // J W, 2x3 row-major
+    float a, b, c;     // dilated 2D covariance
+    float A, B, C;     // conic
+    float mx, my;
+};
+
+// Shared forward geometry of one Gaussian; false when it is culled by depth or determinant.
+__device__ __forceinline__ bool geometry(const float* m, const float* ls, const float* q,
+                                         const KernelCamera& cam, Geo& g) {
+    const float* R = cam.R;
+    const float* t = cam.t;
+    // view-space position; the depth is the fixed fused multiply-add chain used as sort key
+    g.p[2] = __fmaf_rn(R[6], m[0], __fmaf_rn(R[7], m[1], __fmaf_rn(R[8], m[2], t[2])));
+    if (!(g.p[2] > cam.near_z)) return false;
+    g.p[0] = __fmaf_rn(R[0], m[0], __fmaf_rn(R[1], m[1], __fmaf_rn(R[2], m[2], t[0])));
+    g.p[1] = __fmaf_rn(R[3], m[0], __fmaf_rn(R[4], m[1], __fmaf_rn(R[5], m[2], t[1])));
+
+    const float qq = q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3];
+    g.qinv = rsqrtf(qq);
+    const float w = q[0] * g.qinv, x = q[1] * g.qinv, y = q[2] * g.qinv, z = q[3] * g.qinv;
+    g.qn[0] = w; g.qn[1] = x; g.qn[2] = y; g.qn[3] = z;
+    float* Rq = g.Rq;
+    Rq[0] = 1.f - 2.f * (y * y + z * z); Rq[1] = 2.f * (x * y - w * z);       Rq[2] = 2.f * (x * z + w * y);
+    Rq[3] = 2.f * (x * y + w * z);       Rq[4] = 1.f - 2.f * (x * x + z * z); Rq[5] = 2.f * (y * z - w * x);
+    Rq[6] = 2.f * (x * z - w * y);       Rq[7] = 2.f * (y * z + w * x);       Rq[8] = 1.f - 2.f * (x * x + y * y);
+    for (int k = 0; k < 3; ++k) g.s[k] = expf(ls[k]);
+    // M = Rq diag(s); Sigma = M M^T
+    float M[9];
+    for (int i = 0; i < 3; ++i)
+        for (int k = 0; k < 3; ++k) M[3 * i + k] = Rq[3 * i + k] * g.s[k];
+    g.Sig[0] = M[0] * M[0] + M[1] * M[1] + M[2] * M[2];
+    g.Sig[1] = M[0] * M[3] + M[1] * M[4] + M[2] * M[5];
+    g.Sig[2] = M[0] * M[6] + M[1] * M[7] + M[2] * M[8];
+    g.Sig[3] = M[3] * M[3] + M[4] * M[4] + M[5] * M[5];
+    g.Sig[4] = M[3] * M[6] + M[4] * M[7] + M[5] * M[8];
+    g.Sig[5] = M[6] * M[6] + M[7] * M[7] + M[8] * M[8];
+
+    // pinhole Jacobian at p with x/z, y/z clamped to the widened field of view
+    const float zi = 1.f / g.p[2];
+    float u = g.p[0] * zi, v = g.p[1] * zi;
+    g.clx = fabsf(u) > cam.limx;
+    g.cly = fabsf(v) > cam.limy;
+    if (g.clx) u = copysignf(cam.limx, u);
+    if (g.cly) v = copysignf(cam.limy, v);
+    g.J00 = cam.fx * zi;
+    g.J02 = -cam.fx * u * zi;
+    g.J11 = cam.fy * zi;
+    g.J12 = -cam.fy * v * zi;
+    // T = J W (W = camera rotation)
+    for (int j = 0; j < 3; ++j) {
+        g.T[j] = g.J00 * R[j] + g.J02 * R[6 + j];
+        g.T[3 + j] = g.J11 * R[3 + j] + g.J12 * R[6 + j];
+    }
+    const float* S = g.Sig;
+    float TS[6];  // T Sigma
+    for (int i = 0; i < 2; ++i) {
+        const float* Ti = g.T + 3 * i;
+        TS[3 * i + 0] = Ti[0] * S[0] + Ti[1] * S[1] + Ti[2] * S[2];
+        TS[3 * i + 1] = Ti[0] * S[1] + Ti[1] * S[3] + Ti[2] * S[4];
+        TS[3 * i + 2] = Ti[0] * S[2] + Ti[1] * S[4] + Ti[2] * S[5];
+    }
+    g.a = TS[0] * g.T[0] + TS[1] * g.T[1] + TS[2] * g.T[2] + cam.lowpass;
+    g.b = TS[0] * g.T[3] + TS[1] * g.T[4] + TS[2] * g.T[5];
+    g.c = TS[3] * g.T[3] + TS[4] * g.T[4] + TS[5] * g.T[5] + cam.lowpass;
+    const float det = g.a * g.c - g.b * g.b;
+    if (!(det > 0.f)) return false;
+    const float di = 1.f / det;
+    g.A = g.c * di;
+    g.B = -g.b * di;
+    g.C = g.a * di;
+    g.mx = cam.fx * g.p[0] * zi + cam.cx;
+    g.my = cam.fy * g.p[1] * zi + cam.cy;
+    return true;
+}
+
+template <int DEG>
+__global__ void __launch_bounds__(256) k_preprocess(int n, const float* __restrict__ mean3d,
+                                                    const float* __restrict__ log_scale,
+                                                    const float* __restrict__ quat,
+                                                    const float* __restrict__ logit,
+                                                    const float* __restrict__ sh, const KernelCamera cam,
+                                                    float4* __restrict__ rec, float* __restrict__ depth,
+                                                    int* __restrict__ radius,
+                                                    unsigned* __restrict__ tiles_touched) {
+    constexpr int K = (DEG + 1) * (DEG + 1);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float m[3] = {mean3d[3 * i], mean3d[3 * i + 1], mean3d[3 * i + 2]};
+    const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
+    const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
+    Geo g;
+    bool ok = geometry(m, ls, q, cam, g);
+    depth[i] = g.p[2];
+    int r = 0;
+    unsigned tt = 0;
+    if (ok) {
+        // largest eigenvalue of the 2D covariance in the cancellation-free form
+        const float hd = 0.5f * (g.a - g.c);
+        const float lam = 0.5f * (g.a + g.c) + sqrtf(hd * hd + g.b * g.b);
+        const float rf = ceilf(3.f * sqrtf(lam));
+        ok = isfinite(g.mx) && isfinite(g.my) && rf < 16777216.0f;  // radius < 2^24 px (also rejects NaN)
+        if (ok) {
+            r = (int)rf;
+            const Rect R = tile_rect(g.mx, g.my, r, cam.tiles_x, cam.tiles_y);
+            ok = R.x0 <= R.x1;
+            if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+        }
+    }
+    if (!ok) {
+        radius[i] = 0;
+        tiles_touched[i] = 0;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        rec[3 * i] = z4;
+        rec[3 * i + 1] = z4;
+        rec[3 * i + 2] = z4;
+        return;
+    }
+    const float op = 1.f / (1.f + expf(-logit[i]));
+    // view direction from the camera centre to the mean
+    float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
+    const float dinv = rsqrtf(dx * dx + dy * dy + dz * dz);
+    dx *= dinv; dy *= dinv; dz *= dinv;
+    float Y[16];
+    sh_basis<DEG>(dx, dy, dz, Y);
+    const float* shg = sh + (size_t)i * K * 3;
+    float col[3] = {0.5f, 0.5f, 0.5f};
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        col[0] += Y[k] * shg[3 * k];
+        col[1] += Y[k] * shg[3 * k + 1];
+        col[2] += Y[k] * shg[3 * k + 2];
+    }
+    rec[3 * i] = make_float4(g.mx, g.my, g.A, g.B);
+    rec[3 * i + 1] = make_float4(g.C, op, fmaxf(col[0], 0.f), fmaxf(col[1], 0.f));
+    rec[3 * i + 2] = make_float4(fmaxf(col[2], 0.f), 0.f, 0.f, 0.f);
+    radius[i] = r;
+    tiles_touched[i] = tt;
+}
+
+template <int DEG>
+__global__ void __launch_bounds__(256) k_preprocess_bwd(
+    int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
+    const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
+    const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
+    float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
+    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate) {
+    constexpr int K = (DEG + 1) * (DEG + 1);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
+    float* dshg = d_sh + (size_t)i * K * 3;
+    const float m[3] = {mean3d[3 * i], mean3d[3 * i + 1], mean3d[3 * i + 2]};
+    Geo g;
+    bool live = radius[i] > 0;
+    if (live) {
+        const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
+        const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
+        live = geometry(m, ls, q, cam, g);
+    }
+    if (!live) {
+        if (!accumulate) {
+            for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] = 0.f; d_log_scale[3 * i + k] = 0.f; }
+            for (int k = 0; k < 4; ++k) d_quat[4 * i + k] = 0.f;
+            d_logit[i] = 0.f;
+            for (int k = 0; k < 3 * K; ++k) dshg[k] = 0.f;
+        }
+        return;
+    }
+    const float4 g0 = grad2d[3 * i], g1 = grad2d[3 * i + 1], g2 = grad2d[3 * i + 2];
+    const float dmx = g0.x, dmy = g0.y, dA = g0.z, dB = g0.w, dC = g1.x, dop = g1.y;
+    const float drgb[3] = {g1.z, g1.w, g2.x};
+
+    // opacity = sigmoid(logit)
+    const float op = 1.f / (1.f + expf(-logit[i]));
+    dlg = dop * op * (1.f - op);
+
+    // colour = sum_k Y_k sh_k + 0.5, clamped at 0
+    float vx = m[0] - cam.campos[0], vy = m[1] - cam.campos[1], vz = m[2] - cam.campos[2];
+    const float vinv = rsqrtf(vx * vx + vy * vy + vz * vz);
+    const float ux = vx * vinv, uy = vy * vinv, uz = vz * vinv;
+    float Y[16];
+    sh_basis<DEG>(ux, uy, uz, Y);
+    const float* shg = sh + (size_t)i * K * 3;
+    float col[3] = {0.5f, 0.5f, 0.5f};
+    for (int k = 0; k < K; ++k) {
+        col[0] += Y[k] * shg[3 * k];
+        col[1] += Y[k] * shg[3 * k + 1];
+        col[2] += Y[k] * shg[3 * k + 2];
+    }
+    float dc[3];
+    for (int ch = 0; ch < 3; ++ch) dc[ch] = (col[ch] < 0.f) ? 0.f : drgb[ch];
+    float wk[16];
+    for (int k = 0; k < K; ++k) {
+        const float s0 = Y[k] * dc[0], s1 = Y[k] * dc[1], s2 = Y[k] * dc[2];
+        if (accumulate) {
+            dshg[3 * k] += s0; dshg[3 * k + 1] += s1; dshg[3 * k + 2] += s2;
+        } else {
+            dshg[3 * k] = s0; dshg[3 * k + 1] = s1; dshg[3 * k + 2] = s2;
+        }
+        wk[k] = shg[3 * k] * dc[0] + shg[3 * k + 1] * dc[1] + shg[3 * k + 2] * dc[2];
+    }
+    if (DEG > 0) {
+        float gd[3] = {0.f, 0.f, 0.f};
+        sh_basis_grad<DEG>(ux, uy, uz, wk, gd);
+        // through the normalisation: (I - u u^T) / |v|
+        const float dot = gd[0] * ux + gd[1] * uy + gd[2] * uz;
+        dm[0] += (gd[0] - dot * ux) * vinv;
+        dm[1] += (gd[1] - dot * uy) * vinv;
+        dm[2] += (gd[2] - dot * uz) * vinv;
+    }
+
+    // conic (A, B, C) = inverse of [[a, b], [b, c]]: dL/dSigma' = -M G M with G = [[dA, dB/2], [dB/2, dC]]
+    const float hb = 0.5f * dB;
+    const float MG00 = g.A * dA + g.B * hb, MG01 = g.A * hb + g.B * dC;
+    const float MG10 = g.B * dA + g.C * hb, MG11 = g.B * hb + g.C * dC;
+    const float da = -(MG00 * g.A + MG01 * g.B);
+    const float dbh = -(MG00 * g.B + MG01 * g.C);  // d/dSigma'_01 (one off-diagonal slot)
+    const float dcc = -(MG10 * g.B + MG11 * g.C);
+    // Sigma' = T Sigma T^T (+ lowpass I): H = [[da, dbh], [dbh, dcc]]
+    // dL/dSigma = T^T H T ; dL/dT = 2 H T Sigma
+    const float* T = g.T;
+    float HT[6];
+    for (int j = 0; j < 3; ++j) {
+        HT[j] = da * T[j] + dbh * T[3 + j];
+        HT[3 + j] = dbh * T[j] + dcc * T[3 + j];
+    }
+    float dSig[9];
+    for (int r0 = 0; r0 < 3; ++r0)
+        for (int c0 = 0; c0 < 3; ++c0) dSig[3 * r0 + c0] = T[r0] * HT[c0] + T[3 + r0] * HT[3 + c0];
+    const float* S = g.Sig;
+    const float Sf[9] = {S[0], S[1], S[2], S[1], S[3], S[4], S[2], S[4], S[5]};
+    float dT[6];
+    for (int r0 = 0; r0 < 2; ++r0)
+        for (int c0 = 0; c0 < 3; ++c0)
+            dT[3 * r0 + c0] = 2.f * (HT[3 * r0] * Sf[c0] + HT[3 * r0 + 1] * Sf[3 + c0] + HT[3 * r0 + 2] * Sf[6 + c0]);
+    // T = J W: dJ = dT W^T (only the non-zero entries of J are needed)
+    const float* R = cam.R;
+    const float dJ00 = dT[0] * R[0] + dT[1] * R[1] + dT[2] * R[2];
+    const float dJ02 = dT[0] * R[6] + dT[1] * R[7] + dT[2] * R[8];
+    const float dJ11 = dT[3] * R[3] + dT[4] * R[4] + dT[5] * R[5];
+    const float dJ12 = dT[3] * R[6] + dT[4] * R[7] + dT[5] * R[8];
+    const float zi = 1.f / g.p[2];
+    const float zi2 = zi * zi;
+    const float u = g.clx ? copysignf(cam.limx, g.p[0]) : g.p[0] * zi;
+    const float v = g.cly ? copysignf(cam.limy, g.p[1]) : g.p[1] * zi;
+    float dp[3];
+    // mean2d = (fx x / z + cx, fy y / z + cy)
+    dp[0] = cam.fx * zi * dmx;
+    dp[1] = cam.fy * zi * dmy;
+    dp[2] = -(cam.fx * g.p[0] * dmx + cam.fy * g.p[1] * dmy) * zi2;
+    // J00 = fx / z, J11 = fy / z, J02 = -fx u / z, J12 = -fy v / z with u = x / z unless clamped
+    dp[2] -= (cam.fx * dJ00 + cam.fy * dJ11) * zi2;
+    dp[2] += (g.clx ? 1.f : 2.f) * cam.fx * u * zi2 * dJ02 + (g.cly ? 1.f : 2.f) * cam.fy * v * zi2 * dJ12;
+    if (!g.clx) dp[0] -= cam.fx * zi2 * dJ02;
+    if (!g.cly) dp[1] -= cam.fy * zi2 * dJ12;
+    // p = W mean + t
+    for (int k = 0; k < 3; ++k) dm[k] += R[k] * dp[0] + R[3 + k] * dp[1] + R[6 + k] * dp[2];
+
+    // Sigma = M M^T, M = Rq diag(s): dM = 2 dSigma M (dSigma symmetric)
+    const float* Rq = g.Rq;
+    float dRq[9];
+    for (int r0 = 0; r0 < 3; ++r0)
+        for (int k = 0; k < 3; ++k) {
+            float acc = 0.f;
+            for (int j = 0; j < 3; ++j) acc += dSig[3 * r0 + j] * Rq[3 * j + k];
+            const float dMrk = 2.f * acc * g.s[k];   // dL/dM[r0][k]
+            dRq[3 * r0 + k] = dMrk * g.s[k];
+            dls[k] += dMrk * Rq[3 * r0 + k] * g.s[k];  // dL/ds_k * s_k
+        }
+    // rotation of the normalised quaternion (w, x, y, z)
+    const float w = g.qn[0], x = g.qn[1], y = g.qn[2], z = g.qn[3];
+    const float* G = dRq;
+    float dqn[4];
+    dqn[0] = 2.f * (-z * G[1] + y * G[2] + z * G[3] - x * G[5] - y * G[6] + x * G[7]);
+    dqn[1] = 2.f * (y * G[1] + z * G[2] + y * G[3] - 2.f * x * G[4] - w * G[5] + z * G[6] + w * G[7] - 2.f * x * G[8]);
+    dqn[2] = 2.f * (-2.f * y * G[0] + x * G[1] + w * G[2] + x * G[3] + z * G[5] - w * G[6] + z * G[7] - 2.f * y * G[8]);
+    dqn[3] = 2.f * (-2.f * z * G[0] - w * G[1] + x * G[2] + w * G[3] - 2.f * z * G[4] + y * G[5] + x * G[6] + y * G[7]);
+    const float dotq = dqn[0] * w + dqn[1] * x + dqn[2] * y + dqn[3] * z;
+    for (int k = 0; k < 4; ++k) dq[k] = (dqn[k] - dotq * g.qn[k]) * g.qinv;
+
+    if (accumulate) {
+        for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] += dm[k]; d_log_scale[3 * i + k] += dls[k]; }
+        for (int k = 0; k < 4; ++k) d_quat[4 * i + k] += dq[k];
+        d_logit[i] += dlg;
+    } else {
+        for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] = dm[k]; d_log_scale[3 * i + k] = dls[k]; }
+        for (int k = 0; k < 4; ++k) d_quat[4 * i + k] = dq[k];
+        d_logit[i] = dlg;
+    }
+}
+
+// ---- host-side launchers ------------------------------------------------------------------------
+
+cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
+                              cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int blocks = (n + 255) / 256;
+    float4* rec = reinterpret_cast<float4*>(out.rec);
+    unsigned* tt = out.tiles_touched;
+    count_launches(1);
+    switch (deg) {
+        case 0: k_preprocess<0><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+        case 1: k_preprocess<1><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+        case 2: k_preprocess<2><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+        default: k_preprocess<3><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
+                                  const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
+                                  int accumulate, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int blocks = (n + 255) / 256;
+    const float4* g2 = reinterpret_cast<const float4*>(grad2d);
+    count_launches(1);
+    switch (deg) {
+        case 0: k_preprocess_bwd<0><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 1: k_preprocess_bwd<1><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 2: k_preprocess_bwd<2><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        default: k_preprocess_bwd<3><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gs

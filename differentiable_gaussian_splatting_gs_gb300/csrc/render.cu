@@ -1,0 +1,487 @@
+// Rendering phase (forward alpha blending) and gradient computation phase (backward) of the tile
+// rasterizer: one 256-thread block per 16x16-pixel tile, one pixel per thread, the tile's sorted
+// list staged in shared memory in batches of 256 records.
+//
+// The backward accumulates each Gaussian's gradient over all pixels with atomics; that
+// accumulation is the bottleneck that DISTWAR (Fast Differentiable Rendering on Raster-based
+// Rendering Pipelines, Abstract) and ARC (Warp-level Adaptive Atomic Reduction in GPUs to
+// Accelerate Differentiable Rendering, Abstract) identify, and the reason for the GS_BWD_* modes.
+//
+// Warp layout: warp w covers the 8x4 pixel block at (8 (w & 1), 4 (w >> 1)) of the tile; lane l
+// is pixel (l & 7, l >> 3) of that block.
+//
+// Warp-level culling. Before blending a batch, each warp keeps only the staged Gaussians whose
+// alpha can reach 1/255 somewhere in its 8x4 block: the set alpha >= 1/255 is the ellipse
+// -power <= tau = ln(255 opacity), whose axis-aligned half-extents are sqrt(2 tau Sigma'_xx) and
+// sqrt(2 tau Sigma'_yy) with Sigma' the inverse of the conic. The extents are widened (tau by
+// 0.1 %, extents by 0.1 % + 0.01 px) so that no pair the per-pixel test would blend is dropped;
+// dropped pairs are exactly ones the per-pixel test skips, so the results do not change.
+#include "gs_common.cuh"
+#include "gs_internal.h"
+
+namespace gs {
+
+constexpr float kAlphaMin = 1.0f / 255.0f;
+constexpr float kTMin = 1e-4f;
+constexpr float kAlphaMax = 0.99f;
+// Bound of the waits that let in-flight bulk copies land before a block exits early; independent
+// of the caller's spin limit so that a small limit cannot leave copies running into a dead block.
+constexpr unsigned kDrainLimit = 1u << 22;
+
+struct StageSmem {
+    float4 rec[2][kBatch][3];      // double-buffered records
+    unsigned gidx[2][kBatch];      // Gaussian index of each staged record
+    float4 box[kBatch];            // (xmin, xmax, ymin, ymax) of the alpha >= 1/255 ellipse
+    unsigned short list[8][kBatch];
+    uint64_t bar[2];
+};
+
+struct BwdSmem {
+    StageSmem st;
+    float acc[kBatch * 9];         // per-batch gradient accumulators (GS_BWD_SM)
+    unsigned wmax[8];
+};
+
+__device__ __forceinline__ float4 cull_box(const float4 r0, const float4 r1) {
+    const float mx = r0.x, my = r0.y, A = r0.z, B = r0.w, C = r1.x, o = r1.y;
+    const float inf = __int_as_float(0x7f800000);
+    if (!(o * 1.00001f >= kAlphaMin)) return make_float4(inf, -inf, inf, -inf);  // never blended
+    const float tau = logf(255.0f * o * 1.00001f) * 1.001f + 0.001f;
+    // det = A C - B^2 with one rounding error (fma-based difference of products)
+    const float w = B * B;
+    const float e = __fmaf_rn(-B, B, w);
+    const float f = __fmaf_rn(A, C, -w);
+    const float det = f + e;
+    if (!(det > 0.f)) return make_float4(-inf, inf, -inf, inf);  // degenerate conic: never culled
+    const float hx = sqrtf(2.f * tau * C / det) * 1.001f + 0.01f;
+    const float hy = sqrtf(2.f * tau * A / det) * 1.001f + 0.01f;
+    if (!(hx < inf && hy < inf)) return make_float4(-inf, inf, -inf, inf);
+    return make_float4(mx - hx, mx + hx, my - hy, my + hy);
+}
+
+// ---- batch staging ----------------------------------------------------------------------------
+
+// Registers the transaction bytes of batch `b` on its barrier (thread 0 only, before any copy of
+// that batch is issued).
+template <int STAGING>
+__device__ __forceinline__ void stage_expect(StageSmem& s, int slot, int n_in) {
+    if (STAGING == GS_STAGE_BULK) mbar_arrive_expect_tx(&s.bar[slot], (unsigned)n_in * 48u);
+}
+
+template <int STAGING>
+__device__ __forceinline__ void stage_issue(StageSmem& s, int slot, const float4* __restrict__ rec,
+                                            const unsigned* __restrict__ vals, int first, int n_in,
+                                            unsigned n_gauss, float4 (&pre)[3], unsigned* err) {
+    const int t = threadIdx.x;
+    if (t < n_in) {
+        unsigned g = vals[first + t];
+        if (g >= n_gauss) {
+            atomicOr(err, kErrCheck);
+            g = 0;
+        }
+        s.gidx[slot][t] = g;
+        if (STAGING == GS_STAGE_BULK) {
+            bulk_copy_g2s(&s.rec[slot][t][0], rec + 3 * (size_t)g, 48u, &s.bar[slot]);
+        } else {
+            pre[0] = __ldg(rec + 3 * (size_t)g);
+            pre[1] = __ldg(rec + 3 * (size_t)g + 1);
+            pre[2] = __ldg(rec + 3 * (size_t)g + 2);
+        }
+    }
+}
+
+// Makes batch `slot` visible in shared memory. For register staging the loads issued by
+// stage_issue are stored here; the caller synchronises the block afterwards.
+template <int STAGING>
+__device__ __forceinline__ bool stage_wait(StageSmem& s, int slot, unsigned parity, int n_in, const float4 (&pre)[3],
+                                           unsigned spin_limit, unsigned* err) {
+    if (STAGING == GS_STAGE_BULK) {
+        return mbar_wait_bounded(&s.bar[slot], parity, spin_limit, err);
+    } else {
+        const int t = threadIdx.x;
+        if (t < n_in) {
+            s.rec[slot][t][0] = pre[0];
+            s.rec[slot][t][1] = pre[1];
+            s.rec[slot][t][2] = pre[2];
+        }
+        return true;
+    }
+}
+
+// Compacts the staged entries [0, n_in) that may be blended in this warp's block (and whose
+// batch position is below `pos_limit`) into s.list[warp], in increasing order. Returns the count.
+__device__ __forceinline__ int compact_warp(StageSmem& s, int n_in, int pos_limit, float wx0, float wx1,
+                                            float wy0, float wy1, int warp, int lane) {
+    int cnt = 0;
+    const int lim = min(n_in, pos_limit);
+#pragma unroll
+    for (int c = 0; c < kBatch / 32; ++c) {
+        const int j = c * 32 + lane;
+        bool hit = false;
+        if (j < lim) {
+            const float4 b = s.box[j];
+            hit = (b.y >= wx0) && (b.x <= wx1) && (b.w >= wy0) && (b.z <= wy1);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (hit) s.list[warp][cnt + __popc(m & lanemask_lt())] = (unsigned short)j;
+        cnt += __popc(m);
+    }
+    __syncwarp();
+    return cnt;
+}
+
+// ---- forward ---------------------------------------------------------------------------------
+
+template <int STAGING>
+__global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
+                                                       const uint2* __restrict__ ranges, const KernelCamera cam,
+                                                       unsigned n_gauss, float* __restrict__ image,
+                                                       float* __restrict__ t_final, unsigned* __restrict__ n_contrib,
+                                                       unsigned spin_limit, unsigned* __restrict__ err) {
+    __shared__ StageSmem s;
+    const int tile = blockIdx.x;
+    const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 4 * (warp >> 1);
+    const int px = bx + (lane & 7), py = by + (lane >> 3);
+    const bool inside = px < cam.width && py < cam.height;
+    const float fpx = (float)px + 0.5f, fpy = (float)py + 0.5f;
+    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 3.f;
+
+    const uint2 rg = ranges[tile];
+    const int start = (int)rg.x;
+    const int count = (int)(rg.y > rg.x ? rg.y - rg.x : 0);
+    const int nb = (count + kBatch - 1) / kBatch;
+
+    float T = 1.f, col0 = 0.f, col1 = 0.f, col2 = 0.f;
+    unsigned last = 0;
+    bool done = !inside;
+    float4 pre[3];
+
+    if (nb > 0) {
+        if (threadIdx.x == 0 && STAGING == GS_STAGE_BULK) {
+            mbar_init(&s.bar[0], 1);
+            mbar_init(&s.bar[1], 1);
+            fence_mbar_init();
+            stage_expect<STAGING>(s, 0, min(kBatch, count));
+            if (nb > 1) stage_expect<STAGING>(s, 1, min(kBatch, count - kBatch));
+        }
+        __syncthreads();
+        stage_issue<STAGING>(s, 0, rec, vals, start, min(kBatch, count), n_gauss, pre, err);
+    }
+    bool ok = true;
+    int issued = nb > 0 ? 0 : -1, consumed = -1;  // batches whose copies were issued / waited for
+    for (int b = 0; b < nb; ++b) {
+        const int slot = b & 1;
+        const int n_in = min(kBatch, count - b * kBatch);
+        float4 nxt[3];
+        if (STAGING == GS_STAGE_LOADS) {
+            // the loads of this batch were issued one iteration earlier (or above)
+            ok = stage_wait<STAGING>(s, slot, 0, n_in, pre, spin_limit, err);
+            if (b + 1 < nb) stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b + 1) * kBatch,
+                                                 min(kBatch, count - (b + 1) * kBatch), n_gauss, nxt, err);
+        } else {
+            if (b + 1 < nb) {
+                stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b + 1) * kBatch,
+                                     min(kBatch, count - (b + 1) * kBatch), n_gauss, nxt, err);
+                issued = b + 1;
+            }
+            ok = stage_wait<STAGING>(s, slot, (unsigned)(b >> 1) & 1u, n_in, pre, spin_limit, err);
+            if (ok) consumed = b;
+        }
+        if (threadIdx.x < n_in) s.box[threadIdx.x] = cull_box(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1]);
+        if (__syncthreads_or(!ok)) break;
+        const int nl = compact_warp(s, n_in, kBatch, wx0, wx1, wy0, wy1, warp, lane);
+        for (int k = 0; k < nl; ++k) {
+            if (__all_sync(0xffffffffu, done)) break;
+            const int j = s.list[warp][k];
+            const float4 r0 = s.rec[slot][j][0];
+            const float4 r1 = s.rec[slot][j][1];
+            if (!done) {
+                const float dx = r0.x - fpx, dy = r0.y - fpy;
+                const float power = -0.5f * (r0.z * dx * dx + r1.x * dy * dy) - r0.w * dx * dy;
+                if (power <= 0.f) {
+                    const float alpha = fminf(kAlphaMax, r1.y * __expf(power));
+                    if (alpha >= kAlphaMin) {
+                        const float test_T = T * (1.f - alpha);
+                        if (test_T < kTMin) {
+                            done = true;
+                        } else {
+                            const float w = alpha * T;
+                            const float cb = s.rec[slot][j][2].x;
+                            col0 += r1.z * w;
+                            col1 += r1.w * w;
+                            col2 += cb * w;
+                            T = test_T;
+                            last = (unsigned)(b * kBatch + j + 1);
+                        }
+                    }
+                }
+            }
+        }
+        if (STAGING == GS_STAGE_LOADS) {
+            pre[0] = nxt[0]; pre[1] = nxt[1]; pre[2] = nxt[2];
+        }
+        if (threadIdx.x == 0 && b + 2 < nb) stage_expect<STAGING>(s, slot, min(kBatch, count - (b + 2) * kBatch));
+        if (__syncthreads_count(!done) == 0) break;
+    }
+    // bulk copies issued but not waited for (early termination or a wait that gave up) must land
+    // before the block exits
+    if (STAGING == GS_STAGE_BULK)
+        for (int k = consumed + 1; k <= issued; ++k) mbar_wait_bounded(&s.bar[k & 1], (unsigned)(k >> 1) & 1u, kDrainLimit, err);
+    if (inside) {
+        const size_t pix = (size_t)py * cam.width + px, plane = (size_t)cam.width * cam.height;
+        image[pix] = col0 + T * cam.bg[0];
+        image[plane + pix] = col1 + T * cam.bg[1];
+        image[2 * plane + pix] = col2 + T * cam.bg[2];
+        t_final[pix] = T;
+        n_contrib[pix] = last;
+    }
+}
+
+// ---- backward --------------------------------------------------------------------------------
+
+// Sum over the 32 lanes of v[0..8]. Afterwards lane l with (l & 3) == 0 holds the total of
+// component l >> 2 (0..7) and every lane holds the total of component 8. A transpose reduction:
+// at each of the first three levels a lane keeps half of its components and sends the other
+// half to its partner, so 9 shuffles reduce 8 components instead of 40.
+__device__ __forceinline__ float warp_reduce9(const float (&v)[9], int lane, float& v8) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b4 ? v[i] : v[i + 4];
+        const float keep = b4 ? v[i + 4] : v[i];
+        u[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? u[i] : u[i + 2];
+        const float keep = b3 ? u[i + 2] : u[i];
+        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? w[0] : w[1];
+    float x = (b2 ? w[1] : w[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    float y = v[8];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+    v8 = y;
+    return x;
+}
+
+template <int MODE, int STAGING>
+__global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
+                                                       const uint2* __restrict__ ranges, const KernelCamera cam,
+                                                       unsigned n_gauss, const float* __restrict__ dl_dimage,
+                                                       const float* __restrict__ t_final,
+                                                       const unsigned* __restrict__ n_contrib,
+                                                       float* __restrict__ grad2d, int thr, unsigned spin_limit,
+                                                       unsigned* __restrict__ err) {
+    __shared__ BwdSmem sm;
+    StageSmem& s = sm.st;
+    const int tile = blockIdx.x;
+    const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 4 * (warp >> 1);
+    const int px = bx + (lane & 7), py = by + (lane >> 3);
+    const bool inside = px < cam.width && py < cam.height;
+    const float fpx = (float)px + 0.5f, fpy = (float)py + 0.5f;
+    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 3.f;
+
+    const uint2 rg = ranges[tile];
+    const int start = (int)rg.x;
+    const int count = (int)(rg.y > rg.x ? rg.y - rg.x : 0);
+
+    const size_t pix = (size_t)py * cam.width + px, plane = (size_t)cam.width * cam.height;
+    unsigned last = 0;
+    float T = 1.f, g0 = 0.f, g1 = 0.f, g2 = 0.f;
+    if (inside) {
+        last = min(n_contrib[pix], (unsigned)count);
+        T = t_final[pix];
+        g0 = dl_dimage[pix];
+        g1 = dl_dimage[plane + pix];
+        g2 = dl_dimage[2 * plane + pix];
+    }
+    // colour blended behind the current Gaussian, background included
+    float S0 = T * cam.bg[0], S1 = T * cam.bg[1], S2 = T * cam.bg[2];
+    const unsigned wmax = __reduce_max_sync(0xffffffffu, last);
+    if (lane == 0) sm.wmax[warp] = wmax;
+    __syncthreads();
+    unsigned tmax = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tmax = max(tmax, sm.wmax[w]);
+    const int nb = ((int)tmax + kBatch - 1) / kBatch;
+    float4 pre[3];
+
+    if (nb > 0) {
+        const int b0 = nb - 1;
+        if (threadIdx.x == 0 && STAGING == GS_STAGE_BULK) {
+            mbar_init(&s.bar[0], 1);
+            mbar_init(&s.bar[1], 1);
+            fence_mbar_init();
+            stage_expect<STAGING>(s, 0, min(kBatch, count - b0 * kBatch));
+            if (nb > 1) stage_expect<STAGING>(s, 1, kBatch);
+        }
+        __syncthreads();
+        stage_issue<STAGING>(s, 0, rec, vals, start + b0 * kBatch, min(kBatch, count - b0 * kBatch), n_gauss, pre, err);
+    }
+    bool ok = true;
+    int issued = nb > 0 ? 0 : -1, consumed = -1;  // iterations whose copies were issued / waited for
+    for (int it = 0; it < nb; ++it) {
+        const int b = nb - 1 - it;          // batches back to front
+        const int slot = it & 1;
+        const int n_in = min(kBatch, count - b * kBatch);
+        float4 nxt[3];
+        if (STAGING == GS_STAGE_LOADS) {
+            ok = stage_wait<STAGING>(s, slot, 0, n_in, pre, spin_limit, err);
+            if (b > 0) stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b - 1) * kBatch, kBatch, n_gauss, nxt, err);
+        } else {
+            if (b > 0) {
+                stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b - 1) * kBatch, kBatch, n_gauss, nxt, err);
+                issued = it + 1;
+            }
+            ok = stage_wait<STAGING>(s, slot, (unsigned)(it >> 1) & 1u, n_in, pre, spin_limit, err);
+            if (ok) consumed = it;
+        }
+        if (threadIdx.x < n_in) s.box[threadIdx.x] = cull_box(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1]);
+        if (MODE == GS_BWD_SM)
+            for (int e = threadIdx.x; e < kBatch * 9; e += kBlock) sm.acc[e] = 0.f;
+        if (__syncthreads_or(!ok)) break;
+        const int pos_limit = (int)wmax - b * kBatch;
+        const int nl = compact_warp(s, n_in, pos_limit, wx0, wx1, wy0, wy1, warp, lane);
+        for (int k = nl - 1; k >= 0; --k) {
+            const int j = s.list[warp][k];
+            const unsigned pos = (unsigned)(b * kBatch + j);
+            const float4 r0 = s.rec[slot][j][0];
+            const float4 r1 = s.rec[slot][j][1];
+            const float dx = r0.x - fpx, dy = r0.y - fpy;
+            const float power = -0.5f * (r0.z * dx * dx + r1.x * dy * dy) - r0.w * dx * dy;
+            const float G = __expf(power);
+            const float oG = r1.y * G;
+            const float alpha = fminf(kAlphaMax, oG);
+            const bool contrib = pos < last && power <= 0.f && alpha >= kAlphaMin;
+            const unsigned ballot = __ballot_sync(0xffffffffu, contrib);
+            if (ballot == 0u) continue;
+            float v[9];
+#pragma unroll
+            for (int c = 0; c < 9; ++c) v[c] = 0.f;
+            if (contrib) {
+                const float cb = s.rec[slot][j][2].x;
+                const float inv = 1.f / (1.f - alpha);
+                T *= inv;                               // transmittance in front of this Gaussian
+                const float aT = alpha * T;
+                v[6] = aT * g0;
+                v[7] = aT * g1;
+                v[8] = aT * g2;
+                const float dalpha = g0 * (r1.z * T - S0 * inv) + g1 * (r1.w * T - S1 * inv) + g2 * (cb * T - S2 * inv);
+                S0 += r1.z * aT;
+                S1 += r1.w * aT;
+                S2 += cb * aT;
+                if (oG <= kAlphaMax) {
+                    const float dpow = oG * dalpha;
+                    v[5] = G * dalpha;
+                    v[0] = -(r0.z * dx + r0.w * dy) * dpow;
+                    v[1] = -(r0.w * dx + r1.x * dy) * dpow;
+                    v[2] = -0.5f * dx * dx * dpow;
+                    v[3] = -dx * dy * dpow;
+                    v[4] = -0.5f * dy * dy * dpow;
+                }
+            }
+            const int nact = __popc(ballot);
+            if (MODE == GS_BWD_DIRECT || (MODE == GS_BWD_ADAPTIVE && nact < thr)) {
+                if (contrib) {
+                    float* gp = grad2d + 12 * (size_t)s.gidx[slot][j];
+#pragma unroll
+                    for (int c = 0; c < 9; ++c) red_add_global(gp + c, v[c]);
+                }
+            } else if (MODE == GS_BWD_SM && nact < thr) {
+                if (contrib) {
+                    float* ap = sm.acc + 9 * j;
+#pragma unroll
+                    for (int c = 0; c < 9; ++c) red_add_shared(ap + c, v[c]);
+                }
+            } else {
+                float v8;
+                const float x = warp_reduce9(v, lane, v8);
+                if (MODE == GS_BWD_SM) {
+                    float* ap = sm.acc + 9 * j;
+                    if ((lane & 3) == 0) red_add_shared(ap + (lane >> 2), x);
+                    if (lane == 1) red_add_shared(ap + 8, v8);
+                } else {
+                    float* gp = grad2d + 12 * (size_t)s.gidx[slot][j];
+                    if ((lane & 3) == 0) red_add_global(gp + (lane >> 2), x);
+                    if (lane == 1) red_add_global(gp + 8, v8);
+                }
+            }
+        }
+        if (STAGING == GS_STAGE_LOADS) {
+            pre[0] = nxt[0]; pre[1] = nxt[1]; pre[2] = nxt[2];
+        }
+        __syncthreads();
+        if (MODE == GS_BWD_SM && threadIdx.x < n_in) {
+            const float* a = sm.acc + 9 * threadIdx.x;
+            const float a0 = a[0], a1 = a[1], a2 = a[2], a3 = a[3], a4 = a[4], a5 = a[5], a6 = a[6], a7 = a[7], a8 = a[8];
+            if ((a0 != 0.f) | (a1 != 0.f) | (a2 != 0.f) | (a3 != 0.f) | (a4 != 0.f) | (a5 != 0.f) | (a6 != 0.f) |
+                (a7 != 0.f) | (a8 != 0.f)) {
+                float* gp = grad2d + 12 * (size_t)s.gidx[slot][threadIdx.x];
+                red_add_global_v4(gp, a0, a1, a2, a3);
+                red_add_global_v4(gp + 4, a4, a5, a6, a7);
+                red_add_global(gp + 8, a8);
+            }
+        }
+        if (threadIdx.x == 0 && b >= 2) stage_expect<STAGING>(s, slot, kBatch);
+        __syncthreads();
+    }
+    // after a wait that gave up, bulk copies still in flight must land before the block exits
+    if (STAGING == GS_STAGE_BULK)
+        for (int k = consumed + 1; k <= issued; ++k) mbar_wait_bounded(&s.bar[k & 1], (unsigned)(k >> 1) & 1u, kDrainLimit, err);
+}
+
+// ---- host-side launchers ------------------------------------------------------------------------
+
+cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* vals, const unsigned* ranges,
+                              const KernelCamera& cam, float* image, float* t_final, unsigned* n_contrib,
+                              unsigned spin_limit, unsigned* err, cudaStream_t st) {
+    const int tiles = cam.tiles_x * cam.tiles_y;
+    const float4* rec = reinterpret_cast<const float4*>(proj.rec);
+    const uint2* rg = reinterpret_cast<const uint2*>(ranges);
+    count_launches(1);
+    if (staging == GS_STAGE_LOADS)
+        k_render_fwd<GS_STAGE_LOADS><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
+    else
+        k_render_fwd<GS_STAGE_BULK><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+static void launch_bwd_mode(int staging, int tiles, const float4* rec, const unsigned* vals, const uint2* rg,
+                            const KernelCamera& cam, unsigned n, const float* dl, const float* tf, const unsigned* nc,
+                            float* g2, int thr, unsigned spin, unsigned* err, cudaStream_t st) {
+    if (staging == GS_STAGE_LOADS)
+        k_render_bwd<MODE, GS_STAGE_LOADS><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
+    else
+        k_render_bwd<MODE, GS_STAGE_BULK><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
+}
+
+cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& proj, const unsigned* vals,
+                              const unsigned* ranges, const KernelCamera& cam, const float* dl_dimage,
+                              const float* t_final, const unsigned* n_contrib, float* grad2d, unsigned spin_limit,
+                              unsigned* err, cudaStream_t st) {
+    const int tiles = cam.tiles_x * cam.tiles_y;
+    const float4* rec = reinterpret_cast<const float4*>(proj.rec);
+    const uint2* rg = reinterpret_cast<const uint2*>(ranges);
+    const unsigned n = (unsigned)proj.n;
+    count_launches(1);
+    switch (mode) {
+        case GS_BWD_DIRECT: launch_bwd_mode<GS_BWD_DIRECT>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
+        case GS_BWD_WARP: launch_bwd_mode<GS_BWD_WARP>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
+        case GS_BWD_ADAPTIVE: launch_bwd_mode<GS_BWD_ADAPTIVE>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
+        default: launch_bwd_mode<GS_BWD_SM>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gs

@@ -1,0 +1,58 @@
+"""One training step of one or more views through the five entry points.
+
+Per view (the phases preprocessing, rendering and backward computation of Odin: Primitive-Level
+Synchronization for Distributed Point-Based Neural Rendering, Figure 7): gs_preprocess,
+gs_bin_and_sort, gs_render_fwd, the loss gradient, gs_render_bwd, gs_preprocess_bwd. The loss is
+the squared error 0.5 |image - target|^2, so dL/dimage = image - target; it is the caller's part
+of the step and is formed here with one torch subtraction. Parameter gradients of the views of
+one step are summed (the first view overwrites, the others accumulate).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import api
+
+
+class StepBuffers:
+    """Device buffers reused across steps for scenes of a fixed size."""
+
+    def __init__(self, n: int, device):
+        self.device = torch.device(device)
+        self.proj = api.alloc_proj(n, self.device)
+        self.sort = api.SortBuffers(self.device)
+        self.grad2d = torch.empty((n, 12), dtype=torch.float32, device=self.device)
+        self.images = {}
+
+    def image_buffers(self, width: int, height: int):
+        key = (width, height)
+        if key not in self.images:
+            d = self.device
+            self.images[key] = (torch.empty((3, height, width), dtype=torch.float32, device=d),
+                                torch.empty((height, width), dtype=torch.float32, device=d),
+                                torch.empty((height, width), dtype=torch.int32, device=d),
+                                torch.empty((3, height, width), dtype=torch.float32, device=d),
+                                torch.empty((((height + 15) // 16) * ((width + 15) // 16), 2), dtype=torch.int32,
+                                            device=d))
+        return self.images[key]
+
+
+def train_step(params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int | None = None,
+               want_keys: bool = True, stream=None) -> dict:
+    """Runs every view and leaves the summed parameter gradients in `grads`. Returns per-view
+    duplicate counts and the last view's image (a view of a reused buffer)."""
+    n_dups = []
+    image = None
+    for v, (cam, target) in enumerate(zip(cameras, targets)):
+        c = api.make_camera(cam)
+        proj = api.gs_preprocess(params, c, opt, out=buffers.proj, stream=stream)
+        image, t_final, n_contrib, dl, ranges = buffers.image_buffers(c.width, c.height)
+        b = api.gs_bin_and_sort(proj, c, opt, capacity=capacity, buffers=buffers.sort, want_keys=want_keys,
+                                ranges=ranges, stream=stream)
+        api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib), stream=stream)
+        torch.sub(image, target, out=dl)
+        api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=buffers.grad2d,
+                          stream=stream)
+        api.gs_preprocess_bwd(params, c, opt, proj, buffers.grad2d, out=grads, accumulate=v > 0, stream=stream)
+        n_dups.append(b.n_dup)
+    return {"n_dup": n_dups, "image": image}

@@ -1,0 +1,218 @@
+/*
+ * gs.h — C ABI of the GB300 (sm_103a) library for the training step of a tile-based 3D Gaussian
+ * splatting rasterizer: per-Gaussian preprocessing, tile binning with a stable radix sort,
+ * front-to-back forward blending, the backward pass with aggregated per-Gaussian gradient
+ * atomics, and the preprocessing backward.
+ *
+ * Method. A 3D Gaussian splatting scene is rendered with a rasterization pipeline and trained by
+ * gradient descent from 2D images; its gradient computation is dominated by the atomic updates
+ * that accumulate per-Gaussian gradients, which overwhelm the GPU's L2 atomic units (DISTWAR:
+ * Fast Differentiable Rendering on Raster-based Rendering Pipelines, Abstract; ARC: Warp-level
+ * Adaptive Atomic Reduction in GPUs to Accelerate Differentiable Rendering, Abstract). One view
+ * runs the phases preprocessing, rendering and backward computation (Odin: Primitive-Level
+ * Synchronization for Distributed Point-Based Neural Rendering, Figure 7); the five compute
+ * entry points below are those phases.
+ *
+ * Conventions common to every call.
+ *   - Pointers to arrays are DEVICE pointers, C-contiguous, row-major, owned by the caller. The
+ *     library allocates no device memory and keeps no state between calls except a per-device
+ *     error word (see gs_device_error) and a per-thread last-error message.
+ *   - Projected records (gs_proj.rec) and 2D gradients (grad2d) must be 16-byte aligned; every
+ *     other array must be 4-byte aligned (8-byte for keys). Misalignment returns GS_ERR_ARG.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls enqueue work on it and
+ *     return without synchronising, except gs_bin_and_sort, which synchronises once to read the
+ *     number of duplicates.
+ *   - Status codes: 0 on success, a negative GS_ERR_* otherwise. No C++ exception crosses the ABI.
+ *     gs_last_error_message() describes the last failure of the calling thread.
+ *   - Non-finite inputs are not errors: a Gaussian whose projection is not finite is culled.
+ *   - Coordinates: the camera maps world points by p_cam = R p_world + t (x right, y down, z
+ *     forward); pixel (i, j) has its centre at (i + 0.5, j + 0.5); the projected mean is
+ *     (fx x / z + cx, fy y / z + cy). Images are 16x16-pixel tiles, T = ceil(W/16) ceil(H/16),
+ *     numbered row-major.
+ */
+#ifndef GS_GB300_H
+#define GS_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------------- */
+#define GS_OK                0
+#define GS_ERR_ARG          -1  /* null or misaligned pointer, negative or oversized count, bad option */
+#define GS_ERR_CAPACITY     -2  /* more duplicates than `capacity`; *n_dup_out holds the number needed */
+#define GS_ERR_CUDA         -3  /* a CUDA runtime call or kernel launch failed */
+#define GS_ERR_TIMEOUT      -4  /* a bounded device-side wait gave up (reported by gs_device_error) */
+#define GS_ERR_DEVICE_CHECK -5  /* a device-side consistency check failed (reported by gs_device_error) */
+
+/* ---- backward accumulation modes (gs_options.bwd_mode) ------------------------------------
+ * How gs_render_bwd accumulates the per-pixel gradient contributions of a Gaussian into its
+ * per-Gaussian gradient. All modes compute the same sums (up to float rounding order).
+ *   DIRECT    every contributing pixel (lane) adds its 9 values with its own global atomics:
+ *             the L2-atomic-bound baseline that DISTWAR speeds up (DISTWAR, Abstract).
+ *   WARP      the warp sums its lanes' contributions in registers (shuffle reduction) and one
+ *             warp instruction issues the 9 global atomics (DISTWAR, Abstract: first key idea).
+ *   ADAPTIVE  per warp and Gaussian: WARP when at least `adaptive_threshold` lanes contribute,
+ *             DIRECT otherwise (DISTWAR, Abstract: second key idea; ARC, title).
+ *   SM        warps add into a per-tile shared-memory accumulator (warp-reduced when at least
+ *             `adaptive_threshold` lanes contribute, per lane otherwise); the tile issues one set
+ *             of global atomics per Gaussian and 256-Gaussian batch.                            */
+#define GS_BWD_DEFAULT  0
+#define GS_BWD_DIRECT   1
+#define GS_BWD_WARP     2
+#define GS_BWD_ADAPTIVE 3
+#define GS_BWD_SM       4
+
+/* ---- batch staging in the render kernels (gs_options.staging) ---------------------------- */
+#define GS_STAGE_DEFAULT 0
+#define GS_STAGE_BULK    1  /* one bulk asynchronous copy (cp.async.bulk) per record, mbarrier completion */
+#define GS_STAGE_LOADS   2  /* per-thread 16-byte loads through registers */
+
+typedef struct gs_camera {
+    float   R[9];        /* world -> camera rotation, row-major */
+    float   t[3];        /* world -> camera translation */
+    float   fx, fy;      /* focal lengths, pixels */
+    float   cx, cy;      /* principal point, pixels (continuous coordinates) */
+    int32_t width, height;
+    float   bg[3];       /* background colour blended behind the last Gaussian */
+} gs_camera;
+
+/* Zero-initialised options select the defaults written beside each field. */
+typedef struct gs_options {
+    int32_t  bwd_mode;            /* GS_BWD_*; 0 = GS_BWD_DEFAULT (the SM mode) */
+    int32_t  adaptive_threshold;  /* lanes, 1..32; 0 = 8 */
+    int32_t  sh_degree;           /* 0..3 (K = (degree + 1)^2 SH coefficients per channel) */
+    int32_t  staging;             /* GS_STAGE_*; 0 = GS_STAGE_BULK */
+    float    near_z;              /* cull when the view-space depth is <= near_z; 0 = 0.2 */
+    float    lowpass;             /* added to the 2D covariance diagonal, px^2; 0 = 0.3, < 0 = none */
+    float    jacobian_clamp;      /* clamp x/z, y/z to +-jacobian_clamp * tan(half FOV) in the
+                                     projection Jacobian; 0 = 1.3, < 0 = no clamp */
+    uint32_t spin_limit;          /* iterations before a device-side wait gives up; 0 = 1<<18 */
+} gs_options;
+
+/* Trainable Gaussian parameters (inputs), N Gaussians, float32:
+ *   mean3d [N][3], log_scale [N][3] (per-axis log standard deviation),
+ *   quat [N][4] (w, x, y, z; normalised inside), opacity_logit [N] (opacity = sigmoid),
+ *   sh [N][K][3] (real spherical-harmonic coefficients, channel last).                      */
+typedef struct gs_params {
+    const float* mean3d;
+    const float* log_scale;
+    const float* quat;
+    const float* opacity_logit;
+    const float* sh;
+    int64_t      n;
+} gs_params;
+
+/* Projected Gaussians, written by gs_preprocess and read by the later calls.
+ *   rec [N][12] float32, 16-byte aligned: (mean_x, mean_y, A, B, C, opacity, r, g, b, 0, 0, 0)
+ *       with (A, B, C) the conic, i.e. the inverse 2D covariance [[A, B], [B, C]];
+ *   depth [N] float32 view-space depth (sort key); radius [N] int32 (0 = culled);
+ *   tiles_touched [N] uint32 (number of tiles in the Gaussian's tile rectangle).             */
+typedef struct gs_proj {
+    float*    rec;
+    float*    depth;
+    int32_t*  radius;
+    uint32_t* tiles_touched;
+    int64_t   n;
+} gs_proj;
+
+/* Preprocessing phase (Odin, Figure 7: "preprocessing"; the rasterization pipeline of DISTWAR,
+ * Abstract). Per Gaussian: view-space position; float32 depth
+ * fma(R20, x, fma(R21, y, fma(R22, z, t2))); cull when depth <= near_z; 3D covariance
+ * R(q) diag(exp(2 log_scale)) R(q)^T; EWA projection with the pinhole Jacobian at the mean
+ * (x/z, y/z clamped), plus `lowpass` on the diagonal; conic = inverse (cull when det <= 0);
+ * radius = ceil(3 sqrt(largest eigenvalue)); tile rectangle of tiles overlapping the square of
+ * half-side radius around the mean (cull when empty); opacity = sigmoid(logit); colour = real
+ * SH of the view direction + 0.5, clamped below at 0. Culled Gaussians get a zero record,
+ * radius 0 and tiles_touched 0.
+ * Arguments: p (inputs, n >= 0, n < 2^31), cam, opt (may be NULL), out (outputs, out->n == p->n).
+ * Errors: GS_ERR_ARG on null/misaligned pointers, bad sh_degree or camera size; GS_ERR_CUDA.  */
+int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* opt, gs_proj* out,
+                  void* stream);
+
+/* Bytes of device workspace gs_bin_and_sort needs for n Gaussians and `capacity` duplicates. */
+size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32_t height);
+
+/* Tile duplication and sort (the rasterization pipeline's binning, DISTWAR, Abstract).
+ * One entry (key = tile << 32 | bits of the float32 depth, value = Gaussian index) per
+ * Gaussian with radius > 0 and per tile of its rectangle, stably sorted by key: the result is
+ * ordered by (tile, depth, Gaussian index). The sort is a hand-written LSD radix sort: the
+ * Gaussians are first sorted by depth bits (4 passes of 8 bits), their duplicates emitted in
+ * that order, and the duplicates sorted by tile id (ceil(log2 T / 8) passes), which equals a
+ * stable sort of the 64-bit keys.
+ * Outputs: keys [D] uint64 (may be NULL: not written), vals [D] uint32, tile_ranges [T][2]
+ * uint32 = [start, end) of each tile in the sorted list, *n_dup_out (HOST int64) = D.
+ * workspace: device buffer of at least gs_sort_workspace_bytes(n, capacity, W, H) bytes.
+ * Synchronises `stream` once to read D. If D > capacity, nothing is written beyond the
+ * workspace, *n_dup_out = D and GS_ERR_CAPACITY is returned; call again with a larger capacity.
+ * capacity must be < 2^32. Errors: GS_ERR_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA.                 */
+int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options* opt,
+                    void* workspace, size_t workspace_bytes, uint64_t* keys, uint32_t* vals,
+                    int64_t capacity, int64_t* n_dup_out, uint32_t* tile_ranges, void* stream);
+
+/* Rendering phase (Odin, Figure 7: "rendering"). One 256-thread block per 16x16 tile stages the
+ * tile's list in batches of 256 records in shared memory and blends front to back per pixel:
+ * power = -(A dx^2 + C dy^2)/2 - B dx dy with d = mean - pixel centre; skip power > 0;
+ * alpha = min(0.99, opacity exp(power)); skip alpha < 1/255; stop before a Gaussian whose
+ * T (1 - alpha) < 1e-4; colour += rgb alpha T; T *= 1 - alpha.
+ * Outputs: image [3][H][W] = colour + T bg, t_final [H][W] = T, n_contrib [H][W] = 1 + the
+ * position (within the tile's list) of the last blended Gaussian, 0 if none.
+ * Errors: GS_ERR_ARG, GS_ERR_CUDA; a staging wait that gives up sets GS_ERR_TIMEOUT in the
+ * device error word.                                                                          */
+int gs_render_fwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges,
+                  const gs_camera* cam, const gs_options* opt, float* image, float* t_final,
+                  uint32_t* n_contrib, void* stream);
+
+/* Gradient computation phase (Odin, Figure 7: "backward computation"; DISTWAR and ARC,
+ * Abstract: the atomic-bound step). Replays each pixel's list back to front from n_contrib,
+ * recovering T by division by (1 - alpha), and accumulates per Gaussian
+ * grad2d[g] = dL/d(mean_x, mean_y, A, B, C, opacity, r, g, b) over all pixels, given
+ * dl_dimage [3][H][W]: dL/drgb = alpha T g; dL/dalpha = sum_ch g_ch (rgb_ch T - S_ch/(1 - alpha))
+ * with S the colour blended behind (background included); the derivative through the 0.99
+ * clamp is 0. grad2d is [N][12] float32, 16-byte aligned; columns 9..11 are left 0. The callee
+ * zeroes grad2d first. Accumulation strategy: opt->bwd_mode (see GS_BWD_*).
+ * Errors: GS_ERR_ARG, GS_ERR_CUDA; staging timeouts as for gs_render_fwd.                    */
+int gs_render_bwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges,
+                  const gs_camera* cam, const gs_options* opt, const float* dl_dimage,
+                  const float* t_final, const uint32_t* n_contrib, float* grad2d, void* stream);
+
+/* Preprocessing backward: chain rule from grad2d to the parameters, recomputing the forward of
+ * gs_preprocess per Gaussian. Outputs d_mean3d [N][3], d_log_scale [N][3], d_quat [N][4]
+ * (through the normalisation), d_opacity_logit [N], d_sh [N][K][3]. Gaussians with radius 0
+ * (culled) get zeros. accumulate != 0 adds to the outputs (views of one step), else overwrites.
+ * Errors: GS_ERR_ARG, GS_ERR_CUDA.                                                           */
+int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options* opt,
+                      const gs_proj* proj, const float* grad2d, float* d_mean3d,
+                      float* d_log_scale, float* d_quat, float* d_opacity_logit, float* d_sh,
+                      int32_t accumulate, void* stream);
+
+/* Text of a status code (static storage). */
+const char* gs_status_string(int status);
+
+/* Description of the last failed call on the calling thread ("" if none). */
+const char* gs_last_error_message(void);
+
+/* Synchronises `stream`, reads and clears the device error word of the current device:
+ * GS_OK, GS_ERR_TIMEOUT (a bounded device wait gave up) or GS_ERR_DEVICE_CHECK. */
+int gs_device_error(void* stream);
+
+/* Self-test of the bounded device-side wait used by the render kernels: launches one block that
+ * waits on a shared-memory barrier nothing will complete, giving up after `spin_limit`
+ * iterations (0 = 1024). The wait sets the timeout bit of the device error word, so a following
+ * gs_device_error() returns GS_ERR_TIMEOUT; the context stays usable. Errors: GS_ERR_CUDA.      */
+int gs_selftest_timeout(uint32_t spin_limit, void* stream);
+
+/* Number of kernels this library has launched in this process (all devices, all threads). */
+int64_t gs_kernel_launches(void);
+
+/* Library version: (major << 16) | minor. */
+int gs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_GB300_H */

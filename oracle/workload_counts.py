@@ -1,0 +1,74 @@
+"""Counts of the benchmark workload measured by the oracle (TEST INFRASTRUCTURE).
+
+Runs the float64 oracle on the outdoor scene (1.6M Gaussians, 1297x840, seeded) and writes
+profiles/workload_counts_outdoor.md: duplicates D, (pixel, Gaussian) pairs evaluated and blended,
+active (8x4 pixel block, Gaussian) and (tile, Gaussian) pairs with the histogram of blending
+pixels per active block, and the algorithmic bytes of the backward raster:
+    per tile, its list up to the largest contributor count x (4-byte index + 48-byte record),
+    + per pixel 20 bytes (dL/dpixel, T_final, contributor count),
+    + per Gaussian 48 bytes (the 2D gradient record written).
+The benchmark divides these by measured kernel times; nothing of the CUDA library is used here.
+
+    python -m oracle.workload_counts
+"""
+from __future__ import annotations
+
+import json
+import os
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import gs_scenes  # noqa: E402
+import oracle  # noqa: E402
+
+
+def counts(cfg: int = 2) -> dict:
+    s = gs_scenes.make_scene(cfg)
+    cam = s.cameras[0]
+    t0 = time.perf_counter()
+    out = oracle.view_step(s)
+    dt = time.perf_counter() - t0
+    st = out["bwd_stats"]
+    nc = out["fwd"]["n_contrib"]
+    ranges = out["ranges"]
+    TX = cam.tiles_x
+    ys, xs = np.mgrid[0:cam.height, 0:cam.width]
+    tile = (ys // 16) * TX + xs // 16
+    tmax = np.zeros(cam.n_tiles, np.int64)
+    np.maximum.at(tmax, tile.ravel(), nc.ravel().astype(np.int64))
+    tlen = (ranges[:, 1].astype(np.int64) - ranges[:, 0].astype(np.int64))
+    listed = int(np.minimum(tlen, tmax).sum())
+    P = cam.width * cam.height
+    return {"workload": "outdoor 1.6M Gaussians 1297x840 seed 2", "n_gaussians": s.n, "pixels": P,
+            "duplicates": int(len(out["vals"])), "pairs_evaluated": int(st["pairs_evaluated"]),
+            "pairs_blended": int(st["pairs_blended"]), "warp_gauss_active": int(st["warp_gauss_active"]),
+            "tile_gauss_active": int(st["tile_gauss_active"]), "lane_hist": [int(v) for v in st["lane_hist"]],
+            "bwd_list_entries": listed, "bwd_bytes": listed * 52 + P * 20 + s.n * 48,
+            "marginal_pixels": int(st["marginal_pixels"]), "oracle_seconds": dt, "threads": os.cpu_count()}
+
+
+def main():
+    c = counts()
+    path = os.path.join(ROOT, "profiles", "workload_counts_outdoor.md")
+    hist = c["lane_hist"]
+    with open(path, "w") as f:
+        f.write("# Workload counts: outdoor scene (1.6M Gaussians, 1297x840, seed 2)\n\n")
+        f.write("Written by `python -m oracle.workload_counts` (float64 oracle only). The benchmark's\n")
+        f.write("roofline numerators use `pairs_blended` and `bwd_bytes`.\n\n")
+        f.write(f"- duplicates D = {c['duplicates']:,}\n- pairs evaluated = {c['pairs_evaluated']:,}\n")
+        f.write(f"- pairs blended = {c['pairs_blended']:,}\n")
+        f.write(f"- active (8x4 block, Gaussian) = {c['warp_gauss_active']:,}; "
+                f"active (tile, Gaussian) = {c['tile_gauss_active']:,}\n")
+        full = hist[32] / max(1, sum(hist))
+        f.write(f"- share of active blocks with all 32 pixels blending: {full:.1%}\n\n")
+        f.write("```json\n" + json.dumps(c) + "\n```\n")
+    print(path)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,94 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds, loads, exports every entry
+point include/gs.h declares, sizes the sort workspace, and rejects bad arguments before touching
+the device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from differentiable_gaussian_splatting_gs_gb300 import _abi, api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return _abi.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "gs.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gs_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_phases():
+    names = declared_symbols()
+    for n in ("gs_preprocess", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd", "gs_preprocess_bwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert set(names) == set(_abi.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.gs_version() >> 16 == 1
+    for st in (_abi.GS_OK, _abi.GS_ERR_ARG, _abi.GS_ERR_CAPACITY, _abi.GS_ERR_CUDA, _abi.GS_ERR_TIMEOUT,
+               _abi.GS_ERR_DEVICE_CHECK):
+        assert lib.gs_status_string(st).decode().startswith("GS_")
+
+
+def test_workspace_size_grows_with_inputs(lib):
+    a = lib.gs_sort_workspace_bytes(1000, 10_000, 128, 128)
+    b = lib.gs_sort_workspace_bytes(1_000_000, 10_000_000, 1297, 840)
+    assert 0 < a < b
+    assert b >= 16 * 1_000_000 + 12 * 10_000_000
+    assert lib.gs_sort_workspace_bytes(-1, 0, 1, 1) == 0
+
+
+def _cam(w=64, h=64, f=64.0):
+    c = _abi.gs_camera()
+    c.R[:] = [1, 0, 0, 0, 1, 0, 0, 0, 1]
+    c.fx = c.fy = f
+    c.cx, c.cy, c.width, c.height = w / 2, h / 2, w, h
+    return c
+
+
+def test_bad_arguments_are_rejected_on_the_host(lib):
+    cam, opt = _cam(), api.make_options(0)
+    p = _abi.gs_params(n=10)  # null pointers with n > 0
+    proj = _abi.gs_proj(n=10)
+    assert lib.gs_preprocess(C.byref(p), C.byref(cam), C.byref(opt), C.byref(proj), None) == _abi.GS_ERR_ARG
+    assert b"NULL" in lib.gs_last_error_message()
+    assert lib.gs_preprocess(C.byref(p), None, C.byref(opt), C.byref(proj), None) == _abi.GS_ERR_ARG
+    bad = api.make_options(7)
+    assert lib.gs_preprocess(C.byref(p), C.byref(cam), C.byref(bad), C.byref(proj), None) == _abi.GS_ERR_ARG
+    assert b"sh_degree" in lib.gs_last_error_message()
+    neg = _abi.gs_params(n=-1)
+    assert lib.gs_preprocess(C.byref(neg), C.byref(cam), C.byref(opt), C.byref(proj), None) == _abi.GS_ERR_ARG
+    big = _cam(w=100000)
+    assert lib.gs_preprocess(C.byref(p), C.byref(big), C.byref(opt), C.byref(proj), None) == _abi.GS_ERR_ARG
+    mode = api.make_options(0, bwd_mode=9)
+    assert lib.gs_render_bwd(C.byref(proj), None, None, C.byref(cam), C.byref(mode), None, None, None, None,
+                             None) == _abi.GS_ERR_ARG
+    d = C.c_int64(0)
+    assert lib.gs_bin_and_sort(C.byref(proj), C.byref(cam), C.byref(opt), None, 0, None, None, -5, C.byref(d),
+                               None, None) == _abi.GS_ERR_ARG
+    misaligned = _abi.gs_proj(rec=8, depth=16, radius=16, tiles_touched=16, n=10)
+    assert lib.gs_render_fwd(C.byref(misaligned), 16, 16, C.byref(cam), C.byref(opt), 16, 16, 16,
+                             None) == _abi.GS_ERR_ARG
+    assert b"16-byte" in lib.gs_last_error_message()
+
+
+def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _abi.load()

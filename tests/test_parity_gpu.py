@@ -1,0 +1,313 @@
+"""Parity of the CUDA library (through its C ABI) with the float64 oracle, stage by stage and end
+to end, on seeded scenes shaped like the five configurations (smaller sizes that span many tiles
+and a ragged image edge) plus edge cases, and on the full 1.6M-Gaussian 1297x840 scene.
+
+Bars: bit-exact for depth keys, duplicate counts, sorted (tile, depth, index) lists, tile ranges
+and contributor counts (outside the oracle's marginal decisions); 1e-5 max abs error on pixels;
+1e-4 of max|grad| per gradient tensor.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import gs_scenes  # noqa: E402
+import oracle  # noqa: E402
+from differentiable_gaussian_splatting_gs_gb300 import _abi, api, step  # noqa: E402
+
+from _cases import CASES, GRAD2D_GROUPS, GRAD_KEYS, PARAM_NAMES, grad_close, scene, stage_inputs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+MODES = ["direct", "warp", "adaptive", "sm"]
+STAGINGS = [_abi.GS_STAGE_BULK, _abi.GS_STAGE_LOADS]
+
+
+def u32(t):
+    return t.detach().cpu().numpy().view(np.uint32)
+
+
+def dev_params(s):
+    return {k: torch.from_numpy(np.ascontiguousarray(getattr(s, k))).to(DEV) for k in PARAM_NAMES}
+
+
+def dev_proj(rec):
+    return api.proj_from_arrays(rec["mean2d"], rec["conic"], rec["opacity"], rec["rgb"], rec["depth"], rec["radius"],
+                                DEV)
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    yield
+    assert api.gs_device_error() == _abi.GS_OK, "device error word set"
+
+
+# --------------------------------------------------------------------------------- bounded wait
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    lib = _abi.load()
+    assert lib.gs_selftest_timeout(64, None) == 0
+    assert api.gs_device_error() == _abi.GS_ERR_TIMEOUT
+    assert api.gs_device_error() == _abi.GS_OK  # cleared, context still usable
+    x = torch.arange(10, device=DEV).sum().item()
+    assert x == 45
+
+
+# --------------------------------------------------------------------------------- preprocess
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_preprocess_matches_oracle(name):
+    d = stage_inputs(name)
+    s, cam, pre = d["scene"], d["cam"], d["pre"]
+    proj = api.gs_preprocess(dev_params(s), cam, api.make_options(s.sh_degree))
+    rec = proj.rec.cpu().numpy()
+    radius = proj.radius.cpu().numpy()
+    tt = u32(proj.tiles_touched)
+    depth = proj.depth.cpu().numpy()
+    assert np.array_equal(depth.view(np.uint32), pre["depth"].view(np.uint32)), "depth keys differ"
+    marginal = (pre["flags"] & 6) != 0
+    ok = ~marginal
+    assert np.array_equal(radius[ok], pre["radius"][ok])
+    assert np.array_equal(tt[ok], pre["tiles_touched"][ok])
+    live = ok & (pre["radius"] > 0)
+    for cols, ref in ((slice(0, 2), pre["mean2d"]), (slice(2, 5), pre["conic"]), (slice(5, 6), pre["opacity"][:, None]),
+                      (slice(6, 9), pre["rgb"])):
+        got, want = rec[live, cols].astype(np.float64), ref[live]
+        err = np.abs(got - want)
+        bound = 1e-5 * np.abs(want) + 1e-6 * np.abs(want).max(axis=0)
+        assert np.all(err <= bound), f"cols {cols}: worst {(err / np.maximum(bound, 1e-30)).max():.3g} x bound"
+    assert np.all(rec[~(radius > 0)] == 0.0)
+    assert marginal.sum() <= max(2, 1e-3 * s.n)
+
+
+def test_preprocess_empty_and_all_culled():
+    opt = api.make_options(0)
+    cam = gs_scenes.make_scene(0).cameras[0]
+    empty = {k: torch.empty((0,) + shp, dtype=torch.float32, device=DEV)
+             for k, shp in (("mean3d", (3,)), ("log_scale", (3,)), ("quat", (4,)), ("opacity_logit", ()),
+                            ("sh", (1, 3)))}
+    proj = api.gs_preprocess(empty, cam, opt)
+    assert proj.n == 0
+    s = gs_scenes.make_scene(0, n=500)
+    s.mean3d[:, 2] = -1.0  # everything behind the camera
+    proj = api.gs_preprocess(dev_params(s), cam, opt)
+    assert int(proj.radius.max()) == 0 and int(proj.tiles_touched.max()) == 0
+    b = api.gs_bin_and_sort(proj, cam, opt)
+    assert b.n_dup == 0 and int(b.ranges.abs().max()) == 0
+    img, tf, nc = api.gs_render_fwd(proj, b.vals, b.ranges, cam, opt)
+    assert float(img.abs().max()) == 0.0 and float(tf.min()) == 1.0 and int(nc.max()) == 0
+
+
+# --------------------------------------------------------------------------------- binning / sort
+
+def _check_bin(rec, cam, b):
+    keys, vals, ranges = oracle.bin_and_sort(rec["mean2d"], rec["depth"], rec["radius"], cam.width, cam.height)
+    assert b.n_dup == len(vals)
+    assert np.array_equal(u32(b.vals), vals)
+    if b.keys is not None:
+        assert np.array_equal(b.keys.cpu().numpy().view(np.uint64), keys)
+    assert np.array_equal(u32(b.ranges), ranges)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_bin_and_sort_bit_exact(name):
+    d = stage_inputs(name)
+    proj = dev_proj(d["rec"])
+    b = api.gs_bin_and_sort(proj, d["cam"], api.make_options(d["scene"].sh_degree))
+    assert b.n_dup == len(d["vals"])
+    assert np.array_equal(u32(b.vals), d["vals"])
+    assert np.array_equal(b.keys.cpu().numpy().view(np.uint64), d["keys"])
+    assert np.array_equal(u32(b.ranges), d["ranges"])
+
+
+@pytest.mark.parametrize("W,H,n", [(16, 16, 300), (17, 9, 200), (200, 120, 3000), (4112, 4112, 400)])
+def test_bin_and_sort_tile_pass_counts_and_ties(W, H, n):
+    """Single tile (no tile pass), ragged edges, one and two passes, and > 65536 tiles (three
+    passes); a third of the depths tie exactly, so index order decides."""
+    rng = np.random.default_rng(W * 7 + H)
+    mean2d = np.stack([rng.uniform(-40, W + 40, n), rng.uniform(-40, H + 40, n)], 1).astype(np.float32)
+    mean2d[: n // 10] = np.floor(mean2d[: n // 10]) + 0.5
+    radius = rng.integers(0, min(60, 2 * max(W, H)), n).astype(np.int32)
+    depth = rng.uniform(1, 3, n).astype(np.float32)
+    depth[::3] = depth[0]
+    rec = dict(mean2d=mean2d, conic=np.tile([0.1, 0.0, 0.1], (n, 1)), opacity=np.full(n, 0.5),
+               rgb=np.full((n, 3), 0.5), depth=depth, radius=radius)
+    cam = gs_scenes.Camera(R=np.eye(3, dtype=np.float32).reshape(9), t=np.zeros(3, np.float32), fx=100.0, fy=100.0,
+                           cx=W / 2, cy=H / 2, width=W, height=H, bg=np.zeros(3, np.float32))
+    b = api.gs_bin_and_sort(dev_proj(rec), cam, api.make_options(0))
+    _check_bin(rec, cam, b)
+
+
+def test_bin_and_sort_capacity_error_reports_required_size():
+    d = stage_inputs("tiny")
+    proj = dev_proj(d["rec"])
+    with pytest.raises(_abi.GsError) as ei:
+        api.gs_bin_and_sort(proj, d["cam"], api.make_options(0), capacity=10)
+    assert ei.value.status == _abi.GS_ERR_CAPACITY
+    b = api.gs_bin_and_sort(proj, d["cam"], api.make_options(0), capacity=len(d["vals"]))
+    assert np.array_equal(u32(b.vals), d["vals"])
+
+
+def test_bin_and_sort_without_keys():
+    d = stage_inputs("object")
+    b = api.gs_bin_and_sort(dev_proj(d["rec"]), d["cam"], api.make_options(3), want_keys=False)
+    assert b.keys is None and np.array_equal(u32(b.vals), d["vals"])
+
+
+# --------------------------------------------------------------------------------- forward
+
+def _fwd(d, staging):
+    proj = dev_proj(d["rec"])
+    opt = api.make_options(d["scene"].sh_degree, staging=staging)
+    b = api.gs_bin_and_sort(proj, d["cam"], opt)
+    img, tf, nc = api.gs_render_fwd(proj, b.vals, b.ranges, d["cam"], opt)
+    return proj, b, opt, img, tf, nc
+
+
+@pytest.mark.parametrize("staging", STAGINGS)
+@pytest.mark.parametrize("name", list(CASES))
+def test_render_fwd_matches_oracle(name, staging):
+    d = stage_inputs(name)
+    _, _, _, img, tf, nc = _fwd(d, staging)
+    f = d["fwd"]
+    ok = f["pix_flags"] == 0
+    assert (~ok).sum() <= max(3, 1e-2 * ok.size), f"{(~ok).sum()} marginal pixels"
+    err = np.abs(img.cpu().numpy() - f["image"])
+    assert err[:, ok].max() <= 1e-5, err[:, ok].max()
+    assert np.array_equal(u32(nc)[ok], f["n_contrib"][ok])
+    assert np.allclose(tf.cpu().numpy()[ok], f["t_final"][ok], rtol=1e-4, atol=1e-7)
+    # marginal pixels differ at most by the last Gaussian's contribution
+    assert err.max() <= 0.02
+
+
+# --------------------------------------------------------------------------------- backward
+
+@pytest.mark.parametrize("staging", STAGINGS)
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("name", list(CASES))
+def test_render_bwd_matches_oracle(name, mode, staging):
+    d = stage_inputs(name)
+    proj, b, _, img, tf, nc = _fwd(d, staging)
+    opt = api.make_options(d["scene"].sh_degree, bwd_mode=mode, staging=staging)
+    g2 = api.gs_render_bwd(proj, b.vals, b.ranges, d["cam"], opt, torch.from_numpy(d["dl"]).to(DEV), tf, nc)
+    got = g2.cpu().numpy()
+    assert np.all(got[:, 9:] == 0.0)
+    for group, cols in GRAD2D_GROUPS.items():
+        ok, err, tol = grad_close(got[:, cols], d["grad2d"][:, cols])
+        assert ok, f"{group}: error {err:.3g} > {tol:.3g}"
+
+
+@pytest.mark.parametrize("thr", [1, 16, 33])
+def test_adaptive_threshold_extremes(thr):
+    d = stage_inputs("contention")
+    proj, b, _, img, tf, nc = _fwd(d, _abi.GS_STAGE_BULK)
+    for mode in ("adaptive", "sm"):
+        opt = api.make_options(0, bwd_mode=mode, adaptive_threshold=thr)
+        got = api.gs_render_bwd(proj, b.vals, b.ranges, d["cam"], opt, torch.from_numpy(d["dl"]).to(DEV), tf,
+                                nc).cpu().numpy()
+        for group, cols in GRAD2D_GROUPS.items():
+            ok, err, tol = grad_close(got[:, cols], d["grad2d"][:, cols])
+            assert ok, f"{mode}/{thr}/{group}: {err:.3g} > {tol:.3g}"
+
+
+# --------------------------------------------------------------------------------- preprocess backward
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_preprocess_bwd_matches_oracle(name):
+    d = stage_inputs(name)
+    s, cam = d["scene"], d["cam"]
+    params = dev_params(s)
+    opt = api.make_options(s.sh_degree)
+    proj = api.gs_preprocess(params, cam, opt)
+    g2 = torch.zeros((s.n, 12), dtype=torch.float32, device=DEV)
+    g2[:, :9] = torch.from_numpy(d["grad2d32"]).to(DEV)
+    grads = api.gs_preprocess_bwd(params, cam, opt, proj, g2)
+    ok_rows = (d["pre"]["flags"] & 6) == 0
+    for name_p in PARAM_NAMES:
+        got = grads[name_p].cpu().numpy().reshape(s.n, -1)
+        want = d["grads"][GRAD_KEYS[name_p]].reshape(s.n, -1)
+        ok, err, tol = grad_close(got, want, mask=ok_rows)
+        assert ok, f"{name_p}: {err:.3g} > {tol:.3g}"
+
+
+def test_preprocess_bwd_accumulates_views():
+    s, _ = scene("large")
+    params = dev_params(s)
+    opt = api.make_options(s.sh_degree)
+    grads = api.alloc_param_grads(params)
+    want = None
+    for v, cam in enumerate(s.cameras):
+        g2n = np.random.default_rng(v).standard_normal((s.n, 9)).astype(np.float32)
+        proj = api.gs_preprocess(params, cam, opt)
+        g2 = torch.zeros((s.n, 12), dtype=torch.float32, device=DEV)
+        g2[:, :9] = torch.from_numpy(g2n).to(DEV)
+        api.gs_preprocess_bwd(params, cam, opt, proj, g2, out=grads, accumulate=v > 0)
+        o = oracle.preprocess_bwd(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, s.sh_degree, cam, g2n)
+        want = o if want is None else {k: want[k] + o[k] for k in o}
+    for name_p in PARAM_NAMES:
+        got = grads[name_p].cpu().numpy().reshape(s.n, -1)
+        ok, err, tol = grad_close(got, want[GRAD_KEYS[name_p]].reshape(s.n, -1))
+        assert ok, f"{name_p}: {err:.3g} > {tol:.3g}"
+
+
+# --------------------------------------------------------------------------------- end to end
+
+def _filter_lists(vals, ranges, drop):
+    """Per-tile lists with the entries of Gaussians in `drop` removed."""
+    return [tuple(g for g in vals[a:b] if not drop[g]) for a, b in ranges]
+
+
+def _end_to_end(s, view, mode="sm"):
+    cam = s.cameras[view]
+    params = dev_params(s)
+    opt = api.make_options(s.sh_degree, bwd_mode=mode)
+    ref = oracle.view_step(s, view=view)
+    bufs = step.StepBuffers(s.n, DEV)
+    proj = api.gs_preprocess(params, cam, opt, out=bufs.proj)
+    b = api.gs_bin_and_sort(proj, cam, opt, buffers=bufs.sort)
+    img, tf, nc = api.gs_render_fwd(proj, b.vals, b.ranges, cam, opt)
+    g2 = api.gs_render_bwd(proj, b.vals, b.ranges, cam, opt, torch.from_numpy(ref["dl_dimage"]).to(DEV), tf, nc)
+    grads = api.gs_preprocess_bwd(params, cam, opt, proj, g2)
+    pre = ref["pre"]
+    flagged = (pre["flags"] & 6) != 0
+    # sorted lists: identical after removing the entries of Gaussians with a marginal radius or rectangle
+    gl = _filter_lists(u32(b.vals), u32(b.ranges), flagged)
+    ol = _filter_lists(ref["vals"], ref["ranges"], flagged)
+    assert gl == ol
+    # tiles whose full lists differ (a marginal Gaussian decided differently) are left out of the pixel check
+    gfull = _filter_lists(u32(b.vals), u32(b.ranges), np.zeros(s.n, bool))
+    ofull = _filter_lists(ref["vals"], ref["ranges"], np.zeros(s.n, bool))
+    bad_tiles = np.array([a != c for a, c in zip(gfull, ofull)])
+    TX = (cam.width + 15) // 16
+    ys, xs = np.mgrid[0:cam.height, 0:cam.width]
+    pix_bad = bad_tiles[(ys // 16) * TX + xs // 16]
+    ok = (ref["fwd"]["pix_flags"] == 0) & ~pix_bad
+    err = np.abs(img.cpu().numpy() - ref["fwd"]["image"])
+    assert err[:, ok].max() <= 1e-5, err[:, ok].max()
+    assert np.array_equal(u32(nc)[ok], ref["fwd"]["n_contrib"][ok])
+    for name_p in PARAM_NAMES:
+        got = grads[name_p].cpu().numpy().reshape(s.n, -1)
+        want = ref["grads"][GRAD_KEYS[name_p]].reshape(s.n, -1)
+        okg, e, tol = grad_close(got, want, mask=~flagged)
+        assert okg, f"{name_p}: {e:.3g} > {tol:.3g}"
+    return ref, b
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_end_to_end_matches_oracle(name):
+    s, view = scene(name)
+    _end_to_end(s, view)
+
+
+def test_full_size_outdoor_scene():
+    """The 1.6M-Gaussian 1297x840 scene in the launch configuration the benchmark times: the
+    whole training step against the whole oracle."""
+    s = gs_scenes.make_scene(2)
+    ref, b = _end_to_end(s, 0)
+    assert b.n_dup == pytest.approx(len(ref["vals"]), abs=64)
