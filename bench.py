@@ -118,6 +118,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Maximum of x over all ranks (the slowest rank's time); identity for one rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput_mpix(world: int, pixels_per_view: int, ms_per_step: float) -> float:
+    """Whole-job Mpix/s: every rank renders one view per step; the step takes the slowest rank's time."""
+    return world * pixels_per_view / (ms_per_step / 1e3) / 1e6
+
+
 def load_json(path):
     try:
         with open(path) as f:
@@ -277,12 +293,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     torch.cuda.synchronize()
     launches = lib.gs_kernel_launches() - launches0
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * P / (ms / 1e3) / 1e6
+    ms = reduce_max(sum(step_ms) / len(step_ms), world, dev)
+    value = throughput_mpix(world, P, ms)
 
     # ---- end to end: inputs from pinned host memory, gradients back, inside the timed region
     e2e = None
@@ -305,12 +317,8 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize()
             e_ms.append(e0.elapsed_time(e1))
         barrier()
-        em = sum(e_ms) / len(e_ms)
-        if world > 1:
-            t = torch.tensor([em], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            em = float(t.item())
-        e2e = {"value": world * P / (em / 1e3) / 1e6, "unit": "Mpix/s", "ms_per_step": em,
+        em = reduce_max(sum(e_ms) / len(e_ms), world, dev)
+        e2e = {"value": throughput_mpix(world, P, em), "unit": "Mpix/s", "ms_per_step": em,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
     assert api.gs_device_error() == 0
 

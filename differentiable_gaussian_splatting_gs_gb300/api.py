@@ -24,8 +24,20 @@ __all__ = ["Proj", "BinResult", "make_camera", "make_options", "alloc_proj", "gs
            "gs_device_error", "GsError", "GS_BWD_DIRECT", "GS_BWD_WARP", "GS_BWD_ADAPTIVE", "GS_BWD_SM"]
 
 
+_dummy = {}
+
+
 def _ptr(t) -> int | None:
-    return None if t is None else t.data_ptr()
+    """Device address of a tensor; an empty tensor gets the address of a small valid buffer
+    (torch reports 0 for it, which the C ABI rejects as NULL)."""
+    if t is None:
+        return None
+    if t.numel() == 0:
+        key = str(t.device)
+        if key not in _dummy:
+            _dummy[key] = torch.zeros(64, dtype=torch.float32, device=t.device)
+        return _dummy[key].data_ptr()
+    return t.data_ptr()
 
 
 def _stream(stream) -> int:

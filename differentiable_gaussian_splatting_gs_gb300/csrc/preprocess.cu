@@ -17,14 +17,25 @@ struct Geo {
     float qinv;        // 1 / |q|
     float Rq[9];       // rotation of the Gaussian
     float s[3];        // scales
-    float Sig[6];      // 3D covariance (xx, xy, xz, yy, yz, zz)
+    float M3[9];       // Rq diag(s): Sigma = M3 M3^T
     float J00, J02, J11, J12;
     bool clx, cly;     // x/z, y/z were clamped
     float T[6];        // J W, 2x3 row-major
+    float K[6];        // T M3, 2x3: the 2D covariance before dilation is K K^T
+    float n[3];        // K0 x K1 (rows of K), its components are the 2x2 minors of K
     float a, b, c;     // dilated 2D covariance
+    float det;         // a c - b^2
     float A, B, C;     // conic
     float mx, my;
 };
+
+// a d - b c with one rounding error (fma-based difference of products)
+__device__ __forceinline__ float diff_of_products(float a, float d, float b, float c) {
+    const float w = b * c;
+    const float e = __fmaf_rn(-b, c, w);
+    const float f = __fmaf_rn(a, d, -w);
+    return f + e;
+}
 
 // Shared forward geometry of one Gaussian; false when it is culled by depth or determinant.
 __device__ __forceinline__ bool geometry(const float* m, const float* ls, const float* q,
@@ -38,7 +49,7 @@ __device__ __forceinline__ bool geometry(const float* m, const float* ls, const 
     g.p[1] = __fmaf_rn(R[3], m[0], __fmaf_rn(R[4], m[1], __fmaf_rn(R[5], m[2], t[1])));
 
     const float qq = q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3];
-    g.qinv = rsqrtf(qq);
+    g.qinv = 1.f / sqrtf(qq);
     const float w = q[0] * g.qinv, x = q[1] * g.qinv, y = q[2] * g.qinv, z = q[3] * g.qinv;
     g.qn[0] = w; g.qn[1] = x; g.qn[2] = y; g.qn[3] = z;
     float* Rq = g.Rq;
@@ -46,16 +57,8 @@ __device__ __forceinline__ bool geometry(const float* m, const float* ls, const 
     Rq[3] = 2.f * (x * y + w * z);       Rq[4] = 1.f - 2.f * (x * x + z * z); Rq[5] = 2.f * (y * z - w * x);
     Rq[6] = 2.f * (x * z - w * y);       Rq[7] = 2.f * (y * z + w * x);       Rq[8] = 1.f - 2.f * (x * x + y * y);
     for (int k = 0; k < 3; ++k) g.s[k] = expf(ls[k]);
-    // M = Rq diag(s); Sigma = M M^T
-    float M[9];
     for (int i = 0; i < 3; ++i)
-        for (int k = 0; k < 3; ++k) M[3 * i + k] = Rq[3 * i + k] * g.s[k];
-    g.Sig[0] = M[0] * M[0] + M[1] * M[1] + M[2] * M[2];
-    g.Sig[1] = M[0] * M[3] + M[1] * M[4] + M[2] * M[5];
-    g.Sig[2] = M[0] * M[6] + M[1] * M[7] + M[2] * M[8];
-    g.Sig[3] = M[3] * M[3] + M[4] * M[4] + M[5] * M[5];
-    g.Sig[4] = M[3] * M[6] + M[4] * M[7] + M[5] * M[8];
-    g.Sig[5] = M[6] * M[6] + M[7] * M[7] + M[8] * M[8];
+        for (int k = 0; k < 3; ++k) g.M3[3 * i + k] = Rq[3 * i + k] * g.s[k];
 
     // pinhole Jacobian at p with x/z, y/z clamped to the widened field of view
     const float zi = 1.f / g.p[2];
@@ -68,23 +71,29 @@ __device__ __forceinline__ bool geometry(const float* m, const float* ls, const 
     g.J02 = -cam.fx * u * zi;
     g.J11 = cam.fy * zi;
     g.J12 = -cam.fy * v * zi;
-    // T = J W (W = camera rotation)
+    // T = J W (W = camera rotation), K = T M3
     for (int j = 0; j < 3; ++j) {
         g.T[j] = g.J00 * R[j] + g.J02 * R[6 + j];
         g.T[3 + j] = g.J11 * R[3 + j] + g.J12 * R[6 + j];
     }
-    const float* S = g.Sig;
-    float TS[6];  // T Sigma
-    for (int i = 0; i < 2; ++i) {
-        const float* Ti = g.T + 3 * i;
-        TS[3 * i + 0] = Ti[0] * S[0] + Ti[1] * S[1] + Ti[2] * S[2];
-        TS[3 * i + 1] = Ti[0] * S[1] + Ti[1] * S[3] + Ti[2] * S[4];
-        TS[3 * i + 2] = Ti[0] * S[2] + Ti[1] * S[4] + Ti[2] * S[5];
-    }
-    g.a = TS[0] * g.T[0] + TS[1] * g.T[1] + TS[2] * g.T[2] + cam.lowpass;
-    g.b = TS[0] * g.T[3] + TS[1] * g.T[4] + TS[2] * g.T[5];
-    g.c = TS[3] * g.T[3] + TS[4] * g.T[4] + TS[5] * g.T[5] + cam.lowpass;
-    const float det = g.a * g.c - g.b * g.b;
+    for (int r = 0; r < 2; ++r)
+        for (int k = 0; k < 3; ++k)
+            g.K[3 * r + k] = g.T[3 * r] * g.M3[k] + g.T[3 * r + 1] * g.M3[3 + k] + g.T[3 * r + 2] * g.M3[6 + k];
+    const float* K = g.K;
+    const float a0 = K[0] * K[0] + K[1] * K[1] + K[2] * K[2];
+    const float c0 = K[3] * K[3] + K[4] * K[4] + K[5] * K[5];
+    g.b = K[0] * K[3] + K[1] * K[4] + K[2] * K[5];
+    // det(K K^T) as the sum of the squared 2x2 minors of K (Cauchy-Binet): no cancellation
+    const float m01 = diff_of_products(K[0], K[4], K[1], K[3]);
+    const float m02 = diff_of_products(K[0], K[5], K[2], K[3]);
+    const float m12 = diff_of_products(K[1], K[5], K[2], K[4]);
+    const float det0 = m01 * m01 + m02 * m02 + m12 * m12;
+    g.n[0] = m12; g.n[1] = -m02; g.n[2] = m01;
+    const float lp = cam.lowpass;
+    g.a = a0 + lp;
+    g.c = c0 + lp;
+    const float det = det0 + lp * (a0 + c0) + lp * lp;
+    g.det = det;
     if (!(det > 0.f)) return false;
     const float di = 1.f / det;
     g.A = g.c * di;
@@ -231,30 +240,42 @@ __global__ void __launch_bounds__(256) k_preprocess_bwd(
         dm[2] += (gd[2] - dot * uz) * vinv;
     }
 
-    // conic (A, B, C) = inverse of [[a, b], [b, c]]: dL/dSigma' = -M G M with G = [[dA, dB/2], [dB/2, dC]]
-    const float hb = 0.5f * dB;
-    const float MG00 = g.A * dA + g.B * hb, MG01 = g.A * hb + g.B * dC;
-    const float MG10 = g.B * dA + g.C * hb, MG11 = g.B * hb + g.C * dC;
-    const float da = -(MG00 * g.A + MG01 * g.B);
-    const float dbh = -(MG00 * g.B + MG01 * g.C);  // d/dSigma'_01 (one off-diagonal slot)
-    const float dcc = -(MG10 * g.B + MG11 * g.C);
-    // Sigma' = T Sigma T^T (+ lowpass I): H = [[da, dbh], [dbh, dcc]]
-    // dL/dSigma = T^T H T ; dL/dT = 2 H T Sigma
-    const float* T = g.T;
-    float HT[6];
-    for (int j = 0; j < 3; ++j) {
-        HT[j] = da * T[j] + dbh * T[3 + j];
-        HT[3 + j] = dbh * T[j] + dcc * T[3 + j];
+    // Conic M = Sigma'^-1 with Sigma' = K K^T + lp I. With G = [[dA, dB/2], [dB/2, dC]] (B sits in both
+    // off-diagonal slots), dL/dSigma' = -M G M and dL/dK = -2 M G M K. Forming M G M and then
+    // multiplying by K cancels catastrophically for elongated Gaussians, so the chain is evaluated as
+    //   Y = M K = [lp K0 + K1 x n ; lp K1 - K0 x n] / det    (n = K0 x K1; from a K0 - b K1 expanded with
+    //                                                          the vector triple product, no cancellation)
+    //   W = G Y,   dL/dK = -2 M W (M applied through the adjugate),
+    //   dL/dlog s_k = -2 y_k^T G y_k = -2 (Y0_k W0_k + Y1_k W1_k)   (y_k = column k of Y).
+    const float* Kp = g.K;
+    const float* nv = g.n;
+    const float lp = cam.lowpass, idet = 1.f / g.det;
+    float Y0[3], Y1[3];
+    {
+        const float c0x = diff_of_products(Kp[4], nv[2], Kp[5], nv[1]);  // K1 x n
+        const float c0y = diff_of_products(Kp[5], nv[0], Kp[3], nv[2]);
+        const float c0z = diff_of_products(Kp[3], nv[1], Kp[4], nv[0]);
+        const float c1x = diff_of_products(Kp[1], nv[2], Kp[2], nv[1]);  // K0 x n
+        const float c1y = diff_of_products(Kp[2], nv[0], Kp[0], nv[2]);
+        const float c1z = diff_of_products(Kp[0], nv[1], Kp[1], nv[0]);
+        Y0[0] = (lp * Kp[0] + c0x) * idet; Y0[1] = (lp * Kp[1] + c0y) * idet; Y0[2] = (lp * Kp[2] + c0z) * idet;
+        Y1[0] = (lp * Kp[3] - c1x) * idet; Y1[1] = (lp * Kp[4] - c1y) * idet; Y1[2] = (lp * Kp[5] - c1z) * idet;
     }
-    float dSig[9];
-    for (int r0 = 0; r0 < 3; ++r0)
-        for (int c0 = 0; c0 < 3; ++c0) dSig[3 * r0 + c0] = T[r0] * HT[c0] + T[3 + r0] * HT[3 + c0];
-    const float* S = g.Sig;
-    const float Sf[9] = {S[0], S[1], S[2], S[1], S[3], S[4], S[2], S[4], S[5]};
+    const float hb = 0.5f * dB;
+    float dK[6];
+    for (int j = 0; j < 3; ++j) {
+        const float W0 = dA * Y0[j] + hb * Y1[j];
+        const float W1 = hb * Y0[j] + dC * Y1[j];
+        dK[j] = -2.f * (g.c * W0 - g.b * W1) * idet;
+        dK[3 + j] = -2.f * (g.a * W1 - g.b * W0) * idet;
+        dls[j] = -2.f * (Y0[j] * W0 + Y1[j] * W1);
+    }
+    const float* T = g.T;
+    const float* M3 = g.M3;
     float dT[6];
     for (int r0 = 0; r0 < 2; ++r0)
         for (int c0 = 0; c0 < 3; ++c0)
-            dT[3 * r0 + c0] = 2.f * (HT[3 * r0] * Sf[c0] + HT[3 * r0 + 1] * Sf[3 + c0] + HT[3 * r0 + 2] * Sf[6 + c0]);
+            dT[3 * r0 + c0] = dK[3 * r0] * M3[3 * c0] + dK[3 * r0 + 1] * M3[3 * c0 + 1] + dK[3 * r0 + 2] * M3[3 * c0 + 2];
     // T = J W: dJ = dT W^T (only the non-zero entries of J are needed)
     const float* R = cam.R;
     const float dJ00 = dT[0] * R[0] + dT[1] * R[1] + dT[2] * R[2];
@@ -278,17 +299,11 @@ __global__ void __launch_bounds__(256) k_preprocess_bwd(
     // p = W mean + t
     for (int k = 0; k < 3; ++k) dm[k] += R[k] * dp[0] + R[3 + k] * dp[1] + R[6 + k] * dp[2];
 
-    // Sigma = M M^T, M = Rq diag(s): dM = 2 dSigma M (dSigma symmetric)
+    // M3 = Rq diag(s): dL/dM3 = T^T dL/dK, dRq = dL/dM3 diag(s)
     const float* Rq = g.Rq;
     float dRq[9];
     for (int r0 = 0; r0 < 3; ++r0)
-        for (int k = 0; k < 3; ++k) {
-            float acc = 0.f;
-            for (int j = 0; j < 3; ++j) acc += dSig[3 * r0 + j] * Rq[3 * j + k];
-            const float dMrk = 2.f * acc * g.s[k];   // dL/dM[r0][k]
-            dRq[3 * r0 + k] = dMrk * g.s[k];
-            dls[k] += dMrk * Rq[3 * r0 + k] * g.s[k];  // dL/ds_k * s_k
-        }
+        for (int k = 0; k < 3; ++k) dRq[3 * r0 + k] = (T[r0] * dK[k] + T[3 + r0] * dK[3 + k]) * g.s[k];
     // rotation of the normalised quaternion (w, x, y, z)
     const float w = g.qn[0], x = g.qn[1], y = g.qn[2], z = g.qn[3];
     const float* G = dRq;

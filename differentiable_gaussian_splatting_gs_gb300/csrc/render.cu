@@ -16,6 +16,9 @@
 // sqrt(2 tau Sigma'_yy) with Sigma' the inverse of the conic. The extents are widened (tau by
 // 0.1 %, extents by 0.1 % + 0.01 px) so that no pair the per-pixel test would blend is dropped;
 // dropped pairs are exactly ones the per-pixel test skips, so the results do not change.
+//
+// The "skip when power > 0" rule never fires here: power is evaluated as a sum of non-negative
+// terms times -1/2 (see prepare_record), which cannot be positive.
 #include "gs_common.cuh"
 #include "gs_internal.h"
 
@@ -42,17 +45,34 @@ struct BwdSmem {
     unsigned wmax[8];
 };
 
-__device__ __forceinline__ float4 cull_box(const float4 r0, const float4 r1) {
+// Prepares a staged record for evaluation and returns its culling box.
+//
+// The quadratic form -power = (A dx^2 + C dy^2)/2 + B dx dy is evaluated by completing the square,
+// (A u^2 + D dy^2) / 2 with u = dx + r dy, r = B / A and D = det / A, det = A C - B^2: both terms
+// are non-negative, so the evaluation has no cancellation even for very elongated Gaussians
+// (where the three terms of the plain form are large and nearly cancel). det is computed with
+// one rounding error. The record's C slot is replaced by D and slot 9 receives r; A and B stay.
+// A record whose conic is not positive definite is never blended (empty box).
+//
+// Box: the set alpha >= 1/255 is -power <= tau = ln(255 opacity), whose axis-aligned half-extents
+// are sqrt(2 tau Sigma'_xx) = sqrt(2 tau C / det) and sqrt(2 tau A / det).
+__device__ __forceinline__ float4 prepare_record(float4& r0, float4& r1, float4& r2) {
     const float mx = r0.x, my = r0.y, A = r0.z, B = r0.w, C = r1.x, o = r1.y;
     const float inf = __int_as_float(0x7f800000);
-    if (!(o * 1.00001f >= kAlphaMin)) return make_float4(inf, -inf, inf, -inf);  // never blended
-    const float tau = logf(255.0f * o * 1.00001f) * 1.001f + 0.001f;
-    // det = A C - B^2 with one rounding error (fma-based difference of products)
+    const float4 empty = make_float4(inf, -inf, inf, -inf);
     const float w = B * B;
     const float e = __fmaf_rn(-B, B, w);
     const float f = __fmaf_rn(A, C, -w);
     const float det = f + e;
-    if (!(det > 0.f)) return make_float4(-inf, inf, -inf, inf);  // degenerate conic: never culled
+    if (!(A > 0.f) || !(det > 0.f) || !(det < inf)) {
+        r1.x = 0.f;
+        r2.y = 0.f;
+        return empty;
+    }
+    r1.x = det / A;   // D
+    r2.y = B / A;     // r
+    if (!(o * 1.00001f >= kAlphaMin)) return empty;  // alpha = min(0.99, o G) <= o < 1/255: never blended
+    const float tau = logf(255.0f * o * 1.00001f) * 1.001f + 0.001f;
     const float hx = sqrtf(2.f * tau * C / det) * 1.001f + 0.01f;
     const float hy = sqrtf(2.f * tau * A / det) * 1.001f + 0.01f;
     if (!(hx < inf && hy < inf)) return make_float4(-inf, inf, -inf, inf);
@@ -189,7 +209,9 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
             ok = stage_wait<STAGING>(s, slot, (unsigned)(b >> 1) & 1u, n_in, pre, spin_limit, err);
             if (ok) consumed = b;
         }
-        if (threadIdx.x < n_in) s.box[threadIdx.x] = cull_box(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1]);
+        if (threadIdx.x < n_in)
+            s.box[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
+                                                s.rec[slot][threadIdx.x][2]);
         if (__syncthreads_or(!ok)) break;
         const int nl = compact_warp(s, n_in, kBatch, wx0, wx1, wy0, wy1, warp, lane);
         for (int k = 0; k < nl; ++k) {
@@ -198,9 +220,11 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
             const float4 r0 = s.rec[slot][j][0];
             const float4 r1 = s.rec[slot][j][1];
             if (!done) {
+                const float2 r2 = *reinterpret_cast<const float2*>(&s.rec[slot][j][2]);  // (b, r)
                 const float dx = r0.x - fpx, dy = r0.y - fpy;
-                const float power = -0.5f * (r0.z * dx * dx + r1.x * dy * dy) - r0.w * dx * dy;
-                if (power <= 0.f) {
+                const float u = __fmaf_rn(r2.y, dy, dx);
+                const float power = -0.5f * (r0.z * u * u + r1.x * dy * dy);  // <= 0 by construction
+                {
                     const float alpha = fminf(kAlphaMax, r1.y * __expf(power));
                     if (alpha >= kAlphaMin) {
                         const float test_T = T * (1.f - alpha);
@@ -208,7 +232,7 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
                             done = true;
                         } else {
                             const float w = alpha * T;
-                            const float cb = s.rec[slot][j][2].x;
+                            const float cb = r2.x;
                             col0 += r1.z * w;
                             col1 += r1.w * w;
                             col2 += cb * w;
@@ -346,7 +370,9 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
             ok = stage_wait<STAGING>(s, slot, (unsigned)(it >> 1) & 1u, n_in, pre, spin_limit, err);
             if (ok) consumed = it;
         }
-        if (threadIdx.x < n_in) s.box[threadIdx.x] = cull_box(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1]);
+        if (threadIdx.x < n_in)
+            s.box[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
+                                                s.rec[slot][threadIdx.x][2]);
         if (MODE == GS_BWD_SM)
             for (int e = threadIdx.x; e < kBatch * 9; e += kBlock) sm.acc[e] = 0.f;
         if (__syncthreads_or(!ok)) break;
@@ -357,19 +383,22 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
             const unsigned pos = (unsigned)(b * kBatch + j);
             const float4 r0 = s.rec[slot][j][0];
             const float4 r1 = s.rec[slot][j][1];
+            const float2 r2 = *reinterpret_cast<const float2*>(&s.rec[slot][j][2]);  // (b, r)
             const float dx = r0.x - fpx, dy = r0.y - fpy;
-            const float power = -0.5f * (r0.z * dx * dx + r1.x * dy * dy) - r0.w * dx * dy;
+            const float u = __fmaf_rn(r2.y, dy, dx);
+            const float Au = r0.z * u;
+            const float power = -0.5f * (Au * u + r1.x * dy * dy);  // <= 0 by construction
             const float G = __expf(power);
             const float oG = r1.y * G;
             const float alpha = fminf(kAlphaMax, oG);
-            const bool contrib = pos < last && power <= 0.f && alpha >= kAlphaMin;
+            const bool contrib = pos < last && alpha >= kAlphaMin;
             const unsigned ballot = __ballot_sync(0xffffffffu, contrib);
             if (ballot == 0u) continue;
             float v[9];
 #pragma unroll
             for (int c = 0; c < 9; ++c) v[c] = 0.f;
             if (contrib) {
-                const float cb = s.rec[slot][j][2].x;
+                const float cb = r2.x;
                 const float inv = 1.f / (1.f - alpha);
                 T *= inv;                               // transmittance in front of this Gaussian
                 const float aT = alpha * T;
@@ -383,8 +412,9 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
                 if (oG <= kAlphaMax) {
                     const float dpow = oG * dalpha;
                     v[5] = G * dalpha;
-                    v[0] = -(r0.z * dx + r0.w * dy) * dpow;
-                    v[1] = -(r0.w * dx + r1.x * dy) * dpow;
+                    // d power / d mean = -(A dx + B dy, B dx + C dy) = -(A u, B u + D dy)
+                    v[0] = -Au * dpow;
+                    v[1] = -(r0.w * u + r1.x * dy) * dpow;
                     v[2] = -0.5f * dx * dx * dpow;
                     v[3] = -dx * dy * dpow;
                     v[4] = -0.5f * dy * dy * dpow;

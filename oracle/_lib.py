@@ -56,11 +56,12 @@ def lib():
         if _lib is None:
             _lib = C.CDLL(build())
             P = C.c_void_p
-            _lib.or_preprocess.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 9
+            _lib.or_preprocess.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 10
             _lib.or_preprocess.restype = C.c_int
             _lib.or_bin.argtypes = [C.c_int64, P, P, P, C.c_int32, C.c_int32, P, P, C.c_int64, P]
             _lib.or_bin.restype = C.c_int64
-            _lib.or_render.argtypes = [C.c_int64] + [P] * 6 + [P] + [P] * 8 + [P, C.c_int]
+            _lib.or_render.argtypes = ([C.c_int64] + [P] * 6 + [P] + [P] * 8 + [P, C.c_int] +
+                                        [P, C.c_double, C.c_double])
             _lib.or_render.restype = C.c_int
             _lib.or_preprocess_bwd.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 6
             _lib.or_preprocess_bwd.restype = C.c_int
@@ -112,12 +113,13 @@ def preprocess(mean3d, log_scale, quat, opacity_logit, sh, sh_degree, cam, threa
                         _c(opacity_logit, np.float64), _c(sh, np.float64))
     out = dict(mean2d=np.zeros((n, 2)), conic=np.zeros((n, 3)), opacity=np.zeros(n), rgb=np.zeros((n, 3)),
                depth=np.zeros(n, np.float32), radius=np.zeros(n, np.int32),
-               tiles_touched=np.zeros(n, np.uint32), flags=np.zeros(n, np.uint8), cov2d=np.zeros((n, 3)))
+               tiles_touched=np.zeros(n, np.uint32), flags=np.zeros(n, np.uint8), cov2d=np.zeros((n, 3)),
+               mean_tol=np.zeros(n))
     c, o = camera(cam), options(sh_degree, threads=threads, **opt)
     rc = lib().or_preprocess(n, _p(m), _p(ls), _p(q), _p(lg), _p(sh), C.byref(c), C.byref(o),
                              _p(out["mean2d"]), _p(out["conic"]), _p(out["opacity"]), _p(out["rgb"]),
                              _p(out["depth"]), _p(out["radius"]), _p(out["tiles_touched"]),
-                             _p(out["flags"]), _p(out["cov2d"]))
+                             _p(out["flags"]), _p(out["cov2d"]), _p(out["mean_tol"]))
     assert rc == 0
     return out
 
@@ -138,7 +140,9 @@ def bin_and_sort(mean2d_f32, depth_f32, radius, width, height, capacity=None):
         cap = int(D)
 
 
-def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threads=0, bg=None):
+def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threads=0, bg=None, record_tol=None):
+    """record_tol = (mean_tol [N] px, conic_rel, opacity_rel) widens the marginal-decision bands by
+    how much another implementation's records may differ from these (None: same records)."""
     n = int(np.asarray(opacity).shape[0])
     W, H = int(cam.width), int(cam.height)
     m, cn, op, cl = (_c(mean2d, np.float64), _c(conic, np.float64), _c(opacity, np.float64),
@@ -151,9 +155,12 @@ def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threa
     grad = np.zeros((n, 9)) if dl is not None else None
     st = OrRenderStats()
     c = camera(cam, bg)
+    mt, crel, orel = (None, 0.0, 0.0) if record_tol is None else record_tol
+    mt = None if mt is None else _c(mt, np.float64)
     rc = lib().or_render(n, _p(m), _p(cn), _p(op), _p(cl), _p(v), _p(rg), C.byref(c), _p(dl),
                          _p(out["image"]), _p(out["t_final"]), _p(out["n_contrib"]), _p(out["n_blended"]),
-                         _p(out["pix_flags"]), _p(out["pix_sig"]), _p(grad), C.byref(st), int(threads))
+                         _p(out["pix_flags"]), _p(out["pix_sig"]), _p(grad), C.byref(st), int(threads),
+                         _p(mt), float(crel), float(orel))
     assert rc == 0
     out["grad2d"] = grad
     out["stats"] = dict(pairs_evaluated=st.pairs_evaluated, pairs_blended=st.pairs_blended,
@@ -178,13 +185,40 @@ def preprocess_bwd(mean3d, log_scale, quat, opacity_logit, sh, sh_degree, cam, g
     return out
 
 
-def view_step(scene, view=0, dl_dimage=None, with_backward=True, threads=0, **opt):
+def marginal_mask(pre, fwd, cam):
+    """Pixels whose float32 result may legitimately differ from this float64 oracle: pixels with a
+    marginal decision, and the pixels of every tile a Gaussian with a marginal radius or tile
+    rectangle may gain or lose: the tiles of its rectangle at radius r + 1 that are not in its
+    rectangle at radius r - 1 (one pixel of radius covers more than the mean's float32 error).
+    Returns a bool [H, W] array (True = marginal)."""
+    mask = fwd["pix_flags"] != 0
+    flagged = np.nonzero((pre["flags"] & 6) != 0)[0]
+    T = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
+    ring = np.zeros(T, bool)
+    m32 = pre["mean2d"].astype(np.float32)
+    for g in flagged:
+        r = int(pre["radius"][g]) if pre["radius"][g] > 0 else int(np.ceil(3.0 * np.sqrt(
+            0.5 * (pre["cov2d"][g, 0] + pre["cov2d"][g, 2]) +
+            np.sqrt(0.25 * (pre["cov2d"][g, 0] - pre["cov2d"][g, 2]) ** 2 + pre["cov2d"][g, 1] ** 2))))
+        tiles = []
+        for rr in (r + 1, max(r - 1, 0)):
+            _, _, rg = bin_and_sort(m32[g:g + 1], pre["depth"][g:g + 1], np.array([rr], np.int32),
+                                    cam.width, cam.height)
+            tiles.append(rg[:, 1] > rg[:, 0])
+        ring |= tiles[0] & ~tiles[1]
+    if ring.any():
+        hit = ring.reshape((cam.height + 15) // 16, (cam.width + 15) // 16)
+        mask |= np.kron(hit, np.ones((16, 16), bool))[: cam.height, : cam.width]
+    return mask
+
+
+def view_step(scene, view=0, dl_dimage=None, with_backward=True, threads=0, mask_marginal=False, **opt):
     """Whole training step of one view: preprocess, binning and sort, render, and (when
     `with_backward`) the gradient computation and the preprocess backward.
 
     The upstream gradient defaults to dL/dimage = image - target (the squared-error loss
     0.5 |image - target|^2), with the target image of the view; the oracle's own float64 image
-    is used, rounded to float32.
+    is used, rounded to float32. With `mask_marginal` it is zeroed on `marginal_mask` pixels.
     """
     cam = scene.cameras[view]
     pre = preprocess(scene.mean3d, scene.log_scale, scene.quat, scene.opacity_logit, scene.sh,
@@ -192,12 +226,20 @@ def view_step(scene, view=0, dl_dimage=None, with_backward=True, threads=0, **op
     m32 = pre["mean2d"].astype(np.float32)
     keys, vals, ranges = bin_and_sort(m32, pre["depth"], pre["radius"], cam.width, cam.height,
                                       capacity=int(pre["tiles_touched"].sum(dtype=np.int64)))
-    fwd = render(pre["mean2d"], pre["conic"], pre["opacity"], pre["rgb"], vals, ranges, cam, threads=threads)
+    # In mask_marginal mode the decision bands also cover a float32 preprocess of the same scene
+    # (means within mean_tol, conics within 1e-5, opacities within 1e-6 relative).
+    rt = (pre["mean_tol"], 1e-5, 1e-6) if mask_marginal else None
+    fwd = render(pre["mean2d"], pre["conic"], pre["opacity"], pre["rgb"], vals, ranges, cam, threads=threads,
+                 record_tol=rt)
     out = dict(pre=pre, keys=keys, vals=vals, ranges=ranges, fwd=fwd)
     if not with_backward:
         return out
     if dl_dimage is None:
         dl_dimage = (fwd["image"] - scene.targets[view]).astype(np.float32)
+    if mask_marginal:
+        # pixels where a float32 implementation may decide differently get no upstream gradient
+        out["marginal"] = marginal_mask(pre, fwd, cam)
+        dl_dimage = np.where(out["marginal"][None], 0.0, dl_dimage).astype(np.float32)
     bwd = render(pre["mean2d"], pre["conic"], pre["opacity"], pre["rgb"], vals, ranges, cam,
                  dl_dimage=dl_dimage, threads=threads)
     g3 = preprocess_bwd(scene.mean3d, scene.log_scale, scene.quat, scene.opacity_logit, scene.sh,

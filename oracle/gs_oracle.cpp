@@ -349,7 +349,7 @@ void or_quat_to_rotmat(const double* q, double* R) {
 int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, const double* quat,
                   const double* logit, const double* sh, const OrCamera* cam, const OrOptions* opt,
                   double* mean2d, double* conic, double* opacity, double* rgb, float* depth,
-                  int32_t* radius, uint32_t* tiles_touched, uint8_t* flags, double* cov2d) {
+                  int32_t* radius, uint32_t* tiles_touched, uint8_t* flags, double* cov2d, double* mean_tol) {
     if (n < 0 || !cam || !opt) return -1;
     const int deg = opt->sh_degree, K = (deg + 1) * (deg + 1);
     const int tiles_x = (cam->width + kTile - 1) / kTile, tiles_y = (cam->height + kTile - 1) / kTile;
@@ -385,6 +385,21 @@ int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, cons
             if (cov2d) cov2d[3 * g + i] = P.culled ? 0.0 : P.cov2d[i];
         }
         opacity[g] = P.culled ? 0.0 : P.opacity;
+        if (mean_tol) {
+            // Bound on how far a float32 evaluation of the projected mean may lie from this one:
+            // 2^-20 (16 units in the last place) of the magnitudes it is computed from.
+            double mag = std::fabs(P.mean2d[0]) + std::fabs(P.mean2d[1]);
+            if (!P.culled) {
+                const double z = P.depth32;
+                double sx = std::fabs((double)cam->t[0]), sy = std::fabs((double)cam->t[1]);
+                for (int i = 0; i < 3; ++i) {
+                    sx += std::fabs((double)cam->R[i] * mu[i]);
+                    sy += std::fabs((double)cam->R[3 + i] * mu[i]);
+                }
+                mag += (cam->fx * sx + cam->fy * sy) / z;
+            }
+            mean_tol[g] = std::ldexp(mag, -20);
+        }
     }
     return 0;
 }
@@ -434,7 +449,7 @@ int64_t or_bin(int64_t n, const float* mean2d, const float* depth, const int32_t
 //
 // Forward, per pixel (centre at (px + 0.5, py + 0.5)), front to back over its tile's list:
 //   d = mean2d - centre, power = -(A dx^2 + C dy^2) / 2 - B dx dy;
-//   skip when power > 0; alpha = min(0.99, opacity exp(power)); skip when alpha < float32(1/255);
+//   skip records whose conic [[A, B], [B, C]] is not positive definite; skip when power > 0; alpha = min(0.99, opacity exp(power)); skip when alpha < float32(1/255);
 //   stop before a Gaussian whose T (1 - alpha) < float32(1e-4) (that Gaussian is not blended);
 //   colour += rgb alpha T; T *= 1 - alpha.
 //   image = colour + T bg; t_final = T; n_contrib = 1 + position (in the tile's list) of the last
@@ -449,7 +464,8 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
               const double* rgb, const uint32_t* vals, const uint32_t* ranges, const OrCamera* cam,
               const float* dl_dimage, double* image, double* t_final, uint32_t* n_contrib,
               uint32_t* n_blended, uint8_t* pix_flags, uint64_t* pix_sig, double* grad2d,
-              OrRenderStats* stats, int threads) {
+              OrRenderStats* stats, int threads, const double* mean_tol, double conic_rel,
+              double opacity_rel) {
     (void)n;
     const int W = cam->width, H = cam->height;
     const int tiles_x = (W + kTile - 1) / kTile, tiles_y = (H + kTile - 1) / kTile;
@@ -490,6 +506,8 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                         ls.pairs_evaluated++;
                         const double dx = mean2d[2 * g] - cxp, dy = mean2d[2 * g + 1] - cyp;
                         const double A = conic[3 * g], B = conic[3 * g + 1], C = conic[3 * g + 2];
+                        // a record whose conic is not positive definite is not a Gaussian: never blended
+                        if (!(A > 0.0) || !(A * C - B * B > 0.0)) continue;
                         const double power = -0.5 * (A * dx * dx + C * dy * dy) - B * dx * dy;
                         // float32 error bound of power: about 8 units in the last place of the sum of
                         // its term magnitudes
@@ -497,11 +515,17 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                                                   std::fabs(B * dx * dy)) + 1e-7;
                         if (std::fabs(power) <= ep) pf |= 4;
                         if (power > 0.0) continue;
+                        // uncertainty of power when the records themselves may differ from these
+                        // (a float32 preprocess): mean by mean_tol px, conic by conic_rel, opacity by opacity_rel
+                        double ein = opacity_rel;
+                        if (mean_tol)
+                            ein += mean_tol[g] * (std::fabs(A * dx + B * dy) + std::fabs(B * dx + C * dy));
+                        ein += conic_rel * (0.5 * (std::fabs(A) * dx * dx + std::fabs(C) * dy * dy) + std::fabs(B * dx * dy));
                         const double G = std::exp(power);
                         const double oG = opacity[g] * G;
                         const bool clamped = oG > 0.99;
                         const double alpha = clamped ? 0.99 : oG;
-                        const double ea = ep + 1e-6;  // relative float32 error bound of alpha (exp included)
+                        const double ea = ep + 1e-6 + ein;  // relative bound on alpha (exp and inputs included)
                         if (!clamped && std::fabs(std::log(alpha / alpha_min)) < ea) pf |= 1;
                         if (alpha < alpha_min) continue;
                         const double test_T = Tr * (1.0 - alpha);

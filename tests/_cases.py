@@ -51,10 +51,16 @@ def stage_inputs(name: str):
     dl = (fwd["image"] - s.targets[view]).astype(np.float32)
     bwd = oracle.render(f64(rec["mean2d"]), f64(rec["conic"]), f64(rec["opacity"]), f64(rec["rgb"]), vals, ranges,
                         cam, dl_dimage=dl)
+    # the same upstream gradient with the marginal pixels zeroed: their float32 decisions may
+    # legitimately differ from float64 ones, which moves every gradient they feed
+    dl_m = np.where(fwd["pix_flags"][None] != 0, 0.0, dl).astype(np.float32)
+    bwd_m = oracle.render(f64(rec["mean2d"]), f64(rec["conic"]), f64(rec["opacity"]), f64(rec["rgb"]), vals, ranges,
+                          cam, dl_dimage=dl_m)
     grad2d32 = bwd["grad2d"].astype(np.float32)
     g3 = oracle.preprocess_bwd(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, s.sh_degree, cam, grad2d32)
     return dict(scene=s, cam=cam, view=view, pre=pre, rec=rec, keys=keys, vals=vals, ranges=ranges, fwd=fwd,
-                dl=dl, grad2d=bwd["grad2d"], grad2d32=grad2d32, grads=g3, stats=bwd["stats"])
+                dl=dl, grad2d=bwd["grad2d"], dl_masked=dl_m, grad2d_masked=bwd_m["grad2d"], grad2d32=grad2d32,
+                grads=g3, stats=bwd["stats"])
 
 
 def grad_close(got: np.ndarray, want: np.ndarray, rel: float = 1e-4, mask=None) -> tuple[bool, float, float]:

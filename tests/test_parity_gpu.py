@@ -195,12 +195,19 @@ def test_render_bwd_matches_oracle(name, mode, staging):
     d = stage_inputs(name)
     proj, b, _, img, tf, nc = _fwd(d, staging)
     opt = api.make_options(d["scene"].sh_degree, bwd_mode=mode, staging=staging)
-    g2 = api.gs_render_bwd(proj, b.vals, b.ranges, d["cam"], opt, torch.from_numpy(d["dl"]).to(DEV), tf, nc)
+    # upstream gradient zero on the oracle's marginal pixels: the 1e-4 bar
+    g2 = api.gs_render_bwd(proj, b.vals, b.ranges, d["cam"], opt, torch.from_numpy(d["dl_masked"]).to(DEV), tf, nc)
     got = g2.cpu().numpy()
     assert np.all(got[:, 9:] == 0.0)
     for group, cols in GRAD2D_GROUPS.items():
-        ok, err, tol = grad_close(got[:, cols], d["grad2d"][:, cols])
+        ok, err, tol = grad_close(got[:, cols], d["grad2d_masked"][:, cols])
         assert ok, f"{group}: error {err:.3g} > {tol:.3g}"
+    # full upstream gradient: marginal pixels may move sums a little more
+    got = api.gs_render_bwd(proj, b.vals, b.ranges, d["cam"], opt, torch.from_numpy(d["dl"]).to(DEV), tf,
+                            nc).cpu().numpy()
+    for group, cols in GRAD2D_GROUPS.items():
+        ok, err, tol = grad_close(got[:, cols], d["grad2d"][:, cols], rel=1e-2)
+        assert ok, f"unmasked {group}: error {err:.3g} > {tol:.3g}"
 
 
 @pytest.mark.parametrize("thr", [1, 16, 33])
@@ -209,10 +216,10 @@ def test_adaptive_threshold_extremes(thr):
     proj, b, _, img, tf, nc = _fwd(d, _abi.GS_STAGE_BULK)
     for mode in ("adaptive", "sm"):
         opt = api.make_options(0, bwd_mode=mode, adaptive_threshold=thr)
-        got = api.gs_render_bwd(proj, b.vals, b.ranges, d["cam"], opt, torch.from_numpy(d["dl"]).to(DEV), tf,
+        got = api.gs_render_bwd(proj, b.vals, b.ranges, d["cam"], opt, torch.from_numpy(d["dl_masked"]).to(DEV), tf,
                                 nc).cpu().numpy()
         for group, cols in GRAD2D_GROUPS.items():
-            ok, err, tol = grad_close(got[:, cols], d["grad2d"][:, cols])
+            ok, err, tol = grad_close(got[:, cols], d["grad2d_masked"][:, cols])
             assert ok, f"{mode}/{thr}/{group}: {err:.3g} > {tol:.3g}"
 
 
@@ -258,16 +265,19 @@ def test_preprocess_bwd_accumulates_views():
 
 # --------------------------------------------------------------------------------- end to end
 
-def _filter_lists(vals, ranges, drop):
-    """Per-tile lists with the entries of Gaussians in `drop` removed."""
-    return [tuple(g for g in vals[a:b] if not drop[g]) for a, b in ranges]
+def _tile_entries(vals, ranges):
+    """(tile id, Gaussian index) of every entry of a sorted list, in list order."""
+    lens = (ranges[:, 1].astype(np.int64) - ranges[:, 0].astype(np.int64))
+    tiles = np.repeat(np.arange(len(ranges)), lens)
+    order = np.concatenate([np.arange(a, b_) for a, b_ in ranges if b_ > a]) if lens.sum() else np.zeros(0, int)
+    return tiles, vals[order]
 
 
 def _end_to_end(s, view, mode="sm"):
     cam = s.cameras[view]
     params = dev_params(s)
     opt = api.make_options(s.sh_degree, bwd_mode=mode)
-    ref = oracle.view_step(s, view=view)
+    ref = oracle.view_step(s, view=view, mask_marginal=True)
     bufs = step.StepBuffers(s.n, DEV)
     proj = api.gs_preprocess(params, cam, opt, out=bufs.proj)
     b = api.gs_bin_and_sort(proj, cam, opt, buffers=bufs.sort)
@@ -277,17 +287,11 @@ def _end_to_end(s, view, mode="sm"):
     pre = ref["pre"]
     flagged = (pre["flags"] & 6) != 0
     # sorted lists: identical after removing the entries of Gaussians with a marginal radius or rectangle
-    gl = _filter_lists(u32(b.vals), u32(b.ranges), flagged)
-    ol = _filter_lists(ref["vals"], ref["ranges"], flagged)
-    assert gl == ol
-    # tiles whose full lists differ (a marginal Gaussian decided differently) are left out of the pixel check
-    gfull = _filter_lists(u32(b.vals), u32(b.ranges), np.zeros(s.n, bool))
-    ofull = _filter_lists(ref["vals"], ref["ranges"], np.zeros(s.n, bool))
-    bad_tiles = np.array([a != c for a, c in zip(gfull, ofull)])
-    TX = (cam.width + 15) // 16
-    ys, xs = np.mgrid[0:cam.height, 0:cam.width]
-    pix_bad = bad_tiles[(ys // 16) * TX + xs // 16]
-    ok = (ref["fwd"]["pix_flags"] == 0) & ~pix_bad
+    gt, gv = _tile_entries(u32(b.vals), u32(b.ranges))
+    ot, ov = _tile_entries(ref["vals"], ref["ranges"])
+    kg, ko = ~flagged[gv], ~flagged[ov]
+    assert np.array_equal(gt[kg], ot[ko]) and np.array_equal(gv[kg], ov[ko])
+    ok = ~ref["marginal"]
     err = np.abs(img.cpu().numpy() - ref["fwd"]["image"])
     assert err[:, ok].max() <= 1e-5, err[:, ok].max()
     assert np.array_equal(u32(nc)[ok], ref["fwd"]["n_contrib"][ok])
