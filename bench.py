@@ -254,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
         c = api.make_camera(cam)
         proj = api.gs_preprocess(params, c, opt, out=bufs.proj)
         image, t_final, n_contrib, dl, ranges = bufs.image_buffers(c.width, c.height)
-        b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges)
+        b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges, want_keys=False)
         api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib))
         torch.sub(image, target, out=dl)
         if ev_bwd is not None:

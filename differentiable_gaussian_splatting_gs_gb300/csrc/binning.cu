@@ -90,33 +90,26 @@ __global__ void __launch_bounds__(1024) k_radix_scan(unsigned* __restrict__ hist
 
 // Stable scatter of one 8-bit digit. IOTA: the values are the item indices. KEY64: also write
 // the 64-bit key (key << 32 | depth_bits[value]) of every item.
+//
+// Each warp ranks its 512 items (16 rounds of 32, in index order) with match_any; the block then
+// reorders its 4096 items by digit in shared memory and writes every digit's run to consecutive
+// global addresses, so the global writes are coalesced.
 template <bool IOTA, bool KEY64>
 __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
     const unsigned* __restrict__ keys_in, const unsigned* __restrict__ vals_in, unsigned* __restrict__ keys_out,
     unsigned* __restrict__ vals_out, int n, int shift, unsigned mask, const unsigned* __restrict__ hist,
     const unsigned* __restrict__ totals, int nblocks, unsigned long long* __restrict__ keys64,
     const unsigned* __restrict__ depth_bits) {
-    __shared__ unsigned woff[8][256];
-    __shared__ unsigned dbase[256];
+    __shared__ unsigned woff[8][256];      // per-warp digit counts, then block-local offsets
+    __shared__ unsigned lbase[256];        // block-local start of each digit
+    __shared__ unsigned gbase[256];        // global start of this block's run of each digit
     __shared__ unsigned wsum[8];
+    __shared__ unsigned sk[kSortItems], sv[kSortItems];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // exclusive scan of the digit totals
-    {
-        const unsigned v = totals[threadIdx.x];
-        unsigned x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        unsigned pre = 0;
-        for (int w = 0; w < warp; ++w) pre += wsum[w];
-        dbase[threadIdx.x] = pre + x - v;
-    }
+    const int block_first = blockIdx.x * kSortItems;
+    const int n_block = min(kSortItems, n - block_first);
     unsigned k[kSortRounds], v[kSortRounds];
-    const int base = blockIdx.x * kSortItems + warp * kWarpItems + lane;
+    const int base = block_first + warp * kWarpItems + lane;
 #pragma unroll
     for (int r = 0; r < kSortRounds; ++r) {
         const int idx = base + r * 32;
@@ -137,14 +130,43 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
     }
     __syncthreads();
     {
+        // digit d = thread: block count, exclusive scans over warps and over digits
         const int d = threadIdx.x;
-        unsigned run = dbase[d] + hist[(size_t)d * nblocks + blockIdx.x];
+        unsigned c = 0;
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
             const unsigned t = woff[w][d];
-            woff[w][d] = run;
-            run += t;
+            woff[w][d] = c;
+            c += t;
         }
+        unsigned x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        // global digit start: exclusive scan of the digit totals
+        const unsigned tv = totals[d];
+        unsigned tx = tv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, tx, o);
+            if (lane >= o) tx += y;
+        }
+        __syncthreads();
+        unsigned pre = 0;
+        for (int w = 0; w < warp; ++w) pre += wsum[w];
+        const unsigned lb = pre + x - c;
+        lbase[d] = lb;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) woff[w][d] += lb;
+        __syncthreads();
+        if (lane == 31) wsum[warp] = tx;
+        __syncthreads();
+        unsigned tpre = 0;
+        for (int w = 0; w < warp; ++w) tpre += wsum[w];
+        gbase[d] = tpre + tx - tv + hist[(size_t)d * nblocks + blockIdx.x];
     }
     __syncthreads();
 #pragma unroll
@@ -153,14 +175,22 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
         const unsigned d = valid ? (k[r] >> shift) & mask : 0x100u;
         const unsigned peers = __match_any_sync(0xffffffffu, d);
         if (valid) {
-            const unsigned pos = woff[warp][d] + __popc(peers & lanemask_lt());
-            keys_out[pos] = k[r];
-            vals_out[pos] = v[r];
-            if (KEY64) keys64[pos] = ((unsigned long long)k[r] << 32) | depth_bits[v[r]];
+            const unsigned lp = woff[warp][d] + __popc(peers & lanemask_lt());
+            sk[lp] = k[r];
+            sv[lp] = v[r];
         }
         __syncwarp();
         if (valid && (peers & lanemask_lt()) == 0u) woff[warp][d] += __popc(peers);
         __syncwarp();
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_block; i += kSortThreads) {
+        const unsigned key = sk[i], val = sv[i];
+        const unsigned d = (key >> shift) & mask;
+        const unsigned pos = gbase[d] + (unsigned)i - lbase[d];
+        keys_out[pos] = key;
+        vals_out[pos] = val;
+        if (KEY64) keys64[pos] = ((unsigned long long)key << 32) | depth_bits[val];
     }
 }
 
@@ -301,13 +331,22 @@ __global__ void k_make_keys(unsigned d, const unsigned* __restrict__ tiles, cons
     if (i < d) keys64[i] = ((unsigned long long)tiles[i] << 32) | depth_bits[vals[i]];
 }
 
-// [start, end) of every tile from the sorted tile ids (ranges zeroed beforehand).
+// [start, end) of every tile from the sorted tile ids (ranges zeroed beforehand); each thread
+// looks at 4 consecutive entries.
 __global__ void k_ranges(unsigned d, const unsigned* __restrict__ tiles, uint2* __restrict__ ranges) {
-    const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= d) return;
-    const unsigned t = tiles[i];
-    if (i == 0 || tiles[i - 1] != t) ranges[t].x = i;
-    if (i == d - 1 || tiles[i + 1] != t) ranges[t].y = i + 1;
+    const unsigned i0 = 4u * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i0 >= d) return;
+    unsigned prev = i0 > 0 ? tiles[i0 - 1] : 0xffffffffu;
+    const unsigned iend = min(i0 + 4u, d);
+    for (unsigned i = i0; i < iend; ++i) {
+        const unsigned t = tiles[i];
+        if (t != prev) {
+            ranges[t].x = i;
+            if (i > 0) ranges[prev].y = i;
+        }
+        prev = t;
+    }
+    if (iend == d) ranges[prev].y = d;
 }
 
 // ---- host orchestration ----------------------------------------------------------------------
@@ -415,7 +454,7 @@ cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigne
         k_make_keys<<<(d + 255) / 256, 256, 0, st>>>(d, tbuf[cur], vals, depth_bits, k64);
     }
     count_launches(1);
-    k_ranges<<<(d + 255) / 256, 256, 0, st>>>(d, tbuf[cur], reinterpret_cast<uint2*>(ranges));
+    k_ranges<<<(d + 1023) / 1024, 256, 0, st>>>(d, tbuf[cur], reinterpret_cast<uint2*>(ranges));
     return cudaGetLastError();
 }
 

@@ -62,7 +62,7 @@ struct Opts {
 int resolve_options(const gs_options* o, Opts& r) {
     gs_options z{};
     if (!o) o = &z;
-    r.bwd_mode = o->bwd_mode == GS_BWD_DEFAULT ? GS_BWD_SM : o->bwd_mode;
+    r.bwd_mode = o->bwd_mode == GS_BWD_DEFAULT ? GS_BWD_ADAPTIVE : o->bwd_mode;
     if (r.bwd_mode < GS_BWD_DIRECT || r.bwd_mode > GS_BWD_SM) return fail(GS_ERR_ARG, "bad bwd_mode %d", o->bwd_mode);
     r.thr = o->adaptive_threshold == 0 ? 8 : o->adaptive_threshold;
     if (r.thr < 1 || r.thr > 33) return fail(GS_ERR_ARG, "adaptive_threshold %d outside 1..33", o->adaptive_threshold);

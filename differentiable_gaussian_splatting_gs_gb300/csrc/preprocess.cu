@@ -168,35 +168,59 @@ __global__ void __launch_bounds__(256) k_preprocess(int n, const float* __restri
     tiles_touched[i] = tt;
 }
 
+constexpr int kBwdThreads = 128;
+
+// Copies the SH coefficients of the warp's 32 Gaussians (contiguous K3 floats each) between global
+// memory and a padded shared-memory tile (row stride K3 + 1: conflict-free per-thread rows) with
+// coalesced accesses. LOAD: global -> shared; else shared -> global (ADD: added to global).
+template <int K3, bool LOAD, bool ADD>
+__device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, int n, int lane) {
+    const int cnt = min(32, n - first);
+    if (cnt <= 0) return;
+    const int total = cnt * K3;
+    float* gw = g + (size_t)first * K3;
+    for (int e = lane; e < total; e += 32) {
+        const int row = e / K3, col = e - row * K3;
+        if (LOAD) tile[row * (K3 + 1) + col] = gw[e];
+        else if (ADD) gw[e] += tile[row * (K3 + 1) + col];
+        else gw[e] = tile[row * (K3 + 1) + col];
+    }
+}
+
 template <int DEG>
-__global__ void __launch_bounds__(256) k_preprocess_bwd(
+__global__ void __launch_bounds__(kBwdThreads) k_preprocess_bwd(
     int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
     const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
     const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
     float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
     float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate) {
     constexpr int K = (DEG + 1) * (DEG + 1);
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
+    constexpr int K3 = 3 * K;
+    __shared__ float tile_all[kBwdThreads / 32][32 * (K3 + 1)];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* tile = tile_all[warp];
+    const int warp_first = blockIdx.x * kBwdThreads + warp * 32;
+    const int i = warp_first + lane;
+    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane);
+    __syncwarp();
+    float* my = tile + lane * (K3 + 1);   // this thread's coefficients, then its SH gradients
     float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
-    float* dshg = d_sh + (size_t)i * K * 3;
-    const float m[3] = {mean3d[3 * i], mean3d[3 * i + 1], mean3d[3 * i + 2]};
+    bool live = false;
     Geo g;
-    bool live = radius[i] > 0;
-    if (live) {
-        const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
-        const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
-        live = geometry(m, ls, q, cam, g);
-    }
-    if (!live) {
-        if (!accumulate) {
-            for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] = 0.f; d_log_scale[3 * i + k] = 0.f; }
-            for (int k = 0; k < 4; ++k) d_quat[4 * i + k] = 0.f;
-            d_logit[i] = 0.f;
-            for (int k = 0; k < 3 * K; ++k) dshg[k] = 0.f;
+    float m[3] = {0.f, 0.f, 0.f};
+    if (i < n) {
+        m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
+        live = radius[i] > 0;
+        if (live) {
+            const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
+            const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
+            live = geometry(m, ls, q, cam, g);
         }
-        return;
     }
+    if (i < n && !live) {
+        for (int k = 0; k < K3; ++k) my[k] = 0.f;
+    }
+    if (i < n && live) {
     const float4 g0 = grad2d[3 * i], g1 = grad2d[3 * i + 1], g2 = grad2d[3 * i + 2];
     const float dmx = g0.x, dmy = g0.y, dA = g0.z, dB = g0.w, dC = g1.x, dop = g1.y;
     const float drgb[3] = {g1.z, g1.w, g2.x};
@@ -211,24 +235,22 @@ __global__ void __launch_bounds__(256) k_preprocess_bwd(
     const float ux = vx * vinv, uy = vy * vinv, uz = vz * vinv;
     float Y[16];
     sh_basis<DEG>(ux, uy, uz, Y);
-    const float* shg = sh + (size_t)i * K * 3;
     float col[3] = {0.5f, 0.5f, 0.5f};
+#pragma unroll
     for (int k = 0; k < K; ++k) {
-        col[0] += Y[k] * shg[3 * k];
-        col[1] += Y[k] * shg[3 * k + 1];
-        col[2] += Y[k] * shg[3 * k + 2];
+        col[0] += Y[k] * my[3 * k];
+        col[1] += Y[k] * my[3 * k + 1];
+        col[2] += Y[k] * my[3 * k + 2];
     }
     float dc[3];
     for (int ch = 0; ch < 3; ++ch) dc[ch] = (col[ch] < 0.f) ? 0.f : drgb[ch];
     float wk[16];
+#pragma unroll
     for (int k = 0; k < K; ++k) {
-        const float s0 = Y[k] * dc[0], s1 = Y[k] * dc[1], s2 = Y[k] * dc[2];
-        if (accumulate) {
-            dshg[3 * k] += s0; dshg[3 * k + 1] += s1; dshg[3 * k + 2] += s2;
-        } else {
-            dshg[3 * k] = s0; dshg[3 * k + 1] = s1; dshg[3 * k + 2] = s2;
-        }
-        wk[k] = shg[3 * k] * dc[0] + shg[3 * k + 1] * dc[1] + shg[3 * k + 2] * dc[2];
+        wk[k] = my[3 * k] * dc[0] + my[3 * k + 1] * dc[1] + my[3 * k + 2] * dc[2];
+        my[3 * k] = Y[k] * dc[0];      // the row now holds dL/dsh
+        my[3 * k + 1] = Y[k] * dc[1];
+        my[3 * k + 2] = Y[k] * dc[2];
     }
     if (DEG > 0) {
         float gd[3] = {0.f, 0.f, 0.f};
@@ -315,15 +337,21 @@ __global__ void __launch_bounds__(256) k_preprocess_bwd(
     const float dotq = dqn[0] * w + dqn[1] * x + dqn[2] * y + dqn[3] * z;
     for (int k = 0; k < 4; ++k) dq[k] = (dqn[k] - dotq * g.qn[k]) * g.qinv;
 
-    if (accumulate) {
-        for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] += dm[k]; d_log_scale[3 * i + k] += dls[k]; }
-        for (int k = 0; k < 4; ++k) d_quat[4 * i + k] += dq[k];
-        d_logit[i] += dlg;
-    } else {
-        for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] = dm[k]; d_log_scale[3 * i + k] = dls[k]; }
-        for (int k = 0; k < 4; ++k) d_quat[4 * i + k] = dq[k];
-        d_logit[i] = dlg;
+    }  // live
+    if (i < n) {
+        if (accumulate) {
+            for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] += dm[k]; d_log_scale[3 * i + k] += dls[k]; }
+            for (int k = 0; k < 4; ++k) d_quat[4 * i + k] += dq[k];
+            d_logit[i] += dlg;
+        } else {
+            for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] = dm[k]; d_log_scale[3 * i + k] = dls[k]; }
+            for (int k = 0; k < 4; ++k) d_quat[4 * i + k] = dq[k];
+            d_logit[i] = dlg;
+        }
     }
+    __syncwarp();
+    if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane);
+    else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane);
 }
 
 // ---- host-side launchers ------------------------------------------------------------------------

@@ -27,6 +27,7 @@ namespace gs {
 constexpr float kAlphaMin = 1.0f / 255.0f;
 constexpr float kTMin = 1e-4f;
 constexpr float kAlphaMax = 0.99f;
+constexpr float kNegHalfLog2e = -0.72134752044448170f;  // -log2(e) / 2
 // Bound of the waits that let in-flight bulk copies land before a block exits early; independent
 // of the caller's spin limit so that a small limit cannot leave copies running into a dead block.
 constexpr unsigned kDrainLimit = 1u << 22;
@@ -52,7 +53,9 @@ struct BwdSmem {
 // are non-negative, so the evaluation has no cancellation even for very elongated Gaussians
 // (where the three terms of the plain form are large and nearly cancel). det is computed with
 // one rounding error. The record's C slot is replaced by D and slot 9 receives r; A and B stay.
-// A record whose conic is not positive definite is never blended (empty box).
+// A record whose conic is not positive definite is never blended (empty box). Slots 10 and 11
+// receive A and D scaled by -log2(e)/2, so that the kernels take exp(power) as 2^(A' u^2 + D' dy^2)
+// with the hardware base-2 exponential.
 //
 // Box: the set alpha >= 1/255 is -power <= tau = ln(255 opacity), whose axis-aligned half-extents
 // are sqrt(2 tau Sigma'_xx) = sqrt(2 tau C / det) and sqrt(2 tau A / det).
@@ -67,10 +70,15 @@ __device__ __forceinline__ float4 prepare_record(float4& r0, float4& r1, float4&
     if (!(A > 0.f) || !(det > 0.f) || !(det < inf)) {
         r1.x = 0.f;
         r2.y = 0.f;
+        r2.z = 0.f;
+        r2.w = 0.f;
         return empty;
     }
-    r1.x = det / A;   // D
+    const float D = det / A;
+    r1.x = D;
     r2.y = B / A;     // r
+    r2.z = kNegHalfLog2e * A;
+    r2.w = kNegHalfLog2e * D;
     if (!(o * 1.00001f >= kAlphaMin)) return empty;  // alpha = min(0.99, o G) <= o < 1/255: never blended
     const float tau = logf(255.0f * o * 1.00001f) * 1.001f + 0.001f;
     const float hx = sqrtf(2.f * tau * C / det) * 1.001f + 0.01f;
@@ -217,15 +225,15 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
         for (int k = 0; k < nl; ++k) {
             if (__all_sync(0xffffffffu, done)) break;
             const int j = s.list[warp][k];
-            const float4 r0 = s.rec[slot][j][0];
-            const float4 r1 = s.rec[slot][j][1];
             if (!done) {
-                const float2 r2 = *reinterpret_cast<const float2*>(&s.rec[slot][j][2]);  // (b, r)
+                const float2 r0 = *reinterpret_cast<const float2*>(&s.rec[slot][j][0]);  // mean
+                const float4 r1 = s.rec[slot][j][1];                                     // (D, o, r, g)
+                const float4 r2 = s.rec[slot][j][2];                                     // (b, r, A', D')
                 const float dx = r0.x - fpx, dy = r0.y - fpy;
                 const float u = __fmaf_rn(r2.y, dy, dx);
-                const float power = -0.5f * (r0.z * u * u + r1.x * dy * dy);  // <= 0 by construction
+                const float p2 = __fmaf_rn(r2.z * u, u, r2.w * dy * dy);  // power log2(e) <= 0
                 {
-                    const float alpha = fminf(kAlphaMax, r1.y * __expf(power));
+                    const float alpha = fminf(kAlphaMax, r1.y * ex2_approx(p2));
                     if (alpha >= kAlphaMin) {
                         const float test_T = T * (1.f - alpha);
                         if (test_T < kTMin) {
@@ -381,14 +389,13 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
         for (int k = nl - 1; k >= 0; --k) {
             const int j = s.list[warp][k];
             const unsigned pos = (unsigned)(b * kBatch + j);
-            const float4 r0 = s.rec[slot][j][0];
-            const float4 r1 = s.rec[slot][j][1];
-            const float2 r2 = *reinterpret_cast<const float2*>(&s.rec[slot][j][2]);  // (b, r)
+            const float4 r0 = s.rec[slot][j][0];   // (mean_x, mean_y, A, B)
+            const float4 r1 = s.rec[slot][j][1];   // (D, o, r, g)
+            const float4 r2 = s.rec[slot][j][2];   // (b, r, A', D')
             const float dx = r0.x - fpx, dy = r0.y - fpy;
             const float u = __fmaf_rn(r2.y, dy, dx);
             const float Au = r0.z * u;
-            const float power = -0.5f * (Au * u + r1.x * dy * dy);  // <= 0 by construction
-            const float G = __expf(power);
+            const float G = ex2_approx(__fmaf_rn(r2.z * u, u, r2.w * dy * dy));  // exp(power)
             const float oG = r1.y * G;
             const float alpha = fminf(kAlphaMax, oG);
             const bool contrib = pos < last && alpha >= kAlphaMin;
@@ -399,7 +406,7 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
             for (int c = 0; c < 9; ++c) v[c] = 0.f;
             if (contrib) {
                 const float cb = r2.x;
-                const float inv = 1.f / (1.f - alpha);
+                const float inv = rcp_approx(1.f - alpha);
                 T *= inv;                               // transmittance in front of this Gaussian
                 const float aT = alpha * T;
                 v[6] = aT * g0;

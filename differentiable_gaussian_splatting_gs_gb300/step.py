@@ -38,7 +38,7 @@ class StepBuffers:
 
 
 def train_step(params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int | None = None,
-               want_keys: bool = True, stream=None) -> dict:
+               want_keys: bool = False, stream=None) -> dict:
     """Runs every view and leaves the summed parameter gradients in `grads`. Returns per-view
     duplicate counts and the last view's image (a view of a reused buffer)."""
     n_dups = []

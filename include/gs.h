@@ -82,7 +82,7 @@ typedef struct gs_camera {
 
 /* Zero-initialised options select the defaults written beside each field. */
 typedef struct gs_options {
-    int32_t  bwd_mode;            /* GS_BWD_*; 0 = GS_BWD_DEFAULT (the SM mode) */
+    int32_t  bwd_mode;            /* GS_BWD_*; 0 = GS_BWD_DEFAULT (the ADAPTIVE mode) */
     int32_t  adaptive_threshold;  /* lanes, 1..32; 0 = 8 */
     int32_t  sh_degree;           /* 0..3 (K = (degree + 1)^2 SH coefficients per channel) */
     int32_t  staging;             /* GS_STAGE_*; 0 = GS_STAGE_BULK */

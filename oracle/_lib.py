@@ -61,7 +61,7 @@ def lib():
             _lib.or_bin.argtypes = [C.c_int64, P, P, P, C.c_int32, C.c_int32, P, P, C.c_int64, P]
             _lib.or_bin.restype = C.c_int64
             _lib.or_render.argtypes = ([C.c_int64] + [P] * 6 + [P] + [P] * 8 + [P, C.c_int] +
-                                        [P, C.c_double, C.c_double])
+                                        [P, C.c_double, C.c_double, P])
             _lib.or_render.restype = C.c_int
             _lib.or_preprocess_bwd.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 6
             _lib.or_preprocess_bwd.restype = C.c_int
@@ -142,7 +142,9 @@ def bin_and_sort(mean2d_f32, depth_f32, radius, width, height, capacity=None):
 
 def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threads=0, bg=None, record_tol=None):
     """record_tol = (mean_tol [N] px, conic_rel, opacity_rel) widens the marginal-decision bands by
-    how much another implementation's records may differ from these (None: same records)."""
+    how much another implementation's records may differ from these (None: same records):
+    means within mean_tol px, the conic's quadratic form within a relative conic_rel, opacities
+    within a relative opacity_rel."""
     n = int(np.asarray(opacity).shape[0])
     W, H = int(cam.width), int(cam.height)
     m, cn, op, cl = (_c(mean2d, np.float64), _c(conic, np.float64), _c(opacity, np.float64),
@@ -151,7 +153,7 @@ def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threa
     dl = None if dl_dimage is None else _c(dl_dimage, np.float32)
     out = dict(image=np.zeros((3, H, W)), t_final=np.zeros((H, W)), n_contrib=np.zeros((H, W), np.uint32),
                n_blended=np.zeros((H, W), np.uint32), pix_flags=np.zeros((H, W), np.uint8),
-               pix_sig=np.zeros((H, W), np.uint64))
+               pix_sig=np.zeros((H, W), np.uint64), pix_err=np.zeros((H, W)))
     grad = np.zeros((n, 9)) if dl is not None else None
     st = OrRenderStats()
     c = camera(cam, bg)
@@ -160,7 +162,7 @@ def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threa
     rc = lib().or_render(n, _p(m), _p(cn), _p(op), _p(cl), _p(v), _p(rg), C.byref(c), _p(dl),
                          _p(out["image"]), _p(out["t_final"]), _p(out["n_contrib"]), _p(out["n_blended"]),
                          _p(out["pix_flags"]), _p(out["pix_sig"]), _p(grad), C.byref(st), int(threads),
-                         _p(mt), float(crel), float(orel))
+                         _p(mt), float(crel), float(orel), _p(out["pix_err"]))
     assert rc == 0
     out["grad2d"] = grad
     out["stats"] = dict(pairs_evaluated=st.pairs_evaluated, pairs_blended=st.pairs_blended,
@@ -227,7 +229,8 @@ def view_step(scene, view=0, dl_dimage=None, with_backward=True, threads=0, mask
     keys, vals, ranges = bin_and_sort(m32, pre["depth"], pre["radius"], cam.width, cam.height,
                                       capacity=int(pre["tiles_touched"].sum(dtype=np.int64)))
     # In mask_marginal mode the decision bands also cover a float32 preprocess of the same scene
-    # (means within mean_tol, conics within 1e-5, opacities within 1e-6 relative).
+    # (means within mean_tol, the conic's quadratic form within 1e-5 and opacities within 1e-6
+    # relative: several times what a float32 preprocess was measured to differ by).
     rt = (pre["mean_tol"], 1e-5, 1e-6) if mask_marginal else None
     fwd = render(pre["mean2d"], pre["conic"], pre["opacity"], pre["rgb"], vals, ranges, cam, threads=threads,
                  record_tol=rt)

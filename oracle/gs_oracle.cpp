@@ -387,7 +387,7 @@ int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, cons
         opacity[g] = P.culled ? 0.0 : P.opacity;
         if (mean_tol) {
             // Bound on how far a float32 evaluation of the projected mean may lie from this one:
-            // 2^-20 (16 units in the last place) of the magnitudes it is computed from.
+            // 2^-22 (4 units in the last place) of the magnitudes it is computed from.
             double mag = std::fabs(P.mean2d[0]) + std::fabs(P.mean2d[1]);
             if (!P.culled) {
                 const double z = P.depth32;
@@ -398,7 +398,7 @@ int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, cons
                 }
                 mag += (cam->fx * sx + cam->fy * sy) / z;
             }
-            mean_tol[g] = std::ldexp(mag, -20);
+            mean_tol[g] = std::ldexp(mag, -22);
         }
     }
     return 0;
@@ -465,7 +465,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
               const float* dl_dimage, double* image, double* t_final, uint32_t* n_contrib,
               uint32_t* n_blended, uint8_t* pix_flags, uint64_t* pix_sig, double* grad2d,
               OrRenderStats* stats, int threads, const double* mean_tol, double conic_rel,
-              double opacity_rel) {
+              double opacity_rel, double* pix_err) {
     (void)n;
     const int W = cam->width, H = cam->height;
     const int tiles_x = (W + kTile - 1) / kTile, tiles_y = (H + kTile - 1) / kTile;
@@ -497,6 +497,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                     const double cxp = px + 0.5, cyp = py + 0.5;
                     double Tr = 1.0, col[3] = {0.0, 0.0, 0.0};
                     double eT = 0.0;  // bound on the relative float32 error of T
+                    double eC = 0.0;  // bound on the colour error propagated from the alpha bounds
                     uint32_t contrib = 0, nbl = 0;
                     uint8_t pf = 0;
                     uint64_t sig = 1469598103934665603ull;  // FNV-1a over (position, clamped) of blended entries
@@ -509,18 +510,24 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                         // a record whose conic is not positive definite is not a Gaussian: never blended
                         if (!(A > 0.0) || !(A * C - B * B > 0.0)) continue;
                         const double power = -0.5 * (A * dx * dx + C * dy * dy) - B * dx * dy;
-                        // float32 error bound of power: about 8 units in the last place of the sum of
-                        // its term magnitudes
-                        const double ep = 5e-7 * (0.5 * (std::fabs(A) * dx * dx + std::fabs(C) * dy * dy) +
-                                                  std::fabs(B * dx * dy)) + 1e-7;
+                        // Bound on the float32 error of power when it is evaluated as
+                        // -(A u^2 + D dy^2)/2 with u = dx + (B/A) dy, D = (A C - B^2)/A (terms >= 0): u carries
+                        // eps (|u| + |B/A dy|), A u^2 and D dy^2 a few eps each; 4e-7 is about 7 eps.
+                        const double ur = B / A * dy, u = dx + ur, D = (A * C - B * B) / A;
+                        const double ep = 4e-7 * (A * std::fabs(u) * (std::fabs(u) + std::fabs(ur)) + A * u * u +
+                                                  2.0 * D * dy * dy) + 1e-7;
                         if (std::fabs(power) <= ep) pf |= 4;
                         if (power > 0.0) continue;
                         // uncertainty of power when the records themselves may differ from these
-                        // (a float32 preprocess): mean by mean_tol px, conic by conic_rel, opacity by opacity_rel
-                        double ein = opacity_rel;
+                        // (a float32 preprocess): the mean by mean_tol px, the conic's quadratic form by a
+                        // relative conic_rel plus the rounding of its three float32 entries (4e-7 of
+                        // the term magnitudes; for elongated Gaussians this dominates along the long
+                        // axis), the opacity by a relative opacity_rel
+                        double ein = opacity_rel + conic_rel * std::fabs(power);
+                        if (conic_rel > 0.0)
+                            ein += 4e-7 * (0.5 * (std::fabs(A) * dx * dx + std::fabs(C) * dy * dy) + std::fabs(B * dx * dy));
                         if (mean_tol)
                             ein += mean_tol[g] * (std::fabs(A * dx + B * dy) + std::fabs(B * dx + C * dy));
-                        ein += conic_rel * (0.5 * (std::fabs(A) * dx * dx + std::fabs(C) * dy * dy) + std::fabs(B * dx * dy));
                         const double G = std::exp(power);
                         const double oG = opacity[g] * G;
                         const bool clamped = oG > 0.99;
@@ -533,6 +540,14 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                         if (std::fabs(test_T / t_min - 1.0) < 2.0 * eT_next + 1e-6) pf |= 2;
                         if (test_T < t_min) break;
                         for (int ch = 0; ch < 3; ++ch) col[ch] += rgb[3 * g + ch] * alpha * Tr;
+                        {
+                            // |dC/dalpha_i| <= T_i (|c_i| + max colour behind); the colour behind is bounded
+                            // by the largest colour or background value
+                            double cm = 0.0;
+                            for (int ch = 0; ch < 3; ++ch)
+                                cm = std::max(cm, std::max(std::fabs(rgb[3 * g + ch]), std::fabs((double)cam->bg[ch])));
+                            eC += 2.0 * cm * (clamped ? 0.0 : ea) * alpha * Tr;
+                        }
                         bl.push_back({pos, g, alpha, Tr, G, dx, dy, clamped});
                         sig = (sig ^ (uint64_t)(2 * (pos - s) + (clamped ? 1 : 0))) * 1099511628211ull;
                         Tr = test_T;
@@ -549,6 +564,11 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                     if (n_blended) n_blended[pix] = nbl;
                     if (pix_flags) pix_flags[pix] = pf;
                     if (pix_sig) pix_sig[pix] = sig;
+                    if (pix_err) {
+                        double bm = 0.0;
+                        for (int ch = 0; ch < 3; ++ch) bm = std::max(bm, std::fabs((double)cam->bg[ch]));
+                        pix_err[pix] = eC + Tr * eT * bm;
+                    }
                     if (pf) ls.marginal_pixels++;
                     if (!grad2d) continue;
                     double gpix[3];

@@ -293,7 +293,12 @@ def _end_to_end(s, view, mode="sm"):
     assert np.array_equal(gt[kg], ot[ko]) and np.array_equal(gv[kg], ov[ko])
     ok = ~ref["marginal"]
     err = np.abs(img.cpu().numpy() - ref["fwd"]["image"])
-    assert err[:, ok].max() <= 1e-5, err[:, ok].max()
+    # each side computes its own records here, so the 1e-5 bar is widened by the oracle's bound on
+    # the colour change those record differences can cause (alpha bounds propagated per pixel)
+    bound = 1e-5 + ref["fwd"]["pix_err"]
+    assert np.all(err[:, ok] <= bound[None][:, ok]), (err - bound[None])[:, ok].max()
+    assert np.median(ref["fwd"]["pix_err"][ok]) < 5e-4, "the propagated bound is not informative"
+    assert np.mean(err[:, ok] <= 1e-5) > 0.99, "more than 1% of the pixels above 1e-5"
     assert np.array_equal(u32(nc)[ok], ref["fwd"]["n_contrib"][ok])
     for name_p in PARAM_NAMES:
         got = grads[name_p].cpu().numpy().reshape(s.n, -1)
