@@ -376,14 +376,14 @@ cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const Kern
                                   const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
                                   int accumulate, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
-    const int blocks = (n + 255) / 256;
+    const int blocks = (n + kBwdThreads - 1) / kBwdThreads;
     const float4* g2 = reinterpret_cast<const float4*>(grad2d);
     count_launches(1);
     switch (deg) {
-        case 0: k_preprocess_bwd<0><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
-        case 1: k_preprocess_bwd<1><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
-        case 2: k_preprocess_bwd<2><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
-        default: k_preprocess_bwd<3><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 0: k_preprocess_bwd<0><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 1: k_preprocess_bwd<1><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 2: k_preprocess_bwd<2><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        default: k_preprocess_bwd<3><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
     }
     return cudaGetLastError();
 }
