@@ -50,7 +50,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", default="sm", choices=["sm", "direct", "warp", "adaptive"])
+    ap.add_argument("--mode", default="adaptive", choices=["sm", "direct", "warp", "adaptive"])
+    ap.add_argument("--threshold", type=int, default=0, help="adaptive threshold in lanes (0 = library default)")
     ap.add_argument("--staging", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -245,7 +246,8 @@ def run_ours(args, rank, world, local_rank):
     target = host_target.to(dev)
     grads = api.alloc_param_grads(params)
     host_grads = {k: torch.empty_like(host[k]).pin_memory() for k in names}
-    opt = api.make_options(scene.sh_degree, bwd_mode=args.mode, staging=args.staging)
+    opt = api.make_options(scene.sh_degree, bwd_mode=args.mode, staging=args.staging,
+                           adaptive_threshold=args.threshold)
     bufs = step.StepBuffers(scene.n, dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
