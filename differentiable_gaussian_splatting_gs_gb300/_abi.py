@@ -28,7 +28,8 @@ BWD_MODES = {"direct": GS_BWD_DIRECT, "warp": GS_BWD_WARP, "adaptive": GS_BWD_AD
 # every symbol include/gs.h declares
 EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd",
            "gs_preprocess_bwd", "gs_status_string", "gs_last_error_message", "gs_device_error",
-           "gs_selftest_timeout", "gs_kernel_launches", "gs_version")
+           "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static")
+GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
 
 
 class gs_camera(C.Structure):
@@ -90,6 +91,8 @@ def load():
         lib.gs_device_error.argtypes = [P]
         lib.gs_version.argtypes = []
         lib.gs_selftest_timeout.argtypes = [C.c_uint32, P]
+        lib.gs_bin_and_sort_static.argtypes = [pproj, pcam, popt, P, P, I64, C.POINTER(I64), P, P]
+        lib.gs_bin_and_sort_static.restype = C.c_int
         lib.gs_kernel_launches.argtypes = []
         lib.gs_kernel_launches.restype = C.c_int64
         for name in ("gs_preprocess", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd",

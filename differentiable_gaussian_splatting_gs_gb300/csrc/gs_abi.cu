@@ -16,6 +16,9 @@ namespace gs {
 // Device error word of this library, one per device.
 __device__ unsigned int g_error_word = 0u;
 
+// Scratch space of gs_bin_and_sort_static: reserved on every device that loads the library.
+static __device__ __align__(256) unsigned char g_static_sort_ws[GS_STATIC_SORT_WORKSPACE_BYTES];
+
 static std::atomic<long long> g_launches{0};
 void count_launches(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 
@@ -149,6 +152,23 @@ unsigned* error_word(int* status) {
     return cache[dev];
 }
 
+// Device address of g_static_sort_ws for the current device (looked up once per device; in host
+// code the array's name is only a stand-in, so kernels must be given this address).
+unsigned char* static_sort_workspace(int* status) {
+    static unsigned char* cache[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e || dev < 0 || dev >= 256) { *status = cuda_fail(e ? e : cudaErrorInvalidDevice, "cudaGetDevice"); return nullptr; }
+    if (!cache[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_sort_ws);
+        if (e) { *status = cuda_fail(e, "cudaGetSymbolAddress(static sort workspace)"); return nullptr; }
+        cache[dev] = static_cast<unsigned char*>(p);
+    }
+    *status = GS_OK;
+    return cache[dev];
+}
+
 }  // namespace
 }  // namespace gs
 
@@ -245,6 +265,44 @@ int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options*
     e = bin_emit_sort(*proj, kc.tiles_x, kc.tiles_y, (unsigned)d, (unsigned long long)capacity, w, keys, vals,
                       tile_ranges, err, st);
     return e ? cuda_fail(e, "gs_bin_and_sort: emit/sort") : GS_OK;
+}
+
+int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, uint64_t* keys,
+                           uint32_t* vals, int64_t capacity, int64_t* n_dup_out, uint32_t* tile_ranges,
+                           void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_proj_n(proj))) return s;
+    if (!n_dup_out) return fail(GS_ERR_ARG, "n_dup_out is NULL");
+    if (capacity < 0 || capacity > 0x7fffffffll) return fail(GS_ERR_ARG, "capacity outside 0..2^31-1");
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or not 8-byte aligned");
+    if (capacity > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
+    if (keys && !aligned(keys, 8)) return fail(GS_ERR_ARG, "keys not 8-byte aligned");
+    const size_t need = carve_workspace(nullptr, proj->n, capacity).bytes;
+    if (need > (size_t)GS_STATIC_SORT_WORKSPACE_BYTES)
+        return fail(GS_ERR_ARG,
+                    "n = %lld with capacity %lld needs %zu bytes of sort workspace; the static workspace holds %u "
+                    "bytes: use gs_bin_and_sort with a caller-provided workspace",
+                    (long long)proj->n, (long long)capacity, need, (unsigned)GS_STATIC_SORT_WORKSPACE_BYTES);
+    unsigned char* ws = static_sort_workspace(&s);
+    if (!ws) return s;
+    const SortWorkspace w = carve_workspace(ws, proj->n, capacity);
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, st);
+    if (e) return cuda_fail(e, "gs_bin_and_sort_static: count");
+    unsigned long long d = 0;
+    if ((e = cudaMemcpyAsync(&d, w.total, 8, cudaMemcpyDeviceToHost, st)))
+        return cuda_fail(e, "gs_bin_and_sort_static: read D");
+    if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "gs_bin_and_sort_static: synchronize");
+    *n_dup_out = (int64_t)d;
+    if (d > (unsigned long long)capacity)
+        return fail(GS_ERR_CAPACITY, "%llu duplicates exceed capacity %lld", d, (long long)capacity);
+    e = bin_emit_sort(*proj, kc.tiles_x, kc.tiles_y, (unsigned)d, (unsigned long long)capacity, w, keys, vals,
+                      tile_ranges, err, st);
+    return e ? cuda_fail(e, "gs_bin_and_sort_static: emit/sort") : GS_OK;
 }
 
 int gs_render_fwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges, const gs_camera* cam,

@@ -189,6 +189,31 @@ int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options
                       float* d_log_scale, float* d_quat, float* d_opacity_logit, float* d_sh,
                       int32_t accumulate, void* stream);
 
+/* Size of the device workspace that gs_bin_and_sort_static uses instead of a caller buffer. */
+#define GS_STATIC_SORT_WORKSPACE_BYTES (32u << 20)
+
+/* gs_bin_and_sort without a workspace argument, for callers that cannot allocate device memory:
+ * code running where a cudaMalloc is not allowed or not wanted (inside a region being captured
+ * into a CUDA graph, a real-time loop with a fixed memory budget, a plug-in that only receives
+ * buffers from its host). It computes exactly what gs_bin_and_sort computes (same outputs, same
+ * errors) but takes its scratch space from a statically sized device array inside this library,
+ * GS_STATIC_SORT_WORKSPACE_BYTES (32 MiB), which every GPU that loads the library keeps reserved
+ * until the process exits. The pages describe no such entry point; it is a convenience of this
+ * library.
+ *   - Limit: the call needs gs_sort_workspace_bytes(n, capacity, W, H) <= 32 MiB (for example
+ *     n = 500,000 Gaussians with capacity = 1,500,000 duplicates); larger requests return
+ *     GS_ERR_ARG without touching the device. The call itself allocates nothing.
+ *   - Set-up: the first call on a device looks up the device address of the array (once per
+ *     device, with that device current). Make that first call before any stream capture.
+ *   - Sharing: all calls in the process use the same array, which keeps the last call's contents
+ *     (nothing in it needs to start at zero). Calls whose GPU work overlaps (different streams, or
+ *     different host threads on one device) race on it and give wrong results: order them on one
+ *     stream or synchronise between them.
+ * Arguments and errors otherwise as gs_bin_and_sort.                                          */
+int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, uint64_t* keys,
+                           uint32_t* vals, int64_t capacity, int64_t* n_dup_out, uint32_t* tile_ranges,
+                           void* stream);
+
 /* Text of a status code (static storage). */
 const char* gs_status_string(int status);
 
