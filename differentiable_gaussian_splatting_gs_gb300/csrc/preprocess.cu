@@ -188,7 +188,7 @@ __device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, i
 }
 
 template <int DEG>
-__global__ void __launch_bounds__(kBwdThreads) k_preprocess_bwd(
+__global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
     const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
     const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,

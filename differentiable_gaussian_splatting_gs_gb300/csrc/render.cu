@@ -12,10 +12,14 @@
 //
 // Warp-level culling. Before blending a batch, each warp keeps only the staged Gaussians whose
 // alpha can reach 1/255 somewhere in its 8x4 block: the set alpha >= 1/255 is the ellipse
-// -power <= tau = ln(255 opacity), whose axis-aligned half-extents are sqrt(2 tau Sigma'_xx) and
-// sqrt(2 tau Sigma'_yy) with Sigma' the inverse of the conic. The extents are widened (tau by
-// 0.1 %, extents by 0.1 % + 0.01 px) so that no pair the per-pixel test would blend is dropped;
-// dropped pairs are exactly ones the per-pixel test skips, so the results do not change.
+// q(d) = A dx^2 + 2 B dx dy + C dy^2 <= L = 2 tau, tau = ln(255 opacity), and the test is whether
+// the minimum of q over the block's rectangle of pixel centres is <= L. q is convex, so for a fixed
+// dy its minimum over dx in [ax, bx] is at dx = clamp(-(B/A) dy, ax, bx); what remains is a convex
+// function of dy whose minimiser over the real line is dy = -(B/C) clamp(0, ax, bx), and over
+// [ay, by] its clamp. Three clamps give the minimising point, and q there decides. The rectangle
+// is widened by 0.01 px and tau by 0.1 % + 0.001 so that rounding cannot drop a pair the per-pixel
+// test would blend; dropped pairs are exactly ones the per-pixel test skips, so the results do not
+// change.
 //
 // The "skip when power > 0" rule never fires here: power is evaluated as a sum of non-negative
 // terms times -1/2 (see prepare_record), which cannot be positive.
@@ -35,7 +39,8 @@ constexpr unsigned kDrainLimit = 1u << 22;
 struct StageSmem {
     float4 rec[2][kBatch][3];      // double-buffered records
     unsigned gidx[2][kBatch];      // Gaussian index of each staged record
-    float4 box[kBatch];            // (xmin, xmax, ymin, ymax) of the alpha >= 1/255 ellipse
+    float4 cull[kBatch];           // (mean_x, mean_y, B / C, B / A) for the warp culling test
+    float2 cull2[kBatch];          // (D / A, L / A) with D = det / A and L = 2 tau
     unsigned short list[8][kBatch];
     uint64_t bar[2];
 };
@@ -46,23 +51,23 @@ struct BwdSmem {
     unsigned wmax[8];
 };
 
-// Prepares a staged record for evaluation and returns its culling box.
+// Prepares a staged record for evaluation and returns its culling record.
 //
 // The quadratic form -power = (A dx^2 + C dy^2)/2 + B dx dy is evaluated by completing the square,
 // (A u^2 + D dy^2) / 2 with u = dx + r dy, r = B / A and D = det / A, det = A C - B^2: both terms
 // are non-negative, so the evaluation has no cancellation even for very elongated Gaussians
 // (where the three terms of the plain form are large and nearly cancel). det is computed with
 // one rounding error. The record's C slot is replaced by D and slot 9 receives r; A and B stay.
-// A record whose conic is not positive definite is never blended (empty box). Slots 10 and 11
+// A record whose conic is not positive definite is never blended (culled by every warp). Slots 10 and 11
 // receive A and D scaled by -log2(e)/2, so that the kernels take exp(power) as 2^(A' u^2 + D' dy^2)
 // with the hardware base-2 exponential.
 //
-// Box: the set alpha >= 1/255 is -power <= tau = ln(255 opacity), whose axis-aligned half-extents
-// are sqrt(2 tau Sigma'_xx) = sqrt(2 tau C / det) and sqrt(2 tau A / det).
-__device__ __forceinline__ float4 prepare_record(float4& r0, float4& r1, float4& r2) {
+// Culling record: the quantities of the warp test (see the file header) with q divided by A,
+// q / A = (dx + (B/A) dy)^2 + (D/A) dy^2 <= L / A. Records that are never blended get L / A = -1.
+__device__ __forceinline__ float4 prepare_record(float4& r0, float4& r1, float4& r2, float2& cull2) {
     const float mx = r0.x, my = r0.y, A = r0.z, B = r0.w, C = r1.x, o = r1.y;
     const float inf = __int_as_float(0x7f800000);
-    const float4 empty = make_float4(inf, -inf, inf, -inf);
+    cull2 = make_float2(0.f, -1.f);
     const float w = B * B;
     const float e = __fmaf_rn(-B, B, w);
     const float f = __fmaf_rn(A, C, -w);
@@ -72,19 +77,18 @@ __device__ __forceinline__ float4 prepare_record(float4& r0, float4& r1, float4&
         r2.y = 0.f;
         r2.z = 0.f;
         r2.w = 0.f;
-        return empty;
+        return make_float4(mx, my, 0.f, 0.f);
     }
     const float D = det / A;
+    const float r = B / A;
     r1.x = D;
-    r2.y = B / A;     // r
+    r2.y = r;
     r2.z = kNegHalfLog2e * A;
     r2.w = kNegHalfLog2e * D;
-    if (!(o * 1.00001f >= kAlphaMin)) return empty;  // alpha = min(0.99, o G) <= o < 1/255: never blended
+    if (!(o * 1.00001f >= kAlphaMin)) return make_float4(mx, my, 0.f, 0.f);  // alpha <= o < 1/255: never
     const float tau = logf(255.0f * o * 1.00001f) * 1.001f + 0.001f;
-    const float hx = sqrtf(2.f * tau * C / det) * 1.001f + 0.01f;
-    const float hy = sqrtf(2.f * tau * A / det) * 1.001f + 0.01f;
-    if (!(hx < inf && hy < inf)) return make_float4(-inf, inf, -inf, inf);
-    return make_float4(mx - hx, mx + hx, my - hy, my + hy);
+    cull2 = make_float2(D / A, 2.f * tau / A);
+    return make_float4(mx, my, B / C, r);
 }
 
 // ---- batch staging ----------------------------------------------------------------------------
@@ -142,13 +146,20 @@ __device__ __forceinline__ int compact_warp(StageSmem& s, int n_in, int pos_limi
                                             float wy0, float wy1, int warp, int lane) {
     int cnt = 0;
     const int lim = min(n_in, pos_limit);
+    const float x0 = wx0 - 0.01f, x1 = wx1 + 0.01f, y0 = wy0 - 0.01f, y1 = wy1 + 0.01f;
 #pragma unroll
     for (int c = 0; c < kBatch / 32; ++c) {
         const int j = c * 32 + lane;
         bool hit = false;
         if (j < lim) {
-            const float4 b = s.box[j];
-            hit = (b.y >= wx0) && (b.x <= wx1) && (b.w >= wy0) && (b.z <= wy1);
+            const float4 q = s.cull[j];
+            const float2 q2 = s.cull2[j];
+            const float ax = x0 - q.x, bx = x1 - q.x, ay = y0 - q.y, by = y1 - q.y;
+            const float cx = fminf(fmaxf(0.f, ax), bx);
+            const float dy = fminf(fmaxf(-q.z * cx, ay), by);
+            const float dx = fminf(fmaxf(-q.w * dy, ax), bx);
+            const float u = __fmaf_rn(q.w, dy, dx);
+            hit = !(__fmaf_rn(u, u, q2.x * dy * dy) > q2.y);  // NaN keeps the pair
         }
         const unsigned m = __ballot_sync(0xffffffffu, hit);
         if (hit) s.list[warp][cnt + __popc(m & lanemask_lt())] = (unsigned short)j;
@@ -218,8 +229,8 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
             if (ok) consumed = b;
         }
         if (threadIdx.x < n_in)
-            s.box[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
-                                                s.rec[slot][threadIdx.x][2]);
+            s.cull[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
+                                                 s.rec[slot][threadIdx.x][2], s.cull2[threadIdx.x]);
         if (__syncthreads_or(!ok)) break;
         const int nl = compact_warp(s, n_in, kBatch, wx0, wx1, wy0, wy1, warp, lane);
         for (int k = 0; k < nl; ++k) {
@@ -379,8 +390,8 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
             if (ok) consumed = it;
         }
         if (threadIdx.x < n_in)
-            s.box[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
-                                                s.rec[slot][threadIdx.x][2]);
+            s.cull[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
+                                                 s.rec[slot][threadIdx.x][2], s.cull2[threadIdx.x]);
         if (MODE == GS_BWD_SM)
             for (int e = threadIdx.x; e < kBatch * 9; e += kBlock) sm.acc[e] = 0.f;
         if (__syncthreads_or(!ok)) break;
