@@ -4,54 +4,76 @@
 // rasterizer).
 //
 // Result: for every Gaussian with radius > 0 and every tile of its tile rectangle one entry,
-// ordered by (tile, float32 depth bits, Gaussian index). Instead of sorting the D = sum of tiles
-// 64-bit (tile << 32 | depth) keys with 32 + log2(T) bits of passes, the Gaussians are sorted
-// by their 32 depth bits (N items, 4 stable passes), their duplicates are emitted in that order,
-// and the duplicates are sorted stably by tile id (ceil(log2(T) / 8) passes over D items). A
-// stable LSD radix sort on the low key bits followed by passes on the high bits is exactly what
-// a stable sort of the full keys computes, and the emission copies a Gaussian's position in the
-// depth order to all of its duplicates, so the result equals the stable sort of the 64-bit keys
-// of the index-ordered duplicate list.
+// ordered by (tile, float32 depth bits, Gaussian index): the stable sort of the 64-bit keys
+// (tile << 32 | depth bits) of the index-ordered duplicate list. It is computed as an LSD radix
+// sort whose low digits run over the Gaussians instead of their duplicates:
+//   1. the Gaussians with radius > 0 are sorted stably by their 32 depth bits (4 passes of 8 bits;
+//      the first pass drops culled Gaussians, so the others run over the V visible ones);
+//   2. the most significant digit, the whole tile id, is one stable counting pass over the
+//      duplicates of the depth-ordered Gaussians (images of up to 49,152 tiles; see the counting
+//      pass below). Duplicates of one tile keep the depth order, and Gaussians of equal depth bits
+//      keep index order from the stable depth passes.
+// Larger images fall back to emitting the duplicates in depth order and radix-sorting them by
+// tile id in 8-bit passes.
 //
-// Radix pass = histogram (per 4096-item block, 8-bit digit), scan (per digit over blocks),
-// stable scatter (per warp: 16 rounds of 32 consecutive items ranked with match_any).
+// Radix pass = histogram (per 2048-item block, 8-bit digit), scan (per digit over blocks),
+// stable scatter (per warp: 8 rounds of 32 consecutive items ranked with match_any, then the
+// block's items reordered by digit in shared memory and written as coalesced runs).
 #include "gs_common.cuh"
 #include "gs_internal.h"
 
 namespace gs {
 
 constexpr int kSortThreads = 256;
-constexpr int kSortRounds = 16;                          // rounds of 32 items per warp
-constexpr int kSortItems = kSortThreads * kSortRounds;  // 4096 items per block
-constexpr int kWarpItems = 32 * kSortRounds;            // 512 items per warp
+constexpr int kSortRounds = 8;                           // rounds of 32 items per warp
+constexpr int kSortItems = kSortThreads * kSortRounds;  // 2048 items per block
+constexpr int kWarpItems = 32 * kSortRounds;            // 256 items per warp
 
-__global__ void __launch_bounds__(kSortThreads) k_radix_hist(const unsigned* __restrict__ keys, int n, int shift,
-                                                             unsigned mask, unsigned* __restrict__ hist, int nblocks) {
+// Number of items of a pass: the host bound n, or the count the previous pass left on the device.
+__device__ __forceinline__ int item_count(int n, const unsigned* n_dev) {
+    return n_dev ? min(n, (int)*n_dev) : n;
+}
+
+// Item validity: inside the count and, when `radius` is given (first depth pass, whose values are
+// the Gaussian indices), a Gaussian that was not culled.
+__device__ __forceinline__ bool item_valid(int idx, int n, const int* radius) {
+    return idx < n && (!radius || radius[idx] > 0);
+}
+
+__global__ void __launch_bounds__(kSortThreads) k_radix_hist(const unsigned* __restrict__ keys, int n_bound,
+                                                             const unsigned* __restrict__ n_dev,
+                                                             const int* __restrict__ radius, int shift, unsigned mask,
+                                                             unsigned* __restrict__ hist, int nblocks) {
     __shared__ unsigned h[8][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = item_count(n_bound, n_dev);
     for (int i = threadIdx.x; i < 8 * 256; i += kSortThreads) (&h[0][0])[i] = 0u;
-    __syncthreads();
     const int base = blockIdx.x * kSortItems + warp * kWarpItems + lane;
-#pragma unroll 4
+    unsigned d[kSortRounds];
+#pragma unroll
     for (int r = 0; r < kSortRounds; ++r) {
         const int idx = base + r * 32;
-        const bool valid = idx < n;
-        const unsigned d = valid ? (keys[idx] >> shift) & mask : 0x100u;
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        if (valid && (peers & lanemask_lt()) == 0u) h[warp][d] += __popc(peers);
+        d[r] = item_valid(idx, n, radius) ? (keys[idx] >> shift) & mask : 0x100u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kSortRounds; ++r) {
+        const unsigned peers = __match_any_sync(0xffffffffu, d[r]);
+        if (d[r] != 0x100u && (peers & lanemask_lt()) == 0u) h[warp][d[r]] += __popc(peers);
         __syncwarp();
     }
     __syncthreads();
-    const int d = threadIdx.x;
+    const int dg = threadIdx.x;
     unsigned sum = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) sum += h[w][d];
-    hist[(size_t)d * nblocks + blockIdx.x] = sum;
+    for (int w = 0; w < 8; ++w) sum += h[w][dg];
+    hist[(size_t)dg * nblocks + blockIdx.x] = sum;
 }
 
 // Exclusive scan of one digit's row of per-block counts (one block of 1024 threads per digit).
+// count_out (optional, zeroed beforehand) receives the number of valid items of the pass.
 __global__ void __launch_bounds__(1024) k_radix_scan(unsigned* __restrict__ hist, int nblocks,
-                                                     unsigned* __restrict__ totals) {
+                                                     unsigned* __restrict__ totals, unsigned* __restrict__ count_out) {
     __shared__ unsigned wsum[32];
     __shared__ unsigned carry;
     unsigned* row = hist + (size_t)blockIdx.x * nblocks;
@@ -85,47 +107,51 @@ __global__ void __launch_bounds__(1024) k_radix_scan(unsigned* __restrict__ hist
         if (threadIdx.x == 0) carry += wsum[31];
         __syncthreads();
     }
-    if (threadIdx.x == 0) totals[blockIdx.x] = carry;
+    if (threadIdx.x == 0) {
+        totals[blockIdx.x] = carry;
+        if (count_out) atomicAdd(count_out, carry);
+    }
 }
 
 // Stable scatter of one 8-bit digit. IOTA: the values are the item indices. KEY64: also write
 // the 64-bit key (key << 32 | depth_bits[value]) of every item.
 //
-// Each warp ranks its 512 items (16 rounds of 32, in index order) with match_any; the block then
-// reorders its 4096 items by digit in shared memory and writes every digit's run to consecutive
-// global addresses, so the global writes are coalesced.
+// Each warp ranks its 256 items (8 rounds of 32, in index order) with match_any; the block then
+// reorders its valid items by digit in shared memory and writes every digit's run to consecutive
+// global addresses, so the global writes are coalesced. Invalid items (beyond the count, or culled
+// in the first depth pass) take no part: the output holds the valid items only.
 template <bool IOTA, bool KEY64>
 __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
     const unsigned* __restrict__ keys_in, const unsigned* __restrict__ vals_in, unsigned* __restrict__ keys_out,
-    unsigned* __restrict__ vals_out, int n, int shift, unsigned mask, const unsigned* __restrict__ hist,
-    const unsigned* __restrict__ totals, int nblocks, unsigned long long* __restrict__ keys64,
-    const unsigned* __restrict__ depth_bits) {
+    unsigned* __restrict__ vals_out, int n_bound, const unsigned* __restrict__ n_dev, const int* __restrict__ radius,
+    int shift, unsigned mask, const unsigned* __restrict__ hist, const unsigned* __restrict__ totals, int nblocks,
+    unsigned long long* __restrict__ keys64, const unsigned* __restrict__ depth_bits) {
     __shared__ unsigned woff[8][256];      // per-warp digit counts, then block-local offsets
     __shared__ unsigned lbase[256];        // block-local start of each digit
     __shared__ unsigned gbase[256];        // global start of this block's run of each digit
     __shared__ unsigned wsum[8];
+    __shared__ unsigned s_nvalid;
     __shared__ unsigned sk[kSortItems], sv[kSortItems];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int block_first = blockIdx.x * kSortItems;
-    const int n_block = min(kSortItems, n - block_first);
-    unsigned k[kSortRounds], v[kSortRounds];
-    const int base = block_first + warp * kWarpItems + lane;
+    const int n = item_count(n_bound, n_dev);
+    const int base = blockIdx.x * kSortItems + warp * kWarpItems + lane;
+    unsigned k[kSortRounds], v[kSortRounds], dg[kSortRounds];
 #pragma unroll
     for (int r = 0; r < kSortRounds; ++r) {
         const int idx = base + r * 32;
-        const bool valid = idx < n;
+        const bool valid = item_valid(idx, n, radius);
         k[r] = valid ? keys_in[idx] : 0u;
         v[r] = IOTA ? (unsigned)idx : (valid ? vals_in[idx] : 0u);
+        dg[r] = valid ? (k[r] >> shift) & mask : 0x100u;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) woff[warp][lane + 32 * i] = 0u;
     __syncwarp();
 #pragma unroll
     for (int r = 0; r < kSortRounds; ++r) {
-        const bool valid = base + r * 32 < n;
-        const unsigned d = valid ? (k[r] >> shift) & mask : 0x100u;
+        const unsigned d = dg[r];
         const unsigned peers = __match_any_sync(0xffffffffu, d);
-        if (valid && (peers & lanemask_lt()) == 0u) woff[warp][d] += __popc(peers);
+        if (d != 0x100u && (peers & lanemask_lt()) == 0u) woff[warp][d] += __popc(peers);
         __syncwarp();
     }
     __syncthreads();
@@ -159,6 +185,7 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
         for (int w = 0; w < warp; ++w) pre += wsum[w];
         const unsigned lb = pre + x - c;
         lbase[d] = lb;
+        if (d == 255) s_nvalid = lb + c;
 #pragma unroll
         for (int w = 0; w < 8; ++w) woff[w][d] += lb;
         __syncthreads();
@@ -171,8 +198,8 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < kSortRounds; ++r) {
-        const bool valid = base + r * 32 < n;
-        const unsigned d = valid ? (k[r] >> shift) & mask : 0x100u;
+        const unsigned d = dg[r];
+        const bool valid = d != 0x100u;
         const unsigned peers = __match_any_sync(0xffffffffu, d);
         if (valid) {
             const unsigned lp = woff[warp][d] + __popc(peers & lanemask_lt());
@@ -184,6 +211,7 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
         __syncwarp();
     }
     __syncthreads();
+    const int n_block = (int)s_nvalid;
     for (int i = threadIdx.x; i < n_block; i += kSortThreads) {
         const unsigned key = sk[i], val = sv[i];
         const unsigned d = (key >> shift) & mask;
@@ -195,20 +223,31 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
 }
 
 // Block sums (256 Gaussians per block, in depth order) of the number of tiles of each rectangle.
-__global__ void __launch_bounds__(256) k_count(int n, const unsigned* __restrict__ perm, const float4* __restrict__ rec,
+// With `crect`, also the packed rectangle of every depth-ordered Gaussian,
+// crect[i] = (x0 | y0 << 16, w | h << 16), w = h = 0 when empty (tile ids below 2^16).
+__global__ void __launch_bounds__(256) k_count(int n_bound, const unsigned* __restrict__ n_dev,
+                                               const unsigned* __restrict__ perm, const float4* __restrict__ rec,
                                                const int* __restrict__ radius, int tiles_x, int tiles_y,
-                                               unsigned long long* __restrict__ block_sums) {
+                                               unsigned long long* __restrict__ block_sums,
+                                               uint2* __restrict__ crect) {
     __shared__ unsigned long long ws[8];
+    const int n = item_count(n_bound, n_dev);
     const int i = blockIdx.x * 256 + threadIdx.x;
     unsigned long long cnt = 0;
     if (i < n) {
         const unsigned g = perm[i];
         const int r = radius[g];
+        uint2 packed = make_uint2(0u, 0u);
         if (r > 0) {
             const float4 r0 = rec[3 * (size_t)g];
             const Rect R = tile_rect(r0.x, r0.y, r, tiles_x, tiles_y);
-            if (R.x0 <= R.x1) cnt = (unsigned long long)(R.x1 - R.x0 + 1) * (unsigned long long)(R.y1 - R.y0 + 1);
+            if (R.x0 <= R.x1 && R.y0 <= R.y1) {
+                cnt = (unsigned long long)(R.x1 - R.x0 + 1) * (unsigned long long)(R.y1 - R.y0 + 1);
+                packed = make_uint2((unsigned)R.x0 | ((unsigned)R.y0 << 16),
+                                    (unsigned)(R.x1 - R.x0 + 1) | ((unsigned)(R.y1 - R.y0 + 1) << 16));
+            }
         }
+        if (crect) crect[i] = packed;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
@@ -263,7 +302,8 @@ __global__ void __launch_bounds__(1024) k_scan_u64(const unsigned long long* __r
 // Emits the duplicates of 256 consecutive Gaussians (depth order) into their block's contiguous
 // output range: output o goes to the Gaussian whose prefix range contains o (binary search over
 // the block's 256 offsets), and is its (o - offset)-th tile in row-major rectangle order.
-__global__ void __launch_bounds__(256) k_emit(int n, const unsigned* __restrict__ perm, const float4* __restrict__ rec,
+__global__ void __launch_bounds__(256) k_emit(int n_bound, const unsigned* __restrict__ n_dev,
+                                              const unsigned* __restrict__ perm, const float4* __restrict__ rec,
                                               const int* __restrict__ radius, int tiles_x, int tiles_y,
                                               const unsigned long long* __restrict__ block_offs,
                                               unsigned long long capacity, unsigned* __restrict__ tile_out,
@@ -272,6 +312,7 @@ __global__ void __launch_bounds__(256) k_emit(int n, const unsigned* __restrict_
     __shared__ int s_x0[256], s_y0[256], s_w[256];
     __shared__ unsigned s_g[256];
     __shared__ unsigned wsum[8];
+    const int n = item_count(n_bound, n_dev);
     const int i = blockIdx.x * 256 + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned cnt = 0, g = 0;
@@ -349,6 +390,296 @@ __global__ void k_ranges(unsigned d, const unsigned* __restrict__ tiles, uint2* 
     if (iend == d) ranges[prev].y = d;
 }
 
+// ---- tile pass as one stable counting pass (images of up to kMaxCountTiles tiles) -------------
+//
+// The depth-ordered Gaussians are cut into chunks. For every chunk a shared-memory histogram over
+// the tiles counts the Gaussians whose rectangle covers each tile; a scan down each tile's column
+// of the chunk x tile table gives the chunk's first position inside every tile's list, and the
+// tile totals give the ranges and D. Each chunk then places its entries in depth order (see
+// k_chunk_place). This is the stable counting sort of the duplicates by tile id (an LSD radix pass
+// whose digit is the whole tile id) applied to the depth-ordered list: equal tile ids keep depth
+// order.
+//
+// Depth order puts the Gaussians nearest to the camera, which are the largest on screen, first: at
+// the outdoor scene the first 512 of them cover 17x the mean number of tiles. A chunk therefore
+// ends after kChunk Gaussians or about kChunkDup entries, whichever comes first: Gaussian i
+// (depth order, P(i) entries before it) belongs to chunk floor(i / kChunk) + floor(P(i) / kChunkDup),
+// which never decreases with i (ids that are skipped are empty chunks). Within a chunk, rectangles
+// are spread over lanes, and placement splits the chunk into bands of tile rows.
+constexpr int kChunk = 512;             // Gaussians per chunk at most
+constexpr long long kChunkDup = 16384;  // entries after which a chunk ends early
+constexpr int kMaxCountTiles = 49152;   // tile counters that fit in shared memory (192 KB)
+constexpr int kSmallRect = 8;           // rectangles of up to this many tiles: one lane each
+
+// Upper bound of the chunk ids for n Gaussians and at most `cap` entries (ids are clamped to it,
+// which only matters when the entries exceed `cap`, a capacity error).
+static long long max_chunks(long long n, long long cap) { return (n + kChunk - 1) / kChunk + cap / kChunkDup + 1; }
+
+__device__ __forceinline__ int chunk_of(int i, unsigned long long before, int cmax) {
+    const unsigned long long c = (unsigned long long)(i / kChunk) + before / (unsigned long long)kChunkDup;
+    return (int)min(c, (unsigned long long)(cmax - 1));
+}
+
+// First Gaussian of every chunk (chunk_first[c] for c < nchunks, chunk_first[nchunks] = V) and the
+// number of chunks used. block_offs: entries before each 256-Gaussian block (k_count, k_scan_u64).
+__global__ void __launch_bounds__(256) k_chunk_bounds(int n_bound, const unsigned* __restrict__ n_dev,
+                                                      const uint2* __restrict__ crect,
+                                                      const unsigned long long* __restrict__ block_offs, int cmax,
+                                                      unsigned* __restrict__ chunk_first,
+                                                      unsigned* __restrict__ nchunks) {
+    __shared__ unsigned long long wsum[8];
+    __shared__ int s_c[256];
+    const int n = item_count(n_bound, n_dev);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    unsigned long long area = 0;
+    if (i < n) {
+        const uint2 r = crect[i];
+        area = (unsigned long long)(r.y & 0xffffu) * (r.y >> 16);
+    }
+    unsigned long long x = area;  // inclusive scan over the block
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    unsigned long long wpre = 0;
+    for (int w = 0; w < warp; ++w) wpre += wsum[w];
+    const unsigned long long before = block_offs[blockIdx.x] + wpre + x - area;
+    const int c = chunk_of(i, before, cmax);
+    s_c[threadIdx.x] = c;
+    __syncthreads();
+    if (i >= n) return;
+    int cprev = -1;
+    if (threadIdx.x > 0) {
+        cprev = s_c[threadIdx.x - 1];
+    } else if (i > 0) {
+        const uint2 r = crect[i - 1];
+        cprev = chunk_of(i - 1, before - (unsigned long long)(r.y & 0xffffu) * (r.y >> 16), cmax);
+    }
+    for (int k = cprev + 1; k <= c; ++k) chunk_first[k] = (unsigned)i;
+    if (i == n - 1) {
+        chunk_first[c + 1] = (unsigned)n;
+        *nchunks = (unsigned)(c + 1);
+    }
+}
+
+// Counts per tile of one chunk (one block per chunk id; ids at or beyond the count return).
+__global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__ nchunks,
+                                                    const unsigned* __restrict__ chunk_first,
+                                                    const uint2* __restrict__ crect, int tiles_x, int T,
+                                                    unsigned* __restrict__ table) {
+    extern __shared__ unsigned cnt[];
+    const unsigned full = 0xffffffffu;
+    const int c = blockIdx.x;
+    if (c >= (int)*nchunks) return;
+    const int first = (int)chunk_first[c], last = (int)chunk_first[c + 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int t = threadIdx.x; t < T; t += blockDim.x) cnt[t] = 0u;
+    __syncthreads();
+    for (int base = first + 32 * warp; base < last; base += (int)blockDim.x) {  // warp-uniform
+        const int i = base + lane;
+        int x0 = 0, y0 = 0, w = 0, area = 0;
+        if (i < last) {
+            const uint2 r = crect[i];
+            x0 = (int)(r.x & 0xffffu);
+            y0 = (int)(r.x >> 16);
+            w = (int)(r.y & 0xffffu);
+            area = w * (int)(r.y >> 16);
+        }
+        if (area <= kSmallRect) {
+            for (int k = 0; k < area; ++k) {
+                const int rk = k / w;
+                atomicAdd(&cnt[(y0 + rk) * tiles_x + x0 + (k - rk * w)], 1u);
+            }
+        }
+        unsigned big = __ballot_sync(full, area > kSmallRect);
+        while (big) {  // large rectangles: all lanes of the warp
+            const int j = __ffs(big) - 1;
+            big &= big - 1u;
+            const int jx = __shfl_sync(full, x0, j), jy = __shfl_sync(full, y0, j), jw = __shfl_sync(full, w, j);
+            const int ja = __shfl_sync(full, area, j);
+            for (int k = lane; k < ja; k += 32) {
+                const int rk = k / jw;
+                atomicAdd(&cnt[(jy + rk) * tiles_x + jx + (k - rk * jw)], 1u);
+            }
+        }
+    }
+    __syncthreads();
+    unsigned* row = table + (size_t)c * T;
+    for (int t = threadIdx.x; t < T; t += blockDim.x) row[t] = cnt[t];
+}
+
+// Exclusive scan down each tile's column of the chunk x tile table (in place) and the tile totals.
+// Block: 32 tiles (one per lane) x 32 warps, each warp a contiguous range of chunks.
+constexpr int kScanWarps = 32;
+__global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* __restrict__ nchunks, int T,
+                                                                unsigned* __restrict__ table,
+                                                                unsigned* __restrict__ tile_total) {
+    __shared__ unsigned part[kScanWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * 32 + lane;
+    const int nc = (int)*nchunks;
+    const int per = (nc + kScanWarps - 1) / kScanWarps;
+    const int c0 = min(nc, warp * per), c1 = min(nc, c0 + per);
+    unsigned sum = 0;
+    if (t < T) {
+        int c = c0;
+        for (; c + 8 <= c1; c += 8) {
+            unsigned v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = table[(size_t)(c + k) * T + t];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sum += v[k];
+        }
+        for (; c < c1; ++c) sum += table[(size_t)c * T + t];
+    }
+    part[warp][lane] = sum;
+    __syncthreads();
+    unsigned run = 0;
+    for (int w = 0; w < warp; ++w) run += part[w][lane];
+    if (t < T) {
+        int c = c0;
+        for (; c + 8 <= c1; c += 8) {
+            unsigned v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = table[(size_t)(c + k) * T + t];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                table[(size_t)(c + k) * T + t] = run;
+                run += v[k];
+            }
+        }
+        for (; c < c1; ++c) {
+            unsigned* e = &table[(size_t)c * T + t];
+            const unsigned v = *e;
+            *e = run;
+            run += v;
+        }
+        if (warp == kScanWarps - 1) tile_total[t] = run;
+    }
+}
+
+// Exclusive scan of the tile totals (one block): tile_start[t]; total[0] = D.
+__global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __restrict__ tile_total,
+                                                    unsigned* __restrict__ tile_start,
+                                                    unsigned long long* __restrict__ total) {
+    __shared__ unsigned long long wsum[32];
+    __shared__ unsigned long long carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0ull;
+    __syncthreads();
+    for (int base = 0; base < T; base += 1024) {
+        const int i = base + threadIdx.x;
+        const unsigned long long v = i < T ? tile_total[i] : 0ull;
+        unsigned long long x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            unsigned long long s2 = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, s2, o);
+                if (lane >= o) s2 += y;
+            }
+            wsum[lane] = s2;
+        }
+        __syncthreads();
+        const unsigned long long wpre = warp ? wsum[warp - 1] : 0ull;
+        if (i < T) tile_start[i] = (unsigned)(carry + wpre + x - v);
+        __syncthreads();
+        if (threadIdx.x == 0) carry += wsum[31];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) total[0] = carry;
+}
+
+__global__ void k_write_ranges(int T, const unsigned* __restrict__ tile_start, const unsigned* __restrict__ tile_total,
+                               uint2* __restrict__ ranges) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < T) ranges[t] = tile_total[t] ? make_uint2(tile_start[t], tile_start[t] + tile_total[t]) : make_uint2(0u, 0u);
+}
+
+// Placement: one warp per (chunk, band of tile rows). The warp copies the chunk's starting offset
+// inside each of the band's tiles into shared memory, then walks the chunk's Gaussians in depth
+// order; for each one whose rectangle meets the band, its lanes cover the rectangle's tiles inside
+// the band (distinct tiles, so no two lanes share an offset) and append the Gaussian there. Entries
+// therefore land in depth order within every tile; bands own disjoint tiles.
+constexpr int kPlaceWarps = 8;        // warps per block when shared memory allows
+constexpr int kBandTiles = 256;       // tiles per band (whole tile rows, at least one)
+
+__global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
+    const unsigned* __restrict__ nchunks, const unsigned* __restrict__ chunk_first, const unsigned* __restrict__ perm,
+    const uint2* __restrict__ crect, int tiles_x, int tiles_y, int band_rows, int nbands,
+    const unsigned* __restrict__ table, const unsigned* __restrict__ tile_start, unsigned capacity,
+    unsigned* __restrict__ vals, unsigned long long* __restrict__ keys64, const unsigned* __restrict__ depth_bits,
+    unsigned* __restrict__ err) {
+    extern __shared__ unsigned smem_off[];
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
+    const int chunk = (int)(gw / nbands), band = (int)(gw - (long long)chunk * nbands);
+    if (chunk >= (int)*nchunks) return;
+    const int first = (int)chunk_first[chunk], last = (int)chunk_first[chunk + 1];
+    if (first >= last) return;
+    const int T = tiles_x * tiles_y;
+    const int r0 = band * band_rows, r1 = min(r0 + band_rows, tiles_y);
+    const int tb0 = r0 * tiles_x, ntb = (r1 - r0) * tiles_x;
+    unsigned* off = smem_off + (size_t)warp * band_rows * tiles_x;
+    const unsigned* row = table + (size_t)chunk * T + tb0;
+    const unsigned* ts = tile_start + tb0;
+    for (int t = lane; t < ntb; t += 32) off[t] = ts[t] + row[t];
+    __syncwarp();
+    unsigned g_next = 0u;
+    uint2 r_next = make_uint2(0u, 0u);
+    if (first + lane < last) {
+        g_next = perm[first + lane];
+        r_next = crect[first + lane];
+    }
+    for (int base = first; base < last; base += 32) {
+        const unsigned g = g_next;
+        const uint2 pr = r_next;
+        const int nx = base + 32 + lane;  // prefetch the next 32 Gaussians
+        g_next = 0u;
+        r_next = make_uint2(0u, 0u);
+        if (nx < last) {
+            g_next = perm[nx];
+            r_next = crect[nx];
+        }
+        const int x0 = (int)(pr.x & 0xffffu), y0 = (int)(pr.x >> 16), w = (int)(pr.y & 0xffffu);
+        const int ya = max(y0, r0), yb = min(y0 + (int)(pr.y >> 16), r1);
+        unsigned hit = __ballot_sync(full, w > 0 && ya < yb);
+        while (hit) {
+            const int j = __ffs(hit) - 1;
+            hit &= hit - 1u;
+            const unsigned jg = __shfl_sync(full, g, j);
+            const int jx = __shfl_sync(full, x0, j), jw = __shfl_sync(full, w, j);
+            const int jya = __shfl_sync(full, ya, j), jyb = __shfl_sync(full, yb, j);
+            const int area = jw * (jyb - jya);
+            for (int k = lane; k < area; k += 32) {
+                const int rk = k / jw;
+                const int tl = (jya - r0 + rk) * tiles_x + jx + (k - rk * jw);  // band-local tile
+                const unsigned pos = off[tl];
+                off[tl] = pos + 1u;
+                if (pos < capacity) {
+                    vals[pos] = jg;
+                    if (keys64) keys64[pos] = ((unsigned long long)(tb0 + tl) << 32) | depth_bits[jg];
+                } else {
+                    atomicOr(err, kErrCheck);
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
 // ---- host orchestration ----------------------------------------------------------------------
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -361,91 +692,156 @@ int tile_bits_of(long long tiles) {
     return b;
 }
 
-SortWorkspace carve_workspace(void* base, long long n, long long cap) {
+bool counting_path(long long tiles) { return tiles <= kMaxCountTiles; }
+
+SortWorkspace carve_workspace(void* base, long long n, long long cap, long long tiles) {
     SortWorkspace w{};
     char* p = static_cast<char*>(base);
     size_t off = 0;
     auto take = [&](size_t bytes) { char* q = p ? p + off : nullptr; off += align256(bytes); return q; };
-    const long long nn = n > 0 ? n : 1, cc = cap > 0 ? cap : 1;
+    const long long nn = n > 0 ? n : 1, cc = cap > 0 ? cap : 1, tt = tiles > 0 ? tiles : 1;
+    const bool counting = counting_path(tt);
     w.dkA = (unsigned*)take(4 * nn);
     w.dkB = (unsigned*)take(4 * nn);
     w.dvA = (unsigned*)take(4 * nn);
     w.dvB = (unsigned*)take(4 * nn);
-    const int nbmax = sort_blocks(nn > cc ? nn : cc);
+    const int nbmax = sort_blocks(counting ? nn : (nn > cc ? nn : cc));
     w.hist = (unsigned*)take((size_t)256 * nbmax * 4);
     w.totals = (unsigned*)take(256 * 4);
+    w.total = (unsigned long long*)take(8);
+    w.nvis = (unsigned*)take(4);
     const long long gblocks = (nn + 255) / 256;
     w.bsum = (unsigned long long*)take(8 * gblocks);
     w.boff = (unsigned long long*)take(8 * gblocks);
-    w.total = (unsigned long long*)take(8);
-    w.tA = (unsigned*)take(4 * cc);
-    w.tB = (unsigned*)take(4 * cc);
-    w.vB = (unsigned*)take(4 * cc);
+    if (counting) {
+        w.cmax = max_chunks(nn, cc);
+        w.table = (unsigned*)take((size_t)w.cmax * tt * 4);
+        w.crect = (uint2*)take(8 * nn);
+        w.tile_total = (unsigned*)take(4 * tt);
+        w.tile_start = (unsigned*)take(4 * tt);
+        w.chunk_first = (unsigned*)take(4 * (w.cmax + 1));
+        w.nchunks = (unsigned*)take(4);
+        w.dsum = (unsigned long long*)take(8);
+    } else {
+        w.tA = (unsigned*)take(4 * cc);
+        w.tB = (unsigned*)take(4 * cc);
+        w.vB = (unsigned*)take(4 * cc);
+    }
     w.bytes = off;
     return w;
 }
 
-static cudaError_t radix_pass(const unsigned* kin, const unsigned* vin, unsigned* kout, unsigned* vout, int n, int shift,
-                              int bits, bool iota, unsigned long long* keys64, const unsigned* depth_bits,
+static cudaError_t radix_pass(const unsigned* kin, const unsigned* vin, unsigned* kout, unsigned* vout, int n,
+                              const unsigned* n_dev, const int* radius, unsigned* count_out, int shift, int bits,
+                              bool iota, unsigned long long* keys64, const unsigned* depth_bits,
                               const SortWorkspace& w, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     const int nb = sort_blocks(n);
     const unsigned mask = (1u << bits) - 1u;
     count_launches(3);
-    k_radix_hist<<<nb, kSortThreads, 0, st>>>(kin, n, shift, mask, w.hist, nb);
-    k_radix_scan<<<256, 1024, 0, st>>>(w.hist, nb, w.totals);
+    k_radix_hist<<<nb, kSortThreads, 0, st>>>(kin, n, n_dev, radius, shift, mask, w.hist, nb);
+    k_radix_scan<<<256, 1024, 0, st>>>(w.hist, nb, w.totals, count_out);
     if (iota)
-        k_radix_scatter<true, false><<<nb, kSortThreads, 0, st>>>(kin, vin, kout, vout, n, shift, mask, w.hist, w.totals, nb, nullptr, nullptr);
+        k_radix_scatter<true, false><<<nb, kSortThreads, 0, st>>>(kin, vin, kout, vout, n, n_dev, radius, shift, mask,
+                                                                  w.hist, w.totals, nb, nullptr, nullptr);
     else if (keys64)
-        k_radix_scatter<false, true><<<nb, kSortThreads, 0, st>>>(kin, vin, kout, vout, n, shift, mask, w.hist, w.totals, nb, keys64, depth_bits);
+        k_radix_scatter<false, true><<<nb, kSortThreads, 0, st>>>(kin, vin, kout, vout, n, n_dev, radius, shift, mask,
+                                                                  w.hist, w.totals, nb, keys64, depth_bits);
     else
-        k_radix_scatter<false, false><<<nb, kSortThreads, 0, st>>>(kin, vin, kout, vout, n, shift, mask, w.hist, w.totals, nb, nullptr, nullptr);
+        k_radix_scatter<false, false><<<nb, kSortThreads, 0, st>>>(kin, vin, kout, vout, n, n_dev, radius, shift, mask,
+                                                                   w.hist, w.totals, nb, nullptr, nullptr);
     return cudaGetLastError();
 }
 
-// Phase 1: depth sort and duplicate count; leaves the total in w.total (device).
+// Phase 1: depth sort of the visible Gaussians (the first pass drops radius-0 Gaussians and
+// leaves their number V on the device; later passes and the count run over V items) and the
+// duplicate count; leaves the total D in w.total (device).
 cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, cudaStream_t st) {
     const int n = (int)proj.n;
     if (n == 0) return cudaMemsetAsync(w.total, 0, 8, st);
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     cudaError_t e;
-    if ((e = radix_pass(depth_bits, nullptr, w.dkA, w.dvA, n, 0, 8, true, nullptr, nullptr, w, st))) return e;
-    if ((e = radix_pass(w.dkA, w.dvA, w.dkB, w.dvB, n, 8, 8, false, nullptr, nullptr, w, st))) return e;
-    if ((e = radix_pass(w.dkB, w.dvB, w.dkA, w.dvA, n, 16, 8, false, nullptr, nullptr, w, st))) return e;
-    if ((e = radix_pass(w.dkA, w.dvA, w.dkB, w.dvB, n, 24, 8, false, nullptr, nullptr, w, st))) return e;
-    const int gblocks = (n + 255) / 256;
+    if ((e = cudaMemsetAsync(w.nvis, 0, 4, st))) return e;
+    if ((e = radix_pass(depth_bits, nullptr, w.dkA, w.dvA, n, nullptr, proj.radius, w.nvis, 0, 8, true, nullptr,
+                        nullptr, w, st)))
+        return e;
+    if ((e = radix_pass(w.dkA, w.dvA, w.dkB, w.dvB, n, w.nvis, nullptr, nullptr, 8, 8, false, nullptr, nullptr, w, st)))
+        return e;
+    if ((e = radix_pass(w.dkB, w.dvB, w.dkA, w.dvA, n, w.nvis, nullptr, nullptr, 16, 8, false, nullptr, nullptr, w, st)))
+        return e;
+    if ((e = radix_pass(w.dkA, w.dvA, w.dkB, w.dvB, n, w.nvis, nullptr, nullptr, 24, 8, false, nullptr, nullptr, w, st)))
+        return e;
     const float4* rec = reinterpret_cast<const float4*>(proj.rec);
+    const int T = tiles_x * tiles_y;
+    const int gblocks = (n + 255) / 256;
+    if (counting_path(T)) {
+        const size_t smem = (size_t)T * 4;
+        if ((e = cudaFuncSetAttribute(k_chunk_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+            return e;
+        if ((e = cudaMemsetAsync(w.nchunks, 0, 4, st))) return e;
+        count_launches(6);
+        k_count<<<gblocks, 256, 0, st>>>(n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y, w.bsum, w.crect);
+        k_scan_u64<<<1, 1024, 0, st>>>(w.bsum, gblocks, w.boff, w.dsum);
+        k_chunk_bounds<<<gblocks, 256, 0, st>>>(n, w.nvis, w.crect, w.boff, (int)w.cmax, w.chunk_first, w.nchunks);
+        k_chunk_hist<<<(unsigned)w.cmax, 256, smem, st>>>(w.nchunks, w.chunk_first, w.crect, tiles_x, T, w.table);
+        k_chunk_scan<<<(T + 31) / 32, 32 * kScanWarps, 0, st>>>(w.nchunks, T, w.table, w.tile_total);
+        k_tile_scan<<<1, 1024, 0, st>>>(T, w.tile_total, w.tile_start, w.total);
+        return cudaGetLastError();
+    }
     count_launches(2);
-    k_count<<<gblocks, 256, 0, st>>>(n, w.dvB, rec, proj.radius, tiles_x, tiles_y, w.bsum);
+    k_count<<<gblocks, 256, 0, st>>>(n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y, w.bsum, nullptr);
     k_scan_u64<<<1, 1024, 0, st>>>(w.bsum, gblocks, w.boff, w.total);
     return cudaGetLastError();
 }
 
-// Phase 2: emission in depth order, tile passes, ranges. d = number of duplicates (<= capacity).
+// Phase 2: placement (counting pass) or emission + tile radix passes, and the ranges.
+// d = number of duplicates (<= capacity).
 cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
                           cudaStream_t st) {
     const int n = (int)proj.n;
     const long long T = (long long)tiles_x * tiles_y;
-    cudaError_t e = cudaMemsetAsync(ranges, 0, (size_t)T * 8, st);
-    if (e) return e;
-    if (d == 0) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    if (n == 0 || d == 0 || !counting_path(T)) {
+        if ((e = cudaMemsetAsync(ranges, 0, (size_t)T * 8, st))) return e;
+        if (n == 0 || d == 0) return cudaSuccess;
+    }
+    const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
+    unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
+    if (counting_path(T)) {
+        count_launches(1);
+        k_write_ranges<<<(int)((T + 255) / 256), 256, 0, st>>>((int)T, w.tile_start, w.tile_total,
+                                                               reinterpret_cast<uint2*>(ranges));
+        const int band_rows = tiles_x >= kBandTiles ? 1 : kBandTiles / tiles_x;
+        const int nbands = (tiles_y + band_rows - 1) / band_rows;
+        const size_t band_bytes = (size_t)band_rows * tiles_x * 4;
+        int wpb = (int)((200 * 1024) / band_bytes);
+        wpb = wpb < 1 ? 1 : (wpb > kPlaceWarps ? kPlaceWarps : wpb);
+        const size_t smem = (size_t)wpb * band_bytes;
+        if ((e = cudaFuncSetAttribute(k_chunk_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+            return e;
+        const long long warps = w.cmax * nbands;
+        count_launches(1);
+        k_chunk_place<<<(unsigned)((warps + wpb - 1) / wpb), 32 * wpb, smem, st>>>(
+            w.nchunks, w.chunk_first, w.dvB, w.crect, tiles_x, tiles_y, band_rows, nbands, w.table, w.tile_start,
+            (unsigned)capacity, vals, k64, depth_bits, err);
+        return cudaGetLastError();
+    }
     const int tb = tile_bits_of(T);
     const int passes = (tb + 7) / 8;
-    const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     unsigned* tbuf[2] = {w.tA, w.tB};
     unsigned* vbuf[2] = {vals, w.vB};
     int cur = passes & 1;  // emission target so that the last pass lands in `vals`
     const int gblocks = (n + 255) / 256;
     const float4* rec = reinterpret_cast<const float4*>(proj.rec);
     count_launches(1);
-    k_emit<<<gblocks, 256, 0, st>>>(n, w.dvB, rec, proj.radius, tiles_x, tiles_y, w.boff, capacity, tbuf[cur], vbuf[cur], err);
-    unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
+    k_emit<<<gblocks, 256, 0, st>>>(n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y, w.boff, capacity, tbuf[cur],
+                                    vbuf[cur], err);
     for (int p = 0; p < passes; ++p) {
         const int bits = (tb - 8 * p) < 8 ? (tb - 8 * p) : 8;
         const bool lastp = p == passes - 1;
-        if ((e = radix_pass(tbuf[cur], vbuf[cur], tbuf[cur ^ 1], vbuf[cur ^ 1], (int)d, 8 * p, bits, false,
-                            lastp ? k64 : nullptr, depth_bits, w, st)))
+        if ((e = radix_pass(tbuf[cur], vbuf[cur], tbuf[cur ^ 1], vbuf[cur ^ 1], (int)d, nullptr, nullptr, nullptr,
+                            8 * p, bits, false, lastp ? k64 : nullptr, depth_bits, w, st)))
             return e;
         cur ^= 1;
     }

@@ -229,10 +229,9 @@ int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* op
 }
 
 size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32_t height) {
-    (void)width;
-    (void)height;
-    if (n < 0 || capacity < 0) return 0;
-    return carve_workspace(nullptr, n, capacity).bytes;
+    if (n < 0 || capacity < 0 || width <= 0 || height <= 0) return 0;
+    const long long tiles = (long long)((width + kTile - 1) / kTile) * ((height + kTile - 1) / kTile);
+    return carve_workspace(nullptr, n, capacity, tiles).bytes;
 }
 
 int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, void* workspace,
@@ -247,10 +246,11 @@ int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options*
     if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or not 8-byte aligned");
     if (capacity > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
     if (keys && !aligned(keys, 8)) return fail(GS_ERR_ARG, "keys not 8-byte aligned");
-    const size_t need = carve_workspace(nullptr, proj->n, capacity).bytes;
+    const long long tiles = (long long)kc.tiles_x * kc.tiles_y;
+    const size_t need = carve_workspace(nullptr, proj->n, capacity, tiles).bytes;
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
         return fail(GS_ERR_ARG, "workspace NULL, not 256-byte aligned or smaller than %zu bytes", need);
-    const SortWorkspace w = carve_workspace(workspace, proj->n, capacity);
+    const SortWorkspace w = carve_workspace(workspace, proj->n, capacity, tiles);
     unsigned* err = error_word(&s);
     if (!err) return s;
     cudaStream_t st = as_stream(stream);
@@ -279,7 +279,8 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
     if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or not 8-byte aligned");
     if (capacity > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
     if (keys && !aligned(keys, 8)) return fail(GS_ERR_ARG, "keys not 8-byte aligned");
-    const size_t need = carve_workspace(nullptr, proj->n, capacity).bytes;
+    const long long tiles = (long long)kc.tiles_x * kc.tiles_y;
+    const size_t need = carve_workspace(nullptr, proj->n, capacity, tiles).bytes;
     if (need > (size_t)GS_STATIC_SORT_WORKSPACE_BYTES)
         return fail(GS_ERR_ARG,
                     "n = %lld with capacity %lld needs %zu bytes of sort workspace; the static workspace holds %u "
@@ -287,7 +288,7 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
                     (long long)proj->n, (long long)capacity, need, (unsigned)GS_STATIC_SORT_WORKSPACE_BYTES);
     unsigned char* ws = static_sort_workspace(&s);
     if (!ws) return s;
-    const SortWorkspace w = carve_workspace(ws, proj->n, capacity);
+    const SortWorkspace w = carve_workspace(ws, proj->n, capacity, tiles);
     unsigned* err = error_word(&s);
     if (!err) return s;
     cudaStream_t st = as_stream(stream);

@@ -45,12 +45,23 @@ def test_status_strings_and_version(lib):
         assert lib.gs_status_string(st).decode().startswith("GS_")
 
 
-def test_workspace_size_grows_with_inputs(lib):
+def test_workspace_size_matches_the_documented_layout(lib):
     a = lib.gs_sort_workspace_bytes(1000, 10_000, 128, 128)
-    b = lib.gs_sort_workspace_bytes(1_000_000, 10_000_000, 1297, 840)
+    n, T = 1_000_000, 82 * 53
+    b = lib.gs_sort_workspace_bytes(n, 10_000_000, 1297, 840)
     assert 0 < a < b
-    assert b >= 16 * 1_000_000 + 12 * 10_000_000
+    # counting tile pass: depth sort, packed rectangles and the chunk x tile table, whose rows are
+    # chunks of at most 512 Gaussians or about 16384 entries
+    rows = (n + 511) // 512 + 10_000_000 // 16384 + 1
+    assert b >= 24 * n + 4 * T * rows
+    small = lib.gs_sort_workspace_bytes(n, 1, 1297, 840)
+    assert 0 < b - small <= 4 * T * (10_000_000 // 16384) + 4096
+    # more than 49,152 tiles: radix tile passes, 12 more bytes per duplicate of capacity
+    big1 = lib.gs_sort_workspace_bytes(n, 1_000_000, 4112, 4112)
+    big2 = lib.gs_sort_workspace_bytes(n, 2_000_000, 4112, 4112)
+    assert big2 - big1 >= 12 * 1_000_000
     assert lib.gs_sort_workspace_bytes(-1, 0, 1, 1) == 0
+    assert lib.gs_sort_workspace_bytes(10, 10, 0, 16) == 0
 
 
 def _cam(w=64, h=64, f=64.0):

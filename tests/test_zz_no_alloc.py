@@ -62,11 +62,16 @@ def test_static_workspace_sort_matches_regular_entry_point_twice(cfg, n, res):
 
 
 def test_static_workspace_rejects_requests_beyond_its_size():
-    s = gs_scenes.make_scene(0)
-    cam = s.cameras[0]
-    proj = _proj(s, cam)
-    too_big = 4_000_000  # 12 bytes per duplicate alone exceed 32 MiB
-    assert api.gs_sort_workspace_bytes(proj.n, too_big, cam.width, cam.height) > _abi.GS_STATIC_SORT_WORKSPACE_BYTES
-    st, D, _, _, _ = _static_call(proj, cam, api.make_options(0), too_big)
+    # two million culled Gaussians (all inputs valid, zeroed) need more than 32 MiB of workspace:
+    # the call must refuse before touching the device
+    n = 2_000_000
+    cam = gs_scenes.make_scene(0).cameras[0]
+    proj = api.Proj(rec=torch.zeros((n, 12), dtype=torch.float32, device=DEV),
+                    depth=torch.zeros(n, dtype=torch.float32, device=DEV),
+                    radius=torch.zeros(n, dtype=torch.int32, device=DEV),
+                    tiles_touched=torch.zeros(n, dtype=torch.int32, device=DEV))
+    cap = 1000
+    assert api.gs_sort_workspace_bytes(n, cap, cam.width, cam.height) > _abi.GS_STATIC_SORT_WORKSPACE_BYTES
+    st, D, _, _, _ = _static_call(proj, cam, api.make_options(0), cap)
     assert st == _abi.GS_ERR_ARG
     assert b"static workspace" in _abi.load().gs_last_error_message()
