@@ -411,6 +411,11 @@ constexpr long long kChunkDup = 16384;  // entries after which a chunk ends earl
 constexpr int kMaxCountTiles = 49152;   // tile counters that fit in shared memory (192 KB)
 constexpr int kSmallRect = 8;           // rectangles of up to this many tiles: one lane each
 
+// k / w for 0 <= k, w < 2^16 as a multiply-high: with m = floor((2^32 - 1) / w) + 1 (w >= 2) the
+// product k m / 2^32 exceeds k / w by less than k / 2^32 < 1 / w, so its floor is exact.
+__device__ __forceinline__ unsigned div_magic(unsigned w) { return w > 1u ? 0xffffffffu / w + 1u : 0u; }
+__device__ __forceinline__ unsigned div_by(unsigned k, unsigned w, unsigned m) { return w > 1u ? __umulhi(k, m) : k; }
+
 // Upper bound of the chunk ids for n Gaussians and at most `cap` entries (ids are clamped to it,
 // which only matters when the entries exceed `cap`, a capacity error).
 static long long max_chunks(long long n, long long cap) { return (n + kChunk - 1) / kChunk + cap / kChunkDup + 1; }
@@ -490,20 +495,20 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__
             area = w * (int)(r.y >> 16);
         }
         if (area <= kSmallRect) {
-            for (int k = 0; k < area; ++k) {
-                const int rk = k / w;
-                atomicAdd(&cnt[(y0 + rk) * tiles_x + x0 + (k - rk * w)], 1u);
-            }
+            for (int y = 0; y < area / max(w, 1); ++y)
+                for (int x = 0; x < w; ++x) atomicAdd(&cnt[(y0 + y) * tiles_x + x0 + x], 1u);
         }
+        const unsigned m = div_magic((unsigned)w);
         unsigned big = __ballot_sync(full, area > kSmallRect);
         while (big) {  // large rectangles: all lanes of the warp
             const int j = __ffs(big) - 1;
             big &= big - 1u;
-            const int jx = __shfl_sync(full, x0, j), jy = __shfl_sync(full, y0, j), jw = __shfl_sync(full, w, j);
-            const int ja = __shfl_sync(full, area, j);
-            for (int k = lane; k < ja; k += 32) {
-                const int rk = k / jw;
-                atomicAdd(&cnt[(jy + rk) * tiles_x + jx + (k - rk * jw)], 1u);
+            const unsigned jw = (unsigned)__shfl_sync(full, w, j), jm = __shfl_sync(full, m, j);
+            const unsigned ja = (unsigned)__shfl_sync(full, area, j);
+            const unsigned t0 = (unsigned)(__shfl_sync(full, y0, j) * tiles_x + __shfl_sync(full, x0, j));
+            for (unsigned k = lane; k < ja; k += 32u) {
+                const unsigned rk = div_by(k, jw, jm);
+                atomicAdd(&cnt[t0 + rk * (unsigned)tiles_x + (k - rk * jw)], 1u);
             }
         }
     }
@@ -611,9 +616,10 @@ __global__ void k_write_ranges(int T, const unsigned* __restrict__ tile_start, c
 // inside each of the band's tiles into shared memory, then walks the chunk's Gaussians in depth
 // order; for each one whose rectangle meets the band, its lanes cover the rectangle's tiles inside
 // the band (distinct tiles, so no two lanes share an offset) and append the Gaussian there. Entries
-// therefore land in depth order within every tile; bands own disjoint tiles.
+// therefore land in depth order within every tile; bands own disjoint tiles. Chunks end after
+// about 16k entries, so a warp never walks more than a bounded amount of work.
 constexpr int kPlaceWarps = 8;        // warps per block when shared memory allows
-constexpr int kBandTiles = 256;       // tiles per band (whole tile rows, at least one)
+constexpr int kPlaceBands = 8;        // bands per chunk (whole tile rows)
 
 __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
     const unsigned* __restrict__ nchunks, const unsigned* __restrict__ chunk_first, const unsigned* __restrict__ perm,
@@ -631,6 +637,7 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
     if (first >= last) return;
     const int T = tiles_x * tiles_y;
     const int r0 = band * band_rows, r1 = min(r0 + band_rows, tiles_y);
+    if (r0 >= r1) return;
     const int tb0 = r0 * tiles_x, ntb = (r1 - r0) * tiles_x;
     unsigned* off = smem_off + (size_t)warp * band_rows * tiles_x;
     const unsigned* row = table + (size_t)chunk * T + tb0;
@@ -653,19 +660,25 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
             g_next = perm[nx];
             r_next = crect[nx];
         }
-        const int x0 = (int)(pr.x & 0xffffu), y0 = (int)(pr.x >> 16), w = (int)(pr.y & 0xffffu);
-        const int ya = max(y0, r0), yb = min(y0 + (int)(pr.y >> 16), r1);
-        unsigned hit = __ballot_sync(full, w > 0 && ya < yb);
+        // this lane's Gaussian inside the band: columns [x0, x0 + w), rows [ya, yb) (band-local)
+        const unsigned w = pr.y & 0xffffu;
+        const int y0 = (int)(pr.x >> 16);
+        const int ya = max(y0, r0) - r0, yb = min(y0 + (int)(pr.y >> 16), r1) - r0;
+        const unsigned xw = (pr.x & 0xffffu) | (w << 16);
+        const unsigned yab = (unsigned)ya | ((unsigned)max(yb, 0) << 16);
+        const unsigned m = div_magic(w);
+        unsigned hit = __ballot_sync(full, w > 0u && ya < yb);
         while (hit) {
             const int j = __ffs(hit) - 1;
             hit &= hit - 1u;
-            const unsigned jg = __shfl_sync(full, g, j);
-            const int jx = __shfl_sync(full, x0, j), jw = __shfl_sync(full, w, j);
-            const int jya = __shfl_sync(full, ya, j), jyb = __shfl_sync(full, yb, j);
-            const int area = jw * (jyb - jya);
-            for (int k = lane; k < area; k += 32) {
-                const int rk = k / jw;
-                const int tl = (jya - r0 + rk) * tiles_x + jx + (k - rk * jw);  // band-local tile
+            const unsigned jg = __shfl_sync(full, g, j), jxw = __shfl_sync(full, xw, j);
+            const unsigned jyab = __shfl_sync(full, yab, j), jm = __shfl_sync(full, m, j);
+            const unsigned jw = jxw >> 16, jya = jyab & 0xffffu;
+            const unsigned area = jw * ((jyab >> 16) - jya);
+            const unsigned tl0 = jya * (unsigned)tiles_x + (jxw & 0xffffu);
+            for (unsigned k = lane; k < area; k += 32u) {
+                const unsigned rk = div_by(k, jw, jm);
+                const unsigned tl = tl0 + rk * (unsigned)tiles_x + (k - rk * jw);  // band-local tile
                 const unsigned pos = off[tl];
                 off[tl] = pos + 1u;
                 if (pos < capacity) {
@@ -812,7 +825,7 @@ cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigne
         count_launches(1);
         k_write_ranges<<<(int)((T + 255) / 256), 256, 0, st>>>((int)T, w.tile_start, w.tile_total,
                                                                reinterpret_cast<uint2*>(ranges));
-        const int band_rows = tiles_x >= kBandTiles ? 1 : kBandTiles / tiles_x;
+        const int band_rows = (tiles_y + kPlaceBands - 1) / kPlaceBands;
         const int nbands = (tiles_y + band_rows - 1) / band_rows;
         const size_t band_bytes = (size_t)band_rows * tiles_x * 4;
         int wpb = (int)((200 * 1024) / band_bytes);

@@ -94,6 +94,14 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsign
         : "memory");
 }
 
+// Asynchronous 4-byte global -> shared copy (no register staging; completes at cp_async_wait_all,
+// which waits for the calling thread's own copies).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     unsigned ok;
     asm volatile(

@@ -104,48 +104,85 @@ __device__ __forceinline__ bool geometry(const float* m, const float* ls, const 
     return true;
 }
 
+constexpr int kFwdThreads = 128;
+
+// Copies the SH coefficients of the warp's 32 Gaussians (contiguous K3 floats each) between global
+// memory and a padded shared-memory tile (row stride K3 + 1: conflict-free per-thread rows) with
+// coalesced accesses, for the rows whose bit is set in `rows` (lane order). LOAD: global -> shared
+// (asynchronous copies, waited for before returning; the caller then synchronises the warp);
+// else shared -> global (ADD: added to global).
+template <int K3, bool LOAD, bool ADD>
+__device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, int n, int lane, unsigned rows) {
+    const int cnt = min(32, n - first);
+    if (cnt <= 0 || rows == 0u) return;
+    const int total = cnt * K3;
+    float* gw = g + (size_t)first * K3;
+    // loads are asynchronous copies, all in flight at once; the caller synchronises the warp
+#pragma unroll 4
+    for (int e = lane; e < total; e += 32) {
+        const int row = e / K3, col = e - row * K3;
+        if (!((rows >> row) & 1u)) continue;
+        if (LOAD) cp_async4(&tile[row * (K3 + 1) + col], gw + e);
+        else if (ADD) gw[e] += tile[row * (K3 + 1) + col];
+        else gw[e] = tile[row * (K3 + 1) + col];
+    }
+    if (LOAD) cp_async_wait_all();
+}
+
 template <int DEG>
-__global__ void __launch_bounds__(256) k_preprocess(int n, const float* __restrict__ mean3d,
-                                                    const float* __restrict__ log_scale,
-                                                    const float* __restrict__ quat,
-                                                    const float* __restrict__ logit,
-                                                    const float* __restrict__ sh, const KernelCamera cam,
-                                                    float4* __restrict__ rec, float* __restrict__ depth,
-                                                    int* __restrict__ radius,
-                                                    unsigned* __restrict__ tiles_touched) {
+__global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* __restrict__ mean3d,
+                                                            const float* __restrict__ log_scale,
+                                                            const float* __restrict__ quat,
+                                                            const float* __restrict__ logit,
+                                                            const float* __restrict__ sh, const KernelCamera cam,
+                                                            float4* __restrict__ rec, float* __restrict__ depth,
+                                                            int* __restrict__ radius,
+                                                            unsigned* __restrict__ tiles_touched) {
     constexpr int K = (DEG + 1) * (DEG + 1);
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const float m[3] = {mean3d[3 * i], mean3d[3 * i + 1], mean3d[3 * i + 2]};
-    const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
-    const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
+    constexpr int K3 = 3 * K;
+    __shared__ float tile_all[kFwdThreads / 32][32 * (K3 + 1)];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int warp_first = blockIdx.x * kFwdThreads + warp * 32;
+    if (warp_first >= n) return;  // whole warp
+    const int i = warp_first + lane;
+    float m[3] = {0.f, 0.f, 0.f};
     Geo g;
-    bool ok = geometry(m, ls, q, cam, g);
-    depth[i] = g.p[2];
+    bool ok = false;
     int r = 0;
     unsigned tt = 0;
-    if (ok) {
-        // largest eigenvalue of the 2D covariance in the cancellation-free form
-        const float hd = 0.5f * (g.a - g.c);
-        const float lam = 0.5f * (g.a + g.c) + sqrtf(hd * hd + g.b * g.b);
-        const float rf = ceilf(3.f * sqrtf(lam));
-        ok = isfinite(g.mx) && isfinite(g.my) && rf < 16777216.0f;  // radius < 2^24 px (also rejects NaN)
+    if (i < n) {
+        m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
+        const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
+        const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
+        ok = geometry(m, ls, q, cam, g);
+        depth[i] = g.p[2];
         if (ok) {
-            r = (int)rf;
-            const Rect R = tile_rect(g.mx, g.my, r, cam.tiles_x, cam.tiles_y);
-            ok = R.x0 <= R.x1;
-            if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+            // largest eigenvalue of the 2D covariance in the cancellation-free form
+            const float hd = 0.5f * (g.a - g.c);
+            const float lam = 0.5f * (g.a + g.c) + sqrtf(hd * hd + g.b * g.b);
+            const float rf = ceilf(3.f * sqrtf(lam));
+            ok = isfinite(g.mx) && isfinite(g.my) && rf < 16777216.0f;  // radius < 2^24 px (also rejects NaN)
+            if (ok) {
+                r = (int)rf;
+                const Rect R = tile_rect(g.mx, g.my, r, cam.tiles_x, cam.tiles_y);
+                ok = R.x0 <= R.x1;
+                if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+            }
+        }
+        if (!ok) {
+            radius[i] = 0;
+            tiles_touched[i] = 0;
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            rec[3 * i] = z4;
+            rec[3 * i + 1] = z4;
+            rec[3 * i + 2] = z4;
         }
     }
-    if (!ok) {
-        radius[i] = 0;
-        tiles_touched[i] = 0;
-        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        rec[3 * i] = z4;
-        rec[3 * i + 1] = z4;
-        rec[3 * i + 2] = z4;
-        return;
-    }
+    // SH coefficients of the warp's visible Gaussians only, with coalesced loads
+    float* tile = tile_all[warp];
+    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, __ballot_sync(0xffffffffu, ok));
+    __syncwarp();
+    if (!ok) return;
     const float op = 1.f / (1.f + expf(-logit[i]));
     // view direction from the camera centre to the mean
     float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
@@ -153,7 +190,7 @@ __global__ void __launch_bounds__(256) k_preprocess(int n, const float* __restri
     dx *= dinv; dy *= dinv; dz *= dinv;
     float Y[16];
     sh_basis<DEG>(dx, dy, dz, Y);
-    const float* shg = sh + (size_t)i * K * 3;
+    const float* shg = tile + lane * (K3 + 1);
     float col[3] = {0.5f, 0.5f, 0.5f};
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -170,23 +207,6 @@ __global__ void __launch_bounds__(256) k_preprocess(int n, const float* __restri
 
 constexpr int kBwdThreads = 128;
 
-// Copies the SH coefficients of the warp's 32 Gaussians (contiguous K3 floats each) between global
-// memory and a padded shared-memory tile (row stride K3 + 1: conflict-free per-thread rows) with
-// coalesced accesses. LOAD: global -> shared; else shared -> global (ADD: added to global).
-template <int K3, bool LOAD, bool ADD>
-__device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, int n, int lane) {
-    const int cnt = min(32, n - first);
-    if (cnt <= 0) return;
-    const int total = cnt * K3;
-    float* gw = g + (size_t)first * K3;
-    for (int e = lane; e < total; e += 32) {
-        const int row = e / K3, col = e - row * K3;
-        if (LOAD) tile[row * (K3 + 1) + col] = gw[e];
-        else if (ADD) gw[e] += tile[row * (K3 + 1) + col];
-        else gw[e] = tile[row * (K3 + 1) + col];
-    }
-}
-
 template <int DEG>
 __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
@@ -201,7 +221,9 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     float* tile = tile_all[warp];
     const int warp_first = blockIdx.x * kBwdThreads + warp * 32;
     const int i = warp_first + lane;
-    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane);
+    // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only
+    const unsigned seen = __ballot_sync(0xffffffffu, i < n && radius[i] > 0);
+    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
     __syncwarp();
     float* my = tile + lane * (K3 + 1);   // this thread's coefficients, then its SH gradients
     float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
@@ -209,9 +231,9 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     Geo g;
     float m[3] = {0.f, 0.f, 0.f};
     if (i < n) {
-        m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
-        live = radius[i] > 0;
+        live = (seen >> lane) & 1u;
         if (live) {
+            m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
             const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
             const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
             live = geometry(m, ls, q, cam, g);
@@ -350,8 +372,9 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
         }
     }
     __syncwarp();
-    if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane);
-    else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane);
+    // accumulating: rows of Gaussians with radius 0 add nothing and are skipped
+    if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane, seen);
+    else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane, 0xffffffffu);
 }
 
 // ---- host-side launchers ------------------------------------------------------------------------
@@ -359,15 +382,15 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
                               cudaStream_t st) {
     if (n == 0) return cudaSuccess;
-    const int blocks = (n + 255) / 256;
+    const int blocks = (n + kFwdThreads - 1) / kFwdThreads;
     float4* rec = reinterpret_cast<float4*>(out.rec);
     unsigned* tt = out.tiles_touched;
     count_launches(1);
     switch (deg) {
-        case 0: k_preprocess<0><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
-        case 1: k_preprocess<1><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
-        case 2: k_preprocess<2><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
-        default: k_preprocess<3><<<blocks, 256, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+        case 0: k_preprocess<0><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+        case 1: k_preprocess<1><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+        case 2: k_preprocess<2><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
+        default: k_preprocess<3><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
     }
     return cudaGetLastError();
 }

@@ -348,8 +348,9 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
         g1 = dl_dimage[plane + pix];
         g2 = dl_dimage[2 * plane + pix];
     }
-    // colour blended behind the current Gaussian, background included
-    float S0 = T * cam.bg[0], S1 = T * cam.bg[1], S2 = T * cam.bg[2];
+    // sum over channels of dL/dpixel_c x (colour blended behind the current Gaussian, background
+    // included): the only form in which that colour enters dL/dalpha
+    float gS = T * (g0 * cam.bg[0] + g1 * cam.bg[1] + g2 * cam.bg[2]);
     const unsigned wmax = __reduce_max_sync(0xffffffffu, last);
     if (lane == 0) sm.wmax[warp] = wmax;
     __syncthreads();
@@ -423,10 +424,9 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
                 v[6] = aT * g0;
                 v[7] = aT * g1;
                 v[8] = aT * g2;
-                const float dalpha = g0 * (r1.z * T - S0 * inv) + g1 * (r1.w * T - S1 * inv) + g2 * (cb * T - S2 * inv);
-                S0 += r1.z * aT;
-                S1 += r1.w * aT;
-                S2 += cb * aT;
+                const float gc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2 * cb));
+                const float dalpha = __fmaf_rn(T, gc, -inv * gS);
+                gS = __fmaf_rn(aT, gc, gS);
                 if (oG <= kAlphaMax) {
                     const float dpow = oG * dalpha;
                     v[5] = G * dalpha;
