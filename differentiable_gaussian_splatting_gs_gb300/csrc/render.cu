@@ -1,14 +1,17 @@
 // Rendering phase (forward alpha blending) and gradient computation phase (backward) of the tile
-// rasterizer: one 256-thread block per 16x16-pixel tile, one pixel per thread, the tile's sorted
-// list staged in shared memory in batches of 256 records.
+// rasterizer: one block per 16x16-pixel tile, the tile's sorted list staged in shared memory in
+// batches of records (forward: 256 threads, one pixel each, 256-record batches; backward: 128
+// threads, two pixels each, 128-record batches).
 //
 // The backward accumulates each Gaussian's gradient over all pixels with atomics; that
 // accumulation is the bottleneck that DISTWAR (Fast Differentiable Rendering on Raster-based
 // Rendering Pipelines, Abstract) and ARC (Warp-level Adaptive Atomic Reduction in GPUs to
 // Accelerate Differentiable Rendering, Abstract) identify, and the reason for the GS_BWD_* modes.
 //
-// Warp layout: warp w covers the 8x4 pixel block at (8 (w & 1), 4 (w >> 1)) of the tile; lane l
-// is pixel (l & 7, l >> 3) of that block.
+// Warp layout. Forward: warp w covers the 8x4 pixel block at (8 (w & 1), 4 (w >> 1)) of the tile;
+// lane l is pixel (l & 7, l >> 3) of that block. Backward: warp w covers the 8x8 block at
+// (8 (w & 1), 8 (w >> 1)); lane l holds pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4), so that
+// a Gaussian's record loads, warp reduction and atomics serve 64 pixels.
 //
 // Warp-level culling. Before blending a batch, each warp keeps only the staged Gaussians whose
 // alpha can reach 1/255 somewhere in its 8x4 block: the set alpha >= 1/255 is the ellipse
@@ -36,19 +39,31 @@ constexpr float kNegHalfLog2e = -0.72134752044448170f;  // -log2(e) / 2
 // of the caller's spin limit so that a small limit cannot leave copies running into a dead block.
 constexpr unsigned kDrainLimit = 1u << 22;
 
-struct StageSmem {
-    float4 rec[2][kBatch][3];      // double-buffered records
-    unsigned gidx[2][kBatch];      // Gaussian index of each staged record
-    float4 cull[kBatch];           // (mean_x, mean_y, B / C, B / A) for the warp culling test
-    float2 cull2[kBatch];          // (D / A, L / A) with D = det / A and L = 2 tau
-    unsigned short list[8][kBatch];
+// Shared-memory staging ring of BATCH records for a block of WARPS warps (one record per thread).
+template <int BATCH, int WARPS>
+struct StageSmemT {
+    static constexpr int kB = BATCH;
+    float4 rec[2][BATCH][3];       // double-buffered records
+    unsigned gidx[2][BATCH];       // Gaussian index of each staged record
+    float4 cull[BATCH];            // (mean_x, mean_y, B / C, B / A) for the warp culling test
+    float2 cull2[BATCH];           // (D / A, L / A) with D = det / A and L = 2 tau
+    unsigned short list[WARPS][BATCH];
     uint64_t bar[2];
 };
 
+// Forward: 256 threads per tile, one pixel each; warp w covers the 8x4 block at (8 (w & 1), 4 (w >> 1)).
+using FwdStage = StageSmemT<kBatch, 8>;
+
+// Backward: 128 threads per tile, two pixels each; warp w covers the 8x8 block at
+// (8 (w & 1), 8 (w >> 1)), lane l the pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4) of it.
+constexpr int kBwdBlock = 128;
+constexpr int kBwdBatch = 128;
+using BwdStage = StageSmemT<kBwdBatch, 4>;
+
 struct BwdSmem {
-    StageSmem st;
-    float acc[kBatch * 9];         // per-batch gradient accumulators (GS_BWD_SM)
-    unsigned wmax[8];
+    BwdStage st;
+    float acc[kBwdBatch * 9];      // per-batch gradient accumulators (GS_BWD_SM)
+    unsigned wmax[4];
 };
 
 // Prepares a staged record for evaluation and returns its culling record.
@@ -95,13 +110,13 @@ __device__ __forceinline__ float4 prepare_record(float4& r0, float4& r1, float4&
 
 // Registers the transaction bytes of batch `b` on its barrier (thread 0 only, before any copy of
 // that batch is issued).
-template <int STAGING>
-__device__ __forceinline__ void stage_expect(StageSmem& s, int slot, int n_in) {
+template <int STAGING, class S>
+__device__ __forceinline__ void stage_expect(S& s, int slot, int n_in) {
     if (STAGING == GS_STAGE_BULK) mbar_arrive_expect_tx(&s.bar[slot], (unsigned)n_in * 48u);
 }
 
-template <int STAGING>
-__device__ __forceinline__ void stage_issue(StageSmem& s, int slot, const float4* __restrict__ rec,
+template <int STAGING, class S>
+__device__ __forceinline__ void stage_issue(S& s, int slot, const float4* __restrict__ rec,
                                             const unsigned* __restrict__ vals, int first, int n_in,
                                             unsigned n_gauss, float4 (&pre)[3], unsigned* err) {
     const int t = threadIdx.x;
@@ -124,8 +139,8 @@ __device__ __forceinline__ void stage_issue(StageSmem& s, int slot, const float4
 
 // Makes batch `slot` visible in shared memory. For register staging the loads issued by
 // stage_issue are stored here; the caller synchronises the block afterwards.
-template <int STAGING>
-__device__ __forceinline__ bool stage_wait(StageSmem& s, int slot, unsigned parity, int n_in, const float4 (&pre)[3],
+template <int STAGING, class S>
+__device__ __forceinline__ bool stage_wait(S& s, int slot, unsigned parity, int n_in, const float4 (&pre)[3],
                                            unsigned spin_limit, unsigned* err) {
     if (STAGING == GS_STAGE_BULK) {
         return mbar_wait_bounded(&s.bar[slot], parity, spin_limit, err);
@@ -142,13 +157,14 @@ __device__ __forceinline__ bool stage_wait(StageSmem& s, int slot, unsigned pari
 
 // Compacts the staged entries [0, n_in) that may be blended in this warp's block (and whose
 // batch position is below `pos_limit`) into s.list[warp], in increasing order. Returns the count.
-__device__ __forceinline__ int compact_warp(StageSmem& s, int n_in, int pos_limit, float wx0, float wx1,
+template <class S>
+__device__ __forceinline__ int compact_warp(S& s, int n_in, int pos_limit, float wx0, float wx1,
                                             float wy0, float wy1, int warp, int lane) {
     int cnt = 0;
     const int lim = min(n_in, pos_limit);
     const float x0 = wx0 - 0.01f, x1 = wx1 + 0.01f, y0 = wy0 - 0.01f, y1 = wy1 + 0.01f;
 #pragma unroll
-    for (int c = 0; c < kBatch / 32; ++c) {
+    for (int c = 0; c < S::kB / 32; ++c) {
         const int j = c * 32 + lane;
         bool hit = false;
         if (j < lim) {
@@ -177,7 +193,7 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
                                                        unsigned n_gauss, float* __restrict__ image,
                                                        float* __restrict__ t_final, unsigned* __restrict__ n_contrib,
                                                        unsigned spin_limit, unsigned* __restrict__ err) {
-    __shared__ StageSmem s;
+    __shared__ FwdStage s;
     const int tile = blockIdx.x;
     const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -315,76 +331,113 @@ __device__ __forceinline__ float warp_reduce9(const float (&v)[9], int lane, flo
     return x;
 }
 
+// Adds one pixel's contribution to a Gaussian's 9 gradient components and steps the pixel's
+// backward state past that Gaussian: T becomes the transmittance in front of it, gS gains its
+// colour. r0, r1, r2: the prepared record; g0..g2: dL/dpixel.
+__device__ __forceinline__ void add_pixel(float (&v)[9], float alpha, float oG, float G, float dx, float dy, float u,
+                                          const float4& r0, const float4& r1, const float4& r2, float& T, float& gS,
+                                          float g0, float g1, float g2) {
+    const float inv = rcp_approx(1.f - alpha);
+    T *= inv;
+    const float aT = alpha * T;
+    v[6] = __fmaf_rn(aT, g0, v[6]);
+    v[7] = __fmaf_rn(aT, g1, v[7]);
+    v[8] = __fmaf_rn(aT, g2, v[8]);
+    const float gc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2 * r2.x));
+    const float dalpha = __fmaf_rn(T, gc, -inv * gS);
+    gS = __fmaf_rn(aT, gc, gS);
+    if (oG <= kAlphaMax) {
+        const float dpow = oG * dalpha;
+        v[5] = __fmaf_rn(G, dalpha, v[5]);
+        // d power / d mean = -(A dx + B dy, B dx + C dy) = -(A u, B u + D dy)
+        v[0] = __fmaf_rn(-r0.z * u, dpow, v[0]);
+        v[1] = __fmaf_rn(-__fmaf_rn(r0.w, u, r1.x * dy), dpow, v[1]);
+        v[2] = __fmaf_rn(-0.5f * dx * dx, dpow, v[2]);
+        v[3] = __fmaf_rn(-dx * dy, dpow, v[3]);
+        v[4] = __fmaf_rn(-0.5f * dy * dy, dpow, v[4]);
+    }
+}
+
 template <int MODE, int STAGING>
-__global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
-                                                       const uint2* __restrict__ ranges, const KernelCamera cam,
-                                                       unsigned n_gauss, const float* __restrict__ dl_dimage,
-                                                       const float* __restrict__ t_final,
-                                                       const unsigned* __restrict__ n_contrib,
-                                                       float* __restrict__ grad2d, int thr, unsigned spin_limit,
-                                                       unsigned* __restrict__ err) {
+__global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restrict__ rec,
+                                                          const unsigned* __restrict__ vals,
+                                                          const uint2* __restrict__ ranges, const KernelCamera cam,
+                                                          unsigned n_gauss, const float* __restrict__ dl_dimage,
+                                                          const float* __restrict__ t_final,
+                                                          const unsigned* __restrict__ n_contrib,
+                                                          float* __restrict__ grad2d, int thr, unsigned spin_limit,
+                                                          unsigned* __restrict__ err) {
+    constexpr int kB = kBwdBatch;
     __shared__ BwdSmem sm;
-    StageSmem& s = sm.st;
+    BwdStage& s = sm.st;
     const int tile = blockIdx.x;
     const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 4 * (warp >> 1);
-    const int px = bx + (lane & 7), py = by + (lane >> 3);
-    const bool inside = px < cam.width && py < cam.height;
-    const float fpx = (float)px + 0.5f, fpy = (float)py + 0.5f;
-    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 3.f;
+    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 8 * (warp >> 1);
+    const int px = bx + (lane & 7), py0 = by + (lane >> 3), py1 = py0 + 4;
+    const float fpx = (float)px + 0.5f, fpy0 = (float)py0 + 0.5f, fpy1 = (float)py1 + 0.5f;
+    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 7.f;
 
     const uint2 rg = ranges[tile];
     const int start = (int)rg.x;
     const int count = (int)(rg.y > rg.x ? rg.y - rg.x : 0);
 
-    const size_t pix = (size_t)py * cam.width + px, plane = (size_t)cam.width * cam.height;
-    unsigned last = 0;
-    float T = 1.f, g0 = 0.f, g1 = 0.f, g2 = 0.f;
-    if (inside) {
-        last = min(n_contrib[pix], (unsigned)count);
-        T = t_final[pix];
-        g0 = dl_dimage[pix];
-        g1 = dl_dimage[plane + pix];
-        g2 = dl_dimage[2 * plane + pix];
+    const size_t plane = (size_t)cam.width * cam.height;
+    // per pixel: contributor count, transmittance (from T_final backwards), dL/dpixel and the sum
+    // over channels of dL/dpixel_c x (colour blended behind the current Gaussian, background
+    // included), the only form in which that colour enters dL/dalpha
+    unsigned last0 = 0, last1 = 0;
+    float T0 = 1.f, T1 = 1.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f;
+    if (px < cam.width && py0 < cam.height) {
+        const size_t pix = (size_t)py0 * cam.width + px;
+        last0 = min(n_contrib[pix], (unsigned)count);
+        T0 = t_final[pix];
+        a0 = dl_dimage[pix];
+        a1 = dl_dimage[plane + pix];
+        a2 = dl_dimage[2 * plane + pix];
     }
-    // sum over channels of dL/dpixel_c x (colour blended behind the current Gaussian, background
-    // included): the only form in which that colour enters dL/dalpha
-    float gS = T * (g0 * cam.bg[0] + g1 * cam.bg[1] + g2 * cam.bg[2]);
-    const unsigned wmax = __reduce_max_sync(0xffffffffu, last);
+    if (px < cam.width && py1 < cam.height) {
+        const size_t pix = (size_t)py1 * cam.width + px;
+        last1 = min(n_contrib[pix], (unsigned)count);
+        T1 = t_final[pix];
+        b0 = dl_dimage[pix];
+        b1 = dl_dimage[plane + pix];
+        b2 = dl_dimage[2 * plane + pix];
+    }
+    float gS0 = T0 * (a0 * cam.bg[0] + a1 * cam.bg[1] + a2 * cam.bg[2]);
+    float gS1 = T1 * (b0 * cam.bg[0] + b1 * cam.bg[1] + b2 * cam.bg[2]);
+    const unsigned wmax = __reduce_max_sync(0xffffffffu, max(last0, last1));
     if (lane == 0) sm.wmax[warp] = wmax;
     __syncthreads();
-    unsigned tmax = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tmax = max(tmax, sm.wmax[w]);
-    const int nb = ((int)tmax + kBatch - 1) / kBatch;
+    const unsigned tmax = max(max(sm.wmax[0], sm.wmax[1]), max(sm.wmax[2], sm.wmax[3]));
+    const int nb = ((int)tmax + kB - 1) / kB;
     float4 pre[3];
 
     if (nb > 0) {
-        const int b0 = nb - 1;
+        const int bl = nb - 1;
         if (threadIdx.x == 0 && STAGING == GS_STAGE_BULK) {
             mbar_init(&s.bar[0], 1);
             mbar_init(&s.bar[1], 1);
             fence_mbar_init();
-            stage_expect<STAGING>(s, 0, min(kBatch, count - b0 * kBatch));
-            if (nb > 1) stage_expect<STAGING>(s, 1, kBatch);
+            stage_expect<STAGING>(s, 0, min(kB, count - bl * kB));
+            if (nb > 1) stage_expect<STAGING>(s, 1, kB);
         }
         __syncthreads();
-        stage_issue<STAGING>(s, 0, rec, vals, start + b0 * kBatch, min(kBatch, count - b0 * kBatch), n_gauss, pre, err);
+        stage_issue<STAGING>(s, 0, rec, vals, start + bl * kB, min(kB, count - bl * kB), n_gauss, pre, err);
     }
     bool ok = true;
     int issued = nb > 0 ? 0 : -1, consumed = -1;  // iterations whose copies were issued / waited for
     for (int it = 0; it < nb; ++it) {
         const int b = nb - 1 - it;          // batches back to front
         const int slot = it & 1;
-        const int n_in = min(kBatch, count - b * kBatch);
+        const int n_in = min(kB, count - b * kB);
         float4 nxt[3];
         if (STAGING == GS_STAGE_LOADS) {
             ok = stage_wait<STAGING>(s, slot, 0, n_in, pre, spin_limit, err);
-            if (b > 0) stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b - 1) * kBatch, kBatch, n_gauss, nxt, err);
+            if (b > 0) stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b - 1) * kB, kB, n_gauss, nxt, err);
         } else {
             if (b > 0) {
-                stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b - 1) * kBatch, kBatch, n_gauss, nxt, err);
+                stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b - 1) * kB, kB, n_gauss, nxt, err);
                 issued = it + 1;
             }
             ok = stage_wait<STAGING>(s, slot, (unsigned)(it >> 1) & 1u, n_in, pre, spin_limit, err);
@@ -394,56 +447,39 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
             s.cull[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
                                                  s.rec[slot][threadIdx.x][2], s.cull2[threadIdx.x]);
         if (MODE == GS_BWD_SM)
-            for (int e = threadIdx.x; e < kBatch * 9; e += kBlock) sm.acc[e] = 0.f;
+            for (int e = threadIdx.x; e < kB * 9; e += kBwdBlock) sm.acc[e] = 0.f;
         if (__syncthreads_or(!ok)) break;
-        const int pos_limit = (int)wmax - b * kBatch;
+        const int pos_limit = (int)wmax - b * kB;
         const int nl = compact_warp(s, n_in, pos_limit, wx0, wx1, wy0, wy1, warp, lane);
         for (int k = nl - 1; k >= 0; --k) {
             const int j = s.list[warp][k];
-            const unsigned pos = (unsigned)(b * kBatch + j);
+            const unsigned pos = (unsigned)(b * kB + j);
             const float4 r0 = s.rec[slot][j][0];   // (mean_x, mean_y, A, B)
             const float4 r1 = s.rec[slot][j][1];   // (D, o, r, g)
             const float4 r2 = s.rec[slot][j][2];   // (b, r, A', D')
-            const float dx = r0.x - fpx, dy = r0.y - fpy;
-            const float u = __fmaf_rn(r2.y, dy, dx);
-            const float Au = r0.z * u;
-            const float G = ex2_approx(__fmaf_rn(r2.z * u, u, r2.w * dy * dy));  // exp(power)
-            const float oG = r1.y * G;
-            const float alpha = fminf(kAlphaMax, oG);
-            const bool contrib = pos < last && alpha >= kAlphaMin;
-            const unsigned ballot = __ballot_sync(0xffffffffu, contrib);
+            const float dx = r0.x - fpx, dy0 = r0.y - fpy0, dy1 = r0.y - fpy1;
+            const float u0 = __fmaf_rn(r2.y, dy0, dx), u1 = __fmaf_rn(r2.y, dy1, dx);
+            const float G0 = ex2_approx(__fmaf_rn(r2.z * u0, u0, r2.w * dy0 * dy0));  // exp(power)
+            const float G1 = ex2_approx(__fmaf_rn(r2.z * u1, u1, r2.w * dy1 * dy1));
+            const float oG0 = r1.y * G0, oG1 = r1.y * G1;
+            const float alpha0 = fminf(kAlphaMax, oG0), alpha1 = fminf(kAlphaMax, oG1);
+            const bool c0 = pos < last0 && alpha0 >= kAlphaMin;
+            const bool c1 = pos < last1 && alpha1 >= kAlphaMin;
+            const unsigned ballot = __ballot_sync(0xffffffffu, c0 || c1);
             if (ballot == 0u) continue;
             float v[9];
 #pragma unroll
             for (int c = 0; c < 9; ++c) v[c] = 0.f;
-            if (contrib) {
-                const float cb = r2.x;
-                const float inv = rcp_approx(1.f - alpha);
-                T *= inv;                               // transmittance in front of this Gaussian
-                const float aT = alpha * T;
-                v[6] = aT * g0;
-                v[7] = aT * g1;
-                v[8] = aT * g2;
-                const float gc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2 * cb));
-                const float dalpha = __fmaf_rn(T, gc, -inv * gS);
-                gS = __fmaf_rn(aT, gc, gS);
-                if (oG <= kAlphaMax) {
-                    const float dpow = oG * dalpha;
-                    v[5] = G * dalpha;
-                    // d power / d mean = -(A dx + B dy, B dx + C dy) = -(A u, B u + D dy)
-                    v[0] = -Au * dpow;
-                    v[1] = -(r0.w * u + r1.x * dy) * dpow;
-                    v[2] = -0.5f * dx * dx * dpow;
-                    v[3] = -dx * dy * dpow;
-                    v[4] = -0.5f * dy * dy * dpow;
-                }
-            }
+            if (c0) add_pixel(v, alpha0, oG0, G0, dx, dy0, u0, r0, r1, r2, T0, gS0, a0, a1, a2);
+            if (c1) add_pixel(v, alpha1, oG1, G1, dx, dy1, u1, r0, r1, r2, T1, gS1, b0, b1, b2);
+            const bool contrib = c0 || c1;
             const int nact = __popc(ballot);
             if (MODE == GS_BWD_DIRECT || (MODE == GS_BWD_ADAPTIVE && nact < thr)) {
                 if (contrib) {
                     float* gp = grad2d + 12 * (size_t)s.gidx[slot][j];
-#pragma unroll
-                    for (int c = 0; c < 9; ++c) red_add_global(gp + c, v[c]);
+                    red_add_global_v4(gp, v[0], v[1], v[2], v[3]);
+                    red_add_global_v4(gp + 4, v[4], v[5], v[6], v[7]);
+                    red_add_global(gp + 8, v[8]);
                 }
             } else if (MODE == GS_BWD_SM && nact < thr) {
                 if (contrib) {
@@ -471,16 +507,16 @@ __global__ void __launch_bounds__(kBlock) k_render_bwd(const float4* __restrict_
         __syncthreads();
         if (MODE == GS_BWD_SM && threadIdx.x < n_in) {
             const float* a = sm.acc + 9 * threadIdx.x;
-            const float a0 = a[0], a1 = a[1], a2 = a[2], a3 = a[3], a4 = a[4], a5 = a[5], a6 = a[6], a7 = a[7], a8 = a[8];
-            if ((a0 != 0.f) | (a1 != 0.f) | (a2 != 0.f) | (a3 != 0.f) | (a4 != 0.f) | (a5 != 0.f) | (a6 != 0.f) |
-                (a7 != 0.f) | (a8 != 0.f)) {
+            const float e0 = a[0], e1 = a[1], e2 = a[2], e3 = a[3], e4 = a[4], e5 = a[5], e6 = a[6], e7 = a[7], e8 = a[8];
+            if ((e0 != 0.f) | (e1 != 0.f) | (e2 != 0.f) | (e3 != 0.f) | (e4 != 0.f) | (e5 != 0.f) | (e6 != 0.f) |
+                (e7 != 0.f) | (e8 != 0.f)) {
                 float* gp = grad2d + 12 * (size_t)s.gidx[slot][threadIdx.x];
-                red_add_global_v4(gp, a0, a1, a2, a3);
-                red_add_global_v4(gp + 4, a4, a5, a6, a7);
-                red_add_global(gp + 8, a8);
+                red_add_global_v4(gp, e0, e1, e2, e3);
+                red_add_global_v4(gp + 4, e4, e5, e6, e7);
+                red_add_global(gp + 8, e8);
             }
         }
-        if (threadIdx.x == 0 && b >= 2) stage_expect<STAGING>(s, slot, kBatch);
+        if (threadIdx.x == 0 && b >= 2) stage_expect<STAGING>(s, slot, kB);
         __syncthreads();
     }
     // after a wait that gave up, bulk copies still in flight must land before the block exits
@@ -509,9 +545,9 @@ static void launch_bwd_mode(int staging, int tiles, const float4* rec, const uns
                             const KernelCamera& cam, unsigned n, const float* dl, const float* tf, const unsigned* nc,
                             float* g2, int thr, unsigned spin, unsigned* err, cudaStream_t st) {
     if (staging == GS_STAGE_LOADS)
-        k_render_bwd<MODE, GS_STAGE_LOADS><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
+        k_render_bwd<MODE, GS_STAGE_LOADS><<<tiles, kBwdBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
     else
-        k_render_bwd<MODE, GS_STAGE_BULK><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
+        k_render_bwd<MODE, GS_STAGE_BULK><<<tiles, kBwdBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
 }
 
 cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& proj, const unsigned* vals,

@@ -51,15 +51,17 @@ extern "C" {
 /* ---- backward accumulation modes (gs_options.bwd_mode) ------------------------------------
  * How gs_render_bwd accumulates the per-pixel gradient contributions of a Gaussian into its
  * per-Gaussian gradient. All modes compute the same sums (up to float rounding order).
- *   DIRECT    every contributing pixel (lane) adds its 9 values with its own global atomics:
- *             the L2-atomic-bound baseline that DISTWAR speeds up (DISTWAR, Abstract).
+ * A lane of the backward holds two pixels of its warp's 8x8 block; a lane contributes when
+ * either of its pixels does, and adds the sum of its pixels' values.
+ *   DIRECT    every contributing lane adds its 9 values with its own global atomics: the
+ *             L2-atomic-bound baseline that DISTWAR speeds up (DISTWAR, Abstract).
  *   WARP      the warp sums its lanes' contributions in registers (shuffle reduction) and one
  *             warp instruction issues the 9 global atomics (DISTWAR, Abstract: first key idea).
  *   ADAPTIVE  per warp and Gaussian: WARP when at least `adaptive_threshold` lanes contribute,
  *             DIRECT otherwise (DISTWAR, Abstract: second key idea; ARC, title).
  *   SM        warps add into a per-tile shared-memory accumulator (warp-reduced when at least
  *             `adaptive_threshold` lanes contribute, per lane otherwise); the tile issues one set
- *             of global atomics per Gaussian and 256-Gaussian batch.                            */
+ *             of global atomics per Gaussian and 128-Gaussian batch.                            */
 #define GS_BWD_DEFAULT  0
 #define GS_BWD_DIRECT   1
 #define GS_BWD_WARP     2
