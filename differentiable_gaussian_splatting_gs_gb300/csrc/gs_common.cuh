@@ -9,8 +9,6 @@
 namespace gs {
 
 constexpr int kTile = 16;          // tile side, pixels
-constexpr int kBlock = 256;        // threads per render block (one pixel each)
-constexpr int kBatch = 256;        // Gaussians staged per batch
 constexpr int kRecFloats = 12;     // floats per projected record (48 bytes)
 
 // Bits of the device error word (its address is passed to every kernel that can set it):

@@ -1,20 +1,18 @@
 // Rendering phase (forward alpha blending) and gradient computation phase (backward) of the tile
-// rasterizer: one block per 16x16-pixel tile, the tile's sorted list staged in shared memory in
-// batches of records (forward: 256 threads, one pixel each, 256-record batches; backward: 128
-// threads, two pixels each, 128-record batches).
+// rasterizer: one 128-thread block per 16x16-pixel tile, two pixels per thread, the tile's sorted
+// list staged in shared memory in batches of 128 records.
 //
 // The backward accumulates each Gaussian's gradient over all pixels with atomics; that
 // accumulation is the bottleneck that DISTWAR (Fast Differentiable Rendering on Raster-based
 // Rendering Pipelines, Abstract) and ARC (Warp-level Adaptive Atomic Reduction in GPUs to
 // Accelerate Differentiable Rendering, Abstract) identify, and the reason for the GS_BWD_* modes.
 //
-// Warp layout. Forward: warp w covers the 8x4 pixel block at (8 (w & 1), 4 (w >> 1)) of the tile;
-// lane l is pixel (l & 7, l >> 3) of that block. Backward: warp w covers the 8x8 block at
-// (8 (w & 1), 8 (w >> 1)); lane l holds pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4), so that
-// a Gaussian's record loads, warp reduction and atomics serve 64 pixels.
+// Warp layout: warp w covers the 8x8 pixel block at (8 (w & 1), 8 (w >> 1)) of the tile; lane l
+// holds pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4), so that a Gaussian's record loads and
+// culling test (and in the backward its warp reduction and atomics) serve 64 pixels.
 //
 // Warp-level culling. Before blending a batch, each warp keeps only the staged Gaussians whose
-// alpha can reach 1/255 somewhere in its 8x4 block: the set alpha >= 1/255 is the ellipse
+// alpha can reach 1/255 somewhere in its 8x8 block: the set alpha >= 1/255 is the ellipse
 // q(d) = A dx^2 + 2 B dx dy + C dy^2 <= L = 2 tau, tau = ln(255 opacity), and the test is whether
 // the minimum of q over the block's rectangle of pixel centres is <= L. q is convex, so for a fixed
 // dy its minimum over dx in [ax, bx] is at dx = clamp(-(B/A) dy, ax, bx); what remains is a convex
@@ -51,11 +49,11 @@ struct StageSmemT {
     uint64_t bar[2];
 };
 
-// Forward: 256 threads per tile, one pixel each; warp w covers the 8x4 block at (8 (w & 1), 4 (w >> 1)).
-using FwdStage = StageSmemT<kBatch, 8>;
-
-// Backward: 128 threads per tile, two pixels each; warp w covers the 8x8 block at
+// Both passes: 128 threads per tile, two pixels each; warp w covers the 8x8 block at
 // (8 (w & 1), 8 (w >> 1)), lane l the pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4) of it.
+constexpr int kFwdBlock = 128;
+constexpr int kFwdBatch = 128;
+using FwdStage = StageSmemT<kFwdBatch, 4>;
 constexpr int kBwdBlock = 128;
 constexpr int kBwdBatch = 128;
 using BwdStage = StageSmemT<kBwdBatch, 4>;
@@ -187,30 +185,51 @@ __device__ __forceinline__ int compact_warp(S& s, int n_in, int pos_limit, float
 
 // ---- forward ---------------------------------------------------------------------------------
 
+// Front-to-back blending of one record into one pixel; sets `done` when the pixel terminates.
+__device__ __forceinline__ void blend_pixel(float p2, const float4& r1, float cb, unsigned pos1, float& T, float& c0,
+                                            float& c1, float& c2, unsigned& last, bool& done) {
+    const float alpha = fminf(kAlphaMax, r1.y * ex2_approx(p2));
+    if (alpha >= kAlphaMin) {
+        const float test_T = T * (1.f - alpha);
+        if (test_T < kTMin) {
+            done = true;
+        } else {
+            const float w = alpha * T;
+            c0 = __fmaf_rn(r1.z, w, c0);
+            c1 = __fmaf_rn(r1.w, w, c1);
+            c2 = __fmaf_rn(cb, w, c2);
+            T = test_T;
+            last = pos1;
+        }
+    }
+}
+
 template <int STAGING>
-__global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
-                                                       const uint2* __restrict__ ranges, const KernelCamera cam,
-                                                       unsigned n_gauss, float* __restrict__ image,
-                                                       float* __restrict__ t_final, unsigned* __restrict__ n_contrib,
-                                                       unsigned spin_limit, unsigned* __restrict__ err) {
+__global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restrict__ rec,
+                                                          const unsigned* __restrict__ vals,
+                                                          const uint2* __restrict__ ranges, const KernelCamera cam,
+                                                          unsigned n_gauss, float* __restrict__ image,
+                                                          float* __restrict__ t_final, unsigned* __restrict__ n_contrib,
+                                                          unsigned spin_limit, unsigned* __restrict__ err) {
+    constexpr int kB = kFwdBatch;
     __shared__ FwdStage s;
     const int tile = blockIdx.x;
     const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 4 * (warp >> 1);
-    const int px = bx + (lane & 7), py = by + (lane >> 3);
-    const bool inside = px < cam.width && py < cam.height;
-    const float fpx = (float)px + 0.5f, fpy = (float)py + 0.5f;
-    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 3.f;
+    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 8 * (warp >> 1);
+    const int px = bx + (lane & 7), py0 = by + (lane >> 3), py1 = py0 + 4;
+    const bool in0 = px < cam.width && py0 < cam.height, in1 = px < cam.width && py1 < cam.height;
+    const float fpx = (float)px + 0.5f, fpy0 = (float)py0 + 0.5f, fpy1 = (float)py1 + 0.5f;
+    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 7.f;
 
     const uint2 rg = ranges[tile];
     const int start = (int)rg.x;
     const int count = (int)(rg.y > rg.x ? rg.y - rg.x : 0);
-    const int nb = (count + kBatch - 1) / kBatch;
+    const int nb = (count + kB - 1) / kB;
 
-    float T = 1.f, col0 = 0.f, col1 = 0.f, col2 = 0.f;
-    unsigned last = 0;
-    bool done = !inside;
+    float T0 = 1.f, c00 = 0.f, c01 = 0.f, c02 = 0.f, T1 = 1.f, c10 = 0.f, c11 = 0.f, c12 = 0.f;
+    unsigned last0 = 0, last1 = 0;
+    bool done0 = !in0, done1 = !in1;
     float4 pre[3];
 
     if (nb > 0) {
@@ -218,27 +237,27 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
             mbar_init(&s.bar[0], 1);
             mbar_init(&s.bar[1], 1);
             fence_mbar_init();
-            stage_expect<STAGING>(s, 0, min(kBatch, count));
-            if (nb > 1) stage_expect<STAGING>(s, 1, min(kBatch, count - kBatch));
+            stage_expect<STAGING>(s, 0, min(kB, count));
+            if (nb > 1) stage_expect<STAGING>(s, 1, min(kB, count - kB));
         }
         __syncthreads();
-        stage_issue<STAGING>(s, 0, rec, vals, start, min(kBatch, count), n_gauss, pre, err);
+        stage_issue<STAGING>(s, 0, rec, vals, start, min(kB, count), n_gauss, pre, err);
     }
     bool ok = true;
     int issued = nb > 0 ? 0 : -1, consumed = -1;  // batches whose copies were issued / waited for
     for (int b = 0; b < nb; ++b) {
         const int slot = b & 1;
-        const int n_in = min(kBatch, count - b * kBatch);
+        const int n_in = min(kB, count - b * kB);
         float4 nxt[3];
         if (STAGING == GS_STAGE_LOADS) {
             // the loads of this batch were issued one iteration earlier (or above)
             ok = stage_wait<STAGING>(s, slot, 0, n_in, pre, spin_limit, err);
-            if (b + 1 < nb) stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b + 1) * kBatch,
-                                                 min(kBatch, count - (b + 1) * kBatch), n_gauss, nxt, err);
+            if (b + 1 < nb) stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b + 1) * kB,
+                                                 min(kB, count - (b + 1) * kB), n_gauss, nxt, err);
         } else {
             if (b + 1 < nb) {
-                stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b + 1) * kBatch,
-                                     min(kBatch, count - (b + 1) * kBatch), n_gauss, nxt, err);
+                stage_issue<STAGING>(s, slot ^ 1, rec, vals, start + (b + 1) * kB, min(kB, count - (b + 1) * kB),
+                                     n_gauss, nxt, err);
                 issued = b + 1;
             }
             ok = stage_wait<STAGING>(s, slot, (unsigned)(b >> 1) & 1u, n_in, pre, spin_limit, err);
@@ -248,53 +267,52 @@ __global__ void __launch_bounds__(kBlock) k_render_fwd(const float4* __restrict_
             s.cull[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
                                                  s.rec[slot][threadIdx.x][2], s.cull2[threadIdx.x]);
         if (__syncthreads_or(!ok)) break;
-        const int nl = compact_warp(s, n_in, kBatch, wx0, wx1, wy0, wy1, warp, lane);
+        const int nl = compact_warp(s, n_in, kB, wx0, wx1, wy0, wy1, warp, lane);
         for (int k = 0; k < nl; ++k) {
-            if (__all_sync(0xffffffffu, done)) break;
+            if (__all_sync(0xffffffffu, done0 && done1)) break;
             const int j = s.list[warp][k];
-            if (!done) {
-                const float2 r0 = *reinterpret_cast<const float2*>(&s.rec[slot][j][0]);  // mean
-                const float4 r1 = s.rec[slot][j][1];                                     // (D, o, r, g)
-                const float4 r2 = s.rec[slot][j][2];                                     // (b, r, A', D')
-                const float dx = r0.x - fpx, dy = r0.y - fpy;
+            const float2 r0 = *reinterpret_cast<const float2*>(&s.rec[slot][j][0]);  // mean
+            const float4 r1 = s.rec[slot][j][1];                                     // (D, o, r, g)
+            const float4 r2 = s.rec[slot][j][2];                                     // (b, r, A', D')
+            const unsigned pos1 = (unsigned)(b * kB + j + 1);
+            const float dx = r0.x - fpx;
+            if (!done0) {
+                const float dy = r0.y - fpy0;
                 const float u = __fmaf_rn(r2.y, dy, dx);
-                const float p2 = __fmaf_rn(r2.z * u, u, r2.w * dy * dy);  // power log2(e) <= 0
-                {
-                    const float alpha = fminf(kAlphaMax, r1.y * ex2_approx(p2));
-                    if (alpha >= kAlphaMin) {
-                        const float test_T = T * (1.f - alpha);
-                        if (test_T < kTMin) {
-                            done = true;
-                        } else {
-                            const float w = alpha * T;
-                            const float cb = r2.x;
-                            col0 += r1.z * w;
-                            col1 += r1.w * w;
-                            col2 += cb * w;
-                            T = test_T;
-                            last = (unsigned)(b * kBatch + j + 1);
-                        }
-                    }
-                }
+                blend_pixel(__fmaf_rn(r2.z * u, u, r2.w * dy * dy), r1, r2.x, pos1, T0, c00, c01, c02, last0, done0);
+            }
+            if (!done1) {
+                const float dy = r0.y - fpy1;
+                const float u = __fmaf_rn(r2.y, dy, dx);
+                blend_pixel(__fmaf_rn(r2.z * u, u, r2.w * dy * dy), r1, r2.x, pos1, T1, c10, c11, c12, last1, done1);
             }
         }
         if (STAGING == GS_STAGE_LOADS) {
             pre[0] = nxt[0]; pre[1] = nxt[1]; pre[2] = nxt[2];
         }
-        if (threadIdx.x == 0 && b + 2 < nb) stage_expect<STAGING>(s, slot, min(kBatch, count - (b + 2) * kBatch));
-        if (__syncthreads_count(!done) == 0) break;
+        if (threadIdx.x == 0 && b + 2 < nb) stage_expect<STAGING>(s, slot, min(kB, count - (b + 2) * kB));
+        if (__syncthreads_count(!(done0 && done1)) == 0) break;
     }
     // bulk copies issued but not waited for (early termination or a wait that gave up) must land
     // before the block exits
     if (STAGING == GS_STAGE_BULK)
         for (int k = consumed + 1; k <= issued; ++k) mbar_wait_bounded(&s.bar[k & 1], (unsigned)(k >> 1) & 1u, kDrainLimit, err);
-    if (inside) {
-        const size_t pix = (size_t)py * cam.width + px, plane = (size_t)cam.width * cam.height;
-        image[pix] = col0 + T * cam.bg[0];
-        image[plane + pix] = col1 + T * cam.bg[1];
-        image[2 * plane + pix] = col2 + T * cam.bg[2];
-        t_final[pix] = T;
-        n_contrib[pix] = last;
+    const size_t plane = (size_t)cam.width * cam.height;
+    if (in0) {
+        const size_t pix = (size_t)py0 * cam.width + px;
+        image[pix] = c00 + T0 * cam.bg[0];
+        image[plane + pix] = c01 + T0 * cam.bg[1];
+        image[2 * plane + pix] = c02 + T0 * cam.bg[2];
+        t_final[pix] = T0;
+        n_contrib[pix] = last0;
+    }
+    if (in1) {
+        const size_t pix = (size_t)py1 * cam.width + px;
+        image[pix] = c10 + T1 * cam.bg[0];
+        image[plane + pix] = c11 + T1 * cam.bg[1];
+        image[2 * plane + pix] = c12 + T1 * cam.bg[2];
+        t_final[pix] = T1;
+        n_contrib[pix] = last1;
     }
 }
 
@@ -534,9 +552,9 @@ cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* 
     const uint2* rg = reinterpret_cast<const uint2*>(ranges);
     count_launches(1);
     if (staging == GS_STAGE_LOADS)
-        k_render_fwd<GS_STAGE_LOADS><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
+        k_render_fwd<GS_STAGE_LOADS><<<tiles, kFwdBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
     else
-        k_render_fwd<GS_STAGE_BULK><<<tiles, kBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
+        k_render_fwd<GS_STAGE_BULK><<<tiles, kFwdBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
     return cudaGetLastError();
 }
 
