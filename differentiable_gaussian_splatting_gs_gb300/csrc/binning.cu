@@ -222,6 +222,199 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
     }
 }
 
+// ---- depth sort: one histogram pass, then one kernel per 8-bit digit (decoupled look-back) -----
+//
+// k_depth_hist4 counts the four 8-bit digits of the depth keys of all Gaussians with radius > 0
+// in one pass. Each k_onesweep pass then ranks its 2048-item block locally (as k_radix_scatter),
+// publishes the block's per-digit counts, and finds the number of items of each digit in all
+// earlier blocks by looking back over their published words: a block's inclusive prefix ends the
+// walk, an aggregate is added and the walk continues. Blocks take their index from a ticket in
+// start order, so every block it waits for has started and publishes its aggregate before it
+// waits itself; each wait is bounded (spin_limit polls, then the timeout bit and a zero count).
+constexpr unsigned long long kStatAgg = 1ull << 62, kStatIncl = 2ull << 62, kStatVal = (1ull << 62) - 1ull;
+
+__global__ void __launch_bounds__(256) k_depth_hist4(const unsigned* __restrict__ keys, int n,
+                                                     const int* __restrict__ radius, unsigned* __restrict__ ghist) {
+    __shared__ unsigned h[4][256];
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) (&h[0][0])[i] = 0u;
+    __syncthreads();
+    const int stride = gridDim.x * blockDim.x;
+    constexpr int kAhead = 4;  // rounds whose loads are issued together
+    for (int base = blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < n; base += kAhead * stride) {
+        unsigned kk[kAhead];
+        bool vv[kAhead];
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+            const int i = base + a * stride + lane;
+            vv[a] = i < n && radius[i] > 0;
+            kk[a] = i < n ? keys[i] : 0u;
+        }
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const unsigned d = vv[a] ? (kk[a] >> (8 * p)) & 0xffu : 0x100u;
+                const unsigned peers = __match_any_sync(full, d);
+                if (vv[a] && (peers & lanemask_lt()) == 0u) atomicAdd(&h[p][d], (unsigned)__popc(peers));
+            }
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x)
+        if ((&h[0][0])[i]) atomicAdd(&ghist[i], (&h[0][0])[i]);
+}
+
+// One stable pass of the depth sort over the digit at `shift`. IOTA: the values are the item
+// indices and items with radius 0 are dropped (first pass); later passes take the count of valid
+// items from n_dev (the sum of the digit-0 histogram).
+template <bool IOTA>
+__global__ void __launch_bounds__(kSortThreads) k_onesweep(
+    const unsigned* __restrict__ keys_in, const unsigned* __restrict__ vals_in, unsigned* __restrict__ keys_out,
+    unsigned* __restrict__ vals_out, int n_bound, const unsigned* __restrict__ ghist4, const int* __restrict__ radius,
+    int pass, unsigned* __restrict__ ticket, unsigned long long* __restrict__ status, unsigned* __restrict__ nvis_out,
+    unsigned spin_limit, unsigned* __restrict__ err) {
+    __shared__ unsigned woff[8][256];      // per-warp digit counts, then block-local offsets
+    __shared__ unsigned lbase[256];        // block-local start of each digit
+    __shared__ unsigned gbase[256];        // global start of this block's run of each digit
+    __shared__ unsigned wsum[8];
+    __shared__ unsigned s_nvalid, s_block, s_n;
+    __shared__ unsigned sk[kSortItems], sv[kSortItems];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int shift = 8 * pass;
+    const unsigned* ghist = ghist4 + 256 * pass;
+    if (threadIdx.x == 0) {
+        s_block = atomicAdd(ticket, 1u);
+        s_n = 0u;
+    }
+    __syncthreads();
+    if (!IOTA) {  // number of valid items: the total of the digit histogram
+        const unsigned t = __reduce_add_sync(0xffffffffu, ghist4[threadIdx.x]);
+        if (lane == 0) atomicAdd(&s_n, t);
+        __syncthreads();
+    }
+    const int block = (int)s_block;
+    if (!IOTA && nvis_out && block == 0 && threadIdx.x == 0) *nvis_out = s_n;
+    const int n = IOTA ? n_bound : min(n_bound, (int)s_n);
+    // blocks past the last item: no later block holds items, so none looks back this far
+    if (block > 0 && block * kSortItems >= n) return;
+    const int base = block * kSortItems + warp * kWarpItems + lane;
+    unsigned k[kSortRounds], v[kSortRounds], dg[kSortRounds];
+#pragma unroll
+    for (int r = 0; r < kSortRounds; ++r) {
+        const int idx = base + r * 32;
+        const bool valid = item_valid(idx, n, IOTA ? radius : nullptr);
+        k[r] = valid ? keys_in[idx] : 0u;
+        v[r] = IOTA ? (unsigned)idx : (valid ? vals_in[idx] : 0u);
+        dg[r] = valid ? (k[r] >> shift) & 0xffu : 0x100u;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) woff[warp][lane + 32 * i] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kSortRounds; ++r) {
+        const unsigned d = dg[r];
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (d != 0x100u && (peers & lanemask_lt()) == 0u) woff[warp][d] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    {
+        const int d = threadIdx.x;  // digit d = thread
+        unsigned c = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const unsigned t = woff[w][d];
+            woff[w][d] = c;
+            c += t;
+        }
+        // publish the block's count of digit d, then look back for the earlier blocks' total
+        unsigned long long* my = status + (size_t)block * 256 + d;
+        if (block == 0) {
+            *(volatile unsigned long long*)my = kStatIncl | c;
+        } else {
+            *(volatile unsigned long long*)my = kStatAgg | c;
+        }
+        unsigned long long before = 0;
+        if (block > 0) {
+            int j = block - 1;
+            unsigned polls = 0;
+            while (true) {
+                const unsigned long long sw = *(volatile const unsigned long long*)(status + (size_t)j * 256 + d);
+                if (sw & kStatIncl) {
+                    before += sw & kStatVal;
+                    break;
+                }
+                if (sw & kStatAgg) {
+                    before += sw & kStatVal;
+                    if (--j < 0) break;  // not reached: block 0 publishes its inclusive count at once
+                    continue;
+                }
+                if (++polls >= spin_limit) {
+                    atomicOr(err, kErrTimeout);
+                    break;
+                }
+            }
+            *(volatile unsigned long long*)my = kStatIncl | (before + c);
+        }
+        // block-local exclusive scan over digits
+        unsigned x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        // global digit start: exclusive scan of the pass histogram
+        const unsigned tv = ghist[d];
+        unsigned tx = tv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, tx, o);
+            if (lane >= o) tx += y;
+        }
+        __syncthreads();
+        unsigned pre = 0;
+        for (int w = 0; w < warp; ++w) pre += wsum[w];
+        const unsigned lb = pre + x - c;
+        lbase[d] = lb;
+        if (d == 255) s_nvalid = lb + c;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) woff[w][d] += lb;
+        __syncthreads();
+        if (lane == 31) wsum[warp] = tx;
+        __syncthreads();
+        unsigned tpre = 0;
+        for (int w = 0; w < warp; ++w) tpre += wsum[w];
+        gbase[d] = tpre + tx - tv + (unsigned)before;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kSortRounds; ++r) {
+        const unsigned d = dg[r];
+        const bool valid = d != 0x100u;
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (valid) {
+            const unsigned lp = woff[warp][d] + __popc(peers & lanemask_lt());
+            sk[lp] = k[r];
+            sv[lp] = v[r];
+        }
+        __syncwarp();
+        if (valid && (peers & lanemask_lt()) == 0u) woff[warp][d] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    const int n_block = (int)s_nvalid;
+    for (int i = threadIdx.x; i < n_block; i += kSortThreads) {
+        const unsigned key = sk[i], val = sv[i];
+        const unsigned d = (key >> shift) & 0xffu;
+        const unsigned pos = gbase[d] + (unsigned)i - lbase[d];
+        keys_out[pos] = key;
+        vals_out[pos] = val;
+    }
+}
+
 // Block sums (256 Gaussians per block, in depth order) of the number of tiles of each rectangle.
 // With `crect`, also the packed rectangle of every depth-ordered Gaussian,
 // crect[i] = (x0 | y0 << 16, w | h << 16), w = h = 0 when empty (tile ids below 2^16).
@@ -616,8 +809,10 @@ __global__ void k_write_ranges(int T, const unsigned* __restrict__ tile_start, c
 // inside each of the band's tiles into shared memory, then walks the chunk's Gaussians in depth
 // order; for each one whose rectangle meets the band, its lanes cover the rectangle's tiles inside
 // the band (distinct tiles, so no two lanes share an offset) and append the Gaussian there. Entries
-// therefore land in depth order within every tile; bands own disjoint tiles. Chunks end after
-// about 16k entries, so a warp never walks more than a bounded amount of work.
+// therefore land in depth order within every tile; bands own disjoint tiles. Two consecutive
+// Gaussians whose rectangles in the band are disjoint and small (at most 16 tiles each) are placed
+// in the same step, one per half-warp: they share no tile, so their order does not matter. Chunks
+// end after about 16k entries, so a warp never walks more than a bounded amount of work.
 constexpr int kPlaceWarps = 8;        // warps per block when shared memory allows
 constexpr int kPlaceBands = 8;        // bands per chunk (whole tile rows)
 
@@ -667,16 +862,32 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
         const unsigned xw = (pr.x & 0xffffu) | (w << 16);
         const unsigned yab = (unsigned)ya | ((unsigned)max(yb, 0) << 16);
         const unsigned m = div_magic(w);
-        unsigned hit = __ballot_sync(full, w > 0u && ya < yb);
+        const unsigned area_l = (w > 0u && ya < yb) ? w * (unsigned)(yb - ya) : 0u;
+        unsigned hit = __ballot_sync(full, area_l > 0u);
         while (hit) {
-            const int j = __ffs(hit) - 1;
+            // the next Gaussian, and the one after it when both cover at most 16 tiles of the band
+            // and their rectangles are disjoint: then each half-warp places one of them
+            const int j1 = __ffs(hit) - 1;
             hit &= hit - 1u;
-            const unsigned jg = __shfl_sync(full, g, j), jxw = __shfl_sync(full, xw, j);
-            const unsigned jyab = __shfl_sync(full, yab, j), jm = __shfl_sync(full, m, j);
+            const int j2 = hit ? __ffs(hit) - 1 : j1;
+            const unsigned xw1 = __shfl_sync(full, xw, j1), yab1 = __shfl_sync(full, yab, j1);
+            const unsigned xw2 = __shfl_sync(full, xw, j2), yab2 = __shfl_sync(full, yab, j2);
+            const unsigned a1 = (xw1 >> 16) * ((yab1 >> 16) - (yab1 & 0xffffu));
+            const unsigned a2 = (xw2 >> 16) * ((yab2 >> 16) - (yab2 & 0xffffu));
+            const unsigned x1 = xw1 & 0xffffu, x2 = xw2 & 0xffffu;
+            const bool apart = x1 + (xw1 >> 16) <= x2 || x2 + (xw2 >> 16) <= x1 ||
+                               (yab1 >> 16) <= (yab2 & 0xffffu) || (yab2 >> 16) <= (yab1 & 0xffffu);
+            const bool pair = j2 != j1 && a1 <= 16u && a2 <= 16u && apart;
+            if (pair) hit &= hit - 1u;
+            const bool second = pair && lane >= 16;
+            const int j = second ? j2 : j1;
+            const unsigned jg = __shfl_sync(full, g, j), jm = __shfl_sync(full, m, j);
+            const unsigned jxw = second ? xw2 : xw1, jyab = second ? yab2 : yab1;
             const unsigned jw = jxw >> 16, jya = jyab & 0xffffu;
-            const unsigned area = jw * ((jyab >> 16) - jya);
+            const unsigned area = second ? a2 : a1;
             const unsigned tl0 = jya * (unsigned)tiles_x + (jxw & 0xffffu);
-            for (unsigned k = lane; k < area; k += 32u) {
+            const unsigned step = pair ? 16u : 32u;
+            for (unsigned k = pair ? (lane & 15u) : lane; k < area; k += step) {
                 const unsigned rk = div_by(k, jw, jm);
                 const unsigned tl = tl0 + rk * (unsigned)tiles_x + (k - rk * jw);  // band-local tile
                 const unsigned pos = off[tl];
@@ -723,6 +934,10 @@ SortWorkspace carve_workspace(void* base, long long n, long long cap, long long 
     w.totals = (unsigned*)take(256 * 4);
     w.total = (unsigned long long*)take(8);
     w.nvis = (unsigned*)take(4);
+    // depth sort: 4 digit histograms, 4 tickets, 4 x (blocks x 256) look-back words, one region
+    w.sweep_blocks = sort_blocks(nn);
+    w.sweep_bytes = 4 * 256 * 4 + 256 + (size_t)4 * w.sweep_blocks * 256 * 8;
+    w.sweep = (unsigned char*)take(w.sweep_bytes);
     const long long gblocks = (nn + 255) / 256;
     w.bsum = (unsigned long long*)take(8 * gblocks);
     w.boff = (unsigned long long*)take(8 * gblocks);
@@ -766,24 +981,34 @@ static cudaError_t radix_pass(const unsigned* kin, const unsigned* vin, unsigned
     return cudaGetLastError();
 }
 
-// Phase 1: depth sort of the visible Gaussians (the first pass drops radius-0 Gaussians and
-// leaves their number V on the device; later passes and the count run over V items) and the
-// duplicate count; leaves the total D in w.total (device).
-cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, cudaStream_t st) {
+// Phase 1: depth sort of the visible Gaussians (the first pass drops radius-0 Gaussians; the
+// second leaves their number V on the device, and the count runs over V items) and the duplicate
+// count; leaves the total D in w.total (device). Bounded look-back waits set the timeout bit of
+// `err` when they give up.
+cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, unsigned* err,
+                      unsigned spin_limit, cudaStream_t st) {
     const int n = (int)proj.n;
     if (n == 0) return cudaMemsetAsync(w.total, 0, 8, st);
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     cudaError_t e;
-    if ((e = cudaMemsetAsync(w.nvis, 0, 4, st))) return e;
-    if ((e = radix_pass(depth_bits, nullptr, w.dkA, w.dvA, n, nullptr, proj.radius, w.nvis, 0, 8, true, nullptr,
-                        nullptr, w, st)))
-        return e;
-    if ((e = radix_pass(w.dkA, w.dvA, w.dkB, w.dvB, n, w.nvis, nullptr, nullptr, 8, 8, false, nullptr, nullptr, w, st)))
-        return e;
-    if ((e = radix_pass(w.dkB, w.dvB, w.dkA, w.dvA, n, w.nvis, nullptr, nullptr, 16, 8, false, nullptr, nullptr, w, st)))
-        return e;
-    if ((e = radix_pass(w.dkA, w.dvA, w.dkB, w.dvB, n, w.nvis, nullptr, nullptr, 24, 8, false, nullptr, nullptr, w, st)))
-        return e;
+    if ((e = cudaMemsetAsync(w.sweep, 0, w.sweep_bytes, st))) return e;
+    unsigned* ghist4 = reinterpret_cast<unsigned*>(w.sweep);
+    unsigned* tickets = ghist4 + 4 * 256;
+    unsigned long long* status = reinterpret_cast<unsigned long long*>(w.sweep + 4 * 256 * 4 + 256);
+    const size_t sstride = (size_t)w.sweep_blocks * 256;
+    const int nb = sort_blocks(n);
+    const int hblocks = nb < 4 * 152 ? nb : 4 * 152;
+    count_launches(5);
+    k_depth_hist4<<<hblocks, 256, 0, st>>>(depth_bits, n, proj.radius, ghist4);
+    k_onesweep<true><<<nb, kSortThreads, 0, st>>>(depth_bits, nullptr, w.dkA, w.dvA, n, ghist4, proj.radius, 0,
+                                                  tickets, status, nullptr, spin_limit, err);
+    k_onesweep<false><<<nb, kSortThreads, 0, st>>>(w.dkA, w.dvA, w.dkB, w.dvB, n, ghist4, nullptr, 1, tickets + 1,
+                                                   status + sstride, w.nvis, spin_limit, err);
+    k_onesweep<false><<<nb, kSortThreads, 0, st>>>(w.dkB, w.dvB, w.dkA, w.dvA, n, ghist4, nullptr, 2, tickets + 2,
+                                                   status + 2 * sstride, nullptr, spin_limit, err);
+    k_onesweep<false><<<nb, kSortThreads, 0, st>>>(w.dkA, w.dvA, w.dkB, w.dvB, n, ghist4, nullptr, 3, tickets + 3,
+                                                   status + 3 * sstride, nullptr, spin_limit, err);
+    if ((e = cudaGetLastError())) return e;
     const float4* rec = reinterpret_cast<const float4*>(proj.rec);
     const int T = tiles_x * tiles_y;
     const int gblocks = (n + 255) / 256;

@@ -254,7 +254,7 @@ int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options*
     unsigned* err = error_word(&s);
     if (!err) return s;
     cudaStream_t st = as_stream(stream);
-    cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, st);
+    cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, err, o.spin, st);
     if (e) return cuda_fail(e, "gs_bin_and_sort: count");
     unsigned long long d = 0;
     if ((e = cudaMemcpyAsync(&d, w.total, 8, cudaMemcpyDeviceToHost, st))) return cuda_fail(e, "gs_bin_and_sort: read D");
@@ -292,7 +292,7 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
     unsigned* err = error_word(&s);
     if (!err) return s;
     cudaStream_t st = as_stream(stream);
-    cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, st);
+    cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, err, o.spin, st);
     if (e) return cuda_fail(e, "gs_bin_and_sort_static: count");
     unsigned long long d = 0;
     if ((e = cudaMemcpyAsync(&d, w.total, 8, cudaMemcpyDeviceToHost, st)))

@@ -18,7 +18,10 @@ struct SortWorkspace {
     unsigned *dkA, *dkB, *dvA, *dvB;   // depth-sort keys / values, ping-pong, N each
     unsigned *hist, *totals;           // radix histograms [256][blocks] and digit totals [256]
     unsigned long long *bsum, *boff, *total;  // duplicate counts per 256 Gaussians, offsets, total D
-    unsigned* nvis;                    // number of Gaussians with radius > 0 (left by the first depth pass)
+    unsigned* nvis;                    // number of Gaussians with radius > 0 (left by the second depth pass)
+    unsigned char* sweep;              // depth sort: digit histograms, tickets, look-back words (zeroed per call)
+    size_t sweep_bytes;
+    int sweep_blocks;                  // 2048-item blocks of a depth pass
     unsigned *tA, *tB, *vB;            // radix tile pass: keys ping-pong and values, capacity each
     unsigned* table;                   // counting tile pass: chunk x tile counts, then offsets
     uint2* crect;                      // counting tile pass: packed tile rectangle per depth-ordered Gaussian
@@ -31,7 +34,8 @@ struct SortWorkspace {
 
 // Workspace layout for n Gaussians, at most `cap` duplicates and `tiles` tiles.
 SortWorkspace carve_workspace(void* base, long long n, long long cap, long long tiles);
-cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, cudaStream_t st);
+cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, unsigned* err,
+                      unsigned spin_limit, cudaStream_t st);
 cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
                           cudaStream_t st);
