@@ -55,6 +55,7 @@ def parse_args():
     ap.add_argument("--staging", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip timing the update phase after the step")
     return ap.parse_args()
 
 
@@ -76,13 +77,19 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            self._wait_samples(1)  # a sample right before the timed region
         except OSError:
             self.proc = None
         return self
+
+    def _wait_samples(self, k: int, timeout: float = 3.0):
+        t0 = time.time()
+        while len(self.lines) < k and time.time() - t0 < timeout and self.proc.poll() is None:
+            time.sleep(0.005)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -90,6 +97,7 @@ class ClockSampler:
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            self._wait_samples(len(self.lines) + 1)  # and one right after it
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -324,6 +332,73 @@ def run_ours(args, rank, world, local_rank):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
     assert api.gs_device_error() == 0
 
+    # ---- the update phase after the step (not part of the fwd+bwd metric): sparse Adam over the
+    # Gaussians the view made visible, timed alone with L2 flushed before each launch
+    extras = {}
+    if not args.no_extras:
+        exp_avg = {k: torch.zeros_like(params[k]) for k in names}
+        exp_avg_sq = {k: torch.zeros_like(params[k]) for k in names}
+        radius = bufs.proj.radius
+        n_vis = int((radius > 0).sum().item())
+        floats = sum(params[k][0].numel() for k in names)
+        a_ms = []
+        for t in range(1, 4 + max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            api.gs_adam_step(params, grads, exp_avg, exp_avg_sq, radius,
+                             api.make_adam_options(gs_scenes.ADAM_LR, t, scene.sh_degree))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if t > 3:
+                a_ms.append(e0.elapsed_time(e1))
+        am = sum(a_ms) / len(a_ms)
+        a_bytes = n_vis * floats * 4 * 7 + scene.n * 4  # p, m, v read + written, g read; radius
+        peaks = load_json(PEAKS_PATH) or {}
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
+        extras["sparse_adam"] = {"ms": am, "visible": n_vis, "algorithmic_bytes": a_bytes,
+                                 "achieved_gbs": a_bytes / (am / 1e3) / 1e9,
+                                 "frac_of_measured_hbm": a_bytes / (am / 1e3) / 1e9 / hbm}
+        # post-backward statistics: densification accumulators and per-Gaussian gradient magnitudes
+        acc = torch.zeros(scene.n, device=dev)
+        cnt = torch.zeros(scene.n, dtype=torch.int32, device=dev)
+        mrad = torch.zeros(scene.n, dtype=torch.int32, device=dev)
+        gmag = torch.empty(scene.n, device=dev)
+        s_ms = []
+        for it in range(4 + max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            api.gs_densify_stats(bufs.proj, bufs.grad2d, cam.width, cam.height, acc, cnt, mrad,
+                                 param_grads=grads, grad_mag=gmag, sh_degree=scene.sh_degree)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it > 3:
+                s_ms.append(e0.elapsed_time(e1))
+        sm_ = sum(s_ms) / len(s_ms)
+        s_bytes = scene.n * 8 + n_vis * (32 + 12 + floats * 4)  # radius + magnitude; grad2d sector, stats, grads
+        extras["densify_stats"] = {"ms": sm_, "algorithmic_bytes": s_bytes, "achieved_gbs": s_bytes / (sm_ / 1e3) / 1e9,
+                                   "frac_of_measured_hbm": s_bytes / (sm_ / 1e3) / 1e9 / hbm}
+        # image loss L1 + D-SSIM and dL/dimage of the rendered view
+        image = bufs.image_buffers(cam.width, cam.height)[0]
+        lws = torch.empty(int(lib.gs_loss_workspace_bytes(cam.width, cam.height)), dtype=torch.uint8, device=dev)
+        lout = (torch.empty(1, device=dev), torch.empty_like(image))
+        l_ms = []
+        for it in range(4 + max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            api.gs_loss_l1_dssim(image, target, 0.2, workspace=lws, out=lout)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it > 3:
+                l_ms.append(e0.elapsed_time(e1))
+        lm = sum(l_ms) / len(l_ms)
+        l_bytes = P * 3 * 4 * (2 + 3 + 3 + 2 + 1)  # pass 1: x, y in, 3 maps out; pass 2: 3 maps, x, y in, dL out
+        extras["loss_l1_dssim"] = {"ms": lm, "algorithmic_bytes": l_bytes, "achieved_gbs": l_bytes / (lm / 1e3) / 1e9,
+                                   "frac_of_measured_hbm": l_bytes / (lm / 1e3) / 1e9 / hbm}
+        assert api.gs_device_error() == 0
+
     # ---- roofline of the dominant kernel (the backward)
     peaks = load_json(PEAKS_PATH) or {}
     counts = json_block(COUNTS_PATH) or {}
@@ -354,7 +429,7 @@ def run_ours(args, rank, world, local_rank):
                        "l2": "flushed between timed steps (256 MB write, outside the events)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
-            "bwd_ms": bwd_avg_ms, "step_ms_min": min(step_ms)}
+            "bwd_ms": bwd_avg_ms, "step_ms_min": min(step_ms), "extras": extras}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pix, dt, desc, cores = oracle_sample(scene, 0.5, 0.5)
         line["cpu_baseline"] = {"value": pix / dt / 1e6, "unit": "Mpix/s", "cores": cores, "kind": "oracle",

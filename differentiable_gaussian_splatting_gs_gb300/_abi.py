@@ -28,7 +28,8 @@ BWD_MODES = {"direct": GS_BWD_DIRECT, "warp": GS_BWD_WARP, "adaptive": GS_BWD_AD
 # every symbol include/gs.h declares
 EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd",
            "gs_preprocess_bwd", "gs_status_string", "gs_last_error_message", "gs_device_error",
-           "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static")
+           "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static", "gs_adam_step",
+           "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim")
 GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
 
 
@@ -52,6 +53,18 @@ class gs_params(C.Structure):
 class gs_proj(C.Structure):
     _fields_ = [("rec", C.c_void_p), ("depth", C.c_void_p), ("radius", C.c_void_p),
                 ("tiles_touched", C.c_void_p), ("n", C.c_int64)]
+
+
+class gs_tensors(C.Structure):
+    _fields_ = [("mean3d", C.c_void_p), ("log_scale", C.c_void_p), ("quat", C.c_void_p),
+                ("opacity_logit", C.c_void_p), ("sh", C.c_void_p), ("n", C.c_int64)]
+
+
+class gs_adam_options(C.Structure):
+    _fields_ = [("lr_mean3d", C.c_float), ("lr_log_scale", C.c_float), ("lr_quat", C.c_float),
+                ("lr_opacity", C.c_float), ("lr_sh_dc", C.c_float), ("lr_sh_rest", C.c_float),
+                ("beta1", C.c_float), ("beta2", C.c_float), ("eps", C.c_float), ("step", C.c_int32),
+                ("sh_degree", C.c_int32)]
 
 
 class GsError(RuntimeError):
@@ -95,6 +108,15 @@ def load():
         lib.gs_bin_and_sort_static.restype = C.c_int
         lib.gs_kernel_launches.argtypes = []
         lib.gs_kernel_launches.restype = C.c_int64
+        pten = C.POINTER(gs_tensors)
+        lib.gs_adam_step.argtypes = [pten, pten, pten, pten, P, C.POINTER(gs_adam_options), P]
+        lib.gs_adam_step.restype = C.c_int
+        lib.gs_densify_stats.argtypes = [pproj, P, I32, I32, I32, P, P, P, pten, P, I32, P]
+        lib.gs_densify_stats.restype = C.c_int
+        lib.gs_loss_workspace_bytes.argtypes = [I32, I32]
+        lib.gs_loss_workspace_bytes.restype = C.c_size_t
+        lib.gs_loss_l1_dssim.argtypes = [P, P, I32, I32, C.c_float, P, C.c_size_t, P, P, P]
+        lib.gs_loss_l1_dssim.restype = C.c_int
         for name in ("gs_preprocess", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd",
                      "gs_preprocess_bwd", "gs_device_error", "gs_version", "gs_selftest_timeout"):
             getattr(lib, name).restype = C.c_int

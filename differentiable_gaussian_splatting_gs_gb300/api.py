@@ -248,6 +248,60 @@ def gs_preprocess_bwd(params: dict, cam, opt: gs_options, proj: Proj, grad2d, ou
     return out
 
 
+PARAM_NAMES = ("mean3d", "log_scale", "quat", "opacity_logit", "sh")
+
+
+def _tensors(d: dict) -> _abi.gs_tensors:
+    for k in PARAM_NAMES:
+        t = d[k]
+        if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("Adam tensors must be contiguous float32 CUDA tensors")
+    return _abi.gs_tensors(mean3d=_ptr(d["mean3d"]), log_scale=_ptr(d["log_scale"]), quat=_ptr(d["quat"]),
+                           opacity_logit=_ptr(d["opacity_logit"]), sh=_ptr(d["sh"]), n=int(d["mean3d"].shape[0]))
+
+
+def make_adam_options(lr: dict, step: int, sh_degree: int, beta1: float = 0.0, beta2: float = 0.0,
+                      eps: float = 0.0) -> _abi.gs_adam_options:
+    """lr: learning rates keyed mean3d, log_scale, quat, opacity, sh_dc, sh_rest."""
+    return _abi.gs_adam_options(lr_mean3d=lr["mean3d"], lr_log_scale=lr["log_scale"], lr_quat=lr["quat"],
+                                lr_opacity=lr["opacity"], lr_sh_dc=lr["sh_dc"], lr_sh_rest=lr["sh_rest"],
+                                beta1=beta1, beta2=beta2, eps=eps, step=int(step), sh_degree=int(sh_degree))
+
+
+def gs_adam_step(params: dict, grads: dict, exp_avg: dict, exp_avg_sq: dict, radius, opt: _abi.gs_adam_options,
+                 stream=None) -> None:
+    """Sparse Adam step in place on params / exp_avg / exp_avg_sq for the Gaussians with radius > 0."""
+    P, G, M, V = _tensors(params), _tensors(grads), _tensors(exp_avg), _tensors(exp_avg_sq)
+    check(_abi.load().gs_adam_step(C.byref(P), C.byref(G), C.byref(M), C.byref(V), _ptr(radius), C.byref(opt),
+                                   _stream(stream)), "gs_adam_step")
+
+
+def gs_densify_stats(proj: Proj, grad2d, width: int, height: int, grad_norm_accum, view_count, max_radius,
+                     ndc: bool = False, param_grads: dict | None = None, grad_mag=None, sh_degree: int = 3,
+                     stream=None) -> None:
+    """Adds one view's densification statistics in place (see include/gs.h); with param_grads, also
+    writes each Gaussian's parameter-gradient 2-norm into grad_mag."""
+    ps = proj.struct()
+    pg = C.byref(_tensors(param_grads)) if param_grads is not None else None
+    check(_abi.load().gs_densify_stats(C.byref(ps), _ptr(grad2d), int(width), int(height), int(bool(ndc)),
+                                       _ptr(grad_norm_accum), _ptr(view_count), _ptr(max_radius), pg,
+                                       _ptr(grad_mag) if grad_mag is not None else None, int(sh_degree),
+                                       _stream(stream)), "gs_densify_stats")
+
+
+def gs_loss_l1_dssim(image, target, lam: float = 0.2, workspace=None, out=None, stream=None):
+    """(loss, dL/dimage) of the L1 + D-SSIM image loss; loss is a one-element device tensor."""
+    _, h, w = image.shape
+    need = int(_abi.load().gs_loss_workspace_bytes(int(w), int(h)))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=image.device)
+    loss, dl = out if out is not None else (torch.empty(1, device=image.device), torch.empty_like(image))
+    check(_abi.load().gs_loss_l1_dssim(_ptr(image.contiguous()), _ptr(target.contiguous()), int(w), int(h),
+                                       float(lam), _ptr(workspace), need, _ptr(loss), _ptr(dl), _stream(stream)),
+          "gs_loss_l1_dssim")
+    return loss, dl
+
+
 def gs_device_error(stream=None) -> int:
     """Synchronises and returns (and clears) the device error status: 0, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK."""
     return int(_abi.load().gs_device_error(_stream(stream)))

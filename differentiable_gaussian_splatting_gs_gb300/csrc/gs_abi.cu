@@ -366,4 +366,80 @@ int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options
     return e ? cuda_fail(e, "gs_preprocess_bwd") : GS_OK;
 }
 
+int gs_adam_step(gs_tensors* params, const gs_tensors* grads, gs_tensors* exp_avg, gs_tensors* exp_avg_sq,
+                 const int32_t* radius, const gs_adam_options* opt, void* stream) {
+    if (!params || !grads || !exp_avg || !exp_avg_sq || !opt)
+        return fail(GS_ERR_ARG, "params, grads, exp_avg, exp_avg_sq or opt is NULL");
+    const int64_t n = params->n;
+    if (n < 0 || n > 0x7fffffffll) return fail(GS_ERR_ARG, "n = %lld outside 0..2^31-1", (long long)n);
+    if (grads->n != n || exp_avg->n != n || exp_avg_sq->n != n)
+        return fail(GS_ERR_ARG, "params, grads and moments must have the same n");
+    if (opt->step < 1) return fail(GS_ERR_ARG, "step %d must be >= 1", opt->step);
+    if (opt->sh_degree < 0 || opt->sh_degree > 3) return fail(GS_ERR_ARG, "sh_degree %d outside 0..3", opt->sh_degree);
+    const float b1 = opt->beta1 == 0.f ? 0.9f : opt->beta1, b2 = opt->beta2 == 0.f ? 0.999f : opt->beta2;
+    const float eps = opt->eps == 0.f ? 1e-15f : opt->eps;
+    if (!(b1 > 0.f && b1 < 1.f) || !(b2 > 0.f && b2 < 1.f) || !(eps > 0.f) || !std::isfinite(eps))
+        return fail(GS_ERR_ARG, "betas must lie in (0, 1) and eps be finite and positive");
+    if (n == 0) return GS_OK;
+    const gs_tensors* ts[4] = {params, grads, exp_avg, exp_avg_sq};
+    for (const gs_tensors* t : ts) {
+        const void* ptrs[5] = {t->mean3d, t->log_scale, t->quat, t->opacity_logit, t->sh};
+        for (const void* q : ptrs)
+            if (!q || !aligned(q, 16)) return fail(GS_ERR_ARG, "a tensor pointer is NULL or not 16-byte aligned");
+    }
+    if (!radius || !aligned(radius, 4)) return fail(GS_ERR_ARG, "radius NULL or misaligned");
+    cudaError_t e = launch_adam(*params, *grads, *exp_avg, *exp_avg_sq, radius, *opt, opt->sh_degree, b1, b2, eps,
+                                as_stream(stream));
+    return e ? cuda_fail(e, "gs_adam_step") : GS_OK;
+}
+
+int gs_densify_stats(const gs_proj* proj, const float* grad2d, int32_t width, int32_t height, int32_t ndc,
+                     float* grad_norm_accum, int32_t* view_count, int32_t* max_radius,
+                     const gs_tensors* param_grads, float* grad_mag, int32_t sh_degree, void* stream) {
+    int s;
+    if ((s = check_proj_n(proj))) return s;
+    if (sh_degree < 0 || sh_degree > 3) return fail(GS_ERR_ARG, "sh_degree %d outside 0..3", sh_degree);
+    if (ndc && (width <= 0 || height <= 0)) return fail(GS_ERR_ARG, "ndc needs the image size");
+    const int64_t n = proj->n;
+    if (n == 0) return GS_OK;
+    if (!proj->radius || !aligned(proj->radius, 4)) return fail(GS_ERR_ARG, "proj.radius NULL or misaligned");
+    if (!grad2d || !aligned(grad2d, 16)) return fail(GS_ERR_ARG, "grad2d NULL or not 16-byte aligned");
+    if (!grad_norm_accum || !view_count || !max_radius || !aligned(grad_norm_accum, 4) || !aligned(view_count, 4) ||
+        !aligned(max_radius, 4))
+        return fail(GS_ERR_ARG, "grad_norm_accum, view_count or max_radius NULL or misaligned");
+    if (param_grads) {
+        if (param_grads->n != n) return fail(GS_ERR_ARG, "param_grads.n does not match proj.n");
+        const void* ptrs[5] = {param_grads->mean3d, param_grads->log_scale, param_grads->quat,
+                               param_grads->opacity_logit, param_grads->sh};
+        for (const void* q : ptrs)
+            if (!q || !aligned(q, 16)) return fail(GS_ERR_ARG, "a param_grads pointer is NULL or not 16-byte aligned");
+        if (!grad_mag || !aligned(grad_mag, 4)) return fail(GS_ERR_ARG, "grad_mag NULL or misaligned");
+    }
+    const float sx = ndc ? 0.5f * (float)width : 1.f, sy = ndc ? 0.5f * (float)height : 1.f;
+    cudaError_t e = launch_densify_stats(sh_degree, (int)n, proj->radius, grad2d, sx, sy, grad_norm_accum, view_count,
+                                         max_radius, param_grads, grad_mag, as_stream(stream));
+    return e ? cuda_fail(e, "gs_densify_stats") : GS_OK;
+}
+
+size_t gs_loss_workspace_bytes(int32_t width, int32_t height) {
+    if (width <= 0 || height <= 0 || width > kMaxImageSide || height > kMaxImageSide) return 0;
+    return loss_workspace_bytes(width, height);
+}
+
+int gs_loss_l1_dssim(const float* image, const float* target, int32_t width, int32_t height, float lambda,
+                     void* workspace, size_t workspace_bytes, float* loss, float* dl_dimage, void* stream) {
+    if (width <= 0 || height <= 0 || width > kMaxImageSide || height > kMaxImageSide)
+        return fail(GS_ERR_ARG, "image size %dx%d outside 1..%d", width, height, kMaxImageSide);
+    if (!(lambda >= 0.f && lambda <= 1.f)) return fail(GS_ERR_ARG, "lambda must lie in [0, 1]");
+    if (!image || !target || !loss || !dl_dimage || !aligned(image, 4) || !aligned(target, 4) || !aligned(loss, 4) ||
+        !aligned(dl_dimage, 4))
+        return fail(GS_ERR_ARG, "image, target, loss or dl_dimage NULL or misaligned");
+    const size_t need = loss_workspace_bytes(width, height);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+        return fail(GS_ERR_ARG, "workspace NULL, not 256-byte aligned or smaller than %zu bytes", need);
+    cudaError_t e = launch_loss_l1_dssim(image, target, width, height, lambda, workspace, loss, dl_dimage,
+                                         as_stream(stream));
+    return e ? cuda_fail(e, "gs_loss_l1_dssim") : GS_OK;
+}
+
 }  // extern "C"

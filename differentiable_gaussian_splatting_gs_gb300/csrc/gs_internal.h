@@ -53,4 +53,14 @@ cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& pro
                               const float* t_final, const unsigned* n_contrib, float* grad2d, unsigned spin_limit,
                               unsigned* err, cudaStream_t st);
 
+cudaError_t launch_adam(const gs_tensors& P, const gs_tensors& G, const gs_tensors& M, const gs_tensors& V,
+                        const int* radius, const gs_adam_options& o, int deg, float beta1, float beta2, float eps,
+                        cudaStream_t st);
+cudaError_t launch_densify_stats(int deg, int n, const int* radius, const float* grad2d, float sx, float sy,
+                                 float* accum, int* count, int* max_radius, const gs_tensors* pg, float* grad_mag,
+                                 cudaStream_t st);
+size_t loss_workspace_bytes(int width, int height);
+cudaError_t launch_loss_l1_dssim(const float* img, const float* tgt, int width, int height, float lam, void* ws,
+                                 float* loss, float* dl, cudaStream_t st);
+
 }  // namespace gs

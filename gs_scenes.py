@@ -248,3 +248,27 @@ def scene_summary(s: Scene) -> dict:
     cam = s.cameras[0]
     return dict(name=s.name, n=s.n, width=cam.width, height=cam.height, views=len(s.cameras),
                 sh_degree=s.sh_degree, tiles=cam.n_tiles)
+
+
+# learning rates per tensor of the 3D Gaussian splatting recipe (mean3d scaled by a unit scene extent)
+ADAM_LR = {"mean3d": 1.6e-4, "log_scale": 5e-3, "quat": 1e-3, "opacity": 5e-2, "sh_dc": 2.5e-3,
+           "sh_rest": 2.5e-3 / 20}
+
+
+def make_adam_state(n: int, deg: int, seed: int, visible_frac: float = 0.5) -> dict:
+    """Seeded float32 inputs of one sparse Adam step: parameters, gradients, both moments (as after
+    some earlier steps) and a visibility mask; the gradients of hidden Gaussians are zero, as the
+    backward leaves them."""
+    rng = _rng(10_000 + seed)
+    K = (deg + 1) ** 2
+    shapes = {"mean3d": (n, 3), "log_scale": (n, 3), "quat": (n, 4), "opacity_logit": (n,), "sh": (n, K, 3)}
+    vis = rng.random(n) < visible_frac
+    out = {"visible": vis, "params": {}, "grads": {}, "exp_avg": {}, "exp_avg_sq": {}}
+    for k, shp in shapes.items():
+        out["params"][k] = rng.normal(0.0, 1.0, shp).astype(np.float32)
+        g = (rng.normal(0.0, 1.0, shp) * 10.0 ** rng.uniform(-6, -2, shp)).astype(np.float32)
+        g[~vis] = 0.0
+        out["grads"][k] = g
+        out["exp_avg"][k] = (rng.normal(0.0, 1.0, shp) * 1e-3).astype(np.float32)
+        out["exp_avg_sq"][k] = (rng.normal(0.0, 1.0, shp) * 1e-3).astype(np.float32) ** 2
+    return out

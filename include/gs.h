@@ -196,6 +196,76 @@ int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options
                       float* d_log_scale, float* d_quat, float* d_opacity_logit, float* d_sh,
                       int32_t accumulate, void* stream);
 
+/* ---- optimizer update ------------------------------------------------------------------
+ * The update phase "U" of a training step (Odin: Primitive-Level Synchronization for Distributed
+ * Point-Based Neural Rendering, Figure 7), with the optimizer the Odin review names (Adam;
+ * Review, item 1), applied only to the primitives the view made visible (Odin, Abstract: each
+ * view reads and updates only the visible primitives).
+ *
+ * A set of per-Gaussian float32 tensors in the layout of gs_params; used for the parameters
+ * (updated in place), their gradients and the two Adam moments. Every pointer 16-byte aligned. */
+typedef struct gs_tensors {
+    float*  mean3d;         /* [N][3] */
+    float*  log_scale;      /* [N][3] */
+    float*  quat;           /* [N][4] */
+    float*  opacity_logit;  /* [N]    */
+    float*  sh;             /* [N][K][3], K = (sh_degree + 1)^2 */
+    int64_t n;
+} gs_tensors;
+
+typedef struct gs_adam_options {
+    float   lr_mean3d, lr_log_scale, lr_quat, lr_opacity;  /* learning rates per tensor */
+    float   lr_sh_dc, lr_sh_rest;  /* sh coefficients k = 0 and k >= 1 */
+    float   beta1, beta2, eps;     /* 0 = 0.9, 0.999, 1e-15 */
+    int32_t step;                  /* t >= 1, the step's index: bias corrections 1 - beta^t */
+    int32_t sh_degree;             /* 0..3 */
+} gs_adam_options;
+
+/* Sparse Adam step. For every Gaussian i with radius[i] > 0 (radius: device int32 [N] from
+ * gs_preprocess of the view) and every element x of its parameters, with gradient g:
+ *   m = beta1 m + (1 - beta1) g,  v = beta2 v + (1 - beta2) g^2,
+ *   x = x - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps);
+ * Gaussians with radius 0 keep their parameters and moments. One kernel over all five tensors.
+ * Errors: GS_ERR_ARG (NULL or misaligned pointers, n mismatch, step < 1, bad betas or degree),
+ * GS_ERR_CUDA.                                                                                */
+int gs_adam_step(gs_tensors* params, const gs_tensors* grads, gs_tensors* exp_avg, gs_tensors* exp_avg_sq,
+                 const int32_t* radius, const gs_adam_options* opt, void* stream);
+
+/* ---- post-backward statistics ----------------------------------------------------------
+ * Per-primitive gradient statistics of one view, read after the backward: what 3D Gaussian
+ * splatting's densification accumulates over views, and the per-primitive gradient magnitude that
+ * Odin's post-backward hook reports (Odin: Primitive-Level Synchronization for Distributed
+ * Point-Based Neural Rendering, Review, item 1: the gate reads ||g_A(p)|| per primitive).
+ *
+ * For every Gaussian i with radius[i] > 0 (proj from gs_preprocess of the view; grad2d from
+ * gs_render_bwd):
+ *   grad_norm_accum[i] += sqrt((sx dL/dmean_x)^2 + (sy dL/dmean_y)^2), where (sx, sy) = (1, 1)
+ *       (pixel units) or (width / 2, height / 2) when ndc != 0 (normalised device coordinates);
+ *   view_count[i] += 1;  max_radius[i] = max(max_radius[i], radius[i]).
+ * Hidden Gaussians keep their values. If param_grads is not NULL (the outputs of
+ * gs_preprocess_bwd, layout of gs_tensors, sh with K = (sh_degree + 1)^2), grad_mag [N] receives
+ * for every Gaussian the 2-norm of all its parameter gradients (0 when hidden).
+ * Errors: GS_ERR_ARG (NULL or misaligned pointers, n mismatch, bad degree), GS_ERR_CUDA.      */
+int gs_densify_stats(const gs_proj* proj, const float* grad2d, int32_t width, int32_t height, int32_t ndc,
+                     float* grad_norm_accum, int32_t* view_count, int32_t* max_radius,
+                     const gs_tensors* param_grads, float* grad_mag, int32_t sh_degree, void* stream);
+
+/* ---- image loss ---------------------------------------------------------------------------
+ * The loss whose gradient feeds the gradient computation phase (Odin: Primitive-Level
+ * Synchronization for Distributed Point-Based Neural Rendering, Figure 7: rendering, then backward):
+ *   L = (1 - lambda) mean|x - y| + lambda (1 - mean SSIM(x, y)),
+ * means over the 3 x H x W values; SSIM per channel with an 11x11 Gaussian window (sigma 1.5,
+ * normalised), C1 = 0.01^2, C2 = 0.03^2, zero padding outside the image. (The pages name SSIM as an
+ * evaluation metric, Odin Figure 15; this form is the 3D Gaussian splatting training loss.)
+ * image, target: [3][H][W] float32 device; outputs: *loss (one device float) and dl_dimage
+ * [3][H][W] (the derivative of |x - y| at x = y is taken as 0). lambda in [0, 1] (0.2 in that
+ * recipe). workspace: device buffer of gs_loss_workspace_bytes(W, H) bytes, 256-byte aligned.
+ * Errors: GS_ERR_ARG (NULL or misaligned pointers, bad size or lambda, small workspace),
+ * GS_ERR_CUDA.                                                                                */
+size_t gs_loss_workspace_bytes(int32_t width, int32_t height);
+int gs_loss_l1_dssim(const float* image, const float* target, int32_t width, int32_t height, float lambda,
+                     void* workspace, size_t workspace_bytes, float* loss, float* dl_dimage, void* stream);
+
 /* Size of the device workspace that gs_bin_and_sort_static uses instead of a caller buffer. */
 #define GS_STATIC_SORT_WORKSPACE_BYTES (32u << 20)
 

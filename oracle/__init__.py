@@ -8,6 +8,7 @@ and the CUDA library never imports it.
                    forward/backward with marginal-decision flags, preprocess backward by dual numbers)
     brute.py       numpy brute-force per-pixel renderer for tiny scenes (no tiles list, no sort code)
     gs_oracle.cpp  the float64 implementation
+    optim.py       numpy sparse Adam (the update phase after the backward)
 """
 from ._lib import (bin_and_sort, build, preprocess, preprocess_bwd, quat_to_rotmat, render, sh_basis,
                    view_step)
