@@ -33,14 +33,23 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fwd+bwd ms/view and Mpix/s at 1.6M Gaussians 1297×840; bwd L2-atomic roofline %"
-WORKLOAD = "outdoor: 1.6M Gaussians, 1297x840, SH degree 3, 64-cluster mixture, one view per step"
-CFG = 2
+WORKLOADS = {
+    0: "tiny: 2k Gaussians, 128x128, SH degree 0, one view per step",
+    1: "object: 100k Gaussians, 800x800, SH degree 3, white background, one view per step",
+    2: "outdoor: 1.6M Gaussians, 1297x840, SH degree 3, 64-cluster mixture, one view per step",
+    3: "large: 3M Gaussians, 1959x1090, SH degree 3, 128-cluster mixture + shell, 8 views per step",
+    4: "contention: 50k large Gaussians, 3840x2160, SH degree 0, one view per step",
+}
+CFG = 2  # the configuration the metric is quoted on (the default workload)
+WORKLOAD = WORKLOADS[CFG]
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 COUNTS_PATH = os.path.join(ROOT, "profiles", "workload_counts_outdoor.md")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "render_bwd_outdoor_1600k.md")
-# FP32 operations per blended (pixel, Gaussian) pair in the backward: power 11, alpha 3,
-# transmittance 4, colour gradient 3, alpha gradient 15, colour-behind update 6, opacity and
-# geometry gradients 13.
+# Algorithmic work of the backward raster: every pixel's list is replayed back to front from its
+# last contributor, about 60 FP32 operations per replayed (pixel, Gaussian) pair. A narrower count,
+# 55 operations per blended pair only (power 11, alpha 3, transmittance 4, colour gradient 3, alpha
+# gradient 15, colour-behind update 6, opacity and geometry gradients 13), is reported beside it.
+BWD_FLOPS_PER_REPLAYED_PAIR = 60
 BWD_FLOPS_PER_PAIR = 55
 
 
@@ -56,6 +65,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the update phase after the step")
+    ap.add_argument("--config", type=int, default=CFG, choices=sorted(WORKLOADS),
+                    help="workload; the default is the one the metric is quoted on")
     return ap.parse_args()
 
 
@@ -138,9 +149,9 @@ def reduce_max(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def throughput_mpix(world: int, pixels_per_view: int, ms_per_step: float) -> float:
-    """Whole-job Mpix/s: every rank renders one view per step; the step takes the slowest rank's time."""
-    return world * pixels_per_view / (ms_per_step / 1e3) / 1e6
+def throughput_mpix(world: int, pixels_per_step: int, ms_per_step: float) -> float:
+    """Whole-job Mpix/s: every rank renders one step's views; the step takes the slowest rank's time."""
+    return world * pixels_per_step / (ms_per_step / 1e3) / 1e6
 
 
 def load_json(path):
@@ -244,12 +255,13 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     lib = _abi.load()
 
-    scene = gs_scenes.make_scene(CFG)
+    scene = gs_scenes.make_scene(args.config)
     cam = scene.cameras[0]
-    P = cam.width * cam.height
+    n_views = len(scene.cameras)
+    P = cam.width * cam.height * n_views  # pixels per step (all views have the same size)
     names = ("mean3d", "log_scale", "quat", "opacity_logit", "sh")
     host = {k: torch.from_numpy(np.ascontiguousarray(getattr(scene, k))).pin_memory() for k in names}
-    host_target = torch.from_numpy(scene.targets[0]).pin_memory()
+    host_target = torch.from_numpy(np.stack(scene.targets[:n_views])).pin_memory()
     params = {k: host[k].to(dev) for k in names}
     target = host_target.to(dev)
     grads = api.alloc_param_grads(params)
@@ -260,20 +272,26 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    cams = [api.make_camera(c) for c in scene.cameras]
+
     def one_step(ev_bwd=None):
-        c = api.make_camera(cam)
-        proj = api.gs_preprocess(params, c, opt, out=bufs.proj)
-        image, t_final, n_contrib, dl, ranges = bufs.image_buffers(c.width, c.height)
-        b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges, want_keys=False)
-        api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib))
-        torch.sub(image, target, out=dl)
-        if ev_bwd is not None:
-            ev_bwd[0].record(stream)
-        api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=bufs.grad2d)
-        if ev_bwd is not None:
-            ev_bwd[1].record(stream)
-        api.gs_preprocess_bwd(params, c, opt, proj, bufs.grad2d, out=grads)
-        return b.n_dup
+        """All views of one step; the views' parameter gradients are summed. ev_bwd: one event pair
+        per view around the backward raster."""
+        n_dup = 0
+        for v, c in enumerate(cams):
+            proj = api.gs_preprocess(params, c, opt, out=bufs.proj)
+            image, t_final, n_contrib, dl, ranges = bufs.image_buffers(c.width, c.height)
+            b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges, want_keys=False)
+            api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib))
+            torch.sub(image, target[v], out=dl)
+            if ev_bwd is not None:
+                ev_bwd[v][0].record(stream)
+            api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=bufs.grad2d)
+            if ev_bwd is not None:
+                ev_bwd[v][1].record(stream)
+            api.gs_preprocess_bwd(params, c, opt, proj, bufs.grad2d, out=grads, accumulate=v > 0)
+            n_dup += b.n_dup
+        return n_dup
 
     def barrier():
         if world > 1:
@@ -293,13 +311,13 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(args.steps):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            eb = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            eb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
             e0.record(stream)
             n_dup = one_step(eb)
             e1.record(stream)
             torch.cuda.synchronize()
             step_ms.append(e0.elapsed_time(e1))
-            bwd_ms.append(eb[0].elapsed_time(eb[1]))
+            bwd_ms.append(sum(e[0].elapsed_time(e[1]) for e in eb) / n_views)  # per view
     barrier()
     torch.cuda.synchronize()
     launches = lib.gs_kernel_launches() - launches0
@@ -388,13 +406,13 @@ def run_ours(args, rank, world, local_rank):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            api.gs_loss_l1_dssim(image, target, 0.2, workspace=lws, out=lout)
+            api.gs_loss_l1_dssim(image, target[n_views - 1], 0.2, workspace=lws, out=lout)
             e1.record(stream)
             torch.cuda.synchronize()
             if it > 3:
                 l_ms.append(e0.elapsed_time(e1))
         lm = sum(l_ms) / len(l_ms)
-        l_bytes = P * 3 * 4 * (2 + 3 + 3 + 2 + 1)  # pass 1: x, y in, 3 maps out; pass 2: 3 maps, x, y in, dL out
+        l_bytes = cam.width * cam.height * 3 * 4 * (2 + 3 + 3 + 2 + 1)  # pass 1: x, y in, 3 maps out; pass 2: 3 maps, x, y in, dL out
         extras["loss_l1_dssim"] = {"ms": lm, "algorithmic_bytes": l_bytes, "achieved_gbs": l_bytes / (lm / 1e3) / 1e9,
                                    "frac_of_measured_hbm": l_bytes / (lm / 1e3) / 1e9 / hbm}
         assert api.gs_device_error() == 0
@@ -407,15 +425,19 @@ def run_ours(args, rank, world, local_rank):
     sm_mhz_peak = float(peaks.get("sm_max_mhz", 2070.0))
     alu_peak = 152 * 128 * 2 * sm_mhz_peak * 1e6 / 1e12  # FP32 FMA lanes x 2 flops x max SM clock
     roof = None
-    if "pairs_blended" in counts:
-        flops = counts["pairs_blended"] * BWD_FLOPS_PER_PAIR
+    if "pairs_replayed_bwd" in counts and args.config == CFG:
+        flops = counts["pairs_replayed_bwd"] * BWD_FLOPS_PER_REPLAYED_PAIR
         ach = flops / (bwd_avg_ms / 1e3) / 1e12
+        blended = counts["pairs_blended"] * BWD_FLOPS_PER_PAIR / (bwd_avg_ms / 1e3) / 1e12
         traffic = None
         tr = json_block(TRAFFIC_PATH)
         if tr and tr.get("source_hash") == source_hash("differentiable_gaussian_splatting_gs_gb300/csrc/render.cu"):
             traffic = tr.get("dram_bytes_per_launch")
         roof = {"kernel": "gs_render_bwd (k_render_bwd + gradient zeroing)", "bound": "alu", "achieved": ach,
                 "peak": alu_peak, "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": traffic,
+                "numerator": "60 FP32 operations per (pixel, Gaussian) pair replayed from each pixel's last "
+                             "contributor (the kernel's exact warp culling skips most of these pairs)",
+                "frac_blended_pairs_only": blended / alu_peak,
                 "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock of measured peaks file",
                 "kernel_ms": bwd_avg_ms, "algorithmic_flops": flops,
                 "hbm_frac_of_measured": (counts.get("bwd_bytes", 0) / (bwd_avg_ms / 1e3) / 1e9) /
@@ -424,13 +446,13 @@ def run_ours(args, rank, world, local_rank):
     line = {"metric": METRIC, "value": value, "unit": "Mpix/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "n_gaussians": scene.n, "width": cam.width, "height": cam.height,
-                       "duplicates": int(n_dup), "bwd_mode": args.mode,
+            "config": {"workload": WORKLOADS[args.config], "n_gaussians": scene.n, "width": cam.width,
+                       "height": cam.height, "views_per_step": n_views, "duplicates": int(n_dup), "bwd_mode": args.mode,
                        "l2": "flushed between timed steps (256 MB write, outside the events)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
-            "bwd_ms": bwd_avg_ms, "step_ms_min": min(step_ms), "extras": extras}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            "bwd_ms": bwd_avg_ms, "ms_per_view": ms / n_views, "step_ms_min": min(step_ms), "extras": extras}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and n_views == 1:
         pix, dt, desc, cores = oracle_sample(scene, 0.5, 0.5)
         line["cpu_baseline"] = {"value": pix / dt / 1e6, "unit": "Mpix/s", "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}

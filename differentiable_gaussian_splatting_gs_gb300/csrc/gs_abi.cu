@@ -381,6 +381,9 @@ int gs_adam_step(gs_tensors* params, const gs_tensors* grads, gs_tensors* exp_av
     if (!(b1 > 0.f && b1 < 1.f) || !(b2 > 0.f && b2 < 1.f) || !(eps > 0.f) || !std::isfinite(eps))
         return fail(GS_ERR_ARG, "betas must lie in (0, 1) and eps be finite and positive");
     if (n == 0) return GS_OK;
+    const long long k3 = 3ll * (opt->sh_degree + 1) * (opt->sh_degree + 1);
+    if (n * k3 >= (1ll << 32) || n * (k3 + 11) / 4 + 5 >= (1ll << 32))
+        return fail(GS_ERR_ARG, "n = %lld too large: the sh tensor must hold fewer than 2^32 floats", (long long)n);
     const gs_tensors* ts[4] = {params, grads, exp_avg, exp_avg_sq};
     for (const gs_tensors* t : ts) {
         const void* ptrs[5] = {t->mean3d, t->log_scale, t->quat, t->opacity_logit, t->sh};

@@ -31,23 +31,31 @@ struct AdamArgs {
 __device__ __forceinline__ void adam_elem(float& p, float& m, float& v, float g, float lr, const AdamArgs& a) {
     m = __fmaf_rn(a.beta1, m, a.one_m_beta1 * g);
     v = __fmaf_rn(a.beta2, v, a.one_m_beta2 * g * g);
-    const float mh = m * a.inv_bc1, vh = v * a.inv_bc2;
-    p -= lr * mh / (sqrtf(vh) + a.eps);
+    // step lr m^ / (sqrt(v^) + eps); the division to 2 ulps (the step's tolerance is far wider)
+    p -= __fdividef(lr * (m * a.inv_bc1), sqrtf(v * a.inv_bc2) + a.eps);
 }
 
 // Unit r (floats 4r .. 4r + 3) of a tensor with W floats per Gaussian (W a compile-time constant,
-// so the Gaussian index is a multiply-shift). SH: the sh tensor, whose first 3 floats per Gaussian
-// take lr and the rest lr_rest.
+// so the Gaussian index is a multiply-shift; units are counted in 32 bits, which the launcher
+// guarantees). SH: the sh tensor, whose first 3 floats per Gaussian take lr and the rest lr_rest.
 template <int W, bool SH>
-__device__ __forceinline__ void adam_unit(const AdamSegment& q, long long r, const AdamArgs& a) {
-    const long long e0 = 4 * r;
-    const int cnt = (int)min(4ll, q.len - e0);
+__device__ __forceinline__ void adam_unit(const AdamSegment& q, unsigned r, const AdamArgs& a) {
+    const unsigned e0 = 4u * r;
+    const unsigned len = (unsigned)q.len;
+    const int cnt = (int)min(4u, len - e0);
     bool vis[4];
     bool any = false;
+    if (W % 4 == 0) {  // the unit lies inside one Gaussian
+        const bool v = a.radius[e0 / W] > 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        vis[k] = k < cnt && a.radius[(e0 + k) / W] > 0;
-        any |= vis[k];
+        for (int k = 0; k < 4; ++k) vis[k] = v;
+        any = v;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            vis[k] = k < cnt && a.radius[(e0 + k) / W] > 0;
+            any |= vis[k];
+        }
     }
     if (!any) return;
     float p[4], m[4], v[4], g[4];
@@ -67,10 +75,11 @@ __device__ __forceinline__ void adam_unit(const AdamSegment& q, long long r, con
             g[k] = k < cnt ? q.g[e0 + k] : 0.f;
         }
     }
+    const unsigned col0 = SH ? e0 % W : 0u;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         if (!vis[k]) continue;
-        const float lr = (SH && ((e0 + k) % W) >= 3) ? q.lr_rest : q.lr;
+        const float lr = (SH && col0 + k >= 3u) ? q.lr_rest : q.lr;
         adam_elem(p[k], m[k], v[k], g[k], lr, a);
     }
     if (cnt == 4) {
@@ -88,13 +97,13 @@ __device__ __forceinline__ void adam_unit(const AdamSegment& q, long long r, con
 }
 
 template <int K3>
-__global__ void __launch_bounds__(256) k_adam(const AdamArgs a, long long total_units) {
-    const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(256) k_adam(const AdamArgs a, unsigned total_units) {
+    const unsigned u = blockIdx.x * blockDim.x + threadIdx.x;
     if (u >= total_units) return;
-    long long r = u;
+    unsigned r = u;
     int s = 0;
-    while (s < 4 && r >= a.seg[s].units) {
-        r -= a.seg[s].units;
+    while (s < 4 && r >= (unsigned)a.seg[s].units) {
+        r -= (unsigned)a.seg[s].units;
         ++s;
     }
     switch (s) {
@@ -137,13 +146,16 @@ cudaError_t launch_adam(const gs_tensors& P, const gs_tensors& G, const gs_tenso
     a.inv_bc1 = (float)(1.0 / (1.0 - std::pow((double)beta1, (double)o.step)));
     a.inv_bc2 = (float)(1.0 / (1.0 - std::pow((double)beta2, (double)o.step)));
     a.eps = eps;
+    // element and unit indices are 32-bit: the largest tensor must hold fewer than 2^32 floats
+    if (a.seg[4].len >= (1ll << 32) || total >= (1ll << 32)) return cudaErrorInvalidValue;
     count_launches(1);
     const unsigned blocks = (unsigned)((total + 255) / 256);
+    const unsigned tu = (unsigned)total;
     switch (deg) {
-        case 0: k_adam<3><<<blocks, 256, 0, st>>>(a, total); break;
-        case 1: k_adam<12><<<blocks, 256, 0, st>>>(a, total); break;
-        case 2: k_adam<27><<<blocks, 256, 0, st>>>(a, total); break;
-        default: k_adam<48><<<blocks, 256, 0, st>>>(a, total); break;
+        case 0: k_adam<3><<<blocks, 256, 0, st>>>(a, tu); break;
+        case 1: k_adam<12><<<blocks, 256, 0, st>>>(a, tu); break;
+        case 2: k_adam<27><<<blocks, 256, 0, st>>>(a, tu); break;
+        default: k_adam<48><<<blocks, 256, 0, st>>>(a, tu); break;
     }
     return cudaGetLastError();
 }

@@ -226,8 +226,8 @@ typedef struct gs_adam_options {
  *   m = beta1 m + (1 - beta1) g,  v = beta2 v + (1 - beta2) g^2,
  *   x = x - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps);
  * Gaussians with radius 0 keep their parameters and moments. One kernel over all five tensors.
- * Errors: GS_ERR_ARG (NULL or misaligned pointers, n mismatch, step < 1, bad betas or degree),
- * GS_ERR_CUDA.                                                                                */
+ * Errors: GS_ERR_ARG (NULL or misaligned pointers, n mismatch, step < 1, bad betas or degree,
+ * 2^32 or more floats in the sh tensor), GS_ERR_CUDA.                                          */
 int gs_adam_step(gs_tensors* params, const gs_tensors* grads, gs_tensors* exp_avg, gs_tensors* exp_avg_sq,
                  const int32_t* radius, const gs_adam_options* opt, void* stream);
 

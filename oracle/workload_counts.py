@@ -7,6 +7,8 @@ pixels per active block, and the algorithmic bytes of the backward raster:
     per tile, its list up to the largest contributor count x (4-byte index + 48-byte record),
     + per pixel 20 bytes (dL/dpixel, T_final, contributor count),
     + per Gaussian 48 bytes (the 2D gradient record written).
+    pairs replayed by the backward: the sum over pixels of the contributor count (each pixel's list
+    is replayed back to front from its last contributor).
 The benchmark divides these by measured kernel times; nothing of the CUDA library is used here.
 
     python -m oracle.workload_counts
@@ -49,6 +51,7 @@ def counts(cfg: int = 2) -> dict:
             "pairs_blended": int(st["pairs_blended"]), "warp_gauss_active": int(st["warp_gauss_active"]),
             "tile_gauss_active": int(st["tile_gauss_active"]), "lane_hist": [int(v) for v in st["lane_hist"]],
             "bwd_list_entries": listed, "bwd_bytes": listed * 52 + P * 20 + s.n * 48,
+            "pairs_replayed_bwd": int(nc.astype(np.int64).sum()),
             "marginal_pixels": int(st["marginal_pixels"]), "oracle_seconds": dt, "threads": os.cpu_count()}
 
 
@@ -59,9 +62,10 @@ def main():
     with open(path, "w") as f:
         f.write("# Workload counts: outdoor scene (1.6M Gaussians, 1297x840, seed 2)\n\n")
         f.write("Written by `python -m oracle.workload_counts` (float64 oracle only). The benchmark's\n")
-        f.write("roofline numerators use `pairs_blended` and `bwd_bytes`.\n\n")
+        f.write("roofline numerators use `pairs_replayed_bwd`, `pairs_blended` and `bwd_bytes`.\n\n")
         f.write(f"- duplicates D = {c['duplicates']:,}\n- pairs evaluated = {c['pairs_evaluated']:,}\n")
         f.write(f"- pairs blended = {c['pairs_blended']:,}\n")
+        f.write(f"- pairs replayed by the backward (sum of contributor counts) = {c['pairs_replayed_bwd']:,}\n")
         f.write(f"- active (8x4 block, Gaussian) = {c['warp_gauss_active']:,}; "
                 f"active (tile, Gaussian) = {c['tile_gauss_active']:,}\n")
         full = hist[32] / max(1, sum(hist))
