@@ -274,15 +274,19 @@ def run_ours(args, rank, world, local_rank):
 
     cams = [api.make_camera(c) for c in scene.cameras]
 
-    def one_step(ev_bwd=None):
-        """All views of one step; the views' parameter gradients are summed. ev_bwd: one event pair
-        per view around the backward raster."""
+    def one_step(ev_bwd=None, ev_fwd=None):
+        """All views of one step; the views' parameter gradients are summed. ev_bwd / ev_fwd: one
+        event pair per view around the backward / forward raster."""
         n_dup = 0
         for v, c in enumerate(cams):
             proj = api.gs_preprocess(params, c, opt, out=bufs.proj)
             image, t_final, n_contrib, dl, ranges = bufs.image_buffers(c.width, c.height)
             b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges, want_keys=False)
+            if ev_fwd is not None:
+                ev_fwd[v][0].record(stream)
             api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib))
+            if ev_fwd is not None:
+                ev_fwd[v][1].record(stream)
             torch.sub(image, target[v], out=dl)
             if ev_bwd is not None:
                 ev_bwd[v][0].record(stream)
@@ -303,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
     assert api.gs_device_error() == 0
 
     # ---- device-resident timing: K steps, L2 flushed between steps (outside the events)
-    step_ms, bwd_ms = [], []
+    step_ms, bwd_ms, fwd_ms = [], [], []
     launches0 = lib.gs_kernel_launches()
     barrier()
     torch.cuda.synchronize()
@@ -312,12 +316,14 @@ def run_ours(args, rank, world, local_rank):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             eb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
+            ef = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
             e0.record(stream)
-            n_dup = one_step(eb)
+            n_dup = one_step(eb, ef)
             e1.record(stream)
             torch.cuda.synchronize()
             step_ms.append(e0.elapsed_time(e1))
             bwd_ms.append(sum(e[0].elapsed_time(e[1]) for e in eb) / n_views)  # per view
+            fwd_ms.append(sum(e[0].elapsed_time(e[1]) for e in ef) / n_views)
     barrier()
     torch.cuda.synchronize()
     launches = lib.gs_kernel_launches() - launches0
@@ -451,7 +457,7 @@ def run_ours(args, rank, world, local_rank):
                        "l2": "flushed between timed steps (256 MB write, outside the events)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
-            "bwd_ms": bwd_avg_ms, "ms_per_view": ms / n_views, "step_ms_min": min(step_ms), "extras": extras}
+            "bwd_ms": bwd_avg_ms, "fwd_ms": sum(fwd_ms) / len(fwd_ms), "ms_per_view": ms / n_views, "step_ms_min": min(step_ms), "extras": extras}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and n_views == 1:
         pix, dt, desc, cores = oracle_sample(scene, 0.5, 0.5)
         line["cpu_baseline"] = {"value": pix / dt / 1e6, "unit": "Mpix/s", "cores": cores, "kind": "oracle",

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) k_ssim_fwd(const LossArgs a, const float*
         hs[0][r][c] = m0; hs[1][r][c] = m1; hs[2][r][c] = m2; hs[3][r][c] = m3; hs[4][r][c] = m4;
     }
     __syncthreads();
-    double l1 = 0.0, ss = 0.0;
+    float l1f = 0.f, ssf = 0.f;
     const int c = threadIdx.x;
     for (int rr = threadIdx.y; rr < kLH; rr += blockDim.y) {
         const int gx = x0 + c, gy = y0 + rr;
@@ -82,15 +82,17 @@ __global__ void __launch_bounds__(256) k_ssim_fwd(const LossArgs a, const float*
         const float B = __fmaf_rn(2.f, exy - mx * my, a.c2);
         const float Cc = __fmaf_rn(mx, mx, __fmaf_rn(my, my, a.c1));
         const float D = (exx - mx * mx) + (eyy - my * my) + a.c2;
-        const float inv = 1.f / (Cc * D);
+        const float iC = __frcp_rn(Cc), iD = __frcp_rn(D);
+        const float inv = iC * iD;
         const float S = A * B * inv;
         const size_t o = ch * plane + (size_t)gy * W + gx;
-        p_mu[o] = 2.f * my * (B - A) * inv - 2.f * mx * S * (1.f / Cc - 1.f / D);
-        p_xx[o] = -S / D;
+        p_mu[o] = 2.f * my * (B - A) * inv - 2.f * mx * S * (iC - iD);
+        p_xx[o] = -S * iD;
         p_xy[o] = 2.f * A * inv;
-        l1 += fabs((double)sx[rr + kHalo][c + kHalo] - (double)sy[rr + kHalo][c + kHalo]);
-        ss += (double)S;
+        l1f += fabsf(sx[rr + kHalo][c + kHalo] - sy[rr + kHalo][c + kHalo]);
+        ssf += S;
     }
+    double l1 = (double)l1f, ss = (double)ssf;  // at most 2 terms per thread: float is exact enough
     // block sums of |x - y| and S
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
