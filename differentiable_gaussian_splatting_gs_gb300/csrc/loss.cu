@@ -10,7 +10,7 @@
 // sum(S) with respect to x is w * dS/dmu_x + 2 x (w * dS/dExx) + y (w * dS/dExy) (w is symmetric,
 // so the adjoint of the zero-padded window sum is the same window sum). Pass 1 computes the five
 // windowed moments, S and the three partial derivatives per pixel; pass 2 takes their windowed sums.
-// Both passes stage a 16x32 tile plus a 5-pixel halo in shared memory and filter rows, then columns.
+// Both passes stage a 128x34 tile plus a 5-pixel halo in shared memory.
 #include <cmath>
 
 #include "gs_common.cuh"
@@ -18,8 +18,14 @@
 
 namespace gs {
 
-constexpr int kLW = 32, kLH = 16, kHalo = 5, kTapN = 11;
-constexpr int kInW = kLW + 2 * kHalo, kInH = kLH + 2 * kHalo;
+// Tiles of kLW columns x kLH output rows, one column per thread. A thread takes the horizontal
+// 11-tap sums of its column for each of the kLH + 10 input rows of the tile and adds each into
+// the vertical sums of the 11 output rows it reaches, kept in an 11-slot ring of registers (input
+// row r adds w[t] x its sums to output row r - t); with the row loop unrolled by 11 every ring
+// index is a constant. Output row o is complete after input row o + 10.
+constexpr int kLW = 128, kLH = 34, kHalo = 5, kTapN = 11;
+constexpr int kInW = kLW + 2 * kHalo, kInH = kLH + 2 * kHalo;  // kInH = 44 = 4 x 11
+static_assert(kInH % kTapN == 0, "the input rows of a tile are a multiple of the window");
 
 struct LossArgs {
     float w[kTapN];     // window taps
@@ -27,87 +33,103 @@ struct LossArgs {
     int width, height;
 };
 
-__global__ void __launch_bounds__(256) k_ssim_fwd(const LossArgs a, const float* __restrict__ img,
-                                                  const float* __restrict__ tgt, float* __restrict__ p_mu,
-                                                  float* __restrict__ p_xx, float* __restrict__ p_xy,
-                                                  double* __restrict__ sums) {
-    __shared__ float sx[kInH][kInW], sy[kInH][kInW];
-    __shared__ float hs[5][kInH][kLW];
-    __shared__ double red[2][8];
-    const int W = a.width, H = a.height;
-    const int x0 = blockIdx.x * kLW, y0 = blockIdx.y * kLH, ch = blockIdx.z;
-    const size_t plane = (size_t)W * H;
-    const float* X = img + ch * plane;
-    const float* Y = tgt + ch * plane;
-    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
-    for (int i = tid; i < kInH * kInW; i += 256) {
+// Stages NM maps of the tile (rows y0 - 5 .., columns x0 - 5 ..) with zeros outside the image:
+// asynchronous copies, all in flight at once, waited for before returning (the caller then
+// synchronises the block).
+template <int NM>
+__device__ __forceinline__ void stage_tile(float (*sm)[kInH][kInW], const float* const (&src)[NM], int x0, int y0,
+                                           int W, int H) {
+    for (int i = threadIdx.x; i < kInH * kInW; i += kLW) {
         const int r = i / kInW, c = i - r * kInW;
         const int gy = y0 - kHalo + r, gx = x0 - kHalo + c;
         const bool in = gx >= 0 && gx < W && gy >= 0 && gy < H;
-        sx[r][c] = in ? X[(size_t)gy * W + gx] : 0.f;
-        sy[r][c] = in ? Y[(size_t)gy * W + gx] : 0.f;
-    }
-    __syncthreads();
-    for (int i = tid; i < kInH * kLW; i += 256) {
-        const int r = i / kLW, c = i - r * kLW;
-        float m0 = 0.f, m1 = 0.f, m2 = 0.f, m3 = 0.f, m4 = 0.f;
 #pragma unroll
-        for (int k = 0; k < kTapN; ++k) {
-            const float u = sx[r][c + k], v = sy[r][c + k], wk = a.w[k];
-            m0 = __fmaf_rn(wk, u, m0);
-            m1 = __fmaf_rn(wk, v, m1);
-            m2 = __fmaf_rn(wk, u * u, m2);
-            m3 = __fmaf_rn(wk, v * v, m3);
-            m4 = __fmaf_rn(wk, u * v, m4);
+        for (int m = 0; m < NM; ++m) {
+            if (in) cp_async4(&sm[m][r][c], src[m] + (size_t)gy * W + gx);
+            else sm[m][r][c] = 0.f;
         }
-        hs[0][r][c] = m0; hs[1][r][c] = m1; hs[2][r][c] = m2; hs[3][r][c] = m3; hs[4][r][c] = m4;
     }
+    cp_async_wait_all();
+}
+
+__global__ void __launch_bounds__(kLW) k_ssim_fwd(const LossArgs a, const float* __restrict__ img,
+                                                  const float* __restrict__ tgt, float* __restrict__ p_mu,
+                                                  float* __restrict__ p_xx, float* __restrict__ p_xy,
+                                                  double* __restrict__ sums) {
+    extern __shared__ float smem_loss[];
+    float (*sm)[kInH][kInW] = reinterpret_cast<float (*)[kInH][kInW]>(smem_loss);  // x, y
+    __shared__ double red[2][kLW / 32];
+    const int W = a.width, H = a.height;
+    const int x0 = blockIdx.x * kLW, y0 = blockIdx.y * kLH, ch = blockIdx.z;
+    const size_t plane = (size_t)W * H;
+    const float* const src[2] = {img + ch * plane, tgt + ch * plane};
+    stage_tile<2>(sm, src, x0, y0, W, H);
     __syncthreads();
+    const int c = threadIdx.x, gx = x0 + c;
+    float acc[kTapN][5];
+#pragma unroll
+    for (int s2 = 0; s2 < kTapN; ++s2)
+#pragma unroll
+        for (int m = 0; m < 5; ++m) acc[s2][m] = 0.f;
     float l1f = 0.f, ssf = 0.f;
-    const int c = threadIdx.x;
-    for (int rr = threadIdx.y; rr < kLH; rr += blockDim.y) {
-        const int gx = x0 + c, gy = y0 + rr;
-        if (gx >= W || gy >= H) continue;
-        float mx = 0.f, my = 0.f, exx = 0.f, eyy = 0.f, exy = 0.f;
+    for (int q = 0; q < kInH / kTapN; ++q) {
 #pragma unroll
-        for (int k = 0; k < kTapN; ++k) {
-            const float wk = a.w[k];
-            mx = __fmaf_rn(wk, hs[0][rr + k][c], mx);
-            my = __fmaf_rn(wk, hs[1][rr + k][c], my);
-            exx = __fmaf_rn(wk, hs[2][rr + k][c], exx);
-            eyy = __fmaf_rn(wk, hs[3][rr + k][c], eyy);
-            exy = __fmaf_rn(wk, hs[4][rr + k][c], exy);
+        for (int j = 0; j < kTapN; ++j) {
+            const int r = q * kTapN + j;
+            float h[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < kTapN; ++k) {
+                const float u = sm[0][r][c + k], v = sm[1][r][c + k], wk = a.w[k];
+                h[0] = __fmaf_rn(wk, u, h[0]);
+                h[1] = __fmaf_rn(wk, v, h[1]);
+                h[2] = __fmaf_rn(wk, u * u, h[2]);
+                h[3] = __fmaf_rn(wk, v * v, h[3]);
+                h[4] = __fmaf_rn(wk, u * v, h[4]);
+            }
+#pragma unroll
+            for (int t = 0; t < kTapN; ++t)
+#pragma unroll
+                for (int m = 0; m < 5; ++m) acc[(j - t + kTapN) % kTapN][m] = __fmaf_rn(a.w[t], h[m], acc[(j - t + kTapN) % kTapN][m]);
+            // output row o = r - 10 is complete
+            const int slot = (j + 1) % kTapN;
+            const int o = r - (kTapN - 1), gy = y0 + o;
+            if (o >= 0 && gx < W && gy < H) {
+                const float mx = acc[slot][0], my = acc[slot][1], exx = acc[slot][2], eyy = acc[slot][3];
+                const float exy = acc[slot][4];
+                const float A = __fmaf_rn(2.f * mx, my, a.c1);
+                const float B = __fmaf_rn(2.f, exy - mx * my, a.c2);
+                const float Cc = __fmaf_rn(mx, mx, __fmaf_rn(my, my, a.c1));
+                const float D = (exx - mx * mx) + (eyy - my * my) + a.c2;
+                const float iC = __frcp_rn(Cc), iD = __frcp_rn(D);
+                const float inv = iC * iD;
+                const float S = A * B * inv;
+                const size_t oo = ch * plane + (size_t)gy * W + gx;
+                p_mu[oo] = 2.f * my * (B - A) * inv - 2.f * mx * S * (iC - iD);
+                p_xx[oo] = -S * iD;
+                p_xy[oo] = 2.f * A * inv;
+                l1f += fabsf(sm[0][o + kHalo][c + kHalo] - sm[1][o + kHalo][c + kHalo]);
+                ssf += S;
+            }
+#pragma unroll
+            for (int m = 0; m < 5; ++m) acc[slot][m] = 0.f;
         }
-        const float A = __fmaf_rn(2.f * mx, my, a.c1);
-        const float B = __fmaf_rn(2.f, exy - mx * my, a.c2);
-        const float Cc = __fmaf_rn(mx, mx, __fmaf_rn(my, my, a.c1));
-        const float D = (exx - mx * mx) + (eyy - my * my) + a.c2;
-        const float iC = __frcp_rn(Cc), iD = __frcp_rn(D);
-        const float inv = iC * iD;
-        const float S = A * B * inv;
-        const size_t o = ch * plane + (size_t)gy * W + gx;
-        p_mu[o] = 2.f * my * (B - A) * inv - 2.f * mx * S * (iC - iD);
-        p_xx[o] = -S * iD;
-        p_xy[o] = 2.f * A * inv;
-        l1f += fabsf(sx[rr + kHalo][c + kHalo] - sy[rr + kHalo][c + kHalo]);
-        ssf += S;
     }
-    double l1 = (double)l1f, ss = (double)ssf;  // at most 2 terms per thread: float is exact enough
-    // block sums of |x - y| and S
+    // block sums of |x - y| and S (float per thread, float64 across threads)
+    double l1 = (double)l1f, ss = (double)ssf;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         ss += __shfl_xor_sync(0xffffffffu, ss, off);
     }
-    const int warp = tid >> 5;
-    if ((tid & 31) == 0) {
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
         red[0][warp] = l1;
         red[1][warp] = ss;
     }
     __syncthreads();
-    if (tid == 0) {
+    if (threadIdx.x == 0) {
         double t0 = 0.0, t1 = 0.0;
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < kLW / 32; ++w) {
             t0 += red[0][w];
             t1 += red[1][w];
         }
@@ -116,59 +138,65 @@ __global__ void __launch_bounds__(256) k_ssim_fwd(const LossArgs a, const float*
     }
 }
 
-__global__ void __launch_bounds__(256) k_ssim_bwd(const LossArgs a, const float* __restrict__ img,
+__global__ void __launch_bounds__(kLW) k_ssim_bwd(const LossArgs a, const float* __restrict__ img,
                                                   const float* __restrict__ tgt, const float* __restrict__ p_mu,
                                                   const float* __restrict__ p_xx, const float* __restrict__ p_xy,
                                                   const double* __restrict__ sums, float* __restrict__ loss,
                                                   float* __restrict__ dl) {
-    __shared__ float sp[3][kInH][kInW];
-    __shared__ float hs[3][kInH][kLW];
+    extern __shared__ float smem_loss[];
+    float (*sm)[kInH][kInW] = reinterpret_cast<float (*)[kInH][kInW]>(smem_loss);  // the 3 partial maps
     const int W = a.width, H = a.height;
     const int x0 = blockIdx.x * kLW, y0 = blockIdx.y * kLH, ch = blockIdx.z;
     const size_t plane = (size_t)W * H;
-    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
-    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && ch == 0)
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && ch == 0)
         *loss = (float)((1.0 - a.lam) * sums[0] * a.inv_n + a.lam * (1.0 - sums[1] * a.inv_n));
-    for (int i = tid; i < kInH * kInW; i += 256) {
-        const int r = i / kInW, c = i - r * kInW;
-        const int gy = y0 - kHalo + r, gx = x0 - kHalo + c;
-        const bool in = gx >= 0 && gx < W && gy >= 0 && gy < H;
-        const size_t o = ch * plane + (size_t)gy * W + gx;
-        sp[0][r][c] = in ? p_mu[o] : 0.f;
-        sp[1][r][c] = in ? p_xx[o] : 0.f;
-        sp[2][r][c] = in ? p_xy[o] : 0.f;
-    }
+    const float* const src[3] = {p_mu + ch * plane, p_xx + ch * plane, p_xy + ch * plane};
+    stage_tile<3>(sm, src, x0, y0, W, H);
     __syncthreads();
-    for (int i = tid; i < kInH * kLW; i += 256) {
-        const int r = i / kLW, c = i - r * kLW;
-        float m0 = 0.f, m1 = 0.f, m2 = 0.f;
+    const int c = threadIdx.x, gx = x0 + c;
+    float acc[kTapN][3];
 #pragma unroll
-        for (int k = 0; k < kTapN; ++k) {
-            const float wk = a.w[k];
-            m0 = __fmaf_rn(wk, sp[0][r][c + k], m0);
-            m1 = __fmaf_rn(wk, sp[1][r][c + k], m1);
-            m2 = __fmaf_rn(wk, sp[2][r][c + k], m2);
-        }
-        hs[0][r][c] = m0; hs[1][r][c] = m1; hs[2][r][c] = m2;
-    }
-    __syncthreads();
-    const int c = threadIdx.x;
-    for (int rr = threadIdx.y; rr < kLH; rr += blockDim.y) {
-        const int gx = x0 + c, gy = y0 + rr;
-        if (gx >= W || gy >= H) continue;
-        float g0 = 0.f, g1 = 0.f, g2 = 0.f;
+    for (int s2 = 0; s2 < kTapN; ++s2)
 #pragma unroll
-        for (int k = 0; k < kTapN; ++k) {
-            const float wk = a.w[k];
-            g0 = __fmaf_rn(wk, hs[0][rr + k][c], g0);
-            g1 = __fmaf_rn(wk, hs[1][rr + k][c], g1);
-            g2 = __fmaf_rn(wk, hs[2][rr + k][c], g2);
+        for (int m = 0; m < 3; ++m) acc[s2][m] = 0.f;
+    for (int q = 0; q < kInH / kTapN; ++q) {
+        // image and target at the 11 outputs this group of rows completes, loaded ahead of use
+        float xs[kTapN], ys[kTapN];
+#pragma unroll
+        for (int j = 0; j < kTapN; ++j) {
+            const int o = q * kTapN + j - (kTapN - 1), gy = y0 + o;
+            const bool ok = o >= 0 && gx < W && gy < H;
+            const size_t oo = ch * plane + (size_t)(ok ? gy : 0) * W + (ok ? gx : 0);
+            xs[j] = ok ? img[oo] : 0.f;
+            ys[j] = ok ? tgt[oo] : 0.f;
         }
-        const size_t o = ch * plane + (size_t)gy * W + gx;
-        const float x = img[o], y = tgt[o];
-        const float dssim = __fmaf_rn(2.f * x, g1, __fmaf_rn(y, g2, g0));
-        const float sgn = x > y ? 1.f : (x < y ? -1.f : 0.f);
-        dl[o] = a.inv_n * ((1.f - a.lam) * sgn - a.lam * dssim);
+#pragma unroll
+        for (int j = 0; j < kTapN; ++j) {
+            const int r = q * kTapN + j;
+            float h[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < kTapN; ++k) {
+                const float wk = a.w[k];
+                h[0] = __fmaf_rn(wk, sm[0][r][c + k], h[0]);
+                h[1] = __fmaf_rn(wk, sm[1][r][c + k], h[1]);
+                h[2] = __fmaf_rn(wk, sm[2][r][c + k], h[2]);
+            }
+#pragma unroll
+            for (int t = 0; t < kTapN; ++t)
+#pragma unroll
+                for (int m = 0; m < 3; ++m) acc[(j - t + kTapN) % kTapN][m] = __fmaf_rn(a.w[t], h[m], acc[(j - t + kTapN) % kTapN][m]);
+            const int slot = (j + 1) % kTapN;
+            const int o = r - (kTapN - 1), gy = y0 + o;
+            if (o >= 0 && gx < W && gy < H) {
+                const size_t oo = ch * plane + (size_t)gy * W + gx;
+                const float x = xs[j], y = ys[j];
+                const float dssim = __fmaf_rn(2.f * x, acc[slot][1], __fmaf_rn(y, acc[slot][2], acc[slot][0]));
+                const float sgn = x > y ? 1.f : (x < y ? -1.f : 0.f);
+                dl[oo] = a.inv_n * ((1.f - a.lam) * sgn - a.lam * dssim);
+            }
+#pragma unroll
+            for (int m = 0; m < 3; ++m) acc[slot][m] = 0.f;
+        }
     }
 }
 
@@ -197,10 +225,13 @@ cudaError_t launch_loss_l1_dssim(const float* img, const float* tgt, int width, 
     float* p_xy = p_xx + plane3;
     cudaError_t e = cudaMemsetAsync(sums, 0, 2 * sizeof(double), st);
     if (e) return e;
-    const dim3 grid((width + kLW - 1) / kLW, (height + kLH - 1) / kLH, 3), block(32, 8);
+    const dim3 grid((width + kLW - 1) / kLW, (height + kLH - 1) / kLH, 3);
+    const int smem2 = 2 * kInH * kInW * 4, smem3 = 3 * kInH * kInW * 4;
+    if ((e = cudaFuncSetAttribute(k_ssim_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2))) return e;
+    if ((e = cudaFuncSetAttribute(k_ssim_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem3))) return e;
     count_launches(2);
-    k_ssim_fwd<<<grid, block, 0, st>>>(a, img, tgt, p_mu, p_xx, p_xy, sums);
-    k_ssim_bwd<<<grid, block, 0, st>>>(a, img, tgt, p_mu, p_xx, p_xy, sums, loss, dl);
+    k_ssim_fwd<<<grid, kLW, smem2, st>>>(a, img, tgt, p_mu, p_xx, p_xy, sums);
+    k_ssim_bwd<<<grid, kLW, smem3, st>>>(a, img, tgt, p_mu, p_xx, p_xy, sums, loss, dl);
     return cudaGetLastError();
 }
 

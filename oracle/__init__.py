@@ -7,11 +7,11 @@ and the CUDA library never imports it.
     _lib.py        ctypes binding of gs_oracle.cpp (preprocess, binning + stable sort, render
                    forward/backward with marginal-decision flags, preprocess backward by dual numbers)
     brute.py       numpy brute-force per-pixel renderer for tiny scenes (no tiles list, no sort code)
-    gs_oracle.cpp  the float64 implementation
+    gs_oracle.cpp  the float64 implementation (3D Gaussians, and surfels of 2D Gaussian splatting)
     optim.py       numpy sparse Adam (the update phase after the backward)
 """
-from ._lib import (bin_and_sort, build, preprocess, preprocess_bwd, quat_to_rotmat, render, sh_basis,
-                   view_step)
+from ._lib import (bin_and_sort, build, preprocess, preprocess2d, preprocess2d_bwd, preprocess_bwd, quat_to_rotmat,
+                   render, render2d, sh_basis, view_step, view_step2d)
 
-__all__ = ["bin_and_sort", "build", "preprocess", "preprocess_bwd", "quat_to_rotmat", "render",
-           "sh_basis", "view_step"]
+__all__ = ["bin_and_sort", "build", "preprocess", "preprocess2d", "preprocess2d_bwd", "preprocess_bwd",
+           "quat_to_rotmat", "render", "render2d", "sh_basis", "view_step", "view_step2d"]

@@ -65,6 +65,12 @@ def lib():
             _lib.or_render.restype = C.c_int
             _lib.or_preprocess_bwd.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 6
             _lib.or_preprocess_bwd.restype = C.c_int
+            _lib.or_preprocess2d.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 6
+            _lib.or_preprocess2d.restype = C.c_int
+            _lib.or_render2d.argtypes = [C.c_int64, P, P, P, P, P, P, P, P, P, P, P, C.c_int]
+            _lib.or_render2d.restype = C.c_int
+            _lib.or_preprocess2d_bwd.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 6
+            _lib.or_preprocess2d_bwd.restype = C.c_int
             _lib.or_sh_basis.argtypes = [C.c_int, P, P]
             _lib.or_quat_to_rotmat.argtypes = [P, P]
         return _lib
@@ -184,6 +190,72 @@ def preprocess_bwd(mean3d, log_scale, quat, opacity_logit, sh, sh_degree, cam, g
                                  _p(out["d_mean3d"]), _p(out["d_log_scale"]), _p(out["d_quat"]),
                                  _p(out["d_opacity_logit"]), _p(out["d_sh"]))
     assert rc == 0
+    return out
+
+
+def preprocess2d(mean3d, log_scale, quat, opacity_logit, sh, sh_degree, cam, threads=0, **opt):
+    """Surfel (2D Gaussian splatting) preprocessing: rec2d [N, 16] = (A_u, B_u, C_u, A_v, B_v, C_v,
+    m_x, m_y, z_c, c_x, c_y, opacity, r, g, b, 0), mean2d = bounding-box centre (for the binning),
+    depth, radius, tiles_touched, half extents."""
+    n = int(np.asarray(mean3d).shape[0])
+    m, ls, q, lg, sh = (_c(mean3d, np.float64), _c(log_scale, np.float64), _c(quat, np.float64),
+                        _c(opacity_logit, np.float64), _c(sh, np.float64))
+    out = dict(rec2d=np.zeros((n, 16)), mean2d=np.zeros((n, 2)), depth=np.zeros(n, np.float32),
+               radius=np.zeros(n, np.int32), tiles_touched=np.zeros(n, np.uint32), half=np.zeros((n, 2)))
+    c, o = camera(cam), options(sh_degree, threads=threads, **opt)
+    rc = lib().or_preprocess2d(n, _p(m), _p(ls), _p(q), _p(lg), _p(sh), C.byref(c), C.byref(o), _p(out["rec2d"]),
+                               _p(out["mean2d"]), _p(out["depth"]), _p(out["radius"]), _p(out["tiles_touched"]),
+                               _p(out["half"]))
+    assert rc == 0
+    return out
+
+
+def render2d(rec2d, vals, ranges, cam, dl_dimage=None, threads=0, bg=None):
+    """Surfel render forward (+ backward: grad [N, 16] = dL/d rec2d fields 0..14)."""
+    n = int(np.asarray(rec2d).shape[0])
+    W, H = int(cam.width), int(cam.height)
+    r, v, rg = _c(rec2d, np.float64), _c(vals, np.uint32), _c(ranges, np.uint32)
+    dl = None if dl_dimage is None else _c(dl_dimage, np.float32)
+    out = dict(image=np.zeros((3, H, W)), t_final=np.zeros((H, W)), n_contrib=np.zeros((H, W), np.uint32),
+               pix_flags=np.zeros((H, W), np.uint8), pix_sig=np.zeros((H, W), np.uint64))
+    grad = np.zeros((n, 16)) if dl is not None else None
+    c = camera(cam, bg)
+    rc = lib().or_render2d(n, _p(r), _p(v), _p(rg), C.byref(c), _p(dl), _p(out["image"]), _p(out["t_final"]),
+                           _p(out["n_contrib"]), _p(out["pix_flags"]), _p(out["pix_sig"]), _p(grad), int(threads))
+    assert rc == 0
+    out["grad"] = grad
+    return out
+
+
+def preprocess2d_bwd(mean3d, log_scale, quat, opacity_logit, sh, sh_degree, cam, grad, threads=0, **opt):
+    n = int(np.asarray(mean3d).shape[0])
+    K = (sh_degree + 1) ** 2
+    m, ls, q, lg, shc = (_c(mean3d, np.float64), _c(log_scale, np.float64), _c(quat, np.float64),
+                         _c(opacity_logit, np.float64), _c(sh, np.float64))
+    g = _c(grad, np.float64)
+    out = dict(d_mean3d=np.zeros((n, 3)), d_log_scale=np.zeros((n, 3)), d_quat=np.zeros((n, 4)),
+               d_opacity_logit=np.zeros(n), d_sh=np.zeros((n, K, 3)))
+    c, o = camera(cam), options(sh_degree, threads=threads, **opt)
+    rc = lib().or_preprocess2d_bwd(n, _p(m), _p(ls), _p(q), _p(lg), _p(shc), C.byref(c), C.byref(o), _p(g),
+                                   _p(out["d_mean3d"]), _p(out["d_log_scale"]), _p(out["d_quat"]),
+                                   _p(out["d_opacity_logit"]), _p(out["d_sh"]))
+    assert rc == 0
+    return out
+
+
+def view_step2d(scene, view=0, dl_dimage=None, threads=0):
+    """Surfel training step of one view in float64: preprocess, binning (the same tile sort on the
+    bounding-box centres), render forward, and with dl_dimage the backward to the parameters."""
+    cam = scene.cameras[view]
+    pre = preprocess2d(scene.mean3d, scene.log_scale, scene.quat, scene.opacity_logit, scene.sh, scene.sh_degree,
+                       cam, threads=threads)
+    keys, vals, ranges = bin_and_sort(pre["mean2d"].astype(np.float32), pre["depth"], pre["radius"], cam.width,
+                                      cam.height, capacity=int(pre["tiles_touched"].sum(dtype=np.int64)))
+    fwd = render2d(pre["rec2d"], vals, ranges, cam, dl_dimage, threads=threads)
+    out = dict(pre=pre, keys=keys, vals=vals, ranges=ranges, fwd=fwd)
+    if dl_dimage is not None:
+        out["bwd"] = preprocess2d_bwd(scene.mean3d, scene.log_scale, scene.quat, scene.opacity_logit, scene.sh,
+                                      scene.sh_degree, cam, fwd["grad"], threads=threads)
     return out
 
 

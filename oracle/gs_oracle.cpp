@@ -683,3 +683,323 @@ int or_preprocess_bwd(int64_t n, const double* mean3d, const double* log_scale, 
 }
 
 }  // extern "C"
+
+// =============================================================================================
+// 2D Gaussian splatting (surfels): each Gaussian is a flat disk in 3D, P(u, v) = mean + s_u u t_u
+// + s_v v t_v with t_u, t_v the first two columns of its rotation, evaluated where the pixel's ray
+// meets the disk's plane (Odin: Primitive-Level Synchronization for Distributed Point-Based Neural
+// Rendering, Summary: 2DGS is one of the four pipelines it trains; the formulation is 2DGS's own).
+//
+// Record of a projected surfel (the format both sides share), 11 geometric fields + opacity + rgb:
+//   A_u = s_u fx (W t_u)_x, B_u = s_u fy (W t_u)_y, C_u = s_u (W t_u)_z, likewise A_v, B_v, C_v for
+//   t_v; m = (fx x_c / z_c + cx, fy y_c / z_c + cy) the projected mean and z_c its depth; c the
+//   centre of the screen-space bounding box of the 3-sigma disk. With K the intrinsics, the disk
+//   point (u, v) lands at homogeneous screen position T (u, v, 1), T = [K W s_u t_u | K W s_v t_v |
+//   K p_c], and the pixel (x, y) constrains (u, v) by the two planes h_x = T_0 - x T_2 and
+//   h_y = T_1 - y T_2: h_x = (A_u + (cx - x) C_u, A_v + (cx - x) C_v, z_c (m_x - x)), likewise h_y.
+// =============================================================================================
+
+namespace {
+
+template <class S>
+struct Projected2D {
+    bool culled;
+    float depth32;
+    S rec[11];      // A_u, B_u, C_u, A_v, B_v, C_v, m_x, m_y, z_c, c_x, c_y
+    S opacity;
+    S rgb[3];
+    bool rgb_clamped[3];
+    double half[2];  // half extents of the bounding box of the 3-sigma disk (px)
+    double Y[16];
+};
+
+template <class S>
+void project2d(const S mu[3], const S ls[3], const S q[4], const S& logit, const double* shg, int deg,
+               const OrCamera& cam, const OrOptions& opt, Projected2D<S>& P) {
+    P.culled = false;
+    const float mu32[3] = {(float)val(mu[0]), (float)val(mu[1]), (float)val(mu[2])};
+    P.depth32 = depth_key(cam, mu32);
+    if (!(P.depth32 > (float)opt.near_z)) { P.culled = true; return; }
+    double Rc[9], tc[3];
+    for (int i = 0; i < 9; ++i) Rc[i] = cam.R[i];
+    for (int i = 0; i < 3; ++i) tc[i] = cam.t[i];
+    S p[3];
+    for (int i = 0; i < 3; ++i) p[i] = Rc[3 * i] * mu[0] + Rc[3 * i + 1] * mu[1] + Rc[3 * i + 2] * mu[2] + tc[i];
+    S qn = sqrt(q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3]);
+    S qu[4] = {q[0] / qn, q[1] / qn, q[2] / qn, q[3] / qn};
+    S Rq[9];
+    quat_to_rotmat(qu, Rq);
+    const S su = exp(ls[0]), sv = exp(ls[1]);
+    S wu[3], wv[3];  // W t_u, W t_v (t_u, t_v = columns 0 and 1 of Rq)
+    for (int i = 0; i < 3; ++i) {
+        wu[i] = Rc[3 * i] * Rq[0] + Rc[3 * i + 1] * Rq[3] + Rc[3 * i + 2] * Rq[6];
+        wv[i] = Rc[3 * i] * Rq[1] + Rc[3 * i + 1] * Rq[4] + Rc[3 * i + 2] * Rq[7];
+    }
+    const double fx = cam.fx, fy = cam.fy, cx = cam.cx, cy = cam.cy;
+    P.rec[0] = su * fx * wu[0]; P.rec[1] = su * fy * wu[1]; P.rec[2] = su * wu[2];
+    P.rec[3] = sv * fx * wv[0]; P.rec[4] = sv * fy * wv[1]; P.rec[5] = sv * wv[2];
+    const S z = p[2];
+    P.rec[6] = fx * p[0] / z + cx;
+    P.rec[7] = fy * p[1] / z + cy;
+    P.rec[8] = z;
+    // bounding box of the disk u^2 + v^2 <= 9: from the dual conic C* = T diag(9, 9, -1) T^T, the
+    // lines x = k tangent to the projected disk solve C*00 - 2 k C*02 + k^2 C*22 = 0
+    const S T0[3] = {P.rec[0] + cx * P.rec[2], P.rec[3] + cx * P.rec[5], z * P.rec[6]};
+    const S T1[3] = {P.rec[1] + cy * P.rec[2], P.rec[4] + cy * P.rec[5], z * P.rec[7]};
+    const S T2[3] = {P.rec[2], P.rec[5], z};
+    auto dual = [](const S a[3], const S b[3]) { return 9.0 * (a[0] * b[0] + a[1] * b[1]) - a[2] * b[2]; };
+    const S c00 = dual(T0, T0), c11 = dual(T1, T1), c22 = dual(T2, T2), c02 = dual(T0, T2), c12 = dual(T1, T2);
+    if (!(val(c22) < 0.0)) { P.culled = true; return; }  // the disk reaches the camera plane
+    P.rec[9] = c02 / c22;
+    P.rec[10] = c12 / c22;
+    const double hx2 = val(c02) * val(c02) - val(c00) * val(c22), hy2 = val(c12) * val(c12) - val(c11) * val(c22);
+    P.half[0] = std::sqrt(std::max(hx2, 0.0)) / std::fabs(val(c22));
+    P.half[1] = std::sqrt(std::max(hy2, 0.0)) / std::fabs(val(c22));
+    for (int i = 0; i < 11; ++i)
+        if (!std::isfinite(val(P.rec[i]))) { P.culled = true; return; }
+    P.opacity = 1.0 / (1.0 + exp(-logit));
+    double cpos[3];
+    for (int j = 0; j < 3; ++j) cpos[j] = -(Rc[j] * tc[0] + Rc[3 + j] * tc[1] + Rc[6 + j] * tc[2]);
+    S dvec[3] = {mu[0] - cpos[0], mu[1] - cpos[1], mu[2] - cpos[2]};
+    S dn = sqrt(dvec[0] * dvec[0] + dvec[1] * dvec[1] + dvec[2] * dvec[2]);
+    S Yb[16];
+    sh_basis(deg, dvec[0] / dn, dvec[1] / dn, dvec[2] / dn, Yb);
+    const int K = (deg + 1) * (deg + 1);
+    for (int k = 0; k < K; ++k) P.Y[k] = val(Yb[k]);
+    for (int ch = 0; ch < 3; ++ch) {
+        S acc(0.5);
+        for (int k = 0; k < K; ++k) acc = acc + Yb[k] * shg[k * 3 + ch];
+        P.rgb_clamped[ch] = val(acc) < 0.0;
+        P.rgb[ch] = P.rgb_clamped[ch] ? S(0.0) : acc;
+    }
+}
+
+// Radius of the square the binning uses: the larger half extent, and at least the 3-sigma extent
+// of the screen-space filter (standard deviation sqrt(1/2) px).
+int radius2d(const double half[2]) {
+    const double r = std::ceil(std::max(std::max(half[0], half[1]), 3.0 * std::sqrt(0.5)));
+    return r < 16777216.0 ? (int)r : 0;
+}
+
+// Exponent of the surfel's weight at pixel centre (x, y): the larger of the disk's Gaussian at
+// the ray-plane intersection, -(u^2 + v^2)/2, and the screen-space filter around the box centre,
+// -|(x, y) - c|^2 (a Gaussian of variance 1/2 px^2). u, v by Cramer's rule on the two planes.
+template <class S>
+S power2d(const S r[11], double cx, double cy, double x, double y, S* p3_out = nullptr, S* plp_out = nullptr) {
+    const S hxu = r[0] + (cx - x) * r[2], hxv = r[3] + (cx - x) * r[5], hx1 = r[8] * (r[6] - x);
+    const S hyu = r[1] + (cy - y) * r[2], hyv = r[4] + (cy - y) * r[5], hy1 = r[8] * (r[7] - y);
+    const S det = hxu * hyv - hxv * hyu;
+    S p3;
+    if (val(det) == 0.0) {
+        p3 = S(-std::numeric_limits<double>::infinity());
+    } else {
+        const S u = (hxv * hy1 - hx1 * hyv) / det, v = (hx1 * hyu - hxu * hy1) / det;
+        p3 = -0.5 * (u * u + v * v);
+    }
+    const S dx = r[9] - x, dy = r[10] - y;
+    const S plp = -(dx * dx + dy * dy);
+    if (p3_out) *p3_out = p3;
+    if (plp_out) *plp_out = plp;
+    return val(p3) >= val(plp) ? p3 : plp;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Surfel preprocessing: rec2d [n][16] = (11 geometric fields, opacity, r, g, b, 0), the float32
+// depth, the binning radius (0 = culled), the tile count, and the bounding-box centre as mean2d
+// [n][2] for the binning.
+int or_preprocess2d(int64_t n, const double* mean3d, const double* log_scale, const double* quat,
+                    const double* logit, const double* sh, const OrCamera* cam, const OrOptions* opt,
+                    double* rec2d, double* mean2d, float* depth, int32_t* radius, uint32_t* tiles_touched,
+                    double* half) {
+    if (n < 0 || !cam || !opt) return -1;
+    const int deg = opt->sh_degree, K = (deg + 1) * (deg + 1);
+    const int tiles_x = (cam->width + kTile - 1) / kTile, tiles_y = (cam->height + kTile - 1) / kTile;
+#pragma omp parallel for schedule(static) num_threads(n_threads(opt->threads))
+    for (int64_t g = 0; g < n; ++g) {
+        Projected2D<double> P;
+        project2d<double>(mean3d + 3 * g, log_scale + 3 * g, quat + 4 * g, logit[g], sh + g * K * 3, deg, *cam,
+                          *opt, P);
+        depth[g] = P.depth32;
+        double* r = rec2d + 16 * g;
+        for (int i = 0; i < 16; ++i) r[i] = 0.0;
+        radius[g] = 0;
+        tiles_touched[g] = 0;
+        mean2d[2 * g] = mean2d[2 * g + 1] = 0.0;
+        half[2 * g] = half[2 * g + 1] = 0.0;
+        if (P.culled) continue;
+        const int rad = radius2d(P.half);
+        if (rad == 0) continue;
+        const Rect R = tile_rect((float)P.rec[9], (float)P.rec[10], rad, tiles_x, tiles_y);
+        if (R.empty) continue;
+        for (int i = 0; i < 11; ++i) r[i] = P.rec[i];
+        r[11] = P.opacity;
+        for (int ch = 0; ch < 3; ++ch) r[12 + ch] = P.rgb[ch];
+        radius[g] = rad;
+        tiles_touched[g] = (uint32_t)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+        mean2d[2 * g] = P.rec[9];
+        mean2d[2 * g + 1] = P.rec[10];
+        half[2 * g] = P.half[0];
+        half[2 * g + 1] = P.half[1];
+    }
+    return 0;
+}
+
+// Surfel render forward (and backward when grad != NULL): front to back over each tile's list with
+// the same alpha, threshold, clamp and termination rules as the 3D rasterizer; the backward is the
+// exact derivative of that forward from the stored per-pixel (alpha_i, T_i), with d power / d record
+// by dual numbers over the 11 geometric fields. grad [n][16] = dL/d(rec2d fields 0..14).
+// pix_flags: 1 alpha within 1e-4 of 1/255, 2 T (1 - alpha) within 1e-4 of 1e-4, 4 the two exponents
+// within 1e-4 of each other (the max may switch branches), 8 the intersection ill-conditioned.
+int or_render2d(int64_t n, const double* rec2d, const uint32_t* vals, const uint32_t* ranges, const OrCamera* cam,
+                const float* dl_dimage, double* image, double* t_final, uint32_t* n_contrib, uint8_t* pix_flags,
+                uint64_t* pix_sig, double* grad, int threads) {
+    const int W = cam->width, H = cam->height;
+    const int tiles_x = (W + kTile - 1) / kTile, tiles_y = (H + kTile - 1) / kTile;
+    const int64_t T = (int64_t)tiles_x * tiles_y;
+    const double alpha_min = (double)(1.0f / 255.0f), t_min = (double)1e-4f;
+    const double cx = cam->cx, cy = cam->cy;
+    if (grad) std::memset(grad, 0, sizeof(double) * 16 * (size_t)n);
+#pragma omp parallel num_threads(n_threads(threads))
+    {
+        struct Blend { int64_t pos; uint32_t g; double alpha, T, G; bool clamped; double x, y; };
+        std::vector<Blend> bl;
+        std::vector<double> acc;
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t tile = 0; tile < T; ++tile) {
+            const int tx = (int)(tile % tiles_x), ty = (int)(tile / tiles_x);
+            const int64_t s = ranges[2 * tile], e = ranges[2 * tile + 1];
+            const int64_t len = e - s;
+            if (grad) acc.assign((size_t)len * 16, 0.0);
+            for (int ly = 0; ly < kTile; ++ly)
+                for (int lx = 0; lx < kTile; ++lx) {
+                    const int px = tx * kTile + lx, py = ty * kTile + ly;
+                    if (px >= W || py >= H) continue;
+                    const double x = px + 0.5, y = py + 0.5;
+                    double Tr = 1.0, col[3] = {0.0, 0.0, 0.0};
+                    uint32_t contrib = 0;
+                    uint8_t pf = 0;
+                    uint64_t sig = 1469598103934665603ull;  // FNV-1a over (position, clamp, branch) of blended entries
+                    bl.clear();
+                    for (int64_t pos = s; pos < e; ++pos) {
+                        const uint32_t g = vals[pos];
+                        const double* r = rec2d + 16 * (size_t)g;
+                        double p3, plp;
+                        const double power = power2d<double>(r, cx, cy, x, y, &p3, &plp);
+                        if (std::fabs(p3 - plp) <= 1e-4 * (std::fabs(p3) + std::fabs(plp)) + 1e-7) pf |= 4;
+                        const double G = std::exp(power);
+                        const double oG = r[11] * G;
+                        const bool clamped = oG > 0.99;
+                        const double alpha = clamped ? 0.99 : oG;
+                        if (!clamped && std::fabs(alpha / alpha_min - 1.0) < 1e-4) pf |= 1;
+                        if (alpha < alpha_min) continue;
+                        const double test_T = Tr * (1.0 - alpha);
+                        if (std::fabs(test_T / t_min - 1.0) < 1e-4) pf |= 2;
+                        if (test_T < t_min) break;
+                        for (int ch = 0; ch < 3; ++ch) col[ch] += r[12 + ch] * alpha * Tr;
+                        bl.push_back({pos, g, alpha, Tr, G, clamped, x, y});
+                        sig = (sig ^ (uint64_t)(4 * (pos - s) + (clamped ? 1 : 0) + (p3 >= plp ? 2 : 0))) * 1099511628211ull;
+                        Tr = test_T;
+                        contrib = (uint32_t)(pos - s + 1);
+                    }
+                    const int64_t pix = (int64_t)py * W + px;
+                    for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
+                    t_final[pix] = Tr;
+                    n_contrib[pix] = contrib;
+                    if (pix_flags) pix_flags[pix] = pf;
+                    if (pix_sig) pix_sig[pix] = sig;
+                    if (!grad) continue;
+                    double gpix[3], S[3];
+                    for (int ch = 0; ch < 3; ++ch) {
+                        gpix[ch] = dl_dimage[(int64_t)ch * W * H + pix];
+                        S[ch] = Tr * cam->bg[ch];
+                    }
+                    for (int64_t k = (int64_t)bl.size() - 1; k >= 0; --k) {
+                        const Blend& b = bl[k];
+                        const double* r = rec2d + 16 * (size_t)b.g;
+                        double* a = &acc[(size_t)(b.pos - s) * 16];
+                        double dalpha = 0.0;
+                        for (int ch = 0; ch < 3; ++ch) {
+                            a[12 + ch] += b.alpha * b.T * gpix[ch];
+                            dalpha += gpix[ch] * (r[12 + ch] * b.T - S[ch] / (1.0 - b.alpha));
+                        }
+                        for (int ch = 0; ch < 3; ++ch) S[ch] += r[12 + ch] * b.alpha * b.T;
+                        if (b.clamped) continue;
+                        const double dpower = r[11] * b.G * dalpha;
+                        using D = Dual<11>;
+                        D rd[11];
+                        for (int i = 0; i < 11; ++i) rd[i] = D::var(r[i], i);
+                        const D pw = power2d<D>(rd, cx, cy, b.x, b.y);
+                        for (int i = 0; i < 11; ++i) a[i] += pw.d[i] * dpower;
+                        a[11] += b.G * dalpha;
+                    }
+                }
+            if (grad)
+                for (int64_t k = 0; k < len; ++k) {
+                    const uint32_t g = vals[s + k];
+                    for (int j = 0; j < 15; ++j) {
+                        const double v = acc[(size_t)k * 16 + j];
+                        if (v != 0.0) {
+#pragma omp atomic
+                            grad[16 * (size_t)g + j] += v;
+                        }
+                    }
+                }
+        }
+    }
+    return 0;
+}
+
+// Surfel preprocess backward: gradients of the loss with respect to mean3d, log_scale (the first
+// two; the third gets 0), quat, opacity logit and SH from grad [n][16] = dL/d(record), by running
+// project2d on dual numbers in the 10 non-SH parameters. Culled Gaussians get zeros.
+int or_preprocess2d_bwd(int64_t n, const double* mean3d, const double* log_scale, const double* quat,
+                        const double* logit, const double* sh, const OrCamera* cam, const OrOptions* opt,
+                        const double* grad, double* d_mean3d, double* d_log_scale, double* d_quat, double* d_logit,
+                        double* d_sh) {
+    if (n < 0 || !cam || !opt) return -1;
+    const int deg = opt->sh_degree, K = (deg + 1) * (deg + 1);
+    const int tiles_x = (cam->width + kTile - 1) / kTile, tiles_y = (cam->height + kTile - 1) / kTile;
+    using D = Dual<10>;
+#pragma omp parallel for schedule(static) num_threads(n_threads(opt->threads))
+    for (int64_t g = 0; g < n; ++g) {
+        D mu[3], ls[3], q[4];
+        for (int i = 0; i < 3; ++i) mu[i] = D::var(mean3d[3 * g + i], i);
+        ls[0] = D::var(log_scale[3 * g], 3);
+        ls[1] = D::var(log_scale[3 * g + 1], 4);
+        ls[2] = D(log_scale[3 * g + 2]);
+        for (int i = 0; i < 4; ++i) q[i] = D::var(quat[4 * g + i], 5 + i);
+        D lg = D::var(logit[g], 9);
+        Projected2D<D> P;
+        project2d<D>(mu, ls, q, lg, sh + g * K * 3, deg, *cam, *opt, P);
+        double gr[10] = {0};
+        for (int k = 0; k < K * 3; ++k) d_sh[(size_t)g * K * 3 + k] = 0.0;
+        bool culled = P.culled;
+        if (!culled) {
+            const int rad = radius2d(P.half);
+            culled = rad == 0 || tile_rect((float)P.rec[9].v, (float)P.rec[10].v, rad, tiles_x, tiles_y).empty;
+        }
+        if (!culled) {
+            const double* gi = grad + 16 * (size_t)g;
+            for (int o = 0; o < 11; ++o)
+                for (int v = 0; v < 10; ++v) gr[v] += gi[o] * P.rec[o].d[v];
+            for (int v = 0; v < 10; ++v) gr[v] += gi[11] * P.opacity.d[v];
+            for (int ch = 0; ch < 3; ++ch) {
+                for (int v = 0; v < 10; ++v) gr[v] += gi[12 + ch] * P.rgb[ch].d[v];
+                if (P.rgb_clamped[ch]) continue;
+                for (int k = 0; k < K; ++k) d_sh[(size_t)g * K * 3 + k * 3 + ch] = P.Y[k] * gi[12 + ch];
+            }
+        }
+        for (int i = 0; i < 3; ++i) d_mean3d[3 * g + i] = gr[i];
+        d_log_scale[3 * g] = gr[3];
+        d_log_scale[3 * g + 1] = gr[4];
+        d_log_scale[3 * g + 2] = 0.0;
+        for (int i = 0; i < 4; ++i) d_quat[4 * g + i] = gr[5 + i];
+        d_logit[g] = gr[9];
+    }
+    return 0;
+}
+
+}  // extern "C"
