@@ -421,6 +421,34 @@ def run_ours(args, rank, world, local_rank):
         l_bytes = cam.width * cam.height * 3 * 4 * (2 + 3 + 3 + 2 + 1)  # pass 1: x, y in, 3 maps out; pass 2: 3 maps, x, y in, dL out
         extras["loss_l1_dssim"] = {"ms": lm, "algorithmic_bytes": l_bytes, "achieved_gbs": l_bytes / (lm / 1e3) / 1e9,
                                    "frac_of_measured_hbm": l_bytes / (lm / 1e3) / 1e9 / hbm}
+        # the surfel (2D Gaussian splatting) step on the same parameters and view
+        rec2d = torch.empty((scene.n, 16), dtype=torch.float32, device=dev)
+        g2d = torch.empty((scene.n, 16), dtype=torch.float32, device=dev)
+        c0 = cams[0]
+
+        def step2d():
+            proj2, _ = api.gs_preprocess2d(params, c0, opt, out=bufs.proj, rec2d=rec2d)
+            image2, t2, nc2, dl2, ranges2 = bufs.image_buffers(c0.width, c0.height)
+            b2 = api.gs_bin_and_sort(proj2, c0, opt, buffers=bufs.sort, ranges=ranges2, want_keys=False)
+            api.gs_render2d_fwd(rec2d, b2.vals, b2.ranges, c0, opt, out=(image2, t2, nc2))
+            torch.sub(image2, target[0], out=dl2)
+            api.gs_render2d_bwd(rec2d, b2.vals, b2.ranges, c0, opt, dl2, t2, nc2, grad2d=g2d)
+            api.gs_preprocess2d_bwd(params, c0, opt, proj2, g2d, out=grads)
+            return b2.n_dup
+        for _ in range(3):
+            step2d()
+        s_ms2 = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            d2 = step2d()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            s_ms2.append(e0.elapsed_time(e1))
+        m2 = sum(s_ms2) / len(s_ms2)
+        extras["surfel_step"] = {"ms_per_view": m2, "mpix_per_s": cam.width * cam.height / (m2 / 1e3) / 1e6,
+                                 "duplicates": int(d2)}
         assert api.gs_device_error() == 0
 
     # ---- roofline of the dominant kernel (the backward)

@@ -29,7 +29,8 @@ BWD_MODES = {"direct": GS_BWD_DIRECT, "warp": GS_BWD_WARP, "adaptive": GS_BWD_AD
 EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd",
            "gs_preprocess_bwd", "gs_status_string", "gs_last_error_message", "gs_device_error",
            "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static", "gs_adam_step",
-           "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim")
+           "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim", "gs_preprocess2d",
+           "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd")
 GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
 
 
@@ -117,6 +118,12 @@ def load():
         lib.gs_loss_workspace_bytes.restype = C.c_size_t
         lib.gs_loss_l1_dssim.argtypes = [P, P, I32, I32, C.c_float, P, C.c_size_t, P, P, P]
         lib.gs_loss_l1_dssim.restype = C.c_int
+        lib.gs_preprocess2d.argtypes = [ppar, pcam, popt, pproj, P, P]
+        lib.gs_render2d_fwd.argtypes = [P, I64, P, P, pcam, popt, P, P, P, P]
+        lib.gs_render2d_bwd.argtypes = [P, I64, P, P, pcam, popt, P, P, P, P, P]
+        lib.gs_preprocess2d_bwd.argtypes = [ppar, pcam, popt, pproj, P, P, P, P, P, P, I32, P]
+        for name in ("gs_preprocess2d", "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd"):
+            getattr(lib, name).restype = C.c_int
         for name in ("gs_preprocess", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd",
                      "gs_preprocess_bwd", "gs_device_error", "gs_version", "gs_selftest_timeout"):
             getattr(lib, name).restype = C.c_int

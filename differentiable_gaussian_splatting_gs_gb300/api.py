@@ -302,6 +302,59 @@ def gs_loss_l1_dssim(image, target, lam: float = 0.2, workspace=None, out=None, 
     return loss, dl
 
 
+def gs_preprocess2d(params: dict, cam, opt: gs_options, out: Proj | None = None, rec2d=None, stream=None):
+    """Surfel preprocessing: (Proj for the binning, rec2d [N, 16])."""
+    p = _params(params["mean3d"], params["log_scale"], params["quat"], params["opacity_logit"], params["sh"])
+    dev = params["mean3d"].device
+    if out is None:
+        out = alloc_proj(p.n, dev)
+    if rec2d is None:
+        rec2d = torch.empty((p.n, 16), dtype=torch.float32, device=dev)
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    ps = out.struct()
+    check(_abi.load().gs_preprocess2d(C.byref(p), C.byref(c), C.byref(opt), C.byref(ps), _ptr(rec2d), _stream(stream)),
+          "gs_preprocess2d")
+    return out, rec2d
+
+
+def gs_render2d_fwd(rec2d, vals, ranges, cam, opt: gs_options, out=None, stream=None):
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    dev = rec2d.device
+    if out is None:
+        out = (torch.empty((3, c.height, c.width), dtype=torch.float32, device=dev),
+               torch.empty((c.height, c.width), dtype=torch.float32, device=dev),
+               torch.empty((c.height, c.width), dtype=torch.int32, device=dev))
+    image, t_final, n_contrib = out
+    check(_abi.load().gs_render2d_fwd(_ptr(rec2d), int(rec2d.shape[0]), _ptr(vals), _ptr(ranges), C.byref(c),
+                                      C.byref(opt), _ptr(image), _ptr(t_final), _ptr(n_contrib), _stream(stream)),
+          "gs_render2d_fwd")
+    return image, t_final, n_contrib
+
+
+def gs_render2d_bwd(rec2d, vals, ranges, cam, opt: gs_options, dl_dimage, t_final, n_contrib, grad2d=None, stream=None):
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    if grad2d is None:
+        grad2d = torch.empty((rec2d.shape[0], 16), dtype=torch.float32, device=rec2d.device)
+    check(_abi.load().gs_render2d_bwd(_ptr(rec2d), int(rec2d.shape[0]), _ptr(vals), _ptr(ranges), C.byref(c),
+                                      C.byref(opt), _ptr(dl_dimage.contiguous()), _ptr(t_final), _ptr(n_contrib),
+                                      _ptr(grad2d), _stream(stream)), "gs_render2d_bwd")
+    return grad2d
+
+
+def gs_preprocess2d_bwd(params: dict, cam, opt: gs_options, proj: Proj, grad2d, out: dict | None = None,
+                        accumulate: bool = False, stream=None) -> dict:
+    p = _params(params["mean3d"], params["log_scale"], params["quat"], params["opacity_logit"], params["sh"])
+    if out is None:
+        out = alloc_param_grads(params)
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    ps = proj.struct()
+    check(_abi.load().gs_preprocess2d_bwd(C.byref(p), C.byref(c), C.byref(opt), C.byref(ps), _ptr(grad2d),
+                                          _ptr(out["mean3d"]), _ptr(out["log_scale"]), _ptr(out["quat"]),
+                                          _ptr(out["opacity_logit"]), _ptr(out["sh"]), int(bool(accumulate)),
+                                          _stream(stream)), "gs_preprocess2d_bwd")
+    return out
+
+
 def gs_device_error(stream=None) -> int:
     """Synchronises and returns (and clears) the device error status: 0, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK."""
     return int(_abi.load().gs_device_error(_stream(stream)))

@@ -1,0 +1,765 @@
+// Surfel variant of the training step: 2D Gaussian splatting, one of the four rendering pipelines
+// Odin trains (Odin: Primitive-Level Synchronization for Distributed Point-Based Neural Rendering,
+// Summary). Each Gaussian is a flat disk in 3D, P(u, v) = mean + s_u u t_u + s_v v t_v with t_u, t_v
+// the first two columns of its rotation; a pixel weighs it by the disk's Gaussian at the point
+// where the pixel's ray meets the disk's plane, or by a screen-space filter of variance 1/2 px^2
+// around the disk's bounding-box centre, whichever is larger. Blending, thresholds, termination
+// and the backward replay are those of the 3D rasterizer; the binning is the same tile sort.
+//
+// Record of a projected surfel (16 floats, 64 bytes): the 11 geometric fields
+//   A_u = s_u fx (W t_u)_x, B_u = s_u fy (W t_u)_y, C_u = s_u (W t_u)_z, likewise A_v, B_v, C_v,
+//   m = projected mean (px), z_c its depth, c = centre of the screen box of the 3-sigma disk,
+// then opacity, r, g, b and one unused float. With K the intrinsics and T = [K W s_u t_u |
+// K W s_v t_v | K p_c], the pixel (x, y) constrains (u, v) by the planes h_x = T_0 - x T_2 and
+// h_y = T_1 - y T_2; written from the record, h_x = (A_u + (cx - x) C_u, A_v + (cx - x) C_v,
+// z_c (m_x - x)), which keeps float32 free of the cancellation of T_0 - x T_2 near the mean.
+#include <cmath>
+
+#include "gs_common.cuh"
+#include "gs_internal.h"
+#include "sh.cuh"
+
+namespace gs {
+
+constexpr int kS2 = 16;  // floats per surfel record
+
+// ---- forward-mode dual numbers (float) for the surfel preprocess backward --------------------
+template <int NV>
+struct Df {
+    float v;
+    float d[NV];
+    __device__ Df() {}
+    __device__ Df(float x) : v(x) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) d[i] = 0.f;
+    }
+    __device__ static Df var(float x, int i) {
+        Df r(x);
+        r.d[i] = 1.f;
+        return r;
+    }
+};
+template <int NV> __device__ Df<NV> operator+(const Df<NV>& a, const Df<NV>& b) {
+    Df<NV> r(a.v + b.v);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = a.d[i] + b.d[i];
+    return r;
+}
+template <int NV> __device__ Df<NV> operator-(const Df<NV>& a, const Df<NV>& b) {
+    Df<NV> r(a.v - b.v);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = a.d[i] - b.d[i];
+    return r;
+}
+template <int NV> __device__ Df<NV> operator*(const Df<NV>& a, const Df<NV>& b) {
+    Df<NV> r(a.v * b.v);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = a.d[i] * b.v + a.v * b.d[i];
+    return r;
+}
+template <int NV> __device__ Df<NV> operator/(const Df<NV>& a, const Df<NV>& b) {
+    const float ib = 1.f / b.v;
+    Df<NV> r(a.v * ib);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = (a.d[i] - r.v * b.d[i]) * ib;
+    return r;
+}
+template <int NV> __device__ Df<NV> operator*(float a, const Df<NV>& b) {
+    Df<NV> r(a * b.v);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = a * b.d[i];
+    return r;
+}
+template <int NV> __device__ Df<NV> operator/(float a, const Df<NV>& b) {
+    const float ib = 1.f / b.v;
+    Df<NV> r(a * ib);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = -r.v * b.d[i] * ib;
+    return r;
+}
+template <int NV> __device__ Df<NV> operator+(const Df<NV>& a, float b) {
+    Df<NV> r = a;
+    r.v += b;
+    return r;
+}
+template <int NV> __device__ Df<NV> operator-(float a, const Df<NV>& b) {
+    Df<NV> r(a - b.v);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = -b.d[i];
+    return r;
+}
+template <int NV> __device__ Df<NV> dexp(const Df<NV>& a) {
+    Df<NV> r(expf(a.v));
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = r.v * a.d[i];
+    return r;
+}
+template <int NV> __device__ Df<NV> dsqrt(const Df<NV>& a) {
+    Df<NV> r(sqrtf(a.v));
+    const float h = 0.5f / r.v;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) r.d[i] = h * a.d[i];
+    return r;
+}
+__device__ __forceinline__ float dexp(float a) { return expf(a); }
+__device__ __forceinline__ float dsqrt(float a) { return sqrtf(a); }
+__device__ __forceinline__ float fv(float a) { return a; }
+template <int NV> __device__ __forceinline__ float fv(const Df<NV>& a) { return a.v; }
+
+// r . m + t for a row r of the camera rotation; in float the fused chain the depth key uses
+__device__ __forceinline__ float row_dot(const float* r, const float m[3], float t) {
+    return __fmaf_rn(r[0], m[0], __fmaf_rn(r[1], m[1], __fmaf_rn(r[2], m[2], t)));
+}
+template <int NV> __device__ Df<NV> row_dot(const float* r, const Df<NV> m[3], float t) {
+    return r[0] * m[0] + r[1] * m[1] + r[2] * m[2] + t;
+}
+
+// Geometric record of one surfel (fields 0..10) and the half extents of the screen box of its
+// 3-sigma disk; false when the mean is behind the near plane or the disk reaches the camera plane.
+// The box uses screen coordinates relative to the projected mean, where the dual conic of the disk
+// has no cancelling terms: with e = first two entries of T_0 - m_x T_2 (and f for y), the box
+// centre is m + (9 e.(C_u, C_v), 9 f.(C_u, C_v)) / c22 and its half width is
+// sqrt(c02^2 - c00 c22) / |c22|, c22 = 9 (C_u^2 + C_v^2) - z_c^2 < 0.
+template <class S>
+__device__ __forceinline__ bool surfel_geometry(const S m[3], const S& lsu, const S& lsv, const S q[4],
+                                                const KernelCamera& cam, S rec[11], float half[2]) {
+    const float* R = cam.R;
+    const S z = row_dot(R + 6, m, cam.t[2]);
+    if (!(fv(z) > cam.near_z)) return false;
+    const S px = row_dot(R, m, cam.t[0]), py = row_dot(R + 3, m, cam.t[1]);
+    const S qn = dsqrt(q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3]);
+    const S w = q[0] / qn, x = q[1] / qn, y = q[2] / qn, zq = q[3] / qn;
+    // first two columns of the rotation of the normalised quaternion
+    const S a0 = 1.f - 2.f * (y * y + zq * zq), a1 = 2.f * (x * y + w * zq), a2 = 2.f * (x * zq - w * y);
+    const S b0 = 2.f * (x * y - w * zq), b1 = 1.f - 2.f * (x * x + zq * zq), b2 = 2.f * (y * zq + w * x);
+    const S su = dexp(lsu), sv = dexp(lsv);
+    S wu[3], wv[3];
+    for (int i = 0; i < 3; ++i) {
+        wu[i] = R[3 * i] * a0 + R[3 * i + 1] * a1 + R[3 * i + 2] * a2;
+        wv[i] = R[3 * i] * b0 + R[3 * i + 1] * b1 + R[3 * i + 2] * b2;
+    }
+    rec[0] = cam.fx * (su * wu[0]);
+    rec[1] = cam.fy * (su * wu[1]);
+    rec[2] = su * wu[2];
+    rec[3] = cam.fx * (sv * wv[0]);
+    rec[4] = cam.fy * (sv * wv[1]);
+    rec[5] = sv * wv[2];
+    const S zi = 1.f / z;
+    rec[6] = cam.fx * (px * zi) + cam.cx;
+    rec[7] = cam.fy * (py * zi) + cam.cy;
+    rec[8] = z;
+    const S e0 = rec[0] + (cam.cx - rec[6]) * rec[2], e1 = rec[3] + (cam.cx - rec[6]) * rec[5];
+    const S f0 = rec[1] + (cam.cy - rec[7]) * rec[2], f1 = rec[4] + (cam.cy - rec[7]) * rec[5];
+    const S c22 = 9.f * (rec[2] * rec[2] + rec[5] * rec[5]) - z * z;
+    if (!(fv(c22) < 0.f)) return false;
+    const S c02 = 9.f * (e0 * rec[2] + e1 * rec[5]), c12 = 9.f * (f0 * rec[2] + f1 * rec[5]);
+    rec[9] = rec[6] + c02 / c22;
+    rec[10] = rec[7] + c12 / c22;
+    const float c00 = 9.f * (fv(e0) * fv(e0) + fv(e1) * fv(e1)), c11 = 9.f * (fv(f0) * fv(f0) + fv(f1) * fv(f1));
+    const float nc22 = -fv(c22);
+    half[0] = sqrtf(fv(c02) * fv(c02) + c00 * nc22) / nc22;
+    half[1] = sqrtf(fv(c12) * fv(c12) + c11 * nc22) / nc22;
+    for (int i = 0; i < 11; ++i)
+        if (!isfinite(fv(rec[i]))) return false;
+    return isfinite(half[0]) && isfinite(half[1]);
+}
+
+// Binning radius: the larger half extent, at least the 3-sigma extent of the screen filter.
+__device__ __forceinline__ int surfel_radius(const float half[2]) {
+    const float r = ceilf(fmaxf(fmaxf(half[0], half[1]), 3.f * 0.70710678118654752f));
+    return r < 16777216.f ? (int)r : 0;
+}
+
+template <int DEG>
+__global__ void __launch_bounds__(128) k_preprocess2d(int n, const float* __restrict__ mean3d,
+                                                      const float* __restrict__ log_scale,
+                                                      const float* __restrict__ quat, const float* __restrict__ logit,
+                                                      const float* __restrict__ sh, const KernelCamera cam,
+                                                      float4* __restrict__ proj_rec, float* __restrict__ depth,
+                                                      int* __restrict__ radius, unsigned* __restrict__ tiles_touched,
+                                                      float4* __restrict__ rec2d) {
+    constexpr int K = (DEG + 1) * (DEG + 1);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const float m[3] = {mean3d[3 * i], mean3d[3 * i + 1], mean3d[3 * i + 2]};
+    const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
+    float rec[11], half[2];
+    depth[i] = row_dot(cam.R + 6, m, cam.t[2]);
+    bool ok = surfel_geometry<float>(m, log_scale[3 * i], log_scale[3 * i + 1], q, cam, rec, half);
+    int r = 0;
+    unsigned tt = 0;
+    if (ok) {
+        r = surfel_radius(half);
+        const Rect R = tile_rect(rec[9], rec[10], r, cam.tiles_x, cam.tiles_y);
+        ok = r > 0 && R.x0 <= R.x1;
+        if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+    }
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* o4 = rec2d + 4 * (size_t)i;
+    if (!ok) {
+        radius[i] = 0;
+        tiles_touched[i] = 0;
+        proj_rec[3 * (size_t)i] = z4;
+        proj_rec[3 * (size_t)i + 1] = z4;
+        proj_rec[3 * (size_t)i + 2] = z4;
+        o4[0] = z4; o4[1] = z4; o4[2] = z4; o4[3] = z4;
+        return;
+    }
+    const float op = 1.f / (1.f + expf(-logit[i]));
+    float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
+    const float dinv = rsqrtf(dx * dx + dy * dy + dz * dz);
+    float Y[16];
+    sh_basis<DEG>(dx * dinv, dy * dinv, dz * dinv, Y);
+    const float* shg = sh + (size_t)i * K * 3;
+    float col[3] = {0.5f, 0.5f, 0.5f};
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        col[0] += Y[k] * shg[3 * k];
+        col[1] += Y[k] * shg[3 * k + 1];
+        col[2] += Y[k] * shg[3 * k + 2];
+    }
+    proj_rec[3 * (size_t)i] = make_float4(rec[9], rec[10], 0.f, 0.f);  // the binning reads the box centre
+    proj_rec[3 * (size_t)i + 1] = z4;
+    proj_rec[3 * (size_t)i + 2] = z4;
+    radius[i] = r;
+    tiles_touched[i] = tt;
+    o4[0] = make_float4(rec[0], rec[1], rec[2], rec[3]);
+    o4[1] = make_float4(rec[4], rec[5], rec[6], rec[7]);
+    o4[2] = make_float4(rec[8], rec[9], rec[10], op);
+    o4[3] = make_float4(fmaxf(col[0], 0.f), fmaxf(col[1], 0.f), fmaxf(col[2], 0.f), 0.f);
+}
+
+// ---- render ------------------------------------------------------------------------------------
+
+constexpr int kB2 = 128;  // threads per tile (two pixels each) and records per batch
+constexpr float kAMin2 = 1.0f / 255.0f, kTMin2 = 1e-4f, kAMax2 = 0.99f;
+
+struct Stage2 {
+    float4 rec[2][kB2][4];
+    unsigned gidx[2][kB2];
+    float4 box[kB2];               // (xmin, xmax, ymin, ymax) where alpha can reach 1/255
+    unsigned short list[4][kB2];
+    uint64_t bar[2];
+};
+
+struct Stage2Bwd {
+    Stage2 st;
+    unsigned wmax[4];
+};
+
+// Screen box where the record's alpha can reach 1/255: the union of the box of the disk
+// u^2 + v^2 <= 2 tau (tau = ln(255 opacity)) and of the circle |(x, y) - c|^2 <= tau, widened
+// (tau by 0.1 % + 0.001, extents by 0.1 % + 0.01 px) so that rounding cannot drop a blended pair.
+// (pcx, pcy) is the camera's principal point; the disk box is taken relative to the projected
+// mean as in surfel_geometry.
+__device__ __forceinline__ float4 surfel_box_full(const float4 (&r)[4], float pcx, float pcy) {
+    const float inf = __int_as_float(0x7f800000);
+    const float o = r[2].w;
+    if (!(o * 1.00001f >= kAMin2)) return make_float4(inf, -inf, inf, -inf);
+    const float tau = logf(255.f * o * 1.00001f) * 1.001f + 0.001f;
+    const float Au = r[0].x, Bu = r[0].y, Cu = r[0].z, Av = r[0].w, Bv = r[1].x, Cv = r[1].y;
+    const float mx = r[1].z, my = r[1].w, z = r[2].x, cx = r[2].y, cy = r[2].z;
+    const float rr = 2.f * tau;
+    const float hc = sqrtf(tau) * 1.001f + 0.01f;
+    float4 b = make_float4(cx - hc, cx + hc, cy - hc, cy + hc);
+    const float c22 = rr * (Cu * Cu + Cv * Cv) - z * z;
+    if (!(c22 < 0.f)) return make_float4(-inf, inf, -inf, inf);
+    const float e0 = __fmaf_rn(pcx - mx, Cu, Au), e1 = __fmaf_rn(pcx - mx, Cv, Av);
+    const float f0 = __fmaf_rn(pcy - my, Cu, Bu), f1 = __fmaf_rn(pcy - my, Cv, Bv);
+    const float c02 = rr * (e0 * Cu + e1 * Cv), c12 = rr * (f0 * Cu + f1 * Cv);
+    const float c00 = rr * (e0 * e0 + e1 * e1), c11 = rr * (f0 * f0 + f1 * f1);
+    const float nc = -c22;
+    const float ox = mx - c02 / nc, oy = my - c12 / nc;
+    const float hx = sqrtf(c02 * c02 + c00 * nc) / nc * 1.001f + 0.01f;
+    const float hy = sqrtf(c12 * c12 + c11 * nc) / nc * 1.001f + 0.01f;
+    if (!(hx < inf && hy < inf)) return make_float4(-inf, inf, -inf, inf);
+    b.x = fminf(b.x, ox - hx);
+    b.y = fmaxf(b.y, ox + hx);
+    b.z = fminf(b.z, oy - hy);
+    b.w = fmaxf(b.w, oy + hy);
+    return b;
+}
+
+// Exponent of the surfel's weight at pixel centre (x, y) and the intermediates of its derivative.
+struct SurfelEval {
+    float power, p3, plp;
+    float hxu, hxv, hx1, hyu, hyv, hy1, det, u, v;
+    bool disk;  // the disk term is the larger one
+};
+
+__device__ __forceinline__ SurfelEval surfel_eval(const float4 (&r)[4], float pcx, float pcy, float x, float y) {
+    SurfelEval e;
+    const float ax = pcx - x, ay = pcy - y;
+    e.hxu = __fmaf_rn(ax, r[0].z, r[0].x);
+    e.hxv = __fmaf_rn(ax, r[1].y, r[0].w);
+    e.hx1 = r[2].x * (r[1].z - x);
+    e.hyu = __fmaf_rn(ay, r[0].z, r[0].y);
+    e.hyv = __fmaf_rn(ay, r[1].y, r[1].x);
+    e.hy1 = r[2].x * (r[1].w - y);
+    e.det = e.hxu * e.hyv - e.hxv * e.hyu;
+    if (e.det != 0.f) {
+        const float id = 1.f / e.det;
+        e.u = (e.hxv * e.hy1 - e.hx1 * e.hyv) * id;
+        e.v = (e.hx1 * e.hyu - e.hxu * e.hy1) * id;
+        e.p3 = -0.5f * __fmaf_rn(e.u, e.u, e.v * e.v);
+    } else {
+        e.u = e.v = 0.f;
+        e.p3 = -__int_as_float(0x7f800000);
+    }
+    const float dx = r[2].y - x, dy = r[2].z - y;
+    e.plp = -__fmaf_rn(dx, dx, dy * dy);
+    e.disk = e.p3 >= e.plp;
+    e.power = e.disk ? e.p3 : e.plp;
+    return e;
+}
+
+__device__ __forceinline__ void stage2_issue(Stage2& s, int slot, const float4* __restrict__ rec,
+                                             const unsigned* __restrict__ vals, int first, int n_in, unsigned n_gauss,
+                                             unsigned* err) {
+    const int t = threadIdx.x;
+    if (t < n_in) {
+        unsigned g = vals[first + t];
+        if (g >= n_gauss) {
+            atomicOr(err, kErrCheck);
+            g = 0;
+        }
+        s.gidx[slot][t] = g;
+        bulk_copy_g2s(&s.rec[slot][t][0], rec + 4 * (size_t)g, 64u, &s.bar[slot]);
+    }
+}
+
+__device__ __forceinline__ int compact2(Stage2& s, int n_in, int pos_limit, float wx0, float wx1, float wy0, float wy1,
+                                        int warp, int lane) {
+    int cnt = 0;
+    const int lim = min(n_in, pos_limit);
+#pragma unroll
+    for (int c = 0; c < kB2 / 32; ++c) {
+        const int j = c * 32 + lane;
+        bool hit = false;
+        if (j < lim) {
+            const float4 b = s.box[j];
+            hit = (b.y >= wx0) && (b.x <= wx1) && (b.w >= wy0) && (b.z <= wy1);
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        if (hit) s.list[warp][cnt + __popc(m & lanemask_lt())] = (unsigned short)j;
+        cnt += __popc(m);
+    }
+    __syncwarp();
+    return cnt;
+}
+
+__device__ __forceinline__ void blend2(const SurfelEval& e, const float4 (&r)[4], unsigned pos1, float& T, float& c0,
+                                       float& c1, float& c2, unsigned& last, bool& done) {
+    const float alpha = fminf(kAMax2, r[2].w * expf(e.power));
+    if (alpha >= kAMin2) {
+        const float test_T = T * (1.f - alpha);
+        if (test_T < kTMin2) {
+            done = true;
+        } else {
+            const float w = alpha * T;
+            c0 = __fmaf_rn(r[3].x, w, c0);
+            c1 = __fmaf_rn(r[3].y, w, c1);
+            c2 = __fmaf_rn(r[3].z, w, c2);
+            T = test_T;
+            last = pos1;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kB2) k_render2d_fwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
+                                                      const uint2* __restrict__ ranges, const KernelCamera cam,
+                                                      unsigned n_gauss, float* __restrict__ image,
+                                                      float* __restrict__ t_final, unsigned* __restrict__ n_contrib,
+                                                      unsigned spin_limit, unsigned* __restrict__ err) {
+    __shared__ Stage2 s;
+    const int tile = blockIdx.x;
+    const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 8 * (warp >> 1);
+    const int px = bx + (lane & 7), py0 = by + (lane >> 3), py1 = py0 + 4;
+    const bool in0 = px < cam.width && py0 < cam.height, in1 = px < cam.width && py1 < cam.height;
+    const float fpx = (float)px + 0.5f, fpy0 = (float)py0 + 0.5f, fpy1 = (float)py1 + 0.5f;
+    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 7.f;
+    const uint2 rg = ranges[tile];
+    const int start = (int)rg.x;
+    const int count = (int)(rg.y > rg.x ? rg.y - rg.x : 0);
+    const int nb = (count + kB2 - 1) / kB2;
+    float T0 = 1.f, c00 = 0.f, c01 = 0.f, c02 = 0.f, T1 = 1.f, c10 = 0.f, c11 = 0.f, c12 = 0.f;
+    unsigned last0 = 0, last1 = 0;
+    bool done0 = !in0, done1 = !in1;
+    if (nb > 0) {
+        if (threadIdx.x == 0) {
+            mbar_init(&s.bar[0], 1);
+            mbar_init(&s.bar[1], 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&s.bar[0], (unsigned)min(kB2, count) * 64u);
+            if (nb > 1) mbar_arrive_expect_tx(&s.bar[1], (unsigned)min(kB2, count - kB2) * 64u);
+        }
+        __syncthreads();
+        stage2_issue(s, 0, rec, vals, start, min(kB2, count), n_gauss, err);
+    }
+    int issued = nb > 0 ? 0 : -1, consumed = -1;
+    for (int b = 0; b < nb; ++b) {
+        const int slot = b & 1;
+        const int n_in = min(kB2, count - b * kB2);
+        if (b + 1 < nb) {
+            stage2_issue(s, slot ^ 1, rec, vals, start + (b + 1) * kB2, min(kB2, count - (b + 1) * kB2), n_gauss, err);
+            issued = b + 1;
+        }
+        const bool ok = mbar_wait_bounded(&s.bar[slot], (unsigned)(b >> 1) & 1u, spin_limit, err);
+        if (ok) consumed = b;
+        if (threadIdx.x < n_in) s.box[threadIdx.x] = surfel_box_full(s.rec[slot][threadIdx.x], cam.cx, cam.cy);
+        if (__syncthreads_or(!ok)) break;
+        const int nl = compact2(s, n_in, kB2, wx0, wx1, wy0, wy1, warp, lane);
+        for (int k = 0; k < nl; ++k) {
+            if (__all_sync(0xffffffffu, done0 && done1)) break;
+            const int j = s.list[warp][k];
+            const float4 r[4] = {s.rec[slot][j][0], s.rec[slot][j][1], s.rec[slot][j][2], s.rec[slot][j][3]};
+            const unsigned pos1 = (unsigned)(b * kB2 + j + 1);
+            if (!done0) blend2(surfel_eval(r, cam.cx, cam.cy, fpx, fpy0), r, pos1, T0, c00, c01, c02, last0, done0);
+            if (!done1) blend2(surfel_eval(r, cam.cx, cam.cy, fpx, fpy1), r, pos1, T1, c10, c11, c12, last1, done1);
+        }
+        if (threadIdx.x == 0 && b + 2 < nb)
+            mbar_arrive_expect_tx(&s.bar[slot], (unsigned)min(kB2, count - (b + 2) * kB2) * 64u);
+        if (__syncthreads_count(!(done0 && done1)) == 0) break;
+    }
+    for (int k = consumed + 1; k <= issued; ++k) mbar_wait_bounded(&s.bar[k & 1], (unsigned)(k >> 1) & 1u, 1u << 22, err);
+    const size_t plane = (size_t)cam.width * cam.height;
+    if (in0) {
+        const size_t pix = (size_t)py0 * cam.width + px;
+        image[pix] = c00 + T0 * cam.bg[0];
+        image[plane + pix] = c01 + T0 * cam.bg[1];
+        image[2 * plane + pix] = c02 + T0 * cam.bg[2];
+        t_final[pix] = T0;
+        n_contrib[pix] = last0;
+    }
+    if (in1) {
+        const size_t pix = (size_t)py1 * cam.width + px;
+        image[pix] = c10 + T1 * cam.bg[0];
+        image[plane + pix] = c11 + T1 * cam.bg[1];
+        image[2 * plane + pix] = c12 + T1 * cam.bg[2];
+        t_final[pix] = T1;
+        n_contrib[pix] = last1;
+    }
+}
+
+// One pixel's contribution to the 15 gradient components of a record (adjoint of surfel_eval
+// for the geometric fields; opacity; colour) and the step of its backward state.
+__device__ __forceinline__ void add_pixel2(float (&v)[16], const SurfelEval& e, const float4 (&r)[4], float alpha,
+                                           float oG, float G, float x, float y, float pcx, float pcy, float& T,
+                                           float& gS, float g0, float g1, float g2) {
+    const float inv = 1.f / (1.f - alpha);
+    T *= inv;
+    const float aT = alpha * T;
+    v[12] = __fmaf_rn(aT, g0, v[12]);
+    v[13] = __fmaf_rn(aT, g1, v[13]);
+    v[14] = __fmaf_rn(aT, g2, v[14]);
+    const float gc = __fmaf_rn(g0, r[3].x, __fmaf_rn(g1, r[3].y, g2 * r[3].z));
+    const float dalpha = __fmaf_rn(T, gc, -inv * gS);
+    gS = __fmaf_rn(aT, gc, gS);
+    if (!(oG <= kAMax2)) return;
+    const float dpow = oG * dalpha;
+    v[11] = __fmaf_rn(G, dalpha, v[11]);
+    if (!e.disk) {  // screen filter around the box centre: power = -(dx^2 + dy^2)
+        v[9] = __fmaf_rn(-2.f * (r[2].y - x), dpow, v[9]);
+        v[10] = __fmaf_rn(-2.f * (r[2].z - y), dpow, v[10]);
+        return;
+    }
+    // power = -(u^2 + v^2) / 2 with u = Nu / det, v = Nv / det
+    const float id = 1.f / e.det;
+    const float gu = -e.u * dpow * id, gv = -e.v * dpow * id;      // dL/dNu, dL/dNv
+    const float gdet = -(gu * e.u + gv * e.v);                      // dL/ddet
+    const float dhxu = -gv * e.hy1 + gdet * e.hyv;
+    const float dhxv = gu * e.hy1 - gdet * e.hyu;
+    const float dhx1 = -gu * e.hyv + gv * e.hyu;
+    const float dhyu = gv * e.hx1 - gdet * e.hxv;
+    const float dhyv = -gu * e.hx1 + gdet * e.hxu;
+    const float dhy1 = gu * e.hxv - gv * e.hxu;
+    const float ax = pcx - x, ay = pcy - y;
+    v[0] += dhxu;
+    v[1] += dhyu;
+    v[2] = __fmaf_rn(dhxu, ax, __fmaf_rn(dhyu, ay, v[2]));
+    v[3] += dhxv;
+    v[4] += dhyv;
+    v[5] = __fmaf_rn(dhxv, ax, __fmaf_rn(dhyv, ay, v[5]));
+    v[6] = __fmaf_rn(dhx1, r[2].x, v[6]);
+    v[7] = __fmaf_rn(dhy1, r[2].x, v[7]);
+    v[8] = __fmaf_rn(dhx1, r[1].z - x, __fmaf_rn(dhy1, r[1].w - y, v[8]));
+}
+
+// Transpose reduction of 16 components over the warp: after levels 16, 8, 4, 2 a lane keeps one
+// component summed over 16 lanes, and level 1 completes the sum; lanes 2k and 2k + 1 then hold
+// component k.
+__device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (b4 ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[i + 8], 16);
+    float c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (b3 ? a[i + 4] : a[i]) + __shfl_xor_sync(0xffffffffu, b3 ? a[i] : a[i + 4], 8);
+    float d[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) d[i] = (b2 ? c[i + 2] : c[i]) + __shfl_xor_sync(0xffffffffu, b2 ? c[i] : c[i + 2], 4);
+    float x = (b1 ? d[1] : d[0]) + __shfl_xor_sync(0xffffffffu, b1 ? d[0] : d[1], 2);
+    return x + __shfl_xor_sync(0xffffffffu, x, 1);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kB2) k_render2d_bwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
+                                                      const uint2* __restrict__ ranges, const KernelCamera cam,
+                                                      unsigned n_gauss, const float* __restrict__ dl_dimage,
+                                                      const float* __restrict__ t_final,
+                                                      const unsigned* __restrict__ n_contrib, float* __restrict__ grad,
+                                                      int thr, unsigned spin_limit, unsigned* __restrict__ err) {
+    __shared__ Stage2Bwd sm;
+    Stage2& s = sm.st;
+    const int tile = blockIdx.x;
+    const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 8 * (warp >> 1);
+    const int px = bx + (lane & 7), py0 = by + (lane >> 3), py1 = py0 + 4;
+    const float fpx = (float)px + 0.5f, fpy0 = (float)py0 + 0.5f, fpy1 = (float)py1 + 0.5f;
+    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 7.f;
+    const uint2 rg = ranges[tile];
+    const int start = (int)rg.x;
+    const int count = (int)(rg.y > rg.x ? rg.y - rg.x : 0);
+    const size_t plane = (size_t)cam.width * cam.height;
+    unsigned last0 = 0, last1 = 0;
+    float T0 = 1.f, T1 = 1.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f;
+    if (px < cam.width && py0 < cam.height) {
+        const size_t pix = (size_t)py0 * cam.width + px;
+        last0 = min(n_contrib[pix], (unsigned)count);
+        T0 = t_final[pix];
+        a0 = dl_dimage[pix]; a1 = dl_dimage[plane + pix]; a2 = dl_dimage[2 * plane + pix];
+    }
+    if (px < cam.width && py1 < cam.height) {
+        const size_t pix = (size_t)py1 * cam.width + px;
+        last1 = min(n_contrib[pix], (unsigned)count);
+        T1 = t_final[pix];
+        b0 = dl_dimage[pix]; b1 = dl_dimage[plane + pix]; b2 = dl_dimage[2 * plane + pix];
+    }
+    float gS0 = T0 * (a0 * cam.bg[0] + a1 * cam.bg[1] + a2 * cam.bg[2]);
+    float gS1 = T1 * (b0 * cam.bg[0] + b1 * cam.bg[1] + b2 * cam.bg[2]);
+    const unsigned wmax = __reduce_max_sync(0xffffffffu, max(last0, last1));
+    if (lane == 0) sm.wmax[warp] = wmax;
+    __syncthreads();
+    const unsigned tmax = max(max(sm.wmax[0], sm.wmax[1]), max(sm.wmax[2], sm.wmax[3]));
+    const int nb = ((int)tmax + kB2 - 1) / kB2;
+    if (nb > 0) {
+        const int bl = nb - 1;
+        if (threadIdx.x == 0) {
+            mbar_init(&s.bar[0], 1);
+            mbar_init(&s.bar[1], 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&s.bar[0], (unsigned)min(kB2, count - bl * kB2) * 64u);
+            if (nb > 1) mbar_arrive_expect_tx(&s.bar[1], (unsigned)kB2 * 64u);
+        }
+        __syncthreads();
+        stage2_issue(s, 0, rec, vals, start + bl * kB2, min(kB2, count - bl * kB2), n_gauss, err);
+    }
+    int issued = nb > 0 ? 0 : -1, consumed = -1;
+    for (int it = 0; it < nb; ++it) {
+        const int b = nb - 1 - it;
+        const int slot = it & 1;
+        const int n_in = min(kB2, count - b * kB2);
+        if (b > 0) {
+            stage2_issue(s, slot ^ 1, rec, vals, start + (b - 1) * kB2, kB2, n_gauss, err);
+            issued = it + 1;
+        }
+        const bool ok = mbar_wait_bounded(&s.bar[slot], (unsigned)(it >> 1) & 1u, spin_limit, err);
+        if (ok) consumed = it;
+        if (threadIdx.x < n_in) s.box[threadIdx.x] = surfel_box_full(s.rec[slot][threadIdx.x], cam.cx, cam.cy);
+        if (__syncthreads_or(!ok)) break;
+        const int pos_limit = (int)wmax - b * kB2;
+        const int nl = compact2(s, n_in, pos_limit, wx0, wx1, wy0, wy1, warp, lane);
+        for (int k = nl - 1; k >= 0; --k) {
+            const int j = s.list[warp][k];
+            const unsigned pos = (unsigned)(b * kB2 + j);
+            const float4 r[4] = {s.rec[slot][j][0], s.rec[slot][j][1], s.rec[slot][j][2], s.rec[slot][j][3]};
+            const SurfelEval e0 = surfel_eval(r, cam.cx, cam.cy, fpx, fpy0);
+            const SurfelEval e1 = surfel_eval(r, cam.cx, cam.cy, fpx, fpy1);
+            const float G0 = expf(e0.power), G1 = expf(e1.power);
+            const float oG0 = r[2].w * G0, oG1 = r[2].w * G1;
+            const float al0 = fminf(kAMax2, oG0), al1 = fminf(kAMax2, oG1);
+            const bool c0 = pos < last0 && al0 >= kAMin2;
+            const bool c1 = pos < last1 && al1 >= kAMin2;
+            const unsigned ballot = __ballot_sync(0xffffffffu, c0 || c1);
+            if (ballot == 0u) continue;
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = 0.f;
+            if (c0) add_pixel2(v, e0, r, al0, oG0, G0, fpx, fpy0, cam.cx, cam.cy, T0, gS0, a0, a1, a2);
+            if (c1) add_pixel2(v, e1, r, al1, oG1, G1, fpx, fpy1, cam.cx, cam.cy, T1, gS1, b0, b1, b2);
+            float* gp = grad + kS2 * (size_t)s.gidx[slot][j];
+            if (MODE == GS_BWD_DIRECT || (MODE == GS_BWD_ADAPTIVE && __popc(ballot) < thr)) {
+                if (c0 || c1) {
+                    red_add_global_v4(gp, v[0], v[1], v[2], v[3]);
+                    red_add_global_v4(gp + 4, v[4], v[5], v[6], v[7]);
+                    red_add_global_v4(gp + 8, v[8], v[9], v[10], v[11]);
+                    red_add_global_v4(gp + 12, v[12], v[13], v[14], 0.f);
+                }
+            } else {
+                const float x = warp_reduce16(v, lane);
+                if ((lane & 1) == 0 && (lane >> 1) < 15) red_add_global(gp + (lane >> 1), x);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && b >= 2) mbar_arrive_expect_tx(&s.bar[slot], (unsigned)kB2 * 64u);
+        __syncthreads();
+    }
+    for (int k = consumed + 1; k <= issued; ++k) mbar_wait_bounded(&s.bar[k & 1], (unsigned)(k >> 1) & 1u, 1u << 22, err);
+}
+
+// ---- preprocess backward -------------------------------------------------------------------------
+// The Jacobian of the geometric record with respect to (mean, log-scale u, log-scale v, quaternion)
+// by running surfel_geometry on dual numbers; opacity and colour as in the 3D preprocess backward.
+template <int DEG>
+__global__ void __launch_bounds__(128) k_preprocess2d_bwd(int n, const float* __restrict__ mean3d,
+                                                          const float* __restrict__ log_scale,
+                                                          const float* __restrict__ quat,
+                                                          const float* __restrict__ logit,
+                                                          const float* __restrict__ sh, const KernelCamera cam,
+                                                          const int* __restrict__ radius,
+                                                          const float* __restrict__ grad, float* __restrict__ d_mean3d,
+                                                          float* __restrict__ d_log_scale, float* __restrict__ d_quat,
+                                                          float* __restrict__ d_logit, float* __restrict__ d_sh,
+                                                          int accumulate) {
+    constexpr int K = (DEG + 1) * (DEG + 1);
+    using D = Df<9>;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float gr[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float dlg = 0.f;
+    float dsh[48];
+#pragma unroll
+    for (int k = 0; k < 3 * K; ++k) dsh[k] = 0.f;
+    if (radius[i] > 0) {
+        const float* gi = grad + kS2 * (size_t)i;
+        D m[3], q[4];
+        for (int k = 0; k < 3; ++k) m[k] = D::var(mean3d[3 * i + k], k);
+        const D lsu = D::var(log_scale[3 * i], 3), lsv = D::var(log_scale[3 * i + 1], 4);
+        for (int k = 0; k < 4; ++k) q[k] = D::var(quat[4 * i + k], 5 + k);
+        D rec[11];
+        float half[2];
+        if (surfel_geometry<D>(m, lsu, lsv, q, cam, rec, half)) {
+            for (int f = 0; f < 11; ++f) {
+                const float gf = gi[f];
+#pragma unroll
+                for (int v = 0; v < 9; ++v) gr[v] = __fmaf_rn(gf, rec[f].d[v], gr[v]);
+            }
+        }
+        const float op = 1.f / (1.f + expf(-logit[i]));
+        dlg = gi[11] * op * (1.f - op);
+        // colour = sum_k Y_k sh_k + 0.5 clamped at 0; the direction depends on the mean
+        float vx = mean3d[3 * i] - cam.campos[0], vy = mean3d[3 * i + 1] - cam.campos[1];
+        float vz = mean3d[3 * i + 2] - cam.campos[2];
+        const float vinv = rsqrtf(vx * vx + vy * vy + vz * vz);
+        const float ux = vx * vinv, uy = vy * vinv, uz = vz * vinv;
+        float Y[16];
+        sh_basis<DEG>(ux, uy, uz, Y);
+        const float* shg = sh + (size_t)i * K * 3;
+        float col[3] = {0.5f, 0.5f, 0.5f};
+        for (int k = 0; k < K; ++k)
+            for (int c = 0; c < 3; ++c) col[c] += Y[k] * shg[3 * k + c];
+        float dc[3];
+        for (int c = 0; c < 3; ++c) dc[c] = col[c] < 0.f ? 0.f : gi[12 + c];
+        float wk[16];
+        for (int k = 0; k < K; ++k) {
+            wk[k] = shg[3 * k] * dc[0] + shg[3 * k + 1] * dc[1] + shg[3 * k + 2] * dc[2];
+            for (int c = 0; c < 3; ++c) dsh[3 * k + c] = Y[k] * dc[c];
+        }
+        if (DEG > 0) {
+            float gd[3] = {0.f, 0.f, 0.f};
+            sh_basis_grad<DEG>(ux, uy, uz, wk, gd);
+            const float dot = gd[0] * ux + gd[1] * uy + gd[2] * uz;
+            gr[0] += (gd[0] - dot * ux) * vinv;
+            gr[1] += (gd[1] - dot * uy) * vinv;
+            gr[2] += (gd[2] - dot * uz) * vinv;
+        }
+    }
+    float* dm = d_mean3d + 3 * (size_t)i;
+    float* dl = d_log_scale + 3 * (size_t)i;
+    float* dq = d_quat + 4 * (size_t)i;
+    float* ds = d_sh + (size_t)i * K * 3;
+    if (accumulate) {
+        for (int k = 0; k < 3; ++k) dm[k] += gr[k];
+        dl[0] += gr[3];
+        dl[1] += gr[4];
+        for (int k = 0; k < 4; ++k) dq[k] += gr[5 + k];
+        d_logit[i] += dlg;
+        for (int k = 0; k < 3 * K; ++k) ds[k] += dsh[k];
+    } else {
+        for (int k = 0; k < 3; ++k) dm[k] = gr[k];
+        dl[0] = gr[3];
+        dl[1] = gr[4];
+        dl[2] = 0.f;
+        for (int k = 0; k < 4; ++k) dq[k] = gr[5 + k];
+        d_logit[i] = dlg;
+        for (int k = 0; k < 3 * K; ++k) ds[k] = dsh[k];
+    }
+}
+
+// ---- launchers -------------------------------------------------------------------------------------
+
+cudaError_t launch_preprocess2d(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
+                                float* rec2d, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int blocks = (n + 127) / 128;
+    float4* pr = reinterpret_cast<float4*>(out.rec);
+    float4* r2 = reinterpret_cast<float4*>(rec2d);
+    unsigned* tt = out.tiles_touched;
+    count_launches(1);
+    switch (deg) {
+        case 0: k_preprocess2d<0><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, pr, out.depth, out.radius, tt, r2); break;
+        case 1: k_preprocess2d<1><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, pr, out.depth, out.radius, tt, r2); break;
+        case 2: k_preprocess2d<2><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, pr, out.depth, out.radius, tt, r2); break;
+        default: k_preprocess2d<3><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, pr, out.depth, out.radius, tt, r2); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_render2d_fwd(const float* rec2d, unsigned n, const unsigned* vals, const unsigned* ranges,
+                                const KernelCamera& cam, float* image, float* t_final, unsigned* n_contrib,
+                                unsigned spin_limit, unsigned* err, cudaStream_t st) {
+    const int tiles = cam.tiles_x * cam.tiles_y;
+    count_launches(1);
+    k_render2d_fwd<<<tiles, kB2, 0, st>>>(reinterpret_cast<const float4*>(rec2d), vals,
+                                          reinterpret_cast<const uint2*>(ranges), cam, n, image, t_final, n_contrib,
+                                          spin_limit, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_render2d_bwd(int mode, int thr, const float* rec2d, unsigned n, const unsigned* vals,
+                                const unsigned* ranges, const KernelCamera& cam, const float* dl_dimage,
+                                const float* t_final, const unsigned* n_contrib, float* grad, unsigned spin_limit,
+                                unsigned* err, cudaStream_t st) {
+    const int tiles = cam.tiles_x * cam.tiles_y;
+    const float4* r = reinterpret_cast<const float4*>(rec2d);
+    const uint2* rg = reinterpret_cast<const uint2*>(ranges);
+    count_launches(1);
+    if (mode == GS_BWD_DIRECT)
+        k_render2d_bwd<GS_BWD_DIRECT><<<tiles, kB2, 0, st>>>(r, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad, thr, spin_limit, err);
+    else if (mode == GS_BWD_WARP)
+        k_render2d_bwd<GS_BWD_WARP><<<tiles, kB2, 0, st>>>(r, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad, thr, spin_limit, err);
+    else
+        k_render2d_bwd<GS_BWD_ADAPTIVE><<<tiles, kB2, 0, st>>>(r, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad, thr, spin_limit, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess2d_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
+                                    const float* grad, float* dm, float* dls, float* dq, float* dlg, float* dsh,
+                                    int accumulate, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int blocks = (n + 127) / 128;
+    count_launches(1);
+    switch (deg) {
+        case 0: k_preprocess2d_bwd<0><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, grad, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 1: k_preprocess2d_bwd<1><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, grad, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 2: k_preprocess2d_bwd<2><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, grad, dm, dls, dq, dlg, dsh, accumulate); break;
+        default: k_preprocess2d_bwd<3><<<blocks, 128, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, grad, dm, dls, dq, dlg, dsh, accumulate); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gs

@@ -445,4 +445,82 @@ int gs_loss_l1_dssim(const float* image, const float* target, int32_t width, int
     return e ? cuda_fail(e, "gs_loss_l1_dssim") : GS_OK;
 }
 
+int gs_preprocess2d(const gs_params* p, const gs_camera* cam, const gs_options* opt, gs_proj* out, float* rec2d,
+                    void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_params(p))) return s;
+    if ((s = check_proj(out, p->n))) return s;
+    if (p->n > 0 && (!rec2d || !aligned(rec2d, 16))) return fail(GS_ERR_ARG, "rec2d NULL or not 16-byte aligned");
+    cudaError_t e = launch_preprocess2d(o.deg, (int)p->n, *p, kc, *out, rec2d, as_stream(stream));
+    return e ? cuda_fail(e, "gs_preprocess2d") : GS_OK;
+}
+
+int gs_render2d_fwd(const float* rec2d, int64_t n, const uint32_t* vals, const uint32_t* tile_ranges,
+                    const gs_camera* cam, const gs_options* opt, float* image, float* t_final, uint32_t* n_contrib,
+                    void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc))) return s;
+    if (n < 0 || n > 0x7fffffffll) return fail(GS_ERR_ARG, "n = %lld outside 0..2^31-1", (long long)n);
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or misaligned");
+    if (!image || !t_final || !n_contrib || !aligned(image, 4) || !aligned(t_final, 4) || !aligned(n_contrib, 4))
+        return fail(GS_ERR_ARG, "image / t_final / n_contrib NULL or misaligned");
+    if (n > 0 && (!vals || !aligned(vals, 4) || !rec2d || !aligned(rec2d, 16)))
+        return fail(GS_ERR_ARG, "vals or rec2d NULL or misaligned (rec2d needs 16 bytes)");
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaError_t e = launch_render2d_fwd(rec2d, (unsigned)n, vals, tile_ranges, kc, image, t_final, n_contrib, o.spin,
+                                        err, as_stream(stream));
+    return e ? cuda_fail(e, "gs_render2d_fwd") : GS_OK;
+}
+
+int gs_render2d_bwd(const float* rec2d, int64_t n, const uint32_t* vals, const uint32_t* tile_ranges,
+                    const gs_camera* cam, const gs_options* opt, const float* dl_dimage, const float* t_final,
+                    const uint32_t* n_contrib, float* grad2d, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc))) return s;
+    if (o.bwd_mode == GS_BWD_SM) return fail(GS_ERR_ARG, "the surfel backward has no GS_BWD_SM mode");
+    if (n < 0 || n > 0x7fffffffll) return fail(GS_ERR_ARG, "n = %lld outside 0..2^31-1", (long long)n);
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or misaligned");
+    if (!dl_dimage || !t_final || !n_contrib || !aligned(dl_dimage, 4) || !aligned(t_final, 4) ||
+        !aligned(n_contrib, 4))
+        return fail(GS_ERR_ARG, "dl_dimage / t_final / n_contrib NULL or misaligned");
+    if (n > 0 && (!vals || !aligned(vals, 4) || !rec2d || !aligned(rec2d, 16) || !grad2d || !aligned(grad2d, 16)))
+        return fail(GS_ERR_ARG, "vals, rec2d or grad2d NULL or misaligned (rec2d and grad2d need 16 bytes)");
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaStream_t st = as_stream(stream);
+    if (n > 0) {
+        cudaError_t e = cudaMemsetAsync(grad2d, 0, (size_t)n * 16 * sizeof(float), st);
+        if (e) return cuda_fail(e, "gs_render2d_bwd: zero grad2d");
+    }
+    cudaError_t e = launch_render2d_bwd(o.bwd_mode, o.thr, rec2d, (unsigned)n, vals, tile_ranges, kc, dl_dimage, t_final,
+                                        n_contrib, grad2d, o.spin, err, st);
+    return e ? cuda_fail(e, "gs_render2d_bwd") : GS_OK;
+}
+
+int gs_preprocess2d_bwd(const gs_params* p, const gs_camera* cam, const gs_options* opt, const gs_proj* proj,
+                        const float* grad2d, float* d_mean3d, float* d_log_scale, float* d_quat, float* d_opacity_logit,
+                        float* d_sh, int32_t accumulate, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_params(p))) return s;
+    if ((s = check_proj(proj, p->n))) return s;
+    if (p->n > 0) {
+        if (!grad2d || !aligned(grad2d, 16)) return fail(GS_ERR_ARG, "grad2d NULL or not 16-byte aligned");
+        const void* outs[5] = {d_mean3d, d_log_scale, d_quat, d_opacity_logit, d_sh};
+        for (const void* q : outs)
+            if (!q || !aligned(q, 4)) return fail(GS_ERR_ARG, "a gradient output is NULL or misaligned");
+    }
+    cudaError_t e = launch_preprocess2d_bwd(o.deg, (int)p->n, *p, kc, proj->radius, grad2d, d_mean3d, d_log_scale,
+                                            d_quat, d_opacity_logit, d_sh, accumulate, as_stream(stream));
+    return e ? cuda_fail(e, "gs_preprocess2d_bwd") : GS_OK;
+}
+
 }  // extern "C"

@@ -62,5 +62,17 @@ cudaError_t launch_densify_stats(int deg, int n, const int* radius, const float*
 size_t loss_workspace_bytes(int width, int height);
 cudaError_t launch_loss_l1_dssim(const float* img, const float* tgt, int width, int height, float lam, void* ws,
                                  float* loss, float* dl, cudaStream_t st);
+cudaError_t launch_preprocess2d(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
+                                float* rec2d, cudaStream_t st);
+cudaError_t launch_render2d_fwd(const float* rec2d, unsigned n, const unsigned* vals, const unsigned* ranges,
+                                const KernelCamera& cam, float* image, float* t_final, unsigned* n_contrib,
+                                unsigned spin_limit, unsigned* err, cudaStream_t st);
+cudaError_t launch_render2d_bwd(int mode, int thr, const float* rec2d, unsigned n, const unsigned* vals,
+                                const unsigned* ranges, const KernelCamera& cam, const float* dl_dimage,
+                                const float* t_final, const unsigned* n_contrib, float* grad, unsigned spin_limit,
+                                unsigned* err, cudaStream_t st);
+cudaError_t launch_preprocess2d_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
+                                    const float* grad, float* dm, float* dls, float* dq, float* dlg, float* dsh,
+                                    int accumulate, cudaStream_t st);
 
 }  // namespace gs

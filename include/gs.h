@@ -266,6 +266,40 @@ size_t gs_loss_workspace_bytes(int32_t width, int32_t height);
 int gs_loss_l1_dssim(const float* image, const float* target, int32_t width, int32_t height, float lambda,
                      void* workspace, size_t workspace_bytes, float* loss, float* dl_dimage, void* stream);
 
+/* ---- surfels: 2D Gaussian splatting --------------------------------------------------------
+ * The rendering pipeline of 2D Gaussian splatting, one of the four pipelines Odin trains (Odin:
+ * Primitive-Level Synchronization for Distributed Point-Based Neural Rendering, Summary). Each
+ * Gaussian is a flat disk, P(u, v) = mean + s_u u t_u + s_v v t_v (t_u, t_v the first two columns
+ * of its rotation, s = exp of log_scale[0..1]; log_scale[2] is unused). A pixel (x, y) weighs it by
+ * max(exp(-(u^2 + v^2)/2), exp(-|(x, y) - c|^2)) with (u, v) where the pixel's ray meets the disk's
+ * plane and c the centre of the screen box of its 3-sigma disk; alpha, thresholds, termination and
+ * blending are those of gs_render_fwd. The binning is gs_bin_and_sort on the gs_proj that
+ * gs_preprocess2d fills (box centre as mean, radius = ceil of the larger box half extent, at least
+ * 3 sqrt(1/2)).
+ *
+ * Surfel record rec2d [N][16] float32, 16-byte aligned: A_u = s_u fx (W t_u)_x, B_u = s_u fy
+ * (W t_u)_y, C_u = s_u (W t_u)_z, A_v, B_v, C_v likewise for t_v, m_x, m_y (projected mean), z_c
+ * (its depth), c_x, c_y (box centre), opacity, r, g, b, 0. Culled Gaussians: radius 0, zero record.
+ * Surfel gradients grad2d [N][16] float32: dL/d(the first 15 record fields).                     */
+int gs_preprocess2d(const gs_params* p, const gs_camera* cam, const gs_options* opt, gs_proj* out,
+                    float* rec2d, void* stream);
+/* Forward of the surfels listed by gs_bin_and_sort (n = number of records). Outputs as
+ * gs_render_fwd. Errors: GS_ERR_ARG, GS_ERR_CUDA; staging timeouts in the device error word.    */
+int gs_render2d_fwd(const float* rec2d, int64_t n, const uint32_t* vals, const uint32_t* tile_ranges,
+                    const gs_camera* cam, const gs_options* opt, float* image, float* t_final,
+                    uint32_t* n_contrib, void* stream);
+/* Backward of gs_render2d_fwd: grad2d [N][16] = dL/d(record fields 0..14), zeroed first by the
+ * callee. bwd_mode DIRECT, WARP or ADAPTIVE (SM is rejected). Errors as gs_render_bwd.           */
+int gs_render2d_bwd(const float* rec2d, int64_t n, const uint32_t* vals, const uint32_t* tile_ranges,
+                    const gs_camera* cam, const gs_options* opt, const float* dl_dimage,
+                    const float* t_final, const uint32_t* n_contrib, float* grad2d, void* stream);
+/* Chain rule from the surfel gradients to the parameters, as gs_preprocess_bwd (d_log_scale[2]
+ * is 0). proj: the gs_proj gs_preprocess2d filled (radius marks the visible surfels).          */
+int gs_preprocess2d_bwd(const gs_params* p, const gs_camera* cam, const gs_options* opt,
+                        const gs_proj* proj, const float* grad2d, float* d_mean3d, float* d_log_scale,
+                        float* d_quat, float* d_opacity_logit, float* d_sh, int32_t accumulate,
+                        void* stream);
+
 /* Size of the device workspace that gs_bin_and_sort_static uses instead of a caller buffer. */
 #define GS_STATIC_SORT_WORKSPACE_BYTES (32u << 20)
 
