@@ -426,29 +426,41 @@ def run_ours(args, rank, world, local_rank):
         g2d = torch.empty((scene.n, 16), dtype=torch.float32, device=dev)
         c0 = cams[0]
 
-        def step2d():
+        def step2d(ev=None):
+            mark = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
             proj2, _ = api.gs_preprocess2d(params, c0, opt, out=bufs.proj, rec2d=rec2d)
+            mark(0)
             image2, t2, nc2, dl2, ranges2 = bufs.image_buffers(c0.width, c0.height)
             b2 = api.gs_bin_and_sort(proj2, c0, opt, buffers=bufs.sort, ranges=ranges2, want_keys=False)
+            mark(1)
             api.gs_render2d_fwd(rec2d, b2.vals, b2.ranges, c0, opt, out=(image2, t2, nc2))
+            mark(2)
             torch.sub(image2, target[0], out=dl2)
+            mark(3)
             api.gs_render2d_bwd(rec2d, b2.vals, b2.ranges, c0, opt, dl2, t2, nc2, grad2d=g2d)
+            mark(4)
             api.gs_preprocess2d_bwd(params, c0, opt, proj2, g2d, out=grads)
             return b2.n_dup
         for _ in range(3):
             step2d()
-        s_ms2 = []
+        s_ms2, parts = [], []
         for _ in range(max(3, args.steps // 2)):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             e0.record(stream)
-            d2 = step2d()
+            d2 = step2d(ev)
             e1.record(stream)
             torch.cuda.synchronize()
             s_ms2.append(e0.elapsed_time(e1))
+            marks = [e0] + ev + [e1]
+            parts.append([marks[i].elapsed_time(marks[i + 1]) for i in range(6)])
         m2 = sum(s_ms2) / len(s_ms2)
-        extras["surfel_step"] = {"ms_per_view": m2, "mpix_per_s": cam.width * cam.height / (m2 / 1e3) / 1e6,
-                                 "duplicates": int(d2)}
+        pm = [sum(p[i] for p in parts) / len(parts) for i in range(6)]
+        extras["surfel_step"] = {"ms_per_view": m2, "mpix_per_s": c0.width * c0.height / (m2 / 1e3) / 1e6,
+                                 "duplicates": int(d2),
+                                 "stage_ms": dict(zip(["preprocess", "bin_and_sort", "render_fwd", "dl_dimage",
+                                                       "render_bwd", "preprocess_bwd"], pm))}
         assert api.gs_device_error() == 0
 
     # ---- roofline of the dominant kernel (the backward)

@@ -1,14 +1,13 @@
 """GPU parity of the surfel (2D Gaussian splatting) path against the float64 oracle, stage by stage
 as for the 3D path: each stage gets the oracle's previous outputs rounded to float32.
 
-Tolerances, from the float32 arithmetic of the surfel path: record fields are products and
-quotients of a few float32 values (relative 1e-5 of the field's scale over the scene, i.e. of its
-largest magnitude); the box centre is the projected mean plus a quotient (1e-3 px, it enters only
-through the tile rectangle and the screen filter); the ray-plane intersection solves a 2x2 system
-whose float32 error grows with its condition, so pixels are compared within 1e-4 where the oracle
-flags no decision within 1e-4 of its threshold; gradients within 1e-3 of each tensor's largest
-magnitude with the upstream gradient zeroed on flagged pixels (a decision that legitimately differs
-moves every gradient of its pixel).
+Tolerances: the step's bars, as for the 3D path: pixels within 1e-5 where the oracle flags no
+alpha or termination decision within 1e-4 of its threshold, and every gradient tensor within 1e-4
+of its largest magnitude, with the upstream gradient zeroed on flagged pixels (a decision that
+legitimately differs moves every gradient of its pixel). Record fields are products and quotients
+of a few float32 values: 2e-6 of each field's largest magnitude over the scene; the box centre is
+the projected mean plus a quotient of dual-conic entries and enters only through the tile
+rectangle and the screen filter: 1e-3 px.
 """
 import functools
 
@@ -75,7 +74,7 @@ def test_surfel_preprocess_matches_oracle(name):
     o = pre["rec2d"]
     for f in range(9):  # A, B, C (u, v), m, z
         scale = np.abs(o[vis, f]).max()
-        assert np.abs(r[vis, f] - o[vis, f]).max() <= 1e-5 * scale, (name, f)
+        assert np.abs(r[vis, f] - o[vis, f]).max() <= 2e-6 * scale, (name, f)
     assert np.abs(r[vis, 9:11] - o[vis, 9:11]).max() <= 1e-3  # box centre (px)
     assert np.allclose(r[vis, 11:15], o[vis, 11:15], rtol=1e-5, atol=1e-6)  # opacity, colour
     assert api.gs_device_error() == 0
@@ -93,7 +92,7 @@ def test_surfel_render_forward_matches_oracle(name):
     ok = (fwd["pix_flags"] & 3) == 0
     assert (~ok).sum() <= max(3, 1e-2 * ok.size)
     err = np.abs(image.cpu().numpy() - fwd["image"])
-    assert err[:, ok].max() <= 1e-4, err[:, ok].max()
+    assert err[:, ok].max() <= 1e-5, err[:, ok].max()
     assert np.array_equal(n_contrib.cpu().numpy().astype(np.uint32)[ok], fwd["n_contrib"][ok])
     assert api.gs_device_error() == 0
 
@@ -114,7 +113,7 @@ def test_surfel_render_backward_matches_oracle(name, mode):
     for lo, hi in [(0, 3), (3, 6), (6, 8), (8, 9), (9, 11), (11, 12), (12, 15)]:
         scale = np.abs(ref[:, lo:hi]).max()
         err = np.abs(g[:, lo:hi] - ref[:, lo:hi]).max()
-        assert err <= 1e-3 * scale + 1e-12, (name, mode, lo, err / max(scale, 1e-30))
+        assert err <= 1e-4 * scale + 1e-12, (name, mode, lo, err / max(scale, 1e-30))
     assert np.all(g[:, 15] == 0)
     assert api.gs_device_error() == 0
 
@@ -134,5 +133,5 @@ def test_surfel_preprocess_backward_matches_oracle(name):
         a = out[k].cpu().numpy().astype(np.float64)
         b = g3[ok]
         scale = np.abs(b).max()
-        assert np.abs(a - b).max() <= 1e-3 * scale + 1e-12, (name, k, np.abs(a - b).max() / max(scale, 1e-30))
+        assert np.abs(a - b).max() <= 1e-4 * scale + 1e-12, (name, k, np.abs(a - b).max() / max(scale, 1e-30))
     assert api.gs_device_error() == 0
