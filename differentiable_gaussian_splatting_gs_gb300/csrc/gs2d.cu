@@ -230,14 +230,40 @@ __global__ void __launch_bounds__(128) k_preprocess2d(int n, const float* __rest
 }
 
 // ---- render ------------------------------------------------------------------------------------
+//
+// Plane form. With dx = x - m_x, dy = y - m_y the two planes of a pixel are h_x = (e0 - C_u dx,
+// e1 - C_v dx, -z dx) and h_y = (f0 - C_u dy, f1 - C_v dy, -z dy), where (e0, e1) and (f0, f1) are
+// the planes' first two entries at the projected mean. Solving them by Cramer's rule, the dx dy
+// terms of the 2x2 determinant cancel and the intersection is a projective map of the pixel:
+//   (u, v) = z (f1 dx - e1 dy, e0 dy - f0 dx) / det,   det = d0 + dq dx + dp dy,
+//   d0 = e0 f1 - e1 f0, dq = C_v f0 - C_u f1, dp = e1 C_u - e0 C_v.
+// Each staged record is rewritten once per tile into this form, so that a pixel costs a few
+// multiply-adds, one reciprocal and the squares; the same algebra gives the backward its sums
+// (see k_render2d_bwd) and k_render2d_grad_fields turns them into record gradients.
+//
+// Precision. For a surfel seen nearly edge-on the numerators cancel: far from the mean along the
+// ellipse's long axis |f1 dx| and |e1 dy| are hundreds of times |f1 dx - e1 dy|, so float32
+// coefficients would cost that factor in relative accuracy (1e-5 in alpha on the test scenes).
+// The coefficients z (f1, -e1, -f0, e0) are therefore kept as double-floats (head + tail) and each
+// numerator is formed with exact products, and d0, dq, dp are formed from unrounded plane entries;
+// alpha then agrees with a float64 evaluation of the same record to about 2e-7.
 
 constexpr int kB2 = 128;  // threads per tile (two pixels each) and records per batch
 constexpr float kAMin2 = 1.0f / 255.0f, kTMin2 = 1e-4f, kAMax2 = 0.99f;
+constexpr float kNegLog2e = -1.4426950408889634f;
+// kappa = sqrt(log2(e) / 2): det is stored divided by kappa, so that -(N_u^2 + N_v^2) / det'^2 is
+// the disk term in base 2
+constexpr float kInvKappa = 1.1774100225154747f;   // 1 / kappa
+constexpr float kInvKappa2 = 1.3862943611198906f;  // 1 / kappa^2 = 2 ln 2
+constexpr float kInvKappa3 = 1.6322368749392457f;  // 1 / kappa^3
 
 struct Stage2 {
     float4 rec[2][kB2][4];
+    float4 tail[2][kB2];  // tails of the numerator coefficients r[0]
     unsigned gidx[2][kB2];
-    float4 box[kB2];               // (xmin, xmax, ymin, ymax) where alpha can reach 1/255
+    float4 cull_a[kB2];  // (o_x, o_y, B / C, B / A) of the disk's alpha ellipse (conic A, B, C)
+    float4 cull_b[kB2];  // (D / A, L / A) of that ellipse, filter centre (c_x, c_y)
+    float cull_tau[kB2]; // squared radius of the filter's alpha disk
     unsigned short list[4][kB2];
     uint64_t bar[2];
 };
@@ -247,70 +273,114 @@ struct Stage2Bwd {
     unsigned wmax[4];
 };
 
-// Screen box where the record's alpha can reach 1/255: the union of the box of the disk
-// u^2 + v^2 <= 2 tau (tau = ln(255 opacity)) and of the circle |(x, y) - c|^2 <= tau, widened
-// (tau by 0.1 % + 0.001, extents by 0.1 % + 0.01 px) so that rounding cannot drop a blended pair.
-// (pcx, pcy) is the camera's principal point; the disk box is taken relative to the projected
-// mean as in surfel_geometry.
-__device__ __forceinline__ float4 surfel_box_full(const float4 (&r)[4], float pcx, float pcy) {
-    const float inf = __int_as_float(0x7f800000);
-    const float o = r[2].w;
-    if (!(o * 1.00001f >= kAMin2)) return make_float4(inf, -inf, inf, -inf);
-    const float tau = logf(255.f * o * 1.00001f) * 1.001f + 0.001f;
-    const float Au = r[0].x, Bu = r[0].y, Cu = r[0].z, Av = r[0].w, Bv = r[1].x, Cv = r[1].y;
-    const float mx = r[1].z, my = r[1].w, z = r[2].x, cx = r[2].y, cy = r[2].z;
-    const float rr = 2.f * tau;
-    const float hc = sqrtf(tau) * 1.001f + 0.01f;
-    float4 b = make_float4(cx - hc, cx + hc, cy - hc, cy + hc);
-    const float c22 = rr * (Cu * Cu + Cv * Cv) - z * z;
-    if (!(c22 < 0.f)) return make_float4(-inf, inf, -inf, inf);
-    const float e0 = __fmaf_rn(pcx - mx, Cu, Au), e1 = __fmaf_rn(pcx - mx, Cv, Av);
-    const float f0 = __fmaf_rn(pcy - my, Cu, Bu), f1 = __fmaf_rn(pcy - my, Cv, Bv);
-    const float c02 = rr * (e0 * Cu + e1 * Cv), c12 = rr * (f0 * Cu + f1 * Cv);
-    const float c00 = rr * (e0 * e0 + e1 * e1), c11 = rr * (f0 * f0 + f1 * f1);
-    const float nc = -c22;
-    const float ox = mx - c02 / nc, oy = my - c12 / nc;
-    const float hx = sqrtf(c02 * c02 + c00 * nc) / nc * 1.001f + 0.01f;
-    const float hy = sqrtf(c12 * c12 + c11 * nc) / nc * 1.001f + 0.01f;
-    if (!(hx < inf && hy < inf)) return make_float4(-inf, inf, -inf, inf);
-    b.x = fminf(b.x, ox - hx);
-    b.y = fmaxf(b.y, ox + hx);
-    b.z = fminf(b.z, oy - hy);
-    b.w = fmaxf(b.w, oy + hy);
-    return b;
-}
-
-// Exponent of the surfel's weight at pixel centre (x, y) and the intermediates of its derivative.
-struct SurfelEval {
-    float power, p3, plp;
-    float hxu, hxv, hx1, hyu, hyv, hy1, det, u, v;
-    bool disk;  // the disk term is the larger one
+// Double-float values (h + l, |l| <= ulp(h) / 2) for the plane form: the determinants d0, dq, dp
+// cancel for surfels seen nearly edge-on, so they are formed from unrounded plane entries
+// (Knuth's two-sum, the fused multiply-add exact product) and rounded once.
+struct F2 {
+    float h, l;
 };
 
-__device__ __forceinline__ SurfelEval surfel_eval(const float4 (&r)[4], float pcx, float pcy, float x, float y) {
-    SurfelEval e;
-    const float ax = pcx - x, ay = pcy - y;
-    e.hxu = __fmaf_rn(ax, r[0].z, r[0].x);
-    e.hxv = __fmaf_rn(ax, r[1].y, r[0].w);
-    e.hx1 = r[2].x * (r[1].z - x);
-    e.hyu = __fmaf_rn(ay, r[0].z, r[0].y);
-    e.hyv = __fmaf_rn(ay, r[1].y, r[1].x);
-    e.hy1 = r[2].x * (r[1].w - y);
-    e.det = e.hxu * e.hyv - e.hxv * e.hyu;
-    if (e.det != 0.f) {
-        const float id = 1.f / e.det;
-        e.u = (e.hxv * e.hy1 - e.hx1 * e.hyv) * id;
-        e.v = (e.hx1 * e.hyu - e.hxu * e.hy1) * id;
-        e.p3 = -0.5f * __fmaf_rn(e.u, e.u, e.v * e.v);
+__device__ __forceinline__ F2 two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+
+// a + b c with b a double-float.
+__device__ __forceinline__ F2 plane_entry(float a, F2 b, float c) {
+    const float ph = b.h * c;
+    const float pl = __fmaf_rn(b.h, c, -ph) + b.l * c;
+    const F2 t = two_sum(a, ph);
+    const float l = t.l + pl;
+    const float h = t.h + l;
+    return {h, l - (h - t.h)};
+}
+
+// x y - z w of double-floats, rounded once up to the tails' second-order terms.
+__device__ __forceinline__ float det2(F2 x, F2 y, F2 z, F2 w) {
+    const float p = x.h * y.h, q = z.h * w.h;
+    const float pe = __fmaf_rn(x.h, y.h, -p), qe = __fmaf_rn(z.h, w.h, -q);
+    const float tail = (pe - qe) + (x.h * y.l + x.l * y.h) - (z.h * w.l + z.l * w.h);
+    return (p - q) + tail;
+}
+
+struct SurfelPlanes {
+    F2 e0, e1, f0, f1;
+    float d0, dq, dp;
+};
+
+// The plane form of a record (fields A_u, B_u, C_u, A_v, B_v, C_v, m_x, m_y), (pcx, pcy) the
+// principal point.
+__device__ __forceinline__ SurfelPlanes surfel_planes(float Au, float Bu, float Cu, float Av, float Bv, float Cv,
+                                                      float mx, float my, float pcx, float pcy) {
+    const F2 ax = two_sum(pcx, -mx), ay = two_sum(pcy, -my);
+    const F2 e0 = plane_entry(Au, ax, Cu), e1 = plane_entry(Av, ax, Cv);
+    const F2 f0 = plane_entry(Bu, ay, Cu), f1 = plane_entry(Bv, ay, Cv);
+    const F2 cu = {Cu, 0.f}, cv = {Cv, 0.f};
+    SurfelPlanes p;
+    p.e0 = e0;
+    p.e1 = e1;
+    p.f0 = f0;
+    p.f1 = f1;
+    p.d0 = det2(e0, f1, e1, f0);
+    p.dq = det2(cv, f0, cu, f1);
+    p.dp = det2(e1, cu, e0, cv);
+    return p;
+}
+
+// z times a double-float, as a double-float.
+__device__ __forceinline__ F2 scale_f2(float z, F2 a) {
+    const float p = z * a.h;
+    return {p, __fmaf_rn(z, a.h, -p) + z * a.l};
+}
+
+// Rewrites a staged record into its evaluation form and fills its culling entries:
+//   r[0] = z (f1, -e1, -f0, e0) (heads; tails in `tail`), so that N_u = r[0].x dx + r[0].y dy and
+//          N_v = r[0].z dx + r[0].w dy;
+//   r[1] = (d0, dq, dp) / kappa and opacity;  r[2] = (m_x, m_y, c_x, c_y);  r[3] = colour, unchanged.
+// The disk term in base 2 is then -(N_u^2 + N_v^2) / det'^2 with det' = r[1].x + r[1].y dx + r[1].z dy.
+// Culling: alpha >= 1/255 where the disk term reaches -tau (tau = ln(255 opacity)), i.e. inside the
+// screen image of the circle u^2 + v^2 <= 2 tau. When that circle lies in front of the camera its
+// image is the ellipse (p - o)^T S^-1 (p - o) <= 1 read off the dual conic C* = T diag(2 tau,
+// 2 tau, -1) T^T: o = m - (C*_02, C*_12) / n, S = C*_2x2 / n + (o - m)(o - m)^T with n = -C*_22,
+// and det S = (d0 2 tau z)^2 / n^3. The filter term reaches -tau inside the disk |p - c|^2 <= tau.
+// tau is widened by 0.1 % + 0.001 and the ellipse by 0.2 % so that rounding cannot drop a pair
+// the per-pixel test blends; a circle that reaches the camera plane gives no bound (kept).
+__device__ __forceinline__ void prepare2d(float4 (&r)[4], float4& tl, float pcx, float pcy, float4& ca, float4& cb,
+                                          float& ct) {
+    const float Au = r[0].x, Bu = r[0].y, Cu = r[0].z, Av = r[0].w, Bv = r[1].x, Cv = r[1].y;
+    const float mx = r[1].z, my = r[1].w, z = r[2].x, cx = r[2].y, cy = r[2].z, o = r[2].w;
+    const SurfelPlanes p = surfel_planes(Au, Bu, Cu, Av, Bv, Cv, mx, my, pcx, pcy);
+    const F2 a1 = scale_f2(z, p.f1), a2 = scale_f2(-z, p.e1), b1 = scale_f2(-z, p.f0), b2 = scale_f2(z, p.e0);
+    r[0] = make_float4(a1.h, a2.h, b1.h, b2.h);
+    tl = make_float4(a1.l, a2.l, b1.l, b2.l);
+    r[1] = make_float4(kInvKappa * p.d0, kInvKappa * p.dq, kInvKappa * p.dp, o);
+    r[2] = make_float4(mx, my, cx, cy);
+    const float e0 = p.e0.h, e1 = p.e1.h, f0 = p.f0.h, f1 = p.f1.h;
+    const float inf = __int_as_float(0x7f800000);
+    ca = make_float4(mx, my, 0.f, 0.f);
+    cb = make_float4(0.f, -1.f, cx, cy);
+    ct = -1.f;
+    if (!(o * 1.00001f >= kAMin2)) return;  // alpha <= opacity < 1/255: never blended
+    const float tau = logf(255.f * o * 1.00001f) * 1.001f + 0.001f;
+    ct = tau;
+    const float rr = 2.f * tau;
+    const float n = __fmaf_rn(-rr, __fmaf_rn(Cu, Cu, Cv * Cv), z * z);
+    const float in = 1.f / n;
+    const float ox = -rr * __fmaf_rn(e0, Cu, e1 * Cv) * in, oy = -rr * __fmaf_rn(f0, Cu, f1 * Cv) * in;
+    const float sxx = __fmaf_rn(rr * __fmaf_rn(e0, e0, e1 * e1), in, ox * ox);
+    const float sxy = __fmaf_rn(rr * __fmaf_rn(e0, f0, e1 * f1), in, ox * oy);
+    const float syy = __fmaf_rn(rr * __fmaf_rn(f0, f0, f1 * f1), in, oy * oy);
+    const float t = p.d0 * rr * z * in;
+    const float dets = t * t * in;
+    const float ra = -sxy / syy, rc = -sxy / sxx, da = dets / (syy * syy), la = dets / syy * 1.002f;
+    if (n > 0.f && dets > 0.f && ra == ra && rc == rc && da < inf && la < inf && fabsf(ox) < inf && fabsf(oy) < inf) {
+        ca = make_float4(mx + ox, my + oy, rc, ra);
+        cb.x = da;
+        cb.y = la;
     } else {
-        e.u = e.v = 0.f;
-        e.p3 = -__int_as_float(0x7f800000);
+        cb.y = inf;  // no bound on the disk term: every warp keeps the pair
     }
-    const float dx = r[2].y - x, dy = r[2].z - y;
-    e.plp = -__fmaf_rn(dx, dx, dy * dy);
-    e.disk = e.p3 >= e.plp;
-    e.power = e.disk ? e.p3 : e.plp;
-    return e;
 }
 
 __device__ __forceinline__ void stage2_issue(Stage2& s, int slot, const float4* __restrict__ rec,
@@ -328,17 +398,28 @@ __device__ __forceinline__ void stage2_issue(Stage2& s, int slot, const float4* 
     }
 }
 
+// Keeps the staged records whose alpha can reach 1/255 in the warp's 8x8 block: the minimum of the
+// ellipse's quadratic form over the block's rectangle of pixel centres (three clamps, as for the
+// 3D conic), or the distance from the filter centre to the rectangle.
 __device__ __forceinline__ int compact2(Stage2& s, int n_in, int pos_limit, float wx0, float wx1, float wy0, float wy1,
                                         int warp, int lane) {
     int cnt = 0;
     const int lim = min(n_in, pos_limit);
+    const float x0 = wx0 - 0.01f, x1 = wx1 + 0.01f, y0 = wy0 - 0.01f, y1 = wy1 + 0.01f;
 #pragma unroll
     for (int c = 0; c < kB2 / 32; ++c) {
         const int j = c * 32 + lane;
         bool hit = false;
         if (j < lim) {
-            const float4 b = s.box[j];
-            hit = (b.y >= wx0) && (b.x <= wx1) && (b.w >= wy0) && (b.z <= wy1);
+            const float4 a = s.cull_a[j], b = s.cull_b[j];
+            const float ax = x0 - a.x, bx = x1 - a.x, ay = y0 - a.y, by = y1 - a.y;
+            const float cx = fminf(fmaxf(0.f, ax), bx);
+            const float dy = fminf(fmaxf(-a.z * cx, ay), by);
+            const float dx = fminf(fmaxf(-a.w * dy, ax), bx);
+            const float u = __fmaf_rn(a.w, dy, dx);
+            const bool disk = !(__fmaf_rn(u, u, b.x * dy * dy) > b.y);  // NaN keeps the pair
+            const float qx = fminf(fmaxf(b.z, x0), x1) - b.z, qy = fminf(fmaxf(b.w, y0), y1) - b.w;
+            hit = disk || __fmaf_rn(qx, qx, qy * qy) <= s.cull_tau[j];
         }
         const unsigned m = __ballot_sync(0xffffffffu, hit);
         if (hit) s.list[warp][cnt + __popc(m & lanemask_lt())] = (unsigned short)j;
@@ -348,22 +429,65 @@ __device__ __forceinline__ int compact2(Stage2& s, int n_in, int pos_limit, floa
     return cnt;
 }
 
-__device__ __forceinline__ void blend2(const SurfelEval& e, const float4 (&r)[4], unsigned pos1, float& T, float& c0,
+// Parts of a record's evaluation shared by a lane's two pixels (same x): the numerators' dx
+// terms as exact head + tail, det's dx part, the base-2 filter term's dx part.
+struct Col2 {
+    float dx, fx, uh, ut, vh, vt, dex, fxx;
+};
+
+__device__ __forceinline__ Col2 column2(const float4& r0, const float4& tl, const float4& r1, const float4& r2,
+                                        float x) {
+    Col2 c;
+    c.dx = x - r2.x;
+    c.fx = r2.z - x;
+    c.uh = r0.x * c.dx;
+    c.ut = __fmaf_rn(tl.x, c.dx, __fmaf_rn(r0.x, c.dx, -c.uh));
+    c.vh = r0.z * c.dx;
+    c.vt = __fmaf_rn(tl.z, c.dx, __fmaf_rn(r0.z, c.dx, -c.vh));
+    c.dex = __fmaf_rn(r1.y, c.dx, r1.x);
+    c.fxx = kNegLog2e * c.fx * c.fx;
+    return c;
+}
+
+// Base-2 exponents of the two terms at one pixel and the intermediates of their derivatives
+// (dy = y - m_y, fy = c_y - y).
+struct Pix2 {
+    float p3, plp, id, nu, nv;
+};
+
+__device__ __forceinline__ Pix2 eval2(const float4& r0, const float4& tl, const float4& r1, const Col2& c, float dy,
+                                      float fy) {
+    Pix2 e;
+    e.nu = __fmaf_rn(r0.y, dy, c.uh) + __fmaf_rn(tl.y, dy, c.ut);
+    e.nv = __fmaf_rn(r0.w, dy, c.vh) + __fmaf_rn(tl.w, dy, c.vt);
+    e.id = rcp_approx(__fmaf_rn(r1.z, dy, c.dex));
+    e.p3 = -__fmaf_rn(e.nu, e.nu, e.nv * e.nv) * (e.id * e.id);  // det = 0: -inf, or NaN that fmaxf drops
+    e.plp = __fmaf_rn(kNegLog2e * fy, fy, c.fxx);
+    return e;
+}
+
+__device__ __forceinline__ void blend2(float pw, float o, const float4& col, unsigned pos1, float& T, float& c0,
                                        float& c1, float& c2, unsigned& last, bool& done) {
-    const float alpha = fminf(kAMax2, r[2].w * expf(e.power));
+    const float alpha = fminf(kAMax2, o * ex2_approx(pw));
     if (alpha >= kAMin2) {
         const float test_T = T * (1.f - alpha);
         if (test_T < kTMin2) {
             done = true;
         } else {
             const float w = alpha * T;
-            c0 = __fmaf_rn(r[3].x, w, c0);
-            c1 = __fmaf_rn(r[3].y, w, c1);
-            c2 = __fmaf_rn(r[3].z, w, c2);
+            c0 = __fmaf_rn(col.x, w, c0);
+            c1 = __fmaf_rn(col.y, w, c1);
+            c2 = __fmaf_rn(col.z, w, c2);
             T = test_T;
             last = pos1;
         }
     }
+}
+
+// Makes a staged batch usable: plane form and culling entries of every record.
+__device__ __forceinline__ void prepare_batch(Stage2& s, int slot, int n_in, const KernelCamera& cam) {
+    const int t = threadIdx.x;
+    if (t < n_in) prepare2d(s.rec[slot][t], s.tail[slot][t], cam.cx, cam.cy, s.cull_a[t], s.cull_b[t], s.cull_tau[t]);
 }
 
 __global__ void __launch_bounds__(kB2) k_render2d_fwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
@@ -408,16 +532,24 @@ __global__ void __launch_bounds__(kB2) k_render2d_fwd(const float4* __restrict__
         }
         const bool ok = mbar_wait_bounded(&s.bar[slot], (unsigned)(b >> 1) & 1u, spin_limit, err);
         if (ok) consumed = b;
-        if (threadIdx.x < n_in) s.box[threadIdx.x] = surfel_box_full(s.rec[slot][threadIdx.x], cam.cx, cam.cy);
+        if (ok) prepare_batch(s, slot, n_in, cam);
         if (__syncthreads_or(!ok)) break;
         const int nl = compact2(s, n_in, kB2, wx0, wx1, wy0, wy1, warp, lane);
         for (int k = 0; k < nl; ++k) {
             if (__all_sync(0xffffffffu, done0 && done1)) break;
             const int j = s.list[warp][k];
-            const float4 r[4] = {s.rec[slot][j][0], s.rec[slot][j][1], s.rec[slot][j][2], s.rec[slot][j][3]};
+            const float4 r0 = s.rec[slot][j][0], r1 = s.rec[slot][j][1], r2 = s.rec[slot][j][2];
+            const float4 tl = s.tail[slot][j];
+            const Col2 c = column2(r0, tl, r1, r2, fpx);
             const unsigned pos1 = (unsigned)(b * kB2 + j + 1);
-            if (!done0) blend2(surfel_eval(r, cam.cx, cam.cy, fpx, fpy0), r, pos1, T0, c00, c01, c02, last0, done0);
-            if (!done1) blend2(surfel_eval(r, cam.cx, cam.cy, fpx, fpy1), r, pos1, T1, c10, c11, c12, last1, done1);
+            if (!done0) {
+                const Pix2 e = eval2(r0, tl, r1, c, fpy0 - r2.y, r2.w - fpy0);
+                blend2(fmaxf(e.p3, e.plp), r1.w, s.rec[slot][j][3], pos1, T0, c00, c01, c02, last0, done0);
+            }
+            if (!done1) {
+                const Pix2 e = eval2(r0, tl, r1, c, fpy1 - r2.y, r2.w - fpy1);
+                blend2(fmaxf(e.p3, e.plp), r1.w, s.rec[slot][j][3], pos1, T1, c10, c11, c12, last1, done1);
+            }
         }
         if (threadIdx.x == 0 && b + 2 < nb)
             mbar_arrive_expect_tx(&s.bar[slot], (unsigned)min(kB2, count - (b + 2) * kB2) * 64u);
@@ -443,48 +575,42 @@ __global__ void __launch_bounds__(kB2) k_render2d_fwd(const float4* __restrict__
     }
 }
 
-// One pixel's contribution to the 15 gradient components of a record (adjoint of surfel_eval
-// for the geometric fields; opacity; colour) and the step of its backward state.
-__device__ __forceinline__ void add_pixel2(float (&v)[16], const SurfelEval& e, const float4 (&r)[4], float alpha,
-                                           float oG, float G, float x, float y, float pcx, float pcy, float& T,
-                                           float& gS, float g0, float g1, float g2) {
-    const float inv = 1.f / (1.f - alpha);
+// One pixel's contribution to a record's 15 backward sums and the step of its backward state.
+// Sums (dpow = dL/dpower in natural units, id = 1 / det', tN = dpow N id^2, tdet = dpow p3 id,
+// base-2 p3):
+//   0..2 tN_u (1, dx, dy), 3..5 tN_v (1, dx, dy), 6..8 tdet (1, dx, dy), 9, 10 dpow (c - x) of the
+//   filter term, 11 dL/dopacity, 12..14 dL/dcolour.
+__device__ __forceinline__ void add_pixel2(float (&v)[16], const Pix2& e, float dx, float dy, float fx, float fy,
+                                           float alpha, float oG, float G, const float4& col, float& T, float& gS,
+                                           float g0, float g1, float g2) {
+    const float inv = rcp_approx(1.f - alpha);
     T *= inv;
     const float aT = alpha * T;
     v[12] = __fmaf_rn(aT, g0, v[12]);
     v[13] = __fmaf_rn(aT, g1, v[13]);
     v[14] = __fmaf_rn(aT, g2, v[14]);
-    const float gc = __fmaf_rn(g0, r[3].x, __fmaf_rn(g1, r[3].y, g2 * r[3].z));
+    const float gc = __fmaf_rn(g0, col.x, __fmaf_rn(g1, col.y, g2 * col.z));
     const float dalpha = __fmaf_rn(T, gc, -inv * gS);
     gS = __fmaf_rn(aT, gc, gS);
     if (!(oG <= kAMax2)) return;
     const float dpow = oG * dalpha;
     v[11] = __fmaf_rn(G, dalpha, v[11]);
-    if (!e.disk) {  // screen filter around the box centre: power = -(dx^2 + dy^2)
-        v[9] = __fmaf_rn(-2.f * (r[2].y - x), dpow, v[9]);
-        v[10] = __fmaf_rn(-2.f * (r[2].z - y), dpow, v[10]);
+    if (!(e.p3 >= e.plp)) {  // the filter term is the larger
+        v[9] = __fmaf_rn(dpow, fx, v[9]);
+        v[10] = __fmaf_rn(dpow, fy, v[10]);
         return;
     }
-    // power = -(u^2 + v^2) / 2 with u = Nu / det, v = Nv / det
-    const float id = 1.f / e.det;
-    const float gu = -e.u * dpow * id, gv = -e.v * dpow * id;      // dL/dNu, dL/dNv
-    const float gdet = -(gu * e.u + gv * e.v);                      // dL/ddet
-    const float dhxu = -gv * e.hy1 + gdet * e.hyv;
-    const float dhxv = gu * e.hy1 - gdet * e.hyu;
-    const float dhx1 = -gu * e.hyv + gv * e.hyu;
-    const float dhyu = gv * e.hx1 - gdet * e.hxv;
-    const float dhyv = -gu * e.hx1 + gdet * e.hxu;
-    const float dhy1 = gu * e.hxv - gv * e.hxu;
-    const float ax = pcx - x, ay = pcy - y;
-    v[0] += dhxu;
-    v[1] += dhyu;
-    v[2] = __fmaf_rn(dhxu, ax, __fmaf_rn(dhyu, ay, v[2]));
-    v[3] += dhxv;
-    v[4] += dhyv;
-    v[5] = __fmaf_rn(dhxv, ax, __fmaf_rn(dhyv, ay, v[5]));
-    v[6] = __fmaf_rn(dhx1, r[2].x, v[6]);
-    v[7] = __fmaf_rn(dhy1, r[2].x, v[7]);
-    v[8] = __fmaf_rn(dhx1, r[1].z - x, __fmaf_rn(dhy1, r[1].w - y, v[8]));
+    const float w2 = dpow * (e.id * e.id);
+    const float tu = w2 * e.nu, tv = w2 * e.nv, td = dpow * e.p3 * e.id;
+    v[0] += tu;
+    v[1] = __fmaf_rn(tu, dx, v[1]);
+    v[2] = __fmaf_rn(tu, dy, v[2]);
+    v[3] += tv;
+    v[4] = __fmaf_rn(tv, dx, v[4]);
+    v[5] = __fmaf_rn(tv, dy, v[5]);
+    v[6] += td;
+    v[7] = __fmaf_rn(td, dx, v[7]);
+    v[8] = __fmaf_rn(td, dy, v[8]);
 }
 
 // Transpose reduction of 16 components over the warp: after levels 16, 8, 4, 2 a lane keeps one
@@ -505,6 +631,8 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
     return x + __shfl_xor_sync(0xffffffffu, x, 1);
 }
 
+// Backward replay. Each record's 15 sums (add_pixel2) are accumulated in `grad`; a second kernel
+// (k_render2d_grad_fields) turns them into gradients of the record fields.
 template <int MODE>
 __global__ void __launch_bounds__(kB2) k_render2d_bwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
                                                       const uint2* __restrict__ ranges, const KernelCamera cam,
@@ -569,28 +697,32 @@ __global__ void __launch_bounds__(kB2) k_render2d_bwd(const float4* __restrict__
         }
         const bool ok = mbar_wait_bounded(&s.bar[slot], (unsigned)(it >> 1) & 1u, spin_limit, err);
         if (ok) consumed = it;
-        if (threadIdx.x < n_in) s.box[threadIdx.x] = surfel_box_full(s.rec[slot][threadIdx.x], cam.cx, cam.cy);
+        if (ok) prepare_batch(s, slot, n_in, cam);
         if (__syncthreads_or(!ok)) break;
         const int pos_limit = (int)wmax - b * kB2;
         const int nl = compact2(s, n_in, pos_limit, wx0, wx1, wy0, wy1, warp, lane);
         for (int k = nl - 1; k >= 0; --k) {
             const int j = s.list[warp][k];
             const unsigned pos = (unsigned)(b * kB2 + j);
-            const float4 r[4] = {s.rec[slot][j][0], s.rec[slot][j][1], s.rec[slot][j][2], s.rec[slot][j][3]};
-            const SurfelEval e0 = surfel_eval(r, cam.cx, cam.cy, fpx, fpy0);
-            const SurfelEval e1 = surfel_eval(r, cam.cx, cam.cy, fpx, fpy1);
-            const float G0 = expf(e0.power), G1 = expf(e1.power);
-            const float oG0 = r[2].w * G0, oG1 = r[2].w * G1;
+            const float4 r0 = s.rec[slot][j][0], r1 = s.rec[slot][j][1], r2 = s.rec[slot][j][2];
+            const float4 tl = s.tail[slot][j];
+            const Col2 c = column2(r0, tl, r1, r2, fpx);
+            const float dy0 = fpy0 - r2.y, dy1 = fpy1 - r2.y, fy0 = r2.w - fpy0, fy1 = r2.w - fpy1;
+            const Pix2 e0 = eval2(r0, tl, r1, c, dy0, fy0);
+            const Pix2 e1 = eval2(r0, tl, r1, c, dy1, fy1);
+            const float G0 = ex2_approx(fmaxf(e0.p3, e0.plp)), G1 = ex2_approx(fmaxf(e1.p3, e1.plp));
+            const float oG0 = r1.w * G0, oG1 = r1.w * G1;
             const float al0 = fminf(kAMax2, oG0), al1 = fminf(kAMax2, oG1);
             const bool c0 = pos < last0 && al0 >= kAMin2;
             const bool c1 = pos < last1 && al1 >= kAMin2;
             const unsigned ballot = __ballot_sync(0xffffffffu, c0 || c1);
             if (ballot == 0u) continue;
+            const float4 col = s.rec[slot][j][3];
             float v[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) v[c] = 0.f;
-            if (c0) add_pixel2(v, e0, r, al0, oG0, G0, fpx, fpy0, cam.cx, cam.cy, T0, gS0, a0, a1, a2);
-            if (c1) add_pixel2(v, e1, r, al1, oG1, G1, fpx, fpy1, cam.cx, cam.cy, T1, gS1, b0, b1, b2);
+            if (c0) add_pixel2(v, e0, c.dx, dy0, c.fx, fy0, al0, oG0, G0, col, T0, gS0, a0, a1, a2);
+            if (c1) add_pixel2(v, e1, c.dx, dy1, c.fx, fy1, al1, oG1, G1, col, T1, gS1, b0, b1, b2);
             float* gp = grad + kS2 * (size_t)s.gidx[slot][j];
             if (MODE == GS_BWD_DIRECT || (MODE == GS_BWD_ADAPTIVE && __popc(ballot) < thr)) {
                 if (c0 || c1) {
@@ -609,6 +741,44 @@ __global__ void __launch_bounds__(kB2) k_render2d_bwd(const float4* __restrict__
         __syncthreads();
     }
     for (int k = consumed + 1; k <= issued; ++k) mbar_wait_bounded(&s.bar[k & 1], (unsigned)(k >> 1) & 1u, 1u << 22, err);
+}
+
+// Gradients of the record fields from the backward sums, in place. With the natural-unit sums
+// G_N = -t_N / kappa^2 and G_det = -t_det / kappa^3 (t as in add_pixel2), each field's gradient is
+// the sum over pixels of its per-pixel derivative through the planes h_x, h_y, which is linear in
+// those sums: A_u, A_v, B_u, B_v through the planes' first two entries, C_u, C_v through the same
+// entries times (cx - x) and (cy - y), m and z through the third entries z (m - x), z (m - y).
+// The m terms use only the N sums (the det parts cancel exactly and are left out). The filter term
+// gives dL/dc = -2 sum dpow (c - x).
+__global__ void __launch_bounds__(256) k_render2d_grad_fields(unsigned n, const float4* __restrict__ rec,
+                                                              float4* __restrict__ grad, float pcx, float pcy) {
+    const unsigned i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float4* g = grad + 4 * (size_t)i;
+    const float4 s0 = g[0], s1 = g[1], s2 = g[2];
+    if (s0.x == 0.f && s0.y == 0.f && s0.z == 0.f && s0.w == 0.f && s1.x == 0.f && s1.y == 0.f && s1.z == 0.f &&
+        s1.w == 0.f && s2.x == 0.f && s2.y == 0.f && s2.z == 0.f)
+        return;  // no geometric gradient; opacity and colour are final
+    const float4 r0 = rec[4 * (size_t)i], r1 = rec[4 * (size_t)i + 1], r2 = rec[4 * (size_t)i + 2];
+    const float Cu = r0.z, Cv = r1.y, mx = r1.z, my = r1.w, z = r2.x;
+    const SurfelPlanes p = surfel_planes(r0.x, r0.y, Cu, r0.w, r1.x, Cv, mx, my, pcx, pcy);
+    const float gnu = -kInvKappa2 * s0.x, gnu_x = -kInvKappa2 * s0.y, gnu_y = -kInvKappa2 * s0.z;
+    const float gnv = -kInvKappa2 * s0.w, gnv_x = -kInvKappa2 * s1.x, gnv_y = -kInvKappa2 * s1.y;
+    const float gd = -kInvKappa3 * s1.z, gd_x = -kInvKappa3 * s1.w, gd_y = -kInvKappa3 * s2.x;
+    const float e0 = p.e0.h, e1 = p.e1.h, f0 = p.f0.h, f1 = p.f1.h;
+    const float gz = f1 * gnu_x - e1 * gnu_y + e0 * gnv_y - f0 * gnv_x;
+    const float gf1 = z * gnu_x + e0 * gd - Cu * gd_x;
+    const float ge1 = -z * gnu_y - f0 * gd + Cu * gd_y;
+    const float ge0 = z * gnv_y + f1 * gd - Cv * gd_y;
+    const float gf0 = -z * gnv_x - e1 * gd + Cv * gd_x;
+    const float ax = pcx - mx, ay = pcy - my;
+    const float gcu = -f1 * gd_x + e1 * gd_y + ax * ge0 + ay * gf0;
+    const float gcv = f0 * gd_x - e0 * gd_y + ax * ge1 + ay * gf1;
+    const float gmx = z * (Cv * gnu_y - Cu * gnv_y + f0 * gnv - f1 * gnu);
+    const float gmy = z * (Cu * gnv_x - Cv * gnu_x + e1 * gnu - e0 * gnv);
+    g[0] = make_float4(ge0, gf0, gcu, ge1);
+    g[1] = make_float4(gf1, gcv, gmx, gmy);
+    g[2] = make_float4(gz, -2.f * s2.y, -2.f * s2.z, s2.w);
 }
 
 // ---- preprocess backward -------------------------------------------------------------------------
@@ -744,6 +914,10 @@ cudaError_t launch_render2d_bwd(int mode, int thr, const float* rec2d, unsigned 
         k_render2d_bwd<GS_BWD_WARP><<<tiles, kB2, 0, st>>>(r, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad, thr, spin_limit, err);
     else
         k_render2d_bwd<GS_BWD_ADAPTIVE><<<tiles, kB2, 0, st>>>(r, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad, thr, spin_limit, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || n == 0) return e;
+    count_launches(1);
+    k_render2d_grad_fields<<<(n + 255) / 256, 256, 0, st>>>(n, r, reinterpret_cast<float4*>(grad), cam.cx, cam.cy);
     return cudaGetLastError();
 }
 
