@@ -179,38 +179,49 @@ __global__ void __launch_bounds__(128) k_preprocess2d(int n, const float* __rest
                                                       int* __restrict__ radius, unsigned* __restrict__ tiles_touched,
                                                       float4* __restrict__ rec2d) {
     constexpr int K = (DEG + 1) * (DEG + 1);
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const float m[3] = {mean3d[3 * i], mean3d[3 * i + 1], mean3d[3 * i + 2]};
-    const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
-    float rec[11], half[2];
-    depth[i] = row_dot(cam.R + 6, m, cam.t[2]);
-    bool ok = surfel_geometry<float>(m, log_scale[3 * i], log_scale[3 * i + 1], q, cam, rec, half);
+    constexpr int K3 = 3 * K;
+    __shared__ float tile_all[4][32 * (K3 + 1)];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int warp_first = blockIdx.x * 128 + warp * 32;
+    if (warp_first >= n) return;  // whole warp
+    const int i = warp_first + lane;
+    float m[3] = {0.f, 0.f, 0.f}, rec[11], half[2];
+    bool ok = false;
     int r = 0;
     unsigned tt = 0;
-    if (ok) {
-        r = surfel_radius(half);
-        const Rect R = tile_rect(rec[9], rec[10], r, cam.tiles_x, cam.tiles_y);
-        ok = r > 0 && R.x0 <= R.x1;
-        if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+    if (i < n) {
+        m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
+        const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
+        depth[i] = row_dot(cam.R + 6, m, cam.t[2]);
+        ok = surfel_geometry<float>(m, log_scale[3 * i], log_scale[3 * i + 1], q, cam, rec, half);
+        if (ok) {
+            r = surfel_radius(half);
+            const Rect R = tile_rect(rec[9], rec[10], r, cam.tiles_x, cam.tiles_y);
+            ok = r > 0 && R.x0 <= R.x1;
+            if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+        }
+        if (!ok) {
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            float4* o4 = rec2d + 4 * (size_t)i;
+            radius[i] = 0;
+            tiles_touched[i] = 0;
+            proj_rec[3 * (size_t)i] = z4;
+            proj_rec[3 * (size_t)i + 1] = z4;
+            proj_rec[3 * (size_t)i + 2] = z4;
+            o4[0] = z4; o4[1] = z4; o4[2] = z4; o4[3] = z4;
+        }
     }
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4* o4 = rec2d + 4 * (size_t)i;
-    if (!ok) {
-        radius[i] = 0;
-        tiles_touched[i] = 0;
-        proj_rec[3 * (size_t)i] = z4;
-        proj_rec[3 * (size_t)i + 1] = z4;
-        proj_rec[3 * (size_t)i + 2] = z4;
-        o4[0] = z4; o4[1] = z4; o4[2] = z4; o4[3] = z4;
-        return;
-    }
+    // SH coefficients of the warp's visible surfels only, with coalesced loads
+    float* tile = tile_all[warp];
+    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, __ballot_sync(0xffffffffu, ok));
+    __syncwarp();
+    if (!ok) return;
     const float op = 1.f / (1.f + expf(-logit[i]));
     float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
     const float dinv = rsqrtf(dx * dx + dy * dy + dz * dz);
     float Y[16];
     sh_basis<DEG>(dx * dinv, dy * dinv, dz * dinv, Y);
-    const float* shg = sh + (size_t)i * K * 3;
+    const float* shg = tile + lane * (K3 + 1);
     float col[3] = {0.5f, 0.5f, 0.5f};
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -218,11 +229,13 @@ __global__ void __launch_bounds__(128) k_preprocess2d(int n, const float* __rest
         col[1] += Y[k] * shg[3 * k + 1];
         col[2] += Y[k] * shg[3 * k + 2];
     }
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     proj_rec[3 * (size_t)i] = make_float4(rec[9], rec[10], 0.f, 0.f);  // the binning reads the box centre
     proj_rec[3 * (size_t)i + 1] = z4;
     proj_rec[3 * (size_t)i + 2] = z4;
     radius[i] = r;
     tiles_touched[i] = tt;
+    float4* o4 = rec2d + 4 * (size_t)i;
     o4[0] = make_float4(rec[0], rec[1], rec[2], rec[3]);
     o4[1] = make_float4(rec[4], rec[5], rec[6], rec[7]);
     o4[2] = make_float4(rec[8], rec[9], rec[10], op);
@@ -796,15 +809,22 @@ __global__ void __launch_bounds__(128) k_preprocess2d_bwd(int n, const float* __
                                                           float* __restrict__ d_logit, float* __restrict__ d_sh,
                                                           int accumulate) {
     constexpr int K = (DEG + 1) * (DEG + 1);
+    constexpr int K3 = 3 * K;
     using D = Df<9>;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
+    __shared__ float tile_all[4][32 * (K3 + 1)];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int warp_first = blockIdx.x * 128 + warp * 32;
+    if (warp_first >= n) return;  // whole warp
+    const int i = warp_first + lane;
+    // only surfels with radius > 0 have non-zero gradients: load their SH rows only
+    const unsigned seen = __ballot_sync(0xffffffffu, i < n && radius[i] > 0);
+    float* tile = tile_all[warp];
+    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    __syncwarp();
+    float* my = tile + lane * (K3 + 1);  // this thread's coefficients, then its SH gradients
     float gr[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float dlg = 0.f;
-    float dsh[48];
-#pragma unroll
-    for (int k = 0; k < 3 * K; ++k) dsh[k] = 0.f;
-    if (radius[i] > 0) {
+    if (i < n && ((seen >> lane) & 1u)) {
         const float* gi = grad + kS2 * (size_t)i;
         D m[3], q[4];
         for (int k = 0; k < 3; ++k) m[k] = D::var(mean3d[3 * i + k], k);
@@ -828,16 +848,17 @@ __global__ void __launch_bounds__(128) k_preprocess2d_bwd(int n, const float* __
         const float ux = vx * vinv, uy = vy * vinv, uz = vz * vinv;
         float Y[16];
         sh_basis<DEG>(ux, uy, uz, Y);
-        const float* shg = sh + (size_t)i * K * 3;
         float col[3] = {0.5f, 0.5f, 0.5f};
+#pragma unroll
         for (int k = 0; k < K; ++k)
-            for (int c = 0; c < 3; ++c) col[c] += Y[k] * shg[3 * k + c];
+            for (int c = 0; c < 3; ++c) col[c] += Y[k] * my[3 * k + c];
         float dc[3];
         for (int c = 0; c < 3; ++c) dc[c] = col[c] < 0.f ? 0.f : gi[12 + c];
         float wk[16];
+#pragma unroll
         for (int k = 0; k < K; ++k) {
-            wk[k] = shg[3 * k] * dc[0] + shg[3 * k + 1] * dc[1] + shg[3 * k + 2] * dc[2];
-            for (int c = 0; c < 3; ++c) dsh[3 * k + c] = Y[k] * dc[c];
+            wk[k] = my[3 * k] * dc[0] + my[3 * k + 1] * dc[1] + my[3 * k + 2] * dc[2];
+            for (int c = 0; c < 3; ++c) my[3 * k + c] = Y[k] * dc[c];  // the row now holds dL/dsh
         }
         if (DEG > 0) {
             float gd[3] = {0.f, 0.f, 0.f};
@@ -847,27 +868,32 @@ __global__ void __launch_bounds__(128) k_preprocess2d_bwd(int n, const float* __
             gr[1] += (gd[1] - dot * uy) * vinv;
             gr[2] += (gd[2] - dot * uz) * vinv;
         }
+    } else if (i < n) {
+        for (int k = 0; k < K3; ++k) my[k] = 0.f;
     }
-    float* dm = d_mean3d + 3 * (size_t)i;
-    float* dl = d_log_scale + 3 * (size_t)i;
-    float* dq = d_quat + 4 * (size_t)i;
-    float* ds = d_sh + (size_t)i * K * 3;
-    if (accumulate) {
-        for (int k = 0; k < 3; ++k) dm[k] += gr[k];
-        dl[0] += gr[3];
-        dl[1] += gr[4];
-        for (int k = 0; k < 4; ++k) dq[k] += gr[5 + k];
-        d_logit[i] += dlg;
-        for (int k = 0; k < 3 * K; ++k) ds[k] += dsh[k];
-    } else {
-        for (int k = 0; k < 3; ++k) dm[k] = gr[k];
-        dl[0] = gr[3];
-        dl[1] = gr[4];
-        dl[2] = 0.f;
-        for (int k = 0; k < 4; ++k) dq[k] = gr[5 + k];
-        d_logit[i] = dlg;
-        for (int k = 0; k < 3 * K; ++k) ds[k] = dsh[k];
+    if (i < n) {
+        float* dm = d_mean3d + 3 * (size_t)i;
+        float* dl = d_log_scale + 3 * (size_t)i;
+        float* dq = d_quat + 4 * (size_t)i;
+        if (accumulate) {
+            for (int k = 0; k < 3; ++k) dm[k] += gr[k];
+            dl[0] += gr[3];
+            dl[1] += gr[4];
+            for (int k = 0; k < 4; ++k) dq[k] += gr[5 + k];
+            d_logit[i] += dlg;
+        } else {
+            for (int k = 0; k < 3; ++k) dm[k] = gr[k];
+            dl[0] = gr[3];
+            dl[1] = gr[4];
+            dl[2] = 0.f;
+            for (int k = 0; k < 4; ++k) dq[k] = gr[5 + k];
+            d_logit[i] = dlg;
+        }
     }
+    __syncwarp();
+    // accumulating: rows of surfels with radius 0 add nothing and are skipped
+    if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane, seen);
+    else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane, 0xffffffffu);
 }
 
 // ---- launchers -------------------------------------------------------------------------------------

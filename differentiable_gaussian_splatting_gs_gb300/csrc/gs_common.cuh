@@ -100,6 +100,29 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+// Copies the SH coefficients of the warp's 32 Gaussians (contiguous K3 floats each) between global
+// memory and a padded shared-memory tile (row stride K3 + 1: conflict-free per-thread rows) with
+// coalesced accesses, for the rows whose bit is set in `rows` (lane order). LOAD: global -> shared
+// (asynchronous copies, waited for before returning; the caller then synchronises the warp);
+// else shared -> global (ADD: added to global).
+template <int K3, bool LOAD, bool ADD>
+__device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, int n, int lane, unsigned rows) {
+    const int cnt = min(32, n - first);
+    if (cnt <= 0 || rows == 0u) return;
+    const int total = cnt * K3;
+    float* gw = g + (size_t)first * K3;
+    // loads are asynchronous copies, all in flight at once; the caller synchronises the warp
+#pragma unroll 4
+    for (int e = lane; e < total; e += 32) {
+        const int row = e / K3, col = e - row * K3;
+        if (!((rows >> row) & 1u)) continue;
+        if (LOAD) cp_async4(&tile[row * (K3 + 1) + col], gw + e);
+        else if (ADD) gw[e] += tile[row * (K3 + 1) + col];
+        else gw[e] = tile[row * (K3 + 1) + col];
+    }
+    if (LOAD) cp_async_wait_all();
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     unsigned ok;
     asm volatile(

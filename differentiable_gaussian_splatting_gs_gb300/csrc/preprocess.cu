@@ -106,29 +106,6 @@ __device__ __forceinline__ bool geometry(const float* m, const float* ls, const 
 
 constexpr int kFwdThreads = 128;
 
-// Copies the SH coefficients of the warp's 32 Gaussians (contiguous K3 floats each) between global
-// memory and a padded shared-memory tile (row stride K3 + 1: conflict-free per-thread rows) with
-// coalesced accesses, for the rows whose bit is set in `rows` (lane order). LOAD: global -> shared
-// (asynchronous copies, waited for before returning; the caller then synchronises the warp);
-// else shared -> global (ADD: added to global).
-template <int K3, bool LOAD, bool ADD>
-__device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, int n, int lane, unsigned rows) {
-    const int cnt = min(32, n - first);
-    if (cnt <= 0 || rows == 0u) return;
-    const int total = cnt * K3;
-    float* gw = g + (size_t)first * K3;
-    // loads are asynchronous copies, all in flight at once; the caller synchronises the warp
-#pragma unroll 4
-    for (int e = lane; e < total; e += 32) {
-        const int row = e / K3, col = e - row * K3;
-        if (!((rows >> row) & 1u)) continue;
-        if (LOAD) cp_async4(&tile[row * (K3 + 1) + col], gw + e);
-        else if (ADD) gw[e] += tile[row * (K3 + 1) + col];
-        else gw[e] = tile[row * (K3 + 1) + col];
-    }
-    if (LOAD) cp_async_wait_all();
-}
-
 template <int DEG>
 __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* __restrict__ mean3d,
                                                             const float* __restrict__ log_scale,
@@ -344,7 +321,6 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     for (int k = 0; k < 3; ++k) dm[k] += R[k] * dp[0] + R[3 + k] * dp[1] + R[6 + k] * dp[2];
 
     // M3 = Rq diag(s): dL/dM3 = T^T dL/dK, dRq = dL/dM3 diag(s)
-    const float* Rq = g.Rq;
     float dRq[9];
     for (int r0 = 0; r0 < 3; ++r0)
         for (int k = 0; k < 3; ++k) dRq[3 * r0 + k] = (T[r0] * dK[k] + T[3 + r0] * dK[3 + k]) * g.s[k];
