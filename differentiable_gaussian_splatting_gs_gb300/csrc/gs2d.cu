@@ -271,8 +271,9 @@ constexpr float kInvKappa2 = 1.3862943611198906f;  // 1 / kappa^2 = 2 ln 2
 constexpr float kInvKappa3 = 1.6322368749392457f;  // 1 / kappa^3
 
 struct Stage2 {
-    float4 rec[2][kB2][4];
-    float4 tail[2][kB2];  // tails of the numerator coefficients r[0]
+    // record, then the tails of its numerator coefficients; the 80-byte stride makes the
+    // per-thread float4 accesses of the rewrite conflict-free (64 bytes would be 4-way)
+    float4 rec[2][kB2][5];
     unsigned gidx[2][kB2];
     float4 cull_a[kB2];  // (o_x, o_y, B / C, B / A) of the disk's alpha ellipse (conic A, B, C)
     float4 cull_b[kB2];  // (D / A, L / A) of that ellipse, filter centre (c_x, c_y)
@@ -348,7 +349,7 @@ __device__ __forceinline__ F2 scale_f2(float z, F2 a) {
 }
 
 // Rewrites a staged record into its evaluation form and fills its culling entries:
-//   r[0] = z (f1, -e1, -f0, e0) (heads; tails in `tail`), so that N_u = r[0].x dx + r[0].y dy and
+//   r[0] = z (f1, -e1, -f0, e0) (heads; tails in r[4]), so that N_u = r[0].x dx + r[0].y dy and
 //          N_v = r[0].z dx + r[0].w dy;
 //   r[1] = (d0, dq, dp) / kappa and opacity;  r[2] = (m_x, m_y, c_x, c_y);  r[3] = colour, unchanged.
 // The disk term in base 2 is then -(N_u^2 + N_v^2) / det'^2 with det' = r[1].x + r[1].y dx + r[1].z dy.
@@ -359,14 +360,13 @@ __device__ __forceinline__ F2 scale_f2(float z, F2 a) {
 // and det S = (d0 2 tau z)^2 / n^3. The filter term reaches -tau inside the disk |p - c|^2 <= tau.
 // tau is widened by 0.1 % + 0.001 and the ellipse by 0.2 % so that rounding cannot drop a pair
 // the per-pixel test blends; a circle that reaches the camera plane gives no bound (kept).
-__device__ __forceinline__ void prepare2d(float4 (&r)[4], float4& tl, float pcx, float pcy, float4& ca, float4& cb,
-                                          float& ct) {
+__device__ __forceinline__ void prepare2d(float4 (&r)[5], float pcx, float pcy, float4& ca, float4& cb, float& ct) {
     const float Au = r[0].x, Bu = r[0].y, Cu = r[0].z, Av = r[0].w, Bv = r[1].x, Cv = r[1].y;
     const float mx = r[1].z, my = r[1].w, z = r[2].x, cx = r[2].y, cy = r[2].z, o = r[2].w;
     const SurfelPlanes p = surfel_planes(Au, Bu, Cu, Av, Bv, Cv, mx, my, pcx, pcy);
     const F2 a1 = scale_f2(z, p.f1), a2 = scale_f2(-z, p.e1), b1 = scale_f2(-z, p.f0), b2 = scale_f2(z, p.e0);
     r[0] = make_float4(a1.h, a2.h, b1.h, b2.h);
-    tl = make_float4(a1.l, a2.l, b1.l, b2.l);
+    r[4] = make_float4(a1.l, a2.l, b1.l, b2.l);
     r[1] = make_float4(kInvKappa * p.d0, kInvKappa * p.dq, kInvKappa * p.dp, o);
     r[2] = make_float4(mx, my, cx, cy);
     const float e0 = p.e0.h, e1 = p.e1.h, f0 = p.f0.h, f1 = p.f1.h;
@@ -500,7 +500,7 @@ __device__ __forceinline__ void blend2(float pw, float o, const float4& col, uns
 // Makes a staged batch usable: plane form and culling entries of every record.
 __device__ __forceinline__ void prepare_batch(Stage2& s, int slot, int n_in, const KernelCamera& cam) {
     const int t = threadIdx.x;
-    if (t < n_in) prepare2d(s.rec[slot][t], s.tail[slot][t], cam.cx, cam.cy, s.cull_a[t], s.cull_b[t], s.cull_tau[t]);
+    if (t < n_in) prepare2d(s.rec[slot][t], cam.cx, cam.cy, s.cull_a[t], s.cull_b[t], s.cull_tau[t]);
 }
 
 __global__ void __launch_bounds__(kB2) k_render2d_fwd(const float4* __restrict__ rec, const unsigned* __restrict__ vals,
@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kB2) k_render2d_fwd(const float4* __restrict__
             if (__all_sync(0xffffffffu, done0 && done1)) break;
             const int j = s.list[warp][k];
             const float4 r0 = s.rec[slot][j][0], r1 = s.rec[slot][j][1], r2 = s.rec[slot][j][2];
-            const float4 tl = s.tail[slot][j];
+            const float4 tl = s.rec[slot][j][4];
             const Col2 c = column2(r0, tl, r1, r2, fpx);
             const unsigned pos1 = (unsigned)(b * kB2 + j + 1);
             if (!done0) {
@@ -718,7 +718,7 @@ __global__ void __launch_bounds__(kB2) k_render2d_bwd(const float4* __restrict__
             const int j = s.list[warp][k];
             const unsigned pos = (unsigned)(b * kB2 + j);
             const float4 r0 = s.rec[slot][j][0], r1 = s.rec[slot][j][1], r2 = s.rec[slot][j][2];
-            const float4 tl = s.tail[slot][j];
+            const float4 tl = s.rec[slot][j][4];
             const Col2 c = column2(r0, tl, r1, r2, fpx);
             const float dy0 = fpy0 - r2.y, dy1 = fpy1 - r2.y, fy0 = r2.w - fpy0, fy1 = r2.w - fpy1;
             const Pix2 e0 = eval2(r0, tl, r1, c, dy0, fy0);
