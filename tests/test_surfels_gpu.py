@@ -26,7 +26,10 @@ from differentiable_gaussian_splatting_gs_gb300 import api  # noqa: E402
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
-CASES2D = {"tiny": (0, None, 1.0), "object": (1, 20_000, 1.0), "outdoor": (2, 100_000, 0.5)}
+# the last case is the 1.6M-surfel 1297x840 scene at full size, in the launch configuration the
+# benchmark's surfel step uses
+CASES2D = {"tiny": (0, None, 1.0), "object": (1, 20_000, 1.0), "outdoor": (2, 100_000, 0.5),
+           "outdoor_full": (2, None, 1.0)}
 
 
 @functools.lru_cache(maxsize=None)
@@ -134,4 +137,70 @@ def test_surfel_preprocess_backward_matches_oracle(name):
         b = g3[ok]
         scale = np.abs(b).max()
         assert np.abs(a - b).max() <= 1e-4 * scale + 1e-12, (name, k, np.abs(a - b).max() / max(scale, 1e-30))
+    assert api.gs_device_error() == 0
+
+
+def test_surfel_empty_and_all_culled():
+    opt = api.make_options(0)
+    cam = gs_scenes.make_scene(0).cameras[0]
+    empty = {k: torch.empty((0,) + shp, dtype=torch.float32, device=DEV)
+             for k, shp in (("mean3d", (3,)), ("log_scale", (3,)), ("quat", (4,)), ("opacity_logit", ()),
+                            ("sh", (1, 3)))}
+    proj, rec2d = api.gs_preprocess2d(empty, cam, opt)
+    assert proj.n == 0 and rec2d.shape == (0, 16)
+    s = gs_scenes.make_scene(0, n=500)
+    s.mean3d[:, 2] = -1.0  # everything behind the camera
+    params = _params(s)
+    proj, rec2d = api.gs_preprocess2d(params, cam, opt)
+    assert int(proj.radius.max()) == 0 and int(proj.tiles_touched.max()) == 0
+    assert float(rec2d.abs().max()) == 0.0
+    b = api.gs_bin_and_sort(proj, cam, opt)
+    assert b.n_dup == 0 and int(b.ranges.abs().max()) == 0
+    img, tf, nc = api.gs_render2d_fwd(rec2d, b.vals, b.ranges, cam, opt)
+    bg = torch.tensor(cam.bg, dtype=torch.float32, device=DEV)[:, None, None].expand_as(img)
+    assert torch.equal(img, bg) and float(tf.min()) == 1.0 and int(nc.max()) == 0
+    grad = api.gs_render2d_bwd(rec2d, b.vals, b.ranges, cam, opt, torch.ones_like(img), tf, nc)
+    assert float(grad.abs().max()) == 0.0
+    out = api.gs_preprocess2d_bwd(params, cam, opt, proj, grad)
+    assert all(float(t.abs().max()) == 0.0 for t in out.values())
+    assert api.gs_device_error() == 0
+
+
+def test_surfel_backward_rejects_shared_memory_mode():
+    s, cam, pre, rec32, c32, vals, ranges, fwd, dl_m, *_ = _case("tiny")
+    opt = api.make_options(s.sh_degree, bwd_mode="sm")
+    r = torch.from_numpy(rec32).to(DEV)
+    v = torch.from_numpy(vals.astype(np.int32)).to(DEV)
+    _, t_final, n_contrib = api.gs_render2d_fwd(r, v, _ranges_dev(ranges), cam, opt)
+    with pytest.raises(api.GsError, match="GS_BWD_SM"):
+        api.gs_render2d_bwd(r, v, _ranges_dev(ranges), cam, opt, torch.from_numpy(dl_m).to(DEV), t_final, n_contrib)
+
+
+def test_surfel_preprocess_backward_accumulates_views():
+    """Two views of the multi-view scene: the second call with accumulate adds to the first; the
+    sum equals the sum of the oracle's per-view gradients."""
+    s = gs_scenes.make_scene(3, n=20_000, res_scale=0.25, views=2)
+    params = _params(s)
+    opt = api.make_options(s.sh_degree)
+    grads, want = None, None
+    for v, cam in enumerate(s.cameras):
+        pre = oracle.preprocess2d(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, s.sh_degree, cam)
+        _, vals, ranges = oracle.bin_and_sort(pre["mean2d"].astype(np.float32), pre["depth"], pre["radius"],
+                                              cam.width, cam.height)
+        rec = pre["rec2d"].astype(np.float32).astype(np.float64)
+        fwd = oracle.render2d(rec, vals, ranges, cam)
+        dl = np.where(fwd["pix_flags"][None] != 0, 0.0, fwd["image"] - s.targets[v]).astype(np.float32)
+        g32 = oracle.render2d(rec, vals, ranges, cam, dl)["grad"].astype(np.float32)
+        proj, _ = api.gs_preprocess2d(params, cam, opt)
+        proj.radius.copy_(torch.from_numpy(pre["radius"]))
+        grads = api.gs_preprocess2d_bwd(params, cam, opt, proj, torch.from_numpy(g32).to(DEV), out=grads,
+                                        accumulate=v > 0)
+        o = oracle.preprocess2d_bwd(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, s.sh_degree, cam, g32)
+        want = o if want is None else {k: want[k] + o[k] for k in o}
+    torch.cuda.synchronize()
+    for k, ok in [("mean3d", "d_mean3d"), ("log_scale", "d_log_scale"), ("quat", "d_quat"),
+                  ("opacity_logit", "d_opacity_logit"), ("sh", "d_sh")]:
+        a = grads[k].cpu().numpy().astype(np.float64)
+        b = want[ok]
+        assert np.abs(a - b).max() <= 1e-4 * np.abs(b).max() + 1e-12, k
     assert api.gs_device_error() == 0
