@@ -213,10 +213,13 @@ __global__ void __launch_bounds__(128) k_preprocess2d(int n, const float* __rest
     }
     // SH coefficients of the warp's visible surfels only, with coalesced loads
     float* tile = tile_all[warp];
-    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, __ballot_sync(0xffffffffu, ok));
+    sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane,
+                                         __ballot_sync(0xffffffffu, ok));
+    const float lg = ok ? logit[i] : 0.f;
+    cp_async_wait_all();
     __syncwarp();
     if (!ok) return;
-    const float op = 1.f / (1.f + expf(-logit[i]));
+    const float op = 1.f / (1.f + expf(-lg));
     float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
     const float dinv = rsqrtf(dx * dx + dy * dy + dz * dz);
     float Y[16];
@@ -816,20 +819,35 @@ __global__ void __launch_bounds__(128) k_preprocess2d_bwd(int n, const float* __
     const int warp_first = blockIdx.x * 128 + warp * 32;
     if (warp_first >= n) return;  // whole warp
     const int i = warp_first + lane;
-    // only surfels with radius > 0 have non-zero gradients: load their SH rows only
+    // only surfels with radius > 0 have non-zero gradients: load their SH rows only. The rows'
+    // copies, the parameters and the record gradient are all in flight before the first wait.
     const unsigned seen = __ballot_sync(0xffffffffu, i < n && radius[i] > 0);
     float* tile = tile_all[warp];
-    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    const bool live = i < n && ((seen >> lane) & 1u);
+    float pm[3] = {0.f, 0.f, 0.f}, pq[4] = {1.f, 0.f, 0.f, 0.f}, ls0 = 0.f, ls1 = 0.f, lg = 0.f;
+    float4 gi4[4] = {};
+    if (live) {
+        pm[0] = mean3d[3 * i]; pm[1] = mean3d[3 * i + 1]; pm[2] = mean3d[3 * i + 2];
+        pq[0] = quat[4 * i]; pq[1] = quat[4 * i + 1]; pq[2] = quat[4 * i + 2]; pq[3] = quat[4 * i + 3];
+        ls0 = log_scale[3 * i];
+        ls1 = log_scale[3 * i + 1];
+        lg = logit[i];
+        const float4* g4 = reinterpret_cast<const float4*>(grad) + 4 * (size_t)i;
+        gi4[0] = g4[0]; gi4[1] = g4[1]; gi4[2] = g4[2]; gi4[3] = g4[3];
+    }
+    cp_async_wait_all();
     __syncwarp();
     float* my = tile + lane * (K3 + 1);  // this thread's coefficients, then its SH gradients
     float gr[9] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float dlg = 0.f;
-    if (i < n && ((seen >> lane) & 1u)) {
-        const float* gi = grad + kS2 * (size_t)i;
+    if (live) {
+        const float gi[16] = {gi4[0].x, gi4[0].y, gi4[0].z, gi4[0].w, gi4[1].x, gi4[1].y, gi4[1].z, gi4[1].w,
+                              gi4[2].x, gi4[2].y, gi4[2].z, gi4[2].w, gi4[3].x, gi4[3].y, gi4[3].z, gi4[3].w};
         D m[3], q[4];
-        for (int k = 0; k < 3; ++k) m[k] = D::var(mean3d[3 * i + k], k);
-        const D lsu = D::var(log_scale[3 * i], 3), lsv = D::var(log_scale[3 * i + 1], 4);
-        for (int k = 0; k < 4; ++k) q[k] = D::var(quat[4 * i + k], 5 + k);
+        for (int k = 0; k < 3; ++k) m[k] = D::var(pm[k], k);
+        const D lsu = D::var(ls0, 3), lsv = D::var(ls1, 4);
+        for (int k = 0; k < 4; ++k) q[k] = D::var(pq[k], 5 + k);
         D rec[11];
         float half[2];
         if (surfel_geometry<D>(m, lsu, lsv, q, cam, rec, half)) {
@@ -839,11 +857,11 @@ __global__ void __launch_bounds__(128) k_preprocess2d_bwd(int n, const float* __
                 for (int v = 0; v < 9; ++v) gr[v] = __fmaf_rn(gf, rec[f].d[v], gr[v]);
             }
         }
-        const float op = 1.f / (1.f + expf(-logit[i]));
+        const float op = 1.f / (1.f + expf(-lg));
         dlg = gi[11] * op * (1.f - op);
         // colour = sum_k Y_k sh_k + 0.5 clamped at 0; the direction depends on the mean
-        float vx = mean3d[3 * i] - cam.campos[0], vy = mean3d[3 * i + 1] - cam.campos[1];
-        float vz = mean3d[3 * i + 2] - cam.campos[2];
+        float vx = pm[0] - cam.campos[0], vy = pm[1] - cam.campos[1];
+        float vz = pm[2] - cam.campos[2];
         const float vinv = rsqrtf(vx * vx + vy * vy + vz * vz);
         const float ux = vx * vinv, uy = vy * vinv, uz = vz * vinv;
         float Y[16];

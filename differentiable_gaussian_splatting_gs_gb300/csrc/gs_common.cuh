@@ -103,9 +103,10 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // Copies the SH coefficients of the warp's 32 Gaussians (contiguous K3 floats each) between global
 // memory and a padded shared-memory tile (row stride K3 + 1: conflict-free per-thread rows) with
 // coalesced accesses, for the rows whose bit is set in `rows` (lane order). LOAD: global -> shared
-// (asynchronous copies, waited for before returning; the caller then synchronises the warp);
-// else shared -> global (ADD: added to global).
-template <int K3, bool LOAD, bool ADD>
+// (asynchronous copies, waited for before returning unless WAIT is false, in which case the
+// caller waits with cp_async_wait_all; the caller then synchronises the warp); else shared ->
+// global (ADD: added to global).
+template <int K3, bool LOAD, bool ADD, bool WAIT = true>
 __device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, int n, int lane, unsigned rows) {
     const int cnt = min(32, n - first);
     if (cnt <= 0 || rows == 0u) return;
@@ -120,7 +121,7 @@ __device__ __forceinline__ void sh_tile_copy(float* tile, float* g, int first, i
         else if (ADD) gw[e] += tile[row * (K3 + 1) + col];
         else gw[e] = tile[row * (K3 + 1) + col];
     }
-    if (LOAD) cp_async_wait_all();
+    if (LOAD && WAIT) cp_async_wait_all();
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {

@@ -155,12 +155,16 @@ __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* 
             rec[3 * i + 2] = z4;
         }
     }
-    // SH coefficients of the warp's visible Gaussians only, with coalesced loads
+    // SH coefficients of the warp's visible Gaussians only, with coalesced loads (the opacity
+    // logit is loaded while they are in flight)
     float* tile = tile_all[warp];
-    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, __ballot_sync(0xffffffffu, ok));
+    sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane,
+                                         __ballot_sync(0xffffffffu, ok));
+    const float lg = ok ? logit[i] : 0.f;
+    cp_async_wait_all();
     __syncwarp();
     if (!ok) return;
-    const float op = 1.f / (1.f + expf(-logit[i]));
+    const float op = 1.f / (1.f + expf(-lg));
     // view direction from the camera centre to the mean
     float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
     const float dinv = rsqrtf(dx * dx + dy * dy + dz * dz);
@@ -198,34 +202,35 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     float* tile = tile_all[warp];
     const int warp_first = blockIdx.x * kBwdThreads + warp * 32;
     const int i = warp_first + lane;
-    // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only
+    // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only. The rows'
+    // copies, the geometry and the 2D gradients are all in flight before the first wait.
     const unsigned seen = __ballot_sync(0xffffffffu, i < n && radius[i] > 0);
-    sh_tile_copy<K3, true, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    bool live = i < n && ((seen >> lane) & 1u);
+    float m[3] = {0.f, 0.f, 0.f}, ls[3] = {0.f, 0.f, 0.f}, q[4] = {1.f, 0.f, 0.f, 0.f}, lg = 0.f;
+    float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0, g2 = g0;
+    if (live) {
+        m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
+        ls[0] = log_scale[3 * i]; ls[1] = log_scale[3 * i + 1]; ls[2] = log_scale[3 * i + 2];
+        q[0] = quat[4 * i]; q[1] = quat[4 * i + 1]; q[2] = quat[4 * i + 2]; q[3] = quat[4 * i + 3];
+        g0 = grad2d[3 * i]; g1 = grad2d[3 * i + 1]; g2 = grad2d[3 * i + 2];
+        lg = logit[i];
+    }
+    cp_async_wait_all();
     __syncwarp();
     float* my = tile + lane * (K3 + 1);   // this thread's coefficients, then its SH gradients
     float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
-    bool live = false;
     Geo g;
-    float m[3] = {0.f, 0.f, 0.f};
-    if (i < n) {
-        live = (seen >> lane) & 1u;
-        if (live) {
-            m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
-            const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
-            const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
-            live = geometry(m, ls, q, cam, g);
-        }
-    }
+    if (live) live = geometry(m, ls, q, cam, g);
     if (i < n && !live) {
         for (int k = 0; k < K3; ++k) my[k] = 0.f;
     }
     if (i < n && live) {
-    const float4 g0 = grad2d[3 * i], g1 = grad2d[3 * i + 1], g2 = grad2d[3 * i + 2];
     const float dmx = g0.x, dmy = g0.y, dA = g0.z, dB = g0.w, dC = g1.x, dop = g1.y;
     const float drgb[3] = {g1.z, g1.w, g2.x};
 
     // opacity = sigmoid(logit)
-    const float op = 1.f / (1.f + expf(-logit[i]));
+    const float op = 1.f / (1.f + expf(-lg));
     dlg = dop * op * (1.f - op);
 
     // colour = sum_k Y_k sh_k + 0.5, clamped at 0
