@@ -6,6 +6,9 @@ scene: 1.6M Gaussians, 1297x840, SH degree 3, a 64-cluster mixture (seeded, synt
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--mode sm|direct|warp|adaptive]
 
+The step is captured once into a CUDA graph (every kernel of the step, with the sort call that
+does not synchronise) and each timed step is one replay; `--no-graph` times eager launches.
+
 Prints one JSON line. `value` is the whole-job throughput in Mpix/s (pixels of all ranks' views
 per second of the slowest rank), measured with CUDA events on the device with inputs resident;
 `e2e` is the same metric with each step's inputs copied from pinned host memory and its
@@ -65,6 +68,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the update phase after the step")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of one CUDA graph replay per step")
+    ap.add_argument("--sync-sort", action="store_true",
+                    help="time the step with the synchronising sort call (reads D on the host) instead of the "
+                         "call that keeps the whole step enqueued ahead of the GPU")
     ap.add_argument("--config", type=int, default=CFG, choices=sorted(WORKLOADS),
                     help="workload; the default is the one the metric is quoted on")
     return ap.parse_args()
@@ -274,14 +282,23 @@ def run_ours(args, rank, world, local_rank):
 
     cams = [api.make_camera(c) for c in scene.cameras]
 
+    n_dup_dev = torch.zeros(n_views, dtype=torch.int64, device=dev)
+    sort_sync = [True]  # the warm-up steps size the sort buffers with the synchronising call
+
     def one_step(ev_bwd=None, ev_fwd=None):
         """All views of one step; the views' parameter gradients are summed. ev_bwd / ev_fwd: one
-        event pair per view around the backward / forward raster."""
+        event pair per view around the backward / forward raster. After the warm-up the sort does
+        not synchronise (the whole step is enqueued ahead of the GPU) and D lands in n_dup_dev."""
         n_dup = 0
         for v, c in enumerate(cams):
             proj = api.gs_preprocess(params, c, opt, out=bufs.proj)
             image, t_final, n_contrib, dl, ranges = bufs.image_buffers(c.width, c.height)
-            b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges, want_keys=False)
+            if sort_sync[0]:
+                b = api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, ranges=ranges, want_keys=False)
+                n_dup += b.n_dup
+            else:
+                b = api.gs_bin_and_sort_async(proj, c, opt, bufs.sort.capacity, buffers=bufs.sort, ranges=ranges,
+                                              n_dup=n_dup_dev[v:v + 1])
             if ev_fwd is not None:
                 ev_fwd[v][0].record(stream)
             api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib))
@@ -294,7 +311,6 @@ def run_ours(args, rank, world, local_rank):
             if ev_bwd is not None:
                 ev_bwd[v][1].record(stream)
             api.gs_preprocess_bwd(params, c, opt, proj, bufs.grad2d, out=grads, accumulate=v > 0)
-            n_dup += b.n_dup
         return n_dup
 
     def barrier():
@@ -303,8 +319,31 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(max(args.warmup, 3)):
         n_dup = one_step()
+    sort_sync[0] = args.sync_sort
+    one_step()  # the step as timed, once more untimed
     torch.cuda.synchronize()
     assert api.gs_device_error() == 0
+
+    # ---- the step as one CUDA graph: every kernel of the step with one host launch. The raster
+    # kernels' events are captured in the graph as event record nodes (external events), so they
+    # are timed inside each replay of the timed region.
+    use_graph = not (args.no_graph or args.sync_sort)
+    if use_graph:
+        try:
+            torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:  # a torch without external events: the eager step is timed instead
+            use_graph = False
+    gstep = None
+    if use_graph:
+        def xev():
+            return torch.cuda.Event(enable_timing=True, external=True)
+        gev = [((xev(), xev()), (xev(), xev())) for _ in cams]
+        gstep = step.GraphedStep(params, cams, [target[v] for v in range(n_views)], opt, grads, bufs,
+                                 bufs.sort.capacity, events=gev)
+        for _ in range(3):
+            gstep.replay()
+        torch.cuda.synchronize()
+        assert api.gs_device_error() == 0
 
     # ---- device-resident timing: K steps, L2 flushed between steps (outside the events)
     step_ms, bwd_ms, fwd_ms = [], [], []
@@ -315,18 +354,32 @@ def run_ours(args, rank, world, local_rank):
         for _ in range(args.steps):
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            eb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
-            ef = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
-            e0.record(stream)
-            n_dup = one_step(eb, ef)
-            e1.record(stream)
+            if use_graph:
+                ef, eb = [e[0] for e in gev], [e[1] for e in gev]
+                e0.record(stream)
+                gstep.replay()
+                e1.record(stream)
+            else:
+                eb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
+                ef = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in cams]
+                e0.record(stream)
+                one_step(eb, ef)
+                e1.record(stream)
             torch.cuda.synchronize()
             step_ms.append(e0.elapsed_time(e1))
             bwd_ms.append(sum(e[0].elapsed_time(e[1]) for e in eb) / n_views)  # per view
             fwd_ms.append(sum(e[0].elapsed_time(e[1]) for e in ef) / n_views)
     barrier()
     torch.cuda.synchronize()
-    launches = lib.gs_kernel_launches() - launches0
+    # kernels replayed from a graph are counted once at capture: per replay times the replays
+    launches = gstep.launches * args.steps if use_graph else lib.gs_kernel_launches() - launches0
+    assert api.gs_device_error() == 0
+    if use_graph:
+        n_dup = int(gstep.n_dup.sum())
+    elif not args.sync_sort:
+        n_dup = int(n_dup_dev.sum())
+    launch_mode = (f"one CUDA graph per step ({gstep.launches} library kernels)" if use_graph else
+                   "eager launches" + (", synchronising sort" if args.sync_sort else ", non-synchronising sort"))
     ms = reduce_max(sum(step_ms) / len(step_ms), world, dev)
     value = throughput_mpix(world, P, ms)
 
@@ -344,7 +397,10 @@ def run_ours(args, rank, world, local_rank):
             for k in names:
                 params[k].copy_(host[k], non_blocking=True)
             target.copy_(host_target, non_blocking=True)
-            one_step()
+            if use_graph:
+                gstep.replay()
+            else:
+                one_step()
             for k in names:
                 host_grads[k].copy_(grads[k], non_blocking=True)
             e1.record(stream)
@@ -359,6 +415,20 @@ def run_ours(args, rank, world, local_rank):
     # ---- the update phase after the step (not part of the fwd+bwd metric): sparse Adam over the
     # Gaussians the view made visible, timed alone with L2 flushed before each launch
     extras = {}
+    if not args.no_extras and use_graph:
+        # the same step with eager launches (non-synchronising sort), for comparison with the graph
+        q_ms = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            one_step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            q_ms.append(e0.elapsed_time(e1))
+        qm = sum(q_ms) / len(q_ms)
+        extras["eager_step"] = {"ms_per_step": qm, "mpix_per_s": P / (qm / 1e3) / 1e6}
+        assert api.gs_device_error() == 0
     if not args.no_extras:
         exp_avg = {k: torch.zeros_like(params[k]) for k in names}
         exp_avg_sq = {k: torch.zeros_like(params[k]) for k in names}
@@ -495,7 +565,7 @@ def run_ours(args, rank, world, local_rank):
             "config": {"workload": WORKLOADS[args.config], "n_gaussians": scene.n, "width": cam.width,
                        "height": cam.height, "views_per_step": n_views, "duplicates": int(n_dup), "bwd_mode": args.mode,
                        "l2": "flushed between timed steps (256 MB write, outside the events)",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}", "launch": launch_mode},
             "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
             "bwd_ms": bwd_avg_ms, "fwd_ms": sum(fwd_ms) / len(fwd_ms), "ms_per_view": ms / n_views, "step_ms_min": min(step_ms), "extras": extras}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and n_views == 1:

@@ -30,7 +30,7 @@ EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_re
            "gs_preprocess_bwd", "gs_status_string", "gs_last_error_message", "gs_device_error",
            "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static", "gs_adam_step",
            "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim", "gs_preprocess2d",
-           "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd")
+           "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd", "gs_bin_and_sort_async")
 GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
 
 
@@ -107,6 +107,8 @@ def load():
         lib.gs_selftest_timeout.argtypes = [C.c_uint32, P]
         lib.gs_bin_and_sort_static.argtypes = [pproj, pcam, popt, P, P, I64, C.POINTER(I64), P, P]
         lib.gs_bin_and_sort_static.restype = C.c_int
+        lib.gs_bin_and_sort_async.argtypes = [pproj, pcam, popt, P, C.c_size_t, P, P, I64, P, P, P]
+        lib.gs_bin_and_sort_async.restype = C.c_int
         lib.gs_kernel_launches.argtypes = []
         lib.gs_kernel_launches.restype = C.c_int64
         pten = C.POINTER(gs_tensors)

@@ -20,7 +20,8 @@ from ._abi import (GS_BWD_ADAPTIVE, GS_BWD_DIRECT, GS_BWD_SM, GS_BWD_WARP, GS_ER
                    gs_camera, gs_options, gs_params, gs_proj)
 
 __all__ = ["Proj", "BinResult", "make_camera", "make_options", "alloc_proj", "gs_preprocess",
-           "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd", "gs_preprocess_bwd",
+           "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_bin_and_sort_async", "gs_render_fwd", "gs_render_bwd",
+           "gs_preprocess_bwd",
            "gs_device_error", "GsError", "GS_BWD_DIRECT", "GS_BWD_WARP", "GS_BWD_ADAPTIVE", "GS_BWD_SM"]
 
 
@@ -147,7 +148,7 @@ class BinResult:
     keys: torch.Tensor | None   # [D] int64 (uint64 bits: tile << 32 | depth bits)
     vals: torch.Tensor          # [D] int32 Gaussian indices
     ranges: torch.Tensor        # [T, 2] int32: [start, end) per tile
-    n_dup: int
+    n_dup: int | torch.Tensor  # D (a device int64 tensor [1] from gs_bin_and_sort_async)
 
 
 class SortBuffers:
@@ -198,6 +199,31 @@ def gs_bin_and_sort(proj: Proj, cam, opt: gs_options, capacity: int | None = Non
         D = int(d.value)
         return BinResult(keys=buffers.keys[:D] if want_keys else None, vals=buffers.vals[:D], ranges=ranges, n_dup=D)
     raise AssertionError("unreachable")
+
+
+def gs_bin_and_sort_async(proj: Proj, cam, opt: gs_options, capacity: int, buffers: SortBuffers | None = None,
+                          want_keys: bool = False, ranges: torch.Tensor | None = None,
+                          n_dup: torch.Tensor | None = None, static_workspace: bool = False,
+                          stream=None) -> BinResult:
+    """gs_bin_and_sort without host synchronisation (capturable in a CUDA graph). The result's
+    vals / keys span the whole capacity and its n_dup is a device int64 tensor [1] holding D;
+    overflowing the capacity leaves empty ranges and a device check error."""
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    dev = proj.rec.device
+    T = ((c.width + 15) // 16) * ((c.height + 15) // 16)
+    if ranges is None:
+        ranges = torch.empty((T, 2), dtype=torch.int32, device=dev)
+    if n_dup is None:
+        n_dup = torch.zeros(1, dtype=torch.int64, device=dev)
+    buffers = buffers or SortBuffers(dev)
+    buffers.ensure(0 if static_workspace else proj.n, capacity, c.width, c.height, want_keys)
+    ps = proj.struct()
+    ws = None if static_workspace else buffers.workspace
+    check(_abi.load().gs_bin_and_sort_async(C.byref(ps), C.byref(c), C.byref(opt), _ptr(ws) if ws is not None else None,
+                                            ws.numel() if ws is not None else 0,
+                                            _ptr(buffers.keys) if want_keys else None, _ptr(buffers.vals), capacity,
+                                            _ptr(n_dup), _ptr(ranges), _stream(stream)), "gs_bin_and_sort_async")
+    return BinResult(keys=buffers.keys if want_keys else None, vals=buffers.vals, ranges=ranges, n_dup=n_dup)
 
 
 def gs_render_fwd(proj: Proj, vals: torch.Tensor, ranges: torch.Tensor, cam, opt: gs_options, out=None, stream=None):
@@ -353,6 +379,12 @@ def gs_preprocess2d_bwd(params: dict, cam, opt: gs_options, proj: Proj, grad2d, 
                                           _ptr(out["opacity_logit"]), _ptr(out["sh"]), int(bool(accumulate)),
                                           _stream(stream)), "gs_preprocess2d_bwd")
     return out
+
+
+def gs_kernel_launches() -> int:
+    """Number of kernels this library has launched in the process (a host-side counter; kernels
+    replayed from a CUDA graph are counted once, at capture)."""
+    return int(_abi.load().gs_kernel_launches())
 
 
 def gs_device_error(stream=None) -> int:

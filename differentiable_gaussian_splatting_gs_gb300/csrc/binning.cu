@@ -799,10 +799,18 @@ __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __res
     if (threadIdx.x == 0) total[0] = carry;
 }
 
+// Tile ranges from the tile starts and totals. When the duplicates exceed the capacity (possible
+// only for the call that does not read D on the host) every range is written empty, so that no
+// later kernel reads past the caller's list, and the check bit is set.
 __global__ void k_write_ranges(int T, const unsigned* __restrict__ tile_start, const unsigned* __restrict__ tile_total,
-                               uint2* __restrict__ ranges) {
+                               const unsigned long long* __restrict__ total, unsigned long long capacity,
+                               uint2* __restrict__ ranges, unsigned* __restrict__ err) {
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t < T) ranges[t] = tile_total[t] ? make_uint2(tile_start[t], tile_start[t] + tile_total[t]) : make_uint2(0u, 0u);
+    const bool over = *total > capacity;
+    if (over && t == 0) atomicOr(err, kErrCheck);
+    if (t < T)
+        ranges[t] = (!over && tile_total[t]) ? make_uint2(tile_start[t], tile_start[t] + tile_total[t])
+                                             : make_uint2(0u, 0u);
 }
 
 // Placement: one warp per (chunk, band of tile rows). The warp copies the chunk's starting offset
@@ -1034,6 +1042,33 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
 
 // Phase 2: placement (counting pass) or emission + tile radix passes, and the ranges.
 // d = number of duplicates (<= capacity).
+// Counting-path emission: the tile ranges and the placement of every entry. Reads no count on the
+// host (the number of chunks and the total stay on the device).
+static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, unsigned long long capacity,
+                                 const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
+                                 unsigned* err, cudaStream_t st) {
+    const long long T = (long long)tiles_x * tiles_y;
+    const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
+    unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
+    cudaError_t e;
+    count_launches(1);
+    k_write_ranges<<<(int)((T + 255) / 256), 256, 0, st>>>((int)T, w.tile_start, w.tile_total, w.total, capacity,
+                                                           reinterpret_cast<uint2*>(ranges), err);
+    const int band_rows = (tiles_y + kPlaceBands - 1) / kPlaceBands;
+    const int nbands = (tiles_y + band_rows - 1) / band_rows;
+    const size_t band_bytes = (size_t)band_rows * tiles_x * 4;
+    int wpb = (int)((200 * 1024) / band_bytes);
+    wpb = wpb < 1 ? 1 : (wpb > kPlaceWarps ? kPlaceWarps : wpb);
+    const size_t smem = (size_t)wpb * band_bytes;
+    if ((e = cudaFuncSetAttribute(k_chunk_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
+    const long long warps = w.cmax * nbands;
+    count_launches(1);
+    k_chunk_place<<<(unsigned)((warps + wpb - 1) / wpb), 32 * wpb, smem, st>>>(
+        w.nchunks, w.chunk_first, w.dvB, w.crect, tiles_x, tiles_y, band_rows, nbands, w.table, w.tile_start,
+        (unsigned)capacity, vals, k64, depth_bits, err);
+    return cudaGetLastError();
+}
+
 cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
                           cudaStream_t st) {
@@ -1046,25 +1081,7 @@ cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigne
     }
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
-    if (counting_path(T)) {
-        count_launches(1);
-        k_write_ranges<<<(int)((T + 255) / 256), 256, 0, st>>>((int)T, w.tile_start, w.tile_total,
-                                                               reinterpret_cast<uint2*>(ranges));
-        const int band_rows = (tiles_y + kPlaceBands - 1) / kPlaceBands;
-        const int nbands = (tiles_y + band_rows - 1) / band_rows;
-        const size_t band_bytes = (size_t)band_rows * tiles_x * 4;
-        int wpb = (int)((200 * 1024) / band_bytes);
-        wpb = wpb < 1 ? 1 : (wpb > kPlaceWarps ? kPlaceWarps : wpb);
-        const size_t smem = (size_t)wpb * band_bytes;
-        if ((e = cudaFuncSetAttribute(k_chunk_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
-            return e;
-        const long long warps = w.cmax * nbands;
-        count_launches(1);
-        k_chunk_place<<<(unsigned)((warps + wpb - 1) / wpb), 32 * wpb, smem, st>>>(
-            w.nchunks, w.chunk_first, w.dvB, w.crect, tiles_x, tiles_y, band_rows, nbands, w.table, w.tile_start,
-            (unsigned)capacity, vals, k64, depth_bits, err);
-        return cudaGetLastError();
-    }
+    if (counting_path(T)) return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, ranges, err, st);
     const int tb = tile_bits_of(T);
     const int passes = (tb + 7) / 8;
     unsigned* tbuf[2] = {w.tA, w.tB};
@@ -1090,6 +1107,24 @@ cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigne
     count_launches(1);
     k_ranges<<<(d + 1023) / 1024, 256, 0, st>>>(d, tbuf[cur], reinterpret_cast<uint2*>(ranges));
     return cudaGetLastError();
+}
+
+// The whole binning and sort with no host synchronisation (counting path only): D is copied to
+// n_dup_dev (when given) on the stream; duplicates beyond the capacity are dropped, every range is
+// written empty and the check bit is set.
+cudaError_t bin_sort_async(const gs_proj& proj, int tiles_x, int tiles_y, unsigned long long capacity,
+                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
+                           unsigned long long* n_dup_dev, unsigned* err, unsigned spin_limit, cudaStream_t st) {
+    const long long T = (long long)tiles_x * tiles_y;
+    cudaError_t e = bin_count(proj, tiles_x, tiles_y, w, err, spin_limit, st);
+    if (e) return e;
+    if (proj.n == 0) {
+        e = cudaMemsetAsync(ranges, 0, (size_t)T * 8, st);
+    } else {
+        e = emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, ranges, err, st);
+    }
+    if (e || !n_dup_dev) return e;
+    return cudaMemcpyAsync(n_dup_dev, w.total, 8, cudaMemcpyDeviceToDevice, st);
 }
 
 }  // namespace gs

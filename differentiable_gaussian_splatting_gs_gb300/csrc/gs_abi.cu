@@ -306,6 +306,42 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
     return e ? cuda_fail(e, "gs_bin_and_sort_static: emit/sort") : GS_OK;
 }
 
+int gs_bin_and_sort_async(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, void* workspace,
+                          size_t workspace_bytes, uint64_t* keys, uint32_t* vals, int64_t capacity,
+                          uint64_t* n_dup_device, uint32_t* tile_ranges, void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_proj_n(proj))) return s;
+    if (capacity < 0 || capacity > 0x7fffffffll) return fail(GS_ERR_ARG, "capacity outside 0..2^31-1");
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or not 8-byte aligned");
+    if (capacity > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
+    if (keys && !aligned(keys, 8)) return fail(GS_ERR_ARG, "keys not 8-byte aligned");
+    if (n_dup_device && !aligned(n_dup_device, 8)) return fail(GS_ERR_ARG, "n_dup_device not 8-byte aligned");
+    const long long tiles = (long long)kc.tiles_x * kc.tiles_y;
+    if (!counting_path(tiles))
+        return fail(GS_ERR_ARG, "%lld tiles: the call without host synchronisation handles images of up to 49152 "
+                    "tiles; use gs_bin_and_sort", tiles);
+    const size_t need = carve_workspace(nullptr, proj->n, capacity, tiles).bytes;
+    unsigned char* base = static_cast<unsigned char*>(workspace);
+    if (!workspace) {
+        if (need > (size_t)GS_STATIC_SORT_WORKSPACE_BYTES)
+            return fail(GS_ERR_ARG, "n = %lld with capacity %lld needs %zu bytes of sort workspace; the static "
+                        "workspace holds %u bytes: pass a workspace", (long long)proj->n, (long long)capacity, need,
+                        (unsigned)GS_STATIC_SORT_WORKSPACE_BYTES);
+        if (!(base = static_sort_workspace(&s))) return s;
+    } else if (workspace_bytes < need || !aligned(workspace, 256)) {
+        return fail(GS_ERR_ARG, "workspace not 256-byte aligned or smaller than %zu bytes", need);
+    }
+    const SortWorkspace w = carve_workspace(base, proj->n, capacity, tiles);
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaError_t e = bin_sort_async(*proj, kc.tiles_x, kc.tiles_y, (unsigned long long)capacity, w, keys, vals,
+                                   tile_ranges, reinterpret_cast<unsigned long long*>(n_dup_device), err, o.spin,
+                                   as_stream(stream));
+    return e ? cuda_fail(e, "gs_bin_and_sort_async") : GS_OK;
+}
+
 int gs_render_fwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges, const gs_camera* cam,
                   const gs_options* opt, float* image, float* t_final, uint32_t* n_contrib, void* stream) {
     Opts o;

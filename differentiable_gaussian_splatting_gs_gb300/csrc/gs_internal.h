@@ -39,6 +39,10 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
 cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
                           cudaStream_t st);
+cudaError_t bin_sort_async(const gs_proj& proj, int tiles_x, int tiles_y, unsigned long long capacity,
+                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
+                           unsigned long long* n_dup_dev, unsigned* err, unsigned spin_limit, cudaStream_t st);
+bool counting_path(long long tiles);
 
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
                               cudaStream_t st);

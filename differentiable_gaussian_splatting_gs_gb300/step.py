@@ -56,3 +56,65 @@ def train_step(params: dict, cameras, targets, opt, grads: dict, buffers: StepBu
         api.gs_preprocess_bwd(params, c, opt, proj, buffers.grad2d, out=grads, accumulate=v > 0, stream=stream)
         n_dups.append(b.n_dup)
     return {"n_dup": n_dups, "image": image}
+
+
+def train_step_async(params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
+                     n_dup: torch.Tensor, events=None, stream=None):
+    """train_step without any host synchronisation: the sort is gs_bin_and_sort_async with a
+    fixed capacity, and the views' duplicate counts land in the device tensor n_dup [views]
+    (a view whose count exceeds the capacity renders nothing and sets the device check error).
+    events: optional per view ((fwd start, fwd end), (bwd start, bwd end)) recorded around the
+    two raster kernels (on the current stream)."""
+    image = None
+    for v, (cam, target) in enumerate(zip(cameras, targets)):
+        ev = events[v] if events is not None else None
+        c = cam if isinstance(cam, api.gs_camera) else api.make_camera(cam)
+        proj = api.gs_preprocess(params, c, opt, out=buffers.proj, stream=stream)
+        image, t_final, n_contrib, dl, ranges = buffers.image_buffers(c.width, c.height)
+        b = api.gs_bin_and_sort_async(proj, c, opt, capacity, buffers=buffers.sort, ranges=ranges,
+                                      n_dup=n_dup[v:v + 1], stream=stream)
+        if ev is not None:
+            ev[0][0].record()
+        api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib), stream=stream)
+        if ev is not None:
+            ev[0][1].record()
+        torch.sub(image, target, out=dl)
+        if ev is not None:
+            ev[1][0].record()
+        api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=buffers.grad2d,
+                          stream=stream)
+        if ev is not None:
+            ev[1][1].record()
+        api.gs_preprocess_bwd(params, c, opt, proj, buffers.grad2d, out=grads, accumulate=v > 0, stream=stream)
+    return image
+
+
+class GraphedStep:
+    """The step of fixed views (train_step_async) captured into one CUDA graph: replay() runs
+    every kernel of the step with one launch from the host. Inputs are read from, and gradients
+    written to, the same tensors at every replay (update them in place between replays)."""
+
+    def __init__(self, params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
+                 events=None):
+        """events: as for train_step_async; to time kernels inside the graph they must be created
+        with torch.cuda.Event(enable_timing=True, external=True), which captures them as event
+        record nodes."""
+        self.device = buffers.device
+        self.cams = [c if isinstance(c, api.gs_camera) else api.make_camera(c) for c in cameras]
+        self.n_dup = torch.zeros(len(self.cams), dtype=torch.int64, device=self.device)
+        args = (params, self.cams, targets, opt, grads, buffers, capacity, self.n_dup, events)
+        # one eager run first: buffers, function attributes and device symbols are set up outside the capture
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            train_step_async(*args)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        torch.cuda.synchronize(self.device)
+        before = api.gs_kernel_launches()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            train_step_async(*args)
+        self.launches = api.gs_kernel_launches() - before  # library kernels per replay
+
+    def replay(self):
+        self.graph.replay()

@@ -155,7 +155,7 @@ size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32
  * workspace: device buffer of at least gs_sort_workspace_bytes(n, capacity, W, H) bytes.
  * Synchronises `stream` once to read D. If D > capacity, nothing is written beyond the
  * workspace, *n_dup_out = D and GS_ERR_CAPACITY is returned; call again with a larger capacity.
- * capacity must be < 2^32. Errors: GS_ERR_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA.                 */
+ * 0 <= capacity < 2^31. Errors: GS_ERR_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA.                     */
 int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options* opt,
                     void* workspace, size_t workspace_bytes, uint64_t* keys, uint32_t* vals,
                     int64_t capacity, int64_t* n_dup_out, uint32_t* tile_ranges, void* stream);
@@ -304,9 +304,10 @@ int gs_preprocess2d_bwd(const gs_params* p, const gs_camera* cam, const gs_optio
 #define GS_STATIC_SORT_WORKSPACE_BYTES (32u << 20)
 
 /* gs_bin_and_sort without a workspace argument, for callers that cannot allocate device memory:
- * code running where a cudaMalloc is not allowed or not wanted (inside a region being captured
- * into a CUDA graph, a real-time loop with a fixed memory budget, a plug-in that only receives
- * buffers from its host). It computes exactly what gs_bin_and_sort computes (same outputs, same
+ * code running where a cudaMalloc is not allowed or not wanted (a real-time loop with a fixed
+ * memory budget, a plug-in that only receives buffers from its host; for a region being captured
+ * into a CUDA graph use gs_bin_and_sort_async, which also does not synchronise). It computes
+ * exactly what gs_bin_and_sort computes (same outputs, same
  * errors) but takes its scratch space from a statically sized device array inside this library,
  * GS_STATIC_SORT_WORKSPACE_BYTES (32 MiB), which every GPU that loads the library keeps reserved
  * until the process exits. The pages describe no such entry point; it is a convenience of this
@@ -324,6 +325,25 @@ int gs_preprocess2d_bwd(const gs_params* p, const gs_camera* cam, const gs_optio
 int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, uint64_t* keys,
                            uint32_t* vals, int64_t capacity, int64_t* n_dup_out, uint32_t* tile_ranges,
                            void* stream);
+
+/* gs_bin_and_sort with no host synchronisation, so that a whole training step can be enqueued
+ * ahead of the GPU or captured into a CUDA graph (DISTWAR, Abstract: the binning of the
+ * rasterization pipeline; same outputs as gs_bin_and_sort). It neither synchronises nor
+ * allocates; every launch and copy goes on `stream`.
+ *   - D is not returned on the host: when n_dup_device (device uint64, 8-byte aligned) is not
+ *     NULL, D is copied there on the stream.
+ *   - Capacity: if D > capacity, no entry is written past `capacity`, every tile range is
+ *     written empty (so later kernels read nothing) and the device error word gets the check
+ *     bit (gs_device_error returns GS_ERR_DEVICE_CHECK); *n_dup_device then holds the D needed.
+ *   - workspace: a device buffer of gs_sort_workspace_bytes(n, capacity, W, H) bytes, or NULL
+ *     for the library's static workspace (limit and sharing rules of gs_bin_and_sort_static).
+ *   - Images of up to 49,152 tiles (the counting tile pass); larger images return GS_ERR_ARG.
+ *   - Set-up: make one call (or one call of any other entry point) on the device before a
+ *     stream capture, so that the library's device symbols are looked up outside it.
+ * Errors: GS_ERR_ARG (pointers, sizes, workspace, image size), GS_ERR_CUDA.                    */
+int gs_bin_and_sort_async(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, void* workspace,
+                          size_t workspace_bytes, uint64_t* keys, uint32_t* vals, int64_t capacity,
+                          uint64_t* n_dup_device, uint32_t* tile_ranges, void* stream);
 
 /* Text of a status code (static storage). */
 const char* gs_status_string(int status);
