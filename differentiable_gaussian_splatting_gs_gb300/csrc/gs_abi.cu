@@ -67,7 +67,9 @@ int resolve_options(const gs_options* o, Opts& r) {
     if (!o) o = &z;
     r.bwd_mode = o->bwd_mode == GS_BWD_DEFAULT ? GS_BWD_ADAPTIVE : o->bwd_mode;
     if (r.bwd_mode < GS_BWD_DIRECT || r.bwd_mode > GS_BWD_SM) return fail(GS_ERR_ARG, "bad bwd_mode %d", o->bwd_mode);
-    r.thr = o->adaptive_threshold == 0 ? 8 : o->adaptive_threshold;
+    // defaults measured on GB300 (outdoor, object and contention scenes): a warp reduction pays
+    // off only when at least 28 of the 32 lanes contribute; the shared-memory mode keeps 8
+    r.thr = o->adaptive_threshold != 0 ? o->adaptive_threshold : (r.bwd_mode == GS_BWD_SM ? 8 : 28);
     if (r.thr < 1 || r.thr > 33) return fail(GS_ERR_ARG, "adaptive_threshold %d outside 1..33", o->adaptive_threshold);
     r.deg = o->sh_degree;
     if (r.deg < 0 || r.deg > 3) return fail(GS_ERR_ARG, "sh_degree %d outside 0..3", o->sh_degree);

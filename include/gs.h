@@ -58,7 +58,9 @@ extern "C" {
  *   WARP      the warp sums its lanes' contributions in registers (shuffle reduction) and one
  *             warp instruction issues the 9 global atomics (DISTWAR, Abstract: first key idea).
  *   ADAPTIVE  per warp and Gaussian: WARP when at least `adaptive_threshold` lanes contribute,
- *             DIRECT otherwise (DISTWAR, Abstract: second key idea; ARC, title).
+ *             DIRECT otherwise (DISTWAR, Abstract: second key idea; ARC, title). Default 28: on
+ *             GB300 per-lane vector atomics are cheaper than the reduction's instructions unless
+ *             nearly every lane contributes.
  *   SM        warps add into a per-tile shared-memory accumulator (warp-reduced when at least
  *             `adaptive_threshold` lanes contribute, per lane otherwise); the tile issues one set
  *             of global atomics per Gaussian and 128-Gaussian batch.                            */
@@ -85,7 +87,7 @@ typedef struct gs_camera {
 /* Zero-initialised options select the defaults written beside each field. */
 typedef struct gs_options {
     int32_t  bwd_mode;            /* GS_BWD_*; 0 = GS_BWD_DEFAULT (the ADAPTIVE mode) */
-    int32_t  adaptive_threshold;  /* lanes, 1..32; 0 = 8 */
+    int32_t  adaptive_threshold;  /* lanes, 1..33; 0 = 28 (ADAPTIVE) or 8 (SM) */
     int32_t  sh_degree;           /* 0..3 (K = (degree + 1)^2 SH coefficients per channel) */
     int32_t  staging;             /* GS_STAGE_*; 0 = GS_STAGE_BULK */
     float    near_z;              /* cull when the view-space depth is <= near_z; 0 = 0.2 */
