@@ -253,8 +253,14 @@ __global__ void __launch_bounds__(256) k_depth_hist4(const unsigned* __restrict_
         }
 #pragma unroll
         for (int a = 0; a < kAhead; ++a) {
+            // the two low digits of the depth bits are spread over the 256 buckets: one shared
+            // atomic per lane rarely conflicts; the two high digits take few values (the depth
+            // range), so equal digits are grouped first and each group adds once
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
+            for (int p = 0; p < 2; ++p)
+                if (vv[a]) atomicAdd(&h[p][(kk[a] >> (8 * p)) & 0xffu], 1u);
+#pragma unroll
+            for (int p = 2; p < 4; ++p) {
                 const unsigned d = vv[a] ? (kk[a] >> (8 * p)) & 0xffu : 0x100u;
                 const unsigned peers = __match_any_sync(full, d);
                 if (vv[a] && (peers & lanemask_lt()) == 0u) atomicAdd(&h[p][d], (unsigned)__popc(peers));
@@ -453,41 +459,60 @@ __global__ void __launch_bounds__(256) k_count(int n_bound, const unsigned* __re
     }
 }
 
+// Single-block exclusive scans: each of the 1024 threads takes kScanItems consecutive values per
+// round, so that up to 8192 values need one round (one pass of block-wide synchronisation).
+constexpr int kScanItems = 8;
+
+// Block-wide exclusive scan of one value per thread (1024 threads); returns the thread's
+// exclusive prefix and leaves the block total in *block_total (shared).
+template <typename T>
+__device__ __forceinline__ T block_scan_1024(T v, T* wsum, T* block_total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    T x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const T y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        T w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const T y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;
+        if (lane == 31) *block_total = w;
+    }
+    __syncthreads();
+    return (warp ? wsum[warp - 1] : T(0)) + x - v;
+}
+
 // Exclusive scan of the block sums (single block); total[0] = sum of all.
 __global__ void __launch_bounds__(1024) k_scan_u64(const unsigned long long* __restrict__ in, int m,
                                                    unsigned long long* __restrict__ out,
                                                    unsigned long long* __restrict__ total) {
     __shared__ unsigned long long wsum[32];
-    __shared__ unsigned long long carry;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) carry = 0ull;
-    __syncthreads();
-    for (int base = 0; base < m; base += 1024) {
-        const int i = base + threadIdx.x;
-        const unsigned long long v = i < m ? in[i] : 0ull;
-        unsigned long long x = v;
+    __shared__ unsigned long long round_total;
+    unsigned long long carry = 0;
+    for (int base = 0; base < m; base += 1024 * kScanItems) {
+        const int i0 = base + threadIdx.x * kScanItems;
+        unsigned long long v[kScanItems], sum = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+        for (int k = 0; k < kScanItems; ++k) {
+            v[k] = i0 + k < m ? in[i0 + k] : 0ull;
+            sum += v[k];
         }
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            unsigned long long s = wsum[lane];
+        unsigned long long run = carry + block_scan_1024(sum, wsum, &round_total);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += y;
-            }
-            wsum[lane] = s;
+        for (int k = 0; k < kScanItems; ++k) {
+            if (i0 + k < m) out[i0 + k] = run;
+            run += v[k];
         }
-        __syncthreads();
-        const unsigned long long wpre = warp ? wsum[warp - 1] : 0ull;
-        if (i < m) out[i] = carry + wpre + x - v;
-        __syncthreads();
-        if (threadIdx.x == 0) carry += wsum[31];
-        __syncthreads();
+        carry += round_total;
+        __syncthreads();  // wsum and round_total are rewritten by the next round
     }
     if (threadIdx.x == 0) total[0] = carry;
 }
@@ -760,57 +785,43 @@ __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* 
     }
 }
 
-// Exclusive scan of the tile totals (one block): tile_start[t]; total[0] = D.
+// Exclusive scan of the tile totals (one block): tile_start[t], total[0] = D, and the tile
+// ranges [start, start + count). When D exceeds the capacity every range is written empty, so
+// that no later kernel reads past the caller's list; with `err` (the call that does not read D on
+// the host) the check bit is also set.
 __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __restrict__ tile_total,
                                                     unsigned* __restrict__ tile_start,
-                                                    unsigned long long* __restrict__ total) {
+                                                    unsigned long long* __restrict__ total,
+                                                    unsigned long long capacity, uint2* __restrict__ ranges,
+                                                    unsigned* __restrict__ err) {
     __shared__ unsigned long long wsum[32];
-    __shared__ unsigned long long carry;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) carry = 0ull;
-    __syncthreads();
-    for (int base = 0; base < T; base += 1024) {
-        const int i = base + threadIdx.x;
-        const unsigned long long v = i < T ? tile_total[i] : 0ull;
-        unsigned long long x = v;
+    __shared__ unsigned long long round_total;
+    unsigned long long carry = 0;
+    for (int base = 0; base < T; base += 1024 * kScanItems) {
+        const int t0 = base + threadIdx.x * kScanItems;
+        unsigned v[kScanItems];
+        unsigned long long sum = 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+        for (int k = 0; k < kScanItems; ++k) {
+            v[k] = t0 + k < T ? tile_total[t0 + k] : 0u;
+            sum += v[k];
         }
-        if (lane == 31) wsum[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            unsigned long long s2 = wsum[lane];
+        unsigned long long run = carry + block_scan_1024(sum, wsum, &round_total);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, s2, o);
-                if (lane >= o) s2 += y;
-            }
-            wsum[lane] = s2;
+        for (int k = 0; k < kScanItems; ++k) {
+            if (t0 + k < T) tile_start[t0 + k] = (unsigned)run;
+            run += v[k];
         }
-        __syncthreads();
-        const unsigned long long wpre = warp ? wsum[warp - 1] : 0ull;
-        if (i < T) tile_start[i] = (unsigned)(carry + wpre + x - v);
-        __syncthreads();
-        if (threadIdx.x == 0) carry += wsum[31];
+        carry += round_total;
         __syncthreads();
     }
     if (threadIdx.x == 0) total[0] = carry;
-}
-
-// Tile ranges from the tile starts and totals. When the duplicates exceed the capacity (possible
-// only for the call that does not read D on the host) every range is written empty, so that no
-// later kernel reads past the caller's list, and the check bit is set.
-__global__ void k_write_ranges(int T, const unsigned* __restrict__ tile_start, const unsigned* __restrict__ tile_total,
-                               const unsigned long long* __restrict__ total, unsigned long long capacity,
-                               uint2* __restrict__ ranges, unsigned* __restrict__ err) {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    const bool over = *total > capacity;
-    if (over && t == 0) atomicOr(err, kErrCheck);
-    if (t < T)
-        ranges[t] = (!over && tile_total[t]) ? make_uint2(tile_start[t], tile_start[t] + tile_total[t])
-                                             : make_uint2(0u, 0u);
+    const bool over = carry > capacity;
+    if (over && err && threadIdx.x == 0) atomicOr(err, kErrCheck);
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {  // the last round's barrier made every start visible
+        const unsigned c = tile_total[t];
+        ranges[t] = (!over && c) ? make_uint2(tile_start[t], tile_start[t] + c) : make_uint2(0u, 0u);
+    }
 }
 
 // Placement: one warp per (chunk, band of tile rows). The warp copies the chunk's starting offset
@@ -994,7 +1005,8 @@ static cudaError_t radix_pass(const unsigned* kin, const unsigned* vin, unsigned
 // count; leaves the total D in w.total (device). Bounded look-back waits set the timeout bit of
 // `err` when they give up.
 cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, unsigned* err,
-                      unsigned spin_limit, cudaStream_t st) {
+                      unsigned spin_limit, unsigned long long capacity, unsigned* ranges, unsigned* overflow_err,
+                      cudaStream_t st) {
     const int n = (int)proj.n;
     if (n == 0) return cudaMemsetAsync(w.total, 0, 8, st);
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
@@ -1031,7 +1043,8 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
         k_chunk_bounds<<<gblocks, 256, 0, st>>>(n, w.nvis, w.crect, w.boff, (int)w.cmax, w.chunk_first, w.nchunks);
         k_chunk_hist<<<(unsigned)w.cmax, 256, smem, st>>>(w.nchunks, w.chunk_first, w.crect, tiles_x, T, w.table);
         k_chunk_scan<<<(T + 31) / 32, 32 * kScanWarps, 0, st>>>(w.nchunks, T, w.table, w.tile_total);
-        k_tile_scan<<<1, 1024, 0, st>>>(T, w.tile_total, w.tile_start, w.total);
+        k_tile_scan<<<1, 1024, 0, st>>>(T, w.tile_total, w.tile_start, w.total, capacity,
+                                        reinterpret_cast<uint2*>(ranges), overflow_err);
         return cudaGetLastError();
     }
     count_launches(2);
@@ -1040,20 +1053,14 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
     return cudaGetLastError();
 }
 
-// Phase 2: placement (counting pass) or emission + tile radix passes, and the ranges.
-// d = number of duplicates (<= capacity).
-// Counting-path emission: the tile ranges and the placement of every entry. Reads no count on the
-// host (the number of chunks and the total stay on the device).
+// Counting-path emission: the placement of every entry (the tile ranges were written by the tile
+// scan). Reads no count on the host (the number of chunks and the total stay on the device).
 static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, unsigned long long capacity,
-                                 const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
-                                 unsigned* err, cudaStream_t st) {
-    const long long T = (long long)tiles_x * tiles_y;
+                                 const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* err,
+                                 cudaStream_t st) {
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
     cudaError_t e;
-    count_launches(1);
-    k_write_ranges<<<(int)((T + 255) / 256), 256, 0, st>>>((int)T, w.tile_start, w.tile_total, w.total, capacity,
-                                                           reinterpret_cast<uint2*>(ranges), err);
     const int band_rows = (tiles_y + kPlaceBands - 1) / kPlaceBands;
     const int nbands = (tiles_y + band_rows - 1) / band_rows;
     const size_t band_bytes = (size_t)band_rows * tiles_x * 4;
@@ -1069,6 +1076,8 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
     return cudaGetLastError();
 }
 
+// Phase 2: placement (counting pass) or emission + tile radix passes and the ranges.
+// d = number of duplicates (<= capacity).
 cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
                           cudaStream_t st) {
@@ -1081,7 +1090,7 @@ cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigne
     }
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
-    if (counting_path(T)) return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, ranges, err, st);
+    if (counting_path(T)) return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, err, st);
     const int tb = tile_bits_of(T);
     const int passes = (tb + 7) / 8;
     unsigned* tbuf[2] = {w.tA, w.tB};
@@ -1116,12 +1125,12 @@ cudaError_t bin_sort_async(const gs_proj& proj, int tiles_x, int tiles_y, unsign
                            const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
                            unsigned long long* n_dup_dev, unsigned* err, unsigned spin_limit, cudaStream_t st) {
     const long long T = (long long)tiles_x * tiles_y;
-    cudaError_t e = bin_count(proj, tiles_x, tiles_y, w, err, spin_limit, st);
+    cudaError_t e = bin_count(proj, tiles_x, tiles_y, w, err, spin_limit, capacity, ranges, err, st);
     if (e) return e;
     if (proj.n == 0) {
         e = cudaMemsetAsync(ranges, 0, (size_t)T * 8, st);
     } else {
-        e = emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, ranges, err, st);
+        e = emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, err, st);
     }
     if (e || !n_dup_dev) return e;
     return cudaMemcpyAsync(n_dup_dev, w.total, 8, cudaMemcpyDeviceToDevice, st);

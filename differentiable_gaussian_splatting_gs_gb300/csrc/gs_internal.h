@@ -34,8 +34,12 @@ struct SortWorkspace {
 
 // Workspace layout for n Gaussians, at most `cap` duplicates and `tiles` tiles.
 SortWorkspace carve_workspace(void* base, long long n, long long cap, long long tiles);
+// Phase 1 of the binning (depth sort, duplicate counts, on the counting path also the tile
+// table, starts and ranges); `ranges` and `capacity` are used on the counting path only, and
+// overflow_err (may be NULL) receives the check bit when D exceeds the capacity there.
 cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, unsigned* err,
-                      unsigned spin_limit, cudaStream_t st);
+                      unsigned spin_limit, unsigned long long capacity, unsigned* ranges, unsigned* overflow_err,
+                      cudaStream_t st);
 cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
                           cudaStream_t st);

@@ -155,8 +155,9 @@ size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32
  * Outputs: keys [D] uint64 (may be NULL: not written), vals [D] uint32, tile_ranges [T][2]
  * uint32 = [start, end) of each tile in the sorted list, *n_dup_out (HOST int64) = D.
  * workspace: device buffer of at least gs_sort_workspace_bytes(n, capacity, W, H) bytes.
- * Synchronises `stream` once to read D. If D > capacity, nothing is written beyond the
- * workspace, *n_dup_out = D and GS_ERR_CAPACITY is returned; call again with a larger capacity.
+ * Synchronises `stream` once to read D. If D > capacity, no entry is written, tile_ranges are
+ * written empty, *n_dup_out = D and GS_ERR_CAPACITY is returned; call again with a larger
+ * capacity.
  * 0 <= capacity < 2^31. Errors: GS_ERR_ARG, GS_ERR_CAPACITY, GS_ERR_CUDA.                     */
 int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options* opt,
                     void* workspace, size_t workspace_bytes, uint64_t* keys, uint32_t* vals,
