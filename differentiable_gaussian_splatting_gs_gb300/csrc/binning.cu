@@ -738,6 +738,7 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__
 // Exclusive scan down each tile's column of the chunk x tile table (in place) and the tile totals.
 // Block: 32 tiles (one per lane) x 32 warps, each warp a contiguous range of chunks.
 constexpr int kScanWarps = 32;
+constexpr int kColUnroll = 16;  // table loads in flight per lane
 __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* __restrict__ nchunks, int T,
                                                                 unsigned* __restrict__ table,
                                                                 unsigned* __restrict__ tile_total) {
@@ -750,12 +751,12 @@ __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* 
     unsigned sum = 0;
     if (t < T) {
         int c = c0;
-        for (; c + 8 <= c1; c += 8) {
-            unsigned v[8];
+        for (; c + kColUnroll <= c1; c += kColUnroll) {
+            unsigned v[kColUnroll];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = table[(size_t)(c + k) * T + t];
+            for (int k = 0; k < kColUnroll; ++k) v[k] = table[(size_t)(c + k) * T + t];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) sum += v[k];
+            for (int k = 0; k < kColUnroll; ++k) sum += v[k];
         }
         for (; c < c1; ++c) sum += table[(size_t)c * T + t];
     }
@@ -765,12 +766,12 @@ __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* 
     for (int w = 0; w < warp; ++w) run += part[w][lane];
     if (t < T) {
         int c = c0;
-        for (; c + 8 <= c1; c += 8) {
-            unsigned v[8];
+        for (; c + kColUnroll <= c1; c += kColUnroll) {
+            unsigned v[kColUnroll];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = table[(size_t)(c + k) * T + t];
+            for (int k = 0; k < kColUnroll; ++k) v[k] = table[(size_t)(c + k) * T + t];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < kColUnroll; ++k) {
                 table[(size_t)(c + k) * T + t] = run;
                 run += v[k];
             }

@@ -185,10 +185,10 @@ __device__ __forceinline__ int compact_warp(S& s, int n_in, int pos_limit, float
 
 // ---- forward ---------------------------------------------------------------------------------
 
-// Front-to-back blending of one record into one pixel; sets `done` when the pixel terminates.
-__device__ __forceinline__ void blend_pixel(float p2, const float4& r1, float cb, unsigned pos1, float& T, float& c0,
-                                            float& c1, float& c2, unsigned& last, bool& done) {
-    const float alpha = fminf(kAlphaMax, r1.y * ex2_approx(p2));
+// Front-to-back blending of one record, whose alpha at the pixel is given, into one pixel; sets
+// `done` when the pixel terminates.
+__device__ __forceinline__ void blend_pixel(float alpha, const float4& r1, float cb, unsigned pos1, float& T,
+                                            float& c0, float& c1, float& c2, unsigned& last, bool& done) {
     if (alpha >= kAlphaMin) {
         const float test_T = T * (1.f - alpha);
         if (test_T < kTMin) {
@@ -268,23 +268,32 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
                                                  s.rec[slot][threadIdx.x][2], s.cull2[threadIdx.x]);
         if (__syncthreads_or(!ok)) break;
         const int nl = compact_warp(s, n_in, kB, wx0, wx1, wy0, wy1, warp, lane);
-        for (int k = 0; k < nl; ++k) {
+        // two listed Gaussians per iteration: their alphas do not depend on the transmittance, so
+        // the four exponentials are computed together and only the blending stays in order
+        for (int k = 0; k < nl; k += 2) {
             if (__all_sync(0xffffffffu, done0 && done1)) break;
-            const int j = s.list[warp][k];
-            const float2 r0 = *reinterpret_cast<const float2*>(&s.rec[slot][j][0]);  // mean
-            const float4 r1 = s.rec[slot][j][1];                                     // (D, o, r, g)
-            const float4 r2 = s.rec[slot][j][2];                                     // (b, r, A', D')
-            const unsigned pos1 = (unsigned)(b * kB + j + 1);
-            const float dx = r0.x - fpx;
-            if (!done0) {
-                const float dy = r0.y - fpy0;
-                const float u = __fmaf_rn(r2.y, dy, dx);
-                blend_pixel(__fmaf_rn(r2.z * u, u, r2.w * dy * dy), r1, r2.x, pos1, T0, c00, c01, c02, last0, done0);
-            }
-            if (!done1) {
-                const float dy = r0.y - fpy1;
-                const float u = __fmaf_rn(r2.y, dy, dx);
-                blend_pixel(__fmaf_rn(r2.z * u, u, r2.w * dy * dy), r1, r2.x, pos1, T1, c10, c11, c12, last1, done1);
+            const bool two = k + 1 < nl;  // warp-uniform
+            const int ja = s.list[warp][k], jb = two ? s.list[warp][k + 1] : ja;
+            const float2 a0 = *reinterpret_cast<const float2*>(&s.rec[slot][ja][0]);  // mean
+            const float4 a1 = s.rec[slot][ja][1];                                     // (D, o, r, g)
+            const float4 a2 = s.rec[slot][ja][2];                                     // (b, r, A', D')
+            const float2 b0 = *reinterpret_cast<const float2*>(&s.rec[slot][jb][0]);
+            const float4 b1 = s.rec[slot][jb][1];
+            const float4 b2 = s.rec[slot][jb][2];
+            const float dxa = a0.x - fpx, dya0 = a0.y - fpy0, dya1 = a0.y - fpy1;
+            const float dxb = b0.x - fpx, dyb0 = b0.y - fpy0, dyb1 = b0.y - fpy1;
+            const float ua0 = __fmaf_rn(a2.y, dya0, dxa), ua1 = __fmaf_rn(a2.y, dya1, dxa);
+            const float ub0 = __fmaf_rn(b2.y, dyb0, dxb), ub1 = __fmaf_rn(b2.y, dyb1, dxb);
+            const float al_a0 = fminf(kAlphaMax, a1.y * ex2_approx(__fmaf_rn(a2.z * ua0, ua0, a2.w * dya0 * dya0)));
+            const float al_a1 = fminf(kAlphaMax, a1.y * ex2_approx(__fmaf_rn(a2.z * ua1, ua1, a2.w * dya1 * dya1)));
+            const float al_b0 = fminf(kAlphaMax, b1.y * ex2_approx(__fmaf_rn(b2.z * ub0, ub0, b2.w * dyb0 * dyb0)));
+            const float al_b1 = fminf(kAlphaMax, b1.y * ex2_approx(__fmaf_rn(b2.z * ub1, ub1, b2.w * dyb1 * dyb1)));
+            const unsigned posa = (unsigned)(b * kB + ja + 1), posb = (unsigned)(b * kB + jb + 1);
+            if (!done0) blend_pixel(al_a0, a1, a2.x, posa, T0, c00, c01, c02, last0, done0);
+            if (!done1) blend_pixel(al_a1, a1, a2.x, posa, T1, c10, c11, c12, last1, done1);
+            if (two) {
+                if (!done0) blend_pixel(al_b0, b1, b2.x, posb, T0, c00, c01, c02, last0, done0);
+                if (!done1) blend_pixel(al_b1, b1, b2.x, posb, T1, c10, c11, c12, last1, done1);
             }
         }
         if (STAGING == GS_STAGE_LOADS) {
