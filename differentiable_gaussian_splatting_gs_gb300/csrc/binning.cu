@@ -318,13 +318,16 @@ __global__ void __launch_bounds__(kSortThreads) k_onesweep(
 #pragma unroll
     for (int i = 0; i < 8; ++i) woff[warp][lane + 32 * i] = 0u;
     __syncwarp();
+    // peer masks of the 8 rounds: all match_any first (independent), kept for the scatter below
+    unsigned pm[kSortRounds];
 #pragma unroll
-    for (int r = 0; r < kSortRounds; ++r) {
+    for (int r = 0; r < kSortRounds; ++r) pm[r] = __match_any_sync(0xffffffffu, dg[r]);
+#pragma unroll
+    for (int r = 0; r < kSortRounds; ++r) {  // group leaders of different rounds may share a digit
         const unsigned d = dg[r];
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        if (d != 0x100u && (peers & lanemask_lt()) == 0u) woff[warp][d] += __popc(peers);
-        __syncwarp();
+        if (d != 0x100u && (pm[r] & lanemask_lt()) == 0u) atomicAdd(&woff[warp][d], (unsigned)__popc(pm[r]));
     }
+    __syncwarp();
     __syncthreads();
     {
         const int d = threadIdx.x;  // digit d = thread
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(kSortThreads) k_onesweep(
     for (int r = 0; r < kSortRounds; ++r) {
         const unsigned d = dg[r];
         const bool valid = d != 0x100u;
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const unsigned peers = pm[r];
         if (valid) {
             const unsigned lp = woff[warp][d] + __popc(peers & lanemask_lt());
             sk[lp] = k[r];
