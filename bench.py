@@ -530,6 +530,25 @@ def run_ours(args, rank, world, local_rank):
         s_bytes = scene.n * 8 + n_vis * (32 + 12 + floats * 4)  # radius + magnitude; grad2d sector, stats, grads
         extras["densify_stats"] = {"ms": sm_, "algorithmic_bytes": s_bytes, "achieved_gbs": s_bytes / (sm_ / 1e3) / 1e9,
                                    "frac_of_measured_hbm": s_bytes / (sm_ / 1e3) / 1e9 / hbm}
+        # the same statistics emitted by the preprocess backward itself, against the plain backward
+        pb_ms = {False: [], True: []}
+        for it in range(4 + max(3, args.steps // 2)):
+            for fused in (False, True):
+                flush.fill_(1.0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                if fused:
+                    api.gs_preprocess_bwd_stats(params, cams[n_views - 1], opt, bufs.proj, bufs.grad2d, acc, cnt,
+                                                mrad, grad_mag=gmag, out=grads)
+                else:
+                    api.gs_preprocess_bwd(params, cams[n_views - 1], opt, bufs.proj, bufs.grad2d, out=grads)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if it > 3:
+                    pb_ms[fused].append(e0.elapsed_time(e1))
+        extras["densify_stats"]["fused_into_preprocess_bwd"] = {
+            "preprocess_bwd_ms": sum(pb_ms[False]) / len(pb_ms[False]),
+            "preprocess_bwd_stats_ms": sum(pb_ms[True]) / len(pb_ms[True])}
         # image loss L1 + D-SSIM and dL/dimage of the rendered view
         image = bufs.image_buffers(cam.width, cam.height)[0]
         lws = torch.empty(int(lib.gs_loss_workspace_bytes(cam.width, cam.height)), dtype=torch.uint8, device=dev)

@@ -30,7 +30,8 @@ EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_re
            "gs_preprocess_bwd", "gs_status_string", "gs_last_error_message", "gs_device_error",
            "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static", "gs_adam_step",
            "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim", "gs_preprocess2d",
-           "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd", "gs_bin_and_sort_async")
+           "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd", "gs_bin_and_sort_async",
+           "gs_preprocess_bwd_stats")
 GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
 
 
@@ -54,6 +55,11 @@ class gs_params(C.Structure):
 class gs_proj(C.Structure):
     _fields_ = [("rec", C.c_void_p), ("depth", C.c_void_p), ("radius", C.c_void_p),
                 ("tiles_touched", C.c_void_p), ("n", C.c_int64)]
+
+
+class gs_densify_outputs(C.Structure):
+    _fields_ = [("grad_norm_accum", C.c_void_p), ("view_count", C.c_void_p), ("max_radius", C.c_void_p),
+                ("grad_mag", C.c_void_p), ("ndc", C.c_int32)]
 
 
 class gs_tensors(C.Structure):
@@ -98,6 +104,9 @@ def load():
         lib.gs_render_fwd.argtypes = [pproj, P, P, pcam, popt, P, P, P, P]
         lib.gs_render_bwd.argtypes = [pproj, P, P, pcam, popt, P, P, P, P, P]
         lib.gs_preprocess_bwd.argtypes = [ppar, pcam, popt, pproj, P, P, P, P, P, P, I32, P]
+        lib.gs_preprocess_bwd_stats.argtypes = [ppar, pcam, popt, pproj, P, P, P, P, P, P, I32,
+                                                C.POINTER(gs_densify_outputs), P]
+        lib.gs_preprocess_bwd_stats.restype = C.c_int
         lib.gs_status_string.argtypes = [C.c_int]
         lib.gs_status_string.restype = C.c_char_p
         lib.gs_last_error_message.argtypes = []

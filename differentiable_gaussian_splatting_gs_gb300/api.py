@@ -274,6 +274,26 @@ def gs_preprocess_bwd(params: dict, cam, opt: gs_options, proj: Proj, grad2d, ou
     return out
 
 
+def gs_preprocess_bwd_stats(params: dict, cam, opt: gs_options, proj: Proj, grad2d, grad_norm_accum, view_count,
+                            max_radius, grad_mag=None, ndc: bool = False, out: dict | None = None,
+                            accumulate: bool = False, stream=None) -> dict:
+    """gs_preprocess_bwd that also adds the view's densification statistics (and, with grad_mag,
+    the 2-norm of the view's parameter gradients) in the same kernel."""
+    p = _params(params["mean3d"], params["log_scale"], params["quat"], params["opacity_logit"], params["sh"])
+    if out is None:
+        out = alloc_param_grads(params)
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    ps = proj.struct()
+    st = _abi.gs_densify_outputs(grad_norm_accum=_ptr(grad_norm_accum), view_count=_ptr(view_count),
+                                 max_radius=_ptr(max_radius), grad_mag=_ptr(grad_mag) if grad_mag is not None else None,
+                                 ndc=int(bool(ndc)))
+    check(_abi.load().gs_preprocess_bwd_stats(C.byref(p), C.byref(c), C.byref(opt), C.byref(ps), _ptr(grad2d),
+                                              _ptr(out["mean3d"]), _ptr(out["log_scale"]), _ptr(out["quat"]),
+                                              _ptr(out["opacity_logit"]), _ptr(out["sh"]), int(bool(accumulate)),
+                                              C.byref(st), _stream(stream)), "gs_preprocess_bwd_stats")
+    return out
+
+
 PARAM_NAMES = ("mean3d", "log_scale", "quat", "opacity_logit", "sh")
 
 

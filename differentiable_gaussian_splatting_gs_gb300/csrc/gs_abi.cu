@@ -402,8 +402,35 @@ int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options
             if (!q || !aligned(q, 4)) return fail(GS_ERR_ARG, "a gradient output is NULL or misaligned");
     }
     cudaError_t e = launch_preprocess_bwd(o.deg, (int)p->n, *p, kc, proj->radius, grad2d, d_mean3d, d_log_scale,
-                                          d_quat, d_opacity_logit, d_sh, accumulate, as_stream(stream));
+                                          d_quat, d_opacity_logit, d_sh, accumulate, nullptr, as_stream(stream));
     return e ? cuda_fail(e, "gs_preprocess_bwd") : GS_OK;
+}
+
+int gs_preprocess_bwd_stats(const gs_params* p, const gs_camera* cam, const gs_options* opt, const gs_proj* proj,
+                            const float* grad2d, float* d_mean3d, float* d_log_scale, float* d_quat,
+                            float* d_opacity_logit, float* d_sh, int32_t accumulate, const gs_densify_outputs* stats,
+                            void* stream) {
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_params(p))) return s;
+    if ((s = check_proj(proj, p->n))) return s;
+    if (!stats) return fail(GS_ERR_ARG, "stats is NULL (use gs_preprocess_bwd)");
+    if (p->n > 0) {
+        if (!grad2d || !aligned(grad2d, 16)) return fail(GS_ERR_ARG, "grad2d NULL or not 16-byte aligned");
+        const void* outs[5] = {d_mean3d, d_log_scale, d_quat, d_opacity_logit, d_sh};
+        for (const void* q : outs)
+            if (!q || !aligned(q, 4)) return fail(GS_ERR_ARG, "a gradient output is NULL or misaligned");
+        if (!stats->grad_norm_accum || !stats->view_count || !stats->max_radius ||
+            !aligned(stats->grad_norm_accum, 4) || !aligned(stats->view_count, 4) || !aligned(stats->max_radius, 4) ||
+            (stats->grad_mag && !aligned(stats->grad_mag, 4)))
+            return fail(GS_ERR_ARG, "a statistics output is NULL or misaligned");
+    }
+    DensifyArgs d{stats->grad_norm_accum, stats->view_count, stats->max_radius, stats->grad_mag,
+                  stats->ndc ? 0.5f * (float)kc.width : 1.f, stats->ndc ? 0.5f * (float)kc.height : 1.f};
+    cudaError_t e = launch_preprocess_bwd(o.deg, (int)p->n, *p, kc, proj->radius, grad2d, d_mean3d, d_log_scale,
+                                          d_quat, d_opacity_logit, d_sh, accumulate, &d, as_stream(stream));
+    return e ? cuda_fail(e, "gs_preprocess_bwd_stats") : GS_OK;
 }
 
 int gs_adam_step(gs_tensors* params, const gs_tensors* grads, gs_tensors* exp_avg, gs_tensors* exp_avg_sq,

@@ -50,9 +50,17 @@ bool counting_path(long long tiles);
 
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
                               cudaStream_t st);
+// Post-backward statistics written by the preprocess backward (gs_preprocess_bwd_stats).
+struct DensifyArgs {
+    float* accum;      // += |(sx, sy) * dL/dmean2d| for radius > 0
+    int* count;        // += 1 for radius > 0
+    int* max_radius;   // max with the radius
+    float* grad_mag;   // 2-norm of the view's parameter gradients (NULL: not written)
+    float sx, sy;
+};
 cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
                                   const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
-                                  int accumulate, cudaStream_t st);
+                                  int accumulate, const DensifyArgs* stats, cudaStream_t st);
 cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* vals, const unsigned* ranges,
                               const KernelCamera& cam, float* image, float* t_final, unsigned* n_contrib,
                               unsigned spin_limit, unsigned* err, cudaStream_t st);

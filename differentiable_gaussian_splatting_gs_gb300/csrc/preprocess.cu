@@ -188,13 +188,15 @@ __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* 
 
 constexpr int kBwdThreads = 128;
 
-template <int DEG>
+// STATS: also the post-backward statistics of the view (see DensifyArgs), from the gradients this
+// call computes.
+template <int DEG, bool STATS>
 __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
     const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
     const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
     float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
-    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate) {
+    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate, const DensifyArgs stats) {
     constexpr int K = (DEG + 1) * (DEG + 1);
     constexpr int K3 = 3 * K;
     __shared__ float tile_all[kBwdThreads / 32][32 * (K3 + 1)];
@@ -204,7 +206,8 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     const int i = warp_first + lane;
     // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only. The rows'
     // copies, the geometry and the 2D gradients are all in flight before the first wait.
-    const unsigned seen = __ballot_sync(0xffffffffu, i < n && radius[i] > 0);
+    const int rad = i < n ? radius[i] : 0;
+    const unsigned seen = __ballot_sync(0xffffffffu, rad > 0);
     sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
     bool live = i < n && ((seen >> lane) & 1u);
     float m[3] = {0.f, 0.f, 0.f}, ls[3] = {0.f, 0.f, 0.f}, q[4] = {1.f, 0.f, 0.f, 0.f}, lg = 0.f;
@@ -341,6 +344,32 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     for (int k = 0; k < 4; ++k) dq[k] = (dqn[k] - dotq * g.qn[k]) * g.qinv;
 
     }  // live
+    if (STATS && i < n) {
+        // 3D Gaussian splatting's densification statistics and the 2-norm of this view's parameter
+        // gradients (the tile row holds this view's SH gradients), as gs_densify_stats computes them
+        if (rad > 0) {
+            const float gx = stats.sx * g0.x, gy = stats.sy * g0.y;
+            stats.accum[i] += sqrtf(__fmaf_rn(gx, gx, gy * gy));
+            stats.count[i] += 1;
+            stats.max_radius[i] = max(stats.max_radius[i], rad);
+        }
+        if (stats.grad_mag) {
+            float ss = 0.f;
+            if (rad > 0) {  // the summation order of gs_densify_stats
+                for (int k = 0; k < 3; ++k) ss = __fmaf_rn(dm[k], dm[k], __fmaf_rn(dls[k], dls[k], ss));
+                ss = __fmaf_rn(dq[0], dq[0], __fmaf_rn(dq[1], dq[1], __fmaf_rn(dq[2], dq[2], __fmaf_rn(dq[3], dq[3], ss))));
+                ss = __fmaf_rn(dlg, dlg, ss);
+                if (K3 % 4 == 0) {
+                    for (int k = 0; k < K3; k += 4)
+                        ss = __fmaf_rn(my[k], my[k], __fmaf_rn(my[k + 1], my[k + 1],
+                                       __fmaf_rn(my[k + 2], my[k + 2], __fmaf_rn(my[k + 3], my[k + 3], ss))));
+                } else {
+                    for (int k = 0; k < K3; ++k) ss = __fmaf_rn(my[k], my[k], ss);
+                }
+            }
+            stats.grad_mag[i] = sqrtf(ss);
+        }
+    }
     if (i < n) {
         if (accumulate) {
             for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] += dm[k]; d_log_scale[3 * i + k] += dls[k]; }
@@ -378,17 +407,26 @@ cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCa
 
 cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
                                   const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
-                                  int accumulate, cudaStream_t st) {
+                                  int accumulate, const DensifyArgs* stats, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     const int blocks = (n + kBwdThreads - 1) / kBwdThreads;
     const float4* g2 = reinterpret_cast<const float4*>(grad2d);
+    const DensifyArgs none{};
     count_launches(1);
+#define GS_PREBWD(D)                                                                                                \
+    (stats ? k_preprocess_bwd<D, true><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat,            \
+                                                                       p.opacity_logit, p.sh, cam, radius, g2, dm,  \
+                                                                       dls, dq, dlg, dsh, accumulate, *stats)       \
+           : k_preprocess_bwd<D, false><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat,           \
+                                                                        p.opacity_logit, p.sh, cam, radius, g2, dm, \
+                                                                        dls, dq, dlg, dsh, accumulate, none))
     switch (deg) {
-        case 0: k_preprocess_bwd<0><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
-        case 1: k_preprocess_bwd<1><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
-        case 2: k_preprocess_bwd<2><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
-        default: k_preprocess_bwd<3><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate); break;
+        case 0: GS_PREBWD(0); break;
+        case 1: GS_PREBWD(1); break;
+        case 2: GS_PREBWD(2); break;
+        default: GS_PREBWD(3); break;
     }
+#undef GS_PREBWD
     return cudaGetLastError();
 }
 

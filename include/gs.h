@@ -253,6 +253,30 @@ int gs_densify_stats(const gs_proj* proj, const float* grad2d, int32_t width, in
                      float* grad_norm_accum, int32_t* view_count, int32_t* max_radius,
                      const gs_tensors* param_grads, float* grad_mag, int32_t sh_degree, void* stream);
 
+/* The statistics of gs_densify_stats emitted by the preprocess backward itself (SURVEY's
+ * "nearly free inside the backward": no extra pass over the gradients). Outputs as
+ * gs_densify_stats; ndc != 0 scales dL/dmean2d by (width / 2, height / 2) of `cam`. */
+typedef struct {
+    float*   grad_norm_accum;  /* [N], += for radius > 0 */
+    int32_t* view_count;       /* [N], += 1 for radius > 0 */
+    int32_t* max_radius;       /* [N], max with the radius */
+    float*   grad_mag;         /* [N] or NULL: 2-norm of this view's parameter gradients, 0 when hidden */
+    int32_t  ndc;
+} gs_densify_outputs;
+
+/* gs_preprocess_bwd plus the post-backward statistics of the view, from the gradients this call
+ * computes (Odin: Primitive-Level Synchronization for Distributed Point-Based Neural Rendering,
+ * Review, item 1: the per-primitive gradient magnitude read by a post-backward hook). With
+ * accumulate = 0 the outputs equal gs_preprocess_bwd followed by gs_densify_stats with
+ * param_grads = the gradient outputs, bit for bit; with accumulate != 0 grad_mag is the norm of
+ * this view's own gradients (gs_densify_stats afterwards would see the accumulated sums).
+ * Errors: those of gs_preprocess_bwd; GS_ERR_ARG when stats or one of its arrays is NULL or
+ * misaligned (grad_mag may be NULL). */
+int gs_preprocess_bwd_stats(const gs_params* p, const gs_camera* cam, const gs_options* opt, const gs_proj* proj,
+                            const float* grad2d, float* d_mean3d, float* d_log_scale, float* d_quat,
+                            float* d_opacity_logit, float* d_sh, int32_t accumulate, const gs_densify_outputs* stats,
+                            void* stream);
+
 /* ---- image loss ---------------------------------------------------------------------------
  * The loss whose gradient feeds the gradient computation phase (Odin: Primitive-Level
  * Synchronization for Distributed Point-Based Neural Rendering, Figure 7: rendering, then backward):

@@ -144,3 +144,63 @@ def test_l1_dssim_of_an_image_with_itself():
     loss, dl = api.gs_loss_l1_dssim(x, x.clone(), 0.2)
     torch.cuda.synchronize()
     assert abs(loss.item()) < 1e-6 and dl.abs().max().item() < 1e-4 / x.numel()
+
+
+def _step_grad2d(s, view, params, opt):
+    from differentiable_gaussian_splatting_gs_gb300 import step
+    cam = s.cameras[view]
+    bufs = step.StepBuffers(s.n, DEV)
+    proj = api.gs_preprocess(params, cam, opt, out=bufs.proj)
+    b = api.gs_bin_and_sort(proj, cam, opt, buffers=bufs.sort)
+    img, tf, nc = api.gs_render_fwd(proj, b.vals, b.ranges, cam, opt)
+    dl = img - torch.from_numpy(s.targets[view]).to(DEV)
+    return cam, proj, api.gs_render_bwd(proj, b.vals, b.ranges, cam, opt, dl, tf, nc), bufs
+
+
+@pytest.mark.parametrize("cfg,n,ndc", [(0, None, False), (1, 20_000, True), (1, 20_000, False)])
+def test_fused_statistics_equal_the_separate_call(cfg, n, ndc):
+    """gs_preprocess_bwd_stats = gs_preprocess_bwd followed by gs_densify_stats, bit for bit."""
+    s = gs_scenes.make_scene(cfg, n=n)
+    params = {k: torch.from_numpy(np.ascontiguousarray(getattr(s, k))).to(DEV) for k in optim.NAMES}
+    opt = api.make_options(s.sh_degree)
+    cam, proj, g2, bufs = _step_grad2d(s, 0, params, opt)
+    rng = np.random.default_rng(7)
+    acc0 = torch.from_numpy(rng.uniform(0, 1e-3, s.n).astype(np.float32)).to(DEV)
+    cnt0 = torch.from_numpy(rng.integers(0, 5, s.n).astype(np.int32)).to(DEV)
+    mr0 = torch.from_numpy(rng.integers(0, 40, s.n).astype(np.int32)).to(DEV)
+    a = [t.clone() for t in (acc0, cnt0, mr0)] + [torch.full((s.n,), -1.0, device=DEV)]
+    b = [t.clone() for t in (acc0, cnt0, mr0)] + [torch.full((s.n,), -1.0, device=DEV)]
+    ga = api.gs_preprocess_bwd(params, cam, opt, proj, g2)
+    api.gs_densify_stats(proj, g2, cam.width, cam.height, a[0], a[1], a[2], ndc=ndc, param_grads=ga, grad_mag=a[3],
+                         sh_degree=s.sh_degree)
+    gb = api.gs_preprocess_bwd_stats(params, cam, opt, proj, g2, b[0], b[1], b[2], grad_mag=b[3], ndc=ndc)
+    torch.cuda.synchronize()
+    for k in optim.NAMES:
+        assert torch.equal(ga[k], gb[k]), k
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert int((a[1] != cnt0).sum()) == int((proj.radius > 0).sum())
+    assert api.gs_device_error() == 0
+
+
+def test_fused_statistics_over_two_views():
+    """Accumulating views: the counters add up as two separate calls would, and grad_mag is the
+    norm of the second view's own gradients."""
+    s = gs_scenes.make_scene(3, n=20_000, res_scale=0.25, views=2)
+    params = {k: torch.from_numpy(np.ascontiguousarray(getattr(s, k))).to(DEV) for k in optim.NAMES}
+    opt = api.make_options(s.sh_degree)
+    z = lambda dt: torch.zeros(s.n, dtype=dt, device=DEV)  # noqa: E731
+    acc_f, cnt_f, mr_f, mag_f = z(torch.float32), z(torch.int32), z(torch.int32), z(torch.float32)
+    acc_s, cnt_s, mr_s, mag_s = z(torch.float32), z(torch.int32), z(torch.int32), z(torch.float32)
+    grads = None
+    for v in range(2):
+        cam, proj, g2, bufs = _step_grad2d(s, v, params, opt)
+        grads = api.gs_preprocess_bwd_stats(params, cam, opt, proj, g2, acc_f, cnt_f, mr_f, grad_mag=mag_f,
+                                            out=grads, accumulate=v > 0)
+        own = api.gs_preprocess_bwd(params, cam, opt, proj, g2)  # this view alone
+        api.gs_densify_stats(proj, g2, cam.width, cam.height, acc_s, cnt_s, mr_s, param_grads=own, grad_mag=mag_s,
+                             sh_degree=s.sh_degree)
+    torch.cuda.synchronize()
+    assert torch.equal(acc_f, acc_s) and torch.equal(cnt_f, cnt_s) and torch.equal(mr_f, mr_s)
+    assert torch.equal(mag_f, mag_s)
+    assert int(cnt_f.max()) <= 2 and api.gs_device_error() == 0
