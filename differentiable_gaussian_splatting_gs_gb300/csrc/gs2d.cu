@@ -378,18 +378,20 @@ __device__ __forceinline__ void prepare2d(float4 (&r)[5], float pcx, float pcy, 
     cb = make_float4(0.f, -1.f, cx, cy);
     ct = -1.f;
     if (!(o * 1.00001f >= kAMin2)) return;  // alpha <= opacity < 1/255: never blended
-    const float tau = logf(255.f * o * 1.00001f) * 1.001f + 0.001f;
+    // culling values only (they carry margins): fast logarithm and hardware reciprocals
+    const float tau = __logf(255.f * o * 1.00001f) * 1.001f + 0.001f;
     ct = tau;
     const float rr = 2.f * tau;
     const float n = __fmaf_rn(-rr, __fmaf_rn(Cu, Cu, Cv * Cv), z * z);
-    const float in = 1.f / n;
+    const float in = rcp_approx(n);
     const float ox = -rr * __fmaf_rn(e0, Cu, e1 * Cv) * in, oy = -rr * __fmaf_rn(f0, Cu, f1 * Cv) * in;
     const float sxx = __fmaf_rn(rr * __fmaf_rn(e0, e0, e1 * e1), in, ox * ox);
     const float sxy = __fmaf_rn(rr * __fmaf_rn(e0, f0, e1 * f1), in, ox * oy);
     const float syy = __fmaf_rn(rr * __fmaf_rn(f0, f0, f1 * f1), in, oy * oy);
     const float t = p.d0 * rr * z * in;
     const float dets = t * t * in;
-    const float ra = -sxy / syy, rc = -sxy / sxx, da = dets / (syy * syy), la = dets / syy * 1.002f;
+    const float isyy = rcp_approx(syy);
+    const float ra = -sxy * isyy, rc = -sxy * rcp_approx(sxx), da = dets * isyy * isyy, la = dets * isyy * 1.002f;
     if (n > 0.f && dets > 0.f && ra == ra && rc == rc && da < inf && la < inf && fabsf(ox) < inf && fabsf(oy) < inf) {
         ca = make_float4(mx + ox, my + oy, rc, ra);
         cb.x = da;
