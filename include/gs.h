@@ -253,9 +253,9 @@ int gs_densify_stats(const gs_proj* proj, const float* grad2d, int32_t width, in
                      float* grad_norm_accum, int32_t* view_count, int32_t* max_radius,
                      const gs_tensors* param_grads, float* grad_mag, int32_t sh_degree, void* stream);
 
-/* The statistics of gs_densify_stats emitted by the preprocess backward itself (SURVEY's
- * "nearly free inside the backward": no extra pass over the gradients). Outputs as
- * gs_densify_stats; ndc != 0 scales dL/dmean2d by (width / 2, height / 2) of `cam`. */
+/* The statistics of gs_densify_stats emitted by the preprocess backward itself, where the
+ * gradients are already in registers (no extra pass over them). Outputs as gs_densify_stats;
+ * ndc != 0 scales dL/dmean2d by (width / 2, height / 2) of `cam`. */
 typedef struct {
     float*   grad_norm_accum;  /* [N], += for radius > 0 */
     int32_t* view_count;       /* [N], += 1 for radius > 0 */
