@@ -4,7 +4,7 @@
 // smoke check and the benchmark's CPU-baseline leg may load it. It shares no code, header,
 // table or constant generator with the CUDA path, and the CUDA path never calls it.
 //
-// What it computes. The pages this build follows state the method only at the level of its
+// What it computes. The cited papers state the method only at the level of its
 // phases: a 3D Gaussian splatting scene is rendered by a rasterization pipeline and trained by
 // gradient descent, and the gradient computation accumulates per-Gaussian gradients with a very
 // large number of atomic updates (DISTWAR: Fast Differentiable Rendering on Raster-based
