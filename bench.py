@@ -603,7 +603,23 @@ def run_ours(args, rank, world, local_rank):
             parts.append([marks[i].elapsed_time(marks[i + 1]) for i in range(6)])
         m2 = sum(s_ms2) / len(s_ms2)
         pm = [sum(p[i] for p in parts) / len(parts) for i in range(6)]
+        # the surfel step as one CUDA graph (non-synchronising sort), on the same buffers
+        g2step = step.GraphedStep(params, [c0], [target[0]], opt, grads, bufs, bufs.sort.capacity, surfels=True)
+        for _ in range(3):
+            g2step.replay()
+        q_ms = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g2step.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            q_ms.append(e0.elapsed_time(e1))
+        gm2 = sum(q_ms) / len(q_ms)
         extras["surfel_step"] = {"ms_per_view": m2, "mpix_per_s": c0.width * c0.height / (m2 / 1e3) / 1e6,
+                                 "graph_ms_per_view": gm2,
+                                 "graph_mpix_per_s": c0.width * c0.height / (gm2 / 1e3) / 1e6,
                                  "duplicates": int(d2),
                                  "stage_ms": dict(zip(["preprocess", "bin_and_sort", "render_fwd", "dl_dimage",
                                                        "render_bwd", "preprocess_bwd"], pm))}

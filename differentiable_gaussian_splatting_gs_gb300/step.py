@@ -23,6 +23,15 @@ class StepBuffers:
         self.sort = api.SortBuffers(self.device)
         self.grad2d = torch.empty((n, 12), dtype=torch.float32, device=self.device)
         self.images = {}
+        self.n = n
+        self._surfel = None
+
+    def surfel_buffers(self):
+        """(rec2d [N, 16], grad2d [N, 16]) of the surfel pipeline, allocated on first use."""
+        if self._surfel is None:
+            self._surfel = (torch.empty((self.n, 16), dtype=torch.float32, device=self.device),
+                            torch.empty((self.n, 16), dtype=torch.float32, device=self.device))
+        return self._surfel
 
     def image_buffers(self, width: int, height: int):
         key = (width, height)
@@ -89,16 +98,45 @@ def train_step_async(params: dict, cameras, targets, opt, grads: dict, buffers: 
     return image
 
 
+def train_step_surfels_async(params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
+                             n_dup: torch.Tensor, events=None, stream=None):
+    """train_step_async for the surfel (2D Gaussian splatting) pipeline: gs_preprocess2d, the same
+    sort, gs_render2d_fwd, the loss gradient, gs_render2d_bwd, gs_preprocess2d_bwd."""
+    rec2d, g2d = buffers.surfel_buffers()
+    image = None
+    for v, (cam, target) in enumerate(zip(cameras, targets)):
+        ev = events[v] if events is not None else None
+        c = cam if isinstance(cam, api.gs_camera) else api.make_camera(cam)
+        proj, _ = api.gs_preprocess2d(params, c, opt, out=buffers.proj, rec2d=rec2d, stream=stream)
+        image, t_final, n_contrib, dl, ranges = buffers.image_buffers(c.width, c.height)
+        b = api.gs_bin_and_sort_async(proj, c, opt, capacity, buffers=buffers.sort, ranges=ranges,
+                                      n_dup=n_dup[v:v + 1], stream=stream)
+        if ev is not None:
+            ev[0][0].record()
+        api.gs_render2d_fwd(rec2d, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib), stream=stream)
+        if ev is not None:
+            ev[0][1].record()
+        torch.sub(image, target, out=dl)
+        if ev is not None:
+            ev[1][0].record()
+        api.gs_render2d_bwd(rec2d, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=g2d, stream=stream)
+        if ev is not None:
+            ev[1][1].record()
+        api.gs_preprocess2d_bwd(params, c, opt, proj, g2d, out=grads, accumulate=v > 0, stream=stream)
+    return image
+
+
 class GraphedStep:
     """The step of fixed views (train_step_async) captured into one CUDA graph: replay() runs
     every kernel of the step with one launch from the host. Inputs are read from, and gradients
     written to, the same tensors at every replay (update them in place between replays)."""
 
     def __init__(self, params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
-                 events=None):
+                 events=None, surfels: bool = False):
         """events: as for train_step_async; to time kernels inside the graph they must be created
         with torch.cuda.Event(enable_timing=True, external=True), which captures them as event
-        record nodes."""
+        record nodes. surfels: capture the surfel pipeline (train_step_surfels_async) instead."""
+        run = train_step_surfels_async if surfels else train_step_async
         self.device = buffers.device
         self.cams = [c if isinstance(c, api.gs_camera) else api.make_camera(c) for c in cameras]
         self.n_dup = torch.zeros(len(self.cams), dtype=torch.int64, device=self.device)
@@ -107,13 +145,13 @@ class GraphedStep:
         side = torch.cuda.Stream(self.device)
         side.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(side):
-            train_step_async(*args)
+            run(*args)
         torch.cuda.current_stream(self.device).wait_stream(side)
         torch.cuda.synchronize(self.device)
         before = api.gs_kernel_launches()
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            train_step_async(*args)
+            run(*args)
         self.launches = api.gs_kernel_launches() - before  # library kernels per replay
 
     def replay(self):

@@ -157,3 +157,29 @@ def test_graphed_step_times_its_raster_kernels():
         fwd, bwd = ev[0][0][0].elapsed_time(ev[0][0][1]), ev[0][1][0].elapsed_time(ev[0][1][1])
         assert 0 < fwd < total and 0 < bwd < total and fwd + bwd < total
     assert api.gs_device_error() == _abi.GS_OK
+
+
+def test_graphed_surfel_step_matches_eager_surfel_step():
+    s = gs_scenes.make_scene(1, n=20_000)
+    params = _params(s)
+    opt = api.make_options(s.sh_degree)
+    targets = [torch.from_numpy(s.targets[0]).to(DEV)]
+    bufs = step.StepBuffers(s.n, DEV)
+    cap = api.gs_bin_and_sort(api.gs_preprocess2d(params, s.cameras[0], opt, out=bufs.proj)[0], s.cameras[0], opt,
+                              buffers=bufs.sort).n_dup + 1000
+    n_dup = torch.zeros(1, dtype=torch.int64, device=DEV)
+    grads_ref = api.alloc_param_grads(params)
+    step.train_step_surfels_async(params, s.cameras, targets, opt, grads_ref, bufs, cap, n_dup)
+    torch.cuda.synchronize()
+    grads = api.alloc_param_grads(params)
+    g = step.GraphedStep(params, s.cameras, targets, opt, grads, bufs, cap, surfels=True)
+    for k in NAMES:
+        grads[k].fill_(123.0)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert g.n_dup.cpu().tolist() == n_dup.cpu().tolist()
+    for k in NAMES:
+        a, r = grads[k].cpu().numpy(), grads_ref[k].cpu().numpy()
+        assert np.abs(a - r).max() <= 1e-3 * max(np.abs(r).max(), 1e-30), k
+    assert api.gs_device_error() == _abi.GS_OK
