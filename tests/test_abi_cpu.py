@@ -98,6 +98,33 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert b"16-byte" in lib.gs_last_error_message()
 
 
+def test_new_entry_points_reject_bad_arguments_on_the_host(lib):
+    cam, opt = _cam(), api.make_options(0)
+    # aligned placeholder addresses: every call below fails on the host before any device work
+    proj = _abi.gs_proj(rec=256, depth=256, radius=256, tiles_touched=256, n=10)
+    # the sort without host synchronisation: capacity, ranges, image size
+    assert lib.gs_bin_and_sort_async(C.byref(proj), C.byref(cam), C.byref(opt), None, 0, None, None, -1, None, None,
+                                     None) == _abi.GS_ERR_ARG
+    assert lib.gs_bin_and_sort_async(C.byref(proj), C.byref(cam), C.byref(opt), None, 0, None, None, 100, None, None,
+                                     None) == _abi.GS_ERR_ARG
+    assert b"tile_ranges" in lib.gs_last_error_message()
+    huge = _cam(w=4096, h=4096)  # 65,536 tiles: beyond the counting pass
+    assert lib.gs_bin_and_sort_async(C.byref(proj), C.byref(huge), C.byref(opt), None, 0, None, 256, 100, None, 256,
+                                     None) == _abi.GS_ERR_ARG
+    assert b"49152" in lib.gs_last_error_message()
+    # the preprocess backward with statistics: the statistics block is required
+    p = _abi.gs_params(n=0)
+    empty = _abi.gs_proj(n=0)
+    assert lib.gs_preprocess_bwd_stats(C.byref(p), C.byref(cam), C.byref(opt), C.byref(empty), None, None, None, None,
+                                       None, None, 0, None, None) == _abi.GS_ERR_ARG
+    assert b"stats" in lib.gs_last_error_message()
+    # the surfel backward has no shared-memory mode
+    sm = api.make_options(0, bwd_mode="sm")
+    assert lib.gs_render2d_bwd(None, 0, None, None, C.byref(cam), C.byref(sm), None, None, None, None,
+                               None) == _abi.GS_ERR_ARG
+    assert b"GS_BWD_SM" in lib.gs_last_error_message()
+
+
 def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(_abi, "_lib", None)
