@@ -886,29 +886,30 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
         const unsigned yab = (unsigned)ya | ((unsigned)max(yb, 0) << 16);
         const unsigned m = div_magic(w);
         const unsigned area_l = (w > 0u && ya < yb) ? w * (unsigned)(yb - ya) : 0u;
+        const unsigned tl0_l = (unsigned)ya * (unsigned)tiles_x + (pr.x & 0xffffu);  // band-local first tile
         unsigned hit = __ballot_sync(full, area_l > 0u);
+        // pairing, decided for all lanes at once: a hit lane pairs with the next hit lane when both
+        // cover at most 16 tiles of the band and their rectangles are disjoint; then each half-warp
+        // places one of them (they share no tile, so their order does not matter)
+        const unsigned above = hit & ~((2u << lane) - 1u);
+        const int nxt = above ? __ffs(above) - 1 : lane;
+        const unsigned xw_n = __shfl_sync(full, xw, nxt), yab_n = __shfl_sync(full, yab, nxt);
+        const unsigned area_n = __shfl_sync(full, area_l, nxt);
+        const unsigned x1 = xw & 0xffffu, x2 = xw_n & 0xffffu;
+        const bool apart = x1 + (xw >> 16) <= x2 || x2 + (xw_n >> 16) <= x1 || (yab >> 16) <= (yab_n & 0xffffu) ||
+                           (yab_n >> 16) <= (yab & 0xffffu);
+        const unsigned pairable = __ballot_sync(full, area_l > 0u && above != 0u && area_l <= 16u && area_n <= 16u && apart);
         while (hit) {
-            // the next Gaussian, and the one after it when both cover at most 16 tiles of the band
-            // and their rectangles are disjoint: then each half-warp places one of them
             const int j1 = __ffs(hit) - 1;
             hit &= hit - 1u;
-            const int j2 = hit ? __ffs(hit) - 1 : j1;
-            const unsigned xw1 = __shfl_sync(full, xw, j1), yab1 = __shfl_sync(full, yab, j1);
-            const unsigned xw2 = __shfl_sync(full, xw, j2), yab2 = __shfl_sync(full, yab, j2);
-            const unsigned a1 = (xw1 >> 16) * ((yab1 >> 16) - (yab1 & 0xffffu));
-            const unsigned a2 = (xw2 >> 16) * ((yab2 >> 16) - (yab2 & 0xffffu));
-            const unsigned x1 = xw1 & 0xffffu, x2 = xw2 & 0xffffu;
-            const bool apart = x1 + (xw1 >> 16) <= x2 || x2 + (xw2 >> 16) <= x1 ||
-                               (yab1 >> 16) <= (yab2 & 0xffffu) || (yab2 >> 16) <= (yab1 & 0xffffu);
-            const bool pair = j2 != j1 && a1 <= 16u && a2 <= 16u && apart;
+            const bool pair = (pairable >> j1) & 1u;  // warp-uniform
+            const int j2 = pair ? __ffs(hit) - 1 : j1;
             if (pair) hit &= hit - 1u;
             const bool second = pair && lane >= 16;
             const int j = second ? j2 : j1;
             const unsigned jg = __shfl_sync(full, g, j), jm = __shfl_sync(full, m, j);
-            const unsigned jxw = second ? xw2 : xw1, jyab = second ? yab2 : yab1;
-            const unsigned jw = jxw >> 16, jya = jyab & 0xffffu;
-            const unsigned area = second ? a2 : a1;
-            const unsigned tl0 = jya * (unsigned)tiles_x + (jxw & 0xffffu);
+            const unsigned jw = __shfl_sync(full, w, j), area = __shfl_sync(full, area_l, j);
+            const unsigned tl0 = __shfl_sync(full, tl0_l, j);
             const unsigned step = pair ? 16u : 32u;
             for (unsigned k = pair ? (lane & 15u) : lane; k < area; k += step) {
                 const unsigned rk = div_by(k, jw, jm);
