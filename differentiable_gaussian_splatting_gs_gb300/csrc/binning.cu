@@ -703,20 +703,22 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__
     if (c >= (int)*nchunks) return;
     const int first = (int)chunk_first[c], last = (int)chunk_first[c + 1];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int t = threadIdx.x; t < T; t += blockDim.x) cnt[t] = 0u;
+    for (int t = threadIdx.x; t < T / 4; t += blockDim.x) reinterpret_cast<uint4*>(cnt)[t] = make_uint4(0u, 0u, 0u, 0u);
+    for (int t = (T & ~3) + threadIdx.x; t < T; t += blockDim.x) cnt[t] = 0u;
     __syncthreads();
     for (int base = first + 32 * warp; base < last; base += (int)blockDim.x) {  // warp-uniform
         const int i = base + lane;
-        int x0 = 0, y0 = 0, w = 0, area = 0;
+        int x0 = 0, y0 = 0, w = 0, h = 0, area = 0;
         if (i < last) {
             const uint2 r = crect[i];
             x0 = (int)(r.x & 0xffffu);
             y0 = (int)(r.x >> 16);
             w = (int)(r.y & 0xffffu);
-            area = w * (int)(r.y >> 16);
+            h = (int)(r.y >> 16);
+            area = w * h;
         }
         if (area <= kSmallRect) {
-            for (int y = 0; y < area / max(w, 1); ++y)
+            for (int y = 0; y < h; ++y)
                 for (int x = 0; x < w; ++x) atomicAdd(&cnt[(y0 + y) * tiles_x + x0 + x], 1u);
         }
         const unsigned m = div_magic((unsigned)w);
