@@ -163,9 +163,11 @@ int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options*
                     void* workspace, size_t workspace_bytes, uint64_t* keys, uint32_t* vals,
                     int64_t capacity, int64_t* n_dup_out, uint32_t* tile_ranges, void* stream);
 
-/* Rendering phase (Odin, Figure 7: "rendering"). One 256-thread block per 16x16 tile stages the
- * tile's list in batches of 256 records in shared memory and blends front to back per pixel:
- * power = -(A dx^2 + C dy^2)/2 - B dx dy with d = mean - pixel centre; skip power > 0;
+/* Rendering phase (Odin, Figure 7: "rendering"). One 128-thread block per 16x16 tile (two pixels
+ * per thread) stages the tile's list in batches of 128 records in shared memory (bulk
+ * asynchronous copies) and blends front to back per pixel:
+ * power = -(A dx^2 + C dy^2)/2 - B dx dy with d = mean - pixel centre (evaluated as a sum of
+ * non-negative terms, so it is never positive);
  * alpha = min(0.99, opacity exp(power)); skip alpha < 1/255; stop before a Gaussian whose
  * T (1 - alpha) < 1e-4; colour += rgb alpha T; T *= 1 - alpha.
  * Outputs: image [3][H][W] = colour + T bg, t_final [H][W] = T, n_contrib [H][W] = 1 + the
