@@ -274,9 +274,10 @@ __global__ void __launch_bounds__(256) k_depth_hist4(const unsigned* __restrict_
 
 // One stable pass of the depth sort over the digit at `shift`. IOTA: the values are the item
 // indices and items with radius 0 are dropped (first pass); later passes take the count of valid
-// items from n_dev (the sum of the digit-0 histogram).
+// items from n_dev (the sum of the digit-0 histogram). The first pass is bounded to 40 registers
+// (six resident blocks per SM); the later ones run over the visible Gaussians only.
 template <bool IOTA>
-__global__ void __launch_bounds__(kSortThreads) k_onesweep(
+__global__ void __launch_bounds__(kSortThreads, IOTA ? 6 : 1) k_onesweep(
     const unsigned* __restrict__ keys_in, const unsigned* __restrict__ vals_in, unsigned* __restrict__ keys_out,
     unsigned* __restrict__ vals_out, int n_bound, const unsigned* __restrict__ ghist4, const int* __restrict__ radius,
     int pass, unsigned* __restrict__ ticket, unsigned long long* __restrict__ status, unsigned* __restrict__ nvis_out,
@@ -1025,6 +1026,11 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
     const size_t sstride = (size_t)w.sweep_blocks * 256;
     const int nb = sort_blocks(n);
     const int hblocks = nb < 4 * 152 ? nb : 4 * 152;
+    // the first pass runs over all N Gaussians: six blocks per SM (its launch bound, and shared memory
+    // preferred over L1) keep its 2048-item blocks in one wave up to 1.87M Gaussians
+    if ((e = cudaFuncSetAttribute(k_onesweep<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared)))
+        return e;
     count_launches(5);
     k_depth_hist4<<<hblocks, 256, 0, st>>>(depth_bits, n, proj.radius, ghist4);
     k_onesweep<true><<<nb, kSortThreads, 0, st>>>(depth_bits, nullptr, w.dkA, w.dvA, n, ghist4, proj.radius, 0,
