@@ -235,6 +235,7 @@ constexpr unsigned long long kStatAgg = 1ull << 62, kStatIncl = 2ull << 62, kSta
 
 __global__ void __launch_bounds__(256) k_depth_hist4(const unsigned* __restrict__ keys, int n,
                                                      const int* __restrict__ radius, unsigned* __restrict__ ghist) {
+    pdl_entry();
     __shared__ unsigned h[4][256];
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 6 : 1) k_onesweep(
     unsigned* __restrict__ vals_out, int n_bound, const unsigned* __restrict__ ghist4, const int* __restrict__ radius,
     int pass, unsigned* __restrict__ ticket, unsigned long long* __restrict__ status, unsigned* __restrict__ nvis_out,
     unsigned spin_limit, unsigned* __restrict__ err) {
+    pdl_entry();
     __shared__ unsigned woff[8][256];      // per-warp digit counts, then block-local offsets
     __shared__ unsigned lbase[256];        // block-local start of each digit
     __shared__ unsigned gbase[256];        // global start of this block's run of each digit
@@ -433,6 +435,7 @@ __global__ void __launch_bounds__(256) k_count(int n_bound, const unsigned* __re
                                                const int* __restrict__ radius, int tiles_x, int tiles_y,
                                                unsigned long long* __restrict__ block_sums,
                                                uint2* __restrict__ crect) {
+    pdl_entry();
     __shared__ unsigned long long ws[8];
     const int n = item_count(n_bound, n_dev);
     const int i = blockIdx.x * 256 + threadIdx.x;
@@ -498,6 +501,7 @@ __device__ __forceinline__ T block_scan_1024(T v, T* wsum, T* block_total) {
 __global__ void __launch_bounds__(1024) k_scan_u64(const unsigned long long* __restrict__ in, int m,
                                                    unsigned long long* __restrict__ out,
                                                    unsigned long long* __restrict__ total) {
+    pdl_entry();
     __shared__ unsigned long long wsum[32];
     __shared__ unsigned long long round_total;
     unsigned long long carry = 0;
@@ -654,6 +658,7 @@ __global__ void __launch_bounds__(256) k_chunk_bounds(int n_bound, const unsigne
                                                       const unsigned long long* __restrict__ block_offs, int cmax,
                                                       unsigned* __restrict__ chunk_first,
                                                       unsigned* __restrict__ nchunks) {
+    pdl_entry();
     __shared__ unsigned long long wsum[8];
     __shared__ int s_c[256];
     const int n = item_count(n_bound, n_dev);
@@ -698,6 +703,7 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__
                                                     const unsigned* __restrict__ chunk_first,
                                                     const uint2* __restrict__ crect, int tiles_x, int T,
                                                     unsigned* __restrict__ table) {
+    pdl_entry();
     extern __shared__ unsigned cnt[];
     const unsigned full = 0xffffffffu;
     const int c = blockIdx.x;
@@ -748,6 +754,7 @@ constexpr int kColUnroll = 16;  // table loads in flight per lane
 __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* __restrict__ nchunks, int T,
                                                                 unsigned* __restrict__ table,
                                                                 unsigned* __restrict__ tile_total) {
+    pdl_entry();
     __shared__ unsigned part[kScanWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * 32 + lane;
@@ -792,15 +799,17 @@ __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* 
     }
 }
 
-// Exclusive scan of the tile totals (one block): tile_start[t], total[0] = D, and the tile
-// ranges [start, start + count). When D exceeds the capacity every range is written empty, so
+// Exclusive scan of the tile totals (one block): tile_start[t], total[0] = D (also written to
+// total_copy when given), and the tile ranges [start, start + count). When D exceeds the capacity every range is written empty, so
 // that no later kernel reads past the caller's list; with `err` (the call that does not read D on
 // the host) the check bit is also set.
 __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __restrict__ tile_total,
                                                     unsigned* __restrict__ tile_start,
                                                     unsigned long long* __restrict__ total,
                                                     unsigned long long capacity, uint2* __restrict__ ranges,
-                                                    unsigned* __restrict__ err) {
+                                                    unsigned* __restrict__ err,
+                                                    unsigned long long* __restrict__ total_copy) {
+    pdl_entry();
     __shared__ unsigned long long wsum[32];
     __shared__ unsigned long long round_total;
     unsigned long long carry = 0;
@@ -822,7 +831,10 @@ __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __res
         carry += round_total;
         __syncthreads();
     }
-    if (threadIdx.x == 0) total[0] = carry;
+    if (threadIdx.x == 0) {
+        total[0] = carry;
+        if (total_copy) *total_copy = carry;
+    }
     const bool over = carry > capacity;
     if (over && err && threadIdx.x == 0) atomicOr(err, kErrCheck);
     for (int t = threadIdx.x; t < T; t += blockDim.x) {  // the last round's barrier made every start visible
@@ -848,6 +860,7 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
     const unsigned* __restrict__ table, const unsigned* __restrict__ tile_start, unsigned capacity,
     unsigned* __restrict__ vals, unsigned long long* __restrict__ keys64, const unsigned* __restrict__ depth_bits,
     unsigned* __restrict__ err) {
+    pdl_entry();
     extern __shared__ unsigned smem_off[];
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1014,12 +1027,15 @@ static cudaError_t radix_pass(const unsigned* kin, const unsigned* vin, unsigned
 // `err` when they give up.
 cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, unsigned* err,
                       unsigned spin_limit, unsigned long long capacity, unsigned* ranges, unsigned* overflow_err,
-                      cudaStream_t st) {
+                      unsigned long long* total_copy, cudaStream_t st) {
     const int n = (int)proj.n;
     if (n == 0) return cudaMemsetAsync(w.total, 0, 8, st);
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
+    const int T = tiles_x * tiles_y;
     cudaError_t e;
+    // both memsets first, so that the kernels after them follow one another directly (launch_pdl)
     if ((e = cudaMemsetAsync(w.sweep, 0, w.sweep_bytes, st))) return e;
+    if (counting_path(T) && (e = cudaMemsetAsync(w.nchunks, 0, 4, st))) return e;
     unsigned* ghist4 = reinterpret_cast<unsigned*>(w.sweep);
     unsigned* tickets = ghist4 + 4 * 256;
     unsigned long long* status = reinterpret_cast<unsigned long long*>(w.sweep + 4 * 256 * 4 + 256);
@@ -1032,38 +1048,48 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
                                   (int)cudaSharedmemCarveoutMaxShared)))
         return e;
     count_launches(5);
-    k_depth_hist4<<<hblocks, 256, 0, st>>>(depth_bits, n, proj.radius, ghist4);
-    k_onesweep<true><<<nb, kSortThreads, 0, st>>>(depth_bits, nullptr, w.dkA, w.dvA, n, ghist4, proj.radius, 0,
-                                                  tickets, status, nullptr, spin_limit, err);
-    k_onesweep<false><<<nb, kSortThreads, 0, st>>>(w.dkA, w.dvA, w.dkB, w.dvB, n, ghist4, nullptr, 1, tickets + 1,
-                                                   status + sstride, w.nvis, spin_limit, err);
-    k_onesweep<false><<<nb, kSortThreads, 0, st>>>(w.dkB, w.dvB, w.dkA, w.dvA, n, ghist4, nullptr, 2, tickets + 2,
-                                                   status + 2 * sstride, nullptr, spin_limit, err);
-    k_onesweep<false><<<nb, kSortThreads, 0, st>>>(w.dkA, w.dvA, w.dkB, w.dvB, n, ghist4, nullptr, 3, tickets + 3,
-                                                   status + 3 * sstride, nullptr, spin_limit, err);
-    if ((e = cudaGetLastError())) return e;
+    if ((e = launch_pdl(k_depth_hist4, dim3(hblocks), dim3(256), 0, st, depth_bits, n, proj.radius, ghist4)))
+        return e;
+    if ((e = launch_pdl(k_onesweep<true>, dim3(nb), dim3(kSortThreads), 0, st, depth_bits, nullptr, w.dkA, w.dvA, n,
+                        ghist4, proj.radius, 0, tickets, status, nullptr, spin_limit, err)))
+        return e;
+    if ((e = launch_pdl(k_onesweep<false>, dim3(nb), dim3(kSortThreads), 0, st, w.dkA, w.dvA, w.dkB, w.dvB, n, ghist4,
+                        nullptr, 1, tickets + 1, status + sstride, w.nvis, spin_limit, err)))
+        return e;
+    if ((e = launch_pdl(k_onesweep<false>, dim3(nb), dim3(kSortThreads), 0, st, w.dkB, w.dvB, w.dkA, w.dvA, n, ghist4,
+                        nullptr, 2, tickets + 2, status + 2 * sstride, nullptr, spin_limit, err)))
+        return e;
+    if ((e = launch_pdl(k_onesweep<false>, dim3(nb), dim3(kSortThreads), 0, st, w.dkA, w.dvA, w.dkB, w.dvB, n, ghist4,
+                        nullptr, 3, tickets + 3, status + 3 * sstride, nullptr, spin_limit, err)))
+        return e;
     const float4* rec = reinterpret_cast<const float4*>(proj.rec);
-    const int T = tiles_x * tiles_y;
     const int gblocks = (n + 255) / 256;
     if (counting_path(T)) {
         const size_t smem = (size_t)T * 4;
         if ((e = cudaFuncSetAttribute(k_chunk_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return e;
-        if ((e = cudaMemsetAsync(w.nchunks, 0, 4, st))) return e;
         count_launches(6);
-        k_count<<<gblocks, 256, 0, st>>>(n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y, w.bsum, w.crect);
-        k_scan_u64<<<1, 1024, 0, st>>>(w.bsum, gblocks, w.boff, w.dsum);
-        k_chunk_bounds<<<gblocks, 256, 0, st>>>(n, w.nvis, w.crect, w.boff, (int)w.cmax, w.chunk_first, w.nchunks);
-        k_chunk_hist<<<(unsigned)w.cmax, 256, smem, st>>>(w.nchunks, w.chunk_first, w.crect, tiles_x, T, w.table);
-        k_chunk_scan<<<(T + 31) / 32, 32 * kScanWarps, 0, st>>>(w.nchunks, T, w.table, w.tile_total);
-        k_tile_scan<<<1, 1024, 0, st>>>(T, w.tile_total, w.tile_start, w.total, capacity,
-                                        reinterpret_cast<uint2*>(ranges), overflow_err);
-        return cudaGetLastError();
+        if ((e = launch_pdl(k_count, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.dvB, rec, proj.radius, tiles_x,
+                            tiles_y, w.bsum, w.crect)))
+            return e;
+        if ((e = launch_pdl(k_scan_u64, dim3(1), dim3(1024), 0, st, w.bsum, gblocks, w.boff, w.dsum))) return e;
+        if ((e = launch_pdl(k_chunk_bounds, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.crect, w.boff, (int)w.cmax,
+                            w.chunk_first, w.nchunks)))
+            return e;
+        if ((e = launch_pdl(k_chunk_hist, dim3((unsigned)w.cmax), dim3(256), smem, st, w.nchunks, w.chunk_first,
+                            w.crect, tiles_x, T, w.table)))
+            return e;
+        if ((e = launch_pdl(k_chunk_scan, dim3((T + 31) / 32), dim3(32 * kScanWarps), 0, st, w.nchunks, T, w.table,
+                            w.tile_total)))
+            return e;
+        return launch_pdl(k_tile_scan, dim3(1), dim3(1024), 0, st, T, w.tile_total, w.tile_start, w.total, capacity,
+                          reinterpret_cast<uint2*>(ranges), overflow_err, total_copy);
     }
     count_launches(2);
-    k_count<<<gblocks, 256, 0, st>>>(n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y, w.bsum, nullptr);
-    k_scan_u64<<<1, 1024, 0, st>>>(w.bsum, gblocks, w.boff, w.total);
-    return cudaGetLastError();
+    if ((e = launch_pdl(k_count, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y,
+                        w.bsum, (uint2*)nullptr)))
+        return e;
+    return launch_pdl(k_scan_u64, dim3(1), dim3(1024), 0, st, w.bsum, gblocks, w.boff, w.total);
 }
 
 // Counting-path emission: the placement of every entry (the tile ranges were written by the tile
@@ -1083,10 +1109,9 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
     if ((e = cudaFuncSetAttribute(k_chunk_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
     const long long warps = w.cmax * nbands;
     count_launches(1);
-    k_chunk_place<<<(unsigned)((warps + wpb - 1) / wpb), 32 * wpb, smem, st>>>(
-        w.nchunks, w.chunk_first, w.dvB, w.crect, tiles_x, tiles_y, band_rows, nbands, w.table, w.tile_start,
-        (unsigned)capacity, vals, k64, depth_bits, err);
-    return cudaGetLastError();
+    return launch_pdl(k_chunk_place, dim3((unsigned)((warps + wpb - 1) / wpb)), dim3(32 * wpb), smem, st, w.nchunks,
+                      w.chunk_first, w.dvB, w.crect, tiles_x, tiles_y, band_rows, nbands, w.table, w.tile_start,
+                      (unsigned)capacity, vals, k64, depth_bits, err);
 }
 
 // Phase 2: placement (counting pass) or emission + tile radix passes and the ranges.
@@ -1131,22 +1156,21 @@ cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigne
     return cudaGetLastError();
 }
 
-// The whole binning and sort with no host synchronisation (counting path only): D is copied to
+// The whole binning and sort with no host synchronisation (counting path only): D is written to
 // n_dup_dev (when given) on the stream; duplicates beyond the capacity are dropped, every range is
 // written empty and the check bit is set.
 cudaError_t bin_sort_async(const gs_proj& proj, int tiles_x, int tiles_y, unsigned long long capacity,
                            const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
                            unsigned long long* n_dup_dev, unsigned* err, unsigned spin_limit, cudaStream_t st) {
     const long long T = (long long)tiles_x * tiles_y;
-    cudaError_t e = bin_count(proj, tiles_x, tiles_y, w, err, spin_limit, capacity, ranges, err, st);
+    // the tile scan writes D to n_dup_dev itself (no copy between the placement and the next kernel)
+    cudaError_t e = bin_count(proj, tiles_x, tiles_y, w, err, spin_limit, capacity, ranges, err, n_dup_dev, st);
     if (e) return e;
     if (proj.n == 0) {
-        e = cudaMemsetAsync(ranges, 0, (size_t)T * 8, st);
-    } else {
-        e = emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, err, st);
+        if ((e = cudaMemsetAsync(ranges, 0, (size_t)T * 8, st))) return e;
+        return n_dup_dev ? cudaMemsetAsync(n_dup_dev, 0, 8, st) : cudaSuccess;
     }
-    if (e || !n_dup_dev) return e;
-    return cudaMemcpyAsync(n_dup_dev, w.total, 8, cudaMemcpyDeviceToDevice, st);
+    return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, err, st);
 }
 
 }  // namespace gs

@@ -257,7 +257,7 @@ int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options*
     if (!err) return s;
     cudaStream_t st = as_stream(stream);
     cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, err, o.spin, (unsigned long long)capacity,
-                              tile_ranges, nullptr, st);
+                              tile_ranges, nullptr, nullptr, st);
     if (e) return cuda_fail(e, "gs_bin_and_sort: count");
     unsigned long long d = 0;
     if ((e = cudaMemcpyAsync(&d, w.total, 8, cudaMemcpyDeviceToHost, st))) return cuda_fail(e, "gs_bin_and_sort: read D");
@@ -296,7 +296,7 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
     if (!err) return s;
     cudaStream_t st = as_stream(stream);
     cudaError_t e = bin_count(*proj, kc.tiles_x, kc.tiles_y, w, err, o.spin, (unsigned long long)capacity,
-                              tile_ranges, nullptr, st);
+                              tile_ranges, nullptr, nullptr, st);
     if (e) return cuda_fail(e, "gs_bin_and_sort_static: count");
     unsigned long long d = 0;
     if ((e = cudaMemcpyAsync(&d, w.total, 8, cudaMemcpyDeviceToHost, st)))

@@ -67,6 +67,22 @@ __device__ __forceinline__ unsigned smem_u32(const void* p) {
     return static_cast<unsigned>(__cvta_generic_to_shared(p));
 }
 
+// ---- programmatic dependent launch (inline PTX, sm_90+) ---------------------------------------
+// A kernel launched with programmatic stream serialization (launch_pdl) may have its blocks
+// dispatched while the kernel before it in the stream is still running. pdl_wait blocks until that
+// kernel has completed and its memory operations are visible; it is the first statement of every
+// kernel launched that way, so no such kernel reads anything the stream wrote before it early.
+// Without a programmatic dependency it returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Allows the next kernel in the stream (when launched by launch_pdl) to start dispatching its
+// blocks, which then wait in pdl_wait: its launch overlaps this kernel's last wave.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+// Both, at kernel entry.
+__device__ __forceinline__ void pdl_entry() {
+    pdl_wait();
+    pdl_launch_dependents();
+}
+
 // ---- mbarrier + bulk asynchronous copy (inline PTX, sm_90+) ----------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {

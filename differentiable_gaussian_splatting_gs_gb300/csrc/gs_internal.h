@@ -13,6 +13,27 @@ struct KernelCamera;
 // Adds k to the process-wide count of kernel launches (reported by gs_kernel_launches).
 void count_launches(int k);
 
+// Launches `kernel` on `st` with programmatic stream serialization: its blocks may be dispatched
+// while the previous kernel of the stream is still running (hiding the launch gap between the
+// step's dependent kernels, also inside a captured graph). Every kernel launched this way calls
+// pdl_wait (gs_common.cuh) before touching memory. After a non-kernel operation (a memset, a copy,
+// an event) the launch is ordered as usual.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Sort workspace carved from the caller's buffer (all pieces 256-byte aligned).
 struct SortWorkspace {
     unsigned *dkA, *dkB, *dvA, *dvB;   // depth-sort keys / values, ping-pong, N each
@@ -36,10 +57,11 @@ struct SortWorkspace {
 SortWorkspace carve_workspace(void* base, long long n, long long cap, long long tiles);
 // Phase 1 of the binning (depth sort, duplicate counts, on the counting path also the tile
 // table, starts and ranges); `ranges` and `capacity` are used on the counting path only, and
-// overflow_err (may be NULL) receives the check bit when D exceeds the capacity there.
+// overflow_err (may be NULL) receives the check bit when D exceeds the capacity there;
+// total_copy (may be NULL) receives D on the counting path.
 cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortWorkspace& w, unsigned* err,
                       unsigned spin_limit, unsigned long long capacity, unsigned* ranges, unsigned* overflow_err,
-                      cudaStream_t st);
+                      unsigned long long* total_copy, cudaStream_t st);
 cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigned d, unsigned long long capacity,
                           const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges, unsigned* err,
                           cudaStream_t st);

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* 
                                                             float4* __restrict__ rec, float* __restrict__ depth,
                                                             int* __restrict__ radius,
                                                             unsigned* __restrict__ tiles_touched) {
+    pdl_entry();
     constexpr int K = (DEG + 1) * (DEG + 1);
     constexpr int K3 = 3 * K;
     __shared__ float tile_all[kFwdThreads / 32][32 * (K3 + 1)];
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
     float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
     float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate, const DensifyArgs stats) {
+    pdl_entry();
     constexpr int K = (DEG + 1) * (DEG + 1);
     constexpr int K3 = 3 * K;
     __shared__ float tile_all[kBwdThreads / 32][32 * (K3 + 1)];
@@ -396,13 +398,11 @@ cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCa
     float4* rec = reinterpret_cast<float4*>(out.rec);
     unsigned* tt = out.tiles_touched;
     count_launches(1);
-    switch (deg) {
-        case 0: k_preprocess<0><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
-        case 1: k_preprocess<1><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
-        case 2: k_preprocess<2><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
-        default: k_preprocess<3><<<blocks, kFwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt); break;
-    }
-    return cudaGetLastError();
+    void (*k)(int, const float*, const float*, const float*, const float*, const float*, const KernelCamera, float4*,
+              float*, int*, unsigned*) = deg == 0 ? k_preprocess<0> : deg == 1 ? k_preprocess<1>
+                                                : deg == 2 ? k_preprocess<2> : k_preprocess<3>;
+    return launch_pdl(k, dim3(blocks), dim3(kFwdThreads), 0, st, n, p.mean3d, p.log_scale, p.quat, p.opacity_logit,
+                      p.sh, cam, rec, out.depth, out.radius, tt);
 }
 
 cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
@@ -413,21 +413,22 @@ cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const Kern
     const float4* g2 = reinterpret_cast<const float4*>(grad2d);
     const DensifyArgs none{};
     count_launches(1);
-#define GS_PREBWD(D)                                                                                                \
-    (stats ? k_preprocess_bwd<D, true><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat,            \
-                                                                       p.opacity_logit, p.sh, cam, radius, g2, dm,  \
-                                                                       dls, dq, dlg, dsh, accumulate, *stats)       \
-           : k_preprocess_bwd<D, false><<<blocks, kBwdThreads, 0, st>>>(n, p.mean3d, p.log_scale, p.quat,           \
-                                                                        p.opacity_logit, p.sh, cam, radius, g2, dm, \
-                                                                        dls, dq, dlg, dsh, accumulate, none))
+#define GS_PREBWD(D)                                                                                          \
+    (stats ? launch_pdl(k_preprocess_bwd<D, true>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,         \
+                        p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh,      \
+                        accumulate, *stats)                                                                     \
+           : launch_pdl(k_preprocess_bwd<D, false>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,        \
+                        p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh,      \
+                        accumulate, none))
+    cudaError_t e;
     switch (deg) {
-        case 0: GS_PREBWD(0); break;
-        case 1: GS_PREBWD(1); break;
-        case 2: GS_PREBWD(2); break;
-        default: GS_PREBWD(3); break;
+        case 0: e = GS_PREBWD(0); break;
+        case 1: e = GS_PREBWD(1); break;
+        case 2: e = GS_PREBWD(2); break;
+        default: e = GS_PREBWD(3); break;
     }
 #undef GS_PREBWD
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace gs

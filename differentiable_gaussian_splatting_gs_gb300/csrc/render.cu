@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
                                                           unsigned n_gauss, float* __restrict__ image,
                                                           float* __restrict__ t_final, unsigned* __restrict__ n_contrib,
                                                           unsigned spin_limit, unsigned* __restrict__ err) {
+    pdl_entry();
     constexpr int kB = kFwdBatch;
     __shared__ FwdStage s;
     const int tile = blockIdx.x;
@@ -398,6 +399,7 @@ __global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restri
                                                           const unsigned* __restrict__ n_contrib,
                                                           float* __restrict__ grad2d, int thr, unsigned spin_limit,
                                                           unsigned* __restrict__ err) {
+    pdl_entry();
     constexpr int kB = kBwdBatch;
     __shared__ BwdSmem sm;
     BwdStage& s = sm.st;
@@ -564,21 +566,18 @@ cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* 
     const float4* rec = reinterpret_cast<const float4*>(proj.rec);
     const uint2* rg = reinterpret_cast<const uint2*>(ranges);
     count_launches(1);
-    if (staging == GS_STAGE_LOADS)
-        k_render_fwd<GS_STAGE_LOADS><<<tiles, kFwdBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
-    else
-        k_render_fwd<GS_STAGE_BULK><<<tiles, kFwdBlock, 0, st>>>(rec, vals, rg, cam, (unsigned)proj.n, image, t_final, n_contrib, spin_limit, err);
-    return cudaGetLastError();
+    return launch_pdl(staging == GS_STAGE_LOADS ? k_render_fwd<GS_STAGE_LOADS> : k_render_fwd<GS_STAGE_BULK>,
+                      dim3(tiles), dim3(kFwdBlock), 0, st, rec, vals, rg, cam, (unsigned)proj.n, image, t_final,
+                      n_contrib, spin_limit, err);
 }
 
 template <int MODE>
-static void launch_bwd_mode(int staging, int tiles, const float4* rec, const unsigned* vals, const uint2* rg,
-                            const KernelCamera& cam, unsigned n, const float* dl, const float* tf, const unsigned* nc,
-                            float* g2, int thr, unsigned spin, unsigned* err, cudaStream_t st) {
-    if (staging == GS_STAGE_LOADS)
-        k_render_bwd<MODE, GS_STAGE_LOADS><<<tiles, kBwdBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
-    else
-        k_render_bwd<MODE, GS_STAGE_BULK><<<tiles, kBwdBlock, 0, st>>>(rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
+static cudaError_t launch_bwd_mode(int staging, int tiles, const float4* rec, const unsigned* vals, const uint2* rg,
+                                   const KernelCamera& cam, unsigned n, const float* dl, const float* tf,
+                                   const unsigned* nc, float* g2, int thr, unsigned spin, unsigned* err,
+                                   cudaStream_t st) {
+    return launch_pdl(staging == GS_STAGE_LOADS ? k_render_bwd<MODE, GS_STAGE_LOADS> : k_render_bwd<MODE, GS_STAGE_BULK>,
+                      dim3(tiles), dim3(kBwdBlock), 0, st, rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
 }
 
 cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& proj, const unsigned* vals,
@@ -591,12 +590,11 @@ cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& pro
     const unsigned n = (unsigned)proj.n;
     count_launches(1);
     switch (mode) {
-        case GS_BWD_DIRECT: launch_bwd_mode<GS_BWD_DIRECT>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
-        case GS_BWD_WARP: launch_bwd_mode<GS_BWD_WARP>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
-        case GS_BWD_ADAPTIVE: launch_bwd_mode<GS_BWD_ADAPTIVE>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
-        default: launch_bwd_mode<GS_BWD_SM>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st); break;
+        case GS_BWD_DIRECT: return launch_bwd_mode<GS_BWD_DIRECT>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
+        case GS_BWD_WARP: return launch_bwd_mode<GS_BWD_WARP>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
+        case GS_BWD_ADAPTIVE: return launch_bwd_mode<GS_BWD_ADAPTIVE>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
+        default: return launch_bwd_mode<GS_BWD_SM>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace gs

@@ -360,7 +360,7 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
  * rasterization pipeline; same outputs as gs_bin_and_sort). It neither synchronises nor
  * allocates; every launch and copy goes on `stream`.
  *   - D is not returned on the host: when n_dup_device (device uint64, 8-byte aligned) is not
- *     NULL, D is copied there on the stream.
+ *     NULL, D is written there on the stream (by the tile scan).
  *   - Capacity: if D > capacity, no entry is written past `capacity`, every tile range is
  *     written empty (so later kernels read nothing) and the device error word gets the check
  *     bit (gs_device_error returns GS_ERR_DEVICE_CHECK); *n_dup_device then holds the D needed.
