@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 6 : 1) k_onesweep(
     unsigned* __restrict__ vals_out, int n_bound, const unsigned* __restrict__ ghist4, const int* __restrict__ radius,
     int pass, unsigned* __restrict__ ticket, unsigned long long* __restrict__ status, unsigned* __restrict__ nvis_out,
     unsigned spin_limit, unsigned* __restrict__ err) {
-    pdl_entry();
+    if (IOTA) pdl_entry();  // the histograms were written by the kernel just before this pass
     __shared__ unsigned woff[8][256];      // per-warp digit counts, then block-local offsets
     __shared__ unsigned lbase[256];        // block-local start of each digit
     __shared__ unsigned gbase[256];        // global start of this block's run of each digit
@@ -303,6 +303,12 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 6 : 1) k_onesweep(
         if (lane == 0) atomicAdd(&s_n, t);
         __syncthreads();
     }
+    const unsigned tv = ghist[threadIdx.x];  // items of digit d = thread in the whole pass
+    // Later passes read their ticket and the histograms before waiting: both were written two or
+    // more kernels back (the memset, the histogram kernel), which have completed once any block of
+    // this pass runs, because the pass before lets its dependents launch only after its own wait.
+    // The keys of the pass before are read after waiting for it.
+    if (!IOTA) pdl_entry();
     const int block = (int)s_block;
     if (!IOTA && nvis_out && block == 0 && threadIdx.x == 0) *nvis_out = s_n;
     const int n = IOTA ? n_bound : min(n_bound, (int)s_n);
@@ -379,7 +385,6 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 6 : 1) k_onesweep(
         }
         if (lane == 31) wsum[warp] = x;
         // global digit start: exclusive scan of the pass histogram
-        const unsigned tv = ghist[d];
         unsigned tx = tv;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
