@@ -70,9 +70,11 @@ __device__ __forceinline__ unsigned smem_u32(const void* p) {
 // ---- programmatic dependent launch (inline PTX, sm_90+) ---------------------------------------
 // A kernel launched with programmatic stream serialization (launch_pdl) may have its blocks
 // dispatched while the kernel before it in the stream is still running. pdl_wait blocks until that
-// kernel has completed and its memory operations are visible; it is the first statement of every
-// kernel launched that way, so no such kernel reads anything the stream wrote before it early.
-// Without a programmatic dependency it returns at once.
+// kernel has completed and its memory operations are visible. Every kernel launched that way calls
+// it before touching memory that kernel may write or read, normally as its first statement. Since
+// each kernel lets its dependents launch only after its own wait, anything written two or more
+// kernels back is complete when a block starts and may be read before the wait (the later
+// depth-sort passes do so). Without a programmatic dependency it returns at once.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 // Allows the next kernel in the stream (when launched by launch_pdl) to start dispatching its
 // blocks, which then wait in pdl_wait: its launch overlaps this kernel's last wave.
