@@ -696,11 +696,17 @@ def run_ours(args, rank, world, local_rank):
         flops = counts["pairs_replayed_bwd"] * BWD_FLOPS_PER_REPLAYED_PAIR
         ach = flops / (bwd_avg_ms / 1e3) / 1e12
         blended = counts["pairs_blended"] * BWD_FLOPS_PER_PAIR / (bwd_avg_ms / 1e3) / 1e12
-        traffic = None
+        traffic = l2_red = None
         tr = json_block(TRAFFIC_PATH)
         # the counters hold while the kernel source and its launch defaults (the C ABI file) are unchanged
         if tr and tr.get("source_hash") == source_hash(*TRAFFIC_SOURCES):
             traffic = tr.get("dram_bytes_per_launch")
+            if "l2_red_frac_of_peak" in tr:
+                # the L2-atomic roofline: reduction sectors the gradient atomics put through the L2,
+                # against the L2's sustained reduction rate (ncu, one launch)
+                l2_red = {"sectors_per_launch": tr.get("l2_red_sectors_per_launch"),
+                          "frac_of_peak": tr["l2_red_frac_of_peak"],
+                          "source": "ncu, profiles/" + os.path.basename(TRAFFIC_PATH)}
         roof = {"kernel": "gs_render_bwd (k_render_bwd + gradient zeroing)", "bound": "alu", "achieved": ach,
                 "peak": alu_peak, "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": traffic,
                 "numerator": "60 FP32 operations per (pixel, Gaussian) pair replayed from each pixel's last "
@@ -709,7 +715,8 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock of measured peaks file",
                 "kernel_ms": bwd_avg_ms, "algorithmic_flops": flops,
                 "hbm_frac_of_measured": (counts.get("bwd_bytes", 0) / (bwd_avg_ms / 1e3) / 1e9) /
-                float(peaks.get("hbm_gbs", 6800.0))}
+                float(peaks.get("hbm_gbs", 6800.0)),
+                "l2_atomic": l2_red}
 
     line = {"metric": METRIC, "value": value, "unit": "Mpix/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
