@@ -183,3 +183,36 @@ def test_graphed_surfel_step_matches_eager_surfel_step():
         a, r = grads[k].cpu().numpy(), grads_ref[k].cpu().numpy()
         assert np.abs(a - r).max() <= 1e-3 * max(np.abs(r).max(), 1e-30), k
     assert api.gs_device_error() == _abi.GS_OK
+
+
+def test_back_to_back_views_without_synchronisation():
+    """Three views' preprocess and sort enqueued back to back on one stream with no synchronisation
+    in between, each into its own buffers (the kernels of consecutive calls may overlap through
+    programmatic dependent launch), against the synchronising sort of each view run alone."""
+    s = gs_scenes.make_scene(3, n=20_000, res_scale=0.25, views=3)
+    params = _params(s)
+    opt = api.make_options(s.sh_degree)
+    refs = []
+    for cam in s.cameras:
+        refs.append(api.gs_bin_and_sort(api.gs_preprocess(params, cam, opt), cam, opt))
+    projs, bufs, ranges, ndup = [], [], [], []
+    for cam, r in zip(s.cameras, refs):
+        projs.append(api.alloc_proj(s.n, DEV))
+        b = api.SortBuffers(DEV)
+        b.ensure(s.n, r.n_dup + 100, cam.width, cam.height, False)
+        bufs.append(b)
+        ranges.append(torch.empty((((cam.width + 15) // 16) * ((cam.height + 15) // 16), 2), dtype=torch.int32,
+                                  device=DEV))
+        ndup.append(torch.zeros(1, dtype=torch.int64, device=DEV))
+    torch.cuda.synchronize()
+    outs = []
+    for v, cam in enumerate(s.cameras):
+        proj = api.gs_preprocess(params, cam, opt, out=projs[v])
+        outs.append(api.gs_bin_and_sort_async(proj, cam, opt, refs[v].n_dup + 100, buffers=bufs[v],
+                                              ranges=ranges[v], n_dup=ndup[v]))
+    torch.cuda.synchronize()
+    for r, o in zip(refs, outs):
+        D = r.n_dup
+        assert int(o.n_dup.item()) == D
+        assert torch.equal(o.vals[:D], r.vals) and torch.equal(o.ranges, r.ranges)
+    assert api.gs_device_error() == _abi.GS_OK
