@@ -24,8 +24,9 @@
  *     number of duplicates.
  *   - The 3D path's kernels are launched with programmatic dependent launch (programmatic stream
  *     serialization): their blocks may be dispatched while the kernel enqueued before them is
- *     still running, but each waits for that kernel's completion and memory before touching
- *     anything that kernel may read or write, so stream order holds as for ordinary launches.
+ *     still running, but each waits for that kernel's completion and memory before reading
+ *     anything it may write or writing anything it may read, so stream order holds as for
+ *     ordinary launches.
  *   - Status codes: 0 on success, a negative GS_ERR_* otherwise. No C++ exception crosses the ABI.
  *     gs_last_error_message() describes the last failure of the calling thread.
  *   - Non-finite inputs are not errors: a Gaussian whose projection is not finite is culled.
