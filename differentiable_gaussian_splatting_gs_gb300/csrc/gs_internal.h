@@ -17,8 +17,8 @@ void count_launches(int k);
 // while the previous kernel of the stream is still running (hiding the launch gap between the
 // step's dependent kernels, also inside a captured graph). Every kernel launched this way calls
 // pdl_wait (gs_common.cuh) before reading what the kernel before it may write or writing what it
-// may read. After a
-// non-kernel operation (a memset, a copy, an event) the launch is ordered as usual.
+// may read. After a non-kernel operation (a memset, a copy, an event) the launch is ordered as
+// usual.
 template <class... KArgs, class... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                               Args... args) {
