@@ -16,7 +16,7 @@
 // Larger images fall back to emitting the duplicates in depth order and radix-sorting them by
 // tile id in 8-bit passes.
 //
-// Radix pass = histogram (per 2048-item block, 8-bit digit), scan (per digit over blocks),
+// Radix pass = histogram (per 4096-item block, 8-bit digit), scan (per digit over blocks),
 // stable scatter (per warp: 8 rounds of 32 consecutive items ranked with match_any, then the
 // block's items reordered by digit in shared memory and written as coalesced runs).
 #include "gs_common.cuh"
@@ -25,9 +25,9 @@
 namespace gs {
 
 constexpr int kSortThreads = 256;
-constexpr int kSortRounds = 8;                           // rounds of 32 items per warp
-constexpr int kSortItems = kSortThreads * kSortRounds;  // 2048 items per block
-constexpr int kWarpItems = 32 * kSortRounds;            // 256 items per warp
+constexpr int kSortRounds = 16;                          // rounds of 32 items per warp
+constexpr int kSortItems = kSortThreads * kSortRounds;  // 4096 items per block
+constexpr int kWarpItems = 32 * kSortRounds;            // 512 items per warp
 
 // Number of items of a pass: the host bound n, or the count the previous pass left on the device.
 __device__ __forceinline__ int item_count(int n, const unsigned* n_dev) {
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
 // ---- depth sort: one histogram pass, then one kernel per 8-bit digit (decoupled look-back) -----
 //
 // k_depth_hist4 counts the four 8-bit digits of the depth keys of all Gaussians with radius > 0
-// in one pass. Each k_onesweep pass then ranks its 2048-item block locally (as k_radix_scatter),
+// in one pass. Each k_onesweep pass then ranks its 4096-item block locally (as k_radix_scatter),
 // publishes the block's per-digit counts, and finds the number of items of each digit in all
 // earlier blocks by looking back over their published words: a block's inclusive prefix ends the
 // walk, an aggregate is added and the walk continues. Blocks take their index from a ticket in
@@ -275,10 +275,11 @@ __global__ void __launch_bounds__(256) k_depth_hist4(const unsigned* __restrict_
 
 // One stable pass of the depth sort over the digit at `shift`. IOTA: the values are the item
 // indices and items with radius 0 are dropped (first pass); later passes take the count of valid
-// items from n_dev (the sum of the digit-0 histogram). The first pass is bounded to 40 registers
-// (six resident blocks per SM); the later ones run over the visible Gaussians only.
+// items from n_dev (the sum of the digit-0 histogram). The first pass is bounded to 85 registers
+// (three resident blocks per SM); the later ones run over the visible Gaussians only (two blocks
+// per SM hold 1.2M of them in one wave).
 template <bool IOTA>
-__global__ void __launch_bounds__(kSortThreads, IOTA ? 6 : 1) k_onesweep(
+__global__ void __launch_bounds__(kSortThreads, IOTA ? 3 : 1) k_onesweep(
     const unsigned* __restrict__ keys_in, const unsigned* __restrict__ vals_in, unsigned* __restrict__ keys_out,
     unsigned* __restrict__ vals_out, int n_bound, const unsigned* __restrict__ ghist4, const int* __restrict__ radius,
     int pass, unsigned* __restrict__ ticket, unsigned long long* __restrict__ status, unsigned* __restrict__ nvis_out,
@@ -1047,8 +1048,8 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
     const size_t sstride = (size_t)w.sweep_blocks * 256;
     const int nb = sort_blocks(n);
     const int hblocks = nb < 4 * 152 ? nb : 4 * 152;
-    // the first pass runs over all N Gaussians: six blocks per SM (its launch bound, and shared memory
-    // preferred over L1) keep its 2048-item blocks in one wave up to 1.87M Gaussians
+    // the first pass runs over all N Gaussians: three blocks per SM (its launch bound, and shared
+    // memory preferred over L1) keep its 4096-item blocks in one wave up to 1.87M Gaussians
     if ((e = cudaFuncSetAttribute(k_onesweep<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                   (int)cudaSharedmemCarveoutMaxShared)))
         return e;

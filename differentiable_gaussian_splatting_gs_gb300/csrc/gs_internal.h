@@ -43,7 +43,7 @@ struct SortWorkspace {
     unsigned* nvis;                    // number of Gaussians with radius > 0 (left by the second depth pass)
     unsigned char* sweep;              // depth sort: digit histograms, tickets, look-back words (zeroed per call)
     size_t sweep_bytes;
-    int sweep_blocks;                  // 2048-item blocks of a depth pass
+    int sweep_blocks;                  // 4096-item blocks of a depth pass
     unsigned *tA, *tB, *vB;            // radix tile pass: keys ping-pong and values, capacity each
     unsigned* table;                   // counting tile pass: chunk x tile counts, then offsets
     uint2* crect;                      // counting tile pass: packed tile rectangle per depth-ordered Gaussian
