@@ -31,8 +31,9 @@ EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_re
            "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static", "gs_adam_step",
            "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim", "gs_preprocess2d",
            "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd", "gs_bin_and_sort_async",
-           "gs_preprocess_bwd_stats")
+           "gs_preprocess_bwd_stats", "gs_selftest_sort_timeout")
 GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
+GS_SELFTEST_SORT_WORKSPACE_BYTES = 128 << 10
 
 
 class gs_camera(C.Structure):
@@ -114,6 +115,8 @@ def load():
         lib.gs_device_error.argtypes = [P]
         lib.gs_version.argtypes = []
         lib.gs_selftest_timeout.argtypes = [C.c_uint32, P]
+        lib.gs_selftest_sort_timeout.argtypes = [P, C.c_size_t, C.c_uint32, P]
+        lib.gs_selftest_sort_timeout.restype = C.c_int
         lib.gs_bin_and_sort_static.argtypes = [pproj, pcam, popt, P, P, I64, C.POINTER(I64), P, P]
         lib.gs_bin_and_sort_static.restype = C.c_int
         lib.gs_bin_and_sort_async.argtypes = [pproj, pcam, popt, P, C.c_size_t, P, P, I64, P, P, P]

@@ -448,7 +448,9 @@ __global__ void __launch_bounds__(256) k_count(int n_bound, const unsigned* __re
     unsigned long long cnt = 0;
     if (i < n) {
         const unsigned g = perm[i];
-        const int r = radius[g];
+        // an index outside the Gaussians (only after a depth pass whose look-back gave up and set
+        // the timeout bit) counts as culled, so that nothing is read out of range
+        const int r = g < (unsigned)n_bound ? radius[g] : 0;
         uint2 packed = make_uint2(0u, 0u);
         if (r > 0) {
             const float4 r0 = rec[3 * (size_t)g];
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(256) k_emit(int n_bound, const unsigned* __res
     int x0 = 0, y0 = 0, w = 1;
     if (i < n) {
         g = perm[i];
-        const int r = radius[g];
+        const int r = g < (unsigned)n_bound ? radius[g] : 0;  // out of range only after a look-back timeout
         if (r > 0) {
             const float4 r0 = rec[3 * (size_t)g];
             const Rect R = tile_rect(r0.x, r0.y, r, tiles_x, tiles_y);
@@ -948,6 +950,43 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
             __syncwarp();
         }
     }
+}
+
+// ---- self-test of the bounded look-back ------------------------------------------------------
+
+// Pass histogram and ticket of the look-back self-test: 8192 items of digit 0, and the ticket
+// counter starting at 1, so that the single block launched takes index 1 and its predecessor,
+// block 0, never exists.
+__global__ void k_selftest_lookback_init(unsigned* __restrict__ ghist4, unsigned* __restrict__ ticket) {
+    if (threadIdx.x == 0) {
+        ghist4[0] = 2u * kSortItems;
+        ticket[0] = 1u;
+    }
+}
+
+// One block of the first depth pass runs as block 1 over items 4096..8191 (all keys 0). Its
+// look-back polls block 0's status words, which nothing writes: each poll finds them empty, and
+// after spin_limit polls the wait gives up and sets the timeout bit. The block then places its
+// items at positions 0..4095 of the output arrays. Workspace layout (106,512 bytes): keys in,
+// keys out, values out (8192 words each), the four pass histograms (1024 words), four tickets,
+// two blocks' status words (512 x 8 bytes).
+cudaError_t selftest_lookback(unsigned char* ws, unsigned spin_limit, unsigned* err, cudaStream_t st) {
+    constexpr int kItems = 2 * kSortItems;
+    unsigned* keys_in = reinterpret_cast<unsigned*>(ws);
+    unsigned* keys_out = keys_in + kItems;
+    unsigned* vals_out = keys_out + kItems;
+    unsigned* ghist4 = vals_out + kItems;
+    unsigned* ticket = ghist4 + 4 * 256;
+    unsigned long long* status = reinterpret_cast<unsigned long long*>(ticket + 4);
+    static_assert((3 * kItems + 4 * 256 + 4) * 4 + 2 * 256 * 8 == kSelftestLookbackBytes, "self-test layout");
+    cudaError_t e = cudaMemsetAsync(ws, 0, kSelftestLookbackBytes, st);
+    if (e) return e;
+    count_launches(2);
+    k_selftest_lookback_init<<<1, 32, 0, st>>>(ghist4, ticket);
+    if ((e = cudaGetLastError())) return e;
+    k_onesweep<true><<<1, kSortThreads, 0, st>>>(keys_in, nullptr, keys_out, vals_out, kItems, ghist4, nullptr, 0,
+                                                 ticket, status, nullptr, spin_limit, err);
+    return cudaGetLastError();
 }
 
 // ---- host orchestration ----------------------------------------------------------------------

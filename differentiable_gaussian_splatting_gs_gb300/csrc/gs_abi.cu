@@ -138,37 +138,38 @@ int check_proj_n(const gs_proj* q) {
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Device address of g_error_word for the current device (looked up once per device).
-unsigned* error_word(int* status) {
-    static unsigned* cache[256] = {};
+// Per-device cache of a device symbol's address. Host threads may look it up concurrently: every
+// entry is an atomic, so two first calls on one device at worst both query the runtime and store
+// the same address.
+template <class T>
+T* symbol_address(std::atomic<T*> (&cache)[256], const void* symbol, const char* what, int* status) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e || dev < 0 || dev >= 256) { *status = cuda_fail(e ? e : cudaErrorInvalidDevice, "cudaGetDevice"); return nullptr; }
-    if (!cache[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_error_word);
-        if (e) { *status = cuda_fail(e, "cudaGetSymbolAddress(error word)"); return nullptr; }
-        cache[dev] = static_cast<unsigned*>(p);
+    T* p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void* q = nullptr;
+        e = cudaGetSymbolAddress(&q, symbol);
+        if (e) { *status = cuda_fail(e, what); return nullptr; }
+        p = static_cast<T*>(q);
+        cache[dev].store(p, std::memory_order_release);
     }
     *status = GS_OK;
-    return cache[dev];
+    return p;
+}
+
+// Device address of g_error_word for the current device (looked up once per device).
+unsigned* error_word(int* status) {
+    static std::atomic<unsigned*> cache[256] = {};
+    return symbol_address(cache, (const void*)&g_error_word, "cudaGetSymbolAddress(error word)", status);
 }
 
 // Device address of g_static_sort_ws for the current device (looked up once per device; in host
 // code the array's name is only a stand-in, so kernels must be given this address).
 unsigned char* static_sort_workspace(int* status) {
-    static unsigned char* cache[256] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e || dev < 0 || dev >= 256) { *status = cuda_fail(e ? e : cudaErrorInvalidDevice, "cudaGetDevice"); return nullptr; }
-    if (!cache[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_sort_ws);
-        if (e) { *status = cuda_fail(e, "cudaGetSymbolAddress(static sort workspace)"); return nullptr; }
-        cache[dev] = static_cast<unsigned char*>(p);
-    }
-    *status = GS_OK;
-    return cache[dev];
+    static std::atomic<unsigned char*> cache[256] = {};
+    return symbol_address(cache, (const void*)g_static_sort_ws, "cudaGetSymbolAddress(static sort workspace)",
+                          status);
 }
 
 }  // namespace
@@ -218,6 +219,21 @@ int gs_selftest_timeout(uint32_t spin_limit, void* stream) {
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     return e ? cuda_fail(e, "gs_selftest_timeout") : GS_OK;
+}
+
+static_assert(kSelftestLookbackBytes <= GS_SELFTEST_SORT_WORKSPACE_BYTES, "self-test workspace too small");
+
+int gs_selftest_sort_timeout(void* workspace, size_t workspace_bytes, uint32_t spin_limit, void* stream) {
+    if (!workspace || !aligned(workspace, 16)) return fail(GS_ERR_ARG, "workspace is NULL or not 16-byte aligned");
+    if (workspace_bytes < GS_SELFTEST_SORT_WORKSPACE_BYTES)
+        return fail(GS_ERR_ARG, "workspace of %zu bytes, need %u", workspace_bytes,
+                    (unsigned)GS_SELFTEST_SORT_WORKSPACE_BYTES);
+    int s;
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaError_t e = selftest_lookback(static_cast<unsigned char*>(workspace), spin_limit ? spin_limit : 1024u, err,
+                                      as_stream(stream));
+    return e ? cuda_fail(e, "gs_selftest_sort_timeout") : GS_OK;
 }
 
 int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* opt, gs_proj* out, void* stream) {

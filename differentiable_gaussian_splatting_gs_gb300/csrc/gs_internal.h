@@ -70,6 +70,10 @@ cudaError_t bin_sort_async(const gs_proj& proj, int tiles_x, int tiles_y, unsign
                            const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
                            unsigned long long* n_dup_dev, unsigned* err, unsigned spin_limit, cudaStream_t st);
 bool counting_path(long long tiles);
+// Self-test of the depth sort's bounded look-back (a predecessor that never publishes); needs
+// kSelftestLookbackBytes of device workspace, 16-byte aligned.
+constexpr size_t kSelftestLookbackBytes = 106512;
+cudaError_t selftest_lookback(unsigned char* ws, unsigned spin_limit, unsigned* err, cudaStream_t st);
 
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
                               cudaStream_t st);

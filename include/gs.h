@@ -338,9 +338,9 @@ int gs_preprocess2d_bwd(const gs_params* p, const gs_camera* cam, const gs_optio
 #define GS_STATIC_SORT_WORKSPACE_BYTES (32u << 20)
 
 /* gs_bin_and_sort without a workspace argument, for callers that cannot allocate device memory:
- * code running where a cudaMalloc is not allowed or not wanted (a real-time loop with a fixed
- * memory budget, a plug-in that only receives buffers from its host; for a region being captured
- * into a CUDA graph use gs_bin_and_sort_async, which also does not synchronise). It computes
+ * a plug-in that only receives its input and output buffers from a host application which owns
+ * all device memory under a fixed budget (it may not call cudaMalloc itself), or a real-time loop
+ * in which an allocation could stall or fail in the middle of a frame. It computes
  * exactly what gs_bin_and_sort computes (same outputs, same
  * errors) but takes its scratch space from a statically sized device array inside this library,
  * GS_STATIC_SORT_WORKSPACE_BYTES (32 MiB), which every GPU that loads the library keeps reserved
@@ -394,6 +394,15 @@ int gs_device_error(void* stream);
  * iterations (0 = 1024). The wait sets the timeout bit of the device error word, so a following
  * gs_device_error() returns GS_ERR_TIMEOUT; the context stays usable. Errors: GS_ERR_CUDA.      */
 int gs_selftest_timeout(uint32_t spin_limit, void* stream);
+
+/* Self-test of the bounded look-back in the depth sort of gs_bin_and_sort: runs one block of a
+ * depth pass whose predecessor block never publishes its counts, so the block's look-back finds
+ * nothing, gives up after `spin_limit` polls (0 = 1024) and sets the timeout bit of the device
+ * error word; a following gs_device_error() returns GS_ERR_TIMEOUT and the context stays usable.
+ * workspace: device buffer of at least GS_SELFTEST_SORT_WORKSPACE_BYTES, 16-byte aligned, owned
+ * by the caller (overwritten). Errors: GS_ERR_ARG (workspace), GS_ERR_CUDA.                     */
+#define GS_SELFTEST_SORT_WORKSPACE_BYTES (128u << 10)
+int gs_selftest_sort_timeout(void* workspace, size_t workspace_bytes, uint32_t spin_limit, void* stream);
 
 /* Number of kernels this library has launched in this process (all devices, all threads). */
 int64_t gs_kernel_launches(void);

@@ -1,9 +1,10 @@
 """The sort entry point that allocates nothing (gs_bin_and_sort_static) against the regular one.
 
-Some callers cannot hand the library a workspace: code inside a region being captured into a
-CUDA graph, where a cudaMalloc is not allowed, or a plug-in that only receives its input and
-output buffers from a host application with a fixed memory budget. gs_bin_and_sort_static serves
-them from a 32 MiB device array inside the library. This file is collected last on purpose: it
+Some callers cannot hand the library a workspace: a plug-in that only receives its input and
+output buffers from a host application which owns all device memory under a fixed budget (the
+plug-in may not call cudaMalloc itself), or a real-time loop in which an allocation could stall or
+fail in the middle of a frame. gs_bin_and_sort_static serves them from a 32 MiB device array
+inside the library. This file is collected last on purpose: it
 calls the static entry point twice in a row (the array keeps the previous call's contents) and
 must give exactly what gs_bin_and_sort gives, whether it runs alone or after the other tests.
 """
