@@ -68,12 +68,13 @@ def train_step(params: dict, cameras, targets, opt, grads: dict, buffers: StepBu
 
 
 def train_step_async(params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
-                     n_dup: torch.Tensor, events=None, stream=None):
+                     n_dup: torch.Tensor, events=None, stream=None, upstream=None):
     """train_step without any host synchronisation: the sort is gs_bin_and_sort_async with a
     fixed capacity, and the views' duplicate counts land in the device tensor n_dup [views]
     (a view whose count exceeds the capacity renders nothing and sets the device check error).
     events: optional per view ((fwd start, fwd end), (bwd start, bwd end)) recorded around the
-    two raster kernels (on the current stream)."""
+    two raster kernels (on the current stream). upstream: optional per-view dL/dimage [3, H, W]
+    tensors supplied by the caller (a loss computed elsewhere); the targets are then unused."""
     image = None
     for v, (cam, target) in enumerate(zip(cameras, targets)):
         ev = events[v] if events is not None else None
@@ -87,7 +88,10 @@ def train_step_async(params: dict, cameras, targets, opt, grads: dict, buffers: 
         api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib), stream=stream)
         if ev is not None:
             ev[0][1].record()
-        torch.sub(image, target, out=dl)
+        if upstream is None:
+            torch.sub(image, target, out=dl)
+        else:
+            dl = upstream[v]
         if ev is not None:
             ev[1][0].record()
         api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=buffers.grad2d,
@@ -132,15 +136,22 @@ class GraphedStep:
     written to, the same tensors at every replay (update them in place between replays)."""
 
     def __init__(self, params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
-                 events=None, surfels: bool = False):
+                 events=None, surfels: bool = False, upstream=None):
         """events: as for train_step_async; to time kernels inside the graph they must be created
         with torch.cuda.Event(enable_timing=True, external=True), which captures them as event
-        record nodes. surfels: capture the surfel pipeline (train_step_surfels_async) instead."""
-        run = train_step_surfels_async if surfels else train_step_async
+        record nodes. surfels: capture the surfel pipeline (train_step_surfels_async) instead.
+        upstream: per-view dL/dimage tensors read at every replay instead of image - target
+        (3D pipeline only)."""
         self.device = buffers.device
         self.cams = [c if isinstance(c, api.gs_camera) else api.make_camera(c) for c in cameras]
         self.n_dup = torch.zeros(len(self.cams), dtype=torch.int64, device=self.device)
         args = (params, self.cams, targets, opt, grads, buffers, capacity, self.n_dup, events)
+        if surfels:
+            assert upstream is None, "upstream gradients are supported by the 3D pipeline only"
+            run = train_step_surfels_async
+        else:
+            def run(*a):
+                return train_step_async(*a, upstream=upstream)
         # one eager run first: buffers, function attributes and device symbols are set up outside the capture
         side = torch.cuda.Stream(self.device)
         side.wait_stream(torch.cuda.current_stream(self.device))

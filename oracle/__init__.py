@@ -10,8 +10,8 @@ and the CUDA library never imports it.
     gs_oracle.cpp  the float64 implementation (3D Gaussians, and surfels of 2D Gaussian splatting)
     optim.py       numpy sparse Adam (the update phase after the backward)
 """
-from ._lib import (bin_and_sort, build, preprocess, preprocess2d, preprocess2d_bwd, preprocess_bwd, quat_to_rotmat,
-                   render, render2d, sh_basis, view_step, view_step2d)
+from ._lib import (MARGINAL, bin_and_sort, build, preprocess, preprocess2d, preprocess2d_bwd, preprocess_bwd,
+                   quat_to_rotmat, render, render2d, sh_basis, view_step, view_step2d)
 
-__all__ = ["bin_and_sort", "build", "preprocess", "preprocess2d", "preprocess2d_bwd", "preprocess_bwd",
+__all__ = ["MARGINAL", "bin_and_sort", "build", "preprocess", "preprocess2d", "preprocess2d_bwd", "preprocess_bwd",
            "quat_to_rotmat", "render", "render2d", "sh_basis", "view_step", "view_step2d"]

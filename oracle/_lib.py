@@ -20,6 +20,12 @@ _lock = threading.Lock()
 _lib = None
 
 
+# Gaussian flags of preprocess(): bit 0 culled; these three mark a Gaussian whose float32 projection
+# may legitimately differ from this oracle's (radius at a ceiling boundary, tile rectangle at a tile
+# edge, projection ill-conditioned in float32)
+MARGINAL = 2 | 4 | 8
+
+
 class OrCamera(C.Structure):
     _fields_ = [("R", C.c_float * 9), ("t", C.c_float * 3), ("fx", C.c_float), ("fy", C.c_float),
                 ("cx", C.c_float), ("cy", C.c_float), ("width", C.c_int32), ("height", C.c_int32),
@@ -56,14 +62,14 @@ def lib():
         if _lib is None:
             _lib = C.CDLL(build())
             P = C.c_void_p
-            _lib.or_preprocess.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 10
+            _lib.or_preprocess.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 11
             _lib.or_preprocess.restype = C.c_int
             _lib.or_bin.argtypes = [C.c_int64, P, P, P, C.c_int32, C.c_int32, P, P, C.c_int64, P]
             _lib.or_bin.restype = C.c_int64
             _lib.or_render.argtypes = ([C.c_int64] + [P] * 6 + [P] + [P] * 8 + [P, C.c_int] +
-                                        [P, C.c_double, C.c_double, P])
+                                        [P, C.c_double, P, C.c_double, P])
             _lib.or_render.restype = C.c_int
-            _lib.or_preprocess_bwd.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 6
+            _lib.or_preprocess_bwd.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 7
             _lib.or_preprocess_bwd.restype = C.c_int
             _lib.or_preprocess2d.argtypes = [C.c_int64] + [P] * 5 + [P, P] + [P] * 6
             _lib.or_preprocess2d.restype = C.c_int
@@ -120,12 +126,12 @@ def preprocess(mean3d, log_scale, quat, opacity_logit, sh, sh_degree, cam, threa
     out = dict(mean2d=np.zeros((n, 2)), conic=np.zeros((n, 3)), opacity=np.zeros(n), rgb=np.zeros((n, 3)),
                depth=np.zeros(n, np.float32), radius=np.zeros(n, np.int32),
                tiles_touched=np.zeros(n, np.uint32), flags=np.zeros(n, np.uint8), cov2d=np.zeros((n, 3)),
-               mean_tol=np.zeros(n))
+               mean_tol=np.zeros(n), conic_tol=np.zeros(n))
     c, o = camera(cam), options(sh_degree, threads=threads, **opt)
     rc = lib().or_preprocess(n, _p(m), _p(ls), _p(q), _p(lg), _p(sh), C.byref(c), C.byref(o),
                              _p(out["mean2d"]), _p(out["conic"]), _p(out["opacity"]), _p(out["rgb"]),
                              _p(out["depth"]), _p(out["radius"]), _p(out["tiles_touched"]),
-                             _p(out["flags"]), _p(out["cov2d"]), _p(out["mean_tol"]))
+                             _p(out["flags"]), _p(out["cov2d"]), _p(out["mean_tol"]), _p(out["conic_tol"]))
     assert rc == 0
     return out
 
@@ -147,10 +153,11 @@ def bin_and_sort(mean2d_f32, depth_f32, radius, width, height, capacity=None):
 
 
 def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threads=0, bg=None, record_tol=None):
-    """record_tol = (mean_tol [N] px, conic_rel, opacity_rel) widens the marginal-decision bands by
-    how much another implementation's records may differ from these (None: same records):
-    means within mean_tol px, the conic's quadratic form within a relative conic_rel, opacities
-    within a relative opacity_rel."""
+    """record_tol = (mean_tol [N] px, conic_rel, opacity_rel, conic_scale_tol [N] or None) widens
+    the marginal-decision bands by how much another implementation's records may differ from
+    these (None: same records): means within mean_tol px, the conic's quadratic form within a
+    relative conic_rel, opacities within a relative opacity_rel, and where conic_scale_tol > 0
+    each conic entry within that fraction of its scale (|A|, |C|, sqrt(A C) for B)."""
     n = int(np.asarray(opacity).shape[0])
     W, H = int(cam.width), int(cam.height)
     m, cn, op, cl = (_c(mean2d, np.float64), _c(conic, np.float64), _c(opacity, np.float64),
@@ -163,12 +170,13 @@ def render(mean2d, conic, opacity, rgb, vals, ranges, cam, dl_dimage=None, threa
     grad = np.zeros((n, 9)) if dl is not None else None
     st = OrRenderStats()
     c = camera(cam, bg)
-    mt, crel, orel = (None, 0.0, 0.0) if record_tol is None else record_tol
+    mt, crel, orel, cst = (None, 0.0, 0.0, None) if record_tol is None else record_tol
     mt = None if mt is None else _c(mt, np.float64)
+    cst = None if cst is None else _c(cst, np.float64)
     rc = lib().or_render(n, _p(m), _p(cn), _p(op), _p(cl), _p(v), _p(rg), C.byref(c), _p(dl),
                          _p(out["image"]), _p(out["t_final"]), _p(out["n_contrib"]), _p(out["n_blended"]),
                          _p(out["pix_flags"]), _p(out["pix_sig"]), _p(grad), C.byref(st), int(threads),
-                         _p(mt), float(crel), float(orel), _p(out["pix_err"]))
+                         _p(mt), float(crel), _p(cst), float(orel), _p(out["pix_err"]))
     assert rc == 0
     out["grad2d"] = grad
     out["stats"] = dict(pairs_evaluated=st.pairs_evaluated, pairs_blended=st.pairs_blended,
@@ -185,11 +193,15 @@ def preprocess_bwd(mean3d, log_scale, quat, opacity_logit, sh, sh_degree, cam, g
     g2 = _c(grad2d, np.float64)
     out = dict(d_mean3d=np.zeros((n, 3)), d_log_scale=np.zeros((n, 3)), d_quat=np.zeros((n, 4)),
                d_opacity_logit=np.zeros(n), d_sh=np.zeros((n, K, 3)))
+    mag = np.zeros((n, 11))
     c, o = camera(cam), options(sh_degree, threads=threads, **opt)
     rc = lib().or_preprocess_bwd(n, _p(m), _p(ls), _p(q), _p(lg), _p(shc), C.byref(c), C.byref(o), _p(g2),
                                  _p(out["d_mean3d"]), _p(out["d_log_scale"]), _p(out["d_quat"]),
-                                 _p(out["d_opacity_logit"]), _p(out["d_sh"]))
+                                 _p(out["d_opacity_logit"]), _p(out["d_sh"]), _p(mag))
     assert rc == 0
+    # magnitudes of the terms each gradient sums (the SH gradients are single terms)
+    out["mag"] = dict(d_mean3d=mag[:, 0:3], d_log_scale=mag[:, 3:6], d_quat=mag[:, 6:10], d_opacity_logit=mag[:, 10],
+                      d_sh=np.abs(out["d_sh"]))
     return out
 
 
@@ -266,7 +278,7 @@ def marginal_mask(pre, fwd, cam):
     rectangle at radius r - 1 (one pixel of radius covers more than the mean's float32 error).
     Returns a bool [H, W] array (True = marginal)."""
     mask = fwd["pix_flags"] != 0
-    flagged = np.nonzero((pre["flags"] & 6) != 0)[0]
+    flagged = np.nonzero((pre["flags"] & MARGINAL) != 0)[0]
     T = ((cam.width + 15) // 16) * ((cam.height + 15) // 16)
     ring = np.zeros(T, bool)
     m32 = pre["mean2d"].astype(np.float32)
@@ -286,24 +298,33 @@ def marginal_mask(pre, fwd, cam):
     return mask
 
 
-def view_step(scene, view=0, dl_dimage=None, with_backward=True, threads=0, mask_marginal=False, **opt):
+def view_step(scene, view=0, dl_dimage=None, with_backward=True, threads=0, mask_marginal=False, pre=None,
+              bins=None, **opt):
     """Whole training step of one view: preprocess, binning and sort, render, and (when
     `with_backward`) the gradient computation and the preprocess backward.
 
     The upstream gradient defaults to dL/dimage = image - target (the squared-error loss
     0.5 |image - target|^2), with the target image of the view; the oracle's own float64 image
     is used, rounded to float32. With `mask_marginal` it is zeroed on `marginal_mask` pixels.
+    `pre` and `bins` = (keys, vals, ranges) may pass in this view's preprocess and binning results
+    computed earlier by this module (they are then not recomputed).
     """
     cam = scene.cameras[view]
-    pre = preprocess(scene.mean3d, scene.log_scale, scene.quat, scene.opacity_logit, scene.sh,
-                     scene.sh_degree, cam, threads=threads, **opt)
+    if pre is None:
+        pre = preprocess(scene.mean3d, scene.log_scale, scene.quat, scene.opacity_logit, scene.sh,
+                         scene.sh_degree, cam, threads=threads, **opt)
     m32 = pre["mean2d"].astype(np.float32)
-    keys, vals, ranges = bin_and_sort(m32, pre["depth"], pre["radius"], cam.width, cam.height,
-                                      capacity=int(pre["tiles_touched"].sum(dtype=np.int64)))
+    if bins is None:
+        bins = bin_and_sort(m32, pre["depth"], pre["radius"], cam.width, cam.height,
+                            capacity=int(pre["tiles_touched"].sum(dtype=np.int64)))
+    keys, vals, ranges = bins
     # In mask_marginal mode the decision bands also cover a float32 preprocess of the same scene
     # (means within mean_tol, the conic's quadratic form within 1e-5 and opacities within 1e-6
-    # relative: several times what a float32 preprocess was measured to differ by).
-    rt = (pre["mean_tol"], 1e-5, 1e-6) if mask_marginal else None
+    # relative: several times what a float32 preprocess was measured to differ by; and for the
+    # Gaussians whose projection is ill-conditioned in float32 (flag 8), each conic entry within
+    # the oracle's conditioning bound conic_tol of its scale).
+    ill = (pre["flags"] & 8) != 0
+    rt = (pre["mean_tol"], 1e-5, 1e-6, np.where(ill, pre["conic_tol"], 0.0)) if mask_marginal else None
     fwd = render(pre["mean2d"], pre["conic"], pre["opacity"], pre["rgb"], vals, ranges, cam, threads=threads,
                  record_tol=rt)
     out = dict(pre=pre, keys=keys, vals=vals, ranges=ranges, fwd=fwd)

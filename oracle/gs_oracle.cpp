@@ -24,7 +24,8 @@
 // an explicit bound on the float32 error; the tests compare everything else exactly.
 //
 // Parallelism: OpenMP over Gaussians (preprocess) and over tiles (render). Every per-pixel and
-// per-Gaussian computation is sequential and in the order the method states.
+// per-Gaussian computation is sequential and in the order the method states; per-Gaussian gradient
+// sums are formed per tile and added in tile order, so results do not depend on the thread count.
 
 #include <algorithm>
 #include <cmath>
@@ -58,9 +59,10 @@ struct OrRenderStats {
     int64_t pairs_evaluated;   // (pixel, list entry) pairs visited before termination
     int64_t pairs_blended;     // pairs that were alpha-blended
     int64_t marginal_pixels;   // pixels with at least one marginal decision
-    int64_t warp_gauss_active; // (tile, 8x4 pixel block, Gaussian) triples with >= 1 blending pixel
+    int64_t warp_gauss_active; // (tile, 8x8 pixel block, Gaussian) triples with >= 1 blending pixel
     int64_t tile_gauss_active; // (tile, Gaussian) pairs with >= 1 blending pixel
-    int64_t lane_hist[33];     // histogram of blending pixels per active (8x4 block, Gaussian)
+    int64_t lane_hist[33];     // histogram over active (8x8 block, Gaussian) of the lanes (pixel pairs
+                               // (x, y), (x, y + 4) of the block) with a blending pixel
 };
 
 }  // extern "C"
@@ -320,6 +322,78 @@ void project(const S mu[3], const S ls[3], const S q[4], const S& logit, const d
     }
 }
 
+// Bound on the relative error of a float32 evaluation of the conic of one Gaussian (first-order
+// rounding error analysis). The 2D covariance is S = K K^T + lowpass I with K = T Rq diag(s), T = J W
+// the projection Jacobian times the camera rotation. A float32 evaluation of each entry
+// K_rk = s_k sum_i T_ri Rq_ik carries an absolute error of at most about 24 eps s_k sum_i |T_ri|
+// (eps = 2^-24: the roundings of the normalised quaternion and the rotation entries, of exp, of J
+// and T, of the products and the sum). The conic C = S^-1 then moves by
+// dC = -C (dK K^T + K dK^T) C to first order; summing the magnitude of each entry's contribution
+// bounds the error of the conic of the float32 K, and 8 eps of each entry's scale covers the
+// float32 evaluation of the conic from K. When a Gaussian's long axis points nearly along the
+// viewing ray, K is a small difference of large terms and the bound is large: the projection is
+// ill-conditioned in float32. Returns (conic_rel, lambda_rel): the conic entries' error relative
+// to their scale (|A|, |C|, sqrt(A C) for B) and the relative error of the largest eigenvalue of S.
+std::pair<double, double> projection_rel_error(const double mu[3], const double ls[3], const double q[4],
+                                               const OrCamera& cam, const OrOptions& opt,
+                                               const Projected<double>& P) {
+    const double eps = std::ldexp(1.0, -24);
+    double p[3];
+    for (int i = 0; i < 3; ++i) p[i] = (double)cam.R[3 * i] * mu[0] + (double)cam.R[3 * i + 1] * mu[1] +
+                                       (double)cam.R[3 * i + 2] * mu[2] + (double)cam.t[i];
+    const double qn = std::sqrt(q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3]);
+    const double qu[4] = {q[0] / qn, q[1] / qn, q[2] / qn, q[3] / qn};
+    double Rq[9];
+    quat_to_rotmat<double>(qu, Rq);
+    double u = p[0] / p[2], v = p[1] / p[2];
+    if (opt.jacobian_clamp > 0.0) {
+        const double limx = opt.jacobian_clamp * (0.5 * cam.width / (double)cam.fx);
+        const double limy = opt.jacobian_clamp * (0.5 * cam.height / (double)cam.fy);
+        u = std::max(-limx, std::min(limx, u));
+        v = std::max(-limy, std::min(limy, v));
+    }
+    const double J[2][3] = {{cam.fx / p[2], 0.0, -cam.fx * u / p[2]}, {0.0, cam.fy / p[2], -cam.fy * v / p[2]}};
+    double T[2][3], K[2][3], E[2][3];
+    for (int r = 0; r < 2; ++r)
+        for (int j = 0; j < 3; ++j) {
+            T[r][j] = 0.0;
+            for (int k = 0; k < 3; ++k) T[r][j] += J[r][k] * (double)cam.R[3 * k + j];
+        }
+    for (int r = 0; r < 2; ++r)
+        for (int k = 0; k < 3; ++k) {
+            const double sk = std::exp(ls[k]);
+            double val = 0.0, mag = 0.0;
+            for (int i = 0; i < 3; ++i) {
+                val += T[r][i] * Rq[3 * i + k];
+                mag += std::fabs(T[r][i]);
+            }
+            K[r][k] = sk * val;
+            E[r][k] = 24.0 * eps * sk * mag;
+        }
+    const double Cm[2][2] = {{P.conic[0], P.conic[1]}, {P.conic[1], P.conic[2]}};
+    double bound[2][2] = {{0.0, 0.0}, {0.0, 0.0}}, dlam = 0.0;
+    for (int r = 0; r < 2; ++r)
+        for (int k = 0; k < 3; ++k) {
+            // dS / dK_rk = e_r K_k^T + K_k e_r^T, K_k the k-th column of K
+            double D[2][2];
+            for (int i = 0; i < 2; ++i)
+                for (int j = 0; j < 2; ++j) D[i][j] = (i == r ? K[j][k] : 0.0) + (j == r ? K[i][k] : 0.0);
+            for (int i = 0; i < 2; ++i)
+                for (int j = 0; j < 2; ++j) {
+                    double x = 0.0;
+                    for (int a = 0; a < 2; ++a)
+                        for (int b = 0; b < 2; ++b) x += Cm[i][a] * D[a][b] * Cm[b][j];
+                    bound[i][j] += std::fabs(x) * E[r][k];
+                }
+            dlam += 2.0 * std::sqrt(K[0][k] * K[0][k] + K[1][k] * K[1][k]) * E[r][k];
+        }
+    const double A = P.conic[0], C = P.conic[2];
+    const double conic_rel = std::max(std::max(bound[0][0] / std::fabs(A), bound[1][1] / std::fabs(C)),
+                                      bound[0][1] / std::sqrt(A * C)) + 8.0 * eps;
+    const double lambda_rel = dlam / P.lambda_max + 8.0 * eps;
+    return {conic_rel, lambda_rel};
+}
+
 int n_threads(int t) {
 #ifdef _OPENMP
     return t > 0 ? t : omp_get_max_threads();
@@ -327,6 +401,49 @@ int n_threads(int t) {
     (void)t;
     return 1;
 #endif
+}
+
+// Per-Gaussian gradient sums in a fixed order. The render backward keeps, for every entry of the
+// sorted list (one (tile, Gaussian) pair), that entry's partial sum over the tile's pixels; the
+// partials are then added into each Gaussian's total in list order, which is tile order. The
+// result therefore does not depend on the number of threads or on how tiles were scheduled.
+// Tiles are processed in groups of consecutive tiles whose lists hold at most kGroupEntries
+// entries together (a longer list forms a group of its own), to bound the memory of the partials.
+constexpr int64_t kGroupEntries = int64_t(1) << 23;
+
+struct TileGroup { int64_t t0, t1, p0, p1; };  // tiles [t0, t1), list positions [p0, p1)
+
+std::vector<TileGroup> tile_groups(const uint32_t* ranges, int64_t T) {
+    std::vector<TileGroup> out;
+    int64_t t = 0;
+    while (t < T) {
+        TileGroup g{t, t, -1, -1};
+        int64_t held = 0;
+        for (; g.t1 < T; ++g.t1) {
+            const int64_t s = ranges[2 * g.t1], e = ranges[2 * g.t1 + 1];
+            const int64_t len = e > s ? e - s : 0;
+            if (g.t1 > g.t0 && held + len > kGroupEntries) break;
+            held += len;
+            if (len > 0) {
+                if (g.p0 < 0) g.p0 = s;
+                g.p1 = e;
+            }
+        }
+        if (g.p0 < 0) g.p0 = g.p1 = 0;
+        out.push_back(g);
+        t = g.t1;
+    }
+    return out;
+}
+
+// out[vals[pos] * out_stride + j] += part[(pos - p0) * stride + j] for pos = p0 .. p1 - 1 in that
+// order, j < ncomp. Components are independent sums, so they run on separate threads.
+void add_partials_in_list_order(const std::vector<double>& part, int stride, int ncomp, const uint32_t* vals,
+                                int64_t p0, int64_t p1, double* out, int out_stride, int threads) {
+#pragma omp parallel for schedule(static) num_threads(std::min(ncomp, n_threads(threads)))
+    for (int j = 0; j < ncomp; ++j)
+        for (int64_t pos = p0; pos < p1; ++pos)
+            out[(size_t)vals[pos] * out_stride + j] += part[(size_t)(pos - p0) * stride + j];
 }
 
 }  // namespace
@@ -345,11 +462,14 @@ void or_quat_to_rotmat(const double* q, double* R) {
     quat_to_rotmat<double>(qu, R);
 }
 
-// flags: bit0 culled, bit1 radius marginal, bit2 tile-rectangle marginal.
+// flags: bit0 culled, bit1 radius marginal, bit2 tile-rectangle marginal, bit3 projection
+// ill-conditioned in float32 (conic_tol above 1e-4). conic_tol (may be NULL): the bound of
+// projection_rel_error on the conic's relative float32 error.
 int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, const double* quat,
                   const double* logit, const double* sh, const OrCamera* cam, const OrOptions* opt,
                   double* mean2d, double* conic, double* opacity, double* rgb, float* depth,
-                  int32_t* radius, uint32_t* tiles_touched, uint8_t* flags, double* cov2d, double* mean_tol) {
+                  int32_t* radius, uint32_t* tiles_touched, uint8_t* flags, double* cov2d, double* mean_tol,
+                  double* conic_tol) {
     if (n < 0 || !cam || !opt) return -1;
     const int deg = opt->sh_degree, K = (deg + 1) * (deg + 1);
     const int tiles_x = (cam->width + kTile - 1) / kTile, tiles_y = (cam->height + kTile - 1) / kTile;
@@ -364,10 +484,15 @@ int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, cons
         int r = 0;
         uint32_t tt = 0;
         if (!P.culled && !(std::ceil(3.0 * std::sqrt(P.lambda_max)) < 16777216.0)) P.culled = true;  // radius >= 2^24 px
+        double ctol = 0.0;
         if (!P.culled) {
+            const auto rel = projection_rel_error(mu, ls, q, *cam, *opt, P);
+            ctol = rel.first;
+            if (ctol > 1e-4) f |= 8;
             double s = 3.0 * std::sqrt(P.lambda_max);
             r = (int)std::ceil(s);
-            if (std::fabs(s - std::nearbyint(s)) < 1e-5 * s) f |= 2;
+            // 3 sqrt(lambda) carries half of lambda's relative error
+            if (std::fabs(s - std::nearbyint(s)) < std::max(1e-5, rel.second) * s) f |= 2;
             Rect R = tile_rect((float)P.mean2d[0], (float)P.mean2d[1], r, tiles_x, tiles_y);
             if (R.marginal) f |= 4;
             if (R.empty) P.culled = true;
@@ -385,6 +510,7 @@ int or_preprocess(int64_t n, const double* mean3d, const double* log_scale, cons
             if (cov2d) cov2d[3 * g + i] = P.culled ? 0.0 : P.cov2d[i];
         }
         opacity[g] = P.culled ? 0.0 : P.opacity;
+        if (conic_tol) conic_tol[g] = P.culled ? 0.0 : ctol;
         if (mean_tol) {
             // Bound on how far a float32 evaluation of the projected mean may lie from this one:
             // 2^-22 (4 units in the last place) of the magnitudes it is computed from.
@@ -465,7 +591,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
               const float* dl_dimage, double* image, double* t_final, uint32_t* n_contrib,
               uint32_t* n_blended, uint8_t* pix_flags, uint64_t* pix_sig, double* grad2d,
               OrRenderStats* stats, int threads, const double* mean_tol, double conic_rel,
-              double opacity_rel, double* pix_err) {
+              const double* conic_scale_tol, double opacity_rel, double* pix_err) {
     (void)n;
     const int W = cam->width, H = cam->height;
     const int tiles_x = (W + kTile - 1) / kTile, tiles_y = (H + kTile - 1) / kTile;
@@ -473,159 +599,174 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
     const double alpha_min = (double)(1.0f / 255.0f);
     const double t_min = (double)1e-4f;
     const double eps32 = std::ldexp(1.0, -24);
+    const double clamp_gap = std::fabs((double)0.99f - 0.99) / (1.0 - 0.99);
     if (grad2d) std::memset(grad2d, 0, sizeof(double) * 9 * (size_t)n);
     OrRenderStats st{};
+    std::vector<double> part;  // per list entry: its gradient partial sum over the tile's pixels
 
+    for (const TileGroup& grp : tile_groups(ranges, T)) {
+        if (grad2d) part.assign((size_t)(grp.p1 - grp.p0) * 9, 0.0);
 #pragma omp parallel num_threads(n_threads(threads))
-    {
-        OrRenderStats ls{};
-        struct Blend { int64_t pos; uint32_t g; double alpha, T, G, dx, dy; bool clamped; };
-        std::vector<Blend> bl;
-        std::vector<double> acc;       // per-tile gradient accumulator, by list position
-        std::vector<uint8_t> wcount;   // per-tile [8 blocks of 8x4 pixels][len] blending-pixel counts
-#pragma omp for schedule(dynamic, 4)
-        for (int64_t tile = 0; tile < T; ++tile) {
-            const int tx = (int)(tile % tiles_x), ty = (int)(tile / tiles_x);
-            const int64_t s = ranges[2 * tile], e = ranges[2 * tile + 1];
-            const int64_t len = e - s;
-            if (grad2d) acc.assign((size_t)len * 9, 0.0);
-            wcount.assign((size_t)len * 8, 0);
-            for (int ly = 0; ly < kTile; ++ly)
-                for (int lx = 0; lx < kTile; ++lx) {
-                    const int px = tx * kTile + lx, py = ty * kTile + ly;
-                    if (px >= W || py >= H) continue;
-                    const double cxp = px + 0.5, cyp = py + 0.5;
-                    double Tr = 1.0, col[3] = {0.0, 0.0, 0.0};
-                    double eT = 0.0;  // bound on the relative float32 error of T
-                    double eC = 0.0;  // bound on the colour error propagated from the alpha bounds
-                    uint32_t contrib = 0, nbl = 0;
-                    uint8_t pf = 0;
-                    uint64_t sig = 1469598103934665603ull;  // FNV-1a over (position, clamped) of blended entries
-                    bl.clear();
-                    for (int64_t pos = s; pos < e; ++pos) {
-                        const uint32_t g = vals[pos];
-                        ls.pairs_evaluated++;
-                        const double dx = mean2d[2 * g] - cxp, dy = mean2d[2 * g + 1] - cyp;
-                        const double A = conic[3 * g], B = conic[3 * g + 1], C = conic[3 * g + 2];
-                        // a record whose conic is not positive definite is not a Gaussian: never blended
-                        if (!(A > 0.0) || !(A * C - B * B > 0.0)) continue;
-                        const double power = -0.5 * (A * dx * dx + C * dy * dy) - B * dx * dy;
-                        // Bound on the float32 error of power when it is evaluated as
-                        // -(A u^2 + D dy^2)/2 with u = dx + (B/A) dy, D = (A C - B^2)/A (terms >= 0): u carries
-                        // eps (|u| + |B/A dy|), A u^2 and D dy^2 a few eps each; 4e-7 is about 7 eps.
-                        const double ur = B / A * dy, u = dx + ur, D = (A * C - B * B) / A;
-                        const double ep = 4e-7 * (A * std::fabs(u) * (std::fabs(u) + std::fabs(ur)) + A * u * u +
-                                                  2.0 * D * dy * dy) + 1e-7;
-                        if (std::fabs(power) <= ep) pf |= 4;
-                        if (power > 0.0) continue;
-                        // uncertainty of power when the records themselves may differ from these
-                        // (a float32 preprocess): the mean by mean_tol px, the conic's quadratic form by a
-                        // relative conic_rel plus the rounding of its three float32 entries (4e-7 of
-                        // the term magnitudes; for elongated Gaussians this dominates along the long
-                        // axis), the opacity by a relative opacity_rel
-                        double ein = opacity_rel + conic_rel * std::fabs(power);
-                        if (conic_rel > 0.0)
-                            ein += 4e-7 * (0.5 * (std::fabs(A) * dx * dx + std::fabs(C) * dy * dy) + std::fabs(B * dx * dy));
-                        if (mean_tol)
-                            ein += mean_tol[g] * (std::fabs(A * dx + B * dy) + std::fabs(B * dx + C * dy));
-                        const double G = std::exp(power);
-                        const double oG = opacity[g] * G;
-                        const bool clamped = oG > 0.99;
-                        const double alpha = clamped ? 0.99 : oG;
-                        const double ea = ep + 1e-6 + ein;  // relative bound on alpha (exp and inputs included)
-                        if (!clamped && std::fabs(std::log(alpha / alpha_min)) < ea) pf |= 1;
-                        if (alpha < alpha_min) continue;
-                        const double test_T = Tr * (1.0 - alpha);
-                        const double eT_next = eT + (clamped ? 0.0 : ea * alpha / (1.0 - alpha)) + 2.0 * eps32;
-                        if (std::fabs(test_T / t_min - 1.0) < 2.0 * eT_next + 1e-6) pf |= 2;
-                        if (test_T < t_min) break;
-                        for (int ch = 0; ch < 3; ++ch) col[ch] += rgb[3 * g + ch] * alpha * Tr;
-                        {
-                            // |dC/dalpha_i| <= T_i (|c_i| + max colour behind); the colour behind is bounded
-                            // by the largest colour or background value
-                            double cm = 0.0;
-                            for (int ch = 0; ch < 3; ++ch)
-                                cm = std::max(cm, std::max(std::fabs(rgb[3 * g + ch]), std::fabs((double)cam->bg[ch])));
-                            eC += 2.0 * cm * (clamped ? 0.0 : ea) * alpha * Tr;
-                        }
-                        bl.push_back({pos, g, alpha, Tr, G, dx, dy, clamped});
-                        sig = (sig ^ (uint64_t)(2 * (pos - s) + (clamped ? 1 : 0))) * 1099511628211ull;
-                        Tr = test_T;
-                        eT = eT_next;
-                        contrib = (uint32_t)(pos - s + 1);
-                        nbl++;
-                        ls.pairs_blended++;
-                        wcount[(size_t)((ly / 4) * 2 + lx / 8) * len + (pos - s)]++;
-                    }
-                    const int64_t pix = (int64_t)py * W + px;
-                    for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
-                    t_final[pix] = Tr;
-                    n_contrib[pix] = contrib;
-                    if (n_blended) n_blended[pix] = nbl;
-                    if (pix_flags) pix_flags[pix] = pf;
-                    if (pix_sig) pix_sig[pix] = sig;
-                    if (pix_err) {
-                        double bm = 0.0;
-                        for (int ch = 0; ch < 3; ++ch) bm = std::max(bm, std::fabs((double)cam->bg[ch]));
-                        pix_err[pix] = eC + Tr * eT * bm;
-                    }
-                    if (pf) ls.marginal_pixels++;
-                    if (!grad2d) continue;
-                    double gpix[3];
-                    for (int ch = 0; ch < 3; ++ch) gpix[ch] = dl_dimage[(int64_t)ch * W * H + pix];
-                    double S[3];
-                    for (int ch = 0; ch < 3; ++ch) S[ch] = Tr * cam->bg[ch];
-                    for (int64_t k = (int64_t)bl.size() - 1; k >= 0; --k) {
-                        const Blend& b = bl[k];
-                        const double* c = rgb + 3 * b.g;
-                        double* a = &acc[(size_t)(b.pos - s) * 9];
-                        double dalpha = 0.0;
-                        for (int ch = 0; ch < 3; ++ch) {
-                            a[6 + ch] += b.alpha * b.T * gpix[ch];
-                            dalpha += gpix[ch] * (c[ch] * b.T - S[ch] / (1.0 - b.alpha));
-                        }
-                        for (int ch = 0; ch < 3; ++ch) S[ch] += c[ch] * b.alpha * b.T;
-                        if (b.clamped) continue;
-                        const double o = opacity[b.g];
-                        const double dpower = o * b.G * dalpha;
-                        const double A = conic[3 * b.g], B = conic[3 * b.g + 1], C = conic[3 * b.g + 2];
-                        a[0] += -(A * b.dx + B * b.dy) * dpower;
-                        a[1] += -(B * b.dx + C * b.dy) * dpower;
-                        a[2] += -0.5 * b.dx * b.dx * dpower;
-                        a[3] += -b.dx * b.dy * dpower;
-                        a[4] += -0.5 * b.dy * b.dy * dpower;
-                        a[5] += b.G * dalpha;
-                    }
-                }
-            for (int64_t k = 0; k < len; ++k) {
-                bool any = false;
-                for (int w = 0; w < 8; ++w) {
-                    uint8_t c = wcount[(size_t)w * len + k];
-                    if (c) { ls.warp_gauss_active++; ls.lane_hist[c]++; any = true; }
-                }
-                if (any) ls.tile_gauss_active++;
-            }
-            if (grad2d)
-                for (int64_t k = 0; k < len; ++k) {
-                    const uint32_t g = vals[s + k];
-                    for (int j = 0; j < 9; ++j) {
-                        double v = acc[(size_t)k * 9 + j];
-                        if (v != 0.0) {
-#pragma omp atomic
-                            grad2d[9 * (size_t)g + j] += v;
-                        }
-                    }
-                }
-        }
-#pragma omp critical
         {
-            st.pairs_evaluated += ls.pairs_evaluated;
-            st.pairs_blended += ls.pairs_blended;
-            st.marginal_pixels += ls.marginal_pixels;
-            st.warp_gauss_active += ls.warp_gauss_active;
-            st.tile_gauss_active += ls.tile_gauss_active;
-            for (int i = 0; i < 33; ++i) st.lane_hist[i] += ls.lane_hist[i];
+            OrRenderStats ls{};
+            struct Blend { int64_t pos; uint32_t g; double alpha, T, G, dx, dy; bool clamped; };
+            std::vector<Blend> bl;
+            // per tile [4 warps][len]: which lanes have a blending pixel. A warp covers an 8x8 block of
+            // the tile and its lane l the two pixels (l % 8, l / 8) and (l % 8, l / 8 + 4) of it
+            std::vector<uint32_t> wmask;
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t tile = grp.t0; tile < grp.t1; ++tile) {
+                const int tx = (int)(tile % tiles_x), ty = (int)(tile / tiles_x);
+                const int64_t s = ranges[2 * tile], e = ranges[2 * tile + 1];
+                const int64_t len = e - s;
+                // this tile's entries in the group's partials (positions s .. e - 1)
+                double* acc = (grad2d && len > 0) ? part.data() + (size_t)(s - grp.p0) * 9 : nullptr;
+                wmask.assign((size_t)len * 4, 0u);
+                for (int ly = 0; ly < kTile; ++ly)
+                    for (int lx = 0; lx < kTile; ++lx) {
+                        const int px = tx * kTile + lx, py = ty * kTile + ly;
+                        if (px >= W || py >= H) continue;
+                        const double cxp = px + 0.5, cyp = py + 0.5;
+                        double Tr = 1.0, col[3] = {0.0, 0.0, 0.0};
+                        double eT = 0.0;  // bound on the relative float32 error of T
+                        double eC = 0.0;  // bound on the colour error propagated from the alpha bounds
+                        uint32_t contrib = 0, nbl = 0;
+                        uint8_t pf = 0;
+                        uint64_t sig = 1469598103934665603ull;  // FNV-1a over (position, clamped) of blended entries
+                        bl.clear();
+                        for (int64_t pos = s; pos < e; ++pos) {
+                            const uint32_t g = vals[pos];
+                            ls.pairs_evaluated++;
+                            const double dx = mean2d[2 * g] - cxp, dy = mean2d[2 * g + 1] - cyp;
+                            const double A = conic[3 * g], B = conic[3 * g + 1], C = conic[3 * g + 2];
+                            // a record whose conic is not positive definite is not a Gaussian: never blended
+                            if (!(A > 0.0) || !(A * C - B * B > 0.0)) continue;
+                            const double power = -0.5 * (A * dx * dx + C * dy * dy) - B * dx * dy;
+                            // Bound on the float32 error of power when it is evaluated as
+                            // -(A u^2 + D dy^2)/2 with u = dx + (B/A) dy, D = (A C - B^2)/A (terms >= 0): u carries
+                            // eps (|u| + |B/A dy|), A u^2 and D dy^2 a few eps each; 4e-7 is about 7 eps.
+                            const double ur = B / A * dy, u = dx + ur, D = (A * C - B * B) / A;
+                            const double ep = 4e-7 * (A * std::fabs(u) * (std::fabs(u) + std::fabs(ur)) + A * u * u +
+                                                      2.0 * D * dy * dy) + 1e-7;
+                            if (std::fabs(power) <= ep) pf |= 4;
+                            if (power > 0.0) continue;
+                            // uncertainty of power when the records themselves may differ from these
+                            // (a float32 preprocess): the mean by mean_tol px; the conic's quadratic form by
+                            // a relative conic_rel plus the rounding of its three float32 entries (4e-7 of the
+                            // term magnitudes; for elongated Gaussians this dominates along the long axis);
+                            // for a Gaussian with a conditioning bound conic_scale_tol (its conic entries
+                            // within that fraction of their scale |A|, |C|, sqrt(A C)), the form moves by at
+                            // most that times (sqrt(A) |dx| + sqrt(C) |dy|)^2; the opacity by opacity_rel
+                            double ein = opacity_rel + conic_rel * std::fabs(power);
+                            if (conic_rel > 0.0)
+                                ein += 4e-7 * (0.5 * (std::fabs(A) * dx * dx + std::fabs(C) * dy * dy) + std::fabs(B * dx * dy));
+                            if (conic_scale_tol && conic_scale_tol[g] > 0.0) {
+                                const double m = std::sqrt(A) * std::fabs(dx) + std::sqrt(std::fabs(C)) * std::fabs(dy);
+                                ein += conic_scale_tol[g] * 0.5 * m * m;
+                            }
+                            if (mean_tol)
+                                ein += mean_tol[g] * (std::fabs(A * dx + B * dy) + std::fabs(B * dx + C * dy));
+                            const double G = std::exp(power);
+                            const double oG = opacity[g] * G;
+                            const bool clamped = oG > 0.99;
+                            const double alpha = clamped ? 0.99 : oG;
+                            // relative bound on alpha: the power's bound, a float32 exponential (a hardware
+                            // approximation of 2^x within 2 units in the last place) and the rounding of
+                            // opacity x G, 5e-7 together, and the inputs' bound
+                            const double ea = ep + 5e-7 + ein;
+                            if (!clamped && std::fabs(std::log(alpha / alpha_min)) < ea) pf |= 1;
+                            if (alpha < alpha_min) continue;
+                            const double test_T = Tr * (1.0 - alpha);
+                            // relative bound on T (1 - alpha): 1 - alpha carries alpha's bound times
+                            // alpha / (1 - alpha); a clamped alpha is the float32 value of 0.99 on the
+                            // float32 side, whose 1 - alpha differs from 0.01 by clamp_gap; two roundings
+                            const double eT_next = eT + (clamped ? clamp_gap : ea * alpha / (1.0 - alpha)) + 2.0 * eps32;
+                            if (std::fabs(test_T / t_min - 1.0) < 2.0 * eT_next + 4.0 * eps32) pf |= 2;
+                            if (test_T < t_min) break;
+                            for (int ch = 0; ch < 3; ++ch) col[ch] += rgb[3 * g + ch] * alpha * Tr;
+                            {
+                                // |dC/dalpha_i| <= T_i (|c_i| + max colour behind); the colour behind is bounded
+                                // by the largest colour or background value
+                                double cm = 0.0;
+                                for (int ch = 0; ch < 3; ++ch)
+                                    cm = std::max(cm, std::max(std::fabs(rgb[3 * g + ch]), std::fabs((double)cam->bg[ch])));
+                                eC += 2.0 * cm * (clamped ? 0.0 : ea) * alpha * Tr;
+                            }
+                            bl.push_back({pos, g, alpha, Tr, G, dx, dy, clamped});
+                            sig = (sig ^ (uint64_t)(2 * (pos - s) + (clamped ? 1 : 0))) * 1099511628211ull;
+                            Tr = test_T;
+                            eT = eT_next;
+                            contrib = (uint32_t)(pos - s + 1);
+                            nbl++;
+                            ls.pairs_blended++;
+                            wmask[(size_t)((ly / 8) * 2 + lx / 8) * len + (pos - s)] |= 1u << ((lx % 8) + 8 * (ly % 4));
+                        }
+                        const int64_t pix = (int64_t)py * W + px;
+                        for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
+                        t_final[pix] = Tr;
+                        n_contrib[pix] = contrib;
+                        if (n_blended) n_blended[pix] = nbl;
+                        if (pix_flags) pix_flags[pix] = pf;
+                        if (pix_sig) pix_sig[pix] = sig;
+                        if (pix_err) {
+                            double bm = 0.0;
+                            for (int ch = 0; ch < 3; ++ch) bm = std::max(bm, std::fabs((double)cam->bg[ch]));
+                            pix_err[pix] = eC + Tr * eT * bm;
+                        }
+                        if (pf) ls.marginal_pixels++;
+                        if (!grad2d) continue;
+                        double gpix[3];
+                        for (int ch = 0; ch < 3; ++ch) gpix[ch] = dl_dimage[(int64_t)ch * W * H + pix];
+                        double S[3];
+                        for (int ch = 0; ch < 3; ++ch) S[ch] = Tr * cam->bg[ch];
+                        for (int64_t k = (int64_t)bl.size() - 1; k >= 0; --k) {
+                            const Blend& b = bl[k];
+                            const double* c = rgb + 3 * b.g;
+                            double* a = acc + (size_t)(b.pos - s) * 9;
+                            double dalpha = 0.0;
+                            for (int ch = 0; ch < 3; ++ch) {
+                                a[6 + ch] += b.alpha * b.T * gpix[ch];
+                                dalpha += gpix[ch] * (c[ch] * b.T - S[ch] / (1.0 - b.alpha));
+                            }
+                            for (int ch = 0; ch < 3; ++ch) S[ch] += c[ch] * b.alpha * b.T;
+                            if (b.clamped) continue;
+                            const double o = opacity[b.g];
+                            const double dpower = o * b.G * dalpha;
+                            const double A = conic[3 * b.g], B = conic[3 * b.g + 1], C = conic[3 * b.g + 2];
+                            a[0] += -(A * b.dx + B * b.dy) * dpower;
+                            a[1] += -(B * b.dx + C * b.dy) * dpower;
+                            a[2] += -0.5 * b.dx * b.dx * dpower;
+                            a[3] += -b.dx * b.dy * dpower;
+                            a[4] += -0.5 * b.dy * b.dy * dpower;
+                            a[5] += b.G * dalpha;
+                        }
+                    }
+                for (int64_t k = 0; k < len; ++k) {
+                    bool any = false;
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t m = wmask[(size_t)w * len + k];
+                        if (m) {
+                            int c = 0;
+                            for (; m; m &= m - 1) ++c;
+                            ls.warp_gauss_active++;
+                            ls.lane_hist[c]++;
+                            any = true;
+                        }
+                    }
+                    if (any) ls.tile_gauss_active++;
+                }
+            }
+#pragma omp critical
+            {
+                st.pairs_evaluated += ls.pairs_evaluated;
+                st.pairs_blended += ls.pairs_blended;
+                st.marginal_pixels += ls.marginal_pixels;
+                st.warp_gauss_active += ls.warp_gauss_active;
+                st.tile_gauss_active += ls.tile_gauss_active;
+                for (int i = 0; i < 33; ++i) st.lane_hist[i] += ls.lane_hist[i];
+            }
         }
+        if (grad2d) add_partials_in_list_order(part, 9, 9, vals, grp.p0, grp.p1, grad2d, 9, threads);
     }
     if (stats) *stats = st;
     return 0;
@@ -636,10 +777,16 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
 // Gaussian. The Jacobian of the per-Gaussian preprocessing is taken by running project() on dual
 // numbers in the 11 non-SH parameters; SH coefficients enter the colour linearly, so
 // dL/dsh[k][ch] = Y_k dL/drgb_ch where the colour was not clamped. Culled Gaussians get zeros.
+//
+// grad_mag (may be NULL) [n][11]: for each of the 11 non-SH parameters (mean3d, log_scale, quat,
+// logit) the sum of the magnitudes of the terms its gradient adds up, sum_o |dL/dout_o d out_o/dp|.
+// Where it is much larger than the gradient itself, the chain rule cancels, and a float32
+// evaluation (or 2D gradients known to a relative accuracy) can only reach that accuracy times this
+// magnitude.
 int or_preprocess_bwd(int64_t n, const double* mean3d, const double* log_scale, const double* quat,
                       const double* logit, const double* sh, const OrCamera* cam, const OrOptions* opt,
                       const double* grad2d, double* d_mean3d, double* d_log_scale, double* d_quat,
-                      double* d_logit, double* d_sh) {
+                      double* d_logit, double* d_sh, double* grad_mag) {
     if (n < 0 || !cam || !opt) return -1;
     const int deg = opt->sh_degree, K = (deg + 1) * (deg + 1);
     using D = Dual<11>;
@@ -652,7 +799,7 @@ int or_preprocess_bwd(int64_t n, const double* mean3d, const double* log_scale, 
         D lg = D::var(logit[g], 10);
         Projected<D> P;
         project<D>(mu, ls, q, lg, sh + g * K * 3, deg, *cam, *opt, P);
-        double grad[11] = {0};
+        double grad[11] = {0}, mag[11] = {0};
         for (int k = 0; k < K * 3; ++k) d_sh[(size_t)g * K * 3 + k] = 0.0;
         bool culled = P.culled;
         if (!culled) {
@@ -668,7 +815,10 @@ int or_preprocess_bwd(int64_t n, const double* mean3d, const double* log_scale, 
             const D* outs[9] = {&P.mean2d[0], &P.mean2d[1], &P.conic[0], &P.conic[1], &P.conic[2],
                                 &P.opacity, &P.rgb[0], &P.rgb[1], &P.rgb[2]};
             for (int o = 0; o < 9; ++o)
-                for (int v = 0; v < 11; ++v) grad[v] += gi[o] * outs[o]->d[v];
+                for (int v = 0; v < 11; ++v) {
+                    grad[v] += gi[o] * outs[o]->d[v];
+                    mag[v] += std::fabs(gi[o] * outs[o]->d[v]);
+                }
             for (int ch = 0; ch < 3; ++ch) {
                 if (P.rgb_clamped[ch]) continue;
                 for (int k = 0; k < K; ++k) d_sh[(size_t)g * K * 3 + k * 3 + ch] = P.Y[k] * gi[6 + ch];
@@ -678,6 +828,8 @@ int or_preprocess_bwd(int64_t n, const double* mean3d, const double* log_scale, 
         for (int i = 0; i < 3; ++i) d_log_scale[3 * g + i] = grad[3 + i];
         for (int i = 0; i < 4; ++i) d_quat[4 * g + i] = grad[6 + i];
         d_logit[g] = grad[10];
+        if (grad_mag)
+            for (int v = 0; v < 11; ++v) grad_mag[11 * (size_t)g + v] = mag[v];
     }
     return 0;
 }
@@ -862,92 +1014,85 @@ int or_render2d(int64_t n, const double* rec2d, const uint32_t* vals, const uint
     const double alpha_min = (double)(1.0f / 255.0f), t_min = (double)1e-4f;
     const double cx = cam->cx, cy = cam->cy;
     if (grad) std::memset(grad, 0, sizeof(double) * 16 * (size_t)n);
+    std::vector<double> part;  // per list entry: its gradient partial sum over the tile's pixels
+    for (const TileGroup& grp : tile_groups(ranges, T)) {
+        if (grad) part.assign((size_t)(grp.p1 - grp.p0) * 16, 0.0);
 #pragma omp parallel num_threads(n_threads(threads))
-    {
-        struct Blend { int64_t pos; uint32_t g; double alpha, T, G; bool clamped; double x, y; };
-        std::vector<Blend> bl;
-        std::vector<double> acc;
+        {
+            struct Blend { int64_t pos; uint32_t g; double alpha, T, G; bool clamped; double x, y; };
+            std::vector<Blend> bl;
 #pragma omp for schedule(dynamic, 4)
-        for (int64_t tile = 0; tile < T; ++tile) {
-            const int tx = (int)(tile % tiles_x), ty = (int)(tile / tiles_x);
-            const int64_t s = ranges[2 * tile], e = ranges[2 * tile + 1];
-            const int64_t len = e - s;
-            if (grad) acc.assign((size_t)len * 16, 0.0);
-            for (int ly = 0; ly < kTile; ++ly)
-                for (int lx = 0; lx < kTile; ++lx) {
-                    const int px = tx * kTile + lx, py = ty * kTile + ly;
-                    if (px >= W || py >= H) continue;
-                    const double x = px + 0.5, y = py + 0.5;
-                    double Tr = 1.0, col[3] = {0.0, 0.0, 0.0};
-                    uint32_t contrib = 0;
-                    uint8_t pf = 0;
-                    uint64_t sig = 1469598103934665603ull;  // FNV-1a over (position, clamp, branch) of blended entries
-                    bl.clear();
-                    for (int64_t pos = s; pos < e; ++pos) {
-                        const uint32_t g = vals[pos];
-                        const double* r = rec2d + 16 * (size_t)g;
-                        double p3, plp;
-                        const double power = power2d<double>(r, cx, cy, x, y, &p3, &plp);
-                        if (std::fabs(p3 - plp) <= 1e-4 * (std::fabs(p3) + std::fabs(plp)) + 1e-7) pf |= 4;
-                        const double G = std::exp(power);
-                        const double oG = r[11] * G;
-                        const bool clamped = oG > 0.99;
-                        const double alpha = clamped ? 0.99 : oG;
-                        if (!clamped && std::fabs(alpha / alpha_min - 1.0) < 1e-4) pf |= 1;
-                        if (alpha < alpha_min) continue;
-                        const double test_T = Tr * (1.0 - alpha);
-                        if (std::fabs(test_T / t_min - 1.0) < 1e-4) pf |= 2;
-                        if (test_T < t_min) break;
-                        for (int ch = 0; ch < 3; ++ch) col[ch] += r[12 + ch] * alpha * Tr;
-                        bl.push_back({pos, g, alpha, Tr, G, clamped, x, y});
-                        sig = (sig ^ (uint64_t)(4 * (pos - s) + (clamped ? 1 : 0) + (p3 >= plp ? 2 : 0))) * 1099511628211ull;
-                        Tr = test_T;
-                        contrib = (uint32_t)(pos - s + 1);
-                    }
-                    const int64_t pix = (int64_t)py * W + px;
-                    for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
-                    t_final[pix] = Tr;
-                    n_contrib[pix] = contrib;
-                    if (pix_flags) pix_flags[pix] = pf;
-                    if (pix_sig) pix_sig[pix] = sig;
-                    if (!grad) continue;
-                    double gpix[3], S[3];
-                    for (int ch = 0; ch < 3; ++ch) {
-                        gpix[ch] = dl_dimage[(int64_t)ch * W * H + pix];
-                        S[ch] = Tr * cam->bg[ch];
-                    }
-                    for (int64_t k = (int64_t)bl.size() - 1; k >= 0; --k) {
-                        const Blend& b = bl[k];
-                        const double* r = rec2d + 16 * (size_t)b.g;
-                        double* a = &acc[(size_t)(b.pos - s) * 16];
-                        double dalpha = 0.0;
+            for (int64_t tile = grp.t0; tile < grp.t1; ++tile) {
+                const int tx = (int)(tile % tiles_x), ty = (int)(tile / tiles_x);
+                const int64_t s = ranges[2 * tile], e = ranges[2 * tile + 1];
+                const int64_t len = e - s;
+                double* acc = (grad && len > 0) ? part.data() + (size_t)(s - grp.p0) * 16 : nullptr;
+                for (int ly = 0; ly < kTile; ++ly)
+                    for (int lx = 0; lx < kTile; ++lx) {
+                        const int px = tx * kTile + lx, py = ty * kTile + ly;
+                        if (px >= W || py >= H) continue;
+                        const double x = px + 0.5, y = py + 0.5;
+                        double Tr = 1.0, col[3] = {0.0, 0.0, 0.0};
+                        uint32_t contrib = 0;
+                        uint8_t pf = 0;
+                        uint64_t sig = 1469598103934665603ull;  // FNV-1a over (position, clamp, branch) of blended entries
+                        bl.clear();
+                        for (int64_t pos = s; pos < e; ++pos) {
+                            const uint32_t g = vals[pos];
+                            const double* r = rec2d + 16 * (size_t)g;
+                            double p3, plp;
+                            const double power = power2d<double>(r, cx, cy, x, y, &p3, &plp);
+                            if (std::fabs(p3 - plp) <= 1e-4 * (std::fabs(p3) + std::fabs(plp)) + 1e-7) pf |= 4;
+                            const double G = std::exp(power);
+                            const double oG = r[11] * G;
+                            const bool clamped = oG > 0.99;
+                            const double alpha = clamped ? 0.99 : oG;
+                            if (!clamped && std::fabs(alpha / alpha_min - 1.0) < 1e-4) pf |= 1;
+                            if (alpha < alpha_min) continue;
+                            const double test_T = Tr * (1.0 - alpha);
+                            if (std::fabs(test_T / t_min - 1.0) < 1e-4) pf |= 2;
+                            if (test_T < t_min) break;
+                            for (int ch = 0; ch < 3; ++ch) col[ch] += r[12 + ch] * alpha * Tr;
+                            bl.push_back({pos, g, alpha, Tr, G, clamped, x, y});
+                            sig = (sig ^ (uint64_t)(4 * (pos - s) + (clamped ? 1 : 0) + (p3 >= plp ? 2 : 0))) * 1099511628211ull;
+                            Tr = test_T;
+                            contrib = (uint32_t)(pos - s + 1);
+                        }
+                        const int64_t pix = (int64_t)py * W + px;
+                        for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
+                        t_final[pix] = Tr;
+                        n_contrib[pix] = contrib;
+                        if (pix_flags) pix_flags[pix] = pf;
+                        if (pix_sig) pix_sig[pix] = sig;
+                        if (!grad) continue;
+                        double gpix[3], S[3];
                         for (int ch = 0; ch < 3; ++ch) {
-                            a[12 + ch] += b.alpha * b.T * gpix[ch];
-                            dalpha += gpix[ch] * (r[12 + ch] * b.T - S[ch] / (1.0 - b.alpha));
+                            gpix[ch] = dl_dimage[(int64_t)ch * W * H + pix];
+                            S[ch] = Tr * cam->bg[ch];
                         }
-                        for (int ch = 0; ch < 3; ++ch) S[ch] += r[12 + ch] * b.alpha * b.T;
-                        if (b.clamped) continue;
-                        const double dpower = r[11] * b.G * dalpha;
-                        using D = Dual<11>;
-                        D rd[11];
-                        for (int i = 0; i < 11; ++i) rd[i] = D::var(r[i], i);
-                        const D pw = power2d<D>(rd, cx, cy, b.x, b.y);
-                        for (int i = 0; i < 11; ++i) a[i] += pw.d[i] * dpower;
-                        a[11] += b.G * dalpha;
-                    }
-                }
-            if (grad)
-                for (int64_t k = 0; k < len; ++k) {
-                    const uint32_t g = vals[s + k];
-                    for (int j = 0; j < 15; ++j) {
-                        const double v = acc[(size_t)k * 16 + j];
-                        if (v != 0.0) {
-#pragma omp atomic
-                            grad[16 * (size_t)g + j] += v;
+                        for (int64_t k = (int64_t)bl.size() - 1; k >= 0; --k) {
+                            const Blend& b = bl[k];
+                            const double* r = rec2d + 16 * (size_t)b.g;
+                            double* a = acc + (size_t)(b.pos - s) * 16;
+                            double dalpha = 0.0;
+                            for (int ch = 0; ch < 3; ++ch) {
+                                a[12 + ch] += b.alpha * b.T * gpix[ch];
+                                dalpha += gpix[ch] * (r[12 + ch] * b.T - S[ch] / (1.0 - b.alpha));
+                            }
+                            for (int ch = 0; ch < 3; ++ch) S[ch] += r[12 + ch] * b.alpha * b.T;
+                            if (b.clamped) continue;
+                            const double dpower = r[11] * b.G * dalpha;
+                            using D = Dual<11>;
+                            D rd[11];
+                            for (int i = 0; i < 11; ++i) rd[i] = D::var(r[i], i);
+                            const D pw = power2d<D>(rd, cx, cy, b.x, b.y);
+                            for (int i = 0; i < 11; ++i) a[i] += pw.d[i] * dpower;
+                            a[11] += b.G * dalpha;
                         }
                     }
-                }
+            }
         }
+        if (grad) add_partials_in_list_order(part, 16, 15, vals, grp.p0, grp.p1, grad, 16, threads);
     }
     return 0;
 }

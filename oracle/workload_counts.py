@@ -1,9 +1,11 @@
-"""Counts of the benchmark workload measured by the oracle (TEST INFRASTRUCTURE).
+"""Counts of a benchmark workload measured by the oracle (TEST INFRASTRUCTURE).
 
-Runs the float64 oracle on the outdoor scene (1.6M Gaussians, 1297x840, seeded) and writes
-profiles/workload_counts_outdoor.md: duplicates D, (pixel, Gaussian) pairs evaluated and blended,
-active (8x4 pixel block, Gaussian) and (tile, Gaussian) pairs with the histogram of blending
-pixels per active block, and the algorithmic bytes of the backward raster:
+Runs the float64 oracle on one view of a configuration (default: the outdoor scene, 1.6M
+Gaussians, 1297x840, seeded) and writes profiles/workload_counts_<name>.md: duplicates D, (pixel,
+Gaussian) pairs evaluated and blended, active (8x8 pixel block, Gaussian) and (tile, Gaussian)
+pairs with the histogram, over the active blocks, of the lanes with a blending pixel (the backward
+kernel's warp covers an 8x8 block with two pixels per lane: the per-warp popcount of DISTWAR's
+observations), and the algorithmic bytes of the backward raster:
     per tile, its list up to the largest contributor count x (4-byte index + 48-byte record),
     + per pixel 20 bytes (dL/dpixel, T_final, contributor count),
     + per Gaussian 48 bytes (the 2D gradient record written).
@@ -11,7 +13,7 @@ pixels per active block, and the algorithmic bytes of the backward raster:
     is replayed back to front from its last contributor).
 The benchmark divides these by measured kernel times; nothing of the CUDA library is used here.
 
-    python -m oracle.workload_counts
+    python -m oracle.workload_counts [config]      (2 = outdoor, 4 = contention, ...)
 """
 from __future__ import annotations
 
@@ -28,9 +30,11 @@ sys.path.insert(0, ROOT)
 import gs_scenes  # noqa: E402
 import oracle  # noqa: E402
 
+NAMES = {0: "tiny", 1: "object", 2: "outdoor", 3: "large", 4: "contention"}
+
 
 def counts(cfg: int = 2) -> dict:
-    s = gs_scenes.make_scene(cfg)
+    s = gs_scenes.make_scene(cfg, views=1 if cfg == 3 else None)
     cam = s.cameras[0]
     t0 = time.perf_counter()
     out = oracle.view_step(s)
@@ -46,8 +50,8 @@ def counts(cfg: int = 2) -> dict:
     tlen = (ranges[:, 1].astype(np.int64) - ranges[:, 0].astype(np.int64))
     listed = int(np.minimum(tlen, tmax).sum())
     P = cam.width * cam.height
-    return {"workload": "outdoor 1.6M Gaussians 1297x840 seed 2", "n_gaussians": s.n, "pixels": P,
-            "duplicates": int(len(out["vals"])), "pairs_evaluated": int(st["pairs_evaluated"]),
+    return {"workload": f"{NAMES[cfg]} {s.n} Gaussians {cam.width}x{cam.height} seed {cfg}", "n_gaussians": s.n,
+            "pixels": P, "duplicates": int(len(out["vals"])), "pairs_evaluated": int(st["pairs_evaluated"]),
             "pairs_blended": int(st["pairs_blended"]), "warp_gauss_active": int(st["warp_gauss_active"]),
             "tile_gauss_active": int(st["tile_gauss_active"]), "lane_hist": [int(v) for v in st["lane_hist"]],
             "bwd_list_entries": listed, "bwd_bytes": listed * 52 + P * 20 + s.n * 48,
@@ -56,21 +60,28 @@ def counts(cfg: int = 2) -> dict:
 
 
 def main():
-    c = counts()
-    path = os.path.join(ROOT, "profiles", "workload_counts_outdoor.md")
+    cfg = int(sys.argv[1]) if len(sys.argv) > 1 else 2
+    c = counts(cfg)
+    path = os.path.join(ROOT, "profiles", f"workload_counts_{NAMES[cfg]}.md")
     hist = c["lane_hist"]
+    active = max(1, sum(hist))
     with open(path, "w") as f:
-        f.write("# Workload counts: outdoor scene (1.6M Gaussians, 1297x840, seed 2)\n\n")
-        f.write("Written by `python -m oracle.workload_counts` (float64 oracle only). The benchmark's\n")
+        f.write(f"# Workload counts: {c['workload']}\n\n")
+        f.write(f"Written by `python -m oracle.workload_counts {cfg}` (float64 oracle only). The benchmark's\n")
         f.write("roofline numerators use `pairs_replayed_bwd`, `pairs_blended` and `bwd_bytes`.\n\n")
         f.write(f"- duplicates D = {c['duplicates']:,}\n- pairs evaluated = {c['pairs_evaluated']:,}\n")
         f.write(f"- pairs blended = {c['pairs_blended']:,}\n")
         f.write(f"- pairs replayed by the backward (sum of contributor counts) = {c['pairs_replayed_bwd']:,}\n")
-        f.write(f"- active (8x4 block, Gaussian) = {c['warp_gauss_active']:,}; "
+        f.write(f"- active (8x8 block, Gaussian) = {c['warp_gauss_active']:,}; "
                 f"active (tile, Gaussian) = {c['tile_gauss_active']:,}\n")
-        full = hist[32] / max(1, sum(hist))
-        f.write(f"- share of active blocks with all 32 pixels blending: {full:.1%}\n\n")
-        f.write("```json\n" + json.dumps(c) + "\n```\n")
+        f.write("- lanes with a blending pixel per active (8x8 block, Gaussian), the warp's popcount: "
+                f"all 32 in {hist[32] / active:.1%}, at least 28 in {sum(hist[28:]) / active:.1%}, "
+                f"at most 4 in {sum(hist[1:5]) / active:.1%}; mean {sum(i * h for i, h in enumerate(hist)) / active:.1f}\n\n")
+        f.write("| lanes | active blocks | share |\n|---|---|---|\n")
+        for lo, hi in ((1, 4), (5, 8), (9, 12), (13, 16), (17, 20), (21, 24), (25, 27), (28, 31), (32, 32)):
+            n = sum(hist[lo:hi + 1])
+            f.write(f"| {lo}-{hi} | {n:,} | {n / active:.1%} |\n" if lo != hi else f"| {lo} | {n:,} | {n / active:.1%} |\n")
+        f.write("\n```json\n" + json.dumps(c) + "\n```\n")
     print(path)
 
 

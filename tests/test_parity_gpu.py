@@ -1,10 +1,13 @@
 """Parity of the CUDA library (through its C ABI) with the float64 oracle, stage by stage and end
 to end, on seeded scenes shaped like the five configurations (smaller sizes that span many tiles
-and a ragged image edge) plus edge cases, and on the full 1.6M-Gaussian 1297x840 scene.
+and a ragged image edge) plus edge cases. The full-size configurations are in
+test_full_size_gpu.py.
 
 Bars: bit-exact for depth keys, duplicate counts, sorted (tile, depth, index) lists, tile ranges
 and contributor counts (outside the oracle's marginal decisions); 1e-5 max abs error on pixels;
-1e-4 of max|grad| per gradient tensor.
+1e-4 of max|grad| per gradient tensor. The oracle flags at most 5e-6 of the evaluated (pixel,
+Gaussian) pairs as marginal (+3), and at most 1e-4 of the pixels (+3) on scenes with fewer than
+300 evaluated pairs per pixel.
 """
 from __future__ import annotations
 
@@ -21,7 +24,9 @@ import gs_scenes  # noqa: E402
 import oracle  # noqa: E402
 from differentiable_gaussian_splatting_gs_gb300 import _abi, api, step  # noqa: E402
 
-from _cases import CASES, GRAD2D_GROUPS, GRAD_KEYS, PARAM_NAMES, grad_close, scene, stage_inputs  # noqa: E402
+import _gpu_checks as gc  # noqa: E402
+from _cases import (CASES, GRAD2D_GROUPS, GRAD_KEYS, PARAM_NAMES, grad_close, grad_close_mag, scene,  # noqa: E402
+                    stage_inputs)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -59,31 +64,32 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     assert x == 45
 
 
+@pytest.mark.parametrize("spin", [1, 64])
+def test_sort_lookback_gives_up_and_reports_timeout(spin):
+    """The depth sort's look-back, with a predecessor block that never publishes, gives up after
+    `spin` polls: the device error word reports GS_ERR_TIMEOUT, the block still places its items
+    (within its buffers), and the next sort is exact."""
+    lib = _abi.load()
+    ws = torch.full((_abi.GS_SELFTEST_SORT_WORKSPACE_BYTES // 4,), 7, dtype=torch.int32, device=DEV)
+    assert lib.gs_selftest_sort_timeout(ws.data_ptr(), ws.numel() * 4, spin, None) == 0
+    assert api.gs_device_error() == _abi.GS_ERR_TIMEOUT
+    assert api.gs_device_error() == _abi.GS_OK
+    # the block's 4096 items (keys 0, values 4096..8191 in order) landed at positions 0..4095
+    vals_out = ws[2 * 8192: 3 * 8192].cpu().numpy()
+    assert np.array_equal(vals_out[:4096], np.arange(4096, 8192))
+    # too small a workspace is rejected on the host
+    assert lib.gs_selftest_sort_timeout(ws.data_ptr(), 1024, spin, None) == _abi.GS_ERR_ARG
+    d = stage_inputs("tiny")
+    b = api.gs_bin_and_sort(dev_proj(d["rec"]), d["cam"], api.make_options(0))
+    assert np.array_equal(u32(b.vals), d["vals"])
+
+
 # --------------------------------------------------------------------------------- preprocess
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_preprocess_matches_oracle(name):
     d = stage_inputs(name)
-    s, cam, pre = d["scene"], d["cam"], d["pre"]
-    proj = api.gs_preprocess(dev_params(s), cam, api.make_options(s.sh_degree))
-    rec = proj.rec.cpu().numpy()
-    radius = proj.radius.cpu().numpy()
-    tt = u32(proj.tiles_touched)
-    depth = proj.depth.cpu().numpy()
-    assert np.array_equal(depth.view(np.uint32), pre["depth"].view(np.uint32)), "depth keys differ"
-    marginal = (pre["flags"] & 6) != 0
-    ok = ~marginal
-    assert np.array_equal(radius[ok], pre["radius"][ok])
-    assert np.array_equal(tt[ok], pre["tiles_touched"][ok])
-    live = ok & (pre["radius"] > 0)
-    for cols, ref in ((slice(0, 2), pre["mean2d"]), (slice(2, 5), pre["conic"]), (slice(5, 6), pre["opacity"][:, None]),
-                      (slice(6, 9), pre["rgb"])):
-        got, want = rec[live, cols].astype(np.float64), ref[live]
-        err = np.abs(got - want)
-        bound = 1e-5 * np.abs(want) + 1e-6 * np.abs(want).max(axis=0)
-        assert np.all(err <= bound), f"cols {cols}: worst {(err / np.maximum(bound, 1e-30)).max():.3g} x bound"
-    assert np.all(rec[~(radius > 0)] == 0.0)
-    assert marginal.sum() <= max(2, 1e-3 * s.n)
+    gc.check_preprocess(d["scene"], d["cam"], d["pre"])
 
 
 def test_preprocess_empty_and_all_culled():
@@ -177,7 +183,9 @@ def test_render_fwd_matches_oracle(name, staging):
     _, _, _, img, tf, nc = _fwd(d, staging)
     f = d["fwd"]
     ok = f["pix_flags"] == 0
-    assert (~ok).sum() <= max(3, 1e-2 * ok.size), f"{(~ok).sum()} marginal pixels"
+    gc.check_flag_count(f["pix_flags"], d["stats"]["pairs_evaluated"])
+    if d["stats"]["pairs_evaluated"] < 300 * ok.size:
+        assert (~ok).sum() <= 1e-4 * ok.size + 3, f"{(~ok).sum()} marginal pixels"
     err = np.abs(img.cpu().numpy() - f["image"])
     assert err[:, ok].max() <= 1e-5, err[:, ok].max()
     assert np.array_equal(u32(nc)[ok], f["n_contrib"][ok])
@@ -228,19 +236,7 @@ def test_adaptive_threshold_extremes(thr):
 @pytest.mark.parametrize("name", list(CASES))
 def test_preprocess_bwd_matches_oracle(name):
     d = stage_inputs(name)
-    s, cam = d["scene"], d["cam"]
-    params = dev_params(s)
-    opt = api.make_options(s.sh_degree)
-    proj = api.gs_preprocess(params, cam, opt)
-    g2 = torch.zeros((s.n, 12), dtype=torch.float32, device=DEV)
-    g2[:, :9] = torch.from_numpy(d["grad2d32"]).to(DEV)
-    grads = api.gs_preprocess_bwd(params, cam, opt, proj, g2)
-    ok_rows = (d["pre"]["flags"] & 6) == 0
-    for name_p in PARAM_NAMES:
-        got = grads[name_p].cpu().numpy().reshape(s.n, -1)
-        want = d["grads"][GRAD_KEYS[name_p]].reshape(s.n, -1)
-        ok, err, tol = grad_close(got, want, mask=ok_rows)
-        assert ok, f"{name_p}: {err:.3g} > {tol:.3g}"
+    gc.check_preprocess_bwd(d["scene"], d["cam"], d["pre"], d["grad2d32"], d["grads"])
 
 
 def test_preprocess_bwd_accumulates_views():
@@ -256,6 +252,7 @@ def test_preprocess_bwd_accumulates_views():
         g2[:, :9] = torch.from_numpy(g2n).to(DEV)
         api.gs_preprocess_bwd(params, cam, opt, proj, g2, out=grads, accumulate=v > 0)
         o = oracle.preprocess_bwd(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, s.sh_degree, cam, g2n)
+        o.pop("mag")
         want = o if want is None else {k: want[k] + o[k] for k in o}
     for name_p in PARAM_NAMES:
         got = grads[name_p].cpu().numpy().reshape(s.n, -1)
@@ -265,58 +262,41 @@ def test_preprocess_bwd_accumulates_views():
 
 # --------------------------------------------------------------------------------- end to end
 
-def _tile_entries(vals, ranges):
-    """(tile id, Gaussian index) of every entry of a sorted list, in list order."""
-    lens = (ranges[:, 1].astype(np.int64) - ranges[:, 0].astype(np.int64))
-    tiles = np.repeat(np.arange(len(ranges)), lens)
-    order = np.concatenate([np.arange(a, b_) for a, b_ in ranges if b_ > a]) if lens.sum() else np.zeros(0, int)
-    return tiles, vals[order]
-
-
-def _end_to_end(s, view, mode="sm"):
-    cam = s.cameras[view]
-    params = dev_params(s)
-    opt = api.make_options(s.sh_degree, bwd_mode=mode)
-    ref = oracle.view_step(s, view=view, mask_marginal=True)
-    bufs = step.StepBuffers(s.n, DEV)
-    proj = api.gs_preprocess(params, cam, opt, out=bufs.proj)
-    b = api.gs_bin_and_sort(proj, cam, opt, buffers=bufs.sort)
-    img, tf, nc = api.gs_render_fwd(proj, b.vals, b.ranges, cam, opt)
-    g2 = api.gs_render_bwd(proj, b.vals, b.ranges, cam, opt, torch.from_numpy(ref["dl_dimage"]).to(DEV), tf, nc)
-    grads = api.gs_preprocess_bwd(params, cam, opt, proj, g2)
-    pre = ref["pre"]
-    flagged = (pre["flags"] & 6) != 0
-    # sorted lists: identical after removing the entries of Gaussians with a marginal radius or rectangle
-    gt, gv = _tile_entries(u32(b.vals), u32(b.ranges))
-    ot, ov = _tile_entries(ref["vals"], ref["ranges"])
-    kg, ko = ~flagged[gv], ~flagged[ov]
-    assert np.array_equal(gt[kg], ot[ko]) and np.array_equal(gv[kg], ov[ko])
-    ok = ~ref["marginal"]
-    err = np.abs(img.cpu().numpy() - ref["fwd"]["image"])
-    # each side computes its own records here, so the 1e-5 bar is widened by the oracle's bound on
-    # the colour change those record differences can cause (alpha bounds propagated per pixel)
-    bound = 1e-5 + ref["fwd"]["pix_err"]
-    assert np.all(err[:, ok] <= bound[None][:, ok]), (err - bound[None])[:, ok].max()
-    assert np.median(ref["fwd"]["pix_err"][ok]) < 5e-4, "the propagated bound is not informative"
-    assert np.mean(err[:, ok] <= 1e-5) > 0.99, "more than 1% of the pixels above 1e-5"
-    assert np.array_equal(u32(nc)[ok], ref["fwd"]["n_contrib"][ok])
-    for name_p in PARAM_NAMES:
-        got = grads[name_p].cpu().numpy().reshape(s.n, -1)
-        want = ref["grads"][GRAD_KEYS[name_p]].reshape(s.n, -1)
-        okg, e, tol = grad_close(got, want, mask=~flagged)
-        assert okg, f"{name_p}: {e:.3g} > {tol:.3g}"
-    return ref, b
-
-
+@pytest.mark.parametrize("mode", ["adaptive", "direct"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_end_to_end_matches_oracle(name):
+def test_end_to_end_matches_oracle(name, mode):
     s, view = scene(name)
-    _end_to_end(s, view)
+    gc.end_to_end(s, view, mode=mode)
 
 
-def test_full_size_outdoor_scene():
-    """The 1.6M-Gaussian 1297x840 scene in the launch configuration the benchmark times: the
-    whole training step against the whole oracle."""
-    s = gs_scenes.make_scene(2)
-    ref, b = _end_to_end(s, 0)
-    assert b.n_dup == pytest.approx(len(ref["vals"]), abs=64)
+def test_large_scene_views_accumulate_like_the_oracle():
+    """The large scene's step renders 8 views whose parameter gradients are summed (reduced
+    scene): the library's multi-view step (eager and as one captured graph) against the sum of
+    the oracle's per-view steps, each view with its own marginal masking."""
+    s = gs_scenes.make_scene(3, n=60_000, res_scale=0.25)
+    assert len(s.cameras) == 8
+    refs = [oracle.view_step(s, view=v, mask_marginal=True) for v in range(8)]
+    want = {k: sum(r["grads"][k] for r in refs) for k in refs[0]["grads"] if k != "mag"}
+    mags = {k: sum(r["grads"]["mag"][k] for r in refs) for k in refs[0]["grads"]["mag"]}
+    flagged = np.zeros(s.n, bool)
+    for r in refs:
+        flagged |= (r["pre"]["flags"] & oracle.MARGINAL) != 0
+    params = gc.dev_params(s)
+    opt = api.make_options(s.sh_degree)
+    ups = [torch.from_numpy(r["dl_dimage"]).to(DEV) for r in refs]
+    cap = max(int(r["pre"]["tiles_touched"].sum(dtype=np.int64)) for r in refs) + 4096
+    for graph in (False, True):
+        grads = api.alloc_param_grads(params)
+        bufs = step.StepBuffers(s.n, DEV)
+        if graph:
+            g = step.GraphedStep(params, s.cameras, [None] * 8, opt, grads, bufs, cap, upstream=ups)
+            g.replay()
+        else:
+            n_dup = torch.zeros(8, dtype=torch.int64, device=DEV)
+            step.train_step_async(params, s.cameras, [None] * 8, opt, grads, bufs, cap, n_dup, upstream=ups)
+        torch.cuda.synchronize()
+        for name_p in PARAM_NAMES:
+            got = grads[name_p].cpu().numpy().reshape(s.n, -1)
+            okg, ratio = grad_close_mag(got, want[GRAD_KEYS[name_p]].reshape(s.n, -1),
+                                        mags[GRAD_KEYS[name_p]].reshape(s.n, -1), rel_mag=1e-4, mask=~flagged)
+            assert okg, f"graph={graph} {name_p}: error {ratio:.3g} x allowance"
