@@ -54,12 +54,13 @@ COUNTS_PATH = os.path.join(ROOT, "profiles", "workload_counts_outdoor.md")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "render_bwd_outdoor_1600k.md")
 TRAFFIC_SOURCES = ("differentiable_gaussian_splatting_gs_gb300/csrc/render.cu",
                    "differentiable_gaussian_splatting_gs_gb300/csrc/gs_abi.cu")
-# Algorithmic work of the backward raster: every pixel's list is replayed back to front from its
-# last contributor, about 60 FP32 operations per replayed (pixel, Gaussian) pair. A narrower count,
-# 55 operations per blended pair only (power 11, alpha 3, transmittance 4, colour gradient 3, alpha
-# gradient 15, colour-behind update 6, opacity and geometry gradients 13), is reported beside it.
-BWD_FLOPS_PER_REPLAYED_PAIR = 60
-BWD_FLOPS_PER_PAIR = 55
+# Algorithmic work of the backward raster. Every pixel's list is replayed back to front from its
+# last contributor, and each replayed (pixel, Gaussian) pair needs its alpha: offsets 2, quadratic
+# form 9, exponential 1, opacity product 1, clamp 1, threshold 1 = 15 FP32 operations. Each blended
+# pair then needs its gradient: transmittance 4, colour gradient 3, alpha gradient 15, colour-behind
+# update 6, opacity and geometry gradients 13 = 41.
+BWD_FLOPS_ALPHA = 15
+BWD_FLOPS_GRADIENT = 41
 
 
 def parse_args():
@@ -265,6 +266,127 @@ def oracle_sample(scene, frac_x: float, frac_y: float):
     desc = (f"float64 oracle, whole step on the central {cam.width}x{cam.height} tile-aligned window of the "
             f"view ({int(sel.sum())} Gaussians touch it; preprocess over all {scene.n})")
     return cam.width * cam.height, dt, desc, os.cpu_count()
+
+
+def backward_roofline(counts: dict, peaks: dict, bwd_ms: float, dev, mode: str) -> dict:
+    """Roofline line of the backward raster (the dominant kernel) at the outdoor scene.
+
+    Algorithmic work, from the oracle's counts of the workload (profiles/workload_counts_outdoor.md):
+    every (pixel, Gaussian) pair the method replays (each pixel's list back to front from its last
+    contributor) needs its alpha evaluated, BWD_FLOPS_ALPHA FP32 operations; every blended pair
+    needs its gradient, BWD_FLOPS_GRADIENT more. Peak: the device's SM count x 128 FP32 lanes x 2
+    (fused multiply-add) x the measured maximum SM clock. The bound the pages name for this
+    kernel, the L2 atomics, and its HBM traffic are reported beside it with their own fractions,
+    and so is the resource that binds it (instruction issue, from the ncu capture)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+    flops = (counts["pairs_replayed_bwd"] * BWD_FLOPS_ALPHA + counts["pairs_blended"] * BWD_FLOPS_GRADIENT)
+    ach = flops / (bwd_ms / 1e3) / 1e12
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_gbs = counts["bwd_bytes"] / (bwd_ms / 1e3) / 1e9
+    traffic = l2_red = binding = None
+    tr = json_block(TRAFFIC_PATH)
+    # the counters hold while the kernel source and its launch defaults (the C ABI file) are unchanged
+    if tr and tr.get("source_hash") == source_hash(*TRAFFIC_SOURCES) and mode == "adaptive":
+        traffic = tr.get("dram_bytes_per_launch")
+        if "l2_red_frac_of_peak" in tr:
+            l2_red = {"sectors_per_launch": tr.get("l2_red_sectors_per_launch"),
+                      "frac_of_peak": tr["l2_red_frac_of_peak"],
+                      "source": "ncu, profiles/" + os.path.basename(TRAFFIC_PATH)}
+        if "issue_active_frac" in tr:
+            binding = {"resource": "instruction issue", "issue_active_frac": tr["issue_active_frac"],
+                       "fma_pipe_frac": tr.get("fma_pipe_frac"),
+                       "source": "ncu, profiles/" + os.path.basename(TRAFFIC_PATH)}
+    return {"kernel": f"k_render_bwd ({mode} accumulation, bulk staging)", "bound": "alu", "achieved": ach,
+            "peak": peak, "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
+            "numerator": f"{BWD_FLOPS_ALPHA} FP32 operations per replayed (pixel, Gaussian) pair (its alpha) + "
+                         f"{BWD_FLOPS_GRADIENT} per blended pair (its gradient), counts of the oracle",
+            "algorithmic_flops": flops, "kernel_ms": bwd_ms,
+            "peak_source": f"derived: {sms} SMs (device) x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz (measured max SM "
+                           "clock, MEASURED_PEAKS.json)",
+            "binding": binding,
+            "l2_atomic": l2_red,
+            "hbm": {"algorithmic_bytes": counts["bwd_bytes"], "achieved_gbs": hbm_gbs, "peak_gbs": hbm_peak,
+                    "frac_of_measured": hbm_gbs / hbm_peak}}
+
+
+def time_bwd_modes(api, bufs, cam, sh_degree, flush, stream, reps: int) -> dict:
+    """gs_render_bwd alone in each accumulation mode (gradient zeroing included), on the buffers of
+    the step just run; L2 flushed before every launch; mean of `reps` launches per mode."""
+    import torch
+    image, t_final, n_contrib, dl, ranges = bufs.image_buffers(cam.width, cam.height)
+    out = {}
+    for mode in ("direct", "warp", "adaptive", "sm"):
+        opt = api.make_options(sh_degree, bwd_mode=mode)
+        ts = []
+        for it in range(reps + 2):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            api.gs_render_bwd(bufs.proj, bufs.sort.vals, ranges, cam, opt, dl, t_final, n_contrib,
+                              grad2d=bufs.grad2d)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 2:
+                ts.append(e0.elapsed_time(e1))
+        out[f"{mode}_ms"] = sum(ts) / len(ts)
+    out["adaptive_speedup_over_direct"] = out["direct_ms"] / out["adaptive_ms"]
+    out["warp_speedup_over_direct"] = out["direct_ms"] / out["warp_ms"]
+    out["note"] = "each launch alone, L2 flushed before it, gradient zeroing included"
+    return out
+
+
+def config_block(cfg: int, dev, flush, stream, args, cpu: bool) -> dict:
+    """The step of one configuration as one CUDA graph replay per step: ms per view, the raster
+    kernels' times, duplicates per view and Mpix/s (5 timed replays, L2 flushed before each),
+    and the oracle's rate on a window of the first view."""
+    import torch
+    import gs_scenes
+    from differentiable_gaussian_splatting_gs_gb300 import api, step
+    scene = gs_scenes.make_scene(cfg)
+    names = ("mean3d", "log_scale", "quat", "opacity_logit", "sh")
+    params = {k: torch.from_numpy(np.ascontiguousarray(getattr(scene, k))).to(dev) for k in names}
+    grads = api.alloc_param_grads(params)
+    cams = [api.make_camera(c) for c in scene.cameras]
+    targets = [torch.from_numpy(t).to(dev) for t in scene.targets[:len(cams)]]
+    opt = api.make_options(scene.sh_degree)
+    bufs = step.StepBuffers(scene.n, dev)
+    # capacity: the synchronising sort of every view, once
+    cap = 0
+    for c in cams:
+        proj = api.gs_preprocess(params, c, opt, out=bufs.proj)
+        cap = max(cap, api.gs_bin_and_sort(proj, c, opt, buffers=bufs.sort, want_keys=False).n_dup)
+    ev = [((torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True)),
+           (torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True)))
+          for _ in cams]
+    g = step.GraphedStep(params, cams, targets, opt, grads, bufs, cap + 1024, events=ev)
+    for _ in range(3):
+        g.replay()
+    ms, fwd, bwd = [], [], []
+    for _ in range(5):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+        fwd.append(sum(e[0][0].elapsed_time(e[0][1]) for e in ev) / len(cams))
+        bwd.append(sum(e[1][0].elapsed_time(e[1][1]) for e in ev) / len(cams))
+    views = len(cams)
+    P = cams[0].width * cams[0].height
+    m = sum(ms) / len(ms)
+    out = {"workload": WORKLOADS[cfg], "views_per_step": views, "ms_per_view": m / views,
+           "mpix_per_s": P * views / (m / 1e3) / 1e6, "fwd_ms": sum(fwd) / len(fwd), "bwd_ms": sum(bwd) / len(bwd),
+           "duplicates_per_view": int(g.n_dup.sum().item()) / views, "launches_per_step": g.launches}
+    del g, bufs, params, grads, targets
+    if cpu:
+        pix, dt, desc, cores = oracle_sample(scene, 0.25, 0.25)
+        out["cpu_baseline"] = {"value": pix / dt / 1e6, "unit": "Mpix/s", "cores": cores, "kind": "oracle",
+                               "sample": desc, "seconds": dt}
+    return out
 
 
 # ------------------------------------------------------------------------------------ reference arm
@@ -546,6 +668,14 @@ def run_ours(args, rank, world, local_rank):
         extras["eager_step"] = {"ms_per_step": qm, "mpix_per_s": P / (qm / 1e3) / 1e6}
         assert api.gs_device_error() == 0
     if not args.no_extras:
+        # the backward raster in each accumulation mode on this step's own inputs, each launch timed
+        # alone with L2 flushed before it (the pages' comparison: warp-level reduction against direct
+        # per-thread atomics, DISTWAR Abstract)
+        one_step()
+        torch.cuda.synchronize()
+        extras["bwd_modes"] = time_bwd_modes(api, bufs, cams[-1], scene.sh_degree, flush, stream,
+                                             max(5, args.steps // 2))
+        assert api.gs_device_error() == 0
         exp_avg = {k: torch.zeros_like(params[k]) for k in names}
         exp_avg_sq = {k: torch.zeros_like(params[k]) for k in names}
         radius = bufs.proj.radius
@@ -683,40 +813,24 @@ def run_ours(args, rank, world, local_rank):
                                  "stage_ms": dict(zip(["preprocess", "bin_and_sort", "render_fwd", "dl_dimage",
                                                        "render_bwd", "preprocess_bwd"], pm))}
         assert api.gs_device_error() == 0
+    if not args.no_extras and use_graph and world == 1 and args.config == CFG:
+        # every configuration measured the same way in this run (fields of the metric per config),
+        # with the oracle's CPU rate on a window of each view beside it
+        del g2step
+        extras["configs"] = {}
+        for c in sorted(WORKLOADS):
+            extras["configs"][str(c)] = config_block(c, dev, flush, stream, args, cpu=not args.no_cpu_baseline)
+            torch.cuda.empty_cache()
+        assert api.gs_device_error() == 0
 
     # ---- roofline of the dominant kernel (the backward)
     peaks = load_json(PEAKS_PATH) or {}
     counts = json_block(COUNTS_PATH) or {}
     clocks = clk.summary()
     bwd_avg_ms = sum(bwd_ms) / len(bwd_ms)
-    sm_mhz_peak = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak = 152 * 128 * 2 * sm_mhz_peak * 1e6 / 1e12  # FP32 FMA lanes x 2 flops x max SM clock
     roof = None
     if "pairs_replayed_bwd" in counts and args.config == CFG:
-        flops = counts["pairs_replayed_bwd"] * BWD_FLOPS_PER_REPLAYED_PAIR
-        ach = flops / (bwd_avg_ms / 1e3) / 1e12
-        blended = counts["pairs_blended"] * BWD_FLOPS_PER_PAIR / (bwd_avg_ms / 1e3) / 1e12
-        traffic = l2_red = None
-        tr = json_block(TRAFFIC_PATH)
-        # the counters hold while the kernel source and its launch defaults (the C ABI file) are unchanged
-        if tr and tr.get("source_hash") == source_hash(*TRAFFIC_SOURCES):
-            traffic = tr.get("dram_bytes_per_launch")
-            if "l2_red_frac_of_peak" in tr:
-                # the L2-atomic roofline: reduction sectors the gradient atomics put through the L2,
-                # against the L2's sustained reduction rate (ncu, one launch)
-                l2_red = {"sectors_per_launch": tr.get("l2_red_sectors_per_launch"),
-                          "frac_of_peak": tr["l2_red_frac_of_peak"],
-                          "source": "ncu, profiles/" + os.path.basename(TRAFFIC_PATH)}
-        roof = {"kernel": "gs_render_bwd (k_render_bwd + gradient zeroing)", "bound": "alu", "achieved": ach,
-                "peak": alu_peak, "unit": "TFLOP/s", "frac": ach / alu_peak, "traffic": traffic,
-                "numerator": "60 FP32 operations per (pixel, Gaussian) pair replayed from each pixel's last "
-                             "contributor (the kernel's exact warp culling skips most of these pairs)",
-                "frac_blended_pairs_only": blended / alu_peak,
-                "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock of measured peaks file",
-                "kernel_ms": bwd_avg_ms, "algorithmic_flops": flops,
-                "hbm_frac_of_measured": (counts.get("bwd_bytes", 0) / (bwd_avg_ms / 1e3) / 1e9) /
-                float(peaks.get("hbm_gbs", 6800.0)),
-                "l2_atomic": l2_red}
+        roof = backward_roofline(counts, peaks, bwd_avg_ms, dev, args.mode)
 
     line = {"metric": METRIC, "value": value, "unit": "Mpix/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -728,9 +842,14 @@ def run_ours(args, rank, world, local_rank):
             "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
             "bwd_ms": bwd_avg_ms, "fwd_ms": sum(fwd_ms) / len(fwd_ms), "ms_per_view": ms / n_views, "step_ms_min": min(step_ms), "extras": extras}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and n_views == 1:
-        pix, dt, desc, cores = oracle_sample(scene, 0.5, 0.5)
+        # the oracle's whole step on the whole view, repeated until about 10 s of CPU time
+        runs = []
+        while sum(runs) < 10.0 and len(runs) < 5:
+            pix, dt, desc, cores = oracle_sample(scene, 1.0, 1.0)
+            runs.append(dt)
+        dt = sum(runs) / len(runs)
         line["cpu_baseline"] = {"value": pix / dt / 1e6, "unit": "Mpix/s", "cores": cores, "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+                                "sample": f"{desc}; mean of {len(runs)} runs", "seconds": dt}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
