@@ -1,7 +1,8 @@
 """Benchmark of the training step of the tile-based 3D Gaussian splatting rasterizer.
 
-One step = the whole hot path for one view: gs_preprocess, gs_bin_and_sort, gs_render_fwd, the
-loss gradient (image - target), gs_render_bwd, gs_preprocess_bwd. The workload is the outdoor
+One step = the whole hot path for one view: gs_preprocess, gs_bin_and_sort, gs_render_fwd,
+gs_render_bwd_sqerr (the backward with the squared-error loss gradient image - target formed in the
+kernel), gs_preprocess_bwd. The workload is the outdoor
 scene: 1.6M Gaussians, 1297x840, SH degree 3, a 64-cluster mixture (seeded, synthetic).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--mode sm|direct|warp|adaptive]
@@ -312,11 +313,12 @@ def backward_roofline(counts: dict, peaks: dict, bwd_ms: float, dev, mode: str) 
                     "frac_of_measured": hbm_gbs / hbm_peak}}
 
 
-def time_bwd_modes(api, bufs, cam, sh_degree, flush, stream, reps: int) -> dict:
-    """gs_render_bwd alone in each accumulation mode (gradient zeroing included), on the buffers of
-    the step just run; L2 flushed before every launch; mean of `reps` launches per mode."""
+def time_bwd_modes(api, bufs, cam, target, sh_degree, flush, stream, reps: int) -> dict:
+    """The backward (gs_render_bwd_sqerr, as in the step) alone in each accumulation mode
+    (gradient zeroing included), on the buffers of the step just run; L2 flushed before every
+    launch; mean of `reps` launches per mode."""
     import torch
-    image, t_final, n_contrib, dl, ranges = bufs.image_buffers(cam.width, cam.height)
+    image, t_final, n_contrib, _, ranges = bufs.image_buffers(cam.width, cam.height)
     out = {}
     for mode in ("direct", "warp", "adaptive", "sm"):
         opt = api.make_options(sh_degree, bwd_mode=mode)
@@ -325,8 +327,8 @@ def time_bwd_modes(api, bufs, cam, sh_degree, flush, stream, reps: int) -> dict:
             flush.fill_(1.0)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            api.gs_render_bwd(bufs.proj, bufs.sort.vals, ranges, cam, opt, dl, t_final, n_contrib,
-                              grad2d=bufs.grad2d)
+            api.gs_render_bwd_sqerr(bufs.proj, bufs.sort.vals, ranges, cam, opt, image, target, t_final, n_contrib,
+                                    grad2d=bufs.grad2d)
             e1.record(stream)
             torch.cuda.synchronize()
             if it >= 2:
@@ -472,10 +474,10 @@ def run_ours(args, rank, world, local_rank):
             api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib))
             if ev_fwd is not None:
                 ev_fwd[v][1].record(stream)
-            torch.sub(image, target[v], out=dl)
             if ev_bwd is not None:
                 ev_bwd[v][0].record(stream)
-            api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=bufs.grad2d)
+            api.gs_render_bwd_sqerr(proj, b.vals, b.ranges, c, opt, image, target[v], t_final, n_contrib,
+                                    grad2d=bufs.grad2d)
             if ev_bwd is not None:
                 ev_bwd[v][1].record(stream)
             api.gs_preprocess_bwd(params, c, opt, proj, bufs.grad2d, out=grads, accumulate=v > 0)
@@ -673,8 +675,8 @@ def run_ours(args, rank, world, local_rank):
         # per-thread atomics, DISTWAR Abstract)
         one_step()
         torch.cuda.synchronize()
-        extras["bwd_modes"] = time_bwd_modes(api, bufs, cams[-1], scene.sh_degree, flush, stream,
-                                             max(5, args.steps // 2))
+        extras["bwd_modes"] = time_bwd_modes(api, bufs, cams[-1], target[n_views - 1], scene.sh_degree, flush,
+                                             stream, max(5, args.steps // 2))
         assert api.gs_device_error() == 0
         exp_avg = {k: torch.zeros_like(params[k]) for k in names}
         exp_avg_sq = {k: torch.zeros_like(params[k]) for k in names}

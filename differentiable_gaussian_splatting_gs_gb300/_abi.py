@@ -31,7 +31,7 @@ EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_re
            "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static", "gs_adam_step",
            "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim", "gs_preprocess2d",
            "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd", "gs_bin_and_sort_async",
-           "gs_preprocess_bwd_stats", "gs_selftest_sort_timeout")
+           "gs_preprocess_bwd_stats", "gs_selftest_sort_timeout", "gs_render_bwd_sqerr")
 GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
 GS_SELFTEST_SORT_WORKSPACE_BYTES = 128 << 10
 
@@ -104,6 +104,8 @@ def load():
         lib.gs_bin_and_sort.argtypes = [pproj, pcam, popt, P, C.c_size_t, P, P, I64, C.POINTER(I64), P, P]
         lib.gs_render_fwd.argtypes = [pproj, P, P, pcam, popt, P, P, P, P]
         lib.gs_render_bwd.argtypes = [pproj, P, P, pcam, popt, P, P, P, P, P]
+        lib.gs_render_bwd_sqerr.argtypes = [pproj, P, P, pcam, popt, P, P, P, P, P, P, P]
+        lib.gs_render_bwd_sqerr.restype = C.c_int
         lib.gs_preprocess_bwd.argtypes = [ppar, pcam, popt, pproj, P, P, P, P, P, P, I32, P]
         lib.gs_preprocess_bwd_stats.argtypes = [ppar, pcam, popt, pproj, P, P, P, P, P, P, I32,
                                                 C.POINTER(gs_densify_outputs), P]

@@ -254,6 +254,22 @@ def gs_render_bwd(proj: Proj, vals, ranges, cam, opt: gs_options, dl_dimage, t_f
     return grad2d
 
 
+def gs_render_bwd_sqerr(proj: Proj, vals, ranges, cam, opt: gs_options, image, target, t_final, n_contrib,
+                        grad2d=None, loss=None, stream=None) -> torch.Tensor:
+    """gs_render_bwd with dL/dimage = image - target formed inside the kernel (the squared-error
+    loss 0.5 |image - target|^2, written to `loss`, a device float tensor [1], when given).
+    Returns grad2d [N, 12]."""
+    c = make_camera(cam) if not isinstance(cam, gs_camera) else cam
+    if grad2d is None:
+        grad2d = torch.empty((proj.n, 12), dtype=torch.float32, device=proj.rec.device)
+    ps = proj.struct()
+    check(_abi.load().gs_render_bwd_sqerr(C.byref(ps), _ptr(vals), _ptr(ranges), C.byref(c), C.byref(opt),
+                                          _ptr(image.contiguous()), _ptr(target.contiguous()), _ptr(t_final),
+                                          _ptr(n_contrib), _ptr(grad2d), _ptr(loss) if loss is not None else None,
+                                          _stream(stream)), "gs_render_bwd_sqerr")
+    return grad2d
+
+
 def alloc_param_grads(params: dict) -> dict:
     return {"mean3d": torch.zeros_like(params["mean3d"]), "log_scale": torch.zeros_like(params["log_scale"]),
             "quat": torch.zeros_like(params["quat"]), "opacity_logit": torch.zeros_like(params["opacity_logit"]),

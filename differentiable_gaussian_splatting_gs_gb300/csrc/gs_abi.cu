@@ -379,28 +379,50 @@ int gs_render_fwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* til
     return e ? cuda_fail(e, "gs_render_fwd") : GS_OK;
 }
 
-int gs_render_bwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges, const gs_camera* cam,
-                  const gs_options* opt, const float* dl_dimage, const float* t_final, const uint32_t* n_contrib,
-                  float* grad2d, void* stream) {
+// Shared body of gs_render_bwd (target = loss = NULL) and gs_render_bwd_sqerr.
+static int render_bwd(const char* name, const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges,
+               const gs_camera* cam, const gs_options* opt, const float* src, const float* target, float* loss,
+               const float* t_final, const uint32_t* n_contrib, float* grad2d, void* stream) {
     Opts o;
     KernelCamera kc;
     int s;
     if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_proj_n(proj))) return s;
-    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "tile_ranges NULL or misaligned");
-    if (!dl_dimage || !t_final || !n_contrib || !aligned(dl_dimage, 4) || !aligned(t_final, 4) || !aligned(n_contrib, 4))
-        return fail(GS_ERR_ARG, "dl_dimage / t_final / n_contrib NULL or misaligned");
+    if (!tile_ranges || !aligned(tile_ranges, 8)) return fail(GS_ERR_ARG, "%s: tile_ranges NULL or misaligned", name);
+    if (!src || !t_final || !n_contrib || !aligned(src, 4) || !aligned(t_final, 4) || !aligned(n_contrib, 4))
+        return fail(GS_ERR_ARG, "%s: image / dl_dimage, t_final or n_contrib NULL or misaligned", name);
     if (proj->n > 0 && (!vals || !aligned(vals, 4) || !grad2d || !aligned(grad2d, 16)))
-        return fail(GS_ERR_ARG, "vals or grad2d NULL or misaligned (grad2d needs 16 bytes)");
+        return fail(GS_ERR_ARG, "%s: vals or grad2d NULL or misaligned (grad2d needs 16 bytes)", name);
+    if (target && !aligned(target, 4)) return fail(GS_ERR_ARG, "%s: target misaligned", name);
+    if (loss && !aligned(loss, 4)) return fail(GS_ERR_ARG, "%s: loss misaligned", name);
     cudaStream_t st = as_stream(stream);
     if (proj->n > 0) {
         cudaError_t e = cudaMemsetAsync(grad2d, 0, (size_t)proj->n * 12 * sizeof(float), st);
-        if (e) return cuda_fail(e, "gs_render_bwd: zero grad2d");
+        if (e) return cuda_fail(e, name);
+    }
+    if (loss) {
+        cudaError_t e = cudaMemsetAsync(loss, 0, sizeof(float), st);
+        if (e) return cuda_fail(e, name);
     }
     unsigned* err = error_word(&s);
     if (!err) return s;
-    cudaError_t e = launch_render_bwd(o.bwd_mode, o.staging, o.thr, *proj, vals, tile_ranges, kc, dl_dimage, t_final,
-                                      n_contrib, grad2d, o.spin, err, st);
-    return e ? cuda_fail(e, "gs_render_bwd") : GS_OK;
+    cudaError_t e = launch_render_bwd(o.bwd_mode, o.staging, o.thr, *proj, vals, tile_ranges, kc, src, target, loss,
+                                      t_final, n_contrib, grad2d, o.spin, err, st);
+    return e ? cuda_fail(e, name) : GS_OK;
+}
+
+int gs_render_bwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges, const gs_camera* cam,
+                  const gs_options* opt, const float* dl_dimage, const float* t_final, const uint32_t* n_contrib,
+                  float* grad2d, void* stream) {
+    return render_bwd("gs_render_bwd", proj, vals, tile_ranges, cam, opt, dl_dimage, nullptr, nullptr, t_final,
+                      n_contrib, grad2d, stream);
+}
+
+int gs_render_bwd_sqerr(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges, const gs_camera* cam,
+                        const gs_options* opt, const float* image, const float* target, const float* t_final,
+                        const uint32_t* n_contrib, float* grad2d, float* loss, void* stream) {
+    if (!target) return fail(GS_ERR_ARG, "gs_render_bwd_sqerr: target is NULL");
+    return render_bwd("gs_render_bwd_sqerr", proj, vals, tile_ranges, cam, opt, image, target, loss, t_final,
+                      n_contrib, grad2d, stream);
 }
 
 int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options* opt, const gs_proj* proj,

@@ -93,8 +93,8 @@ cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* 
                               unsigned spin_limit, unsigned* err, cudaStream_t st);
 cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& proj, const unsigned* vals,
                               const unsigned* ranges, const KernelCamera& cam, const float* dl_dimage,
-                              const float* t_final, const unsigned* n_contrib, float* grad2d, unsigned spin_limit,
-                              unsigned* err, cudaStream_t st);
+                              const float* target, float* loss, const float* t_final, const unsigned* n_contrib,
+                              float* grad2d, unsigned spin_limit, unsigned* err, cudaStream_t st);
 
 cudaError_t launch_adam(const gs_tensors& P, const gs_tensors& G, const gs_tensors& M, const gs_tensors& V,
                         const int* radius, const gs_adam_options& o, int deg, float beta1, float beta2, float eps,

@@ -363,38 +363,30 @@ __device__ __forceinline__ float warp_reduce9(const float (&v)[9], int lane, flo
     return x;
 }
 
-// Adds one pixel's contribution to a Gaussian's 9 gradient components and steps the pixel's
-// backward state past that Gaussian: T becomes the transmittance in front of it, gS gains its
-// colour. r0, r1, r2: the prepared record; g0..g2: dL/dpixel.
-__device__ __forceinline__ void add_pixel(float (&v)[9], float alpha, float oG, float G, float dx, float dy, float u,
-                                          const float4& r0, const float4& r1, const float4& r2, float& T, float& gS,
-                                          float g0, float g1, float g2) {
+// Steps one pixel's backward state past a Gaussian it blends (alpha, o G at the pixel): T becomes
+// the transmittance in front of the Gaussian and gS gains its colour (gS = sum over channels of
+// dL/dpixel_c x the colour blended behind, background included). Returns alpha T (the weight of
+// the Gaussian's colour) in aT and dL/dpower in dp (0 where alpha was clamped at 0.99).
+// r1, r2: the prepared record; g0..g2: dL/dpixel.
+__device__ __forceinline__ void pixel_step(float alpha, float oG, const float4& r1, const float4& r2, float& T,
+                                           float& gS, float g0, float g1, float g2, float& aT, float& dp) {
     const float inv = rcp_approx(1.f - alpha);
     T *= inv;
-    const float aT = alpha * T;
-    v[6] = __fmaf_rn(aT, g0, v[6]);
-    v[7] = __fmaf_rn(aT, g1, v[7]);
-    v[8] = __fmaf_rn(aT, g2, v[8]);
+    aT = alpha * T;
     const float gc = __fmaf_rn(g0, r1.z, __fmaf_rn(g1, r1.w, g2 * r2.x));
     const float dalpha = __fmaf_rn(T, gc, -inv * gS);
     gS = __fmaf_rn(aT, gc, gS);
-    if (oG <= kAlphaMax) {
-        const float dpow = oG * dalpha;
-        v[5] = __fmaf_rn(G, dalpha, v[5]);
-        // d power / d mean = -(A dx + B dy, B dx + C dy) = -(A u, B u + D dy)
-        v[0] = __fmaf_rn(-r0.z * u, dpow, v[0]);
-        v[1] = __fmaf_rn(-__fmaf_rn(r0.w, u, r1.x * dy), dpow, v[1]);
-        v[2] = __fmaf_rn(-0.5f * dx * dx, dpow, v[2]);
-        v[3] = __fmaf_rn(-dx * dy, dpow, v[3]);
-        v[4] = __fmaf_rn(-0.5f * dy * dy, dpow, v[4]);
-    }
+    dp = oG <= kAlphaMax ? oG * dalpha : 0.f;
 }
 
+// dl_dimage: dL/dpixel, or with `target` the rendered image, and dL/dpixel = image - target (the
+// gradient of the squared error 0.5 |image - target|^2, whose sum is added to *loss when given).
 template <int MODE, int STAGING>
 __global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restrict__ rec,
                                                           const unsigned* __restrict__ vals,
                                                           const uint2* __restrict__ ranges, const KernelCamera cam,
                                                           unsigned n_gauss, const float* __restrict__ dl_dimage,
+                                                          const float* __restrict__ target, float* __restrict__ loss,
                                                           const float* __restrict__ t_final,
                                                           const unsigned* __restrict__ n_contrib,
                                                           float* __restrict__ grad2d, int thr, unsigned spin_limit,
@@ -428,6 +420,11 @@ __global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restri
         a0 = dl_dimage[pix];
         a1 = dl_dimage[plane + pix];
         a2 = dl_dimage[2 * plane + pix];
+        if (target) {
+            a0 -= target[pix];
+            a1 -= target[plane + pix];
+            a2 -= target[2 * plane + pix];
+        }
     }
     if (px < cam.width && py1 < cam.height) {
         const size_t pix = (size_t)py1 * cam.width + px;
@@ -436,6 +433,17 @@ __global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restri
         b0 = dl_dimage[pix];
         b1 = dl_dimage[plane + pix];
         b2 = dl_dimage[2 * plane + pix];
+        if (target) {
+            b0 -= target[pix];
+            b1 -= target[plane + pix];
+            b2 -= target[2 * plane + pix];
+        }
+    }
+    if (loss) {
+        float l = 0.5f * (__fmaf_rn(a0, a0, __fmaf_rn(a1, a1, a2 * a2)) + __fmaf_rn(b0, b0, __fmaf_rn(b1, b1, b2 * b2)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) red_add_global(loss, l);
     }
     float gS0 = T0 * (a0 * cam.bg[0] + a1 * cam.bg[1] + a2 * cam.bg[2]);
     float gS1 = T1 * (b0 * cam.bg[0] + b1 * cam.bg[1] + b2 * cam.bg[2]);
@@ -500,11 +508,28 @@ __global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restri
             const bool c1 = pos < last1 && alpha1 >= kAlphaMin;
             const unsigned ballot = __ballot_sync(0xffffffffu, c0 || c1);
             if (ballot == 0u) continue;
+            float aT0 = 0.f, dp0 = 0.f, aT1 = 0.f, dp1 = 0.f;
+            if (c0) pixel_step(alpha0, oG0, r1, r2, T0, gS0, a0, a1, a2, aT0, dp0);
+            if (c1) pixel_step(alpha1, oG1, r1, r2, T1, gS1, b0, b1, b2, aT1, dp1);
+            // The lane's sums over its two pixels. The geometric gradients are linear in dL/dpower
+            // with pixel-dependent factors: d power / d mean = -(A u, B u + D dy), d power / d(A, B, C)
+            // = -(dx^2 / 2, dx dy, dy^2 / 2), and both pixels share dx, so the lane forms the moments
+            // P = sum dp, M = sum dp u, F = sum dp dy once and converts them; dL/dopacity =
+            // sum G dL/dalpha = P / o.
+            const float P = dp0 + dp1;
+            const float M = __fmaf_rn(dp0, u0, dp1 * u1);
+            const float f0 = dp0 * dy0, f1 = dp1 * dy1;
+            const float F = f0 + f1;
             float v[9];
-#pragma unroll
-            for (int c = 0; c < 9; ++c) v[c] = 0.f;
-            if (c0) add_pixel(v, alpha0, oG0, G0, dx, dy0, u0, r0, r1, r2, T0, gS0, a0, a1, a2);
-            if (c1) add_pixel(v, alpha1, oG1, G1, dx, dy1, u1, r0, r1, r2, T1, gS1, b0, b1, b2);
+            v[0] = -r0.z * M;
+            v[1] = -__fmaf_rn(r0.w, M, r1.x * F);
+            v[2] = (-0.5f * dx * dx) * P;
+            v[3] = -dx * F;
+            v[4] = -0.5f * __fmaf_rn(f0, dy0, f1 * dy1);
+            v[5] = P * rcp_approx(r1.y);
+            v[6] = __fmaf_rn(aT0, a0, aT1 * b0);
+            v[7] = __fmaf_rn(aT0, a1, aT1 * b1);
+            v[8] = __fmaf_rn(aT0, a2, aT1 * b2);
             const bool contrib = c0 || c1;
             const int nact = __popc(ballot);
             if (MODE == GS_BWD_DIRECT || (MODE == GS_BWD_ADAPTIVE && nact < thr)) {
@@ -573,27 +598,28 @@ cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* 
 
 template <int MODE>
 static cudaError_t launch_bwd_mode(int staging, int tiles, const float4* rec, const unsigned* vals, const uint2* rg,
-                                   const KernelCamera& cam, unsigned n, const float* dl, const float* tf,
-                                   const unsigned* nc, float* g2, int thr, unsigned spin, unsigned* err,
-                                   cudaStream_t st) {
+                                   const KernelCamera& cam, unsigned n, const float* dl, const float* target,
+                                   float* loss, const float* tf, const unsigned* nc, float* g2, int thr, unsigned spin,
+                                   unsigned* err, cudaStream_t st) {
     return launch_pdl(staging == GS_STAGE_LOADS ? k_render_bwd<MODE, GS_STAGE_LOADS> : k_render_bwd<MODE, GS_STAGE_BULK>,
-                      dim3(tiles), dim3(kBwdBlock), 0, st, rec, vals, rg, cam, n, dl, tf, nc, g2, thr, spin, err);
+                      dim3(tiles), dim3(kBwdBlock), 0, st, rec, vals, rg, cam, n, dl, target, loss, tf, nc, g2, thr, spin,
+                      err);
 }
 
 cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& proj, const unsigned* vals,
                               const unsigned* ranges, const KernelCamera& cam, const float* dl_dimage,
-                              const float* t_final, const unsigned* n_contrib, float* grad2d, unsigned spin_limit,
-                              unsigned* err, cudaStream_t st) {
+                              const float* target, float* loss, const float* t_final, const unsigned* n_contrib,
+                              float* grad2d, unsigned spin_limit, unsigned* err, cudaStream_t st) {
     const int tiles = cam.tiles_x * cam.tiles_y;
     const float4* rec = reinterpret_cast<const float4*>(proj.rec);
     const uint2* rg = reinterpret_cast<const uint2*>(ranges);
     const unsigned n = (unsigned)proj.n;
     count_launches(1);
     switch (mode) {
-        case GS_BWD_DIRECT: return launch_bwd_mode<GS_BWD_DIRECT>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
-        case GS_BWD_WARP: return launch_bwd_mode<GS_BWD_WARP>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
-        case GS_BWD_ADAPTIVE: return launch_bwd_mode<GS_BWD_ADAPTIVE>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
-        default: return launch_bwd_mode<GS_BWD_SM>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
+        case GS_BWD_DIRECT: return launch_bwd_mode<GS_BWD_DIRECT>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, target, loss, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
+        case GS_BWD_WARP: return launch_bwd_mode<GS_BWD_WARP>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, target, loss, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
+        case GS_BWD_ADAPTIVE: return launch_bwd_mode<GS_BWD_ADAPTIVE>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, target, loss, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
+        default: return launch_bwd_mode<GS_BWD_SM>(staging, tiles, rec, vals, rg, cam, n, dl_dimage, target, loss, t_final, n_contrib, grad2d, thr, spin_limit, err, st);
     }
 }
 

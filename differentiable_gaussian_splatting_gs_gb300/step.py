@@ -2,10 +2,12 @@
 
 Per view (the phases preprocessing, rendering and backward computation of Odin: Primitive-Level
 Synchronization for Distributed Point-Based Neural Rendering, Figure 7): gs_preprocess,
-gs_bin_and_sort, gs_render_fwd, the loss gradient, gs_render_bwd, gs_preprocess_bwd. The loss is
-the squared error 0.5 |image - target|^2, so dL/dimage = image - target; it is the caller's part
-of the step and is formed here with one torch subtraction. Parameter gradients of the views of
-one step are summed (the first view overwrites, the others accumulate).
+gs_bin_and_sort, gs_render_fwd, gs_render_bwd_sqerr, gs_preprocess_bwd. The loss is the squared
+error 0.5 |image - target|^2; its gradient dL/dimage = image - target is formed by the backward
+kernel itself as it reads the image (gs_render_bwd_sqerr), so every kernel of the step is the
+library's. A caller with its own loss passes its dL/dimage (`upstream`) to gs_render_bwd instead.
+Parameter gradients of the views of one step are summed (the first view overwrites, the others
+accumulate).
 """
 from __future__ import annotations
 
@@ -59,22 +61,22 @@ def train_step(params: dict, cameras, targets, opt, grads: dict, buffers: StepBu
         b = api.gs_bin_and_sort(proj, c, opt, capacity=capacity, buffers=buffers.sort, want_keys=want_keys,
                                 ranges=ranges, stream=stream)
         api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib), stream=stream)
-        torch.sub(image, target, out=dl)
-        api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=buffers.grad2d,
-                          stream=stream)
+        api.gs_render_bwd_sqerr(proj, b.vals, b.ranges, c, opt, image, target, t_final, n_contrib,
+                                grad2d=buffers.grad2d, stream=stream)
         api.gs_preprocess_bwd(params, c, opt, proj, buffers.grad2d, out=grads, accumulate=v > 0, stream=stream)
         n_dups.append(b.n_dup)
     return {"n_dup": n_dups, "image": image}
 
 
 def train_step_async(params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
-                     n_dup: torch.Tensor, events=None, stream=None, upstream=None):
+                     n_dup: torch.Tensor, events=None, stream=None, upstream=None, losses=None):
     """train_step without any host synchronisation: the sort is gs_bin_and_sort_async with a
     fixed capacity, and the views' duplicate counts land in the device tensor n_dup [views]
     (a view whose count exceeds the capacity renders nothing and sets the device check error).
     events: optional per view ((fwd start, fwd end), (bwd start, bwd end)) recorded around the
     two raster kernels (on the current stream). upstream: optional per-view dL/dimage [3, H, W]
-    tensors supplied by the caller (a loss computed elsewhere); the targets are then unused."""
+    tensors supplied by the caller (a loss computed elsewhere); the targets are then unused.
+    losses: optional device float tensor [views] receiving each view's squared-error loss."""
     image = None
     for v, (cam, target) in enumerate(zip(cameras, targets)):
         ev = events[v] if events is not None else None
@@ -88,14 +90,14 @@ def train_step_async(params: dict, cameras, targets, opt, grads: dict, buffers: 
         api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib), stream=stream)
         if ev is not None:
             ev[0][1].record()
-        if upstream is None:
-            torch.sub(image, target, out=dl)
-        else:
-            dl = upstream[v]
-        if ev is not None:
             ev[1][0].record()
-        api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, dl, t_final, n_contrib, grad2d=buffers.grad2d,
-                          stream=stream)
+        if upstream is None:
+            api.gs_render_bwd_sqerr(proj, b.vals, b.ranges, c, opt, image, target, t_final, n_contrib,
+                                    grad2d=buffers.grad2d, loss=losses[v:v + 1] if losses is not None else None,
+                                    stream=stream)
+        else:
+            api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, upstream[v], t_final, n_contrib,
+                              grad2d=buffers.grad2d, stream=stream)
         if ev is not None:
             ev[1][1].record()
         api.gs_preprocess_bwd(params, c, opt, proj, buffers.grad2d, out=grads, accumulate=v > 0, stream=stream)
@@ -145,13 +147,14 @@ class GraphedStep:
         self.device = buffers.device
         self.cams = [c if isinstance(c, api.gs_camera) else api.make_camera(c) for c in cameras]
         self.n_dup = torch.zeros(len(self.cams), dtype=torch.int64, device=self.device)
+        self.losses = torch.zeros(len(self.cams), dtype=torch.float32, device=self.device)  # per view (3D pipeline)
         args = (params, self.cams, targets, opt, grads, buffers, capacity, self.n_dup, events)
         if surfels:
             assert upstream is None, "upstream gradients are supported by the 3D pipeline only"
             run = train_step_surfels_async
         else:
             def run(*a):
-                return train_step_async(*a, upstream=upstream)
+                return train_step_async(*a, upstream=upstream, losses=None if upstream is not None else self.losses)
         # one eager run first: buffers, function attributes and device symbols are set up outside the capture
         side = torch.cuda.Stream(self.device)
         side.wait_stream(torch.cuda.current_stream(self.device))

@@ -196,6 +196,20 @@ int gs_render_bwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* til
                   const gs_camera* cam, const gs_options* opt, const float* dl_dimage,
                   const float* t_final, const uint32_t* n_contrib, float* grad2d, void* stream);
 
+/* gs_render_bwd with the loss folded in: the upstream gradient is that of the squared error
+ * L = 0.5 sum over channels and pixels of (image - target)^2, dL/dimage = image - target, formed
+ * per pixel by the backward kernel as it reads the image (the rendering phase's output feeding the
+ * backward computation, Odin: Primitive-Level Synchronization for Distributed Point-Based Neural
+ * Rendering, Figure 7), instead of a separate pass writing dl_dimage.
+ * image, target: [3][H][W] float32 (image: gs_render_fwd's output); loss: one device float or
+ * NULL, set to L (zeroed and accumulated by the callee; its summation order varies, so it is
+ * reproducible to float32 rounding). Other arguments, outputs and errors as gs_render_bwd;
+ * GS_ERR_ARG when target is NULL.                                                           */
+int gs_render_bwd_sqerr(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges,
+                        const gs_camera* cam, const gs_options* opt, const float* image, const float* target,
+                        const float* t_final, const uint32_t* n_contrib, float* grad2d, float* loss,
+                        void* stream);
+
 /* Preprocessing backward: chain rule from grad2d to the parameters, recomputing the forward of
  * gs_preprocess per Gaussian. Outputs d_mean3d [N][3], d_log_scale [N][3], d_quat [N][4]
  * (through the normalisation), d_opacity_logit [N], d_sh [N][K][3]. Gaussians with radius 0

@@ -218,6 +218,28 @@ def test_render_bwd_matches_oracle(name, mode, staging):
         assert ok, f"unmasked {group}: error {err:.3g} > {tol:.3g}"
 
 
+@pytest.mark.parametrize("mode", ["adaptive", "direct"])
+@pytest.mark.parametrize("name", list(CASES))
+def test_render_bwd_sqerr_matches_oracle(name, mode):
+    """The backward that forms dL/dimage = image - target itself: given the oracle's image (rounded
+    to float32) and the target, with the target set to the image on the flagged pixels (zero
+    gradient there), it matches the oracle's backward at 1e-4 of max and reports the loss
+    0.5 sum (image - target)^2 within 1e-5 relative."""
+    d = stage_inputs(name)
+    proj, b, _, img, tf, nc = _fwd(d, _abi.GS_STAGE_BULK)
+    image32 = d["fwd"]["image"].astype(np.float32)
+    target = np.where(d["fwd"]["pix_flags"][None] != 0, image32, d["scene"].targets[d["view"]]).astype(np.float32)
+    loss = torch.zeros(1, device=DEV)
+    g2 = api.gs_render_bwd_sqerr(proj, b.vals, b.ranges, d["cam"], api.make_options(d["scene"].sh_degree, bwd_mode=mode),
+                                 torch.from_numpy(image32).to(DEV), torch.from_numpy(target).to(DEV), tf, nc,
+                                 loss=loss).cpu().numpy()
+    for group, cols in GRAD2D_GROUPS.items():
+        ok, err, tol = grad_close(g2[:, cols], d["grad2d_masked"][:, cols])
+        assert ok, f"{group}: error {err:.3g} > {tol:.3g}"
+    want = 0.5 * float(((image32.astype(np.float64) - target) ** 2).sum())
+    assert float(loss.item()) == pytest.approx(want, rel=1e-5)
+
+
 @pytest.mark.parametrize("thr", [1, 16, 33])
 def test_adaptive_threshold_extremes(thr):
     d = stage_inputs("contention")
