@@ -29,6 +29,20 @@ constexpr int kSortRounds = 16;                          // rounds of 32 items p
 constexpr int kSortItems = kSortThreads * kSortRounds;  // 4096 items per block
 constexpr int kWarpItems = 32 * kSortRounds;            // 512 items per warp
 
+// Super-tiles: blocks of kSuper x kSuper tiles, the coarse level of the two-level counting pass.
+constexpr int kSuper = 4;
+
+// The rectangle of super-tiles overlapped by a packed tile rectangle (x0 | y0 << 16, w | h << 16),
+// packed the same way; empty stays empty.
+__device__ __forceinline__ uint2 super_rect(uint2 r) {
+    const unsigned w = r.y & 0xffffu, h = r.y >> 16;
+    if (w == 0u || h == 0u) return make_uint2(0u, 0u);
+    const unsigned x0 = r.x & 0xffffu, y0 = r.x >> 16;
+    const unsigned sx0 = x0 / kSuper, sy0 = y0 / kSuper;
+    const unsigned sx1 = (x0 + w - 1u) / kSuper, sy1 = (y0 + h - 1u) / kSuper;
+    return make_uint2(sx0 | (sy0 << 16), (sx1 - sx0 + 1u) | ((sy1 - sy0 + 1u) << 16));
+}
+
 // Number of items of a pass: the host bound n, or the count the previous pass left on the device.
 __device__ __forceinline__ int item_count(int n, const unsigned* n_dev) {
     return n_dev ? min(n, (int)*n_dev) : n;
@@ -440,12 +454,13 @@ __global__ void __launch_bounds__(256) k_count(int n_bound, const unsigned* __re
                                                const unsigned* __restrict__ perm, const float4* __restrict__ rec,
                                                const int* __restrict__ radius, int tiles_x, int tiles_y,
                                                unsigned long long* __restrict__ block_sums,
-                                               uint2* __restrict__ crect) {
+                                               uint2* __restrict__ crect,
+                                               unsigned long long* __restrict__ super_sums) {
     pdl_entry();
-    __shared__ unsigned long long ws[8];
+    __shared__ unsigned long long ws[8], ws2[8];
     const int n = item_count(n_bound, n_dev);
     const int i = blockIdx.x * 256 + threadIdx.x;
-    unsigned long long cnt = 0;
+    unsigned long long cnt = 0, cnt2 = 0;
     if (i < n) {
         const unsigned g = perm[i];
         // an index outside the Gaussians (only after a depth pass whose look-back gave up and set
@@ -462,15 +477,29 @@ __global__ void __launch_bounds__(256) k_count(int n_bound, const unsigned* __re
             }
         }
         if (crect) crect[i] = packed;
+        if (super_sums) {
+            const uint2 sr = super_rect(packed);
+            cnt2 = (unsigned long long)(sr.y & 0xffffu) * (sr.y >> 16);
+        }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = cnt;
+    for (int o = 16; o > 0; o >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        cnt2 += __shfl_xor_sync(0xffffffffu, cnt2, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        ws[threadIdx.x >> 5] = cnt;
+        ws2[threadIdx.x >> 5] = cnt2;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
-        unsigned long long s = 0;
-        for (int w = 0; w < 8; ++w) s += ws[w];
+        unsigned long long s = 0, s2 = 0;
+        for (int w = 0; w < 8; ++w) {
+            s += ws[w];
+            s2 += ws2[w];
+        }
         block_sums[blockIdx.x] = s;
+        if (super_sums) super_sums[blockIdx.x] = s2;
     }
 }
 
@@ -505,11 +534,22 @@ __device__ __forceinline__ T block_scan_1024(T v, T* wsum, T* block_total) {
     return (warp ? wsum[warp - 1] : T(0)) + x - v;
 }
 
-// Exclusive scan of the block sums (single block); total[0] = sum of all.
+// Exclusive scan of m block sums per block of 1024 threads; total[0] = sum of all (and
+// *total_copy when given). Block 1, when launched, scans a second array (in2, out2, total2).
 __global__ void __launch_bounds__(1024) k_scan_u64(const unsigned long long* __restrict__ in, int m,
                                                    unsigned long long* __restrict__ out,
-                                                   unsigned long long* __restrict__ total) {
+                                                   unsigned long long* __restrict__ total,
+                                                   unsigned long long* __restrict__ total_copy,
+                                                   const unsigned long long* __restrict__ in2,
+                                                   unsigned long long* __restrict__ out2,
+                                                   unsigned long long* __restrict__ total2) {
     pdl_entry();
+    if (blockIdx.x == 1) {
+        in = in2;
+        out = out2;
+        total = total2;
+        total_copy = nullptr;
+    }
     __shared__ unsigned long long wsum[32];
     __shared__ unsigned long long round_total;
     unsigned long long carry = 0;
@@ -530,7 +570,10 @@ __global__ void __launch_bounds__(1024) k_scan_u64(const unsigned long long* __r
         carry += round_total;
         __syncthreads();  // wsum and round_total are rewritten by the next round
     }
-    if (threadIdx.x == 0) total[0] = carry;
+    if (threadIdx.x == 0) {
+        total[0] = carry;
+        if (total_copy) *total_copy = carry;
+    }
 }
 
 // Emits the duplicates of 256 consecutive Gaussians (depth order) into their block's contiguous
@@ -626,22 +669,25 @@ __global__ void k_ranges(unsigned d, const unsigned* __restrict__ tiles, uint2* 
 
 // ---- tile pass as one stable counting pass (images of up to kMaxCountTiles tiles) -------------
 //
-// The depth-ordered Gaussians are cut into chunks. For every chunk a shared-memory histogram over
-// the tiles counts the Gaussians whose rectangle covers each tile; a scan down each tile's column
-// of the chunk x tile table gives the chunk's first position inside every tile's list, and the
-// tile totals give the ranges and D. Each chunk then places its entries in depth order (see
-// k_chunk_place). This is the stable counting sort of the duplicates by tile id (an LSD radix pass
-// whose digit is the whole tile id) applied to the depth-ordered list: equal tile ids keep depth
-// order.
+// The tile pass is the stable counting sort of the depth-ordered duplicates by tile id (an LSD
+// radix pass whose digit is the whole tile id): equal tile ids keep depth order. It runs in two
+// levels. The coarse level sorts by super-tile (kSuper x kSuper tiles): the depth-ordered Gaussians
+// are cut into chunks; for every chunk a shared-memory histogram counts the Gaussians whose
+// rectangle of super-tiles covers each super-tile; a scan down each super-tile's column of the
+// chunk x super-tile table gives the chunk's first position inside every super-tile's list; each
+// chunk then places the depth positions of its Gaussians in depth order (k_chunk_place). The fine
+// level (below) sorts each super-tile's list by tile. At the coarse level a Gaussian has few
+// entries (the outdoor scene: 2.1M against 11.6M duplicates; the large scene: 16.6M against
+// 179M), so the scattered placement writes few entries; the fine level writes each tile's entries
+// as coalesced runs.
 //
-// Depth order puts the Gaussians nearest to the camera, which are the largest on screen, first: at
-// the outdoor scene the first 512 of them cover 17x the mean number of tiles. A chunk therefore
-// ends after kChunk Gaussians or about kChunkDup entries, whichever comes first: Gaussian i
-// (depth order, P(i) entries before it) belongs to chunk floor(i / kChunk) + floor(P(i) / kChunkDup),
-// which never decreases with i (ids that are skipped are empty chunks). Within a chunk, rectangles
-// are spread over lanes, and placement splits the chunk into bands of tile rows.
-constexpr int kChunk = 512;             // Gaussians per chunk at most
-constexpr long long kChunkDup = 16384;  // entries after which a chunk ends early
+// Depth order puts the Gaussians nearest to the camera, which are the largest on screen, first. A
+// chunk therefore ends after kChunk Gaussians or about kChunkDup coarse entries, whichever comes
+// first: Gaussian i (depth order, P(i) entries before it) belongs to chunk
+// floor(i / kChunk) + floor(P(i) / kChunkDup), which never decreases with i (ids that are skipped
+// are empty chunks). Within a chunk, rectangles are spread over lanes.
+constexpr int kChunk = 256;            // Gaussians per chunk at most
+constexpr long long kChunkDup = 8192;  // coarse entries after which a chunk ends early
 constexpr int kMaxCountTiles = 49152;   // tile counters that fit in shared memory (192 KB)
 constexpr int kSmallRect = 8;           // rectangles of up to this many tiles: one lane each
 
@@ -674,7 +720,7 @@ __global__ void __launch_bounds__(256) k_chunk_bounds(int n_bound, const unsigne
     const int i = blockIdx.x * 256 + threadIdx.x;
     unsigned long long area = 0;
     if (i < n) {
-        const uint2 r = crect[i];
+        const uint2 r = super_rect(crect[i]);
         area = (unsigned long long)(r.y & 0xffffu) * (r.y >> 16);
     }
     unsigned long long x = area;  // inclusive scan over the block
@@ -696,7 +742,7 @@ __global__ void __launch_bounds__(256) k_chunk_bounds(int n_bound, const unsigne
     if (threadIdx.x > 0) {
         cprev = s_c[threadIdx.x - 1];
     } else if (i > 0) {
-        const uint2 r = crect[i - 1];
+        const uint2 r = super_rect(crect[i - 1]);
         cprev = chunk_of(i - 1, before - (unsigned long long)(r.y & 0xffffu) * (r.y >> 16), cmax);
     }
     for (int k = cprev + 1; k <= c; ++k) chunk_first[k] = (unsigned)i;
@@ -706,7 +752,7 @@ __global__ void __launch_bounds__(256) k_chunk_bounds(int n_bound, const unsigne
     }
 }
 
-// Counts per tile of one chunk (one block per chunk id; ids at or beyond the count return).
+// Counts per super-tile of one chunk (one block per chunk id; ids at or beyond the count return).
 __global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__ nchunks,
                                                     const unsigned* __restrict__ chunk_first,
                                                     const uint2* __restrict__ crect, int tiles_x, int T,
@@ -725,7 +771,7 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__
         const int i = base + lane;
         int x0 = 0, y0 = 0, w = 0, h = 0, area = 0;
         if (i < last) {
-            const uint2 r = crect[i];
+            const uint2 r = super_rect(crect[i]);
             x0 = (int)(r.x & 0xffffu);
             y0 = (int)(r.x >> 16);
             w = (int)(r.y & 0xffffu);
@@ -755,20 +801,28 @@ __global__ void __launch_bounds__(256) k_chunk_hist(const unsigned* __restrict__
     for (int t = threadIdx.x; t < T; t += blockDim.x) row[t] = cnt[t];
 }
 
-// Exclusive scan down each tile's column of the chunk x tile table (in place) and the tile totals.
-// Block: 32 tiles (one per lane) x 32 warps, each warp a contiguous range of chunks.
+// Exclusive scan down each super-tile's column of the chunk x super-tile table (in place) and the
+// column totals, in groups of kScanGroup chunk rows so that tables with many rows and few columns
+// still spread over many blocks: k_chunk_colsum sums each group's rows per column, and
+// k_chunk_scan scans each group's rows starting from the sum of the groups before it.
+// Blocks: 32 columns (one per lane) x 32 warps, each warp a contiguous range of the group's rows;
+// blockIdx.y is the group (groups past the used rows return).
 constexpr int kScanWarps = 32;
-constexpr int kColUnroll = 16;  // table loads in flight per lane
-__global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* __restrict__ nchunks, int T,
-                                                                unsigned* __restrict__ table,
-                                                                unsigned* __restrict__ tile_total) {
+constexpr int kColUnroll = 16;   // table loads in flight per lane
+constexpr int kScanGroup = 512;  // chunk rows per group
+
+__global__ void __launch_bounds__(32 * kScanWarps) k_chunk_colsum(const unsigned* __restrict__ nchunks, int T,
+                                                                  const unsigned* __restrict__ table,
+                                                                  unsigned* __restrict__ group_sum) {
     pdl_entry();
     __shared__ unsigned part[kScanWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = blockIdx.x * 32 + lane;
-    const int nc = (int)*nchunks;
-    const int per = (nc + kScanWarps - 1) / kScanWarps;
-    const int c0 = min(nc, warp * per), c1 = min(nc, c0 + per);
+    const int nc = (int)*nchunks, g0 = blockIdx.y * kScanGroup;
+    if (g0 >= nc) return;
+    const int g1 = min(nc, g0 + kScanGroup);
+    const int per = (g1 - g0 + kScanWarps - 1) / kScanWarps;
+    const int c0 = min(g1, g0 + warp * per), c1 = min(g1, c0 + per);
     unsigned sum = 0;
     if (t < T) {
         int c = c0;
@@ -783,7 +837,45 @@ __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* 
     }
     part[warp][lane] = sum;
     __syncthreads();
-    unsigned run = 0;
+    if (warp == 0 && t < T) {
+        unsigned total = 0;
+        for (int w = 0; w < kScanWarps; ++w) total += part[w][lane];
+        group_sum[(size_t)blockIdx.y * T + t] = total;
+    }
+}
+
+__global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* __restrict__ nchunks, int T,
+                                                                unsigned* __restrict__ table,
+                                                                const unsigned* __restrict__ group_sum,
+                                                                unsigned* __restrict__ tile_total) {
+    pdl_entry();
+    __shared__ unsigned part[kScanWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * 32 + lane;
+    const int nc = (int)*nchunks, g0 = blockIdx.y * kScanGroup;
+    const bool last = g0 + kScanGroup >= nc;  // the group that writes the column totals
+    if (g0 >= nc && blockIdx.y != 0) return;  // group 0 runs even without rows: zero totals
+    const int g1 = min(nc, g0 + kScanGroup);
+    const int per = (max(g1 - g0, 0) + kScanWarps - 1) / kScanWarps;
+    const int c0 = min(g1, g0 + warp * per), c1 = min(g1, c0 + per);
+    unsigned carry = 0;  // the groups before this one
+    if (t < T)
+        for (int g = 0; g < (int)blockIdx.y; ++g) carry += group_sum[(size_t)g * T + t];
+    unsigned sum = 0;
+    if (t < T) {
+        int c = c0;
+        for (; c + kColUnroll <= c1; c += kColUnroll) {
+            unsigned v[kColUnroll];
+#pragma unroll
+            for (int k = 0; k < kColUnroll; ++k) v[k] = table[(size_t)(c + k) * T + t];
+#pragma unroll
+            for (int k = 0; k < kColUnroll; ++k) sum += v[k];
+        }
+        for (; c < c1; ++c) sum += table[(size_t)c * T + t];
+    }
+    part[warp][lane] = sum;
+    __syncthreads();
+    unsigned run = carry;
     for (int w = 0; w < warp; ++w) run += part[w][lane];
     if (t < T) {
         int c = c0;
@@ -803,7 +895,7 @@ __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* 
             *e = run;
             run += v;
         }
-        if (warp == kScanWarps - 1) tile_total[t] = run;
+        if (last && warp == kScanWarps - 1) tile_total[t] = run;
     }
 }
 
@@ -851,22 +943,23 @@ __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __res
     }
 }
 
-// Placement: one warp per (chunk, band of tile rows). The warp copies the chunk's starting offset
-// inside each of the band's tiles into shared memory, then walks the chunk's Gaussians in depth
-// order; for each one whose rectangle meets the band, its lanes cover the rectangle's tiles inside
-// the band (distinct tiles, so no two lanes share an offset) and append the Gaussian there. Entries
-// therefore land in depth order within every tile; bands own disjoint tiles. Two consecutive
-// Gaussians whose rectangles in the band are disjoint and small (at most 16 tiles each) are placed
-// in the same step, one per half-warp: they share no tile, so their order does not matter. Chunks
-// end after about 16k entries, so a warp never walks more than a bounded amount of work.
+// Coarse placement: one warp per (chunk, band of super-tile rows). The warp copies the chunk's
+// starting offset inside each of the band's super-tiles into shared memory, then walks the chunk's
+// Gaussians in depth order; for each one whose rectangle of super-tiles meets the band, its lanes
+// cover the rectangle's super-tiles inside the band (distinct super-tiles, so no two lanes share an
+// offset) and append the Gaussian's depth position there (the fine level reads its tile rectangle
+// from it). Entries therefore land in depth order within every super-tile; bands own disjoint
+// super-tiles. Two consecutive Gaussians whose rectangles in the band are disjoint and small (at
+// most 16 super-tiles each) are placed in the same step, one per half-warp: they share no
+// super-tile, so their order does not matter. Chunks end after about kChunkDup entries, so a warp
+// never walks more than a bounded amount of work. tiles_x, tiles_y count super-tiles here.
 constexpr int kPlaceWarps = 8;        // warps per block when shared memory allows
-constexpr int kPlaceBands = 8;        // bands per chunk (whole tile rows)
+constexpr int kPlaceBands = 2;        // bands per chunk (whole super-tile rows)
 
 __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
-    const unsigned* __restrict__ nchunks, const unsigned* __restrict__ chunk_first, const unsigned* __restrict__ perm,
-    const uint2* __restrict__ crect, int tiles_x, int tiles_y, int band_rows, int nbands,
-    const unsigned* __restrict__ table, const unsigned* __restrict__ tile_start, unsigned capacity,
-    unsigned* __restrict__ vals, unsigned long long* __restrict__ keys64, const unsigned* __restrict__ depth_bits,
+    const unsigned* __restrict__ nchunks, const unsigned* __restrict__ chunk_first, const uint2* __restrict__ crect,
+    int tiles_x, int tiles_y, int band_rows, int nbands, const unsigned* __restrict__ table,
+    const unsigned* __restrict__ tile_start, unsigned capacity, unsigned* __restrict__ vals,
     unsigned* __restrict__ err) {
     pdl_entry();
     extern __shared__ unsigned smem_off[];
@@ -877,7 +970,7 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
     if (chunk >= (int)*nchunks) return;
     const int first = (int)chunk_first[chunk], last = (int)chunk_first[chunk + 1];
     if (first >= last) return;
-    const int T = tiles_x * tiles_y;
+    const int T = tiles_x * tiles_y;  // super-tiles
     const int r0 = band * band_rows, r1 = min(r0 + band_rows, tiles_y);
     if (r0 >= r1) return;
     const int tb0 = r0 * tiles_x, ntb = (r1 - r0) * tiles_x;
@@ -889,8 +982,8 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
     unsigned g_next = 0u;
     uint2 r_next = make_uint2(0u, 0u);
     if (first + lane < last) {
-        g_next = perm[first + lane];
-        r_next = crect[first + lane];
+        g_next = (unsigned)(first + lane);
+        r_next = super_rect(crect[first + lane]);
     }
     for (int base = first; base < last; base += 32) {
         const unsigned g = g_next;
@@ -899,8 +992,8 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
         g_next = 0u;
         r_next = make_uint2(0u, 0u);
         if (nx < last) {
-            g_next = perm[nx];
-            r_next = crect[nx];
+            g_next = (unsigned)nx;
+            r_next = super_rect(crect[nx]);
         }
         // this lane's Gaussian inside the band: columns [x0, x0 + w), rows [ya, yb) (band-local)
         const unsigned w = pr.y & 0xffffu;
@@ -942,12 +1035,241 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
                 off[tl] = pos + 1u;
                 if (pos < capacity) {
                     vals[pos] = jg;
-                    if (keys64) keys64[pos] = ((unsigned long long)(tb0 + tl) << 32) | depth_bits[jg];
                 } else {
                     atomicOr(err, kErrCheck);
                 }
             }
             __syncwarp();
+        }
+    }
+}
+
+// ---- fine level of the two-level counting pass -------------------------------------------------
+//
+// The coarse level (the chunk kernels above run on super-tiles) places, for every super-tile, the
+// depth positions of the Gaussians whose rectangle meets it, in depth order. The fine level splits
+// each super-tile's list into segments of kSeg entries. Per segment it counts, for each of the
+// super-tile's kSuper x kSuper tiles, the entries whose tile rectangle covers the tile; a scan down
+// each super-tile's segments gives every segment's first position inside each tile's list; each
+// segment then places its entries round by round (32 entries, one per lane): per covered tile the
+// lanes whose Gaussian covers it write consecutive positions of the tile's list, one coalesced
+// run. Segments, rounds and lanes follow the coarse list, so each tile's entries stay in depth
+// order: the result is the same stable counting pass by tile id.
+constexpr int kSeg = 256;                      // coarse entries per segment
+constexpr int kRounds = kSeg / 32;             // rounds of 32 entries per segment
+constexpr int kSuperTiles = kSuper * kSuper;   // tiles per super-tile
+static_assert(kSuper == 4, "cover_mask packs a super-tile's tiles as 4 bits per row");
+
+// Bit 4 ly + lx set when the packed tile rectangle r covers tile (tx0 + lx, ty0 + ly).
+__device__ __forceinline__ unsigned cover_mask(uint2 r, int tx0, int ty0) {
+    const int w = (int)(r.y & 0xffffu), h = (int)(r.y >> 16);
+    const int x0 = (int)(r.x & 0xffffu) - tx0, y0 = (int)(r.x >> 16) - ty0;
+    const int ax0 = max(x0, 0), ax1 = min(x0 + w, kSuper), ay0 = max(y0, 0), ay1 = min(y0 + h, kSuper);
+    if (ax0 >= ax1 || ay0 >= ay1) return 0u;
+    const unsigned row = ((1u << ax1) - 1u) & ~((1u << ax0) - 1u);
+    const unsigned col = 0x1111u & ((1u << (4 * ay1)) - 1u) & ~((1u << (4 * ay0)) - 1u);
+    return row * col;  // the row pattern repeated in every covered row's nibble
+}
+
+// Segments of the super-tiles' coarse lists: super-tile s has ceil(len_s / kSeg) of them,
+// numbered from seg_first[s]; seg_first[Ts] and *nseg = their number (clamped to seg_cap).
+// One block of 1024 threads.
+__global__ void __launch_bounds__(1024) k_seg_scan(int Ts, const uint2* __restrict__ crange,
+                                                   unsigned* __restrict__ seg_first, unsigned* __restrict__ nseg,
+                                                   unsigned seg_cap) {
+    pdl_entry();
+    __shared__ unsigned wsum[32];
+    __shared__ unsigned round_total;
+    unsigned carry = 0;
+    for (int base = 0; base < Ts; base += 1024 * kScanItems) {
+        const int s0 = base + threadIdx.x * kScanItems;
+        unsigned v[kScanItems], sum = 0;
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            unsigned c = 0;
+            if (s0 + k < Ts) {
+                const uint2 rg = crange[s0 + k];
+                c = rg.y > rg.x ? (rg.y - rg.x + kSeg - 1) / kSeg : 0u;
+            }
+            v[k] = c;
+            sum += c;
+        }
+        unsigned run = carry + block_scan_1024(sum, wsum, &round_total);
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            if (s0 + k < Ts) seg_first[s0 + k] = run;
+            run += v[k];
+        }
+        carry += round_total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        seg_first[Ts] = carry;
+        *nseg = min(carry, seg_cap);
+    }
+}
+
+// The super-tile of segment k: the last s with first[s] <= k (first[] in shared memory).
+__device__ __forceinline__ int segment_tile(const unsigned* first, int Ts, unsigned k) {
+    int lo = 0, hi = Ts;  // first[lo] <= k < first[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (first[mid] <= k) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Per segment (one warp, grid-stride over the segments): F[k][t] = the number of segment k's
+// entries whose tile rectangle covers tile t of its super-tile. Dynamic shared memory holds
+// seg_first[0..Ts].
+__global__ void __launch_bounds__(256) k_fine_count(int Ts, int SX, unsigned n_bound,
+                                                    const unsigned* __restrict__ seg_first,
+                                                    const unsigned* __restrict__ nseg,
+                                                    const uint2* __restrict__ crange,
+                                                    const unsigned* __restrict__ cvals,
+                                                    const uint2* __restrict__ crect, unsigned* __restrict__ F) {
+    pdl_entry();
+    extern __shared__ unsigned s_first[];
+    for (int t = threadIdx.x; t <= Ts; t += blockDim.x) s_first[t] = seg_first[t];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const unsigned ns = *nseg, wpb = blockDim.x >> 5;
+    for (unsigned k = blockIdx.x * wpb + (threadIdx.x >> 5); k < ns; k += gridDim.x * wpb) {
+        const int st = segment_tile(s_first, Ts, k);
+        const uint2 rg = crange[st];
+        const unsigned p0 = rg.x + (k - s_first[st]) * kSeg, p1 = min(p0 + kSeg, rg.y);
+        const int tx0 = (st % SX) * kSuper, ty0 = (st / SX) * kSuper;
+        // all of the segment's entries are loaded first (kRounds independent loads per lane, then
+        // their rectangles), so the latencies overlap instead of adding up round by round
+        unsigned m16[kRounds];
+        {
+            unsigned iv[kRounds];
+#pragma unroll
+            for (int r = 0; r < kRounds; ++r) iv[r] = p0 + 32 * r + lane < p1 ? cvals[p0 + 32 * r + lane] : ~0u;
+#pragma unroll
+            for (int r = 0; r < kRounds; ++r)  // a depth position below V <= n
+                m16[r] = iv[r] < n_bound ? cover_mask(crect[iv[r]], tx0, ty0) : 0u;
+        }
+        unsigned cnt = 0;  // lane t < 16: tile t
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+            const unsigned any = __reduce_or_sync(0xffffffffu, m16[r]);
+#pragma unroll
+            for (int t = 0; t < kSuperTiles; ++t) {
+                if (any & (1u << t)) {  // warp-uniform
+                    const unsigned c = __popc(__ballot_sync(0xffffffffu, (m16[r] >> t) & 1u));
+                    if (lane == t) cnt += c;
+                }
+            }
+        }
+        if (lane < kSuperTiles) F[(size_t)k * kSuperTiles + lane] = cnt;
+    }
+}
+
+// Per super-tile (one warp, grid-stride): for each of its tiles t (lanes t and t + 16 take the first
+// and second half of the segments), the exclusive scan of F[k][t] down the super-tile's segments
+// (in place) and the tile's total tile_total[tile] (every tile of the image is written).
+__global__ void __launch_bounds__(256) k_fine_scan(int Ts, int SX, int tiles_x, int tiles_y,
+                                                   const unsigned* __restrict__ seg_first, unsigned seg_cap,
+                                                   unsigned* __restrict__ F, unsigned* __restrict__ tile_total) {
+    pdl_entry();
+    const int lane = threadIdx.x & 31, t = lane & (kSuperTiles - 1), half = lane >> 4;
+    const unsigned wpb = blockDim.x >> 5;
+    for (unsigned st = blockIdx.x * wpb + (threadIdx.x >> 5); st < (unsigned)Ts; st += gridDim.x * wpb) {
+        const unsigned k0 = min(seg_first[st], seg_cap), k1 = min(seg_first[st + 1], seg_cap);
+        const unsigned mid = k0 + (k1 - k0 + 1u) / 2u;
+        const unsigned a = half ? mid : k0, b = half ? k1 : mid;
+        unsigned sum = 0;
+#pragma unroll 4
+        for (unsigned k = a; k < b; ++k) sum += F[(size_t)k * kSuperTiles + t];
+        const unsigned first_half = __shfl_sync(0xffffffffu, sum, t);
+        unsigned run = half ? first_half : 0u;
+        for (unsigned k = a; k < b; ++k) {
+            unsigned* e = &F[(size_t)k * kSuperTiles + t];
+            const unsigned v = *e;
+            *e = run;
+            run += v;
+        }
+        const int tx = (int)(st % SX) * kSuper + (t & 3), ty = (int)(st / SX) * kSuper + (t >> 2);
+        if (half && tx < tiles_x && ty < tiles_y) tile_total[ty * tiles_x + tx] = run;
+    }
+}
+
+// Per segment (one warp, grid-stride): places the segment's entries. Every lane keeps the next
+// position of each of the 16 tiles (the same values in all lanes); per round and per tile that some
+// lane's Gaussian covers, those lanes write consecutive positions (their rank among the covering
+// lanes) and the tile's position advances. The tile loop is unrolled so that the 16 positions stay
+// in registers and the tiles' updates are independent of one another.
+__global__ void __launch_bounds__(256) k_fine_place(int Ts, int SX, int tiles_x, int tiles_y, unsigned n_bound,
+                                                    const unsigned* __restrict__ seg_first,
+                                                    const unsigned* __restrict__ nseg,
+                                                    const uint2* __restrict__ crange,
+                                                    const unsigned* __restrict__ cvals,
+                                                    const uint2* __restrict__ crect, const unsigned* __restrict__ perm,
+                                                    const unsigned* __restrict__ F,
+                                                    const unsigned* __restrict__ tile_start, unsigned capacity,
+                                                    unsigned* __restrict__ vals, unsigned long long* __restrict__ keys64,
+                                                    const unsigned* __restrict__ depth_bits,
+                                                    unsigned* __restrict__ err) {
+    pdl_entry();
+    extern __shared__ unsigned s_first[];
+    for (int t = threadIdx.x; t <= Ts; t += blockDim.x) s_first[t] = seg_first[t];
+    __syncthreads();
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const unsigned ns = *nseg, wpb = blockDim.x >> 5;
+    for (unsigned k = blockIdx.x * wpb + (threadIdx.x >> 5); k < ns; k += gridDim.x * wpb) {
+        const int st = segment_tile(s_first, Ts, k);
+        const uint2 rg = crange[st];
+        const unsigned p0 = rg.x + (k - s_first[st]) * kSeg, p1 = min(p0 + kSeg, rg.y);
+        const int tx0 = (st % SX) * kSuper, ty0 = (st / SX) * kSuper;
+        unsigned mine_start = 0;  // lane t < 16: first position of tile t for this segment
+        {
+            const int tx = tx0 + (lane & 3), ty = ty0 + ((lane >> 2) & 3);
+            if (lane < kSuperTiles && tx < tiles_x && ty < tiles_y)
+                mine_start = tile_start[ty * tiles_x + tx] + F[(size_t)k * kSuperTiles + lane];
+        }
+        unsigned next[kSuperTiles];
+#pragma unroll
+        for (int t = 0; t < kSuperTiles; ++t) next[t] = __shfl_sync(full, mine_start, t);
+        // all of the segment's entries are loaded first (see k_fine_count)
+        unsigned m16v[kRounds], gv[kRounds];
+        {
+            unsigned iv[kRounds];
+#pragma unroll
+            for (int r = 0; r < kRounds; ++r) iv[r] = p0 + 32 * r + lane < p1 ? cvals[p0 + 32 * r + lane] : ~0u;
+#pragma unroll
+            for (int r = 0; r < kRounds; ++r) {  // a depth position below V <= n
+                const bool ok = iv[r] < n_bound;
+                m16v[r] = ok ? cover_mask(crect[iv[r]], tx0, ty0) : 0u;
+                gv[r] = ok ? perm[iv[r]] : 0u;
+            }
+        }
+        const unsigned lt = lanemask_lt();
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+            const unsigned m16 = m16v[r], g = gv[r];
+            const unsigned any = __reduce_or_sync(full, m16);
+#pragma unroll
+            for (int t = 0; t < kSuperTiles; ++t) {
+                if (any & (1u << t)) {  // warp-uniform
+                    const bool mine = (m16 >> t) & 1u;
+                    const unsigned m = __ballot_sync(full, mine);
+                    if (mine) {
+                        const unsigned pos = next[t] + __popc(m & lt);
+                        if (pos < capacity) {
+                            vals[pos] = g;
+                            if (keys64) {
+                                const unsigned tile = (unsigned)((ty0 + (t >> 2)) * tiles_x + tx0 + (t & 3));
+                                keys64[pos] = ((unsigned long long)tile << 32) | depth_bits[g];
+                            }
+                        } else {
+                            atomicOr(err, kErrCheck);
+                        }
+                    }
+                    next[t] += __popc(m);
+                }
+            }
         }
     }
 }
@@ -1003,8 +1325,9 @@ int tile_bits_of(long long tiles) {
 
 bool counting_path(long long tiles) { return tiles <= kMaxCountTiles; }
 
-SortWorkspace carve_workspace(void* base, long long n, long long cap, long long tiles) {
+SortWorkspace carve_workspace(void* base, long long n, long long cap, int tiles_x, int tiles_y) {
     SortWorkspace w{};
+    const long long tiles = (long long)tiles_x * tiles_y;
     char* p = static_cast<char*>(base);
     size_t off = 0;
     auto take = [&](size_t bytes) { char* q = p ? p + off : nullptr; off += align256(bytes); return q; };
@@ -1027,14 +1350,26 @@ SortWorkspace carve_workspace(void* base, long long n, long long cap, long long 
     w.bsum = (unsigned long long*)take(8 * gblocks);
     w.boff = (unsigned long long*)take(8 * gblocks);
     if (counting) {
+        const long long ts = (long long)((tiles_x + kSuper - 1) / kSuper) * ((tiles_y + kSuper - 1) / kSuper);
         w.cmax = max_chunks(nn, cc);
-        w.table = (unsigned*)take((size_t)w.cmax * tt * 4);
         w.crect = (uint2*)take(8 * nn);
-        w.tile_total = (unsigned*)take(4 * tt);
-        w.tile_start = (unsigned*)take(4 * tt);
+        w.ssum = (unsigned long long*)take(8 * gblocks);
+        w.soff = (unsigned long long*)take(8 * gblocks);
+        w.ctotal = (unsigned long long*)take(8);
+        w.table = (unsigned*)take((size_t)w.cmax * ts * 4);
+        w.group_sum = (unsigned*)take((size_t)((w.cmax + kScanGroup - 1) / kScanGroup) * ts * 4);
+        w.stile_total = (unsigned*)take(4 * ts);
+        w.stile_start = (unsigned*)take(4 * ts);
+        w.crange = (uint2*)take(8 * ts);
+        w.cvals = (unsigned*)take(4 * cc);
         w.chunk_first = (unsigned*)take(4 * (w.cmax + 1));
         w.nchunks = (unsigned*)take(4);
-        w.dsum = (unsigned long long*)take(8);
+        w.seg_cap = cc / kSeg + ts + 1;
+        w.seg_first = (unsigned*)take(4 * (ts + 1));
+        w.nseg = (unsigned*)take(4);
+        w.fcount = (unsigned*)take((size_t)w.seg_cap * kSuperTiles * 4);
+        w.tile_total = (unsigned*)take(4 * tt);
+        w.tile_start = (unsigned*)take(4 * tt);
     } else {
         w.tA = (unsigned*)take(4 * cc);
         w.tB = (unsigned*)take(4 * cc);
@@ -1110,53 +1445,92 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
     const float4* rec = reinterpret_cast<const float4*>(proj.rec);
     const int gblocks = (n + 255) / 256;
     if (counting_path(T)) {
-        const size_t smem = (size_t)T * 4;
+        // duplicate total D (fine), then the coarse level's counts, offsets and super-tile ranges
+        const int sx = (tiles_x + kSuper - 1) / kSuper, sy = (tiles_y + kSuper - 1) / kSuper, ts = sx * sy;
+        const size_t smem = (size_t)ts * 4;
         if ((e = cudaFuncSetAttribute(k_chunk_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return e;
-        count_launches(6);
+        count_launches(7);
         if ((e = launch_pdl(k_count, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.dvB, rec, proj.radius, tiles_x,
-                            tiles_y, w.bsum, w.crect)))
+                            tiles_y, w.bsum, w.crect, w.ssum)))
             return e;
-        if ((e = launch_pdl(k_scan_u64, dim3(1), dim3(1024), 0, st, w.bsum, gblocks, w.boff, w.dsum))) return e;
-        if ((e = launch_pdl(k_chunk_bounds, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.crect, w.boff, (int)w.cmax,
-                            w.chunk_first, w.nchunks)))
+        if ((e = launch_pdl(k_scan_u64, dim3(2), dim3(1024), 0, st, w.bsum, gblocks, w.boff, w.total, total_copy,
+                            (const unsigned long long*)w.ssum, w.soff, w.ctotal)))
             return e;
-        if ((e = launch_pdl(k_chunk_hist, dim3((unsigned)w.cmax), dim3(256), smem, st, w.nchunks, w.chunk_first,
-                            w.crect, tiles_x, T, w.table)))
+        if ((e = launch_pdl(k_chunk_bounds, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.crect, w.soff,
+                            (int)w.cmax, w.chunk_first, w.nchunks)))
             return e;
-        if ((e = launch_pdl(k_chunk_scan, dim3((T + 31) / 32), dim3(32 * kScanWarps), 0, st, w.nchunks, T, w.table,
-                            w.tile_total)))
+        if ((e = launch_pdl(k_chunk_hist, dim3((unsigned)w.cmax), dim3(256), smem, st, w.nchunks,
+                            w.chunk_first, w.crect, sx, ts, w.table)))
             return e;
-        return launch_pdl(k_tile_scan, dim3(1), dim3(1024), 0, st, T, w.tile_total, w.tile_start, w.total, capacity,
-                          reinterpret_cast<uint2*>(ranges), overflow_err, total_copy);
+        const unsigned groups = (unsigned)((w.cmax + kScanGroup - 1) / kScanGroup);
+        if ((e = launch_pdl(k_chunk_colsum, dim3((ts + 31) / 32, groups), dim3(32 * kScanWarps), 0, st, w.nchunks,
+                            ts, (const unsigned*)w.table, w.group_sum)))
+            return e;
+        if ((e = launch_pdl(k_chunk_scan, dim3((ts + 31) / 32, groups), dim3(32 * kScanWarps), 0, st, w.nchunks, ts,
+                            w.table, (const unsigned*)w.group_sum, w.stile_total)))
+            return e;
+        // the coarse lists hold at most D' <= D entries: over the capacity only when D is
+        return launch_pdl(k_tile_scan, dim3(1), dim3(1024), 0, st, ts, w.stile_total, w.stile_start, w.ctotal,
+                          capacity, reinterpret_cast<uint2*>(w.crange), overflow_err,
+                          (unsigned long long*)nullptr);
     }
     count_launches(2);
     if ((e = launch_pdl(k_count, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y,
-                        w.bsum, (uint2*)nullptr)))
+                        w.bsum, (uint2*)nullptr, (unsigned long long*)nullptr)))
         return e;
-    return launch_pdl(k_scan_u64, dim3(1), dim3(1024), 0, st, w.bsum, gblocks, w.boff, w.total);
+    return launch_pdl(k_scan_u64, dim3(1), dim3(1024), 0, st, w.bsum, gblocks, w.boff, w.total,
+                      (unsigned long long*)nullptr, (const unsigned long long*)nullptr, (unsigned long long*)nullptr,
+                      (unsigned long long*)nullptr);
 }
 
-// Counting-path emission: the placement of every entry (the tile ranges were written by the tile
-// scan). Reads no count on the host (the number of chunks and the total stay on the device).
+// Counting-path emission: the coarse placement, the fine counts and scans, the tile ranges and the
+// fine placement. Reads no count on the host (every count stays on the device).
 static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, unsigned long long capacity,
-                                 const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* err,
-                                 cudaStream_t st) {
+                                 const SortWorkspace& w, uint64_t* keys, unsigned* vals, unsigned* ranges,
+                                 unsigned* err, cudaStream_t st) {
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
+    const int sx = (tiles_x + kSuper - 1) / kSuper, sy = (tiles_y + kSuper - 1) / kSuper, ts = sx * sy;
+    const int T = tiles_x * tiles_y;
     cudaError_t e;
-    const int band_rows = (tiles_y + kPlaceBands - 1) / kPlaceBands;
-    const int nbands = (tiles_y + band_rows - 1) / band_rows;
-    const size_t band_bytes = (size_t)band_rows * tiles_x * 4;
+    // coarse placement: one warp per (chunk, band of super-tile rows)
+    const int band_rows = (sy + kPlaceBands - 1) / kPlaceBands;
+    const int nbands = (sy + band_rows - 1) / band_rows;
+    const size_t band_bytes = (size_t)band_rows * sx * 4;
     int wpb = (int)((200 * 1024) / band_bytes);
     wpb = wpb < 1 ? 1 : (wpb > kPlaceWarps ? kPlaceWarps : wpb);
     const size_t smem = (size_t)wpb * band_bytes;
-    if ((e = cudaFuncSetAttribute(k_chunk_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))) return e;
+    if ((e = cudaFuncSetAttribute(k_chunk_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        return e;
+    const size_t fsmem = (size_t)(ts + 1) * 4;
+    if ((e = cudaFuncSetAttribute(k_fine_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem))) return e;
+    if ((e = cudaFuncSetAttribute(k_fine_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem))) return e;
     const long long warps = w.cmax * nbands;
-    count_launches(1);
-    return launch_pdl(k_chunk_place, dim3((unsigned)((warps + wpb - 1) / wpb)), dim3(32 * wpb), smem, st, w.nchunks,
-                      w.chunk_first, w.dvB, w.crect, tiles_x, tiles_y, band_rows, nbands, w.table, w.tile_start,
-                      (unsigned)capacity, vals, k64, depth_bits, err);
+    count_launches(6);
+    if ((e = launch_pdl(k_chunk_place, dim3((unsigned)((warps + wpb - 1) / wpb)), dim3(32 * wpb), smem, st,
+                        w.nchunks, w.chunk_first, w.crect, sx, sy, band_rows, nbands, w.table, w.stile_start,
+                        (unsigned)capacity, w.cvals, err)))
+        return e;
+    if ((e = launch_pdl(k_seg_scan, dim3(1), dim3(1024), 0, st, ts, reinterpret_cast<const uint2*>(w.crange),
+                        w.seg_first, w.nseg, (unsigned)w.seg_cap)))
+        return e;
+    // grid-stride kernels over the segments: at most 8 resident blocks of 8 warps per SM
+    const long long seg_blocks = (w.seg_cap + 7) / 8;
+    const unsigned fblocks = (unsigned)(seg_blocks < 152 * 8 ? seg_blocks : 152 * 8);
+    if ((e = launch_pdl(k_fine_count, dim3(fblocks), dim3(256), fsmem, st, ts, sx, (unsigned)proj.n, w.seg_first,
+                        w.nseg, reinterpret_cast<const uint2*>(w.crange), w.cvals, w.crect, w.fcount)))
+        return e;
+    if ((e = launch_pdl(k_fine_scan, dim3((unsigned)((ts + 7) / 8)), dim3(256), 0, st, ts, sx, tiles_x, tiles_y,
+                        w.seg_first, (unsigned)w.seg_cap, w.fcount, w.tile_total)))
+        return e;
+    if ((e = launch_pdl(k_tile_scan, dim3(1), dim3(1024), 0, st, T, w.tile_total, w.tile_start, w.total, capacity,
+                        reinterpret_cast<uint2*>(ranges), err, (unsigned long long*)nullptr)))
+        return e;
+    return launch_pdl(k_fine_place, dim3(fblocks), dim3(256), fsmem, st, ts, sx, tiles_x, tiles_y,
+                      (unsigned)proj.n, w.seg_first,
+                      w.nseg, reinterpret_cast<const uint2*>(w.crange), w.cvals, w.crect, w.dvB, w.fcount,
+                      w.tile_start, (unsigned)capacity, vals, k64, depth_bits, err);
 }
 
 // Phase 2: placement (counting pass) or emission + tile radix passes and the ranges.
@@ -1173,7 +1547,7 @@ cudaError_t bin_emit_sort(const gs_proj& proj, int tiles_x, int tiles_y, unsigne
     }
     const unsigned* depth_bits = reinterpret_cast<const unsigned*>(proj.depth);
     unsigned long long* k64 = reinterpret_cast<unsigned long long*>(keys);
-    if (counting_path(T)) return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, err, st);
+    if (counting_path(T)) return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, ranges, err, st);
     const int tb = tile_bits_of(T);
     const int passes = (tb + 7) / 8;
     unsigned* tbuf[2] = {w.tA, w.tB};
@@ -1215,7 +1589,7 @@ cudaError_t bin_sort_async(const gs_proj& proj, int tiles_x, int tiles_y, unsign
         if ((e = cudaMemsetAsync(ranges, 0, (size_t)T * 8, st))) return e;
         return n_dup_dev ? cudaMemsetAsync(n_dup_dev, 0, 8, st) : cudaSuccess;
     }
-    return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, err, st);
+    return emit_counting(proj, tiles_x, tiles_y, capacity, w, keys, vals, ranges, err, st);
 }
 
 }  // namespace gs

@@ -248,8 +248,7 @@ int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* op
 
 size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32_t height) {
     if (n < 0 || capacity < 0 || width <= 0 || height <= 0) return 0;
-    const long long tiles = (long long)((width + kTile - 1) / kTile) * ((height + kTile - 1) / kTile);
-    return carve_workspace(nullptr, n, capacity, tiles).bytes;
+    return carve_workspace(nullptr, n, capacity, (width + kTile - 1) / kTile, (height + kTile - 1) / kTile).bytes;
 }
 
 int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options* opt, void* workspace,
@@ -265,10 +264,10 @@ int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options*
     if (capacity > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
     if (keys && !aligned(keys, 8)) return fail(GS_ERR_ARG, "keys not 8-byte aligned");
     const long long tiles = (long long)kc.tiles_x * kc.tiles_y;
-    const size_t need = carve_workspace(nullptr, proj->n, capacity, tiles).bytes;
+    const size_t need = carve_workspace(nullptr, proj->n, capacity, kc.tiles_x, kc.tiles_y).bytes;
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
         return fail(GS_ERR_ARG, "workspace NULL, not 256-byte aligned or smaller than %zu bytes", need);
-    const SortWorkspace w = carve_workspace(workspace, proj->n, capacity, tiles);
+    const SortWorkspace w = carve_workspace(workspace, proj->n, capacity, kc.tiles_x, kc.tiles_y);
     unsigned* err = error_word(&s);
     if (!err) return s;
     cudaStream_t st = as_stream(stream);
@@ -279,8 +278,10 @@ int gs_bin_and_sort(const gs_proj* proj, const gs_camera* cam, const gs_options*
     if ((e = cudaMemcpyAsync(&d, w.total, 8, cudaMemcpyDeviceToHost, st))) return cuda_fail(e, "gs_bin_and_sort: read D");
     if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "gs_bin_and_sort: synchronize");
     *n_dup_out = (int64_t)d;
-    if (d > (unsigned long long)capacity)
+    if (d > (unsigned long long)capacity) {
+        if ((e = cudaMemsetAsync(tile_ranges, 0, (size_t)tiles * 8, st))) return cuda_fail(e, "gs_bin_and_sort");
         return fail(GS_ERR_CAPACITY, "%llu duplicates exceed capacity %lld", d, (long long)capacity);
+    }
     e = bin_emit_sort(*proj, kc.tiles_x, kc.tiles_y, (unsigned)d, (unsigned long long)capacity, w, keys, vals,
                       tile_ranges, err, st);
     return e ? cuda_fail(e, "gs_bin_and_sort: emit/sort") : GS_OK;
@@ -299,7 +300,7 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
     if (capacity > 0 && (!vals || !aligned(vals, 4))) return fail(GS_ERR_ARG, "vals NULL or misaligned");
     if (keys && !aligned(keys, 8)) return fail(GS_ERR_ARG, "keys not 8-byte aligned");
     const long long tiles = (long long)kc.tiles_x * kc.tiles_y;
-    const size_t need = carve_workspace(nullptr, proj->n, capacity, tiles).bytes;
+    const size_t need = carve_workspace(nullptr, proj->n, capacity, kc.tiles_x, kc.tiles_y).bytes;
     if (need > (size_t)GS_STATIC_SORT_WORKSPACE_BYTES)
         return fail(GS_ERR_ARG,
                     "n = %lld with capacity %lld needs %zu bytes of sort workspace; the static workspace holds %u "
@@ -307,7 +308,7 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
                     (long long)proj->n, (long long)capacity, need, (unsigned)GS_STATIC_SORT_WORKSPACE_BYTES);
     unsigned char* ws = static_sort_workspace(&s);
     if (!ws) return s;
-    const SortWorkspace w = carve_workspace(ws, proj->n, capacity, tiles);
+    const SortWorkspace w = carve_workspace(ws, proj->n, capacity, kc.tiles_x, kc.tiles_y);
     unsigned* err = error_word(&s);
     if (!err) return s;
     cudaStream_t st = as_stream(stream);
@@ -319,8 +320,11 @@ int gs_bin_and_sort_static(const gs_proj* proj, const gs_camera* cam, const gs_o
         return cuda_fail(e, "gs_bin_and_sort_static: read D");
     if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "gs_bin_and_sort_static: synchronize");
     *n_dup_out = (int64_t)d;
-    if (d > (unsigned long long)capacity)
+    if (d > (unsigned long long)capacity) {
+        if ((e = cudaMemsetAsync(tile_ranges, 0, (size_t)tiles * 8, st)))
+            return cuda_fail(e, "gs_bin_and_sort_static");
         return fail(GS_ERR_CAPACITY, "%llu duplicates exceed capacity %lld", d, (long long)capacity);
+    }
     e = bin_emit_sort(*proj, kc.tiles_x, kc.tiles_y, (unsigned)d, (unsigned long long)capacity, w, keys, vals,
                       tile_ranges, err, st);
     return e ? cuda_fail(e, "gs_bin_and_sort_static: emit/sort") : GS_OK;
@@ -342,7 +346,7 @@ int gs_bin_and_sort_async(const gs_proj* proj, const gs_camera* cam, const gs_op
     if (!counting_path(tiles))
         return fail(GS_ERR_ARG, "%lld tiles: the call without host synchronisation handles images of up to 49152 "
                     "tiles; use gs_bin_and_sort", tiles);
-    const size_t need = carve_workspace(nullptr, proj->n, capacity, tiles).bytes;
+    const size_t need = carve_workspace(nullptr, proj->n, capacity, kc.tiles_x, kc.tiles_y).bytes;
     unsigned char* base = static_cast<unsigned char*>(workspace);
     if (!workspace) {
         if (need > (size_t)GS_STATIC_SORT_WORKSPACE_BYTES)
@@ -353,7 +357,7 @@ int gs_bin_and_sort_async(const gs_proj* proj, const gs_camera* cam, const gs_op
     } else if (workspace_bytes < need || !aligned(workspace, 256)) {
         return fail(GS_ERR_ARG, "workspace not 256-byte aligned or smaller than %zu bytes", need);
     }
-    const SortWorkspace w = carve_workspace(base, proj->n, capacity, tiles);
+    const SortWorkspace w = carve_workspace(base, proj->n, capacity, kc.tiles_x, kc.tiles_y);
     unsigned* err = error_word(&s);
     if (!err) return s;
     cudaError_t e = bin_sort_async(*proj, kc.tiles_x, kc.tiles_y, (unsigned long long)capacity, w, keys, vals,

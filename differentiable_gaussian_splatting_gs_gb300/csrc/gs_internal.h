@@ -45,17 +45,27 @@ struct SortWorkspace {
     size_t sweep_bytes;
     int sweep_blocks;                  // 4096-item blocks of a depth pass
     unsigned *tA, *tB, *vB;            // radix tile pass: keys ping-pong and values, capacity each
-    unsigned* table;                   // counting tile pass: chunk x tile counts, then offsets
-    uint2* crect;                      // counting tile pass: packed tile rectangle per depth-ordered Gaussian
-    unsigned *tile_total, *tile_start; // counting tile pass: entries per tile, exclusive scan
-    unsigned *chunk_first, *nchunks;   // counting tile pass: first Gaussian of each chunk, chunks used
-    unsigned long long* dsum;          // counting tile pass: duplicate total from the block sums
-    long long cmax;                    // counting tile pass: rows of the chunk x tile table
+    // counting tile pass, two levels: super-tiles of 4x4 tiles (coarse), then tiles (fine)
+    uint2* crect;                      // packed tile rectangle per depth-ordered Gaussian
+    unsigned long long *ssum, *soff;   // super-tile entries per 256 Gaussians, offsets
+    unsigned long long* ctotal;        // super-tile entries in all (D')
+    unsigned* table;                   // coarse: chunk x super-tile counts, then offsets
+    unsigned* group_sum;               // coarse: per group of table rows, the column sums
+    unsigned *stile_total, *stile_start; // coarse: entries per super-tile, exclusive scan
+    uint2* crange;                     // coarse: [start, end) of each super-tile's list
+    unsigned* cvals;                   // coarse: the lists (depth positions), capacity entries
+    unsigned *chunk_first, *nchunks;   // coarse: first Gaussian of each chunk, chunks used
+    long long cmax;                    // coarse: rows of the chunk x super-tile table
+    unsigned *seg_first, *nseg;        // fine: first segment of each super-tile, segments used
+    unsigned* fcount;                  // fine: per segment and tile of its super-tile, counts then offsets
+    long long seg_cap;                 // fine: segments the workspace holds
+    unsigned *tile_total, *tile_start; // fine: entries per tile, exclusive scan
+    int sx, sy;                        // super-tiles per row and column
     size_t bytes;                      // total size
 };
 
-// Workspace layout for n Gaussians, at most `cap` duplicates and `tiles` tiles.
-SortWorkspace carve_workspace(void* base, long long n, long long cap, long long tiles);
+// Workspace layout for n Gaussians, at most `cap` duplicates and tiles_x x tiles_y tiles.
+SortWorkspace carve_workspace(void* base, long long n, long long cap, int tiles_x, int tiles_y);
 // Phase 1 of the binning (depth sort, duplicate counts, on the counting path also the tile
 // table, starts and ranges); `ranges` and `capacity` are used on the counting path only, and
 // overflow_err (may be NULL) receives the check bit when D exceeds the capacity there;

@@ -143,9 +143,10 @@ int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* op
                   void* stream);
 
 /* Bytes of device workspace gs_bin_and_sort needs for n Gaussians and `capacity` duplicates on a
- * width x height image: about 25 n + 4 T (n / 512 + capacity / 16384) bytes (T tiles) for images
- * of up to 49,152 tiles, where the tile pass is one counting pass; beyond that the tile pass falls
- * back to radix passes and needs 12 bytes per duplicate of capacity instead of the table.
+ * width x height image: about 27 n + 4.25 capacity + T (n / 512 + capacity / 16384) bytes
+ * (T tiles) for images of up to 49,152 tiles, where the tile pass is a two-level counting pass
+ * (its coarse lists hold up to `capacity` entries); beyond that the tile pass falls back to radix
+ * passes and needs 12 bytes per duplicate of capacity instead.
  * Returns 0 for negative sizes or an empty image. */
 size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32_t height);
 
@@ -154,9 +155,9 @@ size_t gs_sort_workspace_bytes(int64_t n, int64_t capacity, int32_t width, int32
  * Gaussian with radius > 0 and per tile of its rectangle, stably sorted by key: the result is
  * ordered by (tile, depth, Gaussian index). The sort is a hand-written LSD radix sort: the
  * visible Gaussians are first sorted by depth bits (4 passes of 8 bits), then their duplicates
- * are placed by tile id in one stable counting pass (images of up to 49,152 tiles; larger ones
- * emit the duplicates in depth order and sort them by tile id in 8-bit passes), which equals a
- * stable sort of the 64-bit keys.
+ * are placed by tile id in one stable counting pass, done in two levels: blocks of 4x4 tiles, then
+ * tiles (images of up to 49,152 tiles; larger ones emit the duplicates in depth order and sort them
+ * by tile id in 8-bit passes), which equals a stable sort of the 64-bit keys.
  * Outputs: keys [D] uint64 (may be NULL: not written), vals [D] uint32, tile_ranges [T][2]
  * uint32 = [start, end) of each tile in the sorted list, *n_dup_out (HOST int64) = D.
  * workspace: device buffer of at least gs_sort_workspace_bytes(n, capacity, W, H) bytes.
@@ -361,7 +362,7 @@ int gs_preprocess2d_bwd(const gs_params* p, const gs_camera* cam, const gs_optio
  * until the process exits. The pages describe no such entry point; it is a convenience of this
  * library.
  *   - Limit: the call needs gs_sort_workspace_bytes(n, capacity, W, H) <= 32 MiB (for example
- *     n = 600,000 Gaussians with capacity = 5,000,000 duplicates on an 800 x 800 image); larger
+ *     n = 400,000 Gaussians with capacity = 4,000,000 duplicates on an 800 x 800 image); larger
  *     requests return GS_ERR_ARG without touching the device. The call itself allocates nothing.
  *   - Set-up: the first call on a device looks up the device address of the array (once per
  *     device, with that device current). Make that first call before any stream capture.

@@ -50,12 +50,15 @@ def test_workspace_size_matches_the_documented_layout(lib):
     n, T = 1_000_000, 82 * 53
     b = lib.gs_sort_workspace_bytes(n, 10_000_000, 1297, 840)
     assert 0 < a < b
-    # counting tile pass: depth sort, packed rectangles and the chunk x tile table, whose rows are
-    # chunks of at most 512 Gaussians or about 16384 entries
-    rows = (n + 511) // 512 + 10_000_000 // 16384 + 1
-    assert b >= 24 * n + 4 * T * rows
+    # counting tile pass in two levels: depth sort and packed rectangles (24 bytes per Gaussian), the
+    # coarse lists (4 bytes per duplicate of capacity), the chunk x super-tile table (super-tiles of
+    # 4x4 tiles, here 21 x 14; rows are chunks of at most 256 Gaussians or about 8192 coarse entries)
+    # and the fine counts (16 words per 256-entry segment)
+    ts = ((82 + 3) // 4) * ((53 + 3) // 4)
+    rows = (n + 255) // 256 + 10_000_000 // 8192 + 1
+    assert b >= 24 * n + 4 * 10_000_000 + 4 * ts * rows
     small = lib.gs_sort_workspace_bytes(n, 1, 1297, 840)
-    assert 0 < b - small <= 4 * T * (10_000_000 // 16384) + 4096
+    assert 4 * 10_000_000 < b - small <= 4.25 * 10_000_000 + 4 * ts * (10_000_000 // 8192) * (1 + 1 / 512) + 65536
     # more than 49,152 tiles: radix tile passes, 12 more bytes per duplicate of capacity
     big1 = lib.gs_sort_workspace_bytes(n, 1_000_000, 4112, 4112)
     big2 = lib.gs_sort_workspace_bytes(n, 2_000_000, 4112, 4112)
