@@ -29,8 +29,11 @@ constexpr int kSortRounds = 16;                          // rounds of 32 items p
 constexpr int kSortItems = kSortThreads * kSortRounds;  // 4096 items per block
 constexpr int kWarpItems = 32 * kSortRounds;            // 512 items per warp
 
-// Super-tiles: blocks of kSuper x kSuper tiles, the coarse level of the two-level counting pass.
+// Super-tiles: blocks of kSuper x kSuper tiles, the coarse level of the two-level counting pass;
+// the fine level splits each super-tile's list into segments of kSeg entries.
 constexpr int kSuper = 4;
+constexpr int kSeg = 256;                      // coarse entries per segment
+constexpr int kRounds = kSeg / 32;             // rounds of 32 entries per segment
 
 // The rectangle of super-tiles overlapped by a packed tile rectangle (x0 | y0 << 16, w | h << 16),
 // packed the same way; empty stays empty.
@@ -903,12 +906,18 @@ __global__ void __launch_bounds__(32 * kScanWarps) k_chunk_scan(const unsigned* 
 // total_copy when given), and the tile ranges [start, start + count). When D exceeds the capacity every range is written empty, so
 // that no later kernel reads past the caller's list; with `err` (the call that does not read D on
 // the host) the check bit is also set.
+//
+// With seg_first (the coarse level: the "tiles" are super-tiles), it also numbers the fine level's
+// segments: super-tile s gets ceil(count / kSeg) of them (none when over the capacity), numbered
+// from seg_first[s]; seg_first[T] and *nseg = their number (nseg clamped to seg_cap).
 __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __restrict__ tile_total,
                                                     unsigned* __restrict__ tile_start,
                                                     unsigned long long* __restrict__ total,
                                                     unsigned long long capacity, uint2* __restrict__ ranges,
                                                     unsigned* __restrict__ err,
-                                                    unsigned long long* __restrict__ total_copy) {
+                                                    unsigned long long* __restrict__ total_copy,
+                                                    unsigned* __restrict__ seg_first, unsigned* __restrict__ nseg,
+                                                    unsigned seg_cap) {
     pdl_entry();
     __shared__ unsigned long long wsum[32];
     __shared__ unsigned long long round_total;
@@ -940,6 +949,31 @@ __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __res
     for (int t = threadIdx.x; t < T; t += blockDim.x) {  // the last round's barrier made every start visible
         const unsigned c = tile_total[t];
         ranges[t] = (!over && c) ? make_uint2(tile_start[t], tile_start[t] + c) : make_uint2(0u, 0u);
+    }
+    if (!seg_first) return;
+    __shared__ unsigned swsum[32];
+    __shared__ unsigned sround_total;
+    unsigned scarry = 0;
+    for (int base = 0; base < T; base += 1024 * kScanItems) {
+        const int t0 = base + threadIdx.x * kScanItems;
+        unsigned v[kScanItems], sum = 0;
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            v[k] = (!over && t0 + k < T) ? (tile_total[t0 + k] + kSeg - 1) / kSeg : 0u;
+            sum += v[k];
+        }
+        unsigned run = scarry + block_scan_1024(sum, swsum, &sround_total);
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            if (t0 + k < T) seg_first[t0 + k] = run;
+            run += v[k];
+        }
+        scarry += sround_total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        seg_first[T] = scarry;
+        *nseg = min(scarry, seg_cap);
     }
 }
 
@@ -1055,8 +1089,6 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
 // lanes whose Gaussian covers it write consecutive positions of the tile's list, one coalesced
 // run. Segments, rounds and lanes follow the coarse list, so each tile's entries stay in depth
 // order: the result is the same stable counting pass by tile id.
-constexpr int kSeg = 256;                      // coarse entries per segment
-constexpr int kRounds = kSeg / 32;             // rounds of 32 entries per segment
 constexpr int kSuperTiles = kSuper * kSuper;   // tiles per super-tile
 static_assert(kSuper == 4, "cover_mask packs a super-tile's tiles as 4 bits per row");
 
@@ -1069,44 +1101,6 @@ __device__ __forceinline__ unsigned cover_mask(uint2 r, int tx0, int ty0) {
     const unsigned row = ((1u << ax1) - 1u) & ~((1u << ax0) - 1u);
     const unsigned col = 0x1111u & ((1u << (4 * ay1)) - 1u) & ~((1u << (4 * ay0)) - 1u);
     return row * col;  // the row pattern repeated in every covered row's nibble
-}
-
-// Segments of the super-tiles' coarse lists: super-tile s has ceil(len_s / kSeg) of them,
-// numbered from seg_first[s]; seg_first[Ts] and *nseg = their number (clamped to seg_cap).
-// One block of 1024 threads.
-__global__ void __launch_bounds__(1024) k_seg_scan(int Ts, const uint2* __restrict__ crange,
-                                                   unsigned* __restrict__ seg_first, unsigned* __restrict__ nseg,
-                                                   unsigned seg_cap) {
-    pdl_entry();
-    __shared__ unsigned wsum[32];
-    __shared__ unsigned round_total;
-    unsigned carry = 0;
-    for (int base = 0; base < Ts; base += 1024 * kScanItems) {
-        const int s0 = base + threadIdx.x * kScanItems;
-        unsigned v[kScanItems], sum = 0;
-#pragma unroll
-        for (int k = 0; k < kScanItems; ++k) {
-            unsigned c = 0;
-            if (s0 + k < Ts) {
-                const uint2 rg = crange[s0 + k];
-                c = rg.y > rg.x ? (rg.y - rg.x + kSeg - 1) / kSeg : 0u;
-            }
-            v[k] = c;
-            sum += c;
-        }
-        unsigned run = carry + block_scan_1024(sum, wsum, &round_total);
-#pragma unroll
-        for (int k = 0; k < kScanItems; ++k) {
-            if (s0 + k < Ts) seg_first[s0 + k] = run;
-            run += v[k];
-        }
-        carry += round_total;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        seg_first[Ts] = carry;
-        *nseg = min(carry, seg_cap);
-    }
 }
 
 // The super-tile of segment k: the last s with first[s] <= k (first[] in shared memory).
@@ -1450,7 +1444,7 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
         const size_t smem = (size_t)ts * 4;
         if ((e = cudaFuncSetAttribute(k_chunk_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return e;
-        count_launches(7);
+        count_launches(6);
         if ((e = launch_pdl(k_count, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.dvB, rec, proj.radius, tiles_x,
                             tiles_y, w.bsum, w.crect, w.ssum)))
             return e;
@@ -1463,17 +1457,21 @@ cudaError_t bin_count(const gs_proj& proj, int tiles_x, int tiles_y, const SortW
         if ((e = launch_pdl(k_chunk_hist, dim3((unsigned)w.cmax), dim3(256), smem, st, w.nchunks,
                             w.chunk_first, w.crect, sx, ts, w.table)))
             return e;
+        // the column sums of the row groups are needed only when there can be more than one group
         const unsigned groups = (unsigned)((w.cmax + kScanGroup - 1) / kScanGroup);
-        if ((e = launch_pdl(k_chunk_colsum, dim3((ts + 31) / 32, groups), dim3(32 * kScanWarps), 0, st, w.nchunks,
-                            ts, (const unsigned*)w.table, w.group_sum)))
-            return e;
+        if (groups > 1) {
+            count_launches(1);
+            if ((e = launch_pdl(k_chunk_colsum, dim3((ts + 31) / 32, groups), dim3(32 * kScanWarps), 0, st,
+                                w.nchunks, ts, (const unsigned*)w.table, w.group_sum)))
+                return e;
+        }
         if ((e = launch_pdl(k_chunk_scan, dim3((ts + 31) / 32, groups), dim3(32 * kScanWarps), 0, st, w.nchunks, ts,
                             w.table, (const unsigned*)w.group_sum, w.stile_total)))
             return e;
         // the coarse lists hold at most D' <= D entries: over the capacity only when D is
         return launch_pdl(k_tile_scan, dim3(1), dim3(1024), 0, st, ts, w.stile_total, w.stile_start, w.ctotal,
                           capacity, reinterpret_cast<uint2*>(w.crange), overflow_err,
-                          (unsigned long long*)nullptr);
+                          (unsigned long long*)nullptr, w.seg_first, w.nseg, (unsigned)w.seg_cap);
     }
     count_launches(2);
     if ((e = launch_pdl(k_count, dim3(gblocks), dim3(256), 0, st, n, w.nvis, w.dvB, rec, proj.radius, tiles_x, tiles_y,
@@ -1507,13 +1505,10 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
     if ((e = cudaFuncSetAttribute(k_fine_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem))) return e;
     if ((e = cudaFuncSetAttribute(k_fine_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem))) return e;
     const long long warps = w.cmax * nbands;
-    count_launches(6);
+    count_launches(5);
     if ((e = launch_pdl(k_chunk_place, dim3((unsigned)((warps + wpb - 1) / wpb)), dim3(32 * wpb), smem, st,
                         w.nchunks, w.chunk_first, w.crect, sx, sy, band_rows, nbands, w.table, w.stile_start,
                         (unsigned)capacity, w.cvals, err)))
-        return e;
-    if ((e = launch_pdl(k_seg_scan, dim3(1), dim3(1024), 0, st, ts, reinterpret_cast<const uint2*>(w.crange),
-                        w.seg_first, w.nseg, (unsigned)w.seg_cap)))
         return e;
     // grid-stride kernels over the segments: at most 8 resident blocks of 8 warps per SM
     const long long seg_blocks = (w.seg_cap + 7) / 8;
@@ -1525,7 +1520,8 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
                         w.seg_first, (unsigned)w.seg_cap, w.fcount, w.tile_total)))
         return e;
     if ((e = launch_pdl(k_tile_scan, dim3(1), dim3(1024), 0, st, T, w.tile_total, w.tile_start, w.total, capacity,
-                        reinterpret_cast<uint2*>(ranges), err, (unsigned long long*)nullptr)))
+                        reinterpret_cast<uint2*>(ranges), err, (unsigned long long*)nullptr, (unsigned*)nullptr,
+                        (unsigned*)nullptr, 0u)))
         return e;
     return launch_pdl(k_fine_place, dim3(fblocks), dim3(256), fsmem, st, ts, sx, tiles_x, tiles_y,
                       (unsigned)proj.n, w.seg_first,
