@@ -53,8 +53,10 @@ WORKLOAD = WORKLOADS[CFG]
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 COUNTS_PATH = os.path.join(ROOT, "profiles", "workload_counts_outdoor.md")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "render_bwd_outdoor_1600k.md")
+# the backward kernel's source and its device helpers: the ncu counters hold while these are unchanged
+# (they are attached only to the default ADAPTIVE mode, whose 28-lane threshold they were taken with)
 TRAFFIC_SOURCES = ("differentiable_gaussian_splatting_gs_gb300/csrc/render.cu",
-                   "differentiable_gaussian_splatting_gs_gb300/csrc/gs_abi.cu")
+                   "differentiable_gaussian_splatting_gs_gb300/csrc/gs_common.cuh")
 # Algorithmic work of the backward raster. Every pixel's list is replayed back to front from its
 # last contributor, and each replayed (pixel, Gaussian) pair needs its alpha: offsets 2, quadratic
 # form 9, exponential 1, opacity product 1, clamp 1, threshold 1 = 15 FP32 operations. Each blended

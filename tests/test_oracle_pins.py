@@ -437,3 +437,17 @@ def test_end_to_end_gradients_match_central_differences(deg):
             assert abs(fd - an_all[k]) <= 1e-6 * abs(an_all[k]) + 1e-7 * scale + 1e-9, (pname, k, fd, an_all[k])
             checked += 1
     assert checked > 0.9 * (checked + skipped)
+
+
+def test_backward_sums_do_not_depend_on_the_thread_count():
+    """Per-Gaussian gradient sums are formed per tile and added in tile order: the same bits with
+    one, three or eight threads."""
+    rng = np.random.default_rng(7)
+    W, H, n = 96, 80, 700
+    mean2d, conic, opacity, rgb, depth, radius = _records_2d(n, W, H, rng)
+    m32 = mean2d.astype(np.float32)
+    _, vals, ranges = oracle.bin_and_sort(m32, depth, radius, W, H)
+    g = rng.standard_normal((3, H, W)).astype(np.float32)
+    outs = [oracle.render(m32.astype(np.float64), conic, opacity, rgb, vals, ranges, _cam(W, H, 50.0), dl_dimage=g,
+                          threads=t)["grad2d"] for t in (1, 3, 8)]
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
