@@ -342,6 +342,45 @@ def time_bwd_modes(api, bufs, cam, target, sh_degree, flush, stream, reps: int) 
     return out
 
 
+def time_preprocess(api, params, bufs, cam, opt, grads, sh_degree, flush, stream, reps: int) -> dict:
+    """The two HBM-bound kernels of the step, gs_preprocess and gs_preprocess_bwd (one launch each),
+    timed alone with L2 flushed before every launch (mean of `reps` launches), against their
+    algorithmic bytes: the preprocess reads the geometry (40 B) of every Gaussian and the SH row and
+    opacity logit of the visible ones, and writes the record, depth, radius and tile count (60 B) of
+    every Gaussian; the backward reads every radius and, for the visible Gaussians, the parameters
+    and the 48-byte 2D gradient, and writes every Gaussian's gradient row (zeros when culled)."""
+    import torch
+    peaks = load_json(PEAKS_PATH) or {}
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    n = params["mean3d"].shape[0]
+    sh4 = 3 * (sh_degree + 1) ** 2 * 4
+    out = {}
+    for name in ("preprocess", "preprocess_bwd"):
+        ts = []
+        for it in range(reps + 2):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if name == "preprocess":
+                api.gs_preprocess(params, cam, opt, out=bufs.proj)
+            else:
+                api.gs_preprocess_bwd(params, cam, opt, bufs.proj, bufs.grad2d, out=grads)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= 2:
+                ts.append(e0.elapsed_time(e1))
+        out[f"{name}_ms"] = sum(ts) / len(ts)
+    vis = int((bufs.proj.radius > 0).sum().item())
+    fwd_bytes = n * (40 + 60) + vis * (sh4 + 4)
+    bwd_bytes = n * (4 + 44 + sh4) + vis * (40 + 48 + 4 + sh4)
+    for name, b in (("preprocess", fwd_bytes), ("preprocess_bwd", bwd_bytes)):
+        gbs = b / (out[f"{name}_ms"] / 1e3) / 1e9
+        out[name] = {"algorithmic_bytes": b, "achieved_gbs": gbs, "frac_of_measured_hbm": gbs / hbm}
+    out["visible"] = vis
+    out["note"] = "each launch alone, L2 flushed before it"
+    return out
+
+
 def config_block(cfg: int, dev, flush, stream, args, cpu: bool) -> dict:
     """The step of one configuration as one CUDA graph replay per step: ms per view, the raster
     kernels' times, duplicates per view and Mpix/s (5 timed replays, L2 flushed before each),
@@ -679,6 +718,9 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         extras["bwd_modes"] = time_bwd_modes(api, bufs, cams[-1], target[n_views - 1], scene.sh_degree, flush,
                                              stream, max(5, args.steps // 2))
+        assert api.gs_device_error() == 0
+        extras["preprocess"] = time_preprocess(api, params, bufs, cams[-1], opt, grads, scene.sh_degree, flush,
+                                               stream, max(5, args.steps // 2))
         assert api.gs_device_error() == 0
         exp_avg = {k: torch.zeros_like(params[k]) for k in names}
         exp_avg_sq = {k: torch.zeros_like(params[k]) for k in names}

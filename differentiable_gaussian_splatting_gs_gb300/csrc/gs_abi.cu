@@ -173,6 +173,19 @@ unsigned char* static_sort_workspace(int* status) {
 }
 
 }  // namespace
+
+int device_sm_count() {
+    static std::atomic<int> cache[256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 1;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) return 1;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
 }  // namespace gs
 
 using namespace gs;
@@ -242,7 +255,9 @@ int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* op
     int s;
     if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc)) || (s = check_params(p))) return s;
     if ((s = check_proj(out, p->n))) return s;
-    cudaError_t e = launch_preprocess(o.deg, (int)p->n, *p, kc, *out, as_stream(stream));
+    unsigned* err = error_word(&s);
+    if (!err) return s;
+    cudaError_t e = launch_preprocess(o.deg, (int)p->n, *p, kc, *out, o.spin, err, as_stream(stream));
     return e ? cuda_fail(e, "gs_preprocess") : GS_OK;
 }
 
@@ -443,8 +458,11 @@ int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options
         for (const void* q : outs)
             if (!q || !aligned(q, 4)) return fail(GS_ERR_ARG, "a gradient output is NULL or misaligned");
     }
+    unsigned* err = error_word(&s);
+    if (!err) return s;
     cudaError_t e = launch_preprocess_bwd(o.deg, (int)p->n, *p, kc, proj->radius, grad2d, d_mean3d, d_log_scale,
-                                          d_quat, d_opacity_logit, d_sh, accumulate, nullptr, as_stream(stream));
+                                          d_quat, d_opacity_logit, d_sh, accumulate, nullptr, o.spin, err,
+                                          as_stream(stream));
     return e ? cuda_fail(e, "gs_preprocess_bwd") : GS_OK;
 }
 
@@ -470,8 +488,11 @@ int gs_preprocess_bwd_stats(const gs_params* p, const gs_camera* cam, const gs_o
     }
     DensifyArgs d{stats->grad_norm_accum, stats->view_count, stats->max_radius, stats->grad_mag,
                   stats->ndc ? 0.5f * (float)kc.width : 1.f, stats->ndc ? 0.5f * (float)kc.height : 1.f};
+    unsigned* err = error_word(&s);
+    if (!err) return s;
     cudaError_t e = launch_preprocess_bwd(o.deg, (int)p->n, *p, kc, proj->radius, grad2d, d_mean3d, d_log_scale,
-                                          d_quat, d_opacity_logit, d_sh, accumulate, &d, as_stream(stream));
+                                          d_quat, d_opacity_logit, d_sh, accumulate, &d, o.spin, err,
+                                          as_stream(stream));
     return e ? cuda_fail(e, "gs_preprocess_bwd_stats") : GS_OK;
 }
 

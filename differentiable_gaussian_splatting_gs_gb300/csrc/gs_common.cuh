@@ -110,6 +110,33 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsign
         : "memory");
 }
 
+// Orders the calling thread's earlier shared-memory writes before its later bulk copies that read
+// them (generic proxy -> async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One bulk copy shared -> global of `bytes` (multiple of 16, both addresses 16-byte aligned) in the
+// calling thread's bulk group; the shared source may be reused after bulk_wait_read().
+__device__ __forceinline__ void bulk_copy_s2g(void* dst, const void* src, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// As bulk_copy_s2g, but adds the floats to global memory (one float32 addition per element,
+// performed at the L2).
+__device__ __forceinline__ void bulk_add_s2g(float* dst, const float* src, unsigned bytes) {
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
+// Closes the calling thread's bulk group and waits until its copies have read their shared sources.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Asynchronous 4-byte global -> shared copy (no register staging; completes at cp_async_wait_all,
 // which waits for the calling thread's own copies).
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -153,6 +180,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
         : "memory");
     return ok != 0;
 }
+
+// Bound of the waits that let in-flight bulk copies land before a block exits early; independent
+// of the caller's spin limit so that a small limit cannot leave copies running into a dead block.
+constexpr unsigned kDrainLimit = 1u << 22;
 
 // Bounded wait for phase `parity` of `bar`; false (and the timeout bit set) when it gives up.
 // Every 1024 polls it also gives up if another wait has already set the timeout bit, so that a

@@ -85,8 +85,11 @@ bool counting_path(long long tiles);
 constexpr size_t kSelftestLookbackBytes = 106512;
 cudaError_t selftest_lookback(unsigned char* ws, unsigned spin_limit, unsigned* err, cudaStream_t st);
 
+// Number of SMs of the current device (looked up once per device; 1 if the query fails).
+int device_sm_count();
+
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
-                              cudaStream_t st);
+                              unsigned spin_limit, unsigned* err, cudaStream_t st);
 // Post-backward statistics written by the preprocess backward (gs_preprocess_bwd_stats).
 struct DensifyArgs {
     float* accum;      // += |(sx, sy) * dL/dmean2d| for radius > 0
@@ -97,7 +100,8 @@ struct DensifyArgs {
 };
 cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
                                   const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
-                                  int accumulate, const DensifyArgs* stats, cudaStream_t st);
+                                  int accumulate, const DensifyArgs* stats, unsigned spin_limit, unsigned* err,
+                                  cudaStream_t st);
 cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* vals, const unsigned* ranges,
                               const KernelCamera& cam, float* image, float* t_final, unsigned* n_contrib,
                               unsigned spin_limit, unsigned* err, cudaStream_t st);

@@ -5,6 +5,8 @@
 // Rendering Pipelines, Abstract): view-space position, EWA projection of the 3D covariance to a
 // 2D conic, 3-sigma radius and tile rectangle, sigmoid opacity, spherical-harmonic colour.
 // Backward: the chain rule of that forward, recomputing its intermediates.
+#include <atomic>
+
 #include "gs_common.cuh"
 #include "gs_internal.h"
 #include "sh.cuh"
@@ -106,6 +108,101 @@ __device__ __forceinline__ bool geometry(const float* m, const float* ls, const 
 
 constexpr int kFwdThreads = 128;
 
+// SH rows moved by the bulk-copy engine (one copy per Gaussian's row) need rows of a multiple of
+// 16 bytes (degrees 1 and 3) and 16-byte aligned arrays; the shared row stride is then an odd
+// number of 16-byte chunks, so that each thread's float4 reads of its own row are conflict-free.
+// Otherwise the rows move as coalesced 4-byte asynchronous copies into rows of K3 + 1 floats.
+template <int K3>
+struct ShRows {
+    static constexpr bool kBulkable = K3 % 4 == 0;
+    static constexpr int bulk_stride = ((K3 / 4) & 1) ? K3 : K3 + 4;
+    template <bool BULK>
+    static constexpr int stride = BULK ? bulk_stride : K3 + 1;
+};
+
+// colour = 0.5 + sum_k Y_k sh_k per channel, k in increasing order (one fused multiply-add per
+// term, so both forms round alike), from a thread's row of K3 floats (coefficient-major,
+// channel-minor) read as float4 chunks or as floats.
+template <int K, bool VEC>
+__device__ __forceinline__ void sh_colour(const float* row, const float* Y, float* col) {
+    col[0] = col[1] = col[2] = 0.5f;
+    if constexpr (VEC) {
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll
+        for (int j = 0; j < 3 * K / 4; ++j) {
+            const float4 v = r4[j];
+            const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) col[(4 * j + t) % 3] = __fmaf_rn(Y[(4 * j + t) / 3], e[t], col[(4 * j + t) % 3]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            col[0] = __fmaf_rn(Y[k], row[3 * k], col[0]);
+            col[1] = __fmaf_rn(Y[k], row[3 * k + 1], col[1]);
+            col[2] = __fmaf_rn(Y[k], row[3 * k + 2], col[2]);
+        }
+    }
+}
+
+// Projection of one Gaussian: geometry, radius and tile rectangle; writes its depth, and zeros for
+// its record, radius and tile count when it is culled. Returns whether it is visible.
+__device__ __forceinline__ bool project_one(int i, const float* m, const float* ls, const float* q,
+                                            const KernelCamera& cam, Geo& g, int& r, unsigned& tt,
+                                            float4* __restrict__ rec, float* __restrict__ depth,
+                                            int* __restrict__ radius, unsigned* __restrict__ tiles_touched) {
+    bool ok = geometry(m, ls, q, cam, g);
+    depth[i] = g.p[2];
+    r = 0;
+    tt = 0;
+    if (ok) {
+        // largest eigenvalue of the 2D covariance in the cancellation-free form
+        const float hd = 0.5f * (g.a - g.c);
+        const float lam = 0.5f * (g.a + g.c) + sqrtf(hd * hd + g.b * g.b);
+        const float rf = ceilf(3.f * sqrtf(lam));
+        ok = isfinite(g.mx) && isfinite(g.my) && rf < 16777216.0f;  // radius < 2^24 px (also rejects NaN)
+        if (ok) {
+            r = (int)rf;
+            const Rect R = tile_rect(g.mx, g.my, r, cam.tiles_x, cam.tiles_y);
+            ok = R.x0 <= R.x1;
+            if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
+        }
+    }
+    if (!ok) {
+        radius[i] = 0;
+        tiles_touched[i] = 0;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        rec[3 * i] = z4;
+        rec[3 * i + 1] = z4;
+        rec[3 * i + 2] = z4;
+    }
+    return ok;
+}
+
+// Sigmoid opacity and view-dependent colour of a visible Gaussian; writes its record, radius and
+// tile count.
+template <int DEG, bool VEC>
+__device__ __forceinline__ void shade_one(int i, const float* m, const Geo& g, int r, unsigned tt, float lg,
+                                          const float* row, const KernelCamera& cam, float4* __restrict__ rec,
+                                          int* __restrict__ radius, unsigned* __restrict__ tiles_touched) {
+    const float op = 1.f / (1.f + expf(-lg));
+    // view direction from the camera centre to the mean
+    float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
+    const float dinv = rsqrtf(dx * dx + dy * dy + dz * dz);
+    dx *= dinv; dy *= dinv; dz *= dinv;
+    float Y[16];
+    sh_basis<DEG>(dx, dy, dz, Y);
+    float col[3];
+    sh_colour<(DEG + 1) * (DEG + 1), VEC>(row, Y, col);
+    rec[3 * i] = make_float4(g.mx, g.my, g.A, g.B);
+    rec[3 * i + 1] = make_float4(g.C, op, fmaxf(col[0], 0.f), fmaxf(col[1], 0.f));
+    rec[3 * i + 2] = make_float4(fmaxf(col[2], 0.f), 0.f, 0.f, 0.f);
+    radius[i] = r;
+    tiles_touched[i] = tt;
+}
+
+// One thread per Gaussian, SH rows as coalesced 4-byte asynchronous copies (any SH degree and
+// alignment).
 template <int DEG>
 __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* __restrict__ mean3d,
                                                             const float* __restrict__ log_scale,
@@ -116,9 +213,9 @@ __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* 
                                                             int* __restrict__ radius,
                                                             unsigned* __restrict__ tiles_touched) {
     pdl_entry();
-    constexpr int K = (DEG + 1) * (DEG + 1);
-    constexpr int K3 = 3 * K;
-    __shared__ float tile_all[kFwdThreads / 32][32 * (K3 + 1)];
+    constexpr int K3 = 3 * (DEG + 1) * (DEG + 1);
+    constexpr int S = ShRows<K3>::template stride<false>;
+    __shared__ float tile_all[kFwdThreads / 32][32 * S];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int warp_first = blockIdx.x * kFwdThreads + warp * 32;
     if (warp_first >= n) return;  // whole warp
@@ -132,29 +229,7 @@ __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* 
         m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
         const float ls[3] = {log_scale[3 * i], log_scale[3 * i + 1], log_scale[3 * i + 2]};
         const float q[4] = {quat[4 * i], quat[4 * i + 1], quat[4 * i + 2], quat[4 * i + 3]};
-        ok = geometry(m, ls, q, cam, g);
-        depth[i] = g.p[2];
-        if (ok) {
-            // largest eigenvalue of the 2D covariance in the cancellation-free form
-            const float hd = 0.5f * (g.a - g.c);
-            const float lam = 0.5f * (g.a + g.c) + sqrtf(hd * hd + g.b * g.b);
-            const float rf = ceilf(3.f * sqrtf(lam));
-            ok = isfinite(g.mx) && isfinite(g.my) && rf < 16777216.0f;  // radius < 2^24 px (also rejects NaN)
-            if (ok) {
-                r = (int)rf;
-                const Rect R = tile_rect(g.mx, g.my, r, cam.tiles_x, cam.tiles_y);
-                ok = R.x0 <= R.x1;
-                if (ok) tt = (unsigned)((R.x1 - R.x0 + 1) * (R.y1 - R.y0 + 1));
-            }
-        }
-        if (!ok) {
-            radius[i] = 0;
-            tiles_touched[i] = 0;
-            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            rec[3 * i] = z4;
-            rec[3 * i + 1] = z4;
-            rec[3 * i + 2] = z4;
-        }
+        ok = project_one(i, m, ls, q, cam, g, r, tt, rec, depth, radius, tiles_touched);
     }
     // SH coefficients of the warp's visible Gaussians only, with coalesced loads (the opacity
     // logit is loaded while they are in flight)
@@ -164,53 +239,136 @@ __global__ void __launch_bounds__(kFwdThreads) k_preprocess(int n, const float* 
     const float lg = ok ? logit[i] : 0.f;
     cp_async_wait_all();
     __syncwarp();
-    if (!ok) return;
-    const float op = 1.f / (1.f + expf(-lg));
-    // view direction from the camera centre to the mean
-    float dx = m[0] - cam.campos[0], dy = m[1] - cam.campos[1], dz = m[2] - cam.campos[2];
-    const float dinv = rsqrtf(dx * dx + dy * dy + dz * dz);
-    dx *= dinv; dy *= dinv; dz *= dinv;
-    float Y[16];
-    sh_basis<DEG>(dx, dy, dz, Y);
-    const float* shg = tile + lane * (K3 + 1);
-    float col[3] = {0.5f, 0.5f, 0.5f};
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        col[0] += Y[k] * shg[3 * k];
-        col[1] += Y[k] * shg[3 * k + 1];
-        col[2] += Y[k] * shg[3 * k + 2];
+    if (ok) shade_one<DEG, false>(i, m, g, r, tt, lg, tile + lane * S, cam, rec, radius, tiles_touched);
+}
+
+// Persistent, pipelined form for bulk SH rows (degrees 1 and 3, 16-byte aligned SH array): each
+// warp walks 32-Gaussian groups with a stride of the grid's warp count. A group's SH rows can only
+// be requested once its geometry says which Gaussians are visible, so the warp loads the geometry
+// of its next group before it waits for the rows of the current one: the two dependent round trips
+// of consecutive groups overlap. One bulk copy per visible row, completing on the warp's mbarrier.
+template <int DEG>
+__global__ void __launch_bounds__(kFwdThreads) k_preprocess_pipe(int n, const float* __restrict__ mean3d,
+                                                                 const float* __restrict__ log_scale,
+                                                                 const float* __restrict__ quat,
+                                                                 const float* __restrict__ logit,
+                                                                 const float* __restrict__ sh,
+                                                                 const KernelCamera cam, float4* __restrict__ rec,
+                                                                 float* __restrict__ depth, int* __restrict__ radius,
+                                                                 unsigned* __restrict__ tiles_touched,
+                                                                 unsigned spin_limit, unsigned* __restrict__ err) {
+    pdl_entry();
+    constexpr int K3 = 3 * (DEG + 1) * (DEG + 1);
+    static_assert(ShRows<K3>::kBulkable, "bulk SH rows need a multiple of 16 bytes");
+    constexpr int S = ShRows<K3>::template stride<true>;
+    constexpr int W = kFwdThreads / 32;
+    __shared__ __align__(16) float tile_all[W][32 * S];
+    __shared__ uint64_t bars[W];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int groups = (n + 31) >> 5;
+    const int wstride = gridDim.x * W;
+    int grp = blockIdx.x * W + warp;
+    if (grp >= groups) return;  // whole warp
+    float* tile = tile_all[warp];
+    uint64_t* bar = &bars[warp];
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
     }
-    rec[3 * i] = make_float4(g.mx, g.my, g.A, g.B);
-    rec[3 * i + 1] = make_float4(g.C, op, fmaxf(col[0], 0.f), fmaxf(col[1], 0.f));
-    rec[3 * i + 2] = make_float4(fmaxf(col[2], 0.f), 0.f, 0.f, 0.f);
-    radius[i] = r;
-    tiles_touched[i] = tt;
+    unsigned parity = 0;
+    // the first group's geometry
+    float m[3] = {0.f, 0.f, 0.f}, ls[3] = {0.f, 0.f, 0.f}, q[4] = {1.f, 0.f, 0.f, 0.f};
+    {
+        const int i = grp * 32 + lane;
+        if (i < n) {
+            m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
+            ls[0] = log_scale[3 * i]; ls[1] = log_scale[3 * i + 1]; ls[2] = log_scale[3 * i + 2];
+            q[0] = quat[4 * i]; q[1] = quat[4 * i + 1]; q[2] = quat[4 * i + 2]; q[3] = quat[4 * i + 3];
+        }
+    }
+    for (; grp < groups; grp += wstride) {
+        const int i = grp * 32 + lane;
+        Geo g;
+        int r = 0;
+        unsigned tt = 0;
+        const bool ok = i < n && project_one(i, m, ls, q, cam, g, r, tt, rec, depth, radius, tiles_touched);
+        const unsigned vis = __ballot_sync(0xffffffffu, ok);
+        if (vis) {
+            // the rows of the previous group have been read by every lane (the warp synchronised
+            // at the end of the last iteration) before the copies overwrite them
+            if (lane == 0) mbar_arrive_expect_tx(bar, (unsigned)(K3 * 4) * __popc(vis));
+            __syncwarp();
+            if (ok) {
+                fence_proxy_async_smem();
+                bulk_copy_g2s(tile + lane * S, sh + (size_t)i * K3, K3 * 4, bar);
+            }
+        }
+        const float lg = ok ? logit[i] : 0.f;
+        const float mc[3] = {m[0], m[1], m[2]};
+        const int nxt = grp + wstride;
+        if (nxt < groups) {  // the next group's geometry, in flight while this group's rows land
+            const int j = nxt * 32 + lane;
+            if (j < n) {
+                m[0] = mean3d[3 * j]; m[1] = mean3d[3 * j + 1]; m[2] = mean3d[3 * j + 2];
+                ls[0] = log_scale[3 * j]; ls[1] = log_scale[3 * j + 1]; ls[2] = log_scale[3 * j + 2];
+                q[0] = quat[4 * j]; q[1] = quat[4 * j + 1]; q[2] = quat[4 * j + 2]; q[3] = quat[4 * j + 3];
+            }
+        }
+        if (vis) {
+            if (!mbar_wait_bounded(bar, parity, spin_limit, err)) {
+                mbar_wait_bounded(bar, parity, kDrainLimit, err);  // let the copies land, then give up
+                return;
+            }
+            parity ^= 1u;
+        }
+        if (ok) shade_one<DEG, true>(i, mc, g, r, tt, lg, tile + lane * S, cam, rec, radius, tiles_touched);
+        __syncwarp();
+    }
 }
 
 constexpr int kBwdThreads = 128;
 
 // STATS: also the post-backward statistics of the view (see DensifyArgs), from the gradients this
-// call computes.
-template <int DEG, bool STATS>
+// call computes. BULK: SH rows in and SH-gradient rows out through the bulk-copy engine (see
+// ShRows), the latter as bulk additions when accumulating.
+template <int DEG, bool STATS, bool BULK>
 __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
     const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
     const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
     float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
-    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate, const DensifyArgs stats) {
+    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate, const DensifyArgs stats,
+    unsigned spin_limit, unsigned* __restrict__ err) {
     pdl_entry();
     constexpr int K = (DEG + 1) * (DEG + 1);
     constexpr int K3 = 3 * K;
-    __shared__ float tile_all[kBwdThreads / 32][32 * (K3 + 1)];
+    constexpr int S = ShRows<K3>::template stride<BULK>;
+    static_assert(!BULK || ShRows<K3>::kBulkable, "bulk SH rows need a multiple of 16 bytes");
+    __shared__ __align__(16) float tile_all[kBwdThreads / 32][32 * S];
+    __shared__ uint64_t bars[kBwdThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float* tile = tile_all[warp];
     const int warp_first = blockIdx.x * kBwdThreads + warp * 32;
+    if (BULK && warp_first >= n) return;  // whole warp
     const int i = warp_first + lane;
+    if (BULK && lane == 0) {
+        mbar_init(&bars[warp], 1);
+        fence_mbar_init();
+    }
     // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only. The rows'
     // copies, the geometry and the 2D gradients are all in flight before the first wait.
     const int rad = i < n ? radius[i] : 0;
     const unsigned seen = __ballot_sync(0xffffffffu, rad > 0);
-    sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    float* my = tile + lane * S;   // this thread's coefficients, then its SH gradients
+    if constexpr (BULK) {
+        if (seen) {
+            if (lane == 0) mbar_arrive_expect_tx(&bars[warp], (unsigned)(K3 * 4) * __popc(seen));
+            __syncwarp();
+            if (rad > 0) bulk_copy_g2s(my, sh + (size_t)i * K3, K3 * 4, &bars[warp]);
+        }
+    } else {
+        sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    }
     bool live = i < n && ((seen >> lane) & 1u);
     float m[3] = {0.f, 0.f, 0.f}, ls[3] = {0.f, 0.f, 0.f}, q[4] = {1.f, 0.f, 0.f, 0.f}, lg = 0.f;
     float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0, g2 = g0;
@@ -221,14 +379,24 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
         g0 = grad2d[3 * i]; g1 = grad2d[3 * i + 1]; g2 = grad2d[3 * i + 2];
         lg = logit[i];
     }
-    cp_async_wait_all();
-    __syncwarp();
-    float* my = tile + lane * (K3 + 1);   // this thread's coefficients, then its SH gradients
+    if constexpr (BULK) {
+        if (seen && !mbar_wait_bounded(&bars[warp], 0u, spin_limit, err)) {
+            mbar_wait_bounded(&bars[warp], 0u, kDrainLimit, err);  // let the copies land, then give up
+            return;
+        }
+    } else {
+        cp_async_wait_all();
+        __syncwarp();
+    }
     float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
     Geo g;
     if (live) live = geometry(m, ls, q, cam, g);
     if (i < n && !live) {
-        for (int k = 0; k < K3; ++k) my[k] = 0.f;
+        if constexpr (BULK) {
+            for (int j = 0; j < K3 / 4; ++j) reinterpret_cast<float4*>(my)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            for (int k = 0; k < K3; ++k) my[k] = 0.f;
+        }
     }
     if (i < n && live) {
     const float dmx = g0.x, dmy = g0.y, dA = g0.z, dB = g0.w, dC = g1.x, dop = g1.y;
@@ -237,39 +405,6 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     // opacity = sigmoid(logit)
     const float op = 1.f / (1.f + expf(-lg));
     dlg = dop * op * (1.f - op);
-
-    // colour = sum_k Y_k sh_k + 0.5, clamped at 0
-    float vx = m[0] - cam.campos[0], vy = m[1] - cam.campos[1], vz = m[2] - cam.campos[2];
-    const float vinv = rsqrtf(vx * vx + vy * vy + vz * vz);
-    const float ux = vx * vinv, uy = vy * vinv, uz = vz * vinv;
-    float Y[16];
-    sh_basis<DEG>(ux, uy, uz, Y);
-    float col[3] = {0.5f, 0.5f, 0.5f};
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        col[0] += Y[k] * my[3 * k];
-        col[1] += Y[k] * my[3 * k + 1];
-        col[2] += Y[k] * my[3 * k + 2];
-    }
-    float dc[3];
-    for (int ch = 0; ch < 3; ++ch) dc[ch] = (col[ch] < 0.f) ? 0.f : drgb[ch];
-    float wk[16];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        wk[k] = my[3 * k] * dc[0] + my[3 * k + 1] * dc[1] + my[3 * k + 2] * dc[2];
-        my[3 * k] = Y[k] * dc[0];      // the row now holds dL/dsh
-        my[3 * k + 1] = Y[k] * dc[1];
-        my[3 * k + 2] = Y[k] * dc[2];
-    }
-    if (DEG > 0) {
-        float gd[3] = {0.f, 0.f, 0.f};
-        sh_basis_grad<DEG>(ux, uy, uz, wk, gd);
-        // through the normalisation: (I - u u^T) / |v|
-        const float dot = gd[0] * ux + gd[1] * uy + gd[2] * uz;
-        dm[0] += (gd[0] - dot * ux) * vinv;
-        dm[1] += (gd[1] - dot * uy) * vinv;
-        dm[2] += (gd[2] - dot * uz) * vinv;
-    }
 
     // Conic M = Sigma'^-1 with Sigma' = K K^T + lp I. With G = [[dA, dB/2], [dB/2, dC]] (B sits in both
     // off-diagonal slots), dL/dSigma' = -M G M and dL/dK = -2 M G M K. Forming M G M and then
@@ -345,6 +480,53 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     const float dotq = dqn[0] * w + dqn[1] * x + dqn[2] * y + dqn[3] * z;
     for (int k = 0; k < 4; ++k) dq[k] = (dqn[k] - dotq * g.qn[k]) * g.qinv;
 
+    // colour = sum_k Y_k sh_k + 0.5, clamped at 0 (last: the geometry is no longer live here)
+    float vx = m[0] - cam.campos[0], vy = m[1] - cam.campos[1], vz = m[2] - cam.campos[2];
+    const float vinv = rsqrtf(vx * vx + vy * vy + vz * vz);
+    const float ux = vx * vinv, uy = vy * vinv, uz = vz * vinv;
+    float Y[16];
+    sh_basis<DEG>(ux, uy, uz, Y);
+    float col[3];
+    sh_colour<K, BULK>(my, Y, col);
+    float dc[3];
+    for (int ch = 0; ch < 3; ++ch) dc[ch] = (col[ch] < 0.f) ? 0.f : drgb[ch];
+    // w_k = sum_c sh_kc dc_c (c in increasing order, fused multiply-adds), and the row now holds
+    // dL/dsh_kc = Y_k dc_c
+    float wk[16];
+    if constexpr (BULK) {
+        float4* r4 = reinterpret_cast<float4*>(my);
+#pragma unroll
+        for (int j = 0; j < K3 / 4; ++j) {
+            const float4 v = r4[j];
+            const float e[4] = {v.x, v.y, v.z, v.w};
+            float o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int f = 4 * j + t, k = f / 3, c = f % 3;
+                wk[k] = c == 0 ? e[t] * dc[0] : __fmaf_rn(e[t], dc[c], wk[k]);
+                o[t] = Y[k] * dc[c];
+            }
+            r4[j] = make_float4(o[0], o[1], o[2], o[3]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            wk[k] = __fmaf_rn(my[3 * k + 2], dc[2], __fmaf_rn(my[3 * k + 1], dc[1], my[3 * k] * dc[0]));
+            my[3 * k] = Y[k] * dc[0];
+            my[3 * k + 1] = Y[k] * dc[1];
+            my[3 * k + 2] = Y[k] * dc[2];
+        }
+    }
+    if (DEG > 0) {
+        float gd[3] = {0.f, 0.f, 0.f};
+        sh_basis_grad<DEG>(ux, uy, uz, wk, gd);
+        // through the normalisation: (I - u u^T) / |v|
+        const float dot = gd[0] * ux + gd[1] * uy + gd[2] * uz;
+        dm[0] += (gd[0] - dot * ux) * vinv;
+        dm[1] += (gd[1] - dot * uy) * vinv;
+        dm[2] += (gd[2] - dot * uz) * vinv;
+    }
+
     }  // live
     if (STATS && i < n) {
         // 3D Gaussian splatting's densification statistics and the 2-norm of this view's parameter
@@ -361,10 +543,12 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
                 for (int k = 0; k < 3; ++k) ss = __fmaf_rn(dm[k], dm[k], __fmaf_rn(dls[k], dls[k], ss));
                 ss = __fmaf_rn(dq[0], dq[0], __fmaf_rn(dq[1], dq[1], __fmaf_rn(dq[2], dq[2], __fmaf_rn(dq[3], dq[3], ss))));
                 ss = __fmaf_rn(dlg, dlg, ss);
-                if (K3 % 4 == 0) {
-                    for (int k = 0; k < K3; k += 4)
-                        ss = __fmaf_rn(my[k], my[k], __fmaf_rn(my[k + 1], my[k + 1],
-                                       __fmaf_rn(my[k + 2], my[k + 2], __fmaf_rn(my[k + 3], my[k + 3], ss))));
+                if constexpr (K3 % 4 == 0) {
+                    for (int k = 0; k < K3; k += 4) {
+                        const float4 v = BULK ? reinterpret_cast<const float4*>(my)[k / 4]
+                                              : make_float4(my[k], my[k + 1], my[k + 2], my[k + 3]);
+                        ss = __fmaf_rn(v.x, v.x, __fmaf_rn(v.y, v.y, __fmaf_rn(v.z, v.z, __fmaf_rn(v.w, v.w, ss))));
+                    }
                 } else {
                     for (int k = 0; k < K3; ++k) ss = __fmaf_rn(my[k], my[k], ss);
                 }
@@ -383,21 +567,58 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
             d_logit[i] = dlg;
         }
     }
-    __syncwarp();
     // accumulating: rows of Gaussians with radius 0 add nothing and are skipped
-    if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane, seen);
-    else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane, 0xffffffffu);
+    if constexpr (BULK) {
+        if (i < n && (!accumulate || rad > 0)) {
+            fence_proxy_async_smem();
+            if (accumulate) bulk_add_s2g(d_sh + (size_t)i * K3, my, K3 * 4);
+            else bulk_copy_s2g(d_sh + (size_t)i * K3, my, K3 * 4);
+            bulk_wait_read();
+        }
+    } else {
+        __syncwarp();
+        if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane, seen);
+        else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane, 0xffffffffu);
+    }
 }
 
 // ---- host-side launchers ------------------------------------------------------------------------
 
+namespace {
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+// Blocks of `kernel` (kFwdThreads threads, static shared memory only) resident on the current device
+// at once: SMs x blocks per SM, looked up once per device; 0 if the query fails.
+template <class Kernel>
+int resident_blocks(Kernel kernel, std::atomic<int> (&cache)[256]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        int per = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kFwdThreads, 0) != cudaSuccess) return 0;
+        v = device_sm_count() * (per > 0 ? per : 1);
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
-                              cudaStream_t st) {
+                              unsigned spin_limit, unsigned* err, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     const int blocks = (n + kFwdThreads - 1) / kFwdThreads;
     float4* rec = reinterpret_cast<float4*>(out.rec);
     unsigned* tt = out.tiles_touched;
     count_launches(1);
+    if ((deg == 1 || deg == 3) && aligned16(p.sh)) {
+        static std::atomic<int> cache1[256], cache3[256];
+        auto k = deg == 1 ? k_preprocess_pipe<1> : k_preprocess_pipe<3>;
+        const int res = resident_blocks(k, deg == 1 ? cache1 : cache3);
+        const int grid = res > 0 && res < blocks ? res : blocks;
+        return launch_pdl(k, dim3(grid), dim3(kFwdThreads), 0, st, n, p.mean3d, p.log_scale, p.quat,
+                          p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt, spin_limit, err);
+    }
     void (*k)(int, const float*, const float*, const float*, const float*, const float*, const KernelCamera, float4*,
               float*, int*, unsigned*) = deg == 0 ? k_preprocess<0> : deg == 1 ? k_preprocess<1>
                                                 : deg == 2 ? k_preprocess<2> : k_preprocess<3>;
@@ -407,25 +628,27 @@ cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCa
 
 cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
                                   const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
-                                  int accumulate, const DensifyArgs* stats, cudaStream_t st) {
+                                  int accumulate, const DensifyArgs* stats, unsigned spin_limit, unsigned* err,
+                                  cudaStream_t st) {
     if (n == 0) return cudaSuccess;
     const int blocks = (n + kBwdThreads - 1) / kBwdThreads;
     const float4* g2 = reinterpret_cast<const float4*>(grad2d);
     const DensifyArgs none{};
+    const bool bulk = aligned16(p.sh) && aligned16(dsh);
     count_launches(1);
-#define GS_PREBWD(D)                                                                                          \
-    (stats ? launch_pdl(k_preprocess_bwd<D, true>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,         \
+#define GS_PREBWD(D, B)                                                                                        \
+    (stats ? launch_pdl(k_preprocess_bwd<D, true, B>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,      \
                         p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh,      \
-                        accumulate, *stats)                                                                     \
-           : launch_pdl(k_preprocess_bwd<D, false>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,        \
+                        accumulate, *stats, spin_limit, err)                                                    \
+           : launch_pdl(k_preprocess_bwd<D, false, B>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,     \
                         p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh,      \
-                        accumulate, none))
+                        accumulate, none, spin_limit, err))
     cudaError_t e;
     switch (deg) {
-        case 0: e = GS_PREBWD(0); break;
-        case 1: e = GS_PREBWD(1); break;
-        case 2: e = GS_PREBWD(2); break;
-        default: e = GS_PREBWD(3); break;
+        case 0: e = GS_PREBWD(0, false); break;
+        case 1: e = bulk ? GS_PREBWD(1, true) : GS_PREBWD(1, false); break;
+        case 2: e = GS_PREBWD(2, false); break;
+        default: e = bulk ? GS_PREBWD(3, true) : GS_PREBWD(3, false); break;
     }
 #undef GS_PREBWD
     return e;

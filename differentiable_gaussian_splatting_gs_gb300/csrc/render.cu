@@ -1,6 +1,8 @@
 // Rendering phase (forward alpha blending) and gradient computation phase (backward) of the tile
-// rasterizer: one 128-thread block per 16x16-pixel tile, two pixels per thread, the tile's sorted
-// list staged in shared memory in batches of 128 records.
+// rasterizer: one block per 16x16-pixel tile, the tile's sorted list staged in shared memory in
+// batches of one record per thread. The forward uses 128 threads with two pixels each; the
+// backward 64 threads with four pixels each (or the forward's layout on images of fewer than two
+// tiles per SM).
 //
 // The backward accumulates each Gaussian's gradient over all pixels with atomics; that
 // accumulation is the bottleneck that DISTWAR (Fast Differentiable Rendering on Raster-based
@@ -9,7 +11,8 @@
 //
 // Warp layout: warp w covers the 8x8 pixel block at (8 (w & 1), 8 (w >> 1)) of the tile; lane l
 // holds pixels (l & 7, l >> 3) and (l & 7, (l >> 3) + 4), so that a Gaussian's record loads and
-// culling test (and in the backward its warp reduction and atomics) serve 64 pixels.
+// culling test serve 64 pixels. The backward's 16x8 layout (BwdLayout) has its record loads,
+// culling test, warp reduction and atomics serve 128 pixels.
 //
 // Warp-level culling. Before blending a batch, each warp keeps only the staged Gaussians whose
 // alpha can reach 1/255 somewhere in its 8x8 block: the set alpha >= 1/255 is the ellipse
@@ -33,9 +36,6 @@ constexpr float kAlphaMin = 1.0f / 255.0f;
 constexpr float kTMin = 1e-4f;
 constexpr float kAlphaMax = 0.99f;
 constexpr float kNegHalfLog2e = -0.72134752044448170f;  // -log2(e) / 2
-// Bound of the waits that let in-flight bulk copies land before a block exits early; independent
-// of the caller's spin limit so that a small limit cannot leave copies running into a dead block.
-constexpr unsigned kDrainLimit = 1u << 22;
 
 // Shared-memory staging ring of BATCH records for a block of WARPS warps (one record per thread).
 template <int BATCH, int WARPS>
@@ -54,14 +54,26 @@ struct StageSmemT {
 constexpr int kFwdBlock = 128;
 constexpr int kFwdBatch = 128;
 using FwdStage = StageSmemT<kFwdBatch, 4>;
-constexpr int kBwdBlock = 128;
-constexpr int kBwdBatch = 128;
-using BwdStage = StageSmemT<kBwdBatch, 4>;
+// Backward layouts, PX pixels per lane: PX = 2 is the forward's layout (128 threads, 8x8 warp
+// blocks); PX = 4 gives each warp a 16x8 block (64 threads per tile; warp w covers rows 8w..8w+7,
+// lane l the column l & 15 and the rows (l >> 4) + 2q, q = 0..3). A larger warp block meets each
+// Gaussian fewer times per tile, so the per-Gaussian work of a warp (record loads, culling, the
+// gradient reduction and its atomics) is shared by twice as many pixels. One staged record per
+// thread and batch.
+template <int PX>
+struct BwdLayout {
+    static constexpr int kThreads = PX == 2 ? 128 : 64;
+    static constexpr int kWarps = kThreads / 32;
+    static constexpr int kBatch = kThreads;
+    static constexpr int kBlockW = PX == 2 ? 8 : 16;   // warp block width; its height is 8
+    static constexpr int kRowStep = 32 / kBlockW;      // rows between a lane's pixels
+};
 
-struct BwdSmem {
-    BwdStage st;
-    float acc[kBwdBatch * 9];      // per-batch gradient accumulators (GS_BWD_SM)
-    unsigned wmax[4];
+template <int PX>
+struct BwdSmemT {
+    StageSmemT<BwdLayout<PX>::kBatch, BwdLayout<PX>::kWarps> st;
+    float acc[BwdLayout<PX>::kBatch * 9];   // per-batch gradient accumulators (GS_BWD_SM)
+    unsigned wmax[BwdLayout<PX>::kWarps];
 };
 
 // Prepares a staged record for evaluation and returns its culling record.
@@ -381,76 +393,71 @@ __device__ __forceinline__ void pixel_step(float alpha, float oG, const float4& 
 
 // dl_dimage: dL/dpixel, or with `target` the rendered image, and dL/dpixel = image - target (the
 // gradient of the squared error 0.5 |image - target|^2, whose sum is added to *loss when given).
-template <int MODE, int STAGING>
-__global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restrict__ rec,
-                                                          const unsigned* __restrict__ vals,
-                                                          const uint2* __restrict__ ranges, const KernelCamera cam,
-                                                          unsigned n_gauss, const float* __restrict__ dl_dimage,
-                                                          const float* __restrict__ target, float* __restrict__ loss,
-                                                          const float* __restrict__ t_final,
-                                                          const unsigned* __restrict__ n_contrib,
-                                                          float* __restrict__ grad2d, int thr, unsigned spin_limit,
-                                                          unsigned* __restrict__ err) {
+template <int MODE, int STAGING, int PX>
+__global__ void __launch_bounds__(BwdLayout<PX>::kThreads) k_render_bwd(
+    const float4* __restrict__ rec, const unsigned* __restrict__ vals, const uint2* __restrict__ ranges,
+    const KernelCamera cam, unsigned n_gauss, const float* __restrict__ dl_dimage, const float* __restrict__ target,
+    float* __restrict__ loss, const float* __restrict__ t_final, const unsigned* __restrict__ n_contrib,
+    float* __restrict__ grad2d, int thr, unsigned spin_limit, unsigned* __restrict__ err) {
     pdl_entry();
-    constexpr int kB = kBwdBatch;
-    __shared__ BwdSmem sm;
-    BwdStage& s = sm.st;
+    using L = BwdLayout<PX>;
+    constexpr int kB = L::kBatch;
+    __shared__ BwdSmemT<PX> sm;
+    auto& s = sm.st;
     const int tile = blockIdx.x;
     const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bx = tx * kTile + 8 * (warp & 1), by = ty * kTile + 8 * (warp >> 1);
-    const int px = bx + (lane & 7), py0 = by + (lane >> 3), py1 = py0 + 4;
-    const float fpx = (float)px + 0.5f, fpy0 = (float)py0 + 0.5f, fpy1 = (float)py1 + 0.5f;
-    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 7.f;
+    const int bx = tx * kTile + (PX == 2 ? 8 * (warp & 1) : 0);
+    const int by = ty * kTile + (PX == 2 ? 8 * (warp >> 1) : 8 * warp);
+    const int px = bx + lane % L::kBlockW, py = by + lane / L::kBlockW;
+    const float fpx = (float)px + 0.5f;
+    const float wx0 = (float)bx + 0.5f, wx1 = wx0 + (float)(L::kBlockW - 1), wy0 = (float)by + 0.5f, wy1 = wy0 + 7.f;
 
     const uint2 rg = ranges[tile];
     const int start = (int)rg.x;
     const int count = (int)(rg.y > rg.x ? rg.y - rg.x : 0);
 
     const size_t plane = (size_t)cam.width * cam.height;
-    // per pixel: contributor count, transmittance (from T_final backwards), dL/dpixel and the sum
-    // over channels of dL/dpixel_c x (colour blended behind the current Gaussian, background
-    // included), the only form in which that colour enters dL/dalpha
-    unsigned last0 = 0, last1 = 0;
-    float T0 = 1.f, T1 = 1.f, a0 = 0.f, a1 = 0.f, a2 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f;
-    if (px < cam.width && py0 < cam.height) {
-        const size_t pix = (size_t)py0 * cam.width + px;
-        last0 = min(n_contrib[pix], (unsigned)count);
-        T0 = t_final[pix];
-        a0 = dl_dimage[pix];
-        a1 = dl_dimage[plane + pix];
-        a2 = dl_dimage[2 * plane + pix];
-        if (target) {
-            a0 -= target[pix];
-            a1 -= target[plane + pix];
-            a2 -= target[2 * plane + pix];
+    // per pixel q of the lane: its row offset dyo, contributor count, transmittance (from T_final
+    // backwards), dL/dpixel and the sum over channels of dL/dpixel_c x (colour blended behind the
+    // current Gaussian, background included), the only form in which that colour enters dL/dalpha
+    float fpy[PX], T[PX], gS[PX], ga[PX][3];
+    unsigned last[PX];
+    float lsum = 0.f;
+    unsigned lmax = 0;
+#pragma unroll
+    for (int q = 0; q < PX; ++q) {
+        const int y = py + q * L::kRowStep;
+        fpy[q] = (float)y + 0.5f;
+        last[q] = 0;
+        T[q] = 1.f;
+        ga[q][0] = ga[q][1] = ga[q][2] = 0.f;
+        if (px < cam.width && y < cam.height) {
+            const size_t pix = (size_t)y * cam.width + px;
+            last[q] = min(n_contrib[pix], (unsigned)count);
+            T[q] = t_final[pix];
+#pragma unroll
+            for (int c = 0; c < 3; ++c) {
+                ga[q][c] = dl_dimage[c * plane + pix];
+                if (target) ga[q][c] -= target[c * plane + pix];
+            }
         }
-    }
-    if (px < cam.width && py1 < cam.height) {
-        const size_t pix = (size_t)py1 * cam.width + px;
-        last1 = min(n_contrib[pix], (unsigned)count);
-        T1 = t_final[pix];
-        b0 = dl_dimage[pix];
-        b1 = dl_dimage[plane + pix];
-        b2 = dl_dimage[2 * plane + pix];
-        if (target) {
-            b0 -= target[pix];
-            b1 -= target[plane + pix];
-            b2 -= target[2 * plane + pix];
-        }
+        lsum += __fmaf_rn(ga[q][0], ga[q][0], __fmaf_rn(ga[q][1], ga[q][1], ga[q][2] * ga[q][2]));
+        gS[q] = T[q] * (ga[q][0] * cam.bg[0] + ga[q][1] * cam.bg[1] + ga[q][2] * cam.bg[2]);
+        lmax = max(lmax, last[q]);
     }
     if (loss) {
-        float l = 0.5f * (__fmaf_rn(a0, a0, __fmaf_rn(a1, a1, a2 * a2)) + __fmaf_rn(b0, b0, __fmaf_rn(b1, b1, b2 * b2)));
+        float l = 0.5f * lsum;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         if (lane == 0) red_add_global(loss, l);
     }
-    float gS0 = T0 * (a0 * cam.bg[0] + a1 * cam.bg[1] + a2 * cam.bg[2]);
-    float gS1 = T1 * (b0 * cam.bg[0] + b1 * cam.bg[1] + b2 * cam.bg[2]);
-    const unsigned wmax = __reduce_max_sync(0xffffffffu, max(last0, last1));
+    const unsigned wmax = __reduce_max_sync(0xffffffffu, lmax);
     if (lane == 0) sm.wmax[warp] = wmax;
     __syncthreads();
-    const unsigned tmax = max(max(sm.wmax[0], sm.wmax[1]), max(sm.wmax[2], sm.wmax[3]));
+    unsigned tmax = 0;
+#pragma unroll
+    for (int w = 0; w < L::kWarps; ++w) tmax = max(tmax, sm.wmax[w]);
     const int nb = ((int)tmax + kB - 1) / kB;
     float4 pre[3];
 
@@ -488,7 +495,7 @@ __global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restri
             s.cull[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
                                                  s.rec[slot][threadIdx.x][2], s.cull2[threadIdx.x]);
         if (MODE == GS_BWD_SM)
-            for (int e = threadIdx.x; e < kB * 9; e += kBwdBlock) sm.acc[e] = 0.f;
+            for (int e = threadIdx.x; e < kB * 9; e += L::kThreads) sm.acc[e] = 0.f;
         if (__syncthreads_or(!ok)) break;
         const int pos_limit = (int)wmax - b * kB;
         const int nl = compact_warp(s, n_in, pos_limit, wx0, wx1, wy0, wy1, warp, lane);
@@ -498,52 +505,65 @@ __global__ void __launch_bounds__(kBwdBlock) k_render_bwd(const float4* __restri
             const float4 r0 = s.rec[slot][j][0];   // (mean_x, mean_y, A, B)
             const float4 r1 = s.rec[slot][j][1];   // (D, o, r, g)
             const float4 r2 = s.rec[slot][j][2];   // (b, r, A', D')
-            const float dx = r0.x - fpx, dy0 = r0.y - fpy0, dy1 = r0.y - fpy1;
-            const float u0 = __fmaf_rn(r2.y, dy0, dx), u1 = __fmaf_rn(r2.y, dy1, dx);
-            const float G0 = ex2_approx(__fmaf_rn(r2.z * u0, u0, r2.w * dy0 * dy0));  // exp(power)
-            const float G1 = ex2_approx(__fmaf_rn(r2.z * u1, u1, r2.w * dy1 * dy1));
-            const float oG0 = r1.y * G0, oG1 = r1.y * G1;
-            const float alpha0 = fminf(kAlphaMax, oG0), alpha1 = fminf(kAlphaMax, oG1);
-            const bool c0 = pos < last0 && alpha0 >= kAlphaMin;
-            const bool c1 = pos < last1 && alpha1 >= kAlphaMin;
-            const unsigned ballot = __ballot_sync(0xffffffffu, c0 || c1);
+            const float dx = r0.x - fpx;
+            float dy[PX], u[PX], oG[PX], alpha[PX];
+            bool c[PX];
+            bool any = false;
+#pragma unroll
+            for (int q = 0; q < PX; ++q) {
+                dy[q] = r0.y - fpy[q];
+                u[q] = __fmaf_rn(r2.y, dy[q], dx);
+                oG[q] = r1.y * ex2_approx(__fmaf_rn(r2.z * u[q], u[q], r2.w * dy[q] * dy[q]));  // o exp(power)
+                alpha[q] = fminf(kAlphaMax, oG[q]);
+                c[q] = pos < last[q] && alpha[q] >= kAlphaMin;
+                any |= c[q];
+            }
+            const unsigned ballot = __ballot_sync(0xffffffffu, any);
             if (ballot == 0u) continue;
-            float aT0 = 0.f, dp0 = 0.f, aT1 = 0.f, dp1 = 0.f;
-            if (c0) pixel_step(alpha0, oG0, r1, r2, T0, gS0, a0, a1, a2, aT0, dp0);
-            if (c1) pixel_step(alpha1, oG1, r1, r2, T1, gS1, b0, b1, b2, aT1, dp1);
-            // The lane's sums over its two pixels. The geometric gradients are linear in dL/dpower
+            // The lane's sums over its pixels. The geometric gradients are linear in dL/dpower
             // with pixel-dependent factors: d power / d mean = -(A u, B u + D dy), d power / d(A, B, C)
-            // = -(dx^2 / 2, dx dy, dy^2 / 2), and both pixels share dx, so the lane forms the moments
-            // P = sum dp, M = sum dp u, F = sum dp dy once and converts them; dL/dopacity =
-            // sum G dL/dalpha = P / o.
-            const float P = dp0 + dp1;
-            const float M = __fmaf_rn(dp0, u0, dp1 * u1);
-            const float f0 = dp0 * dy0, f1 = dp1 * dy1;
-            const float F = f0 + f1;
+            // = -(dx^2 / 2, dx dy, dy^2 / 2), and the lane's pixels share dx, so the lane forms the
+            // moments P = sum dp, M = sum dp u, F = sum dp dy, Q = sum dp dy^2 once and converts
+            // them; dL/dopacity = sum G dL/dalpha = P / o.
+            float P = 0.f, M = 0.f, F = 0.f, Q = 0.f, cg0 = 0.f, cg1 = 0.f, cg2 = 0.f;
+#pragma unroll
+            for (int q = 0; q < PX; ++q) {
+                if (c[q]) {
+                    float aT, dp;
+                    pixel_step(alpha[q], oG[q], r1, r2, T[q], gS[q], ga[q][0], ga[q][1], ga[q][2], aT, dp);
+                    P += dp;
+                    M = __fmaf_rn(dp, u[q], M);
+                    const float f = dp * dy[q];
+                    F += f;
+                    Q = __fmaf_rn(f, dy[q], Q);
+                    cg0 = __fmaf_rn(aT, ga[q][0], cg0);
+                    cg1 = __fmaf_rn(aT, ga[q][1], cg1);
+                    cg2 = __fmaf_rn(aT, ga[q][2], cg2);
+                }
+            }
             float v[9];
             v[0] = -r0.z * M;
             v[1] = -__fmaf_rn(r0.w, M, r1.x * F);
             v[2] = (-0.5f * dx * dx) * P;
             v[3] = -dx * F;
-            v[4] = -0.5f * __fmaf_rn(f0, dy0, f1 * dy1);
+            v[4] = -0.5f * Q;
             v[5] = P * rcp_approx(r1.y);
-            v[6] = __fmaf_rn(aT0, a0, aT1 * b0);
-            v[7] = __fmaf_rn(aT0, a1, aT1 * b1);
-            v[8] = __fmaf_rn(aT0, a2, aT1 * b2);
-            const bool contrib = c0 || c1;
+            v[6] = cg0;
+            v[7] = cg1;
+            v[8] = cg2;
             const int nact = __popc(ballot);
             if (MODE == GS_BWD_DIRECT || (MODE == GS_BWD_ADAPTIVE && nact < thr)) {
-                if (contrib) {
+                if (any) {
                     float* gp = grad2d + 12 * (size_t)s.gidx[slot][j];
                     red_add_global_v4(gp, v[0], v[1], v[2], v[3]);
                     red_add_global_v4(gp + 4, v[4], v[5], v[6], v[7]);
                     red_add_global(gp + 8, v[8]);
                 }
             } else if (MODE == GS_BWD_SM && nact < thr) {
-                if (contrib) {
+                if (any) {
                     float* ap = sm.acc + 9 * j;
 #pragma unroll
-                    for (int c = 0; c < 9; ++c) red_add_shared(ap + c, v[c]);
+                    for (int e = 0; e < 9; ++e) red_add_shared(ap + e, v[e]);
                 }
             } else {
                 float v8;
@@ -596,14 +616,29 @@ cudaError_t launch_render_fwd(int staging, const gs_proj& proj, const unsigned* 
                       n_contrib, spin_limit, err);
 }
 
+template <int MODE, int PX>
+static cudaError_t launch_bwd_layout(int staging, int tiles, const float4* rec, const unsigned* vals, const uint2* rg,
+                                     const KernelCamera& cam, unsigned n, const float* dl, const float* target,
+                                     float* loss, const float* tf, const unsigned* nc, float* g2, int thr,
+                                     unsigned spin, unsigned* err, cudaStream_t st) {
+    return launch_pdl(staging == GS_STAGE_LOADS ? k_render_bwd<MODE, GS_STAGE_LOADS, PX>
+                                                : k_render_bwd<MODE, GS_STAGE_BULK, PX>,
+                      dim3(tiles), dim3(BwdLayout<PX>::kThreads), 0, st, rec, vals, rg, cam, n, dl, target, loss, tf, nc,
+                      g2, thr, spin, err);
+}
+
+// The 16x8 warp blocks (two warps per tile) unless the image has fewer than two tiles per SM, where
+// the 8x8 blocks (four warps per tile) keep more warps in flight.
 template <int MODE>
 static cudaError_t launch_bwd_mode(int staging, int tiles, const float4* rec, const unsigned* vals, const uint2* rg,
                                    const KernelCamera& cam, unsigned n, const float* dl, const float* target,
                                    float* loss, const float* tf, const unsigned* nc, float* g2, int thr, unsigned spin,
                                    unsigned* err, cudaStream_t st) {
-    return launch_pdl(staging == GS_STAGE_LOADS ? k_render_bwd<MODE, GS_STAGE_LOADS> : k_render_bwd<MODE, GS_STAGE_BULK>,
-                      dim3(tiles), dim3(kBwdBlock), 0, st, rec, vals, rg, cam, n, dl, target, loss, tf, nc, g2, thr, spin,
-                      err);
+    if (tiles < 2 * device_sm_count())
+        return launch_bwd_layout<MODE, 2>(staging, tiles, rec, vals, rg, cam, n, dl, target, loss, tf, nc, g2, thr, spin,
+                                          err, st);
+    return launch_bwd_layout<MODE, 4>(staging, tiles, rec, vals, rg, cam, n, dl, target, loss, tf, nc, g2, thr, spin,
+                                      err, st);
 }
 
 cudaError_t launch_render_bwd(int mode, int staging, int thr, const gs_proj& proj, const unsigned* vals,

@@ -56,8 +56,9 @@ extern "C" {
 /* ---- backward accumulation modes (gs_options.bwd_mode) ------------------------------------
  * How gs_render_bwd accumulates the per-pixel gradient contributions of a Gaussian into its
  * per-Gaussian gradient. All modes compute the same sums (up to float rounding order).
- * A lane of the backward holds two pixels of its warp's 8x8 block; a lane contributes when
- * either of its pixels does, and adds the sum of its pixels' values.
+ * A lane of the backward holds four pixels (one column of its warp's 16x8 block; two pixels of
+ * an 8x8 block on images of fewer than two tiles per SM); a lane contributes when any of its
+ * pixels does, and adds the sum of its pixels' values.
  *   DIRECT    every contributing lane adds its 9 values with its own global atomics: the
  *             L2-atomic-bound baseline that DISTWAR speeds up (DISTWAR, Abstract).
  *   WARP      the warp sums its lanes' contributions in registers (shuffle reduction) and one
@@ -68,7 +69,7 @@ extern "C" {
  *             nearly every lane contributes.
  *   SM        warps add into a per-tile shared-memory accumulator (warp-reduced when at least
  *             `adaptive_threshold` lanes contribute, per lane otherwise); the tile issues one set
- *             of global atomics per Gaussian and 128-Gaussian batch.                            */
+ *             of global atomics per Gaussian and batch (one record per thread of the tile).   */
 #define GS_BWD_DEFAULT  0
 #define GS_BWD_DIRECT   1
 #define GS_BWD_WARP     2
@@ -136,9 +137,11 @@ typedef struct gs_proj {
  * radius = ceil(3 sqrt(largest eigenvalue)); tile rectangle of tiles overlapping the square of
  * half-side radius around the mean (cull when empty); opacity = sigmoid(logit); colour = real
  * SH of the view direction + 0.5, clamped below at 0. Culled Gaussians get a zero record,
- * radius 0 and tiles_touched 0.
+ * radius 0 and tiles_touched 0. With sh 16-byte aligned and SH degree 1 or 3, a persistent grid
+ * moves the SH rows of visible Gaussians by bulk copies; otherwise by 4-byte copies.
  * Arguments: p (inputs, n >= 0, n < 2^31), cam, opt (may be NULL), out (outputs, out->n == p->n).
- * Errors: GS_ERR_ARG on null/misaligned pointers, bad sh_degree or camera size; GS_ERR_CUDA.  */
+ * Errors: GS_ERR_ARG on null/misaligned pointers, bad sh_degree or camera size; GS_ERR_CUDA; a
+ * bulk-copy wait that gives up sets GS_ERR_TIMEOUT in the device error word.                  */
 int gs_preprocess(const gs_params* p, const gs_camera* cam, const gs_options* opt, gs_proj* out,
                   void* stream);
 
@@ -191,7 +194,9 @@ int gs_render_fwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* til
  * dl_dimage [3][H][W]: dL/drgb = alpha T g; dL/dalpha = sum_ch g_ch (rgb_ch T - S_ch/(1 - alpha))
  * with S the colour blended behind (background included); the derivative through the 0.99
  * clamp is 0. grad2d is [N][12] float32, 16-byte aligned; columns 9..11 are left 0. The callee
- * zeroes grad2d first. Accumulation strategy: opt->bwd_mode (see GS_BWD_*).
+ * zeroes grad2d first. Accumulation strategy: opt->bwd_mode (see GS_BWD_*). One 64-thread block
+ * per tile, four pixels per thread, batches of 64 staged records (the forward's layout on images
+ * of fewer than two tiles per SM).
  * Errors: GS_ERR_ARG, GS_ERR_CUDA; staging timeouts as for gs_render_fwd.                    */
 int gs_render_bwd(const gs_proj* proj, const uint32_t* vals, const uint32_t* tile_ranges,
                   const gs_camera* cam, const gs_options* opt, const float* dl_dimage,
@@ -215,7 +220,10 @@ int gs_render_bwd_sqerr(const gs_proj* proj, const uint32_t* vals, const uint32_
  * gs_preprocess per Gaussian. Outputs d_mean3d [N][3], d_log_scale [N][3], d_quat [N][4]
  * (through the normalisation), d_opacity_logit [N], d_sh [N][K][3]. Gaussians with radius 0
  * (culled) get zeros. accumulate != 0 adds to the outputs (views of one step), else overwrites.
- * Errors: GS_ERR_ARG, GS_ERR_CUDA.                                                           */
+ * With sh and d_sh 16-byte aligned and SH degree 1 or 3, the SH rows are moved by bulk copies (and
+ * added by bulk reductions when accumulating); otherwise by 4-byte copies; the results agree.
+ * Errors: GS_ERR_ARG, GS_ERR_CUDA; a bulk-copy wait that gives up sets GS_ERR_TIMEOUT in the
+ * device error word.                                                                          */
 int gs_preprocess_bwd(const gs_params* p, const gs_camera* cam, const gs_options* opt,
                       const gs_proj* proj, const float* grad2d, float* d_mean3d,
                       float* d_log_scale, float* d_quat, float* d_opacity_logit, float* d_sh,

@@ -59,10 +59,11 @@ struct OrRenderStats {
     int64_t pairs_evaluated;   // (pixel, list entry) pairs visited before termination
     int64_t pairs_blended;     // pairs that were alpha-blended
     int64_t marginal_pixels;   // pixels with at least one marginal decision
-    int64_t warp_gauss_active; // (tile, 8x8 pixel block, Gaussian) triples with >= 1 blending pixel
+    int64_t warp_gauss_active; // (tile, 16x8 pixel block, Gaussian) triples with >= 1 blending pixel
     int64_t tile_gauss_active; // (tile, Gaussian) pairs with >= 1 blending pixel
-    int64_t lane_hist[33];     // histogram over active (8x8 block, Gaussian) of the lanes (pixel pairs
-                               // (x, y), (x, y + 4) of the block) with a blending pixel
+    int64_t lane_hist[33];     // histogram over active (16x8 block, Gaussian) of the lanes (pixel
+                               // columns of four: (x, y), (x, y + 2), (x, y + 4), (x, y + 6) of the
+                               // block) with a blending pixel
 };
 
 }  // extern "C"
@@ -611,8 +612,9 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
             OrRenderStats ls{};
             struct Blend { int64_t pos; uint32_t g; double alpha, T, G, dx, dy; bool clamped; };
             std::vector<Blend> bl;
-            // per tile [4 warps][len]: which lanes have a blending pixel. A warp covers an 8x8 block of
-            // the tile and its lane l the two pixels (l % 8, l / 8) and (l % 8, l / 8 + 4) of it
+            // per tile [2 warps][len]: which lanes have a blending pixel. A warp of the backward covers
+            // a 16x8 block of the tile (rows 8w..8w+7) and its lane l the four pixels
+            // (l % 16, l / 16 + 2q), q = 0..3, of it
             std::vector<uint32_t> wmask;
 #pragma omp for schedule(dynamic, 4)
             for (int64_t tile = grp.t0; tile < grp.t1; ++tile) {
@@ -621,7 +623,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                 const int64_t len = e - s;
                 // this tile's entries in the group's partials (positions s .. e - 1)
                 double* acc = (grad2d && len > 0) ? part.data() + (size_t)(s - grp.p0) * 9 : nullptr;
-                wmask.assign((size_t)len * 4, 0u);
+                wmask.assign((size_t)len * 2, 0u);
                 for (int ly = 0; ly < kTile; ++ly)
                     for (int lx = 0; lx < kTile; ++lx) {
                         const int px = tx * kTile + lx, py = ty * kTile + ly;
@@ -699,7 +701,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                             contrib = (uint32_t)(pos - s + 1);
                             nbl++;
                             ls.pairs_blended++;
-                            wmask[(size_t)((ly / 8) * 2 + lx / 8) * len + (pos - s)] |= 1u << ((lx % 8) + 8 * (ly % 4));
+                            wmask[(size_t)(ly / 8) * len + (pos - s)] |= 1u << (lx + 16 * (ly % 2));
                         }
                         const int64_t pix = (int64_t)py * W + px;
                         for (int ch = 0; ch < 3; ++ch) image[(int64_t)ch * W * H + pix] = col[ch] + Tr * cam->bg[ch];
@@ -743,7 +745,7 @@ int or_render(int64_t n, const double* mean2d, const double* conic, const double
                     }
                 for (int64_t k = 0; k < len; ++k) {
                     bool any = false;
-                    for (int w = 0; w < 4; ++w) {
+                    for (int w = 0; w < 2; ++w) {
                         uint32_t m = wmask[(size_t)w * len + k];
                         if (m) {
                             int c = 0;

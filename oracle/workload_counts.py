@@ -2,10 +2,10 @@
 
 Runs the float64 oracle on one view of a configuration (default: the outdoor scene, 1.6M
 Gaussians, 1297x840, seeded) and writes profiles/workload_counts_<name>.md: duplicates D, (pixel,
-Gaussian) pairs evaluated and blended, active (8x8 pixel block, Gaussian) and (tile, Gaussian)
+Gaussian) pairs evaluated and blended, active (16x8 pixel block, Gaussian) and (tile, Gaussian)
 pairs with the histogram, over the active blocks, of the lanes with a blending pixel (the backward
-kernel's warp covers an 8x8 block with two pixels per lane: the per-warp popcount of DISTWAR's
-observations), and the algorithmic bytes of the backward raster:
+kernel's warp covers a 16x8 block with a column of four pixels per lane: the per-warp popcount of
+DISTWAR's observations), and the algorithmic bytes of the backward raster:
     per tile, its list up to the largest contributor count x (4-byte index + 48-byte record),
     + per pixel 20 bytes (dL/dpixel, T_final, contributor count),
     + per Gaussian 48 bytes (the 2D gradient record written).
@@ -72,9 +72,9 @@ def main():
         f.write(f"- duplicates D = {c['duplicates']:,}\n- pairs evaluated = {c['pairs_evaluated']:,}\n")
         f.write(f"- pairs blended = {c['pairs_blended']:,}\n")
         f.write(f"- pairs replayed by the backward (sum of contributor counts) = {c['pairs_replayed_bwd']:,}\n")
-        f.write(f"- active (8x8 block, Gaussian) = {c['warp_gauss_active']:,}; "
+        f.write(f"- active (16x8 block, Gaussian) = {c['warp_gauss_active']:,}; "
                 f"active (tile, Gaussian) = {c['tile_gauss_active']:,}\n")
-        f.write("- lanes with a blending pixel per active (8x8 block, Gaussian), the warp's popcount: "
+        f.write("- lanes with a blending pixel per active (16x8 block, Gaussian), the warp's popcount: "
                 f"all 32 in {hist[32] / active:.1%}, at least 28 in {sum(hist[28:]) / active:.1%}, "
                 f"at most 4 in {sum(hist[1:5]) / active:.1%}; mean {sum(i * h for i, h in enumerate(hist)) / active:.1f}\n\n")
         f.write("| lanes | active blocks | share |\n|---|---|---|\n")

@@ -282,6 +282,63 @@ def test_preprocess_bwd_accumulates_views():
         assert ok, f"{name_p}: {err:.3g} > {tol:.3g}"
 
 
+def _offset_copy(t):
+    """A contiguous copy of t whose data starts 4 bytes past a 16-byte boundary."""
+    buf = torch.zeros(t.numel() + 4, dtype=t.dtype, device=t.device)
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 16 == 4
+    return v
+
+
+@pytest.mark.parametrize("deg", [0, 1, 2, 3])
+def test_preprocess_sh_layouts_match_oracle(deg):
+    """Every SH degree, with the SH arrays 16-byte aligned (for degrees 1 and 3 the rows then move
+    through the bulk-copy engine, and the gradient rows back by bulk copies or bulk additions) and
+    4 bytes past a 16-byte boundary (coalesced 4-byte copies). Both layouts against the oracle and
+    against each other: depths bit for bit, radii exactly off the oracle's marginal Gaussians, the
+    records and the gradients of one view within 1e-5 of each field's largest magnitude (the
+    kernels may contract different multiply-adds), and a second, accumulated view doubling every
+    gradient exactly. A seventh of the Gaussians sit behind the camera (culled: no SH row is read,
+    their gradient rows are written as zeros)."""
+    s = gs_scenes.make_scene_random_small(40 + deg, 3000, 200, 136, 180.0, deg)
+    s.mean3d[::7, 2] = -1.0
+    cam = s.cameras[0]
+    pre = oracle.preprocess(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, deg, cam)
+    assert 0 < int((pre["radius"] > 0).sum()) < s.n
+    g2n = np.random.default_rng(deg).standard_normal((s.n, 9)).astype(np.float32)
+    want = oracle.preprocess_bwd(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, deg, cam, g2n)
+    opt = api.make_options(deg)
+    res = {}
+    for layout in ("aligned", "offset"):
+        params = dev_params(s)
+        if layout == "offset":
+            params["sh"] = _offset_copy(params["sh"])
+        gc.check_preprocess(s, cam, pre, params=params)
+        gc.check_preprocess_bwd(s, cam, pre, g2n, want, params=params)
+        proj = api.gs_preprocess(params, cam, opt)
+        g2 = torch.zeros((s.n, 12), dtype=torch.float32, device=DEV)
+        g2[:, :9] = torch.from_numpy(g2n).to(DEV)
+        grads = api.alloc_param_grads(params)
+        if layout == "offset":
+            grads["sh"] = _offset_copy(grads["sh"])
+        api.gs_preprocess_bwd(params, cam, opt, proj, g2, out=grads)
+        once = {k: v.clone() for k, v in grads.items()}
+        api.gs_preprocess_bwd(params, cam, opt, proj, g2, out=grads, accumulate=True)
+        res[layout] = ((proj.rec.clone(), proj.depth.clone(), proj.radius.clone()), once, grads)
+    (ra, oa, ga), (rb, ob, gb) = res["aligned"], res["offset"]
+    steady = torch.from_numpy((pre["flags"] & oracle.MARGINAL) == 0).to(DEV)
+    assert torch.equal(ra[1], rb[1]) and torch.equal(ra[2][steady], rb[2][steady])
+    rec_a, rec_b = ra[0].reshape(s.n, -1), rb[0].reshape(s.n, -1)
+    assert bool(((rec_a - rec_b).abs() <= 1e-5 * rec_a.abs().amax(0)).all())
+    culled = torch.from_numpy(pre["radius"] == 0).to(DEV)
+    for k in PARAM_NAMES:
+        assert float((oa[k] - ob[k]).abs().max()) <= 1e-5 * float(oa[k].abs().max()), k
+        for once, acc in ((oa, ga), (ob, gb)):
+            assert torch.equal(acc[k], 2 * once[k]), k
+            assert int(once[k][culled].count_nonzero()) == 0, k
+
+
 # --------------------------------------------------------------------------------- end to end
 
 @pytest.mark.parametrize("mode", ["adaptive", "direct"])
