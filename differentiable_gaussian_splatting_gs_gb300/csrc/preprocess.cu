@@ -328,77 +328,17 @@ __global__ void __launch_bounds__(kFwdThreads) k_preprocess_pipe(int n, const fl
 
 constexpr int kBwdThreads = 128;
 
-// STATS: also the post-backward statistics of the view (see DensifyArgs), from the gradients this
-// call computes. BULK: SH rows in and SH-gradient rows out through the bulk-copy engine (see
-// ShRows), the latter as bulk additions when accumulating.
-template <int DEG, bool STATS, bool BULK>
-__global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
-    int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
-    const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
-    const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
-    float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
-    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate, const DensifyArgs stats,
-    unsigned spin_limit, unsigned* __restrict__ err) {
-    pdl_entry();
+// Gradients of one Gaussian with radius > 0 from its parameters and 2D gradient record (g0..g2):
+// dm, dls, dq, dlg, and its SH row `my` (coefficients on entry, read as float4 chunks when VEC)
+// overwritten with dL/dsh. False when the recomputed geometry culls it (nothing written then).
+template <int DEG, bool VEC>
+__device__ __forceinline__ bool grad_one(const float* m, const float* ls, const float* q, float lg, float4 g0,
+                                         float4 g1, float4 g2, const KernelCamera& cam, float* my, float* dm,
+                                         float* dls, float* dq, float& dlg) {
     constexpr int K = (DEG + 1) * (DEG + 1);
     constexpr int K3 = 3 * K;
-    constexpr int S = ShRows<K3>::template stride<BULK>;
-    static_assert(!BULK || ShRows<K3>::kBulkable, "bulk SH rows need a multiple of 16 bytes");
-    __shared__ __align__(16) float tile_all[kBwdThreads / 32][32 * S];
-    __shared__ uint64_t bars[kBwdThreads / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float* tile = tile_all[warp];
-    const int warp_first = blockIdx.x * kBwdThreads + warp * 32;
-    if (BULK && warp_first >= n) return;  // whole warp
-    const int i = warp_first + lane;
-    if (BULK && lane == 0) {
-        mbar_init(&bars[warp], 1);
-        fence_mbar_init();
-    }
-    // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only. The rows'
-    // copies, the geometry and the 2D gradients are all in flight before the first wait.
-    const int rad = i < n ? radius[i] : 0;
-    const unsigned seen = __ballot_sync(0xffffffffu, rad > 0);
-    float* my = tile + lane * S;   // this thread's coefficients, then its SH gradients
-    if constexpr (BULK) {
-        if (seen) {
-            if (lane == 0) mbar_arrive_expect_tx(&bars[warp], (unsigned)(K3 * 4) * __popc(seen));
-            __syncwarp();
-            if (rad > 0) bulk_copy_g2s(my, sh + (size_t)i * K3, K3 * 4, &bars[warp]);
-        }
-    } else {
-        sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
-    }
-    bool live = i < n && ((seen >> lane) & 1u);
-    float m[3] = {0.f, 0.f, 0.f}, ls[3] = {0.f, 0.f, 0.f}, q[4] = {1.f, 0.f, 0.f, 0.f}, lg = 0.f;
-    float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0, g2 = g0;
-    if (live) {
-        m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
-        ls[0] = log_scale[3 * i]; ls[1] = log_scale[3 * i + 1]; ls[2] = log_scale[3 * i + 2];
-        q[0] = quat[4 * i]; q[1] = quat[4 * i + 1]; q[2] = quat[4 * i + 2]; q[3] = quat[4 * i + 3];
-        g0 = grad2d[3 * i]; g1 = grad2d[3 * i + 1]; g2 = grad2d[3 * i + 2];
-        lg = logit[i];
-    }
-    if constexpr (BULK) {
-        if (seen && !mbar_wait_bounded(&bars[warp], 0u, spin_limit, err)) {
-            mbar_wait_bounded(&bars[warp], 0u, kDrainLimit, err);  // let the copies land, then give up
-            return;
-        }
-    } else {
-        cp_async_wait_all();
-        __syncwarp();
-    }
-    float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
     Geo g;
-    if (live) live = geometry(m, ls, q, cam, g);
-    if (i < n && !live) {
-        if constexpr (BULK) {
-            for (int j = 0; j < K3 / 4; ++j) reinterpret_cast<float4*>(my)[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        } else {
-            for (int k = 0; k < K3; ++k) my[k] = 0.f;
-        }
-    }
-    if (i < n && live) {
+    if (!geometry(m, ls, q, cam, g)) return false;
     const float dmx = g0.x, dmy = g0.y, dA = g0.z, dB = g0.w, dC = g1.x, dop = g1.y;
     const float drgb[3] = {g1.z, g1.w, g2.x};
 
@@ -487,13 +427,13 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     float Y[16];
     sh_basis<DEG>(ux, uy, uz, Y);
     float col[3];
-    sh_colour<K, BULK>(my, Y, col);
+    sh_colour<K, VEC>(my, Y, col);
     float dc[3];
     for (int ch = 0; ch < 3; ++ch) dc[ch] = (col[ch] < 0.f) ? 0.f : drgb[ch];
     // w_k = sum_c sh_kc dc_c (c in increasing order, fused multiply-adds), and the row now holds
     // dL/dsh_kc = Y_k dc_c
     float wk[16];
-    if constexpr (BULK) {
+    if constexpr (VEC) {
         float4* r4 = reinterpret_cast<float4*>(my);
 #pragma unroll
         for (int j = 0; j < K3 / 4; ++j) {
@@ -527,59 +467,182 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
         dm[2] += (gd[2] - dot * uz) * vinv;
     }
 
-    }  // live
-    if (STATS && i < n) {
-        // 3D Gaussian splatting's densification statistics and the 2-norm of this view's parameter
-        // gradients (the tile row holds this view's SH gradients), as gs_densify_stats computes them
-        if (rad > 0) {
-            const float gx = stats.sx * g0.x, gy = stats.sy * g0.y;
-            stats.accum[i] += sqrtf(__fmaf_rn(gx, gx, gy * gy));
-            stats.count[i] += 1;
-            stats.max_radius[i] = max(stats.max_radius[i], rad);
-        }
-        if (stats.grad_mag) {
-            float ss = 0.f;
-            if (rad > 0) {  // the summation order of gs_densify_stats
-                for (int k = 0; k < 3; ++k) ss = __fmaf_rn(dm[k], dm[k], __fmaf_rn(dls[k], dls[k], ss));
-                ss = __fmaf_rn(dq[0], dq[0], __fmaf_rn(dq[1], dq[1], __fmaf_rn(dq[2], dq[2], __fmaf_rn(dq[3], dq[3], ss))));
-                ss = __fmaf_rn(dlg, dlg, ss);
-                if constexpr (K3 % 4 == 0) {
-                    for (int k = 0; k < K3; k += 4) {
-                        const float4 v = BULK ? reinterpret_cast<const float4*>(my)[k / 4]
-                                              : make_float4(my[k], my[k + 1], my[k + 2], my[k + 3]);
-                        ss = __fmaf_rn(v.x, v.x, __fmaf_rn(v.y, v.y, __fmaf_rn(v.z, v.z, __fmaf_rn(v.w, v.w, ss))));
-                    }
-                } else {
-                    for (int k = 0; k < K3; ++k) ss = __fmaf_rn(my[k], my[k], ss);
+    return true;
+}
+
+// Statistics (STATS) and the parameter gradients of Gaussian i (radius rad; `my` holds its SH
+// gradients) written or, when accumulating, added to the outputs; the SH row is stored by the caller.
+template <int K3, bool STATS, bool VEC>
+__device__ __forceinline__ void finish_one(int i, int rad, float4 g0, const float* dm, const float* dls,
+                                           const float* dq, float dlg, const float* my, const DensifyArgs& stats,
+                                           int accumulate, float* __restrict__ d_mean3d,
+                                           float* __restrict__ d_log_scale, float* __restrict__ d_quat,
+                                           float* __restrict__ d_logit) {
+    if (STATS) {
+    // 3D Gaussian splatting's densification statistics and the 2-norm of this view's parameter
+    // gradients (the tile row holds this view's SH gradients), as gs_densify_stats computes them
+    if (rad > 0) {
+        const float gx = stats.sx * g0.x, gy = stats.sy * g0.y;
+        stats.accum[i] += sqrtf(__fmaf_rn(gx, gx, gy * gy));
+        stats.count[i] += 1;
+        stats.max_radius[i] = max(stats.max_radius[i], rad);
+    }
+    if (stats.grad_mag) {
+        float ss = 0.f;
+        if (rad > 0) {  // the summation order of gs_densify_stats
+            for (int k = 0; k < 3; ++k) ss = __fmaf_rn(dm[k], dm[k], __fmaf_rn(dls[k], dls[k], ss));
+            ss = __fmaf_rn(dq[0], dq[0], __fmaf_rn(dq[1], dq[1], __fmaf_rn(dq[2], dq[2], __fmaf_rn(dq[3], dq[3], ss))));
+            ss = __fmaf_rn(dlg, dlg, ss);
+            if constexpr (K3 % 4 == 0) {
+                for (int k = 0; k < K3; k += 4) {
+                    const float4 v = VEC ? reinterpret_cast<const float4*>(my)[k / 4]
+                                          : make_float4(my[k], my[k + 1], my[k + 2], my[k + 3]);
+                    ss = __fmaf_rn(v.x, v.x, __fmaf_rn(v.y, v.y, __fmaf_rn(v.z, v.z, __fmaf_rn(v.w, v.w, ss))));
                 }
+            } else {
+                for (int k = 0; k < K3; ++k) ss = __fmaf_rn(my[k], my[k], ss);
             }
-            stats.grad_mag[i] = sqrtf(ss);
         }
+        stats.grad_mag[i] = sqrtf(ss);
     }
-    if (i < n) {
-        if (accumulate) {
-            for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] += dm[k]; d_log_scale[3 * i + k] += dls[k]; }
-            for (int k = 0; k < 4; ++k) d_quat[4 * i + k] += dq[k];
-            d_logit[i] += dlg;
-        } else {
-            for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] = dm[k]; d_log_scale[3 * i + k] = dls[k]; }
-            for (int k = 0; k < 4; ++k) d_quat[4 * i + k] = dq[k];
-            d_logit[i] = dlg;
-        }
     }
-    // accumulating: rows of Gaussians with radius 0 add nothing and are skipped
-    if constexpr (BULK) {
-        if (i < n && (!accumulate || rad > 0)) {
-            fence_proxy_async_smem();
-            if (accumulate) bulk_add_s2g(d_sh + (size_t)i * K3, my, K3 * 4);
-            else bulk_copy_s2g(d_sh + (size_t)i * K3, my, K3 * 4);
-            bulk_wait_read();
-        }
+    if (accumulate) {
+        for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] += dm[k]; d_log_scale[3 * i + k] += dls[k]; }
+        for (int k = 0; k < 4; ++k) d_quat[4 * i + k] += dq[k];
+        d_logit[i] += dlg;
     } else {
-        __syncwarp();
-        if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane, seen);
-        else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane, 0xffffffffu);
+        for (int k = 0; k < 3; ++k) { d_mean3d[3 * i + k] = dm[k]; d_log_scale[3 * i + k] = dls[k]; }
+        for (int k = 0; k < 4; ++k) d_quat[4 * i + k] = dq[k];
+        d_logit[i] = dlg;
     }
+}
+
+// One thread per Gaussian, SH rows by coalesced 4-byte asynchronous copies (any SH degree and
+// alignment). STATS: also the post-backward statistics of the view (see DensifyArgs), from the
+// gradients this call computes.
+template <int DEG, bool STATS>
+__global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
+    int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
+    const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
+    const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
+    float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
+    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate, const DensifyArgs stats) {
+    pdl_entry();
+    constexpr int K3 = 3 * (DEG + 1) * (DEG + 1);
+    constexpr int S = ShRows<K3>::template stride<false>;
+    __shared__ float tile_all[kBwdThreads / 32][32 * S];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* tile = tile_all[warp];
+    const int warp_first = blockIdx.x * kBwdThreads + warp * 32;
+    const int i = warp_first + lane;
+    // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only. The rows'
+    // copies, the geometry and the 2D gradients are all in flight before the first wait.
+    const int rad = i < n ? radius[i] : 0;
+    const unsigned seen = __ballot_sync(0xffffffffu, rad > 0);
+    sh_tile_copy<K3, true, false, false>(tile, const_cast<float*>(sh), warp_first, n, lane, seen);
+    float* my = tile + lane * S;   // this thread's coefficients, then its SH gradients
+    float m[3] = {0.f, 0.f, 0.f}, ls[3] = {0.f, 0.f, 0.f}, q[4] = {1.f, 0.f, 0.f, 0.f}, lg = 0.f;
+    float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0, g2 = g0;
+    if (rad > 0) {
+        m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
+        ls[0] = log_scale[3 * i]; ls[1] = log_scale[3 * i + 1]; ls[2] = log_scale[3 * i + 2];
+        q[0] = quat[4 * i]; q[1] = quat[4 * i + 1]; q[2] = quat[4 * i + 2]; q[3] = quat[4 * i + 3];
+        g0 = grad2d[3 * i]; g1 = grad2d[3 * i + 1]; g2 = grad2d[3 * i + 2];
+        lg = logit[i];
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    if (i < n) {
+        float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
+        if (!(rad > 0 && grad_one<DEG, false>(m, ls, q, lg, g0, g1, g2, cam, my, dm, dls, dq, dlg)))
+            for (int k = 0; k < K3; ++k) my[k] = 0.f;
+        finish_one<K3, STATS, false>(i, rad, g0, dm, dls, dq, dlg, my, stats, accumulate, d_mean3d, d_log_scale,
+                                     d_quat, d_logit);
+    }
+    __syncwarp();
+    // accumulating: rows of Gaussians with radius 0 add nothing and are skipped
+    if (accumulate) sh_tile_copy<K3, false, true>(tile, d_sh, warp_first, n, lane, seen);
+    else sh_tile_copy<K3, false, false>(tile, d_sh, warp_first, n, lane, 0xffffffffu);
+}
+
+// Persistent, pipelined form for bulk SH rows (degrees 1 and 3, sh and d_sh 16-byte aligned): each
+// warp walks 32-Gaussian groups with a stride of the grid's warp count. It loads the radii of its
+// next group before waiting for the current group's rows, and each group's gradient rows leave by
+// bulk copies (bulk additions when accumulating) that complete while the warp goes on; a lane
+// refills its row only after its own copy out of it has read it.
+template <int DEG, bool STATS>
+__global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd_pipe(
+    int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
+    const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
+    const KernelCamera cam, const int* __restrict__ radius, const float4* __restrict__ grad2d,
+    float* __restrict__ d_mean3d, float* __restrict__ d_log_scale, float* __restrict__ d_quat,
+    float* __restrict__ d_logit, float* __restrict__ d_sh, int accumulate, const DensifyArgs stats,
+    unsigned spin_limit, unsigned* __restrict__ err) {
+    pdl_entry();
+    constexpr int K3 = 3 * (DEG + 1) * (DEG + 1);
+    static_assert(ShRows<K3>::kBulkable, "bulk SH rows need a multiple of 16 bytes");
+    constexpr int S = ShRows<K3>::template stride<true>;
+    constexpr int W = kBwdThreads / 32;
+    __shared__ __align__(16) float tile_all[W][32 * S];
+    __shared__ uint64_t bars[W];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int groups = (n + 31) >> 5;
+    const int wstride = gridDim.x * W;
+    int grp = blockIdx.x * W + warp;
+    if (grp >= groups) return;  // whole warp
+    float* my = tile_all[warp] + lane * S;   // this thread's coefficients, then its SH gradients
+    uint64_t* bar = &bars[warp];
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    unsigned parity = 0;
+    int rad = grp * 32 + lane < n ? radius[grp * 32 + lane] : 0;
+    for (; grp < groups; grp += wstride) {
+        const int i = grp * 32 + lane;
+        // only Gaussians with radius > 0 have non-zero gradients: load their SH rows only, with
+        // their geometry and 2D gradients in flight at the same time
+        const unsigned seen = __ballot_sync(0xffffffffu, rad > 0);
+        bulk_wait_read();  // the previous group's copy out of this row has read it
+        if (seen) {
+            if (lane == 0) mbar_arrive_expect_tx(bar, (unsigned)(K3 * 4) * __popc(seen));
+            __syncwarp();
+            if (rad > 0) bulk_copy_g2s(my, sh + (size_t)i * K3, K3 * 4, bar);
+        }
+        float m[3] = {0.f, 0.f, 0.f}, ls[3] = {0.f, 0.f, 0.f}, q[4] = {1.f, 0.f, 0.f, 0.f}, lg = 0.f;
+        float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0, g2 = g0;
+        if (rad > 0) {
+            m[0] = mean3d[3 * i]; m[1] = mean3d[3 * i + 1]; m[2] = mean3d[3 * i + 2];
+            ls[0] = log_scale[3 * i]; ls[1] = log_scale[3 * i + 1]; ls[2] = log_scale[3 * i + 2];
+            q[0] = quat[4 * i]; q[1] = quat[4 * i + 1]; q[2] = quat[4 * i + 2]; q[3] = quat[4 * i + 3];
+            g0 = grad2d[3 * i]; g1 = grad2d[3 * i + 1]; g2 = grad2d[3 * i + 2];
+            lg = logit[i];
+        }
+        const int nxt = grp + wstride, j = nxt * 32 + lane;
+        const int rad_next = nxt < groups && j < n ? radius[j] : 0;
+        if (seen) {
+            if (!mbar_wait_bounded(bar, parity, spin_limit, err)) {
+                mbar_wait_bounded(bar, parity, kDrainLimit, err);  // let the copies land, then give up
+                return;
+            }
+            parity ^= 1u;
+        }
+        if (i < n) {
+            float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
+            if (!(rad > 0 && grad_one<DEG, true>(m, ls, q, lg, g0, g1, g2, cam, my, dm, dls, dq, dlg)))
+                for (int k = 0; k < K3 / 4; ++k) reinterpret_cast<float4*>(my)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            finish_one<K3, STATS, true>(i, rad, g0, dm, dls, dq, dlg, my, stats, accumulate, d_mean3d, d_log_scale,
+                                        d_quat, d_logit);
+            // accumulating: rows of Gaussians with radius 0 add nothing and are skipped
+            if (!accumulate || rad > 0) {
+                fence_proxy_async_smem();
+                if (accumulate) bulk_add_s2g(d_sh + (size_t)i * K3, my, K3 * 4);
+                else bulk_copy_s2g(d_sh + (size_t)i * K3, my, K3 * 4);
+            }
+        }
+        rad = rad_next;
+    }
+    bulk_wait_read();  // every copy out of shared memory has read it before the block exits
 }
 
 // ---- host-side launchers ------------------------------------------------------------------------
@@ -588,16 +651,16 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace
 
-// Blocks of `kernel` (kFwdThreads threads, static shared memory only) resident on the current device
+// Blocks of `kernel` (`threads` threads, static shared memory only) resident on the current device
 // at once: SMs x blocks per SM, looked up once per device; 0 if the query fails.
 template <class Kernel>
-int resident_blocks(Kernel kernel, std::atomic<int> (&cache)[256]) {
+int resident_blocks(Kernel kernel, int threads, std::atomic<int> (&cache)[256]) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
     int v = cache[dev].load(std::memory_order_relaxed);
     if (v == 0) {
         int per = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, kFwdThreads, 0) != cudaSuccess) return 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, 0) != cudaSuccess) return 0;
         v = device_sm_count() * (per > 0 ? per : 1);
         cache[dev].store(v, std::memory_order_relaxed);
     }
@@ -614,7 +677,7 @@ cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCa
     if ((deg == 1 || deg == 3) && aligned16(p.sh)) {
         static std::atomic<int> cache1[256], cache3[256];
         auto k = deg == 1 ? k_preprocess_pipe<1> : k_preprocess_pipe<3>;
-        const int res = resident_blocks(k, deg == 1 ? cache1 : cache3);
+        const int res = resident_blocks(k, kFwdThreads, deg == 1 ? cache1 : cache3);
         const int grid = res > 0 && res < blocks ? res : blocks;
         return launch_pdl(k, dim3(grid), dim3(kFwdThreads), 0, st, n, p.mean3d, p.log_scale, p.quat,
                           p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt, spin_limit, err);
@@ -626,32 +689,57 @@ cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCa
                       p.sh, cam, rec, out.depth, out.radius, tt);
 }
 
+template <int DEG, bool STATS>
+cudaError_t launch_bwd_pipe(int n, const gs_params& p, const KernelCamera& cam, const int* radius, const float4* g2,
+                            float* dm, float* dls, float* dq, float* dlg, float* dsh, int accumulate,
+                            const DensifyArgs& stats, unsigned spin_limit, unsigned* err, cudaStream_t st) {
+    static std::atomic<int> cache[256];
+    const int blocks = (n + kBwdThreads - 1) / kBwdThreads;
+    const int res = resident_blocks(k_preprocess_bwd_pipe<DEG, STATS>, kBwdThreads, cache);
+    return launch_pdl(k_preprocess_bwd_pipe<DEG, STATS>, dim3(res > 0 && res < blocks ? res : blocks),
+                      dim3(kBwdThreads), 0, st, n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius,
+                      g2, dm, dls, dq, dlg, dsh, accumulate, stats, spin_limit, err);
+}
+
+template <int DEG, bool STATS>
+cudaError_t launch_bwd_plain(int n, const gs_params& p, const KernelCamera& cam, const int* radius, const float4* g2,
+                             float* dm, float* dls, float* dq, float* dlg, float* dsh, int accumulate,
+                             const DensifyArgs& stats, cudaStream_t st) {
+    return launch_pdl(k_preprocess_bwd<DEG, STATS>, dim3((n + kBwdThreads - 1) / kBwdThreads), dim3(kBwdThreads), 0,
+                      st, n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg,
+                      dsh, accumulate, stats);
+}
+
 cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
                                   const float* grad2d, float* dm, float* dls, float* dq, float* dlg, float* dsh,
                                   int accumulate, const DensifyArgs* stats, unsigned spin_limit, unsigned* err,
                                   cudaStream_t st) {
     if (n == 0) return cudaSuccess;
-    const int blocks = (n + kBwdThreads - 1) / kBwdThreads;
     const float4* g2 = reinterpret_cast<const float4*>(grad2d);
     const DensifyArgs none{};
-    const bool bulk = aligned16(p.sh) && aligned16(dsh);
+    const DensifyArgs& sa = stats ? *stats : none;
     count_launches(1);
-#define GS_PREBWD(D, B)                                                                                        \
-    (stats ? launch_pdl(k_preprocess_bwd<D, true, B>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,      \
-                        p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh,      \
-                        accumulate, *stats, spin_limit, err)                                                    \
-           : launch_pdl(k_preprocess_bwd<D, false, B>, dim3(blocks), dim3(kBwdThreads), 0, st, n, p.mean3d,     \
-                        p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh,      \
-                        accumulate, none, spin_limit, err))
-    cudaError_t e;
+    if ((deg == 1 || deg == 3) && aligned16(p.sh) && aligned16(dsh)) {
+        if (deg == 1)
+            return stats ? launch_bwd_pipe<1, true>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
+                                                    spin_limit, err, st)
+                         : launch_bwd_pipe<1, false>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
+                                                     spin_limit, err, st);
+        return stats ? launch_bwd_pipe<3, true>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
+                                                spin_limit, err, st)
+                     : launch_bwd_pipe<3, false>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
+                                                 spin_limit, err, st);
+    }
+#define GS_PREBWD(D)                                                                                           \
+    (stats ? launch_bwd_plain<D, true>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st)         \
+           : launch_bwd_plain<D, false>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st))
     switch (deg) {
-        case 0: e = GS_PREBWD(0, false); break;
-        case 1: e = bulk ? GS_PREBWD(1, true) : GS_PREBWD(1, false); break;
-        case 2: e = GS_PREBWD(2, false); break;
-        default: e = bulk ? GS_PREBWD(3, true) : GS_PREBWD(3, false); break;
+        case 0: return GS_PREBWD(0);
+        case 1: return GS_PREBWD(1);
+        case 2: return GS_PREBWD(2);
+        default: return GS_PREBWD(3);
     }
 #undef GS_PREBWD
-    return e;
 }
 
 }  // namespace gs
