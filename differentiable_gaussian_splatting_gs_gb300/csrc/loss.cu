@@ -10,7 +10,8 @@
 // sum(S) with respect to x is w * dS/dmu_x + 2 x (w * dS/dExx) + y (w * dS/dExy) (w is symmetric,
 // so the adjoint of the zero-padded window sum is the same window sum). Pass 1 computes the five
 // windowed moments, S and the three partial derivatives per pixel; pass 2 takes their windowed sums.
-// Both passes stage a 128x34 tile plus a 5-pixel halo in shared memory.
+// Both passes stage a 128x34 tile plus a 5-pixel halo in shared memory, with the maps summed
+// together held as pairs so that packed float32 pair instructions do two sums at once.
 #include <cmath>
 
 #include "gs_common.cuh"
@@ -33,69 +34,87 @@ struct LossArgs {
     int width, height;
 };
 
-// Stages NM maps of the tile (rows y0 - 5 .., columns x0 - 5 ..) with zeros outside the image:
-// asynchronous copies, all in flight at once, waited for before returning (the caller then
+// Stages the tile (rows y0 - 5 .., columns x0 - 5 ..) of the maps a and b (b may be NULL) with zeros
+// outside the image: PAIR stores them interleaved, sm2[r][c] = (a, b); otherwise a alone into sm1.
+// Asynchronous copies, all in flight at once, waited for before returning (the caller then
 // synchronises the block).
-template <int NM>
-__device__ __forceinline__ void stage_tile(float (*sm)[kInH][kInW], const float* const (&src)[NM], int x0, int y0,
-                                           int W, int H) {
+template <bool PAIR>
+__device__ __forceinline__ void stage_tile(float2 (*sm2)[kInW], float (*sm1)[kInW], const float* a, const float* b,
+                                           int x0, int y0, int W, int H) {
     for (int i = threadIdx.x; i < kInH * kInW; i += kLW) {
         const int r = i / kInW, c = i - r * kInW;
         const int gy = y0 - kHalo + r, gx = x0 - kHalo + c;
         const bool in = gx >= 0 && gx < W && gy >= 0 && gy < H;
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-            if (in) cp_async4(&sm[m][r][c], src[m] + (size_t)gy * W + gx);
-            else sm[m][r][c] = 0.f;
+        const size_t g = (size_t)gy * W + gx;
+        if (PAIR) {
+            if (in) {
+                cp_async4(&sm2[r][c].x, a + g);
+                cp_async4(&sm2[r][c].y, b + g);
+            } else {
+                sm2[r][c] = make_float2(0.f, 0.f);
+            }
+        } else {
+            if (in) cp_async4(&sm1[r][c], a + g);
+            else sm1[r][c] = 0.f;
         }
     }
     cp_async_wait_all();
 }
 
+// Pass 1: the five windowed moments of (x, y) per pixel, the SSIM map S and its partial
+// derivatives with respect to mu_x, E[x^2] and E[xy]. x and y are staged as pairs, so that the
+// moments run as packed pairs (mu_x, mu_y), (E[x^2], E[y^2]) and the scalar E[xy]: every sum takes
+// its terms in the same order and rounding as scalar code would.
 __global__ void __launch_bounds__(kLW) k_ssim_fwd(const LossArgs a, const float* __restrict__ img,
-                                                  const float* __restrict__ tgt, float* __restrict__ p_mu,
-                                                  float* __restrict__ p_xx, float* __restrict__ p_xy,
-                                                  double* __restrict__ sums) {
-    extern __shared__ float smem_loss[];
-    float (*sm)[kInH][kInW] = reinterpret_cast<float (*)[kInH][kInW]>(smem_loss);  // x, y
+                                                  const float* __restrict__ tgt, float2* __restrict__ p_mx,
+                                                  float* __restrict__ p_xy, double* __restrict__ sums) {
+    extern __shared__ float4 smem_loss4[];
+    float2 (*sm)[kInW] = reinterpret_cast<float2 (*)[kInW]>(smem_loss4);  // (x, y)
     __shared__ double red[2][kLW / 32];
     const int W = a.width, H = a.height;
     const int x0 = blockIdx.x * kLW, y0 = blockIdx.y * kLH, ch = blockIdx.z;
     const size_t plane = (size_t)W * H;
-    const float* const src[2] = {img + ch * plane, tgt + ch * plane};
-    stage_tile<2>(sm, src, x0, y0, W, H);
+    stage_tile<true>(sm, nullptr, img + ch * plane, tgt + ch * plane, x0, y0, W, H);
     __syncthreads();
     const int c = threadIdx.x, gx = x0 + c;
-    float acc[kTapN][5];
+    f32x2 w2[kTapN];
 #pragma unroll
-    for (int s2 = 0; s2 < kTapN; ++s2)
+    for (int k = 0; k < kTapN; ++k) w2[k] = f2_pack(a.w[k], a.w[k]);
+    f32x2 acc_m[kTapN], acc_s[kTapN];   // (mu_x, mu_y), (E[x^2], E[y^2]) of the 11 rows in flight
+    float acc_c[kTapN];                 // E[xy]
 #pragma unroll
-        for (int m = 0; m < 5; ++m) acc[s2][m] = 0.f;
+    for (int s2 = 0; s2 < kTapN; ++s2) {
+        acc_m[s2] = acc_s[s2] = 0ull;
+        acc_c[s2] = 0.f;
+    }
     float l1f = 0.f, ssf = 0.f;
     for (int q = 0; q < kInH / kTapN; ++q) {
 #pragma unroll
         for (int j = 0; j < kTapN; ++j) {
             const int r = q * kTapN + j;
-            float h[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+            f32x2 hm = 0ull, hs = 0ull;
+            float hc = 0.f;
 #pragma unroll
             for (int k = 0; k < kTapN; ++k) {
-                const float u = sm[0][r][c + k], v = sm[1][r][c + k], wk = a.w[k];
-                h[0] = __fmaf_rn(wk, u, h[0]);
-                h[1] = __fmaf_rn(wk, v, h[1]);
-                h[2] = __fmaf_rn(wk, u * u, h[2]);
-                h[3] = __fmaf_rn(wk, v * v, h[3]);
-                h[4] = __fmaf_rn(wk, u * v, h[4]);
+                const float2 p = sm[r][c + k];
+                const f32x2 uv = f2_pack(p.x, p.y);
+                hm = f2_fma(w2[k], uv, hm);
+                hs = f2_fma(w2[k], f2_mul(uv, uv), hs);
+                hc = __fmaf_rn(a.w[k], p.x * p.y, hc);
             }
 #pragma unroll
-            for (int t = 0; t < kTapN; ++t)
-#pragma unroll
-                for (int m = 0; m < 5; ++m) acc[(j - t + kTapN) % kTapN][m] = __fmaf_rn(a.w[t], h[m], acc[(j - t + kTapN) % kTapN][m]);
+            for (int t = 0; t < kTapN; ++t) {
+                const int o = (j - t + kTapN) % kTapN;
+                acc_m[o] = f2_fma(w2[t], hm, acc_m[o]);
+                acc_s[o] = f2_fma(w2[t], hs, acc_s[o]);
+                acc_c[o] = __fmaf_rn(a.w[t], hc, acc_c[o]);
+            }
             // output row o = r - 10 is complete
             const int slot = (j + 1) % kTapN;
             const int o = r - (kTapN - 1), gy = y0 + o;
             if (o >= 0 && gx < W && gy < H) {
-                const float mx = acc[slot][0], my = acc[slot][1], exx = acc[slot][2], eyy = acc[slot][3];
-                const float exy = acc[slot][4];
+                const float2 mu = f2_unpack(acc_m[slot]), e2 = f2_unpack(acc_s[slot]);
+                const float mx = mu.x, my = mu.y, exx = e2.x, eyy = e2.y, exy = acc_c[slot];
                 const float A = __fmaf_rn(2.f * mx, my, a.c1);
                 const float B = __fmaf_rn(2.f, exy - mx * my, a.c2);
                 const float Cc = __fmaf_rn(mx, mx, __fmaf_rn(my, my, a.c1));
@@ -104,14 +123,14 @@ __global__ void __launch_bounds__(kLW) k_ssim_fwd(const LossArgs a, const float*
                 const float inv = iC * iD;
                 const float S = A * B * inv;
                 const size_t oo = ch * plane + (size_t)gy * W + gx;
-                p_mu[oo] = 2.f * my * (B - A) * inv - 2.f * mx * S * (iC - iD);
-                p_xx[oo] = -S * iD;
+                p_mx[oo] = make_float2(2.f * my * (B - A) * inv - 2.f * mx * S * (iC - iD), -S * iD);
                 p_xy[oo] = 2.f * A * inv;
-                l1f += fabsf(sm[0][o + kHalo][c + kHalo] - sm[1][o + kHalo][c + kHalo]);
+                const float2 xy = sm[o + kHalo][c + kHalo];
+                l1f += fabsf(xy.x - xy.y);
                 ssf += S;
             }
-#pragma unroll
-            for (int m = 0; m < 5; ++m) acc[slot][m] = 0.f;
+            acc_m[slot] = acc_s[slot] = 0ull;
+            acc_c[slot] = 0.f;
         }
     }
     // block sums of |x - y| and S (float per thread, float64 across threads)
@@ -138,27 +157,43 @@ __global__ void __launch_bounds__(kLW) k_ssim_fwd(const LossArgs a, const float*
     }
 }
 
+// Pass 2: dL/dx from the windowed sums of the three partial maps (dS/dmu_x and dS/dE[x^2] staged
+// as pairs, summed as packed pairs; dS/dE[xy] alone), and the L1 term.
 __global__ void __launch_bounds__(kLW) k_ssim_bwd(const LossArgs a, const float* __restrict__ img,
-                                                  const float* __restrict__ tgt, const float* __restrict__ p_mu,
-                                                  const float* __restrict__ p_xx, const float* __restrict__ p_xy,
-                                                  const double* __restrict__ sums, float* __restrict__ loss,
-                                                  float* __restrict__ dl) {
-    extern __shared__ float smem_loss[];
-    float (*sm)[kInH][kInW] = reinterpret_cast<float (*)[kInH][kInW]>(smem_loss);  // the 3 partial maps
+                                                  const float* __restrict__ tgt, const float2* __restrict__ p_mx,
+                                                  const float* __restrict__ p_xy, const double* __restrict__ sums,
+                                                  float* __restrict__ loss, float* __restrict__ dl) {
+    extern __shared__ float4 smem_loss4[];
+    float2 (*sm2)[kInW] = reinterpret_cast<float2 (*)[kInW]>(smem_loss4);                   // (d mu, d xx)
+    float (*sm1)[kInW] = reinterpret_cast<float (*)[kInW]>(sm2 + kInH);                     // d xy
     const int W = a.width, H = a.height;
     const int x0 = blockIdx.x * kLW, y0 = blockIdx.y * kLH, ch = blockIdx.z;
     const size_t plane = (size_t)W * H;
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && ch == 0)
         *loss = (float)((1.0 - a.lam) * sums[0] * a.inv_n + a.lam * (1.0 - sums[1] * a.inv_n));
-    const float* const src[3] = {p_mu + ch * plane, p_xx + ch * plane, p_xy + ch * plane};
-    stage_tile<3>(sm, src, x0, y0, W, H);
+    {
+        // the pair map: 8-byte copies of (d mu, d xx)
+        const float2* src = p_mx + ch * plane;
+        for (int i = threadIdx.x; i < kInH * kInW; i += kLW) {
+            const int r = i / kInW, c = i - r * kInW;
+            const int gy = y0 - kHalo + r, gx = x0 - kHalo + c;
+            if (gx >= 0 && gx < W && gy >= 0 && gy < H) cp_async8(&sm2[r][c], src + (size_t)gy * W + gx);
+            else sm2[r][c] = make_float2(0.f, 0.f);
+        }
+    }
+    stage_tile<false>(nullptr, sm1, p_xy + ch * plane, nullptr, x0, y0, W, H);
     __syncthreads();
     const int c = threadIdx.x, gx = x0 + c;
-    float acc[kTapN][3];
+    f32x2 w2[kTapN];
 #pragma unroll
-    for (int s2 = 0; s2 < kTapN; ++s2)
+    for (int k = 0; k < kTapN; ++k) w2[k] = f2_pack(a.w[k], a.w[k]);
+    f32x2 acc_p[kTapN];
+    float acc_c[kTapN];
 #pragma unroll
-        for (int m = 0; m < 3; ++m) acc[s2][m] = 0.f;
+    for (int s2 = 0; s2 < kTapN; ++s2) {
+        acc_p[s2] = 0ull;
+        acc_c[s2] = 0.f;
+    }
     for (int q = 0; q < kInH / kTapN; ++q) {
         // image and target at the 11 outputs this group of rows completes, loaded ahead of use
         float xs[kTapN], ys[kTapN];
@@ -173,29 +208,32 @@ __global__ void __launch_bounds__(kLW) k_ssim_bwd(const LossArgs a, const float*
 #pragma unroll
         for (int j = 0; j < kTapN; ++j) {
             const int r = q * kTapN + j;
-            float h[3] = {0.f, 0.f, 0.f};
+            f32x2 hp = 0ull;
+            float hc = 0.f;
 #pragma unroll
             for (int k = 0; k < kTapN; ++k) {
-                const float wk = a.w[k];
-                h[0] = __fmaf_rn(wk, sm[0][r][c + k], h[0]);
-                h[1] = __fmaf_rn(wk, sm[1][r][c + k], h[1]);
-                h[2] = __fmaf_rn(wk, sm[2][r][c + k], h[2]);
+                const float2 p = sm2[r][c + k];
+                hp = f2_fma(w2[k], f2_pack(p.x, p.y), hp);
+                hc = __fmaf_rn(a.w[k], sm1[r][c + k], hc);
             }
 #pragma unroll
-            for (int t = 0; t < kTapN; ++t)
-#pragma unroll
-                for (int m = 0; m < 3; ++m) acc[(j - t + kTapN) % kTapN][m] = __fmaf_rn(a.w[t], h[m], acc[(j - t + kTapN) % kTapN][m]);
+            for (int t = 0; t < kTapN; ++t) {
+                const int o = (j - t + kTapN) % kTapN;
+                acc_p[o] = f2_fma(w2[t], hp, acc_p[o]);
+                acc_c[o] = __fmaf_rn(a.w[t], hc, acc_c[o]);
+            }
             const int slot = (j + 1) % kTapN;
             const int o = r - (kTapN - 1), gy = y0 + o;
             if (o >= 0 && gx < W && gy < H) {
                 const size_t oo = ch * plane + (size_t)gy * W + gx;
                 const float x = xs[j], y = ys[j];
-                const float dssim = __fmaf_rn(2.f * x, acc[slot][1], __fmaf_rn(y, acc[slot][2], acc[slot][0]));
+                const float2 pm = f2_unpack(acc_p[slot]);
+                const float dssim = __fmaf_rn(2.f * x, pm.y, __fmaf_rn(y, acc_c[slot], pm.x));
                 const float sgn = x > y ? 1.f : (x < y ? -1.f : 0.f);
                 dl[oo] = a.inv_n * ((1.f - a.lam) * sgn - a.lam * dssim);
             }
-#pragma unroll
-            for (int m = 0; m < 3; ++m) acc[slot][m] = 0.f;
+            acc_p[slot] = 0ull;
+            acc_c[slot] = 0.f;
         }
     }
 }
@@ -220,18 +258,17 @@ cudaError_t launch_loss_l1_dssim(const float* img, const float* tgt, int width, 
     a.height = height;
     const size_t plane3 = (size_t)3 * width * height;
     double* sums = reinterpret_cast<double*>(ws);
-    float* p_mu = reinterpret_cast<float*>(static_cast<char*>(ws) + 256);
-    float* p_xx = p_mu + plane3;
-    float* p_xy = p_xx + plane3;
+    float2* p_mx = reinterpret_cast<float2*>(static_cast<char*>(ws) + 256);   // (d mu, d xx) pairs
+    float* p_xy = reinterpret_cast<float*>(p_mx + plane3);
     cudaError_t e = cudaMemsetAsync(sums, 0, 2 * sizeof(double), st);
     if (e) return e;
     const dim3 grid((width + kLW - 1) / kLW, (height + kLH - 1) / kLH, 3);
-    const int smem2 = 2 * kInH * kInW * 4, smem3 = 3 * kInH * kInW * 4;
+    const int smem2 = kInH * kInW * 8, smem3 = kInH * kInW * 12;
     if ((e = cudaFuncSetAttribute(k_ssim_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2))) return e;
     if ((e = cudaFuncSetAttribute(k_ssim_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, smem3))) return e;
     count_launches(2);
-    k_ssim_fwd<<<grid, kLW, smem2, st>>>(a, img, tgt, p_mu, p_xx, p_xy, sums);
-    k_ssim_bwd<<<grid, kLW, smem3, st>>>(a, img, tgt, p_mu, p_xx, p_xy, sums, loss, dl);
+    k_ssim_fwd<<<grid, kLW, smem2, st>>>(a, img, tgt, p_mx, p_xy, sums);
+    k_ssim_bwd<<<grid, kLW, smem3, st>>>(a, img, tgt, p_mx, p_xy, sums, loss, dl);
     return cudaGetLastError();
 }
 
