@@ -54,6 +54,15 @@ struct StageSmemT {
 constexpr int kFwdBlock = 128;
 constexpr int kFwdBatch = 128;
 using FwdStage = StageSmemT<kFwdBatch, 4>;
+
+// The forward's per-batch form of each staged record, built from the prepared record: the
+// per-Gaussian constants of the alpha evaluation duplicated into pairs, so that a lane evaluates its
+// two pixels with packed float32 pair instructions (f32x2, rounding each half as the scalar
+// instruction would): (mx, mx, my, my), (r, r, A', A'), (D', D', o, red), (green, blue, -, -).
+struct FwdSmem {
+    FwdStage st;
+    float4 pair[kFwdBatch][4];
+};
 // Backward layouts, PX pixels per lane: PX = 2 is the forward's layout (128 threads, 8x8 warp
 // blocks); PX = 4 gives each warp a 16x8 block (64 threads per tile; warp w covers rows 8w..8w+7,
 // lane l the column l & 15 and the rows (l >> 4) + 2q, q = 0..3). A larger warp block meets each
@@ -203,7 +212,7 @@ __device__ __forceinline__ int compact_warp(S& s, int n_in, int pos_limit, float
 
 // Front-to-back blending of one record, whose alpha at the pixel is given, into one pixel; sets
 // `done` when the pixel terminates.
-__device__ __forceinline__ void blend_pixel(float alpha, const float4& r1, float cb, unsigned pos1, float& T,
+__device__ __forceinline__ void blend_pixel(float alpha, float cr, float cg, float cb, unsigned pos1, float& T,
                                             float& c0, float& c1, float& c2, unsigned& last, bool& done) {
     if (alpha >= kAlphaMin) {
         const float test_T = T * (1.f - alpha);
@@ -211,13 +220,30 @@ __device__ __forceinline__ void blend_pixel(float alpha, const float4& r1, float
             done = true;
         } else {
             const float w = alpha * T;
-            c0 = __fmaf_rn(r1.z, w, c0);
-            c1 = __fmaf_rn(r1.w, w, c1);
+            c0 = __fmaf_rn(cr, w, c0);
+            c1 = __fmaf_rn(cg, w, c1);
             c2 = __fmaf_rn(cb, w, c2);
             T = test_T;
             last = pos1;
         }
     }
+}
+
+// Alphas of one staged Gaussian at a lane's two pixels from its pair record (FwdSmem::pair):
+// o 2^(A' u^2 + D' dy^2) with u = dx + r dy, each half computed in the same order and rounding as
+// the scalar form. fpx2 = (px, px) and fpy2 = (py0, py1) are the pixel centres. Also returns
+// (o, red) and (green, blue).
+__device__ __forceinline__ float2 pair_alphas(const float4 (&pr)[4], f32x2 fpx2, f32x2 fpy2, float2& ored,
+                                              float2& gb) {
+    const ulonglong2 p0 = *reinterpret_cast<const ulonglong2*>(&pr[0]);   // (mx, mx), (my, my)
+    const ulonglong2 p1 = *reinterpret_cast<const ulonglong2*>(&pr[1]);   // (r, r), (A', A')
+    const ulonglong2 p2 = *reinterpret_cast<const ulonglong2*>(&pr[2]);   // (D', D'), (o, red)
+    gb = *reinterpret_cast<const float2*>(&pr[3]);
+    const f32x2 dx = f2_sub(p0.x, fpx2), dy = f2_sub(p0.y, fpy2);
+    const f32x2 u = f2_fma(p1.x, dy, dx);
+    const float2 e = f2_unpack(f2_fma(f2_mul(p1.y, u), u, f2_mul(f2_mul(p2.x, dy), dy)));
+    ored = f2_unpack(p2.y);
+    return make_float2(fminf(kAlphaMax, ored.x * ex2_approx(e.x)), fminf(kAlphaMax, ored.x * ex2_approx(e.y)));
 }
 
 template <int STAGING>
@@ -229,7 +255,8 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
                                                           unsigned spin_limit, unsigned* __restrict__ err) {
     pdl_entry();
     constexpr int kB = kFwdBatch;
-    __shared__ FwdStage s;
+    __shared__ FwdSmem sm;
+    FwdStage& s = sm.st;
     const int tile = blockIdx.x;
     const int tx = tile % cam.tiles_x, ty = tile / cam.tiles_x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -237,6 +264,7 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
     const int px = bx + (lane & 7), py0 = by + (lane >> 3), py1 = py0 + 4;
     const bool in0 = px < cam.width && py0 < cam.height, in1 = px < cam.width && py1 < cam.height;
     const float fpx = (float)px + 0.5f, fpy0 = (float)py0 + 0.5f, fpy1 = (float)py1 + 0.5f;
+    const f32x2 fpx2 = f2_pack(fpx, fpx), fpy2 = f2_pack(fpy0, fpy1);
     const float wx0 = (float)bx + 0.5f, wx1 = wx0 + 7.f, wy0 = (float)by + 0.5f, wy1 = wy0 + 7.f;
 
     const uint2 rg = ranges[tile];
@@ -280,9 +308,15 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
             ok = stage_wait<STAGING>(s, slot, (unsigned)(b >> 1) & 1u, n_in, pre, spin_limit, err);
             if (ok) consumed = b;
         }
-        if (threadIdx.x < n_in)
-            s.cull[threadIdx.x] = prepare_record(s.rec[slot][threadIdx.x][0], s.rec[slot][threadIdx.x][1],
-                                                 s.rec[slot][threadIdx.x][2], s.cull2[threadIdx.x]);
+        if (threadIdx.x < n_in) {
+            float4 q0 = s.rec[slot][threadIdx.x][0], q1 = s.rec[slot][threadIdx.x][1], q2 = s.rec[slot][threadIdx.x][2];
+            s.cull[threadIdx.x] = prepare_record(q0, q1, q2, s.cull2[threadIdx.x]);
+            float4* pr = sm.pair[threadIdx.x];
+            pr[0] = make_float4(q0.x, q0.x, q0.y, q0.y);
+            pr[1] = make_float4(q2.y, q2.y, q2.z, q2.z);
+            pr[2] = make_float4(q2.w, q2.w, q1.y, q1.z);
+            pr[3] = make_float4(q1.w, q2.x, 0.f, 0.f);
+        }
         if (__syncthreads_or(!ok)) break;
         const int nl = compact_warp(s, n_in, kB, wx0, wx1, wy0, wy1, warp, lane);
         // two listed Gaussians per iteration: their alphas do not depend on the transmittance, so
@@ -291,26 +325,15 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
             if (__all_sync(0xffffffffu, done0 && done1)) break;
             const bool two = k + 1 < nl;  // warp-uniform
             const int ja = s.list[warp][k], jb = two ? s.list[warp][k + 1] : ja;
-            const float2 a0 = *reinterpret_cast<const float2*>(&s.rec[slot][ja][0]);  // mean
-            const float4 a1 = s.rec[slot][ja][1];                                     // (D, o, r, g)
-            const float4 a2 = s.rec[slot][ja][2];                                     // (b, r, A', D')
-            const float2 b0 = *reinterpret_cast<const float2*>(&s.rec[slot][jb][0]);
-            const float4 b1 = s.rec[slot][jb][1];
-            const float4 b2 = s.rec[slot][jb][2];
-            const float dxa = a0.x - fpx, dya0 = a0.y - fpy0, dya1 = a0.y - fpy1;
-            const float dxb = b0.x - fpx, dyb0 = b0.y - fpy0, dyb1 = b0.y - fpy1;
-            const float ua0 = __fmaf_rn(a2.y, dya0, dxa), ua1 = __fmaf_rn(a2.y, dya1, dxa);
-            const float ub0 = __fmaf_rn(b2.y, dyb0, dxb), ub1 = __fmaf_rn(b2.y, dyb1, dxb);
-            const float al_a0 = fminf(kAlphaMax, a1.y * ex2_approx(__fmaf_rn(a2.z * ua0, ua0, a2.w * dya0 * dya0)));
-            const float al_a1 = fminf(kAlphaMax, a1.y * ex2_approx(__fmaf_rn(a2.z * ua1, ua1, a2.w * dya1 * dya1)));
-            const float al_b0 = fminf(kAlphaMax, b1.y * ex2_approx(__fmaf_rn(b2.z * ub0, ub0, b2.w * dyb0 * dyb0)));
-            const float al_b1 = fminf(kAlphaMax, b1.y * ex2_approx(__fmaf_rn(b2.z * ub1, ub1, b2.w * dyb1 * dyb1)));
+            float2 oa, ga, ob, gb2;
+            const float2 al_a = pair_alphas(sm.pair[ja], fpx2, fpy2, oa, ga);
+            const float2 al_b = pair_alphas(sm.pair[jb], fpx2, fpy2, ob, gb2);
             const unsigned posa = (unsigned)(b * kB + ja + 1), posb = (unsigned)(b * kB + jb + 1);
-            if (!done0) blend_pixel(al_a0, a1, a2.x, posa, T0, c00, c01, c02, last0, done0);
-            if (!done1) blend_pixel(al_a1, a1, a2.x, posa, T1, c10, c11, c12, last1, done1);
+            if (!done0) blend_pixel(al_a.x, oa.y, ga.x, ga.y, posa, T0, c00, c01, c02, last0, done0);
+            if (!done1) blend_pixel(al_a.y, oa.y, ga.x, ga.y, posa, T1, c10, c11, c12, last1, done1);
             if (two) {
-                if (!done0) blend_pixel(al_b0, b1, b2.x, posb, T0, c00, c01, c02, last0, done0);
-                if (!done1) blend_pixel(al_b1, b1, b2.x, posb, T1, c10, c11, c12, last1, done1);
+                if (!done0) blend_pixel(al_b.x, ob.y, gb2.x, gb2.y, posb, T0, c00, c01, c02, last0, done0);
+                if (!done1) blend_pixel(al_b.y, ob.y, gb2.x, gb2.y, posb, T1, c10, c11, c12, last1, done1);
             }
         }
         if (STAGING == GS_STAGE_LOADS) {
