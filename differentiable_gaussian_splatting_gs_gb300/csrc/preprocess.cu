@@ -470,15 +470,17 @@ __device__ __forceinline__ bool grad_one(const float* m, const float* ls, const 
     return true;
 }
 
-// Statistics (STATS) and the parameter gradients of Gaussian i (radius rad; `my` holds its SH
-// gradients) written or, when accumulating, added to the outputs; the SH row is stored by the caller.
-template <int K3, bool STATS, bool VEC>
+// Statistics (when stats.accum is set) and the parameter gradients of Gaussian i (radius rad; `my`
+// holds its SH gradients) written or, when accumulating, added to the outputs; the SH row is stored
+// by the caller. The statistics are a run-time choice, so that the gradients come from the same
+// machine code with and without them (bit-identical results).
+template <int K3, bool VEC>
 __device__ __forceinline__ void finish_one(int i, int rad, float4 g0, const float* dm, const float* dls,
                                            const float* dq, float dlg, const float* my, const DensifyArgs& stats,
                                            int accumulate, float* __restrict__ d_mean3d,
                                            float* __restrict__ d_log_scale, float* __restrict__ d_quat,
                                            float* __restrict__ d_logit) {
-    if (STATS) {
+    if (stats.accum) {
     // 3D Gaussian splatting's densification statistics and the 2-norm of this view's parameter
     // gradients (the tile row holds this view's SH gradients), as gs_densify_stats computes them
     if (rad > 0) {
@@ -518,9 +520,9 @@ __device__ __forceinline__ void finish_one(int i, int rad, float4 g0, const floa
 }
 
 // One thread per Gaussian, SH rows by coalesced 4-byte asynchronous copies (any SH degree and
-// alignment). STATS: also the post-backward statistics of the view (see DensifyArgs), from the
-// gradients this call computes.
-template <int DEG, bool STATS>
+// alignment). With stats.accum set, also the post-backward statistics of the view (see
+// DensifyArgs), from the gradients this call computes.
+template <int DEG>
 __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
     int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
     const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
@@ -556,7 +558,7 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
         float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
         if (!(rad > 0 && grad_one<DEG, false>(m, ls, q, lg, g0, g1, g2, cam, my, dm, dls, dq, dlg)))
             for (int k = 0; k < K3; ++k) my[k] = 0.f;
-        finish_one<K3, STATS, false>(i, rad, g0, dm, dls, dq, dlg, my, stats, accumulate, d_mean3d, d_log_scale,
+        finish_one<K3, false>(i, rad, g0, dm, dls, dq, dlg, my, stats, accumulate, d_mean3d, d_log_scale,
                                      d_quat, d_logit);
     }
     __syncwarp();
@@ -570,7 +572,7 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd(
 // next group before waiting for the current group's rows, and each group's gradient rows leave by
 // bulk copies (bulk additions when accumulating) that complete while the warp goes on; a lane
 // refills its row only after its own copy out of it has read it.
-template <int DEG, bool STATS>
+template <int DEG>
 __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd_pipe(
     int n, const float* __restrict__ mean3d, const float* __restrict__ log_scale,
     const float* __restrict__ quat, const float* __restrict__ logit, const float* __restrict__ sh,
@@ -631,7 +633,7 @@ __global__ void __launch_bounds__(kBwdThreads, 5) k_preprocess_bwd_pipe(
             float dm[3] = {0.f, 0.f, 0.f}, dls[3] = {0.f, 0.f, 0.f}, dq[4] = {0.f, 0.f, 0.f, 0.f}, dlg = 0.f;
             if (!(rad > 0 && grad_one<DEG, true>(m, ls, q, lg, g0, g1, g2, cam, my, dm, dls, dq, dlg)))
                 for (int k = 0; k < K3 / 4; ++k) reinterpret_cast<float4*>(my)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            finish_one<K3, STATS, true>(i, rad, g0, dm, dls, dq, dlg, my, stats, accumulate, d_mean3d, d_log_scale,
+            finish_one<K3, true>(i, rad, g0, dm, dls, dq, dlg, my, stats, accumulate, d_mean3d, d_log_scale,
                                         d_quat, d_logit);
             // accumulating: rows of Gaussians with radius 0 add nothing and are skipped
             if (!accumulate || rad > 0) {
@@ -689,25 +691,25 @@ cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCa
                       p.sh, cam, rec, out.depth, out.radius, tt);
 }
 
-template <int DEG, bool STATS>
+template <int DEG>
 cudaError_t launch_bwd_pipe(int n, const gs_params& p, const KernelCamera& cam, const int* radius, const float4* g2,
                             float* dm, float* dls, float* dq, float* dlg, float* dsh, int accumulate,
                             const DensifyArgs& stats, unsigned spin_limit, unsigned* err, cudaStream_t st) {
     static std::atomic<int> cache[256];
     const int blocks = (n + kBwdThreads - 1) / kBwdThreads;
-    const int res = resident_blocks(k_preprocess_bwd_pipe<DEG, STATS>, kBwdThreads, cache);
-    return launch_pdl(k_preprocess_bwd_pipe<DEG, STATS>, dim3(res > 0 && res < blocks ? res : blocks),
-                      dim3(kBwdThreads), 0, st, n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius,
-                      g2, dm, dls, dq, dlg, dsh, accumulate, stats, spin_limit, err);
+    const int res = resident_blocks(k_preprocess_bwd_pipe<DEG>, kBwdThreads, cache);
+    return launch_pdl(k_preprocess_bwd_pipe<DEG>, dim3(res > 0 && res < blocks ? res : blocks), dim3(kBwdThreads), 0,
+                      st, n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg,
+                      dsh, accumulate, stats, spin_limit, err);
 }
 
-template <int DEG, bool STATS>
+template <int DEG>
 cudaError_t launch_bwd_plain(int n, const gs_params& p, const KernelCamera& cam, const int* radius, const float4* g2,
                              float* dm, float* dls, float* dq, float* dlg, float* dsh, int accumulate,
                              const DensifyArgs& stats, cudaStream_t st) {
-    return launch_pdl(k_preprocess_bwd<DEG, STATS>, dim3((n + kBwdThreads - 1) / kBwdThreads), dim3(kBwdThreads), 0,
-                      st, n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg,
-                      dsh, accumulate, stats);
+    return launch_pdl(k_preprocess_bwd<DEG>, dim3((n + kBwdThreads - 1) / kBwdThreads), dim3(kBwdThreads), 0, st, n,
+                      p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg, dsh,
+                      accumulate, stats);
 }
 
 cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const KernelCamera& cam, const int* radius,
@@ -717,29 +719,19 @@ cudaError_t launch_preprocess_bwd(int deg, int n, const gs_params& p, const Kern
     if (n == 0) return cudaSuccess;
     const float4* g2 = reinterpret_cast<const float4*>(grad2d);
     const DensifyArgs none{};
-    const DensifyArgs& sa = stats ? *stats : none;
+    const DensifyArgs& sa = stats ? *stats : none;   // none.accum == nullptr: no statistics
     count_launches(1);
-    if ((deg == 1 || deg == 3) && aligned16(p.sh) && aligned16(dsh)) {
-        if (deg == 1)
-            return stats ? launch_bwd_pipe<1, true>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
-                                                    spin_limit, err, st)
-                         : launch_bwd_pipe<1, false>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
-                                                     spin_limit, err, st);
-        return stats ? launch_bwd_pipe<3, true>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
-                                                spin_limit, err, st)
-                     : launch_bwd_pipe<3, false>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa,
-                                                 spin_limit, err, st);
-    }
-#define GS_PREBWD(D)                                                                                           \
-    (stats ? launch_bwd_plain<D, true>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st)         \
-           : launch_bwd_plain<D, false>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st))
+    if ((deg == 1 || deg == 3) && aligned16(p.sh) && aligned16(dsh))
+        return deg == 1 ? launch_bwd_pipe<1>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, spin_limit,
+                                             err, st)
+                        : launch_bwd_pipe<3>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, spin_limit,
+                                             err, st);
     switch (deg) {
-        case 0: return GS_PREBWD(0);
-        case 1: return GS_PREBWD(1);
-        case 2: return GS_PREBWD(2);
-        default: return GS_PREBWD(3);
+        case 0: return launch_bwd_plain<0>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st);
+        case 1: return launch_bwd_plain<1>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st);
+        case 2: return launch_bwd_plain<2>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st);
+        default: return launch_bwd_plain<3>(n, p, cam, radius, g2, dm, dls, dq, dlg, dsh, accumulate, sa, st);
     }
-#undef GS_PREBWD
 }
 
 }  // namespace gs
