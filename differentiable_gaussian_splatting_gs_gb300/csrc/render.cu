@@ -61,7 +61,7 @@ using FwdStage = StageSmemT<kFwdBatch, 4>;
 // instruction would): (mx, mx, my, my), (r, r, A', A'), (D', D', o, red), (green, blue, -, -).
 struct FwdSmem {
     FwdStage st;
-    float4 pair[kFwdBatch][4];
+    float4 pair[4][kFwdBatch];   // [field][record]: conflict-free writes by consecutive threads
 };
 // Backward layouts, PX pixels per lane: PX = 2 is the forward's layout (128 threads, 8x8 warp
 // blocks); PX = 4 gives each warp a 16x8 block (64 threads per tile; warp w covers rows 8w..8w+7,
@@ -233,12 +233,12 @@ __device__ __forceinline__ void blend_pixel(float alpha, float cr, float cg, flo
 // o 2^(A' u^2 + D' dy^2) with u = dx + r dy, each half computed in the same order and rounding as
 // the scalar form. fpx2 = (px, px) and fpy2 = (py0, py1) are the pixel centres. Also returns
 // (o, red) and (green, blue).
-__device__ __forceinline__ float2 pair_alphas(const float4 (&pr)[4], f32x2 fpx2, f32x2 fpy2, float2& ored,
-                                              float2& gb) {
-    const ulonglong2 p0 = *reinterpret_cast<const ulonglong2*>(&pr[0]);   // (mx, mx), (my, my)
-    const ulonglong2 p1 = *reinterpret_cast<const ulonglong2*>(&pr[1]);   // (r, r), (A', A')
-    const ulonglong2 p2 = *reinterpret_cast<const ulonglong2*>(&pr[2]);   // (D', D'), (o, red)
-    gb = *reinterpret_cast<const float2*>(&pr[3]);
+__device__ __forceinline__ float2 pair_alphas(const float4 (&pr)[4][kFwdBatch], int j, f32x2 fpx2, f32x2 fpy2,
+                                              float2& ored, float2& gb) {
+    const ulonglong2 p0 = *reinterpret_cast<const ulonglong2*>(&pr[0][j]);   // (mx, mx), (my, my)
+    const ulonglong2 p1 = *reinterpret_cast<const ulonglong2*>(&pr[1][j]);   // (r, r), (A', A')
+    const ulonglong2 p2 = *reinterpret_cast<const ulonglong2*>(&pr[2][j]);   // (D', D'), (o, red)
+    gb = *reinterpret_cast<const float2*>(&pr[3][j]);
     const f32x2 dx = f2_sub(p0.x, fpx2), dy = f2_sub(p0.y, fpy2);
     const f32x2 u = f2_fma(p1.x, dy, dx);
     const float2 e = f2_unpack(f2_fma(f2_mul(p1.y, u), u, f2_mul(f2_mul(p2.x, dy), dy)));
@@ -311,11 +311,11 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
         if (threadIdx.x < n_in) {
             float4 q0 = s.rec[slot][threadIdx.x][0], q1 = s.rec[slot][threadIdx.x][1], q2 = s.rec[slot][threadIdx.x][2];
             s.cull[threadIdx.x] = prepare_record(q0, q1, q2, s.cull2[threadIdx.x]);
-            float4* pr = sm.pair[threadIdx.x];
-            pr[0] = make_float4(q0.x, q0.x, q0.y, q0.y);
-            pr[1] = make_float4(q2.y, q2.y, q2.z, q2.z);
-            pr[2] = make_float4(q2.w, q2.w, q1.y, q1.z);
-            pr[3] = make_float4(q1.w, q2.x, 0.f, 0.f);
+            const int t = threadIdx.x;
+            sm.pair[0][t] = make_float4(q0.x, q0.x, q0.y, q0.y);
+            sm.pair[1][t] = make_float4(q2.y, q2.y, q2.z, q2.z);
+            sm.pair[2][t] = make_float4(q2.w, q2.w, q1.y, q1.z);
+            sm.pair[3][t] = make_float4(q1.w, q2.x, 0.f, 0.f);
         }
         if (__syncthreads_or(!ok)) break;
         const int nl = compact_warp(s, n_in, kB, wx0, wx1, wy0, wy1, warp, lane);
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kFwdBlock) k_render_fwd(const float4* __restri
             const bool two = k + 1 < nl;  // warp-uniform
             const int ja = s.list[warp][k], jb = two ? s.list[warp][k + 1] : ja;
             float2 oa, ga, ob, gb2;
-            const float2 al_a = pair_alphas(sm.pair[ja], fpx2, fpy2, oa, ga);
-            const float2 al_b = pair_alphas(sm.pair[jb], fpx2, fpy2, ob, gb2);
+            const float2 al_a = pair_alphas(sm.pair, ja, fpx2, fpy2, oa, ga);
+            const float2 al_b = pair_alphas(sm.pair, jb, fpx2, fpy2, ob, gb2);
             const unsigned posa = (unsigned)(b * kB + ja + 1), posb = (unsigned)(b * kB + jb + 1);
             if (!done0) blend_pixel(al_a.x, oa.y, ga.x, ga.y, posa, T0, c00, c01, c02, last0, done0);
             if (!done1) blend_pixel(al_a.y, oa.y, ga.x, ga.y, posa, T1, c10, c11, c12, last1, done1);
