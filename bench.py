@@ -12,12 +12,14 @@ does not synchronise) and each timed step is one replay; `--no-graph` times eage
 
 Prints one JSON line. `value` is the whole-job throughput in Mpix/s (pixels of all ranks' views
 per second of the slowest rank), measured with CUDA events on the device with inputs resident;
-`e2e` is the same metric with each step's inputs copied from pinned host memory and its
-parameter gradients copied back inside the timed region; the copies run on their own streams
-and overlap the neighbouring steps' compute (two parameter and gradient sets; the median of
-three timed pipelines), and the serial figure is reported beside it. `e2e.host_link` is the
-copy-engine bandwidth of the host link measured alone (each direction, and both at once), the
-time one step's copies need at that rate, and its fraction of the pipelined step. With N > 1 (torchrun) every rank runs an
+`e2e` is the same metric through the C ABI's host-buffer entry point, gs_train_step_host: each
+step copies its parameters and target in from pinned host memory and its parameter gradients,
+loss and D back, inside the timed region; three step contexts on three streams take the steps in
+turn, so a step's copies overlap its neighbours' compute and copies (the median of three timed
+runs), and the serial
+figure (one context) is reported beside it. `e2e.host_link` is the copy-engine bandwidth of the
+host link measured alone (each direction, and both at once), the time one step's copies need at
+that rate, and its fraction of the pipelined step. With N > 1 (torchrun) every rank runs an
 independent replica of the step (the path needs no exchange within a view). `--impl reference`
 times the float64 CPU oracle on the host cores instead, on a bounded sample of the same workload.
 """
@@ -604,103 +606,68 @@ def run_ours(args, rank, world, local_rank):
     ms = reduce_max(sum(step_ms) / len(step_ms), world, dev)
     value = throughput_mpix(world, P, ms)
 
-    # ---- end to end: inputs from pinned host memory, gradients back, inside the timed region
+    # ---- end to end through the C ABI's host-buffer entry point (gs_train_step_host): every step
+    # copies its parameters and target in from pinned host memory and its parameter gradients, loss
+    # and D back, inside the timed region
     e2e = None
-    if not args.no_e2e:
-        h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_target.numel() * 4
-        d2h = sum(t.numel() * t.element_size() for t in host_grads.values())
-        e_ms = []
-        barrier()
-        torch.cuda.synchronize()
-        for _ in range(max(3, args.steps // 2)):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for k in names:
-                params[k].copy_(host[k], non_blocking=True)
-            target.copy_(host_target, non_blocking=True)
-            if use_graph:
-                gstep.replay()
-            else:
-                one_step()
-            for k in names:
-                host_grads[k].copy_(grads[k], non_blocking=True)
-            e1.record(stream)
+    if not args.no_e2e and n_views == 1:
+        n_dup_e2e = int(gstep.n_dup.sum()) if use_graph else int(n_dup_dev.sum()) if not args.sync_sort else n_dup
+        cap_e2e = max(1024, int(n_dup_e2e * 1.05) + 1024)
+        NC = 3  # contexts (and streams) that take the steps in turn
+        ctxs = [api.StepContext(scene.n, scene.sh_degree, cam.width, cam.height, cap_e2e) for _ in range(NC)]
+        hin = [host] + [{k: torch.empty_like(v).pin_memory().copy_(v) for k, v in host.items()} for _ in range(NC - 1)]
+        htg = [host_target[0]] + [host_target[0].clone().pin_memory() for _ in range(NC - 1)]
+        hout = [host_grads] + [{k: torch.empty_like(v).pin_memory() for k, v in host.items()} for _ in range(NC - 1)]
+        hloss = [torch.zeros(1).pin_memory() for _ in range(NC)]
+        hdup = [torch.zeros(1, dtype=torch.int64).pin_memory() for _ in range(NC)]
+        streams = [torch.cuda.Stream(dev) for _ in range(NC)]
+        h2d = sum(t.numel() * t.element_size() for t in host.values()) + htg[0].numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in host.values()) + 4 + 8
+
+        def e2e_run(K, nctx):
+            """K steps through gs_train_step_host, alternating over nctx contexts and streams; ms per step."""
             torch.cuda.synchronize()
-            e_ms.append(e0.elapsed_time(e1))
-        barrier()
-        em_serial = reduce_max(sum(e_ms) / len(e_ms), world, dev)
-        em, pipeline = em_serial, "serial: copy in, step, copy out"
-        if use_graph:
-            # Pipelined: two parameter / gradient sets, each with its captured step, and one stream
-            # per copy direction; step k's parameters go in while step k-1 computes and step k-2's
-            # gradients come out (every step still copies all its inputs in and its gradients out).
-            params2 = {k: torch.empty_like(params[k]) for k in names}
-            grads2 = api.alloc_param_grads(params2)
-            host_grads2 = {k: torch.empty_like(host[k]).pin_memory() for k in names}
-            target2 = torch.empty_like(target)
-            for k in names:
-                params2[k].copy_(params[k])
-            target2.copy_(target)
-            gstep2 = step.GraphedStep(params2, cams, [target2[v] for v in range(n_views)], opt, grads2, bufs,
-                                      bufs.sort.capacity)
-            sets = [(params, grads, host_grads, target, gstep), (params2, grads2, host_grads2, target2, gstep2)]
-            s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-            ev_in = [torch.cuda.Event() for _ in range(2)]
-            ev_comp = [torch.cuda.Event() for _ in range(2)]
-            ev_out = [torch.cuda.Event() for _ in range(2)]
-            K = max(6, args.steps)
+            barrier()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t0.record(streams[0])
+            for s_ in streams[1:nctx]:
+                s_.wait_event(t0)
+            for kstep in range(K):
+                b = kstep % nctx
+                api.gs_train_step_host(ctxs[b], hin[b], htg[b], cam, opt, hout[b], hloss[b], hdup[b],
+                                       stream=streams[b])
+            ends = []
+            for s_ in streams[:nctx]:
+                e_ = torch.cuda.Event(enable_timing=True)
+                e_.record(s_)
+                ends.append(e_)
+            torch.cuda.synchronize()
+            barrier()
+            return max(t0.elapsed_time(e_) for e_ in ends) / K
 
-            def run_pipeline(K):
-                for kstep in range(K):
-                    b = kstep % 2
-                    p_, g_, hg_, tg_, gs_ = sets[b]
-                    with torch.cuda.stream(s_in):
-                        if kstep >= 2:
-                            s_in.wait_event(ev_comp[b])  # the set's previous step has read its parameters
-                        for k in names:
-                            p_[k].copy_(host[k], non_blocking=True)
-                        tg_.copy_(host_target, non_blocking=True)
-                        ev_in[b].record(s_in)
-                    with torch.cuda.stream(stream):
-                        stream.wait_event(ev_in[b])
-                        if kstep >= 2:
-                            stream.wait_event(ev_out[b])  # the set's previous gradients have been copied out
-                        gs_.replay()
-                        ev_comp[b].record(stream)
-                    with torch.cuda.stream(s_out):
-                        s_out.wait_event(ev_comp[b])
-                        for k in names:
-                            hg_[k].copy_(g_[k], non_blocking=True)
-                        ev_out[b].record(s_out)
-
-            def pipelined_ms():
-                barrier()
-                torch.cuda.synchronize()
-                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                t0.record(s_in)
-                run_pipeline(K)
-                t1.record(s_out)
-                torch.cuda.synchronize()
-                barrier()
-                return t0.elapsed_time(t1) / K
-
-            # the median of three timed pipelines (host memory and its link are shared with other devices
-            # and processes; one run can be slowed by traffic that is not ours)
-            runs = [pipelined_ms() for _ in range(3)]
-            em = reduce_max(statistics.median(runs), world, dev)
-            pipeline = ("pipelined over steps: copies in and out on their own streams overlap the previous "
-                        "step's compute (two parameter and gradient sets)")
-            assert api.gs_device_error() == 0
+        K = max(6, args.steps)
+        e2e_run(NC, NC)  # warm-up of every context
+        serial = [e2e_run(K, 1) for _ in range(2)]
+        runs = [e2e_run(K, NC) for _ in range(3)]
+        assert api.gs_device_error() == 0
+        assert int(hdup[0][0]) == n_dup_e2e, "the host-buffer step's D differs from the timed step's"
+        em_serial = reduce_max(min(serial), world, dev)
+        # the median of three timed pipelines (host memory and its link are shared with other devices
+        # and processes; one run can be slowed by traffic that is not ours)
+        em = reduce_max(statistics.median(runs), world, dev)
         e2e = {"value": throughput_mpix(world, P, em), "unit": "Mpix/s", "ms_per_step": em,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "pipeline": pipeline,
-               "serial_ms_per_step": em_serial}
-        if use_graph:
-            e2e["pipelined_runs_ms"] = runs
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "call": "gs_train_step_host (C ABI, host buffers in and out, one cudaMemcpyAsync per array)",
+               "pipeline": f"{NC} step contexts on {NC} streams in turn: a step's copies in, compute and copies out "
+                           "overlap its neighbours'",
+               "serial_ms_per_step": em_serial, "pipelined_runs_ms": runs}
         # the host link alone: what the copies of one step take at the link's own rate (copy engines,
         # pinned memory, both directions at once, as in the pipeline), against the step's period
         link = host_link_gbs(host["sh"], torch.empty_like(grads["sh"]), stream)
         link_ms = max(h2d, d2h) / (link["both_gbs_each"] * 1e6)
         e2e["host_link"] = dict(link, copy_ms_per_step=link_ms, frac=link_ms / em)
+        for c_ in ctxs:
+            c_.close()
     assert api.gs_device_error() == 0
 
     # ---- the update phase after the step (not part of the fwd+bwd metric): sparse Adam over the

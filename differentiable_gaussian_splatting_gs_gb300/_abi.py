@@ -31,7 +31,8 @@ EXPORTS = ("gs_preprocess", "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_re
            "gs_selftest_timeout", "gs_kernel_launches", "gs_version", "gs_bin_and_sort_static", "gs_adam_step",
            "gs_densify_stats", "gs_loss_workspace_bytes", "gs_loss_l1_dssim", "gs_preprocess2d",
            "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd", "gs_bin_and_sort_async",
-           "gs_preprocess_bwd_stats", "gs_selftest_sort_timeout", "gs_render_bwd_sqerr")
+           "gs_preprocess_bwd_stats", "gs_selftest_sort_timeout", "gs_render_bwd_sqerr",
+           "gs_step_context_create", "gs_step_context_destroy", "gs_train_step_host")
 GS_STATIC_SORT_WORKSPACE_BYTES = 32 << 20
 GS_SELFTEST_SORT_WORKSPACE_BYTES = 128 << 10
 
@@ -140,6 +141,12 @@ def load():
         lib.gs_preprocess2d_bwd.argtypes = [ppar, pcam, popt, pproj, P, P, P, P, P, P, I32, P]
         for name in ("gs_preprocess2d", "gs_render2d_fwd", "gs_render2d_bwd", "gs_preprocess2d_bwd"):
             getattr(lib, name).restype = C.c_int
+        lib.gs_step_context_create.argtypes = [I64, I32, I32, I32, I64, C.POINTER(C.c_void_p)]
+        lib.gs_step_context_create.restype = C.c_int
+        lib.gs_step_context_destroy.argtypes = [P]
+        lib.gs_step_context_destroy.restype = C.c_int
+        lib.gs_train_step_host.argtypes = [P, ppar, P, pcam, popt, C.POINTER(gs_tensors), P, P, P]
+        lib.gs_train_step_host.restype = C.c_int
         for name in ("gs_preprocess", "gs_bin_and_sort", "gs_render_fwd", "gs_render_bwd",
                      "gs_preprocess_bwd", "gs_device_error", "gs_version", "gs_selftest_timeout"):
             getattr(lib, name).restype = C.c_int

@@ -19,7 +19,7 @@ from . import _abi
 from ._abi import (GS_BWD_ADAPTIVE, GS_BWD_DIRECT, GS_BWD_SM, GS_BWD_WARP, GS_ERR_CAPACITY, GsError, check,
                    gs_camera, gs_options, gs_params, gs_proj)
 
-__all__ = ["Proj", "BinResult", "make_camera", "make_options", "alloc_proj", "gs_preprocess",
+__all__ = ["Proj", "BinResult", "StepContext", "gs_train_step_host", "make_camera", "make_options", "alloc_proj", "gs_preprocess",
            "gs_sort_workspace_bytes", "gs_bin_and_sort", "gs_bin_and_sort_async", "gs_render_fwd", "gs_render_bwd",
            "gs_preprocess_bwd",
            "gs_device_error", "GsError", "GS_BWD_DIRECT", "GS_BWD_WARP", "GS_BWD_ADAPTIVE", "GS_BWD_SM"]
@@ -426,3 +426,55 @@ def gs_kernel_launches() -> int:
 def gs_device_error(stream=None) -> int:
     """Synchronises and returns (and clears) the device error status: 0, GS_ERR_TIMEOUT or GS_ERR_DEVICE_CHECK."""
     return int(_abi.load().gs_device_error(_stream(stream)))
+
+
+class StepContext:
+    """Device buffers of the end-to-end training step with host buffers (gs_step_context_create):
+    n Gaussians of SH degree `sh_degree`, images of at most max_width x max_height, `capacity`
+    duplicates. Freed by close() (or when garbage-collected)."""
+
+    def __init__(self, n: int, sh_degree: int, max_width: int, max_height: int, capacity: int):
+        lib = _abi.load()
+        h = C.c_void_p()
+        _abi.check(lib.gs_step_context_create(int(n), int(sh_degree), int(max_width), int(max_height), int(capacity),
+                                              C.byref(h)), "gs_step_context_create")
+        self._h = h
+        self.n, self.sh_degree, self.capacity = int(n), int(sh_degree), int(capacity)
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _abi.check(_abi.load().gs_step_context_destroy(self._h), "gs_step_context_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _host_ptr(t) -> int:
+    if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != torch.float32:
+        raise ValueError("host buffers must be contiguous float32 CPU tensors")
+    return t.data_ptr()
+
+
+def gs_train_step_host(ctx: StepContext, host_params: dict, host_target, cam, opt: gs_options, host_grads: dict,
+                       host_loss=None, host_n_dup=None, stream=None) -> None:
+    """One training step of one view through the C ABI with host buffers (gs_train_step_host): the
+    parameters and the target are copied in, the step runs on the device, the parameter gradients
+    (and the loss and D when given: a 1-element float32 / int64 CPU tensor) are copied back into
+    `host_grads`. Enqueued on `stream`; synchronise it before reading the outputs."""
+    p = gs_params(mean3d=_host_ptr(host_params["mean3d"]), log_scale=_host_ptr(host_params["log_scale"]),
+                  quat=_host_ptr(host_params["quat"]), opacity_logit=_host_ptr(host_params["opacity_logit"]),
+                  sh=_host_ptr(host_params["sh"]), n=int(host_params["mean3d"].shape[0]))
+    g = _abi.gs_tensors(mean3d=_host_ptr(host_grads["mean3d"]), log_scale=_host_ptr(host_grads["log_scale"]),
+                        quat=_host_ptr(host_grads["quat"]), opacity_logit=_host_ptr(host_grads["opacity_logit"]),
+                        sh=_host_ptr(host_grads["sh"]), n=int(host_grads["mean3d"].shape[0]))
+    if host_n_dup is not None and (host_n_dup.device.type != "cpu" or host_n_dup.dtype != torch.int64):
+        raise ValueError("host_n_dup must be an int64 CPU tensor")
+    c = make_camera(cam)
+    _abi.check(_abi.load().gs_train_step_host(ctx._h, C.byref(p), _host_ptr(host_target), C.byref(c), C.byref(opt),
+                                              C.byref(g), None if host_loss is None else _host_ptr(host_loss),
+                                              None if host_n_dup is None else host_n_dup.data_ptr(), _stream(stream)),
+               "gs_train_step_host")

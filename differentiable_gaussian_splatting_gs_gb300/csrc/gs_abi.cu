@@ -653,4 +653,160 @@ int gs_preprocess2d_bwd(const gs_params* p, const gs_camera* cam, const gs_optio
     return e ? cuda_fail(e, "gs_preprocess2d_bwd") : GS_OK;
 }
 
+// ---- the training step with host buffers --------------------------------------------------
+
 }  // extern "C"
+
+struct gs_step_context {
+    int device;
+    long long n, capacity;
+    int deg, max_w, max_h;
+    // device buffers (each its own allocation, 256-byte aligned)
+    float *mean3d, *log_scale, *quat, *logit, *sh;       // parameters
+    float *d_mean3d, *d_log_scale, *d_quat, *d_logit, *d_sh;  // their gradients
+    float *rec, *depth;
+    int* radius;
+    unsigned* tiles_touched;
+    void* ws;
+    size_t ws_bytes;
+    unsigned *vals, *ranges;
+    unsigned long long* n_dup;
+    float *image, *t_final, *target, *grad2d, *loss;
+    unsigned* n_contrib;
+};
+
+namespace {
+
+void free_context(gs_step_context* c) {
+    void* ptrs[] = {c->mean3d, c->log_scale, c->quat, c->logit, c->sh, c->d_mean3d, c->d_log_scale, c->d_quat,
+                    c->d_logit, c->d_sh, c->rec, c->depth, c->radius, c->tiles_touched, c->ws, c->vals,
+                    c->ranges, c->n_dup, c->image, c->t_final, c->target, c->grad2d, c->loss, c->n_contrib};
+    for (void* q : ptrs)
+        if (q) cudaFree(q);
+    delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gs_step_context_create(int64_t n, int32_t sh_degree, int32_t max_width, int32_t max_height, int64_t capacity,
+                           gs_step_context** out) {
+    if (!out) return fail(GS_ERR_ARG, "gs_step_context_create: out is NULL");
+    if (n < 0 || n >= (1ll << 31)) return fail(GS_ERR_ARG, "gs_step_context_create: n = %lld outside 0..2^31-1",
+                                               (long long)n);
+    if (sh_degree < 0 || sh_degree > 3) return fail(GS_ERR_ARG, "gs_step_context_create: sh_degree %d", sh_degree);
+    if (max_width <= 0 || max_height <= 0 || max_width > kMaxImageSide || max_height > kMaxImageSide)
+        return fail(GS_ERR_ARG, "gs_step_context_create: image %d x %d", max_width, max_height);
+    const long long tx = (max_width + kTile - 1) / kTile, ty = (max_height + kTile - 1) / kTile;
+    if (!counting_path(tx * ty))
+        return fail(GS_ERR_ARG, "gs_step_context_create: %lld tiles; the step without host synchronisation "
+                    "handles images of up to 49152 tiles", tx * ty);
+    if (capacity < 0 || capacity > 0x7fffffffll)
+        return fail(GS_ERR_ARG, "gs_step_context_create: capacity outside 0..2^31-1");
+    auto* c = new gs_step_context{};
+    c->n = n;
+    c->capacity = capacity;
+    c->deg = sh_degree;
+    c->max_w = max_width;
+    c->max_h = max_height;
+    cudaError_t e = cudaGetDevice(&c->device);
+    const size_t nn = (size_t)(n > 0 ? n : 1), K3 = 3 * (size_t)(sh_degree + 1) * (sh_degree + 1);
+    const size_t P = (size_t)max_width * max_height;
+    auto get = [&](auto** p, size_t bytes) {
+        if (!e) e = cudaMalloc(reinterpret_cast<void**>(p), bytes > 0 ? bytes : 4);
+    };
+    get(&c->mean3d, 12 * nn); get(&c->log_scale, 12 * nn); get(&c->quat, 16 * nn); get(&c->logit, 4 * nn);
+    get(&c->sh, 4 * K3 * nn);
+    get(&c->d_mean3d, 12 * nn); get(&c->d_log_scale, 12 * nn); get(&c->d_quat, 16 * nn); get(&c->d_logit, 4 * nn);
+    get(&c->d_sh, 4 * K3 * nn);
+    get(&c->rec, 48 * nn); get(&c->depth, 4 * nn); get(&c->radius, 4 * nn); get(&c->tiles_touched, 4 * nn);
+    c->ws_bytes = gs_sort_workspace_bytes(n, capacity, max_width, max_height);
+    get(&c->ws, c->ws_bytes);
+    get(&c->vals, 4 * (size_t)(capacity > 0 ? capacity : 1)); get(&c->ranges, 8 * (size_t)(tx * ty));
+    get(&c->n_dup, 8);
+    get(&c->image, 12 * P); get(&c->t_final, 4 * P); get(&c->target, 12 * P); get(&c->n_contrib, 4 * P);
+    get(&c->grad2d, 48 * nn); get(&c->loss, 4);
+    if (e) {
+        free_context(c);
+        return cuda_fail(e, "gs_step_context_create");
+    }
+    *out = c;
+    return GS_OK;
+}
+
+int gs_step_context_destroy(gs_step_context* ctx) {
+    if (!ctx) return GS_OK;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(ctx->device);
+    const cudaError_t e = cudaDeviceSynchronize();
+    free_context(ctx);
+    cudaSetDevice(prev);
+    return e ? cuda_fail(e, "gs_step_context_destroy") : GS_OK;
+}
+
+int gs_train_step_host(gs_step_context* ctx, const gs_params* hp, const float* host_target, const gs_camera* cam,
+                       const gs_options* opt, const gs_tensors* hg, float* host_loss, int64_t* host_n_dup,
+                       void* stream) {
+    if (!ctx || !hp || !host_target || !cam || !hg) return fail(GS_ERR_ARG, "gs_train_step_host: NULL argument");
+    Opts o;
+    KernelCamera kc;
+    int s;
+    if ((s = resolve_options(opt, o)) || (s = make_camera(cam, o, kc))) return s;
+    if (o.deg != ctx->deg) return fail(GS_ERR_ARG, "gs_train_step_host: sh_degree %d, context %d", o.deg, ctx->deg);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != ctx->device)
+        return fail(GS_ERR_ARG, "gs_train_step_host: current device %d, the context's is %d", dev, ctx->device);
+    if (hp->n != ctx->n || hg->n != ctx->n)
+        return fail(GS_ERR_ARG, "gs_train_step_host: n = %lld / %lld, context %lld", (long long)hp->n,
+                    (long long)hg->n, ctx->n);
+    if (cam->width > ctx->max_w || cam->height > ctx->max_h)
+        return fail(GS_ERR_ARG, "gs_train_step_host: image %d x %d, context at most %d x %d", cam->width, cam->height,
+                    ctx->max_w, ctx->max_h);
+    const size_t n = (size_t)ctx->n, K3 = 3 * (size_t)(ctx->deg + 1) * (ctx->deg + 1);
+    if (n > 0 && (!hp->mean3d || !hp->log_scale || !hp->quat || !hp->opacity_logit || !hp->sh || !hg->mean3d ||
+                  !hg->log_scale || !hg->quat || !hg->opacity_logit || !hg->sh))
+        return fail(GS_ERR_ARG, "gs_train_step_host: a parameter or gradient array is NULL");
+    cudaStream_t st = as_stream(stream);
+    const size_t P = (size_t)cam->width * cam->height;
+    // host -> device: one asynchronous copy per array
+    struct Cp { void* dst; const void* src; size_t bytes; };
+    const Cp in[] = {{ctx->mean3d, hp->mean3d, 12 * n}, {ctx->log_scale, hp->log_scale, 12 * n},
+                     {ctx->quat, hp->quat, 16 * n}, {ctx->logit, hp->opacity_logit, 4 * n},
+                     {ctx->sh, hp->sh, 4 * K3 * n}, {ctx->target, host_target, 12 * P}};
+    for (const Cp& c : in) {
+        if (c.bytes == 0) continue;
+        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyHostToDevice, st);
+        if (e) return cuda_fail(e, "gs_train_step_host: copy in");
+    }
+    const gs_params dp{ctx->mean3d, ctx->log_scale, ctx->quat, ctx->logit, ctx->sh, ctx->n};
+    gs_proj proj{ctx->rec, ctx->depth, ctx->radius, ctx->tiles_touched, ctx->n};
+    if ((s = gs_preprocess(&dp, cam, opt, &proj, stream))) return s;
+    if ((s = gs_bin_and_sort_async(&proj, cam, opt, ctx->ws, ctx->ws_bytes, nullptr, ctx->vals, ctx->capacity,
+                                   reinterpret_cast<uint64_t*>(ctx->n_dup), ctx->ranges, stream)))
+        return s;
+    if ((s = gs_render_fwd(&proj, ctx->vals, ctx->ranges, cam, opt, ctx->image, ctx->t_final, ctx->n_contrib,
+                           stream)))
+        return s;
+    if ((s = gs_render_bwd_sqerr(&proj, ctx->vals, ctx->ranges, cam, opt, ctx->image, ctx->target, ctx->t_final,
+                                 ctx->n_contrib, ctx->grad2d, ctx->loss, stream)))
+        return s;
+    if ((s = gs_preprocess_bwd(&dp, cam, opt, &proj, ctx->grad2d, ctx->d_mean3d, ctx->d_log_scale, ctx->d_quat,
+                               ctx->d_logit, ctx->d_sh, 0, stream)))
+        return s;
+    // device -> host
+    const Cp out[] = {{hg->mean3d, ctx->d_mean3d, 12 * n}, {hg->log_scale, ctx->d_log_scale, 12 * n},
+                      {hg->quat, ctx->d_quat, 16 * n}, {hg->opacity_logit, ctx->d_logit, 4 * n},
+                      {hg->sh, ctx->d_sh, 4 * K3 * n}, {host_loss, ctx->loss, host_loss ? 4u : 0u},
+                      {host_n_dup, ctx->n_dup, host_n_dup ? 8u : 0u}};
+    for (const Cp& c : out) {
+        if (c.bytes == 0) continue;
+        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToHost, st);
+        if (e) return cuda_fail(e, "gs_train_step_host: copy out");
+    }
+    return GS_OK;
+}
+
+}  // extern "C"
+

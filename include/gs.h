@@ -16,7 +16,9 @@
  * Conventions common to every call.
  *   - Pointers to arrays are DEVICE pointers, C-contiguous, row-major, owned by the caller. The
  *     library allocates no device memory and keeps no state between calls except a per-device
- *     error word (see gs_device_error) and a per-thread last-error message.
+ *     error word (see gs_device_error) and a per-thread last-error message. The one exception is
+ *     the end-to-end pair at the end of this header: gs_step_context_create allocates a context's
+ *     device buffers, and gs_train_step_host takes HOST pointers for its inputs and outputs.
  *   - Projected records (gs_proj.rec) and 2D gradients (grad2d) must be 16-byte aligned; every
  *     other array must be 4-byte aligned (8-byte for keys). Misalignment returns GS_ERR_ARG.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls enqueue work on it and
@@ -426,6 +428,49 @@ int gs_selftest_timeout(uint32_t spin_limit, void* stream);
  * by the caller (overwritten). Errors: GS_ERR_ARG (workspace), GS_ERR_CUDA.                     */
 #define GS_SELFTEST_SORT_WORKSPACE_BYTES (128u << 10)
 int gs_selftest_sort_timeout(void* workspace, size_t workspace_bytes, uint32_t spin_limit, void* stream);
+
+/* ---- the whole training step of one view with host buffers ------------------------------
+ * The step of Odin's Figure 7 (preprocessing, rendering, backward computation; Odin:
+ * Primitive-Level Synchronization for Distributed Point-Based Neural Rendering) driven from host
+ * memory: the parameters and the target image are copied in, the step runs on the device, and
+ * the parameter gradients, the loss and D come back, all asynchronously on one stream.
+ *
+ * gs_step_context_create allocates, on the current device, the device buffers of such steps for n
+ * Gaussians of SH degree sh_degree on images of at most max_width x max_height pixels (at most
+ * 49,152 tiles) with room for `capacity` duplicates: the parameters, their gradients, the
+ * projected records, the sort workspace and lists, the image, transmittance, contributor counts,
+ * target and 2D gradients (about 2 x 4 (14 + 3K) n + 20 capacity + 44 max_width max_height bytes
+ * plus the sort workspace). The context belongs to the caller: one step at a time per context
+ * (two contexts on two streams overlap one step's copies with another's compute).
+ * Errors: GS_ERR_ARG (sizes, degree, NULL out), GS_ERR_CUDA (allocation); *out is set only on
+ * success. gs_step_context_destroy frees it (NULL is accepted) after synchronising the device. */
+typedef struct gs_step_context gs_step_context;
+int gs_step_context_create(int64_t n, int32_t sh_degree, int32_t max_width, int32_t max_height, int64_t capacity,
+                           gs_step_context** out);
+int gs_step_context_destroy(gs_step_context* ctx);
+
+/* One training step of one view with host buffers (the library's end-to-end entry point):
+ *   host_params: the n Gaussians' parameters in host memory (layout of gs_params; n must equal the
+ *     context's); host_target [3][H][W] float32 (the camera's size); both are copied to the device
+ *     with one cudaMemcpyAsync per array;
+ *   then gs_preprocess, gs_bin_and_sort_async (capacity: the context's), gs_render_fwd,
+ *   gs_render_bwd_sqerr (loss 0.5 |image - target|^2) and gs_preprocess_bwd (overwriting) run on
+ *   the device buffers;
+ *   host_grads: the parameter gradients, copied back into host memory (layout of gs_tensors,
+ *     n = the context's); host_loss (one float) and host_n_dup (D, one int64) may be NULL.
+ * Everything is enqueued on `stream` (NULL = the default stream) and the call returns without
+ * waiting: the host buffers must stay valid, and the outputs are ready, once the stream has
+ * reached this point (cudaStreamSynchronize). Page-locked host memory (cudaHostAlloc or
+ * cudaHostRegister) lets the copies run asynchronously and overlap other streams' work; with
+ * pageable memory the copies are staged and synchronous. A capacity overflow drops duplicates
+ * and sets the device check bit (gs_device_error returns GS_ERR_DEVICE_CHECK); host_n_dup then
+ * holds the number that was needed. opt->sh_degree must equal the context's degree, and the
+ * current device the one the context was created on.
+ * Errors: GS_ERR_ARG (NULL or mismatched arguments, an image larger than the context's),
+ * GS_ERR_CUDA; the device-side errors of the calls it makes.                                  */
+int gs_train_step_host(gs_step_context* ctx, const gs_params* host_params, const float* host_target,
+                       const gs_camera* cam, const gs_options* opt, const gs_tensors* host_grads, float* host_loss,
+                       int64_t* host_n_dup, void* stream);
 
 /* Number of kernels this library has launched in this process (all devices, all threads). */
 int64_t gs_kernel_launches(void);

@@ -128,6 +128,26 @@ def test_new_entry_points_reject_bad_arguments_on_the_host(lib):
     assert b"GS_BWD_SM" in lib.gs_last_error_message()
 
 
+def test_host_step_entry_points_reject_bad_arguments_on_the_host(lib):
+    """The end-to-end pair checks its arguments before any CUDA call."""
+    h = C.c_void_p()
+    assert lib.gs_step_context_create(10, 3, 64, 64, 100, None) == _abi.GS_ERR_ARG
+    assert lib.gs_step_context_create(-1, 3, 64, 64, 100, C.byref(h)) == _abi.GS_ERR_ARG
+    assert lib.gs_step_context_create(10, 4, 64, 64, 100, C.byref(h)) == _abi.GS_ERR_ARG
+    assert b"sh_degree" in lib.gs_last_error_message()
+    assert lib.gs_step_context_create(10, 3, 0, 64, 100, C.byref(h)) == _abi.GS_ERR_ARG
+    assert lib.gs_step_context_create(10, 3, 4096, 4096, 100, C.byref(h)) == _abi.GS_ERR_ARG
+    assert b"49152" in lib.gs_last_error_message()
+    assert lib.gs_step_context_create(10, 3, 64, 64, -5, C.byref(h)) == _abi.GS_ERR_ARG
+    assert h.value is None  # not set on failure
+    assert lib.gs_step_context_destroy(None) == _abi.GS_OK
+    cam, opt = _cam(), api.make_options(3)
+    p, g = _abi.gs_params(n=10), _abi.gs_tensors(n=10)
+    assert lib.gs_train_step_host(None, C.byref(p), 256, C.byref(cam), C.byref(opt), C.byref(g), None, None,
+                                  None) == _abi.GS_ERR_ARG
+    assert b"NULL" in lib.gs_last_error_message()
+
+
 def test_product_path_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(_abi, "_lib", None)
