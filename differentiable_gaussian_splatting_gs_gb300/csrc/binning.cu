@@ -1193,7 +1193,32 @@ __global__ void __launch_bounds__(256) k_fine_scan(int Ts, int SX, int tiles_x, 
 // position of each of the 16 tiles (the same values in all lanes); per round and per tile that some
 // lane's Gaussian covers, those lanes write consecutive positions (their rank among the covering
 // lanes) and the tile's position advances. The tile loop is unrolled so that the 16 positions stay
-// in registers and the tiles' updates are independent of one another.
+// in registers and the tiles' updates are independent of one another. The loads of a warp's next
+// segment (its entries, its tiles' first positions) are issued before the current segment is
+// placed, so that their latency overlaps the placement.
+struct FineSeg {
+    unsigned iv[kRounds];   // the segment's entries (depth positions), ~0u past its end
+    unsigned start;         // lane t < 16: first position of tile t for this segment
+    int tx0, ty0;
+};
+
+__device__ __forceinline__ void fine_seg_load(FineSeg& f, unsigned k, int Ts, int SX, int tiles_x, int tiles_y,
+                                              const unsigned* s_first, const uint2* __restrict__ crange,
+                                              const unsigned* __restrict__ cvals, const unsigned* __restrict__ F,
+                                              const unsigned* __restrict__ tile_start, int lane) {
+    const int st = segment_tile(s_first, Ts, k);
+    const uint2 rg = crange[st];
+    const unsigned p0 = rg.x + (k - s_first[st]) * kSeg, p1 = min(p0 + kSeg, rg.y);
+    f.tx0 = (st % SX) * kSuper;
+    f.ty0 = (st / SX) * kSuper;
+    f.start = 0;
+    const int tx = f.tx0 + (lane & 3), ty = f.ty0 + ((lane >> 2) & 3);
+    if (lane < kSuperTiles && tx < tiles_x && ty < tiles_y)
+        f.start = tile_start[ty * tiles_x + tx] + F[(size_t)k * kSuperTiles + lane];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) f.iv[r] = p0 + 32 * r + lane < p1 ? cvals[p0 + 32 * r + lane] : ~0u;
+}
+
 __global__ void __launch_bounds__(256) k_fine_place(int Ts, int SX, int tiles_x, int tiles_y, unsigned n_bound,
                                                     const unsigned* __restrict__ seg_first,
                                                     const unsigned* __restrict__ nseg,
@@ -1211,35 +1236,27 @@ __global__ void __launch_bounds__(256) k_fine_place(int Ts, int SX, int tiles_x,
     __syncthreads();
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    const unsigned ns = *nseg, wpb = blockDim.x >> 5;
-    for (unsigned k = blockIdx.x * wpb + (threadIdx.x >> 5); k < ns; k += gridDim.x * wpb) {
-        const int st = segment_tile(s_first, Ts, k);
-        const uint2 rg = crange[st];
-        const unsigned p0 = rg.x + (k - s_first[st]) * kSeg, p1 = min(p0 + kSeg, rg.y);
-        const int tx0 = (st % SX) * kSuper, ty0 = (st / SX) * kSuper;
-        unsigned mine_start = 0;  // lane t < 16: first position of tile t for this segment
-        {
-            const int tx = tx0 + (lane & 3), ty = ty0 + ((lane >> 2) & 3);
-            if (lane < kSuperTiles && tx < tiles_x && ty < tiles_y)
-                mine_start = tile_start[ty * tiles_x + tx] + F[(size_t)k * kSuperTiles + lane];
+    const unsigned ns = *nseg, wpb = blockDim.x >> 5, stride = gridDim.x * wpb;
+    unsigned k = blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (k >= ns) return;
+    FineSeg cur;
+    fine_seg_load(cur, k, Ts, SX, tiles_x, tiles_y, s_first, crange, cvals, F, tile_start, lane);
+    const unsigned lt = lanemask_lt();
+    for (; k < ns; k += stride) {
+        // the entries' rectangles and Gaussians (dependent loads), then the next segment's loads
+        unsigned m16v[kRounds], gv[kRounds];
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {  // a depth position below V <= n
+            const bool ok = cur.iv[r] < n_bound;
+            m16v[r] = ok ? cover_mask(crect[cur.iv[r]], cur.tx0, cur.ty0) : 0u;
+            gv[r] = ok ? perm[cur.iv[r]] : 0u;
         }
         unsigned next[kSuperTiles];
 #pragma unroll
-        for (int t = 0; t < kSuperTiles; ++t) next[t] = __shfl_sync(full, mine_start, t);
-        // all of the segment's entries are loaded first (see k_fine_count)
-        unsigned m16v[kRounds], gv[kRounds];
-        {
-            unsigned iv[kRounds];
-#pragma unroll
-            for (int r = 0; r < kRounds; ++r) iv[r] = p0 + 32 * r + lane < p1 ? cvals[p0 + 32 * r + lane] : ~0u;
-#pragma unroll
-            for (int r = 0; r < kRounds; ++r) {  // a depth position below V <= n
-                const bool ok = iv[r] < n_bound;
-                m16v[r] = ok ? cover_mask(crect[iv[r]], tx0, ty0) : 0u;
-                gv[r] = ok ? perm[iv[r]] : 0u;
-            }
-        }
-        const unsigned lt = lanemask_lt();
+        for (int t = 0; t < kSuperTiles; ++t) next[t] = __shfl_sync(full, cur.start, t);
+        const int tx0 = cur.tx0, ty0 = cur.ty0;
+        if (k + stride < ns)
+            fine_seg_load(cur, k + stride, Ts, SX, tiles_x, tiles_y, s_first, crange, cvals, F, tile_start, lane);
 #pragma unroll
         for (int r = 0; r < kRounds; ++r) {
             const unsigned m16 = m16v[r], g = gv[r];
@@ -1510,10 +1527,14 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
                         w.nchunks, w.chunk_first, w.crect, sx, sy, band_rows, nbands, w.table, w.stile_start,
                         (unsigned)capacity, w.cvals, err)))
         return e;
-    // grid-stride kernels over the segments: at most 8 resident blocks of 8 warps per SM
+    // grid-stride kernels over the segments (8 warps per block): at most the resident blocks
+    static std::atomic<int> count_cache[256], place_cache[256];
     const long long seg_blocks = (w.seg_cap + 7) / 8;
-    const unsigned fblocks = (unsigned)(seg_blocks < 152 * 8 ? seg_blocks : 152 * 8);
-    if ((e = launch_pdl(k_fine_count, dim3(fblocks), dim3(256), fsmem, st, ts, sx, (unsigned)proj.n, w.seg_first,
+    const int rc = resident_blocks(k_fine_count, 256, fsmem, count_cache);
+    const int rp = resident_blocks(k_fine_place, 256, fsmem, place_cache);
+    const unsigned fcblocks = (unsigned)(rc > 0 && seg_blocks > rc ? rc : seg_blocks);
+    const unsigned fblocks = (unsigned)(rp > 0 && seg_blocks > rp ? rp : seg_blocks);
+    if ((e = launch_pdl(k_fine_count, dim3(fcblocks), dim3(256), fsmem, st, ts, sx, (unsigned)proj.n, w.seg_first,
                         w.nseg, reinterpret_cast<const uint2*>(w.crange), w.cvals, w.crect, w.fcount)))
         return e;
     if ((e = launch_pdl(k_fine_scan, dim3((unsigned)((ts + 7) / 8)), dim3(256), 0, st, ts, sx, tiles_x, tiles_y,

@@ -1,6 +1,8 @@
 // Declarations shared by the library's translation units (host side).
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -87,6 +89,23 @@ cudaError_t selftest_lookback(unsigned char* ws, unsigned spin_limit, unsigned* 
 
 // Number of SMs of the current device (looked up once per device; 1 if the query fails).
 int device_sm_count();
+
+// Blocks of `kernel` (`threads` threads, `smem` bytes of dynamic shared memory) resident on the
+// current device at once: SMs x blocks per SM, looked up once per device (the caller keeps one
+// cache per kernel); 0 if the query fails.
+template <class Kernel>
+int resident_blocks(Kernel kernel, int threads, size_t smem, std::atomic<int> (&cache)[256]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        int per = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, smem) != cudaSuccess) return 0;
+        v = device_sm_count() * (per > 0 ? per : 1);
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
 
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
                               unsigned spin_limit, unsigned* err, cudaStream_t st);

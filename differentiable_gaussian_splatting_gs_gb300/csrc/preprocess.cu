@@ -653,22 +653,6 @@ namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace
 
-// Blocks of `kernel` (`threads` threads, static shared memory only) resident on the current device
-// at once: SMs x blocks per SM, looked up once per device; 0 if the query fails.
-template <class Kernel>
-int resident_blocks(Kernel kernel, int threads, std::atomic<int> (&cache)[256]) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
-    int v = cache[dev].load(std::memory_order_relaxed);
-    if (v == 0) {
-        int per = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kernel, threads, 0) != cudaSuccess) return 0;
-        v = device_sm_count() * (per > 0 ? per : 1);
-        cache[dev].store(v, std::memory_order_relaxed);
-    }
-    return v;
-}
-
 cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCamera& cam, const gs_proj& out,
                               unsigned spin_limit, unsigned* err, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
@@ -679,7 +663,7 @@ cudaError_t launch_preprocess(int deg, int n, const gs_params& p, const KernelCa
     if ((deg == 1 || deg == 3) && aligned16(p.sh)) {
         static std::atomic<int> cache1[256], cache3[256];
         auto k = deg == 1 ? k_preprocess_pipe<1> : k_preprocess_pipe<3>;
-        const int res = resident_blocks(k, kFwdThreads, deg == 1 ? cache1 : cache3);
+        const int res = resident_blocks(k, kFwdThreads, 0, deg == 1 ? cache1 : cache3);
         const int grid = res > 0 && res < blocks ? res : blocks;
         return launch_pdl(k, dim3(grid), dim3(kFwdThreads), 0, st, n, p.mean3d, p.log_scale, p.quat,
                           p.opacity_logit, p.sh, cam, rec, out.depth, out.radius, tt, spin_limit, err);
@@ -697,7 +681,7 @@ cudaError_t launch_bwd_pipe(int n, const gs_params& p, const KernelCamera& cam, 
                             const DensifyArgs& stats, unsigned spin_limit, unsigned* err, cudaStream_t st) {
     static std::atomic<int> cache[256];
     const int blocks = (n + kBwdThreads - 1) / kBwdThreads;
-    const int res = resident_blocks(k_preprocess_bwd_pipe<DEG>, kBwdThreads, cache);
+    const int res = resident_blocks(k_preprocess_bwd_pipe<DEG>, kBwdThreads, 0, cache);
     return launch_pdl(k_preprocess_bwd_pipe<DEG>, dim3(res > 0 && res < blocks ? res : blocks), dim3(kBwdThreads), 0,
                       st, n, p.mean3d, p.log_scale, p.quat, p.opacity_logit, p.sh, cam, radius, g2, dm, dls, dq, dlg,
                       dsh, accumulate, stats, spin_limit, err);
