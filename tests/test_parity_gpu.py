@@ -339,6 +339,32 @@ def test_preprocess_sh_layouts_match_oracle(deg):
             assert int(once[k][culled].count_nonzero()) == 0, k
 
 
+@pytest.mark.parametrize("n", [1, 31, 33, 4097])
+def test_preprocess_bulk_rows_ragged_sizes_and_all_culled(n):
+    """The bulk-copy preprocess kernels (degree 3, aligned arrays, persistent grids) on group counts
+    that are not multiples of the grid, a last group of 1..31 Gaussians, and a scene with every
+    Gaussian behind the camera (no row is copied, every gradient row is written as zeros, and
+    accumulating adds nothing)."""
+    s = gs_scenes.make_scene_random_small(70 + n, n, 96, 80, 90.0, 3)
+    cam = s.cameras[0]
+    pre = oracle.preprocess(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, 3, cam)
+    g2n = np.random.default_rng(n).standard_normal((s.n, 9)).astype(np.float32)
+    want = oracle.preprocess_bwd(s.mean3d, s.log_scale, s.quat, s.opacity_logit, s.sh, 3, cam, g2n)
+    gc.check_preprocess(s, cam, pre)
+    gc.check_preprocess_bwd(s, cam, pre, g2n, want)
+    s.mean3d[:, 2] = -1.0  # everything culled
+    params = dev_params(s)
+    opt = api.make_options(3)
+    proj = api.gs_preprocess(params, cam, opt)
+    assert int(proj.radius.abs().max()) == 0 and float(proj.rec.abs().max()) == 0.0
+    g2 = torch.from_numpy(np.pad(g2n, ((0, 0), (0, 3)))).to(DEV)
+    grads = {k: torch.full_like(v, 7.0) for k, v in params.items()}
+    api.gs_preprocess_bwd(params, cam, opt, proj, g2, out=grads)
+    assert all(float(v.abs().max()) == 0.0 for v in grads.values())
+    api.gs_preprocess_bwd(params, cam, opt, proj, g2, out=grads, accumulate=True)
+    assert all(float(v.abs().max()) == 0.0 for v in grads.values())
+
+
 # --------------------------------------------------------------------------------- end to end
 
 @pytest.mark.parametrize("mode", ["adaptive", "direct"])
