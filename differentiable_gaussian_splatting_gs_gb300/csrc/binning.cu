@@ -1144,19 +1144,30 @@ __global__ void __launch_bounds__(256) k_fine_count(int Ts, int SX, unsigned n_b
             for (int r = 0; r < kRounds; ++r)  // a depth position below V <= n
                 m16[r] = iv[r] < n_bound ? cover_mask(crect[iv[r]], tx0, ty0) : 0u;
         }
-        unsigned cnt = 0;  // lane t < 16: tile t
+        // Per-tile counts of the warp's masks, four tiles per 32-bit word: the nibble of tiles
+        // 4j..4j+3 is spread into the four bytes of a word (x * 0x204081 places bits 0..3 of x at
+        // bits 0, 8, 16, 24 with nothing overlapping them), and one warp add-reduction of each word
+        // sums 32 lanes per byte (at most 32). The sums of the rounds are kept in 16-bit fields
+        // (at most 8 x 32 = 256): acc[2j] holds tiles 4j and 4j + 2, acc[2j + 1] tiles 4j + 1, 4j + 3.
+        unsigned acc[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
         for (int r = 0; r < kRounds; ++r) {
-            const unsigned any = __reduce_or_sync(0xffffffffu, m16[r]);
 #pragma unroll
-            for (int t = 0; t < kSuperTiles; ++t) {
-                if (any & (1u << t)) {  // warp-uniform
-                    const unsigned c = __popc(__ballot_sync(0xffffffffu, (m16[r] >> t) & 1u));
-                    if (lane == t) cnt += c;
-                }
+            for (int j = 0; j < 4; ++j) {
+                const unsigned spread = (((m16[r] >> (4 * j)) & 0xfu) * 0x00204081u) & 0x01010101u;
+                const unsigned sum = __reduce_add_sync(0xffffffffu, spread);
+                acc[2 * j] += sum & 0x00ff00ffu;
+                acc[2 * j + 1] += (sum >> 8) & 0x00ff00ffu;
             }
         }
-        if (lane < kSuperTiles) F[(size_t)k * kSuperTiles + lane] = cnt;
+        if (lane < kSuperTiles) {
+            // tile t = 4j + b: word 2j + (b & 1), field b >> 1 (selected without indexing registers)
+            const int j = lane >> 2, b = lane & 3;
+            unsigned w = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) w = (q == 2 * j + (b & 1)) ? acc[q] : w;
+            F[(size_t)k * kSuperTiles + lane] = (w >> (16 * (b >> 1))) & 0xffffu;
+        }
     }
 }
 
