@@ -439,8 +439,8 @@ int gs_selftest_sort_timeout(void* workspace, size_t workspace_bytes, uint32_t s
  * Gaussians of SH degree sh_degree on images of at most max_width x max_height pixels (at most
  * 49,152 tiles) with room for `capacity` duplicates: the parameters, their gradients, the
  * projected records, the sort workspace and lists, the image, transmittance, contributor counts,
- * target and 2D gradients (about 2 x 4 (14 + 3K) n + 20 capacity + 44 max_width max_height bytes
- * plus the sort workspace). The context belongs to the caller: one step at a time per context
+ * target and 2D gradients (about (196 + 24 K) n + 4 capacity + 32 max_width max_height bytes,
+ * K = (sh_degree + 1)^2, plus gs_sort_workspace_bytes(n, capacity, max_width, max_height)). The context belongs to the caller: one step at a time per context
  * (two contexts on two streams overlap one step's copies with another's compute).
  * Errors: GS_ERR_ARG (sizes, degree, NULL out), GS_ERR_CUDA (allocation); *out is set only on
  * success. gs_step_context_destroy frees it (NULL is accepted) after synchronising the device. */
