@@ -104,6 +104,56 @@ def train_step_async(params: dict, cameras, targets, opt, grads: dict, buffers: 
     return image
 
 
+def train_step_async_overlapped(params: dict, cameras, targets, opt, grads: dict, buffers, capacity: int,
+                                n_dup: torch.Tensor, events=None, upstream=None, losses=None, streams=None):
+    """train_step_async for several views with two buffer sets (`buffers`: two StepBuffers) on two
+    streams: view v runs on stream v % 2 with buffer set v % 2, so that one view's preprocess, sort
+    and rasterization overlap the other's. The preprocess backward of view v waits for view v - 1's,
+    so the views' gradients are added in view order as in train_step_async; a buffer set is reused
+    two views later, after its stream has finished with it. Both streams fork from and join the
+    current stream (so the step can be captured into a CUDA graph from it). streams: the two side
+    streams (created here when None)."""
+    main = torch.cuda.current_stream()
+    if streams is None:
+        streams = [torch.cuda.Stream(main.device), torch.cuda.Stream(main.device)]
+    for st in streams:
+        st.wait_stream(main)
+    prev = None  # event after the previous view's preprocess backward
+    image = None
+    for v, (cam, target) in enumerate(zip(cameras, targets)):
+        st, buf = streams[v % 2], buffers[v % 2]
+        ev = events[v] if events is not None else None
+        c = cam if isinstance(cam, api.gs_camera) else api.make_camera(cam)
+        with torch.cuda.stream(st):
+            proj = api.gs_preprocess(params, c, opt, out=buf.proj, stream=st)
+            image, t_final, n_contrib, dl, ranges = buf.image_buffers(c.width, c.height)
+            b = api.gs_bin_and_sort_async(proj, c, opt, capacity, buffers=buf.sort, ranges=ranges,
+                                          n_dup=n_dup[v:v + 1], stream=st)
+            if ev is not None:
+                ev[0][0].record(st)
+            api.gs_render_fwd(proj, b.vals, b.ranges, c, opt, out=(image, t_final, n_contrib), stream=st)
+            if ev is not None:
+                ev[0][1].record(st)
+                ev[1][0].record(st)
+            if upstream is None:
+                api.gs_render_bwd_sqerr(proj, b.vals, b.ranges, c, opt, image, target, t_final, n_contrib,
+                                        grad2d=buf.grad2d, loss=losses[v:v + 1] if losses is not None else None,
+                                        stream=st)
+            else:
+                api.gs_render_bwd(proj, b.vals, b.ranges, c, opt, upstream[v], t_final, n_contrib,
+                                  grad2d=buf.grad2d, stream=st)
+            if ev is not None:
+                ev[1][1].record(st)
+            if prev is not None:
+                st.wait_event(prev)
+            api.gs_preprocess_bwd(params, c, opt, proj, buf.grad2d, out=grads, accumulate=v > 0, stream=st)
+            prev = torch.cuda.Event()
+            prev.record(st)
+    for st in streams:
+        main.wait_stream(st)
+    return image
+
+
 def train_step_surfels_async(params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
                              n_dup: torch.Tensor, events=None, stream=None):
     """train_step_async for the surfel (2D Gaussian splatting) pipeline: gs_preprocess2d, the same
@@ -138,12 +188,13 @@ class GraphedStep:
     written to, the same tensors at every replay (update them in place between replays)."""
 
     def __init__(self, params: dict, cameras, targets, opt, grads: dict, buffers: StepBuffers, capacity: int,
-                 events=None, surfels: bool = False, upstream=None):
+                 events=None, surfels: bool = False, upstream=None, buffers2: StepBuffers | None = None):
         """events: as for train_step_async; to time kernels inside the graph they must be created
         with torch.cuda.Event(enable_timing=True, external=True), which captures them as event
         record nodes. surfels: capture the surfel pipeline (train_step_surfels_async) instead.
         upstream: per-view dL/dimage tensors read at every replay instead of image - target
-        (3D pipeline only)."""
+        (3D pipeline only). buffers2: a second buffer set; with it and several views the 3D
+        pipeline runs its views on two streams (train_step_async_overlapped)."""
         self.device = buffers.device
         self.cams = [c if isinstance(c, api.gs_camera) else api.make_camera(c) for c in cameras]
         self.n_dup = torch.zeros(len(self.cams), dtype=torch.int64, device=self.device)
@@ -152,6 +203,14 @@ class GraphedStep:
         if surfels:
             assert upstream is None, "upstream gradients are supported by the 3D pipeline only"
             run = train_step_surfels_async
+        elif buffers2 is not None and len(self.cams) > 1:
+            side_streams = [torch.cuda.Stream(self.device), torch.cuda.Stream(self.device)]
+
+            def run(p, cams, tg, o, g, bufs, cap, nd, ev):
+                return train_step_async_overlapped(p, cams, tg, o, g, [bufs, buffers2], cap, nd, events=ev,
+                                                   upstream=upstream,
+                                                   losses=None if upstream is not None else self.losses,
+                                                   streams=side_streams)
         else:
             def run(*a):
                 return train_step_async(*a, upstream=upstream, losses=None if upstream is not None else self.losses)

@@ -103,8 +103,11 @@ def test_async_sort_rejects_images_beyond_the_counting_pass():
         api.gs_bin_and_sort_async(proj, big, opt, 1024)
 
 
-@pytest.mark.parametrize("cfg,n,res,views", [(1, 20_000, 1.0, None), (3, 20_000, 0.25, 3)])
-def test_graphed_step_matches_eager_step(cfg, n, res, views):
+@pytest.mark.parametrize("cfg,n,res,views,two", [(1, 20_000, 1.0, None, False), (3, 20_000, 0.25, 3, False),
+                                                  (3, 20_000, 0.25, 4, True)])
+def test_graphed_step_matches_eager_step(cfg, n, res, views, two):
+    """two: the views on two streams with two buffer sets (train_step_async_overlapped), the
+    preprocess backwards chained in view order."""
     s = gs_scenes.make_scene(cfg, n=n, res_scale=res, views=views)
     params = _params(s)
     opt = api.make_options(s.sh_degree)
@@ -114,7 +117,8 @@ def test_graphed_step_matches_eager_step(cfg, n, res, views):
     out = step.train_step(params, s.cameras, targets, opt, grads_ref, bufs)
     cap = bufs.sort.capacity
     grads = api.alloc_param_grads(params)
-    g = step.GraphedStep(params, s.cameras, targets, opt, grads, bufs, cap)
+    bufs2 = step.StepBuffers(s.n, DEV) if two else None
+    g = step.GraphedStep(params, s.cameras, targets, opt, grads, bufs, cap, buffers2=bufs2)
     for k in NAMES:
         grads[k].fill_(123.0)  # the replay must overwrite them
     for _ in range(2):
