@@ -242,13 +242,15 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
 // ---- depth sort: one histogram pass, then one kernel per 8-bit digit (decoupled look-back) -----
 //
 // k_depth_hist4 counts the four 8-bit digits of the depth keys of all Gaussians with radius > 0
-// in one pass. Each k_onesweep pass then ranks its 4096-item block locally (as k_radix_scatter),
-// publishes the block's per-digit counts, and finds the number of items of each digit in all
-// earlier blocks by looking back over their published words: a block's inclusive prefix ends the
-// walk, an aggregate is added and the walk continues. Blocks take their index from a ticket in
-// start order, so every block it waits for has started and publishes its aggregate before it
-// waits itself; each wait is bounded (spin_limit polls, then the timeout bit and a zero count).
+// in one pass. Each k_onesweep pass then counts the digits of its 4096-item block, publishes the
+// counts, ranks the block's items into shared memory (as k_radix_scatter) and finds the number of
+// items of each digit in all earlier blocks by looking back over their published words: a block's
+// inclusive prefix ends the walk, an aggregate is added and the walk continues. Blocks take their
+// index from a ticket in start order, so every block it waits for has started and publishes its
+// aggregate before it waits itself; each wait is bounded (spin_limit polls of a window of words,
+// then the timeout bit and a zero count).
 constexpr unsigned long long kStatAgg = 1ull << 62, kStatIncl = 2ull << 62, kStatVal = (1ull << 62) - 1ull;
+constexpr int kLookWindow = 8;  // earlier blocks' status words read per look-back round trip
 
 __global__ void __launch_bounds__(256) k_depth_hist4(const unsigned* __restrict__ keys, int n,
                                                      const int* __restrict__ radius, unsigned* __restrict__ ghist) {
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 3 : 1) k_onesweep(
     __shared__ unsigned woff[8][256];      // per-warp digit counts, then block-local offsets
     __shared__ unsigned lbase[256];        // block-local start of each digit
     __shared__ unsigned gbase[256];        // global start of this block's run of each digit
-    __shared__ unsigned wsum[8];
+    __shared__ unsigned wsum[8], wsum_g[8];
     __shared__ unsigned s_nvalid, s_block, s_n;
     __shared__ unsigned sk[kSortItems], sv[kSortItems];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -356,58 +358,34 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 3 : 1) k_onesweep(
     }
     __syncwarp();
     __syncthreads();
-    {
-        const int d = threadIdx.x;  // digit d = thread
-        unsigned c = 0;
+    // Digit d = thread. The block publishes its counts first, ranks its items into shared memory
+    // (block-local order) and only then looks back, so that the items' registers are free during
+    // the walk and other blocks find this block's aggregate as early as possible.
+    const int d = threadIdx.x;
+    unsigned c = 0;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const unsigned t = woff[w][d];
-            woff[w][d] = c;
-            c += t;
-        }
-        // publish the block's count of digit d, then look back for the earlier blocks' total
-        unsigned long long* my = status + (size_t)block * 256 + d;
-        if (block == 0) {
-            *(volatile unsigned long long*)my = kStatIncl | c;
-        } else {
-            *(volatile unsigned long long*)my = kStatAgg | c;
-        }
-        unsigned long long before = 0;
-        if (block > 0) {
-            int j = block - 1;
-            unsigned polls = 0;
-            while (true) {
-                const unsigned long long sw = *(volatile const unsigned long long*)(status + (size_t)j * 256 + d);
-                if (sw & kStatIncl) {
-                    before += sw & kStatVal;
-                    break;
-                }
-                if (sw & kStatAgg) {
-                    before += sw & kStatVal;
-                    if (--j < 0) break;  // not reached: block 0 publishes its inclusive count at once
-                    continue;
-                }
-                if (++polls >= spin_limit) {
-                    atomicOr(err, kErrTimeout);
-                    break;
-                }
-            }
-            *(volatile unsigned long long*)my = kStatIncl | (before + c);
-        }
-        // block-local exclusive scan over digits
-        unsigned x = c;
+    for (int w = 0; w < 8; ++w) {
+        const unsigned t = woff[w][d];
+        woff[w][d] = c;
+        c += t;
+    }
+    unsigned long long* my = status + (size_t)block * 256 + d;
+    *(volatile unsigned long long*)my = (block == 0 ? kStatIncl : kStatAgg) | c;
+    unsigned tx = tv;  // inclusive scan of the pass histogram over the warp's digits
+    {
+        unsigned x = c;  // block-local inclusive scan over the warp's digits
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
+            const unsigned ty = __shfl_up_sync(0xffffffffu, tx, o);
+            if (lane >= o) {
+                x += y;
+                tx += ty;
+            }
         }
-        if (lane == 31) wsum[warp] = x;
-        // global digit start: exclusive scan of the pass histogram
-        unsigned tx = tv;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, tx, o);
-            if (lane >= o) tx += y;
+        if (lane == 31) {
+            wsum[warp] = x;
+            wsum_g[warp] = tx;
         }
         __syncthreads();
         unsigned pre = 0;
@@ -417,27 +395,65 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 3 : 1) k_onesweep(
         if (d == 255) s_nvalid = lb + c;
 #pragma unroll
         for (int w = 0; w < 8; ++w) woff[w][d] += lb;
-        __syncthreads();
-        if (lane == 31) wsum[warp] = tx;
-        __syncthreads();
-        unsigned tpre = 0;
-        for (int w = 0; w < warp; ++w) tpre += wsum[w];
-        gbase[d] = tpre + tx - tv + (unsigned)before;
     }
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < kSortRounds; ++r) {
-        const unsigned d = dg[r];
-        const bool valid = d != 0x100u;
+        const unsigned dr = dg[r];
+        const bool valid = dr != 0x100u;
         const unsigned peers = pm[r];
         if (valid) {
-            const unsigned lp = woff[warp][d] + __popc(peers & lanemask_lt());
+            const unsigned lp = woff[warp][dr] + __popc(peers & lanemask_lt());
             sk[lp] = k[r];
             sv[lp] = v[r];
         }
         __syncwarp();
-        if (valid && (peers & lanemask_lt()) == 0u) woff[warp][d] += __popc(peers);
+        if (valid && (peers & lanemask_lt()) == 0u) woff[warp][dr] += __popc(peers);
         __syncwarp();
+    }
+    // look back for the number of items of digit d in all earlier blocks: the walk reads
+    // kLookWindow earlier blocks' words per round trip (their loads issued together, then read in
+    // order); aggregates are added and passed, an inclusive count ends the walk, and a word not yet
+    // published ends the window (the next window starts at that block)
+    unsigned long long before = 0;
+    if (block > 0) {
+        int j = block - 1;
+        unsigned polls = 0;
+        bool found = false;
+        while (!found) {
+            unsigned long long sw[kLookWindow];
+#pragma unroll
+            for (int w = 0; w < kLookWindow; ++w)
+                sw[w] = j - w >= 0 ? *(volatile const unsigned long long*)(status + (size_t)(j - w) * 256 + d) : 0ull;
+            int passed = 0;
+            bool stop = false;
+#pragma unroll
+            for (int w = 0; w < kLookWindow; ++w) {
+                if (!stop) {
+                    if (sw[w] & kStatIncl) {
+                        before += sw[w] & kStatVal;
+                        found = stop = true;
+                    } else if (sw[w] & kStatAgg) {
+                        before += sw[w] & kStatVal;
+                        ++passed;
+                    } else {
+                        stop = true;
+                    }
+                }
+            }
+            j -= passed;
+            if (found || j < 0) break;  // j < 0 not reached: block 0 publishes its inclusive count at once
+            if (++polls >= spin_limit) {
+                atomicOr(err, kErrTimeout);
+                break;
+            }
+        }
+        *(volatile unsigned long long*)my = kStatIncl | (before + c);
+    }
+    {
+        unsigned tpre = 0;  // global digit start: exclusive scan of the pass histogram
+        for (int w = 0; w < warp; ++w) tpre += wsum_g[w];
+        gbase[d] = tpre + tx - tv + (unsigned)before;
     }
     __syncthreads();
     const int n_block = (int)s_nvalid;
