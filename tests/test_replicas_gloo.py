@@ -30,7 +30,7 @@ def _worker(rank, world, port, out):
 
 def test_two_rank_max_time_and_whole_job_throughput():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this (possibly threaded) process
         out = m.dict()
         mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
         res = dict(out)
