@@ -483,11 +483,13 @@ __global__ void __launch_bounds__(256) k_count(int n_bound, const unsigned* __re
     if (i < n) {
         const unsigned g = perm[i];
         // an index outside the Gaussians (only after a depth pass whose look-back gave up and set
-        // the timeout bit) counts as culled, so that nothing is read out of range
-        const int r = g < (unsigned)n_bound ? radius[g] : 0;
+        // the timeout bit) counts as culled, so that nothing is read out of range; the radius and
+        // the record are loaded together (a culled Gaussian's record is zeros and goes unused)
+        const bool in = g < (unsigned)n_bound;
+        const int r = in ? radius[g] : 0;
+        const float4 r0 = in ? rec[3 * (size_t)g] : make_float4(0.f, 0.f, 0.f, 0.f);
         uint2 packed = make_uint2(0u, 0u);
         if (r > 0) {
-            const float4 r0 = rec[3 * (size_t)g];
             const Rect R = tile_rect(r0.x, r0.y, r, tiles_x, tiles_y);
             if (R.x0 <= R.x1 && R.y0 <= R.y1) {
                 cnt = (unsigned long long)(R.x1 - R.x0 + 1) * (unsigned long long)(R.y1 - R.y0 + 1);
@@ -615,9 +617,10 @@ __global__ void __launch_bounds__(256) k_emit(int n_bound, const unsigned* __res
     int x0 = 0, y0 = 0, w = 1;
     if (i < n) {
         g = perm[i];
-        const int r = g < (unsigned)n_bound ? radius[g] : 0;  // out of range only after a look-back timeout
+        const bool in = g < (unsigned)n_bound;  // out of range only after a look-back timeout
+        const int r = in ? radius[g] : 0;
+        const float4 r0 = in ? rec[3 * (size_t)g] : make_float4(0.f, 0.f, 0.f, 0.f);  // loaded with the radius
         if (r > 0) {
-            const float4 r0 = rec[3 * (size_t)g];
             const Rect R = tile_rect(r0.x, r0.y, r, tiles_x, tiles_y);
             if (R.x0 <= R.x1) {
                 x0 = R.x0; y0 = R.y0; w = R.x1 - R.x0 + 1;
