@@ -188,6 +188,7 @@ __device__ __forceinline__ int compact_warp(S& s, int n_in, int pos_limit, float
     const float x0 = wx0 - 0.01f, x1 = wx1 + 0.01f, y0 = wy0 - 0.01f, y1 = wy1 + 0.01f;
 #pragma unroll
     for (int c = 0; c < S::kB / 32; ++c) {
+        if (c * 32 >= lim) break;  // warp-uniform: the rest of the batch is empty or past the limit
         const int j = c * 32 + lane;
         bool hit = false;
         if (j < lim) {
