@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(
 // items of each digit in all earlier blocks by looking back over their published words: a block's
 // inclusive prefix ends the walk, an aggregate is added and the walk continues. Blocks take their
 // index from a ticket in start order, so every block it waits for has started and publishes its
-// aggregate before it waits itself; each wait is bounded (spin_limit polls of a window of words,
-// then the timeout bit and a zero count).
+// aggregate before it waits itself; each wait is bounded (spin_limit polls that find the next word
+// unpublished, then the timeout bit and a zero count).
 constexpr unsigned long long kStatAgg = 1ull << 62, kStatIncl = 2ull << 62, kStatVal = (1ull << 62) - 1ull;
 constexpr int kLookWindow = 8;  // earlier blocks' status words read per look-back round trip
 
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kSortThreads, IOTA ? 3 : 1) k_onesweep(
             }
             j -= passed;
             if (found || j < 0) break;  // j < 0 not reached: block 0 publishes its inclusive count at once
-            if (++polls >= spin_limit) {
+            if (passed == 0 && ++polls >= spin_limit) {  // a poll that found the next word unpublished
                 atomicOr(err, kErrTimeout);
                 break;
             }
