@@ -1249,26 +1249,19 @@ __device__ __forceinline__ void fine_seg_load(FineSeg& f, unsigned k, int Ts, in
     for (int r = 0; r < kRounds; ++r) f.iv[r] = p0 + 32 * r + lane < p1 ? cvals[p0 + 32 * r + lane] : ~0u;
 }
 
-__global__ void __launch_bounds__(256) k_fine_place(int Ts, int SX, int tiles_x, int tiles_y, unsigned n_bound,
-                                                    const unsigned* __restrict__ seg_first,
-                                                    const unsigned* __restrict__ nseg,
-                                                    const uint2* __restrict__ crange,
-                                                    const unsigned* __restrict__ cvals,
-                                                    const uint2* __restrict__ crect, const unsigned* __restrict__ perm,
-                                                    const unsigned* __restrict__ F,
-                                                    const unsigned* __restrict__ tile_start, unsigned capacity,
-                                                    unsigned* __restrict__ vals, unsigned long long* __restrict__ keys64,
-                                                    const unsigned* __restrict__ depth_bits,
-                                                    unsigned* __restrict__ err) {
-    pdl_entry();
-    extern __shared__ unsigned s_first[];
-    for (int t = threadIdx.x; t <= Ts; t += blockDim.x) s_first[t] = seg_first[t];
-    __syncthreads();
+// The placement loop of k_fine_place. KEY64: also writes the 64-bit keys. CHECK: positions may
+// reach the capacity (D above it), so each store is checked; otherwise every position is below D.
+template <bool KEY64, bool CHECK>
+__device__ __forceinline__ void fine_place_loop(unsigned k, unsigned ns, unsigned stride, int Ts, int SX, int tiles_x,
+                                                int tiles_y, unsigned n_bound, const unsigned* s_first,
+                                                const uint2* __restrict__ crange, const unsigned* __restrict__ cvals,
+                                                const uint2* __restrict__ crect, const unsigned* __restrict__ perm,
+                                                const unsigned* __restrict__ F, const unsigned* __restrict__ tile_start,
+                                                unsigned capacity, unsigned* __restrict__ vals,
+                                                unsigned long long* __restrict__ keys64,
+                                                const unsigned* __restrict__ depth_bits, unsigned* __restrict__ err,
+                                                int lane) {
     const unsigned full = 0xffffffffu;
-    const int lane = threadIdx.x & 31;
-    const unsigned ns = *nseg, wpb = blockDim.x >> 5, stride = gridDim.x * wpb;
-    unsigned k = blockIdx.x * wpb + (threadIdx.x >> 5);
-    if (k >= ns) return;
     FineSeg cur;
     fine_seg_load(cur, k, Ts, SX, tiles_x, tiles_y, s_first, crange, cvals, F, tile_start, lane);
     const unsigned lt = lanemask_lt();
@@ -1296,11 +1289,11 @@ __global__ void __launch_bounds__(256) k_fine_place(int Ts, int SX, int tiles_x,
                 if (any & (1u << t)) {  // warp-uniform
                     const bool mine = (m16 >> t) & 1u;
                     const unsigned m = __ballot_sync(full, mine);
+                    const unsigned pos = next[t] + __popc(m & lt);
                     if (mine) {
-                        const unsigned pos = next[t] + __popc(m & lt);
-                        if (pos < capacity) {
+                        if (!CHECK || pos < capacity) {
                             vals[pos] = g;
-                            if (keys64) {
+                            if (KEY64) {
                                 const unsigned tile = (unsigned)((ty0 + (t >> 2)) * tiles_x + tx0 + (t & 3));
                                 keys64[pos] = ((unsigned long long)tile << 32) | depth_bits[g];
                             }
@@ -1313,6 +1306,37 @@ __global__ void __launch_bounds__(256) k_fine_place(int Ts, int SX, int tiles_x,
             }
         }
     }
+}
+
+// total: D (the fine tile scan's); when it is within the capacity, no position reaches it and the
+// stores go unchecked.
+template <bool KEY64>
+__global__ void __launch_bounds__(256) k_fine_place(int Ts, int SX, int tiles_x, int tiles_y, unsigned n_bound,
+                                                    const unsigned* __restrict__ seg_first,
+                                                    const unsigned* __restrict__ nseg,
+                                                    const uint2* __restrict__ crange,
+                                                    const unsigned* __restrict__ cvals,
+                                                    const uint2* __restrict__ crect, const unsigned* __restrict__ perm,
+                                                    const unsigned* __restrict__ F,
+                                                    const unsigned* __restrict__ tile_start,
+                                                    const unsigned long long* __restrict__ total, unsigned capacity,
+                                                    unsigned* __restrict__ vals, unsigned long long* __restrict__ keys64,
+                                                    const unsigned* __restrict__ depth_bits,
+                                                    unsigned* __restrict__ err) {
+    pdl_entry();
+    extern __shared__ unsigned s_first[];
+    for (int t = threadIdx.x; t <= Ts; t += blockDim.x) s_first[t] = seg_first[t];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const unsigned ns = *nseg, wpb = blockDim.x >> 5, stride = gridDim.x * wpb;
+    const unsigned k = blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (k >= ns) return;
+    if (!KEY64 && *total <= (unsigned long long)capacity)  // the key-writing form keeps one, checked loop
+        fine_place_loop<KEY64, false>(k, ns, stride, Ts, SX, tiles_x, tiles_y, n_bound, s_first, crange, cvals, crect,
+                                      perm, F, tile_start, capacity, vals, keys64, depth_bits, err, lane);
+    else
+        fine_place_loop<KEY64, true>(k, ns, stride, Ts, SX, tiles_x, tiles_y, n_bound, s_first, crange, cvals, crect,
+                                     perm, F, tile_start, capacity, vals, keys64, depth_bits, err, lane);
 }
 
 // ---- self-test of the bounded look-back ------------------------------------------------------
@@ -1550,7 +1574,8 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
         return e;
     const size_t fsmem = (size_t)(ts + 1) * 4;
     if ((e = cudaFuncSetAttribute(k_fine_count, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem))) return e;
-    if ((e = cudaFuncSetAttribute(k_fine_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem))) return e;
+    auto fine_place = k64 ? k_fine_place<true> : k_fine_place<false>;
+    if ((e = cudaFuncSetAttribute(fine_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem))) return e;
     const long long warps = w.cmax * nbands;
     count_launches(5);
     if ((e = launch_pdl(k_chunk_place, dim3((unsigned)((warps + wpb - 1) / wpb)), dim3(32 * wpb), smem, st,
@@ -1558,10 +1583,10 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
                         (unsigned)capacity, w.cvals, err)))
         return e;
     // grid-stride kernels over the segments (8 warps per block): at most the resident blocks
-    static std::atomic<int> count_cache[256], place_cache[256];
+    static std::atomic<int> count_cache[256], place_cache[256], place64_cache[256];
     const long long seg_blocks = (w.seg_cap + 7) / 8;
     const int rc = resident_blocks(k_fine_count, 256, fsmem, count_cache);
-    const int rp = resident_blocks(k_fine_place, 256, fsmem, place_cache);
+    const int rp = resident_blocks(fine_place, 256, fsmem, k64 ? place64_cache : place_cache);
     const unsigned fcblocks = (unsigned)(rc > 0 && seg_blocks > rc ? rc : seg_blocks);
     const unsigned fblocks = (unsigned)(rp > 0 && seg_blocks > rp ? rp : seg_blocks);
     if ((e = launch_pdl(k_fine_count, dim3(fcblocks), dim3(256), fsmem, st, ts, sx, (unsigned)proj.n, w.seg_first,
@@ -1574,10 +1599,10 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
                         reinterpret_cast<uint2*>(ranges), err, (unsigned long long*)nullptr, (unsigned*)nullptr,
                         (unsigned*)nullptr, 0u)))
         return e;
-    return launch_pdl(k_fine_place, dim3(fblocks), dim3(256), fsmem, st, ts, sx, tiles_x, tiles_y,
+    return launch_pdl(fine_place, dim3(fblocks), dim3(256), fsmem, st, ts, sx, tiles_x, tiles_y,
                       (unsigned)proj.n, w.seg_first,
                       w.nseg, reinterpret_cast<const uint2*>(w.crange), w.cvals, w.crect, w.dvB, w.fcount,
-                      w.tile_start, (unsigned)capacity, vals, k64, depth_bits, err);
+                      w.tile_start, (const unsigned long long*)w.total, (unsigned)capacity, vals, k64, depth_bits, err);
 }
 
 // Phase 2: placement (counting pass) or emission + tile radix passes and the ranges.
