@@ -1009,14 +1009,19 @@ __global__ void __launch_bounds__(1024) k_tile_scan(int T, const unsigned* __res
 constexpr int kPlaceWarps = 8;        // warps per block when shared memory allows
 constexpr int kPlaceBands = 2;        // bands per chunk (whole super-tile rows)
 
+// The placement loop of k_chunk_place; CHECK: positions may reach the capacity (D' above it).
+template <bool CHECK>
+__device__ __forceinline__ void chunk_place_loop(int first, int last, int r0, int r1, int tiles_x, unsigned* off,
+                                                 const uint2* __restrict__ crect, unsigned capacity,
+                                                 unsigned* __restrict__ vals, unsigned* __restrict__ err, int lane);
+
 __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
     const unsigned* __restrict__ nchunks, const unsigned* __restrict__ chunk_first, const uint2* __restrict__ crect,
     int tiles_x, int tiles_y, int band_rows, int nbands, const unsigned* __restrict__ table,
-    const unsigned* __restrict__ tile_start, unsigned capacity, unsigned* __restrict__ vals,
-    unsigned* __restrict__ err) {
+    const unsigned* __restrict__ tile_start, const unsigned long long* __restrict__ ctotal, unsigned capacity,
+    unsigned* __restrict__ vals, unsigned* __restrict__ err) {
     pdl_entry();
     extern __shared__ unsigned smem_off[];
-    const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
     const int chunk = (int)(gw / nbands), band = (int)(gw - (long long)chunk * nbands);
@@ -1032,6 +1037,18 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
     const unsigned* ts = tile_start + tb0;
     for (int t = lane; t < ntb; t += 32) off[t] = ts[t] + row[t];
     __syncwarp();
+    // D' (the coarse tile scan's total) within the capacity: no position reaches it
+    if (*ctotal <= (unsigned long long)capacity)
+        chunk_place_loop<false>(first, last, r0, r1, tiles_x, off, crect, capacity, vals, err, lane);
+    else
+        chunk_place_loop<true>(first, last, r0, r1, tiles_x, off, crect, capacity, vals, err, lane);
+}
+
+template <bool CHECK>
+__device__ __forceinline__ void chunk_place_loop(int first, int last, int r0, int r1, int tiles_x, unsigned* off,
+                                                 const uint2* __restrict__ crect, unsigned capacity,
+                                                 unsigned* __restrict__ vals, unsigned* __restrict__ err, int lane) {
+    const unsigned full = 0xffffffffu;
     unsigned g_next = 0u;
     uint2 r_next = make_uint2(0u, 0u);
     if (first + lane < last) {
@@ -1086,7 +1103,7 @@ __global__ void __launch_bounds__(32 * kPlaceWarps) k_chunk_place(
                 const unsigned tl = tl0 + rk * (unsigned)tiles_x + (k - rk * jw);  // band-local tile
                 const unsigned pos = off[tl];
                 off[tl] = pos + 1u;
-                if (pos < capacity) {
+                if (!CHECK || pos < capacity) {
                     vals[pos] = jg;
                 } else {
                     atomicOr(err, kErrCheck);
@@ -1580,7 +1597,7 @@ static cudaError_t emit_counting(const gs_proj& proj, int tiles_x, int tiles_y, 
     count_launches(5);
     if ((e = launch_pdl(k_chunk_place, dim3((unsigned)((warps + wpb - 1) / wpb)), dim3(32 * wpb), smem, st,
                         w.nchunks, w.chunk_first, w.crect, sx, sy, band_rows, nbands, w.table, w.stile_start,
-                        (unsigned)capacity, w.cvals, err)))
+                        (const unsigned long long*)w.ctotal, (unsigned)capacity, w.cvals, err)))
         return e;
     // grid-stride kernels over the segments (8 warps per block): at most the resident blocks
     static std::atomic<int> count_cache[256], place_cache[256], place64_cache[256];
