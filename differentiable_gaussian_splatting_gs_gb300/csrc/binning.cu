@@ -1297,29 +1297,35 @@ __device__ __forceinline__ void fine_place_loop(unsigned k, unsigned ns, unsigne
         const int tx0 = cur.tx0, ty0 = cur.ty0;
         if (k + stride < ns)
             fine_seg_load(cur, k + stride, Ts, SX, tiles_x, tiles_y, s_first, crange, cvals, F, tile_start, lane);
+        // one tile of a round: the lanes whose Gaussian covers tile t write consecutive positions
+        auto place_tile = [&](int t, unsigned m16, unsigned g) {
+            const bool mine = (m16 >> t) & 1u;
+            const unsigned m = __ballot_sync(full, mine);
+            const unsigned pos = next[t] + __popc(m & lt);
+            if (mine) {
+                if (!CHECK || pos < capacity) {
+                    vals[pos] = g;
+                    if (KEY64) {
+                        const unsigned tile = (unsigned)((ty0 + (t >> 2)) * tiles_x + tx0 + (t & 3));
+                        keys64[pos] = ((unsigned long long)tile << 32) | depth_bits[g];
+                    }
+                } else {
+                    atomicOr(err, kErrCheck);
+                }
+            }
+            next[t] += __popc(m);
+        };
 #pragma unroll
         for (int r = 0; r < kRounds; ++r) {
             const unsigned m16 = m16v[r], g = gv[r];
             const unsigned any = __reduce_or_sync(full, m16);
+            if (any == 0xffffu) {  // warp-uniform: every tile is covered by some lane
 #pragma unroll
-            for (int t = 0; t < kSuperTiles; ++t) {
-                if (any & (1u << t)) {  // warp-uniform
-                    const bool mine = (m16 >> t) & 1u;
-                    const unsigned m = __ballot_sync(full, mine);
-                    const unsigned pos = next[t] + __popc(m & lt);
-                    if (mine) {
-                        if (!CHECK || pos < capacity) {
-                            vals[pos] = g;
-                            if (KEY64) {
-                                const unsigned tile = (unsigned)((ty0 + (t >> 2)) * tiles_x + tx0 + (t & 3));
-                                keys64[pos] = ((unsigned long long)tile << 32) | depth_bits[g];
-                            }
-                        } else {
-                            atomicOr(err, kErrCheck);
-                        }
-                    }
-                    next[t] += __popc(m);
-                }
+                for (int t = 0; t < kSuperTiles; ++t) place_tile(t, m16, g);
+            } else {
+#pragma unroll
+                for (int t = 0; t < kSuperTiles; ++t)
+                    if (any & (1u << t)) place_tile(t, m16, g);  // warp-uniform
             }
         }
     }
