@@ -1049,22 +1049,13 @@ __device__ __forceinline__ void chunk_place_loop(int first, int last, int r0, in
                                                  const uint2* __restrict__ crect, unsigned capacity,
                                                  unsigned* __restrict__ vals, unsigned* __restrict__ err, int lane) {
     const unsigned full = 0xffffffffu;
-    unsigned g_next = 0u;
     uint2 r_next = make_uint2(0u, 0u);
-    if (first + lane < last) {
-        g_next = (unsigned)(first + lane);
-        r_next = super_rect(crect[first + lane]);
-    }
+    if (first + lane < last) r_next = super_rect(crect[first + lane]);
     for (int base = first; base < last; base += 32) {
-        const unsigned g = g_next;
-        const uint2 pr = r_next;
+        const uint2 pr = r_next;  // this lane's Gaussian: depth position base + lane
         const int nx = base + 32 + lane;  // prefetch the next 32 Gaussians
-        g_next = 0u;
         r_next = make_uint2(0u, 0u);
-        if (nx < last) {
-            g_next = (unsigned)nx;
-            r_next = super_rect(crect[nx]);
-        }
+        if (nx < last) r_next = super_rect(crect[nx]);
         // this lane's Gaussian inside the band: columns [x0, x0 + w), rows [ya, yb) (band-local)
         const unsigned w = pr.y & 0xffffu;
         const int y0 = (int)(pr.x >> 16);
@@ -1074,6 +1065,7 @@ __device__ __forceinline__ void chunk_place_loop(int first, int last, int r0, in
         const unsigned m = div_magic(w);
         const unsigned area_l = (w > 0u && ya < yb) ? w * (unsigned)(yb - ya) : 0u;
         const unsigned tl0_l = (unsigned)ya * (unsigned)tiles_x + (pr.x & 0xffffu);  // band-local first tile
+        const unsigned wa = w | (area_l << 16);  // width and area (both below 2^16 super-tiles)
         unsigned hit = __ballot_sync(full, area_l > 0u);
         // pairing, decided for all lanes at once: a hit lane pairs with the next hit lane when both
         // cover at most 16 tiles of the band and their rectangles are disjoint; then each half-warp
@@ -1094,9 +1086,10 @@ __device__ __forceinline__ void chunk_place_loop(int first, int last, int r0, in
             if (pair) hit &= hit - 1u;
             const bool second = pair && lane >= 16;
             const int j = second ? j2 : j1;
-            const unsigned jg = __shfl_sync(full, g, j), jm = __shfl_sync(full, m, j);
-            const unsigned jw = __shfl_sync(full, w, j), area = __shfl_sync(full, area_l, j);
+            const unsigned jg = (unsigned)(base + j);  // lane j's Gaussian
+            const unsigned jm = __shfl_sync(full, m, j), jwa = __shfl_sync(full, wa, j);
             const unsigned tl0 = __shfl_sync(full, tl0_l, j);
+            const unsigned jw = jwa & 0xffffu, area = jwa >> 16;
             const unsigned step = pair ? 16u : 32u;
             for (unsigned k = pair ? (lane & 15u) : lane; k < area; k += step) {
                 const unsigned rk = div_by(k, jw, jm);
